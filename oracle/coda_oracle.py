@@ -1,0 +1,355 @@
+"""fp64 CPU oracle for the CODA GEMM-epilogue transformer operators.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline / reference leg may import or call this module.
+The product path (the CUDA library and its Python binding) never imports it,
+and this module imports nothing from the product path.
+
+What it computes: the *canonical, unfused* formula of every operator, in
+float64 NumPy, on the exact values of the bf16/fp32/int32 inputs.  It does not
+use the GEMM-epilogue reparameterisations (those are what the CUDA path does);
+it has no intermediate bf16 rounding, no tiling and no fusion.  Backward passes
+are the textbook chain rule of the canonical forward formulas, derived here
+independently of the CUDA path's fused backward.
+
+Sources (page titles, then section / equation / figure):
+  [P1] "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
+       (HTML text of arXiv 2605.19269, Chinese translation).
+  [P2] "CODA: new research optimizes Transformer training with GEMM-epilogue
+       programming" (news flash, Filipino).
+  [P3] "CODA: 把 Transformer Block 重写成 GEMM-Epilogue 程序 · 干货攻略"
+       (x-tip guide).
+
+Readings where the pages are silent (each is also listed in the design notes):
+  * RMSNorm: rms(x) = sqrt(mean(x^2) + eps), eps inside the root.
+  * RMSNorm gain gamma multiplies after normalising and before the next
+    projection ([P1] §3.2.1 equation).
+  * RoPE: interleaved pairs (2j, 2j+1), angle = pos * theta^(-2j/d),
+    [a, b] -> [a cos - b sin, a sin + b cos]; no frequency scaling.
+  * QK-RMSNorm: per head over head_dim, gains shared by all heads, applied
+    before RoPE.
+  * Cross-entropy: natural log, mean over rows whose label != ignore_index;
+    all rows ignored gives NaN (0/0) and a zero gradient.
+
+Parity status: every function below is pinned by a test in
+``tests/test_oracle_pins.py`` (identities, closed forms, library special
+cases, finite differences); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "rms_inv", "rmsnorm", "rmsnorm_bwd",
+    "rmsnorm_linear_fwd", "rmsnorm_linear_bwd",
+    "linear_residual_fwd", "linear_residual_bwd",
+    "silu", "silu_grad", "swiglu_fwd", "mlp_fwd", "mlp_bwd",
+    "rope_angles", "rope", "rope_inv", "qk_rmsnorm_rope_fwd", "qk_rmsnorm_rope_bwd",
+    "linear_cross_entropy_fwd", "linear_cross_entropy_bwd",
+    "block_fwd", "block_bwd", "block_flops", "mlp_flops", "ce_flops",
+]
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm
+# ---------------------------------------------------------------------------
+
+def rms_inv(x, eps):
+    """r = 1/rms(x) per row, rms(x) = sqrt(mean_k x_k^2 + eps).
+
+    [P1] §3.2.1: r is the row-wise inverse RMS factor of the pattern's
+    equation y = RMSNorm(xW0 + z, gamma) W1 = (r (xW0 + z) ⊙ gamma) W1.
+    eps placement is a reading (inside the root)."""
+    x = np.asarray(x, dtype=np.float64)
+    return 1.0 / np.sqrt(np.mean(x * x, axis=-1) + eps)
+
+
+def rmsnorm(x, gamma, eps):
+    """RMSNorm(x, gamma) = (x * r) ⊙ gamma   ([P1] §3.2.1 equation)."""
+    r = rms_inv(x, eps)
+    return (x * r[..., None]) * gamma
+
+
+def rmsnorm_bwd(x, gamma, eps, dy):
+    """Gradient of y = (x r) ⊙ gamma w.r.t. x and gamma (chain rule).
+
+    n = x r,  dn = dy ⊙ gamma,  dx = r (dn - n * mean_k(n ⊙ dn)),
+    dgamma = sum over all leading axes of dy ⊙ n.
+    The pages give no backward formula ([P2] only states that block-local
+    forwards keep a GEMM-epilogue backward); this is the textbook derivative
+    of the forward definition above."""
+    r = rms_inv(x, eps)[..., None]
+    n = x * r
+    dn = dy * gamma
+    dx = r * (dn - n * np.mean(n * dn, axis=-1, keepdims=True))
+    dgamma = (dy * n).reshape(-1, x.shape[-1]).sum(axis=0)
+    return dx, dgamma
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm followed by a projection (+ residual), workload 2
+# ---------------------------------------------------------------------------
+
+def rmsnorm_linear_fwd(X, gamma, W, eps, R=None):
+    """y = R + RMSNorm(X, gamma) W^T   with W stored [out, in].
+
+    [P1] §3.2.1 equation (second GEMM of the GEMM-RMSNorm-GEMM pattern, the
+    residual being the preceding stream).  Returns (y, r)."""
+    a = rmsnorm(X, gamma, eps)
+    y = a @ W.T
+    if R is not None:
+        y = y + R
+    return y, rms_inv(X, eps)
+
+
+def rmsnorm_linear_bwd(X, gamma, W, eps, G):
+    """Backward of rmsnorm_linear_fwd for upstream gradient G.
+
+    a = RMSNorm(X, gamma); y = a W^T + R.
+    da = G W, dW = G^T a, then RMSNorm backward gives dX and dgamma; dR = G.
+    (Chain rule of the canonical formula; no page prints it.)"""
+    a = rmsnorm(X, gamma, eps)
+    da = G @ W
+    dW = G.T @ a
+    dX, dgamma = rmsnorm_bwd(X, gamma, eps, da)
+    return {"dX": dX, "dW": dW, "dgamma": dgamma, "dR": G}
+
+
+# ---------------------------------------------------------------------------
+# projection + residual (the first GEMM of the pattern)
+# ---------------------------------------------------------------------------
+
+def linear_residual_fwd(X, W, R, eps=1e-6):
+    """u = X W^T + R, the "xW0 + z" of [P1] §3.2.1, and r = 1/rms(u), the
+    row factor that the first GEMM's epilogue prepares (as partial sums of
+    squares) for the next projection."""
+    u = X @ W.T + R
+    return u, rms_inv(u, eps)
+
+
+def linear_residual_bwd(X, W, G):
+    """dX = G W, dW = G^T X, dR = G (chain rule)."""
+    return {"dX": G @ W, "dW": G.T @ X, "dR": G}
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU, workloads 1 and 3
+# ---------------------------------------------------------------------------
+
+def silu(a):
+    """silu(a) = a * sigmoid(a) = a / (1 + exp(-a)).  The SwiGLU gate of
+    [P1] §3.1 class 1 (pairwise maps) and [P3]'s linear_swiglu example."""
+    a = np.asarray(a, dtype=np.float64)
+    return a / (1.0 + np.exp(-a))
+
+
+def silu_grad(a):
+    """d silu / da = s (1 + a (1 - s)), s = sigmoid(a)  (calculus)."""
+    s = 1.0 / (1.0 + np.exp(-np.asarray(a, dtype=np.float64)))
+    return s * (1.0 + a * (1.0 - s))
+
+
+def swiglu_fwd(X, Wg, Wu):
+    """H = silu(X Wg^T) ⊙ (X Wu^T); returns (H, g, u).  Workload 1."""
+    g = X @ Wg.T
+    u = X @ Wu.T
+    return silu(g) * u, g, u
+
+
+def mlp_fwd(X, Wg, Wu, Wd, R, gamma=None, eps=1e-6):
+    """SwiGLU MLP sublayer: a = X (or RMSNorm(X, gamma) when gamma is given),
+    g = a Wg^T, u = a Wu^T, H = silu(g) ⊙ u, y = R + H Wd^T.
+    Returns a dict with y and the intermediates."""
+    a = X if gamma is None else rmsnorm(X, gamma, eps)
+    H, g, u = swiglu_fwd(a, Wg, Wu)
+    y = R + H @ Wd.T
+    return {"y": y, "H": H, "g": g, "u": u, "a": a}
+
+
+def mlp_bwd(X, Wg, Wu, Wd, dY, gamma=None, eps=1e-6):
+    """Backward of mlp_fwd (chain rule).  dR = dY is returned separately;
+    dX is the gradient through the MLP branch only."""
+    f = mlp_fwd(X, Wg, Wu, Wd, np.zeros_like(dY), gamma, eps)
+    g, u, H, a = f["g"], f["u"], f["H"], f["a"]
+    dH = dY @ Wd
+    dWd = dY.T @ H
+    dg = dH * u * silu_grad(g)
+    du = dH * silu(g)
+    da = dg @ Wg + du @ Wu
+    out = {"dWd": dWd, "dWg": dg.T @ a, "dWu": du.T @ a, "dR": dY,
+           "dH": dH, "dg": dg, "du": du}
+    if gamma is None:
+        out["dX"] = da
+    else:
+        out["dX"], out["dgamma"] = rmsnorm_bwd(X, gamma, eps, da)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# QK-RMSNorm + RoPE, workload 5
+# ---------------------------------------------------------------------------
+
+def rope_angles(pos, head_dim, theta):
+    """angle[t, j] = pos[t] * theta^(-2j/head_dim), j < head_dim/2 (reading)."""
+    j = np.arange(head_dim // 2, dtype=np.float64)
+    inv_freq = theta ** (-2.0 * j / head_dim)
+    return np.asarray(pos, dtype=np.float64)[:, None] * inv_freq[None, :]
+
+
+def rope(v, pos, theta):
+    """Rotate interleaved pairs (2j, 2j+1) of v[t, head, d] by angle[t, j].
+    [P1] §3.1 class 1 names RoPE-style rotations as a pairwise map; the
+    convention (interleaved pairs) is a reading."""
+    d = v.shape[-1]
+    ang = rope_angles(pos, d, theta)[:, None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = v[..., 0::2], v[..., 1::2]
+    out = np.empty_like(v)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out
+
+
+def rope_inv(v, pos, theta):
+    """Rotation by the negative angle: the inverse (and transpose) of rope."""
+    return rope(v, -np.asarray(pos, dtype=np.float64), theta)
+
+
+def qk_rmsnorm_rope_fwd(q, gamma, pos, theta, eps):
+    """q[t, head, d] -> RoPE(RMSNorm_d(q) ⊙ gamma, pos).  [P3]'s
+    linear_qknorm_rope names the fused operator: per-head RMSNorm, then RoPE."""
+    return rope(rmsnorm(q, gamma, eps), pos, theta)
+
+
+def qk_rmsnorm_rope_bwd(q, gamma, pos, theta, eps, dout):
+    """Backward: inverse rotation of the gradient, then per-head RMSNorm
+    backward.  Returns (dq, dgamma)."""
+    dn = rope_inv(dout, pos, theta)
+    return rmsnorm_bwd(q, gamma, eps, dn)
+
+
+# ---------------------------------------------------------------------------
+# linear + cross-entropy, workload 4
+# ---------------------------------------------------------------------------
+
+def _lse(z):
+    m = z.max(axis=-1, keepdims=True)
+    return (m + np.log(np.exp(z - m).sum(axis=-1, keepdims=True)))[..., 0]
+
+
+def linear_cross_entropy_fwd(X, W, labels, ignore_index=-100):
+    """z = X W^T; lse_i = log sum_j exp(z_ij); loss_i = lse_i - z_{i, y_i};
+    mean over rows with y_i != ignore_index.
+
+    [P1] §3.1 class 5 (running max / sum-exp state for online log-sum-exp and
+    cross-entropy) and [P3]'s linear_cross_entropy.  Returns a dict with
+    loss (scalar), lse [M], per-row loss [M] (0 on ignored rows), n_valid."""
+    labels = np.asarray(labels)
+    z = X @ W.T
+    lse = _lse(z)
+    valid = labels != ignore_index
+    rows = np.nonzero(valid)[0]
+    per_row = np.zeros(X.shape[0])
+    per_row[rows] = lse[rows] - z[rows, labels[rows]]
+    n_valid = int(valid.sum())
+    loss = per_row[rows].sum() / n_valid if n_valid > 0 else float("nan")
+    return {"loss": loss, "lse": lse, "per_row": per_row, "n_valid": n_valid}
+
+
+def linear_cross_entropy_bwd(X, W, labels, ignore_index=-100, dloss=1.0):
+    """dZ = (softmax(z) - onehot(y)) * dloss / n_valid on valid rows, 0 on
+    ignored rows; dX = dZ W, dW = dZ^T X (chain rule)."""
+    labels = np.asarray(labels)
+    z = X @ W.T
+    p = np.exp(z - _lse(z)[:, None])
+    valid = labels != ignore_index
+    rows = np.nonzero(valid)[0]
+    n_valid = int(valid.sum())
+    dZ = np.zeros_like(z)
+    if n_valid > 0:
+        dZ[rows] = p[rows]
+        dZ[rows, labels[rows]] -= 1.0
+        dZ *= dloss / n_valid
+    return {"dX": dZ @ W, "dW": dZ.T @ X, "dZ": dZ}
+
+
+# ---------------------------------------------------------------------------
+# the non-attention transformer block, workload 5
+# ---------------------------------------------------------------------------
+
+def _heads(t, n, d):
+    return t.reshape(t.shape[0], n, d)
+
+
+def block_fwd(p, n_q, n_kv, head_dim, theta, eps):
+    """Pre-norm block without the attention core (its output A is an input):
+
+      a0 = RMSNorm(x0, gamma_attn);  [q | k | v] = a0 Wqkv^T
+      Q = RoPE(RMSNorm_head(q, gamma_q)), K likewise with gamma_k, V = v
+      x1 = x0 + A Wo^T
+      a1 = RMSNorm(x1, gamma_mlp);  g = a1 Wg^T, u = a1 Wu^T, H = silu(g) u
+      x2 = x1 + H Wd^T
+
+    The two GEMM-residual-RMSNorm-GEMM sites are [P1] §3.2.1 items 1 and 2.
+    ``p`` maps names to float64 arrays (pos as integers)."""
+    d = head_dim
+    a0 = rmsnorm(p["x0"], p["gamma_attn"], eps)
+    qkv = a0 @ p["Wqkv"].T
+    q = _heads(qkv[:, : n_q * d], n_q, d)
+    k = _heads(qkv[:, n_q * d: (n_q + n_kv) * d], n_kv, d)
+    v = qkv[:, (n_q + n_kv) * d:]
+    Q = qk_rmsnorm_rope_fwd(q, p["gamma_q"], p["pos"], theta, eps)
+    K = qk_rmsnorm_rope_fwd(k, p["gamma_k"], p["pos"], theta, eps)
+    x1 = p["x0"] + p["A"] @ p["Wo"].T
+    m = mlp_fwd(x1, p["Wg"], p["Wu"], p["Wd"], x1, p["gamma_mlp"], eps)
+    return {"Q": Q.reshape(Q.shape[0], -1), "K": K.reshape(K.shape[0], -1), "V": v,
+            "x1": x1, "x2": m["y"], "H": m["H"], "g": m["g"], "u": m["u"],
+            "q": q.reshape(q.shape[0], -1), "k": k.reshape(k.shape[0], -1)}
+
+
+def block_bwd(p, n_q, n_kv, head_dim, theta, eps):
+    """Backward of block_fwd given dx2 (gradient of x2) and dQ, dK, dV
+    (gradients of the attention inputs, supplied because attention is out of
+    scope).  Returns the gradients of x0, A, every weight and every gain."""
+    d = head_dim
+    f = block_fwd(p, n_q, n_kv, head_dim, theta, eps)
+    # MLP sublayer: x2 = x1 + mlp(x1)
+    mb = mlp_bwd(f["x1"], p["Wg"], p["Wu"], p["Wd"], p["dx2"], p["gamma_mlp"], eps)
+    dx1 = p["dx2"] + mb["dX"]
+    # attention output projection: x1 = x0 + A Wo^T
+    dA = dx1 @ p["Wo"]
+    dWo = dx1.T @ p["A"]
+    # QKV projection with QK-RMSNorm + RoPE
+    q = _heads(f["q"], n_q, d)
+    k = _heads(f["k"], n_kv, d)
+    dq, dgq = qk_rmsnorm_rope_bwd(q, p["gamma_q"], p["pos"], theta, eps, _heads(p["dQ"], n_q, d))
+    dk, dgk = qk_rmsnorm_rope_bwd(k, p["gamma_k"], p["pos"], theta, eps, _heads(p["dK"], n_kv, d))
+    dqkv = np.concatenate([dq.reshape(dq.shape[0], -1), dk.reshape(dk.shape[0], -1), p["dV"]], axis=1)
+    a0 = rmsnorm(p["x0"], p["gamma_attn"], eps)
+    da0 = dqkv @ p["Wqkv"]
+    dWqkv = dqkv.T @ a0
+    dx0_n, dga = rmsnorm_bwd(p["x0"], p["gamma_attn"], eps, da0)
+    return {"dx0": dx1 + dx0_n, "dA": dA, "dx1": dx1, "dWqkv": dWqkv, "dWo": dWo,
+            "dWg": mb["dWg"], "dWu": mb["dWu"], "dWd": mb["dWd"],
+            "dgamma_attn": dga, "dgamma_mlp": mb["dgamma"], "dgamma_q": dgq, "dgamma_k": dgk,
+            "dqkv": dqkv}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic FLOP counts (2*M*N*K per GEMM; element-wise work not counted)
+# ---------------------------------------------------------------------------
+
+def mlp_flops(tokens, hidden, inter, backward=True):
+    fwd = 2 * tokens * hidden * inter * 3
+    return fwd + (2 * fwd if backward else 0)
+
+
+def ce_flops(tokens, hidden, vocab, backward=True):
+    fwd = 2 * tokens * hidden * vocab
+    # backward recomputes the logits, then dX and dW
+    return fwd + (3 * fwd if backward else 0)
+
+
+def block_flops(tokens, hidden, qkv_out, attn_in, inter, backward=True):
+    fwd = 2 * tokens * hidden * (qkv_out + 3 * inter) + 2 * tokens * attn_in * hidden
+    return fwd + (2 * fwd if backward else 0)

@@ -1,0 +1,393 @@
+"""Checks that pin the fp64 oracle to facts that do not come from the oracle.
+
+Each ``check_*`` function takes the oracle module as an argument and returns
+the largest relative discrepancy it found, so that ``test_oracle_pins`` can run
+it on the real oracle (expects ~0) and on deliberately broken copies of it
+(expects a large value).  The facts used are: identities and special cases the
+pages state, closed forms from calculus, independent library routines
+(torch float64 CPU ops) for special cases, and central finite differences.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+RNG = np.random.default_rng
+
+
+def _rel(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    den = max(np.max(np.abs(b)), 1e-300)
+    return float(np.max(np.abs(a - b)) / den)
+
+
+def _fd_grad(fun, x, h=1e-6):
+    """Central finite differences of scalar fun w.r.t. every entry of x."""
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        old = x[i]
+        x[i] = old + h
+        fp = fun()
+        x[i] = old - h
+        fm = fun()
+        x[i] = old
+        g[i] = (fp - fm) / (2 * h)
+    return g
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm-reparameterised projection
+# ---------------------------------------------------------------------------
+
+def check_reparam_identity(o):
+    """CODA §3.2.1 equation: RMSNorm(x, gamma) W = diag(r) x (diag(gamma) W)
+    with r the per-row inverse RMS.  Written here in the reparameterised form
+    (row scale applied after the product with the gamma-folded weight)."""
+    r = RNG(1)
+    X = r.standard_normal((3, 8))
+    g = 1 + 0.1 * r.standard_normal(8)
+    W = r.standard_normal((5, 8))          # stored [out, in]
+    eps = 1e-6
+    y, rinv = o.rmsnorm_linear_fwd(X, g, W, eps)
+    rms = np.sqrt((X ** 2).sum(axis=1) / 8 + eps)
+    Wfold = W * g[None, :]                 # diag(gamma) folded into the weight
+    y_reparam = (X @ Wfold.T) / rms[:, None]
+    return max(_rel(y, y_reparam), _rel(rinv, 1 / rms))
+
+
+def check_rmsnorm_library(o):
+    """gamma = 1, W = I, no residual reduces to torch's rms_norm (float64)."""
+    r = RNG(2)
+    X = r.standard_normal((4, 16)) * 3
+    eps = 1e-6
+    y, _ = o.rmsnorm_linear_fwd(X, np.ones(16), np.eye(16), eps)
+    ref = F.rms_norm(torch.from_numpy(X), (16,), eps=eps).numpy()
+    g = 1 + 0.1 * r.standard_normal(16)
+    y2 = o.rmsnorm(X, g, eps)
+    ref2 = F.rms_norm(torch.from_numpy(X), (16,), weight=torch.from_numpy(g), eps=eps).numpy()
+    return max(_rel(y, ref), _rel(y2, ref2))
+
+
+def check_rmsnorm_scale_invariance(o):
+    """With eps = 0, RMSNorm(a x) = RMSNorm(x) for a > 0."""
+    r = RNG(3)
+    X = r.standard_normal((3, 8))
+    g = 1 + 0.1 * r.standard_normal(8)
+    W = r.standard_normal((5, 8))
+    y1, _ = o.rmsnorm_linear_fwd(X, g, W, 0.0)
+    y2, _ = o.rmsnorm_linear_fwd(7.5 * X, g, W, 0.0)
+    return _rel(y1, y2)
+
+
+def check_rmsnorm_linear_grad(o):
+    """FD gradients of L = sum(G ⊙ y) for y = R + RMSNorm(X, gamma) W^T."""
+    r = RNG(4)
+    M, K, N = 3, 8, 5
+    X = r.standard_normal((M, K))
+    g = 1 + 0.1 * r.standard_normal(K)
+    W = r.standard_normal((N, K))
+    R = r.standard_normal((M, N))
+    G = r.standard_normal((M, N))
+    eps = 1e-6
+    b = o.rmsnorm_linear_bwd(X, g, W, eps, G)
+
+    def L():
+        return float((G * o.rmsnorm_linear_fwd(X, g, W, eps, R)[0]).sum())
+    errs = [_rel(b["dX"], _fd_grad(L, X)), _rel(b["dW"], _fd_grad(L, W)),
+            _rel(b["dgamma"], _fd_grad(L, g))]
+    fR = _fd_grad(L, R)
+    errs.append(_rel(b["dR"], fR))
+    return max(errs)
+
+
+def check_linear_residual(o):
+    """u = X W^T + R against torch's linear; r from partial sums of squares
+    over column blocks (any split) equals r over the whole row."""
+    r = RNG(5)
+    X = r.standard_normal((4, 12))
+    W = r.standard_normal((10, 12))
+    R = r.standard_normal((4, 10))
+    u, rinv = o.linear_residual_fwd(X, W, R, 1e-6)
+    ref = F.linear(torch.from_numpy(X), torch.from_numpy(W)).numpy() + R
+    parts = [np.sum(ref[:, a:b] ** 2, axis=1) for a, b in ((0, 3), (3, 7), (7, 10))]
+    r_parts = 1 / np.sqrt(sum(parts[::-1]) / 10 + 1e-6)
+    b = o.linear_residual_bwd(X, W, R)   # R as an arbitrary upstream gradient
+
+    def L():
+        return float((R * (X @ W.T)).sum())
+    return max(_rel(u, ref), _rel(rinv, r_parts), _rel(b["dX"], _fd_grad(L, X)),
+               _rel(b["dW"], _fd_grad(L, W)))
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU
+# ---------------------------------------------------------------------------
+
+def check_silu_closed_forms(o):
+    """silu(0) = 0, silu'(0) = 1/2, silu(a) -> a (a -> +inf), -> 0 (a -> -inf),
+    silu = a*sigmoid(a) vs torch, silu_grad vs central differences."""
+    errs = [abs(o.silu(0.0)), abs(o.silu_grad(0.0) - 0.5),
+            abs(o.silu(40.0) - 40.0) / 40.0, abs(o.silu(-40.0)),
+            abs(o.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0)))]
+    a = np.linspace(-8, 8, 41)
+    errs.append(_rel(o.silu(a), F.silu(torch.from_numpy(a)).numpy()))
+    h = 1e-6
+    fd = (o.silu(a + h) - o.silu(a - h)) / (2 * h)
+    errs.append(_rel(o.silu_grad(a), fd))
+    return max(errs)
+
+
+def check_swiglu_library(o):
+    """H = silu(X Wg^T) ⊙ (X Wu^T) against torch linear/silu in float64."""
+    r = RNG(6)
+    X = r.standard_normal((5, 8))
+    Wg = r.standard_normal((6, 8))
+    Wu = r.standard_normal((6, 8))
+    H, g, u = o.swiglu_fwd(X, Wg, Wu)
+    tX = torch.from_numpy(X)
+    ref = (F.silu(F.linear(tX, torch.from_numpy(Wg))) * F.linear(tX, torch.from_numpy(Wu))).numpy()
+    return max(_rel(H, ref), _rel(g, X @ Wg.T), _rel(u, X @ Wu.T))
+
+
+def check_mlp_special_cases(o):
+    """Wd = 0 gives y = R; R = 0 and gamma absent gives y = H Wd^T with H from
+    swiglu_fwd; gamma present equals feeding torch's rms_norm output."""
+    r = RNG(7)
+    X = r.standard_normal((3, 8))
+    Wg, Wu = r.standard_normal((6, 8)), r.standard_normal((6, 8))
+    Wd = r.standard_normal((8, 6))
+    R = r.standard_normal((3, 8))
+    g = 1 + 0.1 * r.standard_normal(8)
+    e1 = _rel(o.mlp_fwd(X, Wg, Wu, np.zeros_like(Wd), R)["y"], R)
+    H, _, _ = o.swiglu_fwd(X, Wg, Wu)
+    e2 = _rel(o.mlp_fwd(X, Wg, Wu, Wd, np.zeros_like(R))["y"], H @ Wd.T)
+    a = F.rms_norm(torch.from_numpy(X), (8,), weight=torch.from_numpy(g), eps=1e-6).numpy()
+    H2, _, _ = o.swiglu_fwd(a, Wg, Wu)
+    e3 = _rel(o.mlp_fwd(X, Wg, Wu, Wd, R, g, 1e-6)["y"], R + H2 @ Wd.T)
+    return max(e1, e2, e3)
+
+
+def check_mlp_grad(o, with_gamma):
+    r = RNG(8 + int(with_gamma))
+    M, K, I = 3, 6, 5
+    X = r.standard_normal((M, K))
+    Wg, Wu = r.standard_normal((I, K)), r.standard_normal((I, K))
+    Wd = r.standard_normal((K, I))
+    dY = r.standard_normal((M, K))
+    g = 1 + 0.1 * r.standard_normal(K) if with_gamma else None
+    b = o.mlp_bwd(X, Wg, Wu, Wd, dY, g, 1e-6)
+
+    def L():
+        return float((dY * o.mlp_fwd(X, Wg, Wu, Wd, np.zeros_like(dY), g, 1e-6)["y"]).sum())
+    errs = [_rel(b["dX"], _fd_grad(L, X)), _rel(b["dWg"], _fd_grad(L, Wg)),
+            _rel(b["dWu"], _fd_grad(L, Wu)), _rel(b["dWd"], _fd_grad(L, Wd))]
+    if with_gamma:
+        errs.append(_rel(b["dgamma"], _fd_grad(L, g)))
+    return max(errs)
+
+
+# ---------------------------------------------------------------------------
+# RoPE and QK-RMSNorm
+# ---------------------------------------------------------------------------
+
+def check_rope_invariants(o):
+    """Pair norms preserved; pos = 0 is the identity; <R_m q, R_n k> depends
+    only on m - n; rope_inv undoes rope; one pair checked against the closed
+    form rotation (angle = pos * theta^(-2j/d))."""
+    r = RNG(10)
+    d, theta = 8, 10000.0
+    v = r.standard_normal((4, 3, d))
+    pos = np.array([0, 1, 5, 17])
+    w = o.rope(v, pos, theta)
+    e = [_rel(np.hypot(w[..., 0::2], w[..., 1::2]), np.hypot(v[..., 0::2], v[..., 1::2]))]
+    e.append(_rel(w[0], v[0]))
+    e.append(_rel(o.rope_inv(w, pos, theta), v))
+    q = r.standard_normal((1, 1, d))
+    k = r.standard_normal((1, 1, d))
+    dots = []
+    for m, n in ((3, 1), (10, 8), (102, 100)):
+        dots.append(float((o.rope(q, [m], theta) * o.rope(k, [n], theta)).sum()))
+    e.append(abs(dots[0] - dots[1]) / abs(dots[0]) + abs(dots[0] - dots[2]) / abs(dots[0]))
+    # pair j = 1 of head_dim 8 at pos 3: angle 3 * 10000^(-1/4) = 0.3 rad
+    unit = np.zeros((1, 1, d))
+    unit[0, 0, 2] = 1.0
+    w1 = o.rope(unit, [3], theta)[0, 0]
+    e.append(abs(w1[2] - math.cos(0.3)) + abs(w1[3] - math.sin(0.3)) + np.abs(np.delete(w1, [2, 3])).sum())
+    return max(e)
+
+
+def check_qknorm_closed_form(o):
+    """gamma = 1 and pos = 0: each head of the output has mean square
+    ms / (ms + eps) where ms is the head's input mean square."""
+    r = RNG(11)
+    q = r.standard_normal((3, 4, 8)) * 0.01
+    eps = 1e-4
+    out = o.qk_rmsnorm_rope_fwd(q, np.ones(8), np.zeros(3), 500000.0, eps)
+    ms = np.mean(q * q, axis=-1)
+    return _rel(np.mean(out * out, axis=-1), ms / (ms + eps))
+
+
+def check_qknorm_grad(o):
+    r = RNG(12)
+    q = r.standard_normal((3, 2, 8))
+    g = 1 + 0.1 * r.standard_normal(8)
+    pos = np.array([0, 7, 300])
+    dout = r.standard_normal(q.shape)
+    dq, dg = o.qk_rmsnorm_rope_bwd(q, g, pos, 500000.0, 1e-6, dout)
+
+    def L():
+        return float((dout * o.qk_rmsnorm_rope_fwd(q, g, pos, 500000.0, 1e-6)).sum())
+    return max(_rel(dq, _fd_grad(L, q)), _rel(dg, _fd_grad(L, g)))
+
+
+# ---------------------------------------------------------------------------
+# linear + cross-entropy
+# ---------------------------------------------------------------------------
+
+def check_ce_uniform(o):
+    """All-equal logits (W = 0) give loss = ln V exactly; V = 128256 is the
+    unembedding size of the linear-CE workload."""
+    V = 128256
+    X = np.ones((2, 4))
+    W = np.zeros((V, 4))
+    f = o.linear_cross_entropy_fwd(X, W, np.array([0, V - 1]))
+    return max(abs(f["loss"] - math.log(V)) / math.log(V), _rel(f["lse"], [math.log(V)] * 2),
+               abs(math.log(V) - 11.761783545564427))
+
+
+def check_ce_library(o):
+    """Against torch cross_entropy(ignore_index=-100) in float64; one dominant
+    logit gives loss -> 0; gradient rows sum to zero; ignored rows have zero
+    gradient; n_valid is an exact count; FD gradients of the mean loss."""
+    r = RNG(13)
+    M, K, V = 6, 5, 11
+    X = r.standard_normal((M, K))
+    W = r.standard_normal((V, K))
+    lab = np.array([0, 10, -100, 3, -100, 7])
+    f = o.linear_cross_entropy_fwd(X, W, lab)
+    z = torch.from_numpy(X @ W.T)
+    ref = F.cross_entropy(z, torch.from_numpy(lab).long(), ignore_index=-100).item()
+    ref_rows = F.cross_entropy(z, torch.from_numpy(lab).long(), ignore_index=-100, reduction="none").numpy()
+    e = [abs(f["loss"] - ref) / abs(ref), _rel(f["per_row"], ref_rows), abs(f["n_valid"] - 4),
+         _rel(f["lse"], torch.logsumexp(z, dim=1).numpy())]
+    b = o.linear_cross_entropy_bwd(X, W, lab)
+    e.append(float(np.max(np.abs(b["dZ"].sum(axis=1)))))
+    e.append(float(np.max(np.abs(b["dZ"][[2, 4]]))))
+
+    def L():
+        return o.linear_cross_entropy_fwd(X, W, lab)["loss"]
+    e += [_rel(b["dX"], _fd_grad(L, X)), _rel(b["dW"], _fd_grad(L, W))]
+    Wd = np.zeros((V, K))
+    Wd[3] = 100.0
+    Xd = np.ones((1, K))
+    e.append(o.linear_cross_entropy_fwd(Xd, Wd, np.array([3]))["loss"])
+    return max(e)
+
+
+def check_ce_all_ignored(o):
+    """Every row ignored: loss = 0/0 = NaN (torch's mean reduction), zero grad."""
+    r = RNG(14)
+    X = r.standard_normal((3, 4))
+    W = r.standard_normal((7, 4))
+    lab = np.array([-100, -100, -100])
+    f = o.linear_cross_entropy_fwd(X, W, lab)
+    b = o.linear_cross_entropy_bwd(X, W, lab)
+    ok = math.isnan(f["loss"]) and f["n_valid"] == 0 and not np.any(b["dX"]) and not np.any(b["dW"])
+    return 0.0 if ok else 1.0
+
+
+# ---------------------------------------------------------------------------
+# the block
+# ---------------------------------------------------------------------------
+
+def tiny_block(seed=15, n_q=2, n_kv=1, d=4, h=8, inter=6, tokens=3):
+    r = RNG(seed)
+    qkv = (n_q + 2 * n_kv) * d
+    p = {
+        "x0": r.standard_normal((tokens, h)), "Wqkv": r.standard_normal((qkv, h)) * 0.5,
+        "Wo": r.standard_normal((h, n_q * d)) * 0.5, "Wg": r.standard_normal((inter, h)) * 0.5,
+        "Wu": r.standard_normal((inter, h)) * 0.5, "Wd": r.standard_normal((h, inter)) * 0.5,
+        "gamma_attn": 1 + 0.1 * r.standard_normal(h), "gamma_mlp": 1 + 0.1 * r.standard_normal(h),
+        "gamma_q": 1 + 0.1 * r.standard_normal(d), "gamma_k": 1 + 0.1 * r.standard_normal(d),
+        "A": r.standard_normal((tokens, n_q * d)), "dx2": r.standard_normal((tokens, h)),
+        "dQ": r.standard_normal((tokens, n_q * d)), "dK": r.standard_normal((tokens, n_kv * d)),
+        "dV": r.standard_normal((tokens, n_kv * d)), "pos": np.arange(tokens) * 5 + 1,
+    }
+    return p, dict(n_q=n_q, n_kv=n_kv, head_dim=d, theta=10000.0, eps=1e-6)
+
+
+def check_block_special_cases(o):
+    """Structure of the block ([P1] §3.2.1 sites 1 and 2): with Wd = 0 the
+    output is x0 + A Wo^T (torch linear); with A = 0 the MLP sees x0 and
+    x2 - x0 equals the MLP branch computed from torch rms_norm/linear/silu;
+    V is the plain projection of RMSNorm(x0); with gamma_q = 1 and pos = 0
+    every Q head has mean square ms/(ms+eps)."""
+    p, cfg = tiny_block()
+    e = []
+    q = dict(p)
+    q["Wd"] = np.zeros_like(p["Wd"])
+    f = o.block_fwd(q, **cfg)
+    ref = p["x0"] + F.linear(torch.from_numpy(p["A"]), torch.from_numpy(p["Wo"])).numpy()
+    e.append(_rel(f["x2"], ref))
+    e.append(_rel(f["x1"], ref))
+    q = dict(p)
+    q["A"] = np.zeros_like(p["A"])
+    f = o.block_fwd(q, **cfg)
+    t = torch.from_numpy
+    a1 = F.rms_norm(t(p["x0"]), (8,), weight=t(p["gamma_mlp"]), eps=cfg["eps"])
+    br = F.linear(F.silu(F.linear(a1, t(p["Wg"]))) * F.linear(a1, t(p["Wu"])), t(p["Wd"])).numpy()
+    e.append(_rel(f["x2"] - p["x0"], br))
+    a0 = F.rms_norm(t(p["x0"]), (8,), weight=t(p["gamma_attn"]), eps=cfg["eps"])
+    qkv = F.linear(a0, t(p["Wqkv"])).numpy()
+    e.append(_rel(f["V"], qkv[:, 12:]))
+    q = dict(p)
+    q["gamma_q"] = np.ones(4)
+    q["pos"] = np.zeros(3, dtype=np.int64)
+    f = o.block_fwd(q, **cfg)
+    qh = qkv[:, :8].reshape(3, 2, 4)
+    ms = np.mean(qh ** 2, axis=-1)
+    e.append(_rel(np.mean(f["Q"].reshape(3, 2, 4) ** 2, axis=-1), ms / (ms + cfg["eps"])))
+    return max(e)
+
+
+def check_block_grad(o):
+    """FD gradients of L = <dx2, x2> + <dQ, Q> + <dK, K> + <dV, V>."""
+    p, cfg = tiny_block()
+    b = o.block_bwd(p, **cfg)
+
+    def L():
+        f = o.block_fwd(p, **cfg)
+        return float((p["dx2"] * f["x2"]).sum() + (p["dQ"] * f["Q"]).sum()
+                     + (p["dK"] * f["K"]).sum() + (p["dV"] * f["V"]).sum())
+    pairs = [("dx0", "x0"), ("dA", "A"), ("dWqkv", "Wqkv"), ("dWo", "Wo"), ("dWg", "Wg"),
+             ("dWu", "Wu"), ("dWd", "Wd"), ("dgamma_attn", "gamma_attn"),
+             ("dgamma_mlp", "gamma_mlp"), ("dgamma_q", "gamma_q"), ("dgamma_k", "gamma_k")]
+    return max(_rel(b[g], _fd_grad(L, p[x])) for g, x in pairs)
+
+
+ALL_CHECKS = {
+    "reparam_identity": (check_reparam_identity, 1e-13),
+    "rmsnorm_library": (check_rmsnorm_library, 1e-13),
+    "rmsnorm_scale_invariance": (check_rmsnorm_scale_invariance, 1e-13),
+    "rmsnorm_linear_grad": (check_rmsnorm_linear_grad, 1e-7),
+    "linear_residual": (check_linear_residual, 1e-7),
+    "silu_closed_forms": (check_silu_closed_forms, 1e-7),
+    "swiglu_library": (check_swiglu_library, 1e-13),
+    "mlp_special_cases": (check_mlp_special_cases, 1e-12),
+    "mlp_grad": (lambda o: check_mlp_grad(o, False), 1e-7),
+    "mlp_grad_gamma": (lambda o: check_mlp_grad(o, True), 1e-7),
+    "rope_invariants": (check_rope_invariants, 1e-12),
+    "qknorm_closed_form": (check_qknorm_closed_form, 1e-12),
+    "qknorm_grad": (check_qknorm_grad, 1e-7),
+    "ce_uniform": (check_ce_uniform, 1e-14),
+    "ce_library": (check_ce_library, 1e-7),
+    "ce_all_ignored": (check_ce_all_ignored, 0.5),
+    "block_special_cases": (check_block_special_cases, 1e-12),
+    "block_grad": (check_block_grad, 1e-7),
+}

@@ -1,0 +1,160 @@
+"""Pins of the fp64 oracle (CPU only).
+
+``test_pin`` runs every check of ``pins.py`` on the oracle.  ``test_mutant``
+plants a plausible mistake in a private copy of the oracle (on the CPU) and
+asserts that at least one pin then fails, so the pins are shown to be able to
+catch that class of error.
+"""
+import importlib.util
+import os
+
+import numpy as np
+import pytest
+
+import pins
+from oracle import coda_oracle
+
+ORACLE_SRC = os.path.join(os.path.dirname(coda_oracle.__file__), "coda_oracle.py")
+
+
+@pytest.mark.parametrize("name", sorted(pins.ALL_CHECKS))
+def test_pin(name):
+    fn, tol = pins.ALL_CHECKS[name]
+    err = fn(coda_oracle)
+    assert err <= tol, f"{name}: {err:.3e} > {tol:.1e}"
+
+
+def _fresh_copy(tag):
+    spec = importlib.util.spec_from_file_location(f"oracle_mutant_{tag}", ORACLE_SRC)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _mut_rms_eps_outside(m):
+    m.rms_inv = lambda x, eps: 1.0 / (np.sqrt(np.mean(np.asarray(x) ** 2, axis=-1)) + eps)
+
+
+def _mut_rmsnorm_bwd_drop_mean(m):
+    def bad(x, gamma, eps, dy):
+        r = m.rms_inv(x, eps)[..., None]
+        dx = r * (dy * gamma)
+        return dx, (dy * x * r).reshape(-1, x.shape[-1]).sum(axis=0)
+    m.rmsnorm_bwd = bad
+
+
+def _mut_rmsnorm_gamma_before(m):
+    m.rmsnorm = lambda x, gamma, eps: (x * gamma) * m.rms_inv(x * gamma, eps)[..., None]
+
+
+def _mut_silu_sign(m):
+    m.silu = lambda a: np.asarray(a, dtype=np.float64) / (1.0 + np.exp(np.asarray(a, dtype=np.float64)))
+
+
+def _mut_swiglu_swapped(m):
+    def bad(X, Wg, Wu):
+        g, u = X @ Wg.T, X @ Wu.T
+        return m.silu(u) * g, g, u
+    m.swiglu_fwd = bad
+
+
+def _mut_rope_sign(m):
+    orig = m.rope
+
+    def bad(v, pos, theta):
+        out = orig(v, pos, theta)
+        out[..., 1::2] *= -1.0
+        return out
+    m.rope = bad
+
+
+def _mut_rope_freq(m):
+    def bad(pos, head_dim, theta):
+        j = np.arange(head_dim // 2, dtype=np.float64)
+        return np.asarray(pos, dtype=np.float64)[:, None] * (theta ** (-j / head_dim))[None, :]
+    m.rope_angles = bad
+
+
+def _mut_ce_mean_over_all(m):
+    orig = m.linear_cross_entropy_fwd
+
+    def bad(X, W, labels, ignore_index=-100):
+        f = orig(X, W, labels, ignore_index)
+        if f["n_valid"] > 0:
+            f["loss"] = f["per_row"].sum() / len(labels)
+        return f
+    m.linear_cross_entropy_fwd = bad
+
+
+def _mut_ce_grad_no_onehot(m):
+    orig = m.linear_cross_entropy_bwd
+
+    def bad(X, W, labels, ignore_index=-100, dloss=1.0):
+        z = X @ W.T
+        p = np.exp(z - m._lse(z)[:, None])
+        valid = np.asarray(labels) != ignore_index
+        dZ = np.where(valid[:, None], p, 0.0) / max(int(valid.sum()), 1)
+        return {"dX": dZ @ W, "dW": dZ.T @ X, "dZ": dZ}
+    m.linear_cross_entropy_bwd = bad
+
+
+def _mut_block_mlp_on_x0(m):
+    orig = m.block_fwd
+
+    def bad(p, n_q, n_kv, head_dim, theta, eps):
+        f = orig(p, n_q, n_kv, head_dim, theta, eps)
+        mm = m.mlp_fwd(p["x0"], p["Wg"], p["Wu"], p["Wd"], p["x0"], p["gamma_mlp"], eps)
+        f["x2"] = mm["y"]
+        return f
+    m.block_fwd = bad
+
+
+def _mut_block_bwd_no_residual(m):
+    orig = m.block_bwd
+
+    def bad(p, n_q, n_kv, head_dim, theta, eps):
+        b = orig(p, n_q, n_kv, head_dim, theta, eps)
+        b["dx0"] = b["dx0"] - b["dx1"]
+        return b
+    m.block_bwd = bad
+
+
+def _mut_mlp_bwd_transposed(m):
+    orig = m.mlp_bwd
+
+    def bad(*a, **k):
+        b = orig(*a, **k)
+        b["dWg"], b["dWu"] = b["dWu"], b["dWg"]
+        return b
+    m.mlp_bwd = bad
+
+
+MUTANTS = {
+    "rms_eps_outside_root": _mut_rms_eps_outside,
+    "rmsnorm_bwd_drop_mean": _mut_rmsnorm_bwd_drop_mean,
+    "rmsnorm_gamma_before_norm": _mut_rmsnorm_gamma_before,
+    "silu_sign": _mut_silu_sign,
+    "swiglu_gate_on_up": _mut_swiglu_swapped,
+    "rope_sign": _mut_rope_sign,
+    "rope_frequency": _mut_rope_freq,
+    "ce_mean_over_all_rows": _mut_ce_mean_over_all,
+    "ce_grad_no_onehot": _mut_ce_grad_no_onehot,
+    "block_mlp_residual_x0": _mut_block_mlp_on_x0,
+    "block_bwd_no_residual": _mut_block_bwd_no_residual,
+    "mlp_bwd_swapped_weights": _mut_mlp_bwd_transposed,
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant(name):
+    m = _fresh_copy(name)
+    MUTANTS[name](m)
+    failed = []
+    for cname, (fn, tol) in pins.ALL_CHECKS.items():
+        try:
+            err = fn(m)
+        except Exception:
+            err = float("inf")
+        if not (err <= tol):
+            failed.append(cname)
+    assert failed, f"planted mistake {name!r} slipped past every pin"
