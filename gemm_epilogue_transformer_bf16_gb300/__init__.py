@@ -1,0 +1,402 @@
+"""Python binding of libcoda.so (C ABI in include/coda.h).
+
+Argument marshalling only: every step of every operator runs in the CUDA
+kernels of libcoda.so.  PyTorch supplies device memory and the current
+stream.  There is no CPU or PyTorch fallback: if the library is missing or a
+tensor is not on a CUDA device, calls raise.
+
+Function names mirror the C entry points without the ``coda_`` prefix.
+Tensors must be contiguous, bf16 tensors ``torch.bfloat16``, vectors
+``torch.float32``, labels/positions ``torch.int32``.  Workspaces are allocated
+with torch (the library never allocates) unless the caller passes ``ws=``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB as _LIB_PATH
+
+__all__ = [
+    "load", "CodaError", "lib_path", "status_string", "get_status", "reset_status",
+    "fold_gamma", "rms_rstd", "rope_table", "gemm_epilogue", "EpilogueDesc",
+    "rmsnorm_linear", "rmsnorm_linear_bwd", "linear_residual", "linear_residual_bwd",
+    "linear_swiglu", "linear_swiglu_bwd", "linear_qknorm_rope", "linear_qknorm_rope_bwd",
+    "linear_cross_entropy", "linear_cross_entropy_bwd", "workspace",
+    "MAP_NONE", "MAP_SWIGLU", "MAP_DSWIGLU", "MAP_QKNORM_ROPE", "MAP_CE_LSE",
+    "MAP_CE_DLOGITS", "MAP_COLDOT", "K_MAJOR", "MN_MAJOR",
+]
+
+K_MAJOR, MN_MAJOR = 0, 1
+BF16, F32 = 0, 1
+(MAP_NONE, MAP_SWIGLU, MAP_DSWIGLU, MAP_QKNORM_ROPE, MAP_CE_LSE, MAP_CE_DLOGITS,
+ MAP_COLDOT) = range(7)
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+# name -> argtypes (restype int unless noted)
+_SIGS = {
+    "coda_version": ([], ctypes.c_char_p),
+    "coda_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "coda_get_status": ([_P, _P], ctypes.c_int),
+    "coda_reset_status": ([_P, _P], ctypes.c_int),
+    "coda_gemm_epilogue_workspace_size": ([], _SZ),
+    "coda_gemm_epilogue": ([_P, _P, _I64, ctypes.c_int, _P, _I64, ctypes.c_int, _P, _I64, ctypes.c_int,
+                            _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_fold_gamma": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
+    "coda_rms_rstd": ([_P, _I64, _I64, _I64, _F, _P, _P], ctypes.c_int),
+    "coda_rope_table": ([_F, _I32, _I32, _P, _P], ctypes.c_int),
+    "coda_rmsnorm_linear_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_rmsnorm_linear": ([_P, _P, _P, _P, _F, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_rmsnorm_linear_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_rmsnorm_linear_bwd": ([_P] * 11 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_residual_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_residual": ([_P, _P, _P, _P, _F, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_residual_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_residual_bwd": ([_P] * 5 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_swiglu_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_swiglu": ([_P] * 7 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_swiglu_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_swiglu_bwd": ([_P] * 18 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_qknorm_rope_workspace_size": ([_I64, _I64, _I32, _I32, _I32], _SZ),
+    "coda_linear_qknorm_rope": ([_P] * 7 + [_I32, _F, _I32, _I32, _I32] + [_P] * 4 + [_I64, _I64, _P, _SZ, _P],
+                                ctypes.c_int),
+    "coda_linear_qknorm_rope_bwd_workspace_size": ([_I64, _I64, _I32, _I32, _I32], _SZ),
+    "coda_linear_qknorm_rope_bwd": ([_P] * 9 + [_I32, _F, _I32, _I32, _I32] + [_P] * 11
+                                    + [_I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_cross_entropy_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_cross_entropy": ([_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_cross_entropy_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_cross_entropy_bwd": ([_P, _P, _P, _I32, _P, _P, _F, _P, _P, _I64, _I64, _I64, _P, _SZ, _P],
+                                      ctypes.c_int),
+}
+
+
+class CodaError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} failed: {status_string(code)} ({code})")
+
+
+_lib = None
+
+
+def lib_path():
+    return _LIB_PATH
+
+
+def load():
+    """Load libcoda.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(there is no fallback implementation)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+    return _lib
+
+
+def status_string(code):
+    return load().coda_status_string(int(code)).decode()
+
+
+class EpilogueDesc(ctypes.Structure):
+    _fields_ = [
+        ("map", _I32), ("row_scale", _P), ("col_scale", _P),
+        ("aux_in", _P * 2), ("ld_aux_in", _I64 * 2), ("row_coef", _P),
+        ("aux_out", _P * 3), ("ld_aux_out", _I64 * 3), ("partials", _P), ("ld_partials", _I64),
+        ("beta", _I32), ("B2", _P), ("ldb2", _I64), ("A2", _P), ("lda2", _I64), ("K2", _I64),
+        ("labels", _P), ("ignore_index", _I32), ("lse", _P), ("n_valid", _P), ("dloss", _F),
+        ("target_logit", _P), ("vocab_tiles_per_unit", _I32),
+        ("positions", _P), ("cos_sin", _P), ("max_pos", _I32), ("n_q_heads", _I32),
+        ("n_kv_heads", _I32), ("head_dim", _I32), ("eps", _F), ("gamma_q", _P), ("gamma_k", _P),
+        ("Q", _P), ("K", _P), ("V", _P),
+    ]
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t.data_ptr()
+
+
+def _bf(t, name="tensor"):
+    return _ptr(t, torch.bfloat16, name)
+
+
+def _f32(t, name="tensor"):
+    return _ptr(t, torch.float32, name)
+
+
+def _i32(t, name="tensor"):
+    return _ptr(t, torch.int32, name)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(fn, code):
+    if code != 0:
+        raise CodaError(fn, code)
+
+
+def workspace(nbytes, device=None):
+    """A zeroed byte workspace (status word cleared) of at least nbytes."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(ws, need, device):
+    if ws is None:
+        return workspace(need, device)
+    if ws.numel() < need:
+        raise ValueError(f"workspace too small: {ws.numel()} < {need}")
+    return ws
+
+
+def get_status(ws, stream=None):
+    return load().coda_get_status(_ptr(ws), _stream(stream))
+
+
+def reset_status(ws, stream=None):
+    _check("coda_reset_status", load().coda_reset_status(_ptr(ws), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# operators
+# ---------------------------------------------------------------------------
+
+def fold_gamma(W, gamma, out=None, stream=None):
+    N, K = W.shape
+    out = torch.empty_like(W) if out is None else out
+    _check("coda_fold_gamma", load().coda_fold_gamma(_bf(W, "W"), _f32(gamma, "gamma"), _bf(out, "Wf"), N, K,
+                                                     _stream(stream)))
+    return out
+
+
+def rms_rstd(X, eps, out=None, stream=None):
+    M, K = X.shape
+    out = torch.empty(M, dtype=torch.float32, device=X.device) if out is None else out
+    _check("coda_rms_rstd", load().coda_rms_rstd(_bf(X, "X"), K, M, K, float(eps), _f32(out, "rstd"),
+                                                 _stream(stream)))
+    return out
+
+
+def rope_table(theta, head_dim, max_pos, device="cuda", out=None, stream=None):
+    out = torch.empty(max_pos, head_dim // 2, 2, dtype=torch.float32, device=device) if out is None else out
+    _check("coda_rope_table", load().coda_rope_table(float(theta), int(head_dim), int(max_pos),
+                                                     _f32(out, "cos_sin"), _stream(stream)))
+    return out
+
+
+def gemm_epilogue(desc, A, B, D, M, N, K, a_major=K_MAJOR, b_major=K_MAJOR, lda=None, ldb=None, ldd=None,
+                  ws=None, stream=None):
+    """Generic GEMM + epilogue (coda_gemm_epilogue).  `desc` is an
+    EpilogueDesc whose pointer fields hold data_ptr() values."""
+    lib = load()
+    lda = lda if lda is not None else (K if a_major == K_MAJOR else M)
+    ldb = ldb if ldb is not None else (K if b_major == K_MAJOR else N)
+    ldd = ldd if ldd is not None else N
+    dtype = F32 if (D is not None and D.dtype == torch.float32) else BF16
+    ws = _ws(ws, lib.coda_gemm_epilogue_workspace_size(), A.device)
+    _check("coda_gemm_epilogue", lib.coda_gemm_epilogue(
+        ctypes.byref(desc), _bf(A, "A"), lda, a_major, _bf(B, "B"), ldb, b_major,
+        _ptr(D, None, "D"), ldd, dtype, M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+def rmsnorm_linear(X, Wf, R=None, rstd_in=None, eps=1e-6, rstd_out=None, Y=None, ws=None, stream=None):
+    lib = load()
+    M, K = X.shape
+    N = Wf.shape[0]
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    if rstd_in is None and rstd_out is None:
+        rstd_out = torch.empty(M, dtype=torch.float32, device=X.device)
+    ws = _ws(ws, lib.coda_rmsnorm_linear_workspace_size(M, N, K), X.device)
+    _check("coda_rmsnorm_linear", lib.coda_rmsnorm_linear(
+        _bf(X, "X"), _f32(rstd_in, "rstd_in"), _bf(Wf, "Wf"), _bf(R, "R"), float(eps), _f32(rstd_out, "rstd_out"),
+        _bf(Y, "Y"), M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
+    return Y, (rstd_in if rstd_in is not None else rstd_out)
+
+
+def rmsnorm_linear_bwd(dY, X, W, Wf, gamma, rstd, Y, R=None, ws=None, out=None, stream=None):
+    lib = load()
+    M, K = X.shape
+    N = W.shape[0]
+    if out is None:
+        out = {"dX": torch.empty_like(X), "dW": torch.empty_like(W),
+               "dgamma": torch.empty(K, dtype=torch.float32, device=X.device)}
+    ws = _ws(ws, lib.coda_rmsnorm_linear_bwd_workspace_size(M, N, K), X.device)
+    _check("coda_rmsnorm_linear_bwd", lib.coda_rmsnorm_linear_bwd(
+        _bf(dY, "dY"), _bf(X, "X"), _bf(W, "W"), _bf(Wf, "Wf"), _f32(gamma, "gamma"), _f32(rstd, "rstd"),
+        _bf(Y, "Y"), _bf(R, "R"), _bf(out["dX"], "dX"), _bf(out["dW"], "dW"), _f32(out["dgamma"], "dgamma"),
+        M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def linear_residual(X, W, R=None, eps=1e-6, want_rstd=False, Y=None, rstd_out=None, ws=None, stream=None):
+    lib = load()
+    M, K = X.shape
+    N = W.shape[0]
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    if want_rstd and rstd_out is None:
+        rstd_out = torch.empty(M, dtype=torch.float32, device=X.device)
+    ws = _ws(ws, lib.coda_linear_residual_workspace_size(M, N, K), X.device)
+    _check("coda_linear_residual", lib.coda_linear_residual(
+        _bf(X, "X"), _bf(W, "W"), _bf(R, "R"), _bf(Y, "Y"), float(eps), _f32(rstd_out, "rstd_out"),
+        M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
+    return (Y, rstd_out) if want_rstd or rstd_out is not None else Y
+
+
+def linear_residual_bwd(dY, X, W, ws=None, out=None, stream=None):
+    lib = load()
+    M, K = X.shape
+    N = W.shape[0]
+    if out is None:
+        out = {"dX": torch.empty_like(X), "dW": torch.empty_like(W)}
+    ws = _ws(ws, lib.coda_linear_residual_bwd_workspace_size(M, N, K), X.device)
+    _check("coda_linear_residual_bwd", lib.coda_linear_residual_bwd(
+        _bf(dY, "dY"), _bf(X, "X"), _bf(W, "W"), _bf(out["dX"], "dX"), _bf(out["dW"], "dW"),
+        M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def linear_swiglu(X, Wg, Wu, rstd=None, save=True, H=None, g=None, u=None, ws=None, stream=None):
+    lib = load()
+    M, K = X.shape
+    I = Wg.shape[0]
+    dev = X.device
+    H = torch.empty(M, I, dtype=torch.bfloat16, device=dev) if H is None else H
+    if save:
+        g = torch.empty(M, I, dtype=torch.bfloat16, device=dev) if g is None else g
+        u = torch.empty(M, I, dtype=torch.bfloat16, device=dev) if u is None else u
+    ws = _ws(ws, lib.coda_linear_swiglu_workspace_size(M, I, K), dev)
+    _check("coda_linear_swiglu", lib.coda_linear_swiglu(
+        _bf(X, "X"), _f32(rstd, "rstd"), _bf(Wg, "Wg"), _bf(Wu, "Wu"), _bf(H, "H"), _bf(g, "g"), _bf(u, "u"),
+        M, I, K, _ptr(ws), ws.numel(), _stream(stream)))
+    return H, g, u
+
+
+def linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=None, gamma=None, Wgf=None, Wuf=None, dX_resid=None,
+                      ws=None, out=None, stream=None):
+    lib = load()
+    M, K = X.shape
+    I = Wg.shape[0]
+    dev = X.device
+    Wgf = Wg if Wgf is None else Wgf
+    Wuf = Wu if Wuf is None else Wuf
+    if out is None:
+        out = {"dX": torch.empty_like(X), "dWg": torch.empty_like(Wg), "dWu": torch.empty_like(Wu),
+               "dWd": torch.empty_like(Wd),
+               "dgamma": torch.empty(K, dtype=torch.float32, device=dev) if rstd is not None else None}
+    ws = _ws(ws, lib.coda_linear_swiglu_bwd_workspace_size(M, I, K), dev)
+    _check("coda_linear_swiglu_bwd", lib.coda_linear_swiglu_bwd(
+        _bf(dY, "dY"), _bf(X, "X"), _f32(rstd, "rstd"), _f32(gamma, "gamma"), _bf(Wg, "Wg"), _bf(Wu, "Wu"),
+        _bf(Wgf, "Wgf"), _bf(Wuf, "Wuf"), _bf(Wd, "Wd"), _bf(g, "g"), _bf(u, "u"), _bf(H, "H"),
+        _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"), _bf(out["dWg"], "dWg"), _bf(out["dWu"], "dWu"),
+        _bf(out["dWd"], "dWd"), _f32(out.get("dgamma"), "dgamma"), M, I, K, _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+def linear_qknorm_rope(X, Wf_qkv, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, rstd=None, eps=1e-6,
+                       head_dim=128, save=True, out=None, ws=None, stream=None):
+    lib = load()
+    M, Kd = X.shape
+    dev = X.device
+    if out is None:
+        out = {"Q": torch.empty(M, n_q * head_dim, dtype=torch.bfloat16, device=dev),
+               "K": torch.empty(M, n_kv * head_dim, dtype=torch.bfloat16, device=dev),
+               "V": torch.empty(M, n_kv * head_dim, dtype=torch.bfloat16, device=dev),
+               "qk_save": torch.empty(M, (n_q + n_kv) * head_dim, dtype=torch.bfloat16, device=dev)
+               if save else None}
+    max_pos = cos_sin.shape[0]
+    ws = _ws(ws, lib.coda_linear_qknorm_rope_workspace_size(M, Kd, n_q, n_kv, head_dim), dev)
+    _check("coda_linear_qknorm_rope", lib.coda_linear_qknorm_rope(
+        _bf(X, "X"), _f32(rstd, "rstd"), _bf(Wf_qkv, "Wf_qkv"), _f32(gamma_q, "gamma_q"),
+        _f32(gamma_k, "gamma_k"), _i32(pos, "pos"), _f32(cos_sin, "cos_sin"), max_pos, float(eps),
+        n_q, n_kv, head_dim, _bf(out["Q"], "Q"), _bf(out["K"], "K"), _bf(out["V"], "V"),
+        _bf(out.get("qk_save"), "qk_save"), M, Kd, _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def linear_qknorm_rope_bwd(dQ, dK, dV, qk_save, V, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, X, W_qkv,
+                           Wf_qkv=None, rstd=None, gamma_in=None, dX_resid=None, eps=1e-6, head_dim=128,
+                           ws=None, out=None, stream=None):
+    lib = load()
+    M, Kd = X.shape
+    dev = X.device
+    Wf_qkv = W_qkv if Wf_qkv is None else Wf_qkv
+    if out is None:
+        out = {"dX": torch.empty_like(X), "dW": torch.empty_like(W_qkv),
+               "dgamma_in": torch.empty(Kd, dtype=torch.float32, device=dev) if rstd is not None else None,
+               "dgamma_q": torch.empty(head_dim, dtype=torch.float32, device=dev),
+               "dgamma_k": torch.empty(head_dim, dtype=torch.float32, device=dev)}
+    max_pos = cos_sin.shape[0]
+    ws = _ws(ws, lib.coda_linear_qknorm_rope_bwd_workspace_size(M, Kd, n_q, n_kv, head_dim), dev)
+    _check("coda_linear_qknorm_rope_bwd", lib.coda_linear_qknorm_rope_bwd(
+        _bf(dQ, "dQ"), _bf(dK, "dK"), _bf(dV, "dV"), _bf(qk_save, "qk_save"), _bf(V, "V"),
+        _f32(gamma_q, "gamma_q"), _f32(gamma_k, "gamma_k"), _i32(pos, "pos"), _f32(cos_sin, "cos_sin"),
+        max_pos, float(eps), n_q, n_kv, head_dim, _bf(X, "X"), _f32(rstd, "rstd"), _f32(gamma_in, "gamma_in"),
+        _bf(W_qkv, "W_qkv"), _bf(Wf_qkv, "Wf_qkv"), _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"),
+        _bf(out["dW"], "dW"), _f32(out.get("dgamma_in"), "dgamma_in"), _f32(out["dgamma_q"], "dgamma_q"),
+        _f32(out["dgamma_k"], "dgamma_k"), M, Kd, _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def linear_cross_entropy(X, W, labels, ignore_index=-100, out=None, ws=None, stream=None):
+    lib = load()
+    M, K = X.shape
+    V = W.shape[0]
+    dev = X.device
+    if out is None:
+        out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
+               "lse": torch.empty(M, dtype=torch.float32, device=dev),
+               "n_valid": torch.empty(1, dtype=torch.int32, device=dev)}
+    ws = _ws(ws, lib.coda_linear_cross_entropy_workspace_size(M, V, K), dev)
+    _check("coda_linear_cross_entropy", lib.coda_linear_cross_entropy(
+        _bf(X, "X"), _bf(W, "W"), _i32(labels, "labels"), int(ignore_index), _f32(out["loss"], "loss"),
+        _f32(out["lse"], "lse"), _i32(out["n_valid"], "n_valid"), M, V, K, _ptr(ws), ws.numel(),
+        _stream(stream)))
+    out["ws"] = ws
+    return out
+
+
+def linear_cross_entropy_bwd(X, W, labels, lse, n_valid, dloss=1.0, ignore_index=-100, out=None, ws=None,
+                             stream=None):
+    lib = load()
+    M, K = X.shape
+    V = W.shape[0]
+    if out is None:
+        out = {"dX": torch.empty_like(X), "dW": torch.empty_like(W)}
+    ws = _ws(ws, lib.coda_linear_cross_entropy_bwd_workspace_size(M, V, K), X.device)
+    _check("coda_linear_cross_entropy_bwd", lib.coda_linear_cross_entropy_bwd(
+        _bf(X, "X"), _bf(W, "W"), _i32(labels, "labels"), int(ignore_index), _f32(lse, "lse"),
+        _i32(n_valid, "n_valid"), float(dloss), _bf(out["dX"], "dX"), _bf(out["dW"], "dW"), M, V, K,
+        _ptr(ws), ws.numel(), _stream(stream)))
+    out["ws"] = ws
+    return out

@@ -1,0 +1,127 @@
+"""The non-attention transformer block as a sequence of GEMM-epilogue calls.
+
+Forward ("CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
+§3.2.1, sites 1 and 2 of the GEMM-residual-RMSNorm-GEMM pattern):
+
+  fold   Wqkv' = Wqkv diag(gamma_attn), Wg' / Wu' = W diag(gamma_mlp)
+  rstd0  r0 = 1/rms(x0)                        (x0 has no producing GEMM here)
+  qkv    Q, K, V = QKnorm+RoPE epilogue of r0 ⊙ (x0 Wqkv'^T)
+         [attention itself is out of scope: its output A is an input]
+  oproj  x1 = x0 + A Wo^T, epilogue partial sums of squares -> r1
+  gateup H = silu(r1 ⊙ x1 Wg'^T) ⊙ (r1 ⊙ x1 Wu'^T)       (SwiGLU epilogue)
+  down   x2 = x1 + H Wd^T                                  (residual epilogue)
+
+Backward (given dx2 and the attention-input gradients dQ, dK, dV):
+
+  mlp    dSwiGLU epilogue on dH = dx2 Wd, reparameterised RMSNorm backward,
+         dx1 = dx2 + mlp branch; dWg, dWu, dWd, dgamma_mlp
+  oproj  dA = dx1 Wo, dWo = dx1^T A
+  qkv    QK-norm+RoPE backward map, reparameterised RMSNorm backward,
+         dx0 = dx1 + qkv branch; dWqkv, dgamma_attn, dgamma_q, dgamma_k
+
+Every step is a libcoda.so call on the current stream; buffers and one shared
+workspace are allocated once, so a step launches only the library's kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (fold_gamma, linear_cross_entropy, linear_cross_entropy_bwd, linear_qknorm_rope,
+               linear_qknorm_rope_bwd, linear_residual, linear_residual_bwd, linear_swiglu, linear_swiglu_bwd,
+               load, rms_rstd, rope_table, workspace)
+
+
+class Block:
+    def __init__(self, shape, weights, device="cuda"):
+        self.s = s = shape
+        self.w = weights
+        lib = load()
+        T, Hd, I, d = s.tokens, s.hidden, s.inter, s.head_dim
+        nqkv = s.qkv_out
+        bf = dict(dtype=torch.bfloat16, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        e = torch.empty
+        self.Wqkv_f = e(nqkv, Hd, **bf)
+        self.Wg_f = e(I, Hd, **bf)
+        self.Wu_f = e(I, Hd, **bf)
+        self.cos_sin = rope_table(s.theta, d, s.seq_len, device=device)
+        self.rstd0 = e(T, **f32)
+        self.rstd1 = e(T, **f32)
+        self.fwd = {"Q": e(T, s.n_q * d, **bf), "K": e(T, s.n_kv * d, **bf), "V": e(T, s.n_kv * d, **bf),
+                    "qk_save": e(T, (s.n_q + s.n_kv) * d, **bf)}
+        self.x1 = e(T, Hd, **bf)
+        self.x2 = e(T, Hd, **bf)
+        self.H = e(T, I, **bf)
+        self.g = e(T, I, **bf)
+        self.u = e(T, I, **bf)
+        self.dx1 = e(T, Hd, **bf)
+        self.grads_mlp = {"dX": self.dx1, "dWg": e(I, Hd, **bf), "dWu": e(I, Hd, **bf), "dWd": e(Hd, I, **bf),
+                          "dgamma": e(Hd, **f32)}
+        self.grads_o = {"dX": e(T, s.n_q * d, **bf), "dW": e(Hd, s.n_q * d, **bf)}
+        self.grads_qkv = {"dX": e(T, Hd, **bf), "dW": e(nqkv, Hd, **bf), "dgamma_in": e(Hd, **f32),
+                          "dgamma_q": e(d, **f32), "dgamma_k": e(d, **f32)}
+        need = max(
+            lib.coda_linear_qknorm_rope_workspace_size(T, Hd, s.n_q, s.n_kv, d),
+            lib.coda_linear_residual_workspace_size(T, Hd, s.n_q * d),
+            lib.coda_linear_swiglu_workspace_size(T, I, Hd),
+            lib.coda_linear_residual_workspace_size(T, Hd, I),
+            lib.coda_linear_swiglu_bwd_workspace_size(T, I, Hd),
+            lib.coda_linear_residual_bwd_workspace_size(T, Hd, s.n_q * d),
+            lib.coda_linear_qknorm_rope_bwd_workspace_size(T, Hd, s.n_q, s.n_kv, d),
+        )
+        self.ws = workspace(need, device)
+
+    # ------------------------------------------------------------------ forward
+    def forward(self, x0, A, pos):
+        s, w = self.s, self.w
+        fold_gamma(w["Wqkv"], w["gamma_attn"], out=self.Wqkv_f)
+        fold_gamma(w["Wg"], w["gamma_mlp"], out=self.Wg_f)
+        fold_gamma(w["Wu"], w["gamma_mlp"], out=self.Wu_f)
+        rms_rstd(x0, s.eps, out=self.rstd0)
+        linear_qknorm_rope(x0, self.Wqkv_f, w["gamma_q"], w["gamma_k"], pos, self.cos_sin, s.n_q, s.n_kv,
+                           rstd=self.rstd0, eps=s.eps, head_dim=s.head_dim, out=self.fwd, ws=self.ws)
+        linear_residual(A, w["Wo"], x0, eps=s.eps, Y=self.x1, rstd_out=self.rstd1, ws=self.ws)
+        linear_swiglu(self.x1, self.Wg_f, self.Wu_f, rstd=self.rstd1, H=self.H, g=self.g, u=self.u, ws=self.ws)
+        linear_residual(self.H, w["Wd"], self.x1, Y=self.x2, ws=self.ws)
+        return {"Q": self.fwd["Q"], "K": self.fwd["K"], "V": self.fwd["V"], "x1": self.x1, "x2": self.x2}
+
+    # ------------------------------------------------------------------ backward
+    def backward(self, x0, A, pos, dx2, dQ, dK, dV):
+        s, w = self.s, self.w
+        linear_swiglu_bwd(dx2, self.x1, w["Wg"], w["Wu"], w["Wd"], self.g, self.u, self.H, rstd=self.rstd1,
+                          gamma=w["gamma_mlp"], Wgf=self.Wg_f, Wuf=self.Wu_f, dX_resid=dx2, ws=self.ws,
+                          out=self.grads_mlp)
+        linear_residual_bwd(self.dx1, A, w["Wo"], ws=self.ws, out=self.grads_o)
+        linear_qknorm_rope_bwd(dQ, dK, dV, self.fwd["qk_save"], self.fwd["V"], w["gamma_q"], w["gamma_k"], pos,
+                               self.cos_sin, s.n_q, s.n_kv, x0, w["Wqkv"], Wf_qkv=self.Wqkv_f, rstd=self.rstd0,
+                               gamma_in=w["gamma_attn"], dX_resid=self.dx1, eps=s.eps, head_dim=s.head_dim,
+                               ws=self.ws, out=self.grads_qkv)
+        return {"dx0": self.grads_qkv["dX"], "dA": self.grads_o["dX"], "dx1": self.dx1,
+                "dWqkv": self.grads_qkv["dW"], "dWo": self.grads_o["dW"], "dWg": self.grads_mlp["dWg"],
+                "dWu": self.grads_mlp["dWu"], "dWd": self.grads_mlp["dWd"],
+                "dgamma_attn": self.grads_qkv["dgamma_in"], "dgamma_mlp": self.grads_mlp["dgamma"],
+                "dgamma_q": self.grads_qkv["dgamma_q"], "dgamma_k": self.grads_qkv["dgamma_k"]}
+
+    def step(self, x0, A, pos, dx2, dQ, dK, dV):
+        self.forward(x0, A, pos)
+        return self.backward(x0, A, pos, dx2, dQ, dK, dV)
+
+
+class LinearCE:
+    """Linear + cross-entropy forward and backward with persistent buffers."""
+
+    def __init__(self, M, V, K, device="cuda"):
+        lib = load()
+        self.out = {"loss": torch.empty(1, dtype=torch.float32, device=device),
+                    "lse": torch.empty(M, dtype=torch.float32, device=device),
+                    "n_valid": torch.empty(1, dtype=torch.int32, device=device)}
+        self.grads = {"dX": torch.empty(M, K, dtype=torch.bfloat16, device=device),
+                      "dW": torch.empty(V, K, dtype=torch.bfloat16, device=device)}
+        self.ws = workspace(max(lib.coda_linear_cross_entropy_workspace_size(M, V, K),
+                                lib.coda_linear_cross_entropy_bwd_workspace_size(M, V, K)), device)
+
+    def step(self, X, W, labels, ignore_index=-100):
+        linear_cross_entropy(X, W, labels, ignore_index, out=self.out, ws=self.ws)
+        linear_cross_entropy_bwd(X, W, labels, self.out["lse"], self.out["n_valid"], 1.0, ignore_index,
+                                 out=self.grads, ws=self.ws)
+        return self.out, self.grads

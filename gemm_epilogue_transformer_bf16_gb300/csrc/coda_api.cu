@@ -1,0 +1,1094 @@
+// Host side of libcoda.so: argument validation, TMA tensor-map encoding,
+// tile-grid planning and the launch sequences of the named operators declared
+// in include/coda.h.  Nothing here allocates device memory: scratch lives in
+// the caller's workspace, whose first 256 bytes are the device status word.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "coda.h"
+#include "coda_internal.h"
+#include "coda_status.h"
+
+using coda::EpiArgs;
+using coda::GemmArgs;
+
+namespace {
+
+constexpr size_t WS_HEADER = 256;
+constexpr int BN = 256;
+constexpr uint64_t TIMEOUT_NS = 2000000000ull;  // 2 s per pipeline wait
+constexpr int CE_TILES_PER_UNIT = 16;
+
+// ------------------------------------------------------------------ helpers
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsCursor {
+  uint8_t* base;
+  size_t off;
+  explicit WsCursor(void* ws) : base(static_cast<uint8_t*>(ws)), off(WS_HEADER) {}
+  template <class T>
+  T* take(size_t count) {
+    T* p = reinterpret_cast<T*>(base + off);
+    off = up256(off + count * sizeof(T));
+    return p;
+  }
+};
+
+struct SizeCursor {
+  size_t off = WS_HEADER;
+  template <class T>
+  void take(size_t count) { off = up256(off + count * sizeof(T)); }
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+int g_num_sms[64] = {0};
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride
+// `ld` elements; box = box_cols x box_rows, 128-byte swizzle, zero fill.
+bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_cols,
+                uint32_t box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// One GEMM + epilogue launch.
+struct Plan {
+  coda::EpiKind kind = coda::EpiKind::Plain;
+  const void* A = nullptr;
+  int64_t lda = 0;
+  int a_mn = 0;
+  const void* B = nullptr;
+  int64_t ldb = 0;
+  int b_mn = 0;
+  const void* A2 = nullptr;  // concatenated-K second pair
+  int64_t lda2 = 0;
+  const void* B2 = nullptr;  // second pair's B, or SwiGLU up weight (b_dual)
+  int64_t ldb2 = 0;
+  int64_t K2 = 0;
+  int b_dual = 0;
+  int64_t M = 0, N = 0, K = 0;
+  int n_per_unit = 1;
+  EpiArgs e{};
+};
+
+int run(const Plan& p, int* status, cudaStream_t s) {
+  if (p.M == 0 || p.N == 0) return CODA_OK;
+  if (!get_encoder()) return CODA_ERR_CUDA;
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  CUtensorMap maps[4];
+  std::memset(maps, 0, sizeof(maps));
+  // A operands
+  auto enc_a = [&](CUtensorMap* m, const void* ptr, int64_t ld, int64_t Kc) {
+    return p.a_mn ? encode_map(m, ptr, Kc, p.M, ld, 64, 64) : encode_map(m, ptr, p.M, Kc, ld, 64, 128);
+  };
+  auto enc_b = [&](CUtensorMap* m, const void* ptr, int64_t ld, int64_t Kc) {
+    return p.b_mn ? encode_map(m, ptr, Kc, p.N, ld, 64, 64) : encode_map(m, ptr, p.N, Kc, ld, 64, BN);
+  };
+  if (!enc_a(&maps[0], p.A, p.lda, p.K)) return CODA_ERR_CUDA;
+  if (p.b_dual) {
+    if (!encode_map(&maps[1], p.B, p.N, p.K, p.ldb, 64, BN / 2)) return CODA_ERR_CUDA;
+    if (!encode_map(&maps[3], p.B2, p.N, p.K, p.ldb2, 64, BN / 2)) return CODA_ERR_CUDA;
+    maps[2] = maps[0];
+  } else {
+    if (!enc_b(&maps[1], p.B, p.ldb, p.K)) return CODA_ERR_CUDA;
+    if (p.K2 > 0) {
+      if (!enc_a(&maps[2], p.A2, p.lda2, p.K2)) return CODA_ERR_CUDA;
+      if (!enc_b(&maps[3], p.B2, p.ldb2, p.K2)) return CODA_ERR_CUDA;
+    } else {
+      maps[2] = maps[0];
+      maps[3] = maps[1];
+    }
+  }
+  GemmArgs a{};
+  a.M = static_cast<int>(p.M);
+  a.N = static_cast<int>(p.N);
+  a.num_m = static_cast<int>(cdiv(p.M, coda::BM));
+  a.num_n = static_cast<int>(cdiv(p.N, p.b_dual ? BN / 2 : BN));
+  a.kb0 = static_cast<int>(cdiv(p.K, coda::BK));
+  a.kb1 = p.K2 > 0 ? static_cast<int>(cdiv(p.K2, coda::BK)) : 0;
+  a.a_mn = p.a_mn;
+  a.b_mn = p.b_mn;
+  a.b_dual = p.b_dual;
+  a.n_per_unit = p.n_per_unit;
+  a.num_units = p.n_per_unit > 1 ? a.num_m * static_cast<int>(cdiv(a.num_n, p.n_per_unit)) : a.num_m * a.num_n;
+  a.group_m = 16;
+  a.idesc = coda::idesc_bf16(coda::BM, BN, p.a_mn, p.b_mn);
+  a.status = status;
+  a.timeout_ns = TIMEOUT_NS;
+  a.e = p.e;
+  const dim3 grid(static_cast<unsigned>(std::min(a.num_units, sms)));
+  cudaError_t err;
+  switch (p.kind) {
+    case coda::EpiKind::Plain: err = coda::launch_gemm_plain(grid, s, maps, a); break;
+    case coda::EpiKind::Swiglu: err = coda::launch_gemm_swiglu(grid, s, maps, a); break;
+    case coda::EpiKind::DSwiglu: err = coda::launch_gemm_dswiglu(grid, s, maps, a); break;
+    case coda::EpiKind::QkRope: err = coda::launch_gemm_qkrope(grid, s, maps, a); break;
+    case coda::EpiKind::CeLse: err = coda::launch_gemm_celse(grid, s, maps, a); break;
+    case coda::EpiKind::CeDlogits: err = coda::launch_gemm_cedlogits(grid, s, maps, a); break;
+    case coda::EpiKind::ColDot: err = coda::launch_gemm_coldot(grid, s, maps, a); break;
+    default: return CODA_ERR_INVALID_ARG;
+  }
+  return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
+}
+
+#define CK(x)                  \
+  do {                         \
+    int _r = (x);              \
+    if (_r != CODA_OK) return _r; \
+  } while (0)
+#define CU(x) \
+  do { if ((x) != cudaSuccess) return CODA_ERR_CUDA; } while (0)
+
+// Argument checks.  `need` pointers must be non-null; every non-null pointer
+// must be 16-byte aligned.
+int req(const void* p) { return p ? CODA_OK : CODA_ERR_INVALID_ARG; }
+int al(const void* p) { return (p == nullptr || al16(p)) ? CODA_OK : CODA_ERR_ALIGNMENT; }
+int ldok(int64_t ld, int64_t cols) {
+  if (ld < cols) return CODA_ERR_INVALID_ARG;
+  return (ld % 8) ? CODA_ERR_ALIGNMENT : CODA_OK;
+}
+int dims_ok(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return CODA_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return CODA_ERR_UNSUPPORTED;
+  if (N % 8 || K % 8) return CODA_ERR_UNSUPPORTED;
+  if (K == 0 && M > 0 && N > 0) return CODA_ERR_UNSUPPORTED;
+  return CODA_OK;
+}
+int ws_ok(const void* ws, size_t have, size_t need) {
+  if (!ws || have < need) return CODA_ERR_WORKSPACE;
+  return al16(ws) ? CODA_OK : CODA_ERR_ALIGNMENT;
+}
+
+cudaStream_t S(coda_stream s) { return static_cast<cudaStream_t>(s); }
+const __nv_bfloat16* BF(const coda_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
+__nv_bfloat16* BF(coda_bf16* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
+
+}  // namespace
+
+extern "C" {
+
+const char* coda_version(void) { return "coda-gb300 0.1.0 (sm_103a)"; }
+
+const char* coda_status_string(int st) {
+  switch (st) {
+    case CODA_OK: return "CODA_OK";
+    case CODA_ERR_INVALID_ARG: return "CODA_ERR_INVALID_ARG";
+    case CODA_ERR_ALIGNMENT: return "CODA_ERR_ALIGNMENT";
+    case CODA_ERR_UNSUPPORTED: return "CODA_ERR_UNSUPPORTED";
+    case CODA_ERR_WORKSPACE: return "CODA_ERR_WORKSPACE";
+    case CODA_ERR_CUDA: return "CODA_ERR_CUDA";
+    case CODA_ERR_TIMEOUT: return "CODA_ERR_TIMEOUT";
+    case CODA_ERR_LABEL_RANGE: return "CODA_ERR_LABEL_RANGE";
+    case CODA_ERR_POSITION_RANGE: return "CODA_ERR_POSITION_RANGE";
+    default: return "CODA_ERR_UNKNOWN";
+  }
+}
+
+int coda_get_status(const void* ws, coda_stream stream) {
+  if (!ws) return CODA_ERR_INVALID_ARG;
+  int word = 0;
+  CU(cudaStreamSynchronize(S(stream)));
+  CU(cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost));
+  if (word & CODA_DEV_TIMEOUT) return CODA_ERR_TIMEOUT;
+  if (word & CODA_DEV_LABEL_RANGE) return CODA_ERR_LABEL_RANGE;
+  if (word & CODA_DEV_POSITION_RANGE) return CODA_ERR_POSITION_RANGE;
+  return CODA_OK;
+}
+
+int coda_reset_status(void* ws, coda_stream stream) {
+  if (!ws) return CODA_ERR_INVALID_ARG;
+  CU(cudaMemsetAsync(ws, 0, sizeof(int), S(stream)));
+  return CODA_OK;
+}
+
+// ------------------------------------------------------------------ generic
+size_t coda_gemm_epilogue_workspace_size(void) { return WS_HEADER; }
+
+int coda_gemm_epilogue(const coda_epilogue_desc* d, const coda_bf16* A, int64_t lda, int a_major,
+                       const coda_bf16* B, int64_t ldb, int b_major, void* D, int64_t ldd, int d_dtype, int64_t M,
+                       int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream) {
+  CK(req(d));
+  CK(dims_ok(M, N, K));
+  CK(ws_ok(ws, ws_bytes, WS_HEADER));
+  if (a_major != CODA_K_MAJOR && a_major != CODA_MN_MAJOR) return CODA_ERR_INVALID_ARG;
+  if (b_major != CODA_K_MAJOR && b_major != CODA_MN_MAJOR) return CODA_ERR_INVALID_ARG;
+  if (d_dtype != CODA_BF16 && d_dtype != CODA_F32) return CODA_ERR_INVALID_ARG;
+  if (d->map < CODA_MAP_NONE || d->map > CODA_MAP_COLDOT) return CODA_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return CODA_OK;
+  CK(req(A));
+  CK(req(B));
+  CK(al(A));
+  CK(al(B));
+  CK(al(D));
+  CK(ldok(lda, a_major == CODA_K_MAJOR ? K : M));
+  if (d->map == CODA_MAP_SWIGLU) {
+    CK(ldok(ldb, K));
+  } else {
+    CK(ldok(ldb, b_major == CODA_K_MAJOR ? K : N));
+  }
+  if (d_dtype == CODA_F32 && d->map != CODA_MAP_NONE) return CODA_ERR_UNSUPPORTED;
+  if (d->map != CODA_MAP_CE_LSE && d->map != CODA_MAP_QKNORM_ROPE) {
+    CK(req(D));
+    CK(ldok(ldd, N));
+  }
+  for (int i = 0; i < 2; ++i) {
+    CK(al(d->aux_in[i]));
+    if (d->aux_in[i]) CK(ldok(d->ld_aux_in[i], N));
+  }
+  for (int i = 0; i < 3; ++i) {
+    CK(al(d->aux_out[i]));
+    if (d->aux_out[i]) CK(ldok(d->ld_aux_out[i], N));
+  }
+  CK(al(d->row_scale));
+  CK(al(d->col_scale));
+  CK(al(d->partials));
+  Plan p;
+  p.A = A;
+  p.lda = lda;
+  p.a_mn = a_major;
+  p.B = B;
+  p.ldb = ldb;
+  p.b_mn = b_major;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  EpiArgs& e = p.e;
+  e.D = D;
+  e.ldd = ldd;
+  e.d_f32 = d_dtype == CODA_F32;
+  e.beta = d->beta;
+  e.row_scale = d->row_scale;
+  e.col_scale = d->col_scale;
+  e.aux0 = reinterpret_cast<const __nv_bfloat16*>(d->aux_in[0]);
+  e.ld_aux0 = d->ld_aux_in[0];
+  e.aux1 = reinterpret_cast<const __nv_bfloat16*>(d->aux_in[1]);
+  e.ld_aux1 = d->ld_aux_in[1];
+  e.row_coef = d->row_coef;
+  e.out1 = reinterpret_cast<__nv_bfloat16*>(d->aux_out[0]);
+  e.ld_out1 = d->ld_aux_out[0];
+  e.out2 = reinterpret_cast<__nv_bfloat16*>(d->aux_out[1]);
+  e.ld_out2 = d->ld_aux_out[1];
+  e.out3 = reinterpret_cast<__nv_bfloat16*>(d->aux_out[2]);
+  e.ld_out3 = d->ld_aux_out[2];
+  e.partials = d->partials;
+  e.ld_part = d->ld_partials;
+  if (d->row_coef && !d->aux_in[1]) return CODA_ERR_INVALID_ARG;
+  if (d->K2 > 0) {
+    if (d->map == CODA_MAP_SWIGLU) return CODA_ERR_UNSUPPORTED;
+    CK(req(d->A2));
+    CK(req(d->B2));
+    CK(al(d->A2));
+    CK(al(d->B2));
+    if (d->K2 % 8) return CODA_ERR_UNSUPPORTED;
+    CK(ldok(d->lda2, a_major == CODA_K_MAJOR ? d->K2 : M));
+    CK(ldok(d->ldb2, b_major == CODA_K_MAJOR ? d->K2 : N));
+    p.A2 = d->A2;
+    p.lda2 = d->lda2;
+    p.B2 = d->B2;
+    p.ldb2 = d->ldb2;
+    p.K2 = d->K2;
+  }
+  switch (d->map) {
+    case CODA_MAP_NONE:
+      p.kind = coda::EpiKind::Plain;
+      if (e.partials && e.ld_part < M) return CODA_ERR_INVALID_ARG;
+      break;
+    case CODA_MAP_SWIGLU:
+      p.kind = coda::EpiKind::Swiglu;
+      if (b_major != CODA_K_MAJOR || !d->B2) return CODA_ERR_UNSUPPORTED;
+      CK(al(d->B2));
+      CK(ldok(d->ldb2, K));
+      p.b_dual = 1;
+      p.B2 = d->B2;
+      p.ldb2 = d->ldb2;
+      break;
+    case CODA_MAP_DSWIGLU:
+      p.kind = coda::EpiKind::DSwiglu;
+      if (!d->aux_in[0] || !d->aux_in[1] || !d->aux_out[0] || !d->aux_out[1]) return CODA_ERR_INVALID_ARG;
+      if (e.partials && e.ld_part < M) return CODA_ERR_INVALID_ARG;
+      break;
+    case CODA_MAP_QKNORM_ROPE:
+      p.kind = coda::EpiKind::QkRope;
+      if (d->head_dim != 128) return CODA_ERR_UNSUPPORTED;
+      if (d->n_q_heads <= 0 || d->n_kv_heads < 0) return CODA_ERR_INVALID_ARG;
+      if (N != static_cast<int64_t>(d->n_q_heads + 2 * d->n_kv_heads) * 128) return CODA_ERR_INVALID_ARG;
+      if (!d->positions || !d->cos_sin || d->max_pos <= 0 || !d->gamma_q || !d->Q) return CODA_ERR_INVALID_ARG;
+      if (d->n_kv_heads > 0 && (!d->gamma_k || !d->K || !d->V)) return CODA_ERR_INVALID_ARG;
+      CK(al(d->Q));
+      CK(al(d->K));
+      CK(al(d->V));
+      CK(al(d->gamma_q));
+      CK(al(d->gamma_k));
+      CK(al(d->cos_sin));
+      e.pos = d->positions;
+      e.cos_sin = reinterpret_cast<const float2*>(d->cos_sin);
+      e.max_pos = d->max_pos;
+      e.n_q = d->n_q_heads;
+      e.n_kv = d->n_kv_heads;
+      e.eps = d->eps;
+      e.gamma_q = d->gamma_q;
+      e.gamma_k = d->gamma_k;
+      e.Q = reinterpret_cast<__nv_bfloat16*>(d->Q);
+      e.Kh = reinterpret_cast<__nv_bfloat16*>(d->K);
+      e.V = reinterpret_cast<__nv_bfloat16*>(d->V);
+      e.ldq = static_cast<int64_t>(d->n_q_heads) * 128;
+      e.ldk = e.ldv = static_cast<int64_t>(d->n_kv_heads) * 128;
+      break;
+    case CODA_MAP_CE_LSE:
+      p.kind = coda::EpiKind::CeLse;
+      if (!d->labels || !d->target_logit || !d->partials) return CODA_ERR_INVALID_ARG;
+      if (d->ld_partials < M) return CODA_ERR_INVALID_ARG;
+      p.n_per_unit = d->vocab_tiles_per_unit > 0 ? d->vocab_tiles_per_unit : CE_TILES_PER_UNIT;
+      e.labels = d->labels;
+      e.target_logit = d->target_logit;
+      break;
+    case CODA_MAP_CE_DLOGITS:
+      p.kind = coda::EpiKind::CeDlogits;
+      if (!d->labels || !d->lse || !d->n_valid) return CODA_ERR_INVALID_ARG;
+      e.labels = d->labels;
+      e.ignore_index = d->ignore_index;
+      e.lse = d->lse;
+      e.n_valid = d->n_valid;
+      e.dloss = d->dloss;
+      break;
+    case CODA_MAP_COLDOT:
+      p.kind = coda::EpiKind::ColDot;
+      if (!d->aux_in[0]) return CODA_ERR_INVALID_ARG;
+      if (e.partials && e.ld_part < N) return CODA_ERR_INVALID_ARG;
+      break;
+  }
+  return run(p, static_cast<int*>(ws), S(stream));
+}
+
+// ------------------------------------------------------------------ RMSNorm pieces
+int coda_fold_gamma(const coda_bf16* W, const float* gamma, coda_bf16* Wf, int64_t N, int64_t K,
+                    coda_stream stream) {
+  CK(dims_ok(N, 8, K));
+  if (N == 0) return CODA_OK;
+  CK(req(W));
+  CK(req(gamma));
+  CK(req(Wf));
+  CK(al(W));
+  CK(al(gamma));
+  CK(al(Wf));
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  CU(coda::launch_fold_gamma(BF(W), gamma, BF(Wf), N, K, sms, S(stream)));
+  return CODA_OK;
+}
+
+int coda_rms_rstd(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, float eps, float* rstd,
+                  coda_stream stream) {
+  CK(dims_ok(M, 8, K));
+  if (M == 0) return CODA_OK;
+  CK(req(X));
+  CK(req(rstd));
+  CK(al(X));
+  CK(ldok(ldx, K));
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  CU(coda::launch_row_rstd(BF(X), ldx, M, K, eps, rstd, sms, S(stream)));
+  return CODA_OK;
+}
+
+int coda_rope_table(float theta, int32_t head_dim, int32_t max_pos, float* cos_sin, coda_stream stream) {
+  if (head_dim <= 0 || head_dim % 2 || max_pos <= 0 || !(theta > 0.f)) return CODA_ERR_INVALID_ARG;
+  CK(req(cos_sin));
+  CK(al(cos_sin));
+  CU(coda::launch_rope_table(static_cast<double>(theta), head_dim, max_pos, reinterpret_cast<float2*>(cos_sin),
+                             S(stream)));
+  return CODA_OK;
+}
+
+// ------------------------------------------------------------------ rmsnorm_linear
+size_t coda_rmsnorm_linear_workspace_size(int64_t, int64_t, int64_t) { return WS_HEADER; }
+
+int coda_rmsnorm_linear(const coda_bf16* X, const float* rstd_in, const coda_bf16* Wf, const coda_bf16* R,
+                        float eps, float* rstd_out, coda_bf16* Y, int64_t M, int64_t N, int64_t K, void* ws,
+                        size_t ws_bytes, coda_stream stream) {
+  CK(dims_ok(M, N, K));
+  CK(ws_ok(ws, ws_bytes, coda_rmsnorm_linear_workspace_size(M, N, K)));
+  if (M == 0) return CODA_OK;
+  CK(req(X));
+  CK(req(Wf));
+  CK(req(Y));
+  if (!rstd_in && !rstd_out) return CODA_ERR_INVALID_ARG;
+  for (const void* q : {(const void*)X, (const void*)Wf, (const void*)R, (const void*)Y, (const void*)rstd_in,
+                        (const void*)rstd_out})
+    CK(al(q));
+  const float* rs = rstd_in;
+  if (!rs) {
+    CK(coda_rms_rstd(X, K, M, K, eps, rstd_out, stream));
+    rs = rstd_out;
+  }
+  Plan p;
+  p.A = X;
+  p.lda = K;
+  p.B = Wf;
+  p.ldb = K;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.e.D = Y;
+  p.e.ldd = N;
+  p.e.row_scale = rs;
+  p.e.aux0 = BF(R);
+  p.e.ld_aux0 = N;
+  return run(p, static_cast<int*>(ws), S(stream));
+}
+
+size_t coda_rmsnorm_linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K) {
+  SizeCursor c;
+  c.take<__nv_bfloat16>(static_cast<size_t>(M) * N);  // G'
+  c.take<float>(M);                                    // s
+  c.take<float>(M);                                    // coef
+  c.take<float>(static_cast<size_t>(4 * cdiv(N, 128)) * K);  // dgamma partials
+  return c.off;
+}
+
+int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W, const coda_bf16* Wf,
+                            const float* gamma, const float* rstd, const coda_bf16* Y, const coda_bf16* R,
+                            coda_bf16* dX, coda_bf16* dW, float* dgamma, int64_t M, int64_t N, int64_t K, void* ws,
+                            size_t ws_bytes, coda_stream stream) {
+  CK(dims_ok(M, N, K));
+  CK(ws_ok(ws, ws_bytes, coda_rmsnorm_linear_bwd_workspace_size(M, N, K)));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)dY, (const void*)X, (const void*)W, (const void*)Wf, (const void*)gamma,
+                        (const void*)rstd, (const void*)Y, (const void*)dX, (const void*)dW, (const void*)dgamma})
+    CK(req(q));
+  for (const void* q : {(const void*)dY, (const void*)X, (const void*)W, (const void*)Wf, (const void*)gamma,
+                        (const void*)rstd, (const void*)Y, (const void*)R, (const void*)dX, (const void*)dW,
+                        (const void*)dgamma})
+    CK(al(q));
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  WsCursor w(ws);
+  __nv_bfloat16* Gp = w.take<__nv_bfloat16>(static_cast<size_t>(M) * N);
+  float* srow = w.take<float>(M);
+  float* coef = w.take<float>(M);
+  const int64_t nmb = cdiv(N, 128);
+  float* dgp = w.take<float>(static_cast<size_t>(4 * nmb) * K);
+  int* status = static_cast<int*>(ws);
+  cudaStream_t s = S(stream);
+  CU(coda::launch_rms_bwd_prepass(BF(dY), BF(Y), BF(R), rstd, M, N, Gp, srow, sms, s));
+  CU(coda::launch_combine_rows(srow, M, 1, M, 1.f / static_cast<float>(K), 0.f, rstd, coef, 1, s));
+  {  // dX = G' Wf - c * X
+    Plan p;
+    p.A = Gp;
+    p.lda = N;
+    p.B = Wf;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.M = M;
+    p.N = K;
+    p.K = N;
+    p.e.D = dX;
+    p.e.ldd = K;
+    p.e.row_coef = coef;
+    p.e.aux1 = BF(X);
+    p.e.ld_aux1 = K;
+    CK(run(p, status, s));
+  }
+  {  // dW = (G'^T X) diag(gamma), dgamma partials
+    Plan p;
+    p.kind = coda::EpiKind::ColDot;
+    p.A = Gp;
+    p.lda = N;
+    p.a_mn = 1;
+    p.B = X;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.M = N;
+    p.N = K;
+    p.K = M;
+    p.e.D = dW;
+    p.e.ldd = K;
+    p.e.col_scale = gamma;
+    p.e.aux0 = BF(W);
+    p.e.ld_aux0 = K;
+    p.e.partials = dgp;
+    p.e.ld_part = K;
+    CK(run(p, status, s));
+  }
+  CU(coda::launch_colsum(dgp, 4 * nmb, K, K, dgamma, s));
+  return CODA_OK;
+}
+
+// ------------------------------------------------------------------ linear_residual
+size_t coda_linear_residual_workspace_size(int64_t M, int64_t N, int64_t) {
+  SizeCursor c;
+  c.take<float>(static_cast<size_t>(cdiv(N, BN)) * M);
+  return c.off;
+}
+
+int coda_linear_residual(const coda_bf16* X, const coda_bf16* W, const coda_bf16* R, coda_bf16* Y, float eps,
+                         float* rstd_out, int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
+                         coda_stream stream) {
+  CK(dims_ok(M, N, K));
+  CK(ws_ok(ws, ws_bytes, coda_linear_residual_workspace_size(M, N, K)));
+  if (M == 0) return CODA_OK;
+  CK(req(X));
+  CK(req(W));
+  CK(req(Y));
+  for (const void* q : {(const void*)X, (const void*)W, (const void*)R, (const void*)Y, (const void*)rstd_out})
+    CK(al(q));
+  WsCursor w(ws);
+  float* part = w.take<float>(static_cast<size_t>(cdiv(N, BN)) * M);
+  Plan p;
+  p.A = X;
+  p.lda = K;
+  p.B = W;
+  p.ldb = K;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.e.D = Y;
+  p.e.ldd = N;
+  p.e.aux0 = BF(R);
+  p.e.ld_aux0 = N;
+  if (rstd_out) {
+    p.e.partials = part;
+    p.e.ld_part = M;
+  }
+  CK(run(p, static_cast<int*>(ws), S(stream)));
+  if (rstd_out)
+    CU(coda::launch_combine_rows(part, M, static_cast<int>(cdiv(N, BN)), M, 1.f / static_cast<float>(N), eps,
+                                 nullptr, rstd_out, 0, S(stream)));
+  return CODA_OK;
+}
+
+size_t coda_linear_residual_bwd_workspace_size(int64_t, int64_t, int64_t) { return WS_HEADER; }
+
+int coda_linear_residual_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W, coda_bf16* dX,
+                             coda_bf16* dW, int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
+                             coda_stream stream) {
+  CK(dims_ok(M, N, K));
+  CK(ws_ok(ws, ws_bytes, WS_HEADER));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)dY, (const void*)X, (const void*)W, (const void*)dX, (const void*)dW}) {
+    CK(req(q));
+    CK(al(q));
+  }
+  int* status = static_cast<int*>(ws);
+  {  // dX = dY W
+    Plan p;
+    p.A = dY;
+    p.lda = N;
+    p.B = W;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.M = M;
+    p.N = K;
+    p.K = N;
+    p.e.D = dX;
+    p.e.ldd = K;
+    CK(run(p, status, S(stream)));
+  }
+  {  // dW = dY^T X
+    Plan p;
+    p.A = dY;
+    p.lda = N;
+    p.a_mn = 1;
+    p.B = X;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.M = N;
+    p.N = K;
+    p.K = M;
+    p.e.D = dW;
+    p.e.ldd = K;
+    CK(run(p, status, S(stream)));
+  }
+  return CODA_OK;
+}
+
+// ------------------------------------------------------------------ linear_swiglu
+size_t coda_linear_swiglu_workspace_size(int64_t, int64_t, int64_t) { return WS_HEADER; }
+
+int coda_linear_swiglu(const coda_bf16* X, const float* rstd, const coda_bf16* Wg, const coda_bf16* Wu,
+                       coda_bf16* H, coda_bf16* g_save, coda_bf16* u_save, int64_t M, int64_t I, int64_t K,
+                       void* ws, size_t ws_bytes, coda_stream stream) {
+  CK(dims_ok(M, I, K));
+  CK(ws_ok(ws, ws_bytes, WS_HEADER));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)X, (const void*)Wg, (const void*)Wu, (const void*)H}) CK(req(q));
+  for (const void* q : {(const void*)X, (const void*)rstd, (const void*)Wg, (const void*)Wu, (const void*)H,
+                        (const void*)g_save, (const void*)u_save})
+    CK(al(q));
+  Plan p;
+  p.kind = coda::EpiKind::Swiglu;
+  p.A = X;
+  p.lda = K;
+  p.B = Wg;
+  p.ldb = K;
+  p.B2 = Wu;
+  p.ldb2 = K;
+  p.b_dual = 1;
+  p.M = M;
+  p.N = I;
+  p.K = K;
+  p.e.D = H;
+  p.e.ldd = I;
+  p.e.row_scale = rstd;
+  p.e.out1 = BF(g_save);
+  p.e.ld_out1 = I;
+  p.e.out2 = BF(u_save);
+  p.e.ld_out2 = I;
+  return run(p, static_cast<int*>(ws), S(stream));
+}
+
+size_t coda_linear_swiglu_bwd_workspace_size(int64_t M, int64_t I, int64_t K) {
+  SizeCursor c;
+  c.take<__nv_bfloat16>(static_cast<size_t>(M) * 2 * I);      // G' = [r dG | r dU]
+  c.take<float>(static_cast<size_t>(cdiv(I, BN)) * M);        // row partials of sum(dG g + dU u)
+  c.take<float>(M);                                            // coef
+  c.take<float>(static_cast<size_t>(8 * cdiv(I, 128)) * K);   // dgamma partials (gate, up)
+  return c.off;
+}
+
+int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float* rstd, const float* gamma,
+                           const coda_bf16* Wg, const coda_bf16* Wu, const coda_bf16* Wgf, const coda_bf16* Wuf,
+                           const coda_bf16* Wd, const coda_bf16* g, const coda_bf16* u, const coda_bf16* H,
+                           const coda_bf16* dX_resid, coda_bf16* dX, coda_bf16* dWg, coda_bf16* dWu, coda_bf16* dWd,
+                           float* dgamma, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
+                           coda_stream stream) {
+  CK(dims_ok(M, I, K));
+  CK(ws_ok(ws, ws_bytes, coda_linear_swiglu_bwd_workspace_size(M, I, K)));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)dY, (const void*)X, (const void*)Wg, (const void*)Wu, (const void*)Wgf,
+                        (const void*)Wuf, (const void*)Wd, (const void*)g, (const void*)u, (const void*)H,
+                        (const void*)dX, (const void*)dWg, (const void*)dWu, (const void*)dWd})
+    CK(req(q));
+  for (const void* q : {(const void*)dY, (const void*)X, (const void*)rstd, (const void*)gamma, (const void*)Wg,
+                        (const void*)Wu, (const void*)Wgf, (const void*)Wuf, (const void*)Wd, (const void*)g,
+                        (const void*)u, (const void*)H, (const void*)dX_resid, (const void*)dX, (const void*)dWg,
+                        (const void*)dWu, (const void*)dWd, (const void*)dgamma})
+    CK(al(q));
+  const bool norm = rstd != nullptr;
+  if (norm && (!gamma || !dgamma)) return CODA_ERR_INVALID_ARG;
+  WsCursor w(ws);
+  __nv_bfloat16* Gp = w.take<__nv_bfloat16>(static_cast<size_t>(M) * 2 * I);
+  float* spart = w.take<float>(static_cast<size_t>(cdiv(I, BN)) * M);
+  float* coef = w.take<float>(M);
+  const int64_t nmb = cdiv(I, 128);
+  float* dgp = w.take<float>(static_cast<size_t>(8 * nmb) * K);
+  int* status = static_cast<int*>(ws);
+  cudaStream_t s = S(stream);
+  {  // dH = dY Wd  ->  dSwiGLU  ->  G' (+ row partials)
+    Plan p;
+    p.kind = coda::EpiKind::DSwiglu;
+    p.A = dY;
+    p.lda = K;
+    p.B = Wd;
+    p.ldb = I;
+    p.b_mn = 1;
+    p.M = M;
+    p.N = I;
+    p.K = K;
+    p.e.aux0 = BF(g);
+    p.e.ld_aux0 = I;
+    p.e.aux1 = BF(u);
+    p.e.ld_aux1 = I;
+    p.e.out1 = Gp;
+    p.e.ld_out1 = 2 * I;
+    p.e.out2 = Gp + I;
+    p.e.ld_out2 = 2 * I;
+    p.e.row_scale = rstd;
+    if (norm) {
+      p.e.partials = spart;
+      p.e.ld_part = M;
+    }
+    CK(run(p, status, s));
+  }
+  if (norm)
+    CU(coda::launch_combine_rows(spart, M, static_cast<int>(cdiv(I, BN)), M, 1.f / static_cast<float>(K), 0.f,
+                                 rstd, coef, 1, s));
+  {  // dX = G'_g Wgf + G'_u Wuf (- c X) (+ dX_resid): one GEMM over K = 2I
+    Plan p;
+    p.A = Gp;
+    p.lda = 2 * I;
+    p.B = Wgf;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.A2 = Gp + I;
+    p.lda2 = 2 * I;
+    p.B2 = Wuf;
+    p.ldb2 = K;
+    p.K2 = I;
+    p.M = M;
+    p.N = K;
+    p.K = I;
+    p.e.D = dX;
+    p.e.ldd = K;
+    p.e.aux0 = BF(dX_resid);
+    p.e.ld_aux0 = K;
+    if (norm) {
+      p.e.row_coef = coef;
+      p.e.aux1 = BF(X);
+      p.e.ld_aux1 = K;
+    }
+    CK(run(p, status, s));
+  }
+  {  // dWd = dY^T H
+    Plan p;
+    p.A = dY;
+    p.lda = K;
+    p.a_mn = 1;
+    p.B = H;
+    p.ldb = I;
+    p.b_mn = 1;
+    p.M = K;
+    p.N = I;
+    p.K = M;
+    p.e.D = dWd;
+    p.e.ldd = I;
+    CK(run(p, status, s));
+  }
+  for (int which = 0; which < 2; ++which) {  // dWg, dWu = (G'^T X) diag(gamma)
+    Plan p;
+    p.kind = norm ? coda::EpiKind::ColDot : coda::EpiKind::Plain;
+    p.A = Gp + which * I;
+    p.lda = 2 * I;
+    p.a_mn = 1;
+    p.B = X;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.M = I;
+    p.N = K;
+    p.K = M;
+    p.e.D = which ? dWu : dWg;
+    p.e.ldd = K;
+    if (norm) {
+      p.e.col_scale = gamma;
+      p.e.aux0 = BF(which ? Wu : Wg);
+      p.e.ld_aux0 = K;
+      p.e.partials = dgp + static_cast<size_t>(which) * 4 * nmb * K;
+      p.e.ld_part = K;
+    }
+    CK(run(p, status, s));
+  }
+  if (norm) CU(coda::launch_colsum(dgp, 8 * nmb, K, K, dgamma, s));
+  return CODA_OK;
+}
+
+// ------------------------------------------------------------------ linear_qknorm_rope
+size_t coda_linear_qknorm_rope_workspace_size(int64_t, int64_t, int32_t, int32_t, int32_t) { return WS_HEADER; }
+
+int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf16* Wf_qkv, const float* gamma_q,
+                            const float* gamma_k, const int32_t* pos, const float* cos_sin, int32_t max_pos,
+                            float eps, int32_t n_q, int32_t n_kv, int32_t head_dim, coda_bf16* Q, coda_bf16* K,
+                            coda_bf16* V, coda_bf16* qk_save, int64_t M, int64_t Kdim, void* ws, size_t ws_bytes,
+                            coda_stream stream) {
+  if (head_dim != 128) return CODA_ERR_UNSUPPORTED;
+  if (n_q <= 0 || n_kv < 0) return CODA_ERR_INVALID_ARG;
+  const int64_t N = static_cast<int64_t>(n_q + 2 * n_kv) * head_dim;
+  CK(dims_ok(M, N, Kdim));
+  CK(ws_ok(ws, ws_bytes, WS_HEADER));
+  if (M == 0) return CODA_OK;
+  coda_epilogue_desc d;
+  std::memset(&d, 0, sizeof(d));
+  d.map = CODA_MAP_QKNORM_ROPE;
+  d.row_scale = rstd;
+  d.aux_out[0] = qk_save;
+  d.ld_aux_out[0] = static_cast<int64_t>(n_q + n_kv) * head_dim;
+  d.positions = pos;
+  d.cos_sin = cos_sin;
+  d.max_pos = max_pos;
+  d.n_q_heads = n_q;
+  d.n_kv_heads = n_kv;
+  d.head_dim = head_dim;
+  d.eps = eps;
+  d.gamma_q = gamma_q;
+  d.gamma_k = gamma_k;
+  d.Q = Q;
+  d.K = K;
+  d.V = V;
+  CK(req(X));
+  CK(req(Wf_qkv));
+  CK(al(rstd));
+  return coda_gemm_epilogue(&d, X, Kdim, CODA_K_MAJOR, Wf_qkv, Kdim, CODA_K_MAJOR, nullptr, N, CODA_BF16, M, N,
+                            Kdim, ws, ws_bytes, stream);
+}
+
+static int qk_bwd_blocks(int64_t M) {
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(M, coda::QK_BWD_WARPS), 1184)));
+}
+
+size_t coda_linear_qknorm_rope_bwd_workspace_size(int64_t M, int64_t Kdim, int32_t n_q, int32_t n_kv,
+                                                  int32_t head_dim) {
+  const int64_t N = static_cast<int64_t>(n_q + 2 * n_kv) * head_dim;
+  SizeCursor c;
+  c.take<__nv_bfloat16>(static_cast<size_t>(M) * N);          // G'
+  c.take<float>(M);                                           // s
+  c.take<float>(M);                                           // coef
+  c.take<float>(static_cast<size_t>(qk_bwd_blocks(M)) * 256);  // dgamma_q|k partials
+  c.take<float>(static_cast<size_t>(4 * cdiv(N, 128)) * Kdim);  // dgamma_in partials
+  return c.off;
+}
+
+int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const coda_bf16* dV,
+                                const coda_bf16* qk_save, const coda_bf16* V, const float* gamma_q,
+                                const float* gamma_k, const int32_t* pos, const float* cos_sin, int32_t max_pos,
+                                float eps, int32_t n_q, int32_t n_kv, int32_t head_dim, const coda_bf16* X,
+                                const float* rstd, const float* gamma_in, const coda_bf16* W_qkv,
+                                const coda_bf16* Wf_qkv, const coda_bf16* dX_resid, coda_bf16* dX, coda_bf16* dW_qkv,
+                                float* dgamma_in, float* dgamma_q, float* dgamma_k, int64_t M, int64_t Kdim, void* ws,
+                                size_t ws_bytes, coda_stream stream) {
+  if (head_dim != 128) return CODA_ERR_UNSUPPORTED;
+  if (n_q <= 0 || n_kv <= 0 || max_pos <= 0) return CODA_ERR_INVALID_ARG;
+  const int64_t N = static_cast<int64_t>(n_q + 2 * n_kv) * head_dim;
+  CK(dims_ok(M, N, Kdim));
+  CK(ws_ok(ws, ws_bytes, coda_linear_qknorm_rope_bwd_workspace_size(M, Kdim, n_q, n_kv, head_dim)));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)dQ, (const void*)dK, (const void*)dV, (const void*)qk_save, (const void*)V,
+                        (const void*)gamma_q, (const void*)gamma_k, (const void*)pos, (const void*)cos_sin,
+                        (const void*)X, (const void*)W_qkv, (const void*)Wf_qkv, (const void*)dX,
+                        (const void*)dW_qkv, (const void*)dgamma_q, (const void*)dgamma_k})
+    CK(req(q));
+  for (const void* q : {(const void*)dQ, (const void*)dK, (const void*)dV, (const void*)qk_save, (const void*)V,
+                        (const void*)gamma_q, (const void*)gamma_k, (const void*)cos_sin, (const void*)X,
+                        (const void*)rstd, (const void*)gamma_in, (const void*)W_qkv, (const void*)Wf_qkv,
+                        (const void*)dX_resid, (const void*)dX, (const void*)dW_qkv, (const void*)dgamma_in,
+                        (const void*)dgamma_q, (const void*)dgamma_k})
+    CK(al(q));
+  const bool norm = rstd != nullptr;
+  if (norm && (!gamma_in || !dgamma_in)) return CODA_ERR_INVALID_ARG;
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  WsCursor w(ws);
+  __nv_bfloat16* Gp = w.take<__nv_bfloat16>(static_cast<size_t>(M) * N);
+  float* srow = w.take<float>(M);
+  float* coef = w.take<float>(M);
+  const int nblk = qk_bwd_blocks(M);
+  float* dgqk = w.take<float>(static_cast<size_t>(nblk) * 256);
+  const int64_t nmb = cdiv(N, 128);
+  float* dgp = w.take<float>(static_cast<size_t>(4 * nmb) * Kdim);
+  int* status = static_cast<int*>(ws);
+  cudaStream_t s = S(stream);
+  CU(coda::launch_qk_bwd(BF(dQ), BF(dK), BF(dV), BF(qk_save), BF(V), gamma_q, gamma_k, pos,
+                         reinterpret_cast<const float2*>(cos_sin), max_pos, eps, n_q, n_kv, rstd, M, Gp, srow, dgqk,
+                         nblk, status, s));
+  CU(coda::launch_colsum(dgqk, nblk, 128, 256, dgamma_q, s));
+  CU(coda::launch_colsum(dgqk + 128, nblk, 128, 256, dgamma_k, s));
+  if (norm)
+    CU(coda::launch_combine_rows(srow, M, 1, M, 1.f / static_cast<float>(Kdim), 0.f, rstd, coef, 1, s));
+  {  // dX = G' Wf_qkv (- c X) (+ dX_resid)
+    Plan p;
+    p.A = Gp;
+    p.lda = N;
+    p.B = Wf_qkv;
+    p.ldb = Kdim;
+    p.b_mn = 1;
+    p.M = M;
+    p.N = Kdim;
+    p.K = N;
+    p.e.D = dX;
+    p.e.ldd = Kdim;
+    p.e.aux0 = BF(dX_resid);
+    p.e.ld_aux0 = Kdim;
+    if (norm) {
+      p.e.row_coef = coef;
+      p.e.aux1 = BF(X);
+      p.e.ld_aux1 = Kdim;
+    }
+    CK(run(p, status, s));
+  }
+  {  // dW_qkv = (G'^T X) diag(gamma_in), dgamma_in partials
+    Plan p;
+    p.kind = norm ? coda::EpiKind::ColDot : coda::EpiKind::Plain;
+    p.A = Gp;
+    p.lda = N;
+    p.a_mn = 1;
+    p.B = X;
+    p.ldb = Kdim;
+    p.b_mn = 1;
+    p.M = N;
+    p.N = Kdim;
+    p.K = M;
+    p.e.D = dW_qkv;
+    p.e.ldd = Kdim;
+    if (norm) {
+      p.e.col_scale = gamma_in;
+      p.e.aux0 = BF(W_qkv);
+      p.e.ld_aux0 = Kdim;
+      p.e.partials = dgp;
+      p.e.ld_part = Kdim;
+    }
+    CK(run(p, status, s));
+  }
+  if (norm) CU(coda::launch_colsum(dgp, 4 * nmb, Kdim, Kdim, dgamma_in, s));
+  return CODA_OK;
+}
+
+// ------------------------------------------------------------------ linear_cross_entropy
+static int ce_chunks(int64_t V) { return static_cast<int>(cdiv(cdiv(V, BN), CE_TILES_PER_UNIT)); }
+static int ce_blocks(int64_t M) {
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(M, coda::CE_COMBINE_THREADS), 256)));
+}
+
+size_t coda_linear_cross_entropy_workspace_size(int64_t M, int64_t V, int64_t) {
+  SizeCursor c;
+  c.take<float>(M);                                               // target logits
+  c.take<float2>(static_cast<size_t>(ce_chunks(V)) * M);          // (max, sumexp) partials
+  c.take<double>(ce_blocks(M));
+  c.take<int>(ce_blocks(M));
+  return c.off;
+}
+
+int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int32_t* labels, int32_t ignore_index,
+                              float* loss_mean, float* lse, int32_t* n_valid, int64_t M, int64_t V, int64_t K,
+                              void* ws, size_t ws_bytes, coda_stream stream) {
+  CK(dims_ok(M, V, K));
+  CK(ws_ok(ws, ws_bytes, coda_linear_cross_entropy_workspace_size(M, V, K)));
+  for (const void* q : {(const void*)X, (const void*)W, (const void*)labels, (const void*)loss_mean,
+                        (const void*)lse, (const void*)n_valid})
+    CK(req(q));
+  CK(al(X));
+  CK(al(W));
+  if (V == 0) return CODA_ERR_INVALID_ARG;
+  WsCursor w(ws);
+  float* target = w.take<float>(M);
+  const int nch = ce_chunks(V);
+  float2* part = w.take<float2>(static_cast<size_t>(nch) * M);
+  const int nblk = ce_blocks(M);
+  double* bl = w.take<double>(nblk);
+  int* bc = w.take<int>(nblk);
+  int* status = static_cast<int*>(ws);
+  cudaStream_t s = S(stream);
+  if (M > 0) {
+    Plan p;
+    p.kind = coda::EpiKind::CeLse;
+    p.A = X;
+    p.lda = K;
+    p.B = W;
+    p.ldb = K;
+    p.M = M;
+    p.N = V;
+    p.K = K;
+    p.n_per_unit = CE_TILES_PER_UNIT;
+    p.e.labels = labels;
+    p.e.target_logit = target;
+    p.e.partials = reinterpret_cast<float*>(part);
+    p.e.ld_part = M;
+    CK(run(p, status, s));
+  }
+  CU(coda::launch_ce_combine(part, M, nch, target, labels, ignore_index, M, V, lse, bl, bc, nblk, loss_mean, n_valid,
+                             status, s));
+  return CODA_OK;
+}
+
+size_t coda_linear_cross_entropy_bwd_workspace_size(int64_t M, int64_t V, int64_t) {
+  SizeCursor c;
+  c.take<__nv_bfloat16>(static_cast<size_t>(M) * V);  // dZ
+  return c.off;
+}
+
+int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const int32_t* labels,
+                                  int32_t ignore_index, const float* lse, const int32_t* n_valid, float dloss,
+                                  coda_bf16* dX, coda_bf16* dW, int64_t M, int64_t V, int64_t K, void* ws,
+                                  size_t ws_bytes, coda_stream stream) {
+  CK(dims_ok(M, V, K));
+  CK(ws_ok(ws, ws_bytes, coda_linear_cross_entropy_bwd_workspace_size(M, V, K)));
+  for (const void* q : {(const void*)X, (const void*)W, (const void*)labels, (const void*)lse,
+                        (const void*)n_valid, (const void*)dX, (const void*)dW})
+    CK(req(q));
+  for (const void* q : {(const void*)X, (const void*)W, (const void*)dX, (const void*)dW}) CK(al(q));
+  if (V == 0) return CODA_ERR_INVALID_ARG;
+  if (M == 0) {
+    CU(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * K * 2, S(stream)));
+    return CODA_OK;
+  }
+  WsCursor w(ws);
+  __nv_bfloat16* dZ = w.take<__nv_bfloat16>(static_cast<size_t>(M) * V);
+  int* status = static_cast<int*>(ws);
+  cudaStream_t s = S(stream);
+  {  // dZ = (softmax - onehot) * dloss / n_valid
+    Plan p;
+    p.kind = coda::EpiKind::CeDlogits;
+    p.A = X;
+    p.lda = K;
+    p.B = W;
+    p.ldb = K;
+    p.M = M;
+    p.N = V;
+    p.K = K;
+    p.e.D = dZ;
+    p.e.ldd = V;
+    p.e.labels = labels;
+    p.e.ignore_index = ignore_index;
+    p.e.lse = lse;
+    p.e.n_valid = n_valid;
+    p.e.dloss = dloss;
+    CK(run(p, status, s));
+  }
+  {  // dX = dZ W
+    Plan p;
+    p.A = dZ;
+    p.lda = V;
+    p.B = W;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.M = M;
+    p.N = K;
+    p.K = V;
+    p.e.D = dX;
+    p.e.ldd = K;
+    CK(run(p, status, s));
+  }
+  {  // dW = dZ^T X
+    Plan p;
+    p.A = dZ;
+    p.lda = V;
+    p.a_mn = 1;
+    p.B = X;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.M = V;
+    p.N = K;
+    p.K = M;
+    p.e.D = dW;
+    p.e.ldd = K;
+    CK(run(p, status, s));
+  }
+  return CODA_OK;
+}
+
+}  // extern "C"

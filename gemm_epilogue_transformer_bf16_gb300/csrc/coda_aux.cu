@@ -1,0 +1,385 @@
+// Auxiliary kernels around the GEMM-epilogue path: the "lightweight
+// auxiliary kernels" that merge tile partials ("CODA: Rewriting Transformer
+// Blocks as GEMM-Epilogue Programs" §3.1 class 4 and §3.2), the gamma fold of
+// the §3.2.1 reparameterisation, and the memory-bound passes that have no
+// producing GEMM here (row RMS of a block input, RMSNorm-backward pre-pass,
+// QK-RMSNorm + RoPE backward).  All are HBM-bound: 16-byte vector accesses,
+// warp-per-row for row work, grids sized to the SM count.
+#include <cmath>
+
+#include "coda_epilogues.cuh"
+#include "coda_internal.h"
+
+namespace coda {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------- gamma fold
+__global__ void fold_gamma_kernel(const __nv_bfloat16* __restrict__ W, const float* __restrict__ gamma,
+                                  __nv_bfloat16* Wf, int64_t N, int64_t K) {
+  const int64_t total8 = N * K / 8;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i * 8;
+    const int64_t k = e % K;
+    float w[8], g[8];
+    load_bf16x8(W + e, w);
+    load_f32x8(gamma + k, g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] *= g[j];
+    store_bf16x8(Wf + e, w);
+  }
+}
+
+cudaError_t launch_fold_gamma(const __nv_bfloat16* W, const float* gamma, __nv_bfloat16* Wf, int64_t N, int64_t K,
+                              int num_sms, cudaStream_t s) {
+  const int64_t total8 = N * K / 8;
+  const int64_t blocks = std::min<int64_t>((total8 + 255) / 256, static_cast<int64_t>(num_sms) * 8);
+  fold_gamma_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(W, gamma, Wf, N, K);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- row rstd
+__global__ void row_rstd_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int64_t M, int64_t K, float eps,
+                                float* rstd) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; row < M; row += warps) {
+    const __nv_bfloat16* x = X + row * ldx;
+    float s = 0.f;
+    for (int64_t k = lane * 8; k < K; k += 256) {
+      float v[8];
+      load_bf16x8(x + k, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s += v[j] * v[j];
+    }
+    s = warp_sum(s);
+    if (lane == 0) rstd[row] = 1.f / sqrtf(s / static_cast<float>(K) + eps);
+  }
+}
+
+cudaError_t launch_row_rstd(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, float eps, float* rstd,
+                            int num_sms, cudaStream_t s) {
+  const int64_t blocks = std::min<int64_t>((M + 7) / 8, static_cast<int64_t>(num_sms) * 8);
+  row_rstd_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(X, ldx, M, K, eps, rstd);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- combine row partials
+__global__ void combine_rows_kernel(const float* __restrict__ p, int64_t ld, int nparts, int64_t M, float inv_k,
+                                    float eps, const float* __restrict__ r, float* out, int mode) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float s = 0.f;
+    for (int t = 0; t < nparts; ++t) s += p[t * ld + i];
+    if (mode == 0) {
+      out[i] = 1.f / sqrtf(s * inv_k + eps);
+    } else {
+      const float ri = r ? r[i] : 1.f;
+      out[i] = ri * ri * s * inv_k;
+    }
+  }
+}
+
+cudaError_t launch_combine_rows(const float* p, int64_t ld, int nparts, int64_t M, float inv_k, float eps,
+                                const float* r, float* out, int mode, cudaStream_t s) {
+  const int64_t blocks = std::min<int64_t>((M + 255) / 256, 4096);
+  combine_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(p, ld, nparts, M, inv_k,
+                                                                                          eps, r, out, mode);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- RMSNorm-bwd pre-pass
+// G' = bf16(r * G);  s_i = sum_n G_in (Y - R)_in
+__global__ void rms_bwd_prepass_kernel(const __nv_bfloat16* __restrict__ G, const __nv_bfloat16* __restrict__ Y,
+                                       const __nv_bfloat16* __restrict__ R, const float* __restrict__ rstd,
+                                       int64_t M, int64_t N, __nv_bfloat16* Gp, float* srow) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; row < M; row += warps) {
+    const float r = rstd[row];
+    float s = 0.f;
+    for (int64_t n = lane * 8; n < N; n += 256) {
+      const int64_t o = row * N + n;
+      float g[8], y[8], rr[8];
+      load_bf16x8(G + o, g);
+      load_bf16x8(Y + o, y);
+      if (R) {
+        load_bf16x8(R + o, rr);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) rr[j] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        s += g[j] * (y[j] - rr[j]);
+        g[j] *= r;
+      }
+      store_bf16x8(Gp + o, g);
+    }
+    s = warp_sum(s);
+    if (lane == 0) srow[row] = s;
+  }
+}
+
+cudaError_t launch_rms_bwd_prepass(const __nv_bfloat16* G, const __nv_bfloat16* Y, const __nv_bfloat16* R,
+                                   const float* rstd, int64_t M, int64_t N, __nv_bfloat16* Gp, float* srow,
+                                   int num_sms, cudaStream_t s) {
+  const int64_t blocks = std::min<int64_t>((M + 7) / 8, static_cast<int64_t>(num_sms) * 8);
+  rms_bwd_prepass_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(G, Y, R, rstd, M, N,
+                                                                                             Gp, srow);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- column sums
+// out[k] = sum_r p[r*ld + k], fixed summation order (deterministic).
+// Block = 32 columns x 32 row groups; row group g sums rows g, g+32, ...;
+// the 32 group sums are then added in order.
+__global__ void colsum_kernel(const float* __restrict__ p, int64_t nrows, int64_t ncols, int64_t ld, float* out) {
+  __shared__ float part[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int64_t col = blockIdx.x * 32 + tx;
+  float s = 0.f;
+  if (col < ncols)
+    for (int64_t r = ty; r < nrows; r += 32) s += p[r * ld + col];
+  part[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && col < ncols) {
+    float t = 0.f;
+    for (int g = 0; g < 32; ++g) t += part[g][tx];
+    out[col] = t;
+  }
+}
+
+cudaError_t launch_colsum(const float* p, int64_t nrows, int64_t ncols, int64_t ld, float* out, cudaStream_t s) {
+  colsum_kernel<<<static_cast<unsigned>((ncols + 31) / 32), 1024, 0, s>>>(p, nrows, ncols, ld, out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- cross-entropy combine
+// Merge the (max, sum-exp) partials of every vocab chunk into lse_i, form
+// loss_i = lse_i - z_{i,y_i} for valid rows, and reduce (double, fixed
+// order) into per-block sums; a one-block finaliser writes the mean.
+__global__ void ce_combine_kernel(const float2* __restrict__ part, int64_t ld, int nchunks,
+                                  const float* __restrict__ target, const int32_t* __restrict__ labels,
+                                  int32_t ignore, int64_t M, int64_t V, float* lse_out, double* blk_loss,
+                                  int* blk_cnt, int* status) {
+  __shared__ double sl[CE_COMBINE_THREADS];
+  __shared__ int sc[CE_COMBINE_THREADS];
+  double acc = 0.0;
+  int cnt = 0;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float m = -INFINITY;
+    for (int c = 0; c < nchunks; ++c) m = fmaxf(m, part[c * ld + i].x);
+    float s = 0.f;
+    for (int c = 0; c < nchunks; ++c) {
+      const float2 q = part[c * ld + i];
+      s += q.y * expf(q.x - m);
+    }
+    const float lse = m + logf(s);
+    lse_out[i] = lse;
+    const int32_t y = labels[i];
+    if (y != ignore) {
+      if (y >= 0 && y < V) {
+        acc += static_cast<double>(lse) - static_cast<double>(target[i]);
+        ++cnt;
+      } else if (status) {
+        atomicOr(status, CODA_DEV_LABEL_RANGE);
+      }
+    }
+  }
+  sl[threadIdx.x] = acc;
+  sc[threadIdx.x] = cnt;
+  __syncthreads();
+  for (int o = CE_COMBINE_THREADS / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) {
+      sl[threadIdx.x] += sl[threadIdx.x + o];
+      sc[threadIdx.x] += sc[threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    blk_loss[blockIdx.x] = sl[0];
+    blk_cnt[blockIdx.x] = sc[0];
+  }
+}
+
+__global__ void ce_finalize_kernel(const double* blk_loss, const int* blk_cnt, int nblk, float* loss_mean,
+                                   int32_t* n_valid) {
+  if (threadIdx.x != 0) return;
+  double s = 0.0;
+  long long c = 0;
+  for (int b = 0; b < nblk; ++b) {
+    s += blk_loss[b];
+    c += blk_cnt[b];
+  }
+  *loss_mean = static_cast<float>(c > 0 ? s / static_cast<double>(c) : NAN);
+  *n_valid = static_cast<int32_t>(c);
+}
+
+cudaError_t launch_ce_combine(const float2* part, int64_t ld, int nchunks, const float* target,
+                              const int32_t* labels, int32_t ignore, int64_t M, int64_t V, float* lse,
+                              double* blk_loss, int* blk_cnt, int nblk, float* loss_mean, int32_t* n_valid,
+                              int* status, cudaStream_t s) {
+  ce_combine_kernel<<<nblk, CE_COMBINE_THREADS, 0, s>>>(part, ld, nchunks, target, labels, ignore, M, V, lse,
+                                                        blk_loss, blk_cnt, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ce_finalize_kernel<<<1, 32, 0, s>>>(blk_loss, blk_cnt, nblk, loss_mean, n_valid);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- RoPE table
+__global__ void rope_table_kernel(double theta, int head_dim, int max_pos, float2* cs) {
+  const int half = head_dim / 2;
+  const int64_t total = static_cast<int64_t>(max_pos) * half;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t p = i / half;
+    const int j = static_cast<int>(i - p * half);
+    const double a = static_cast<double>(p) * pow(theta, -2.0 * j / head_dim);
+    double sn, cn;
+    sincos(a, &sn, &cn);
+    cs[i] = make_float2(static_cast<float>(cn), static_cast<float>(sn));
+  }
+}
+
+cudaError_t launch_rope_table(double theta, int head_dim, int max_pos, float2* cs, cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(max_pos) * (head_dim / 2);
+  const int64_t blocks = std::min<int64_t>((total + 255) / 256, 4096);
+  rope_table_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(theta, head_dim, max_pos,
+                                                                                       cs);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- QK-RMSNorm + RoPE backward
+// Warp per token row; lane owns elements 4*lane .. 4*lane+3 of every
+// 128-wide head, i.e. RoPE pairs 2*lane and 2*lane+1.  For each q/k head:
+//   dn = RoPE^-1(dOut), n = x * rho (x = saved pre-norm head, rho =
+//   rsqrt(mean x^2 + eps)), dgamma += dn*n, dq = rho (dn*g - n mean(n dn g)).
+// v heads pass dV through.  Writes G' = r * [dq | dk | dv] (bf16), the row
+// sum s_i = sum (dq x + dk k + dv v) and per-block dgamma_q | dgamma_k sums.
+__device__ __forceinline__ void load_bf16x4(const __nv_bfloat16* p, float* o) {
+  const uint2 q = *reinterpret_cast<const uint2*>(p);
+  o[0] = bf16_lo(q.x);
+  o[1] = bf16_hi(q.x);
+  o[2] = bf16_lo(q.y);
+  o[3] = bf16_hi(q.y);
+}
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* p, const float* v) {
+  uint2 q;
+  q.x = pack_bf16x2(v[0], v[1]);
+  q.y = pack_bf16x2(v[2], v[3]);
+  *reinterpret_cast<uint2*>(p) = q;
+}
+
+__global__ void __launch_bounds__(QK_BWD_WARPS * 32)
+    qk_bwd_kernel(const __nv_bfloat16* __restrict__ dQ, const __nv_bfloat16* __restrict__ dK,
+                  const __nv_bfloat16* __restrict__ dV, const __nv_bfloat16* __restrict__ qk_save,
+                  const __nv_bfloat16* __restrict__ Vs, const float* __restrict__ gq, const float* __restrict__ gk,
+                  const int32_t* __restrict__ pos, const float2* __restrict__ cs, int max_pos, float eps, int n_q,
+                  int n_kv, const float* __restrict__ rstd, int64_t M, __nv_bfloat16* Gp, float* srow,
+                  float* dgam_part, int* status) {
+  constexpr int D = 128;
+  __shared__ float red[QK_BWD_WARPS][2 * D];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t ldq = static_cast<int64_t>(n_q) * D, ldkv = static_cast<int64_t>(n_kv) * D;
+  const int64_t ldsave = ldq + ldkv, ldg = ldq + 2 * ldkv;
+  float aq[4] = {0.f, 0.f, 0.f, 0.f}, ak[4] = {0.f, 0.f, 0.f, 0.f};
+  float g_q[4], g_k[4];
+  {
+    const float4 a = *reinterpret_cast<const float4*>(gq + 4 * lane);
+    const float4 b = *reinterpret_cast<const float4*>(gk + 4 * lane);
+    g_q[0] = a.x; g_q[1] = a.y; g_q[2] = a.z; g_q[3] = a.w;
+    g_k[0] = b.x; g_k[1] = b.y; g_k[2] = b.z; g_k[3] = b.w;
+  }
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * QK_BWD_WARPS;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * QK_BWD_WARPS + w; row < M; row += nwarps) {
+    int p = pos[row];
+    if (p < 0 || p >= max_pos) {
+      if (lane == 0 && status) atomicOr(status, CODA_DEV_POSITION_RANGE);
+      p = p < 0 ? 0 : max_pos - 1;
+    }
+    const float2 c0 = cs[static_cast<int64_t>(p) * (D / 2) + 2 * lane];
+    const float2 c1 = cs[static_cast<int64_t>(p) * (D / 2) + 2 * lane + 1];
+    const float r = rstd ? rstd[row] : 1.f;
+    float s = 0.f;
+    for (int h = 0; h < n_q + n_kv; ++h) {
+      const bool is_q = h < n_q;
+      const __nv_bfloat16* src = is_q ? dQ + row * ldq + h * D : dK + row * ldkv + (h - n_q) * D;
+      float d[4], x[4];
+      load_bf16x4(src + 4 * lane, d);
+      load_bf16x4(qk_save + row * ldsave + h * D + 4 * lane, x);
+      const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
+      const float rho = rsqrtf(ss * (1.f / D) + eps);
+      float n[4], dn[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) n[i] = x[i] * rho;
+      // inverse rotation of pairs (0,1) with c0 and (2,3) with c1
+      dn[0] = d[0] * c0.x + d[1] * c0.y;
+      dn[1] = -d[0] * c0.y + d[1] * c0.x;
+      dn[2] = d[2] * c1.x + d[3] * c1.y;
+      dn[3] = -d[2] * c1.y + d[3] * c1.x;
+      const float* g = is_q ? g_q : g_k;
+      float* acc = is_q ? aq : ak;
+      float dng[4];
+      float t = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[i] += dn[i] * n[i];
+        dng[i] = dn[i] * g[i];
+        t += n[i] * dng[i];
+      }
+      t = warp_sum(t) * (1.f / D);
+      float dq[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        dq[i] = rho * (dng[i] - n[i] * t);
+        s += dq[i] * x[i];
+        dq[i] *= r;
+      }
+      store_bf16x4(Gp + row * ldg + h * D + 4 * lane, dq);
+    }
+    for (int h = 0; h < n_kv; ++h) {
+      float d[4], v[4];
+      load_bf16x4(dV + row * ldkv + h * D + 4 * lane, d);
+      load_bf16x4(Vs + row * ldkv + h * D + 4 * lane, v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s += d[i] * v[i];
+        d[i] *= r;
+      }
+      store_bf16x4(Gp + row * ldg + ldsave + h * D + 4 * lane, d);
+    }
+    s = warp_sum(s);
+    if (lane == 0) srow[row] = s;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    red[w][4 * lane + i] = aq[i];
+    red[w][D + 4 * lane + i] = ak[i];
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < 2 * D; j += blockDim.x) {
+    float t = 0.f;
+    for (int ww = 0; ww < QK_BWD_WARPS; ++ww) t += red[ww][j];
+    dgam_part[static_cast<int64_t>(blockIdx.x) * 2 * D + j] = t;
+  }
+}
+
+cudaError_t launch_qk_bwd(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, const __nv_bfloat16* dV,
+                          const __nv_bfloat16* qk_save, const __nv_bfloat16* V, const float* gq, const float* gk,
+                          const int32_t* pos, const float2* cs, int max_pos, float eps, int n_q, int n_kv,
+                          const float* rstd, int64_t M, __nv_bfloat16* Gp, float* srow, float* dgam_part,
+                          int nblk, int* status, cudaStream_t s) {
+  qk_bwd_kernel<<<nblk, QK_BWD_WARPS * 32, 0, s>>>(dQ, dK, dV, qk_save, V, gq, gk, pos, cs, max_pos, eps, n_q, n_kv,
+                                                   rstd, M, Gp, srow, dgam_part, status);
+  return cudaGetLastError();
+}
+
+}  // namespace coda

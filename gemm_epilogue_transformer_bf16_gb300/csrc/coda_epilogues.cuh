@@ -1,0 +1,517 @@
+// Epilogue functors for coda_gemm_kernel.
+//
+// Each functor is one composition of the five epilogue primitive classes of
+// "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs" §3.1:
+//   (1) element-wise / pairwise maps, (2) rank-1 vector loads/stores,
+//   (3) rank-2 tile loads/stores, (4) tile row/column reductions to partials
+//   merged by a small second kernel, (5) running state across tiles.
+//
+// Thread layout: epilogue thread = one output row of the 128-row tile
+// (its TMEM lane); it walks the tile's columns 32 at a time.  Row reductions
+// are therefore thread-local; column reductions use a warp reduce-scatter.
+// All TMEM loads are executed by full warps (rows past M only mask their
+// global accesses).
+#pragma once
+#include "coda_gemm.cuh"
+
+namespace coda {
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+__device__ __forceinline__ void load_f32x8(const float* p, float* o) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void store_f32x8(float* p, const float* v) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// ---------------------------------------------------------------------------
+// PLAIN:  D = rs_i * cs_j * acc + aux0 - coef_i * aux1 (+ D if beta)
+// optional row partial  sum_j D_ij^2  (of the stored, rounded values).
+// Covers: plain store, residual add, RMSNorm row-scale (+ residual),
+// accumulate, the residual + partial-RMS epilogue, and dX - c*X of the
+// RMSNorm-reparameterised backward.
+// ---------------------------------------------------------------------------
+template <int BN>
+struct EpiPlain {
+  struct State {};
+  static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+    const int row = t.row;
+    const bool rv = row < t.M;
+    const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
+    const float rc = (e.row_coef && rv) ? e.row_coef[row] : 0.f;
+    float ss = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      const int col0 = t.nb * BN + c;
+      if (col0 >= t.N) break;
+      float v[32];
+      __syncwarp();
+      tmem_ld32(t.taddr + c, v);
+      if (rv) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int cc = col0 + g * 8;
+          if (cc < t.N) {
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = v[g * 8 + i] * rs;
+            if (e.col_scale) {
+              float s8[8];
+              load_f32x8(e.col_scale + cc, s8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[i] *= s8[i];
+            }
+            if (e.aux0) {
+              float r8[8];
+              load_bf16x8(e.aux0 + static_cast<int64_t>(row) * e.ld_aux0 + cc, r8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[i] += r8[i];
+            }
+            if (e.row_coef) {
+              float r8[8];
+              load_bf16x8(e.aux1 + static_cast<int64_t>(row) * e.ld_aux1 + cc, r8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[i] -= rc * r8[i];
+            }
+            if (e.d_f32) {
+              float* d = static_cast<float*>(e.D) + static_cast<int64_t>(row) * e.ldd + cc;
+              if (e.beta) {
+                float o8[8];
+                load_f32x8(d, o8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] += o8[i];
+              }
+              store_f32x8(d, x);
+              if (e.partials) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
+              }
+            } else {
+              __nv_bfloat16* d = static_cast<__nv_bfloat16*>(e.D) + static_cast<int64_t>(row) * e.ldd + cc;
+              if (e.beta) {
+                float o8[8];
+                load_bf16x8(d, o8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] += o8[i];
+              }
+              store_bf16x8(d, x);
+              if (e.partials) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float y = round_bf16(x[i]);
+                  ss += y * y;
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+    if (e.partials && rv) e.partials[static_cast<int64_t>(t.nb) * e.ld_part + row] = ss;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// SWIGLU (pairwise map on co-resident gate/up accumulators):
+//   accumulator columns [0, BN/2) = X Wg^T, [BN/2, BN) = X Wu^T for the same
+//   output columns;  g = rs*acc_g, u = rs*acc_u, H = silu(g) * u.
+//   Optionally stores g and u (bf16) for the backward.
+// ---------------------------------------------------------------------------
+template <int BN>
+struct EpiSwiglu {
+  struct State {};
+  static constexpr int HALF = BN / 2;
+  static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+    const int row = t.row;
+    const bool rv = row < t.M;
+    const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
+#pragma unroll 1
+    for (int c = 0; c < HALF; c += 32) {
+      const int col0 = t.nb * HALF + c;
+      if (col0 >= t.N) break;
+      float g[32], u[32];
+      __syncwarp();
+      tmem_ld32(t.taddr + c, g);
+      tmem_ld32(t.taddr + HALF + c, u);
+      if (rv) {
+        const int64_t off = static_cast<int64_t>(row);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cc = col0 + q * 8;
+          if (cc < t.N) {
+            float gg[8], uu[8], h[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              gg[i] = g[q * 8 + i] * rs;
+              uu[i] = u[q * 8 + i] * rs;
+              h[i] = gg[i] / (1.f + __expf(-gg[i])) * uu[i];
+            }
+            store_bf16x8(static_cast<__nv_bfloat16*>(e.D) + off * e.ldd + cc, h);
+            if (e.out1) store_bf16x8(e.out1 + off * e.ld_out1 + cc, gg);
+            if (e.out2) store_bf16x8(e.out2 + off * e.ld_out2 + cc, uu);
+          }
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// DSWIGLU on the dH = dY Wd GEMM: loads the saved g, u tiles (aux0, aux1),
+//   dG = dH u s (1 + g (1 - s)),  dU = dH g s,   s = sigmoid(g)
+// stores rs*dG (out1) and rs*dU (out2) -- the row-scaled gradients G' that
+// the RMSNorm-reparameterised backward feeds to its GEMMs -- and, when
+// `partials` is set, the row partial sum_j (dG g + dU u) that the RMSNorm
+// backward coefficient needs.  out3 (optional) receives H = silu(g) u.
+// ---------------------------------------------------------------------------
+template <int BN>
+struct EpiDSwiglu {
+  struct State {};
+  static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+    const int row = t.row;
+    const bool rv = row < t.M;
+    const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
+    float dot = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      const int col0 = t.nb * BN + c;
+      if (col0 >= t.N) break;
+      float dh[32];
+      __syncwarp();
+      tmem_ld32(t.taddr + c, dh);
+      if (rv) {
+        const int64_t off = static_cast<int64_t>(row);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cc = col0 + q * 8;
+          if (cc < t.N) {
+            float g8[8], u8[8], dg[8], du[8], h[8];
+            load_bf16x8(e.aux0 + off * e.ld_aux0 + cc, g8);
+            load_bf16x8(e.aux1 + off * e.ld_aux1 + cc, u8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float s = 1.f / (1.f + __expf(-g8[i]));
+              const float sg = g8[i] * s;
+              const float d = dh[q * 8 + i];
+              dg[i] = d * u8[i] * s * (1.f + g8[i] * (1.f - s));
+              du[i] = d * sg;
+              h[i] = sg * u8[i];
+              dot += dg[i] * g8[i] + du[i] * u8[i];
+              dg[i] *= rs;
+              du[i] *= rs;
+            }
+            store_bf16x8(e.out1 + off * e.ld_out1 + cc, dg);
+            store_bf16x8(e.out2 + off * e.ld_out2 + cc, du);
+            if (e.out3) store_bf16x8(e.out3 + off * e.ld_out3 + cc, h);
+          }
+        }
+      }
+    }
+    if (e.partials && rv) e.partials[static_cast<int64_t>(t.nb) * e.ld_part + row] = dot;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// COLDOT (weight-gradient epilogue of the RMSNorm-reparameterised backward):
+// the accumulator is dW'[n, k] (rows = weight output features);
+//   D = cs_k * acc                (dW = dW' diag(gamma))
+//   column partial  sum_n aux0[n, k] * acc[n, k]   (dgamma contribution)
+// written per (m block, warp) to partials[(mb*4 + warp) * ld_part + k].
+// ---------------------------------------------------------------------------
+template <int BN>
+struct EpiColDot {
+  struct State {};
+  static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+    const int row = t.row;
+    const bool rv = row < t.M;
+    const int lane = threadIdx.x & 31;
+    const int q = (threadIdx.x >> 5) & 3;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      const int col0 = t.nb * BN + c;
+      if (col0 >= t.N) break;
+      float v[32];
+      __syncwarp();
+      tmem_ld32(t.taddr + c, v);
+      float p[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) p[i] = 0.f;
+      if (rv) {
+        const int64_t off = static_cast<int64_t>(row);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int cc = col0 + g * 8;
+          if (cc < t.N) {
+            float w8[8], s8[8], x[8];
+            load_bf16x8(e.aux0 + off * e.ld_aux0 + cc, w8);
+            if (e.col_scale) load_f32x8(e.col_scale + cc, s8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              p[g * 8 + i] = v[g * 8 + i] * w8[i];
+              x[i] = e.col_scale ? v[g * 8 + i] * s8[i] : v[g * 8 + i];
+            }
+            store_bf16x8(static_cast<__nv_bfloat16*>(e.D) + off * e.ldd + cc, x);
+          }
+        }
+      }
+      // reduce-scatter over the warp: afterwards lane L holds the column
+      // sum of column col0 + L over this warp's 32 rows.
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const bool hi = lane & 16;
+        const float keep = hi ? p[i + 16] : p[i];
+        const float send = hi ? p[i] : p[i + 16];
+        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const bool hi = lane & 8;
+        const float keep = hi ? p[i + 8] : p[i];
+        const float send = hi ? p[i] : p[i + 8];
+        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool hi = lane & 4;
+        const float keep = hi ? p[i + 4] : p[i];
+        const float send = hi ? p[i] : p[i + 4];
+        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const bool hi = lane & 2;
+        const float keep = hi ? p[i + 2] : p[i];
+        const float send = hi ? p[i] : p[i + 2];
+        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+      }
+      {
+        const bool hi = lane & 1;
+        const float keep = hi ? p[1] : p[0];
+        const float send = hi ? p[0] : p[1];
+        p[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+      }
+      if (e.partials && col0 + lane < t.N)
+        e.partials[static_cast<int64_t>(t.mb * 4 + q) * e.ld_part + col0 + lane] = p[0];
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// CE_LSE (state transition): logits tile z = X W^T never leaves the chip.
+// Per row, a running (max, sum-exp) over the unit's consecutive vocab tiles;
+// the target logit is written when the label falls in the tile; at the end of
+// the unit (one vocab chunk) the state goes to partials[chunk][row] (float2).
+// ---------------------------------------------------------------------------
+template <int BN>
+struct EpiCeLse {
+  struct State {
+    float m, s;
+    int label;
+  };
+  static __device__ __forceinline__ void begin(State& st, const EpiArgs& e, const TileInfo& t) {
+    st.m = -INFINITY;
+    st.s = 0.f;
+    st.label = t.row < t.M ? e.labels[t.row] : -1;
+  }
+  static __device__ __forceinline__ void end(State& st, const EpiArgs& e, const TileInfo& t) {
+    if (t.row < t.M)
+      reinterpret_cast<float2*>(e.partials)[static_cast<int64_t>(t.unit_chunk) * e.ld_part + t.row] =
+          make_float2(st.m, st.s);
+  }
+  static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t, float*) {
+    const bool rv = t.row < t.M;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      const int col0 = t.nb * BN + c;
+      if (col0 >= t.N) break;
+      float z[32];
+      __syncwarp();
+      tmem_ld32(t.taddr + c, z);
+      if (rv) {
+        const int nvalid = min(32, t.N - col0);
+        float mc = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nvalid) mc = fmaxf(mc, z[i]);
+        const float mn = fmaxf(st.m, mc);
+        const float mb = mn * LOG2E;
+        float sc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nvalid) sc += exp2f(fmaf(z[i], LOG2E, -mb));
+        st.s = st.s * exp2f((st.m - mn) * LOG2E) + sc;
+        st.m = mn;
+        const int rel = st.label - col0;
+        if (rel >= 0 && rel < nvalid) {
+          float tv = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i == rel) tv = z[i];
+          e.target_logit[t.row] = tv;
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// CE_DLOGITS (softmax minus one-hot): recomputed logits z,
+//   dZ = (exp(z - lse_i) - [j == y_i]) * w_i,  w_i = dloss / n_valid for a
+//   valid row, 0 for an ignored (or out-of-range) label;  stored bf16.
+// ---------------------------------------------------------------------------
+template <int BN>
+struct EpiCeDlogits {
+  struct State {};
+  static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+    const int row = t.row;
+    const bool rv = row < t.M;
+    int lab = -1;
+    float w = 0.f, lse = 0.f;
+    if (rv) {
+      lab = e.labels[row];
+      const int nv = *e.n_valid;
+      const bool valid = lab != e.ignore_index && lab >= 0 && lab < t.N && nv > 0;
+      w = valid ? e.dloss / static_cast<float>(nv) : 0.f;
+      if (!valid) lab = -1;
+      lse = e.lse[row];
+    }
+    const float lb = lse * LOG2E;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      const int col0 = t.nb * BN + c;
+      if (col0 >= t.N) break;
+      float z[32];
+      __syncwarp();
+      tmem_ld32(t.taddr + c, z);
+      if (rv) {
+        __nv_bfloat16* d = static_cast<__nv_bfloat16*>(e.D) + static_cast<int64_t>(row) * e.ldd;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int cc = col0 + g * 8;
+          if (cc < t.N) {
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float p = exp2f(fmaf(z[g * 8 + i], LOG2E, -lb));
+              x[i] = (p - (cc + i == lab ? 1.f : 0.f)) * w;
+            }
+            store_bf16x8(d + cc, x);
+          }
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// QKNORM_ROPE (row scale + per-head RMSNorm + RoPE rotation, pairwise map):
+// a BN = 256 tile holds two 128-wide heads of the fused [q | k | v]
+// projection.  q/k heads: x = rs*acc, n = x * rsqrt(mean(x^2) + eps) * gamma,
+// pairs (2i, 2i+1) rotated by the (cos, sin) of (pos, i); optional save of x
+// (pre-norm, out1).  v heads: rs*acc stored as is.
+// ---------------------------------------------------------------------------
+template <int BN>
+struct EpiQkRope {
+  static_assert(BN % 128 == 0, "heads are 128 wide");
+  struct State {};
+  static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+    constexpr int D = 128;
+    const int row = t.row;
+    const bool rv = row < t.M;
+    const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
+    int pos = 0;
+    if (rv) {
+      pos = e.pos[row];
+      if (pos < 0 || pos >= e.max_pos) {
+        if (t.status) atomicOr(t.status, CODA_DEV_POSITION_RANGE);
+        pos = pos < 0 ? 0 : e.max_pos - 1;
+      }
+    }
+    const float2* cs = e.cos_sin + static_cast<int64_t>(pos) * (D / 2);
+    const int64_t off = static_cast<int64_t>(row);
+#pragma unroll 1
+    for (int hh = 0; hh < BN / D; ++hh) {
+      const int head = t.nb * (BN / D) + hh;
+      if (head * D >= t.N) break;
+      const uint32_t tcol = t.taddr + hh * D;
+      if (head >= e.n_q + e.n_kv) {
+        __nv_bfloat16* vout = e.V + off * e.ldv + (head - e.n_q - e.n_kv) * D;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          float v[32];
+          __syncwarp();
+          tmem_ld32(tcol + c, v);
+          if (rv) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= rs;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) store_bf16x8(vout + c + g * 8, v + g * 8);
+          }
+        }
+        continue;
+      }
+      const bool is_q = head < e.n_q;
+      const float* gamma = is_q ? e.gamma_q : e.gamma_k;
+      __nv_bfloat16* out = is_q ? e.Q + off * e.ldq + head * D : e.Kh + off * e.ldk + (head - e.n_q) * D;
+      float ss = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        float v[32];
+        __syncwarp();
+        tmem_ld32(tcol + c, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] *= rs;
+          ss += v[i] * v[i];
+        }
+        if (rv && e.out1) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) store_bf16x8(e.out1 + off * e.ld_out1 + head * D + c + g * 8, v + g * 8);
+        }
+      }
+      const float rho = rsqrtf(ss * (1.f / D) + e.eps);
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        float v[32];
+        __syncwarp();
+        tmem_ld32(tcol + c, v);
+        if (rv) {
+          float gm[32];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) load_f32x8(gamma + c + g * 8, gm + g * 8);
+          float o[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 r = cs[c / 2 + i];
+            const float a = v[2 * i] * rs * rho * gm[2 * i];
+            const float b = v[2 * i + 1] * rs * rho * gm[2 * i + 1];
+            o[2 * i] = a * r.x - b * r.y;
+            o[2 * i + 1] = a * r.y + b * r.x;
+          }
+#pragma unroll
+          for (int g = 0; g < 4; ++g) store_bf16x8(out + c + g * 8, o + g * 8);
+        }
+      }
+    }
+  }
+};
+
+}  // namespace coda

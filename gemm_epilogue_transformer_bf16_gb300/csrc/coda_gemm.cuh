@@ -1,0 +1,346 @@
+// Persistent, warp-specialised bf16 GEMM for sm_103a with a programmable
+// epilogue.
+//
+//   D[m, n] = epilogue( sum_k A(m, k) * B(n, k) )   (fp32 accumulation)
+//
+// This is the fixed GEMM mainloop plus per-output-tile epilogue of "CODA:
+// Rewriting Transformer Blocks as GEMM-Epilogue Programs" (§2.2 and §3.1: the
+// epilogue sees one output tile, its accumulator and consistently-indexed
+// auxiliary tensors).  The GB300 mapping:
+//
+//   warp 0        TMA producer: one elected thread streams A/B k-slices
+//                 (64 bf16 = 128 bytes wide, 128-byte swizzle) into a
+//                 STAGES-deep shared-memory ring, completion counted on
+//                 per-stage mbarriers.
+//   warp 1        TMEM owner and UMMA issuer: one thread issues
+//                 tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM
+//                 accumulators, frees smem stages with tcgen05.commit and
+//                 signals a finished accumulator to the epilogue.
+//   warps 2..5    epilogue: tcgen05.ld of their 32-lane quarter of the
+//                 accumulator (thread = output row), the epilogue functor's
+//                 math, vectorised 16-byte global stores.  Two accumulators
+//                 let the epilogue of tile i overlap the mainloop of tile i+1.
+//
+// Operands can be K-major (row-major [rows, K], the nn.Linear weight layout)
+// or MN-major (row-major [K, rows]); backward GEMMs need both.  A second
+// (A, B) descriptor pair continues the contraction (concatenated K), and a
+// second B descriptor can fill the upper half of the tile's N (the SwiGLU
+// gate/up pair).  Every wait is bounded: on expiry the CTA records
+// CODA_DEV_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and
+// returns.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "coda_ptx.cuh"
+
+namespace coda {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARP0 = 2;
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int STAGES = BN >= 256 ? 4 : 6;
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr uint32_t BAR_BYTES = 256;
+  static constexpr uint32_t EPI_SMEM_BYTES = BN * 4;
+  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + EPI_SMEM_BYTES;
+};
+
+// Everything an epilogue may read or write.  Unused fields are null/zero.
+struct EpiArgs {
+  void* D;
+  int64_t ldd;
+  int d_f32;
+  int beta;
+  const float* row_scale;
+  const float* col_scale;
+  const __nv_bfloat16* aux0;
+  int64_t ld_aux0;
+  const __nv_bfloat16* aux1;
+  int64_t ld_aux1;
+  const float* row_coef;
+  __nv_bfloat16* out1;
+  int64_t ld_out1;
+  __nv_bfloat16* out2;
+  int64_t ld_out2;
+  __nv_bfloat16* out3;
+  int64_t ld_out3;
+  float* partials;
+  int64_t ld_part;
+  // cross-entropy
+  const int32_t* labels;
+  int32_t ignore_index;
+  const float* lse;
+  const int32_t* n_valid;
+  float dloss;
+  float* target_logit;
+  // QK-RMSNorm + RoPE
+  const int32_t* pos;
+  const float2* cos_sin;
+  int max_pos;
+  int n_q;
+  int n_kv;
+  float eps;
+  const float* gamma_q;
+  const float* gamma_k;
+  __nv_bfloat16* Q;
+  __nv_bfloat16* Kh;
+  __nv_bfloat16* V;
+  int64_t ldq;
+  int64_t ldk;
+  int64_t ldv;
+};
+
+struct GemmArgs {
+  int M, N;          // output rows / columns seen by the epilogue
+  int num_m, num_n;  // tile grid
+  int kb0, kb1;      // k-blocks of descriptor pair 0 and pair 1
+  int a_mn, b_mn;    // operand major-ness (1 = MN-major)
+  int b_dual;        // B tile = [B0 rows | B1 rows], BN/2 each
+  int n_per_unit;    // consecutive N tiles handled as one unit (running state)
+  int num_units;
+  int group_m;       // raster: M blocks per group
+  uint32_t idesc;
+  int* status;
+  uint64_t timeout_ns;
+  EpiArgs e;
+};
+
+struct TileInfo {
+  int mb, nb, unit_chunk;
+  int row;          // global output row of this thread
+  int M, N;
+  uint32_t taddr;   // TMEM address of this warp's lane quarter, column 0
+  int* status;
+};
+
+// Unit -> (m block, first n block, number of n blocks).
+__device__ __forceinline__ void unit_coords(const GemmArgs& a, int u, int& mb, int& nb0, int& nlen, int& chunk) {
+  if (a.n_per_unit <= 1) {
+    const int per_group = a.group_m * a.num_n;
+    const int g = u / per_group;
+    const int first_m = g * a.group_m;
+    const int gm = min(a.group_m, a.num_m - first_m);
+    const int r = u - g * per_group;
+    mb = first_m + r % gm;
+    nb0 = r / gm;
+    nlen = 1;
+    chunk = nb0;
+  } else {
+    chunk = u / a.num_m;
+    mb = u - chunk * a.num_m;
+    nb0 = chunk * a.n_per_unit;
+    nlen = min(a.n_per_unit, a.num_n - nb0);
+  }
+}
+
+__device__ __forceinline__ void epi_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+template <int BN, class Epi>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    coda_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mB0,
+                     const __grid_constant__ CUtensorMap mA1, const __grid_constant__ CUtensorMap mB1,
+                     const GemmArgs args) {
+  using Cfg = GemmCfg<BN>;
+  constexpr int S = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* epi_smem = reinterpret_cast<float*>(smem + S * Cfg::STAGE_BYTES + Cfg::BAR_BYTES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mA0);
+    tma_prefetch_desc(&mB0);
+    if (args.kb1 > 0) {
+      tma_prefetch_desc(&mA1);
+      tma_prefetch_desc(&mB1);
+    }
+    if (args.b_dual) tma_prefetch_desc(&mB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  for (int i = threadIdx.x; i < BN; i += NUM_THREADS) epi_smem[i] = 0.f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_kb = args.kb0 + args.kb1;
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int u = blockIdx.x; u < args.num_units && !aborted; u += gridDim.x) {
+        int mb, nb0, nlen, chunk;
+        unit_coords(args, u, mb, nb0, nlen, chunk);
+        for (int j = 0; j < nlen && !aborted; ++j) {
+          const int nb = nb0 + j;
+          for (int kb = 0; kb < num_kb; ++kb, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (it / S) & 1;
+            if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, args.status, args.timeout_ns)) {
+              aborted = true;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+            const bool second = kb >= args.kb0;
+            const CUtensorMap* ma = second ? &mA1 : &mA0;
+            const CUtensorMap* mbp = second ? &mB1 : &mB0;
+            const int k = (second ? kb - args.kb0 : kb) * BK;
+            uint8_t* sa = tiles + s * Cfg::STAGE_BYTES;
+            uint8_t* sb = sa + Cfg::A_BYTES;
+            if (!args.a_mn) {
+              tma_load_2d(sa, ma, &full[s], k, mb * BM);
+            } else {
+#pragma unroll
+              for (int c = 0; c < BM / 64; ++c) tma_load_2d(sa + c * 8192, ma, &full[s], mb * BM + c * 64, k);
+            }
+            if (args.b_dual) {
+              tma_load_2d(sb, &mB0, &full[s], k, nb * (BN / 2));
+              tma_load_2d(sb + (BN / 2) * 128, &mB1, &full[s], k, nb * (BN / 2));
+            } else if (!args.b_mn) {
+              tma_load_2d(sb, mbp, &full[s], k, nb * BN);
+            } else {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * 8192, mbp, &full[s], nb * BN + c * 64, k);
+            }
+          }
+        }
+      }
+      if (aborted) {
+        // let every copy already issued land before the CTA's smem is reused
+        const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
+        for (uint32_t j = first; j < it; ++j) mbar_wait_drain(&full[j % S], (j / S) & 1, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, t = 0;
+      bool issued = false;
+      for (int u = blockIdx.x; u < args.num_units && !aborted; u += gridDim.x) {
+        int mb, nb0, nlen, chunk;
+        unit_coords(args, u, mb, nb0, nlen, chunk);
+        for (int j = 0; j < nlen && !aborted; ++j, ++t) {
+          const uint32_t buf = t & 1;
+          if (!mbar_wait_bounded(&tempty[buf], ((t >> 1) & 1) ^ 1, abort_flag, args.status, args.timeout_ns)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+          for (int kb = 0; kb < num_kb; ++kb, ++it) {
+            const int s = it % S;
+            if (!mbar_wait_bounded(&full[s], (it / S) & 1, abort_flag, args.status, args.timeout_ns)) {
+              aborted = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(tiles + s * Cfg::STAGE_BYTES);
+            const uint32_t sb = sa + Cfg::A_BYTES;
+#pragma unroll
+            for (int k16 = 0; k16 < BK / 16; ++k16) {
+              // K-major: rows of 128 B, 8-row swizzle atoms 1024 B apart; a
+              // 16-element k step is +32 B inside the atom.  MN-major: 64-wide
+              // MN chunks 8 KB apart (LBO), 8-row k groups 1 KB apart (SBO);
+              // a 16-row k step is +2 KB.
+              const uint64_t ad = args.a_mn ? sdesc_sw128(sa + k16 * 2048, 8192, 1024)
+                                            : sdesc_sw128(sa + k16 * 32, 16, 1024);
+              const uint64_t bd = args.b_mn ? sdesc_sw128(sb + k16 * 2048, 8192, 1024)
+                                            : sdesc_sw128(sb + k16 * 32, 16, 1024);
+              umma_bf16(d_tmem, ad, bd, args.idesc, (kb | k16) != 0);
+            }
+            issued = true;
+            umma_commit(&empty[s]);
+          }
+          if (aborted) break;
+          umma_commit(&tfull[buf]);
+        }
+      }
+      if (aborted && issued) {
+        umma_commit(drain);
+        mbar_wait_drain(drain, 0, 200000000ull);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint32_t t = 0;
+    for (int u = blockIdx.x; u < args.num_units && !aborted; u += gridDim.x) {
+      int mb, nb0, nlen, chunk;
+      unit_coords(args, u, mb, nb0, nlen, chunk);
+      TileInfo ti;
+      ti.mb = mb;
+      ti.unit_chunk = chunk;
+      ti.row = mb * BM + q * 32 + lane;
+      ti.M = args.M;
+      ti.N = args.N;
+      ti.status = args.status;
+      typename Epi::State st;
+      Epi::begin(st, args.e, ti);
+      for (int j = 0; j < nlen; ++j, ++t) {
+        const uint32_t buf = t & 1;
+        if (!mbar_wait_bounded(&tfull[buf], (t >> 1) & 1, abort_flag, args.status, args.timeout_ns)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        __syncwarp();
+        ti.nb = nb0 + j;
+        ti.taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+        Epi::tile(st, args.e, ti, epi_smem);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+      }
+      if (aborted) break;
+      Epi::end(st, args.e, ti);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace coda

@@ -1,0 +1,50 @@
+// Internal launcher declarations shared by the host library's translation
+// units.  Not part of the public ABI (see include/coda.h).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "coda_gemm.cuh"
+
+namespace coda {
+
+enum class EpiKind : int { Plain = 0, Swiglu, DSwiglu, QkRope, CeLse, CeDlogits, ColDot };
+
+// Tensor maps in the order A0, B0, A1, B1.
+cudaError_t launch_gemm_plain(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
+cudaError_t launch_gemm_swiglu(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
+cudaError_t launch_gemm_dswiglu(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
+cudaError_t launch_gemm_qkrope(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
+cudaError_t launch_gemm_celse(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
+cudaError_t launch_gemm_cedlogits(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
+cudaError_t launch_gemm_coldot(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
+
+// auxiliary kernels (coda_aux.cu)
+cudaError_t launch_fold_gamma(const __nv_bfloat16* W, const float* gamma, __nv_bfloat16* Wf, int64_t N, int64_t K,
+                              int num_sms, cudaStream_t s);
+cudaError_t launch_row_rstd(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, float eps, float* rstd,
+                            int num_sms, cudaStream_t s);
+// mode 0: out = 1/sqrt(sum_t p[t] * inv_k + eps);  mode 1: out = r^2 * sum_t p[t] * inv_k
+cudaError_t launch_combine_rows(const float* p, int64_t ld, int nparts, int64_t M, float inv_k, float eps,
+                                const float* r, float* out, int mode, cudaStream_t s);
+cudaError_t launch_rms_bwd_prepass(const __nv_bfloat16* G, const __nv_bfloat16* Y, const __nv_bfloat16* R,
+                                   const float* rstd, int64_t M, int64_t N, __nv_bfloat16* Gp, float* srow,
+                                   int num_sms, cudaStream_t s);
+cudaError_t launch_colsum(const float* p, int64_t nrows, int64_t ncols, int64_t ld, float* out, cudaStream_t s);
+cudaError_t launch_ce_combine(const float2* part, int64_t ld, int nchunks, const float* target,
+                              const int32_t* labels, int32_t ignore, int64_t M, int64_t V, float* lse,
+                              double* blk_loss, int* blk_cnt, int nblk, float* loss_mean, int32_t* n_valid,
+                              int* status, cudaStream_t s);
+cudaError_t launch_rope_table(double theta, int head_dim, int max_pos, float2* cs, cudaStream_t s);
+cudaError_t launch_qk_bwd(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, const __nv_bfloat16* dV,
+                          const __nv_bfloat16* qk_save, const __nv_bfloat16* V, const float* gq, const float* gk,
+                          const int32_t* pos, const float2* cs, int max_pos, float eps, int n_q, int n_kv,
+                          const float* rstd, int64_t M, __nv_bfloat16* Gp, float* srow, float* dgam_part,
+                          int nblk, int* status, cudaStream_t s);
+
+constexpr int QK_BWD_WARPS = 8;
+constexpr int CE_COMBINE_THREADS = 256;
+
+}  // namespace coda

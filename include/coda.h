@@ -1,0 +1,351 @@
+/*
+ * coda.h -- C ABI of libcoda.so: bf16 GEMMs whose output tiles are
+ * transformed on chip by composable epilogue primitives, and the transformer
+ * operators built from them (GB300 / sm_103a).
+ *
+ * Source of the method: "CODA: Rewriting Transformer Blocks as GEMM-Epilogue
+ * Programs" (arXiv 2605.19269): §2.2 (GEMM mainloop + epilogue, locality
+ * constraint), §3.1 (the five epilogue primitive classes), §3.2 (h = xW,
+ * y[i,j] = f_ij(tile)), §3.2.1 (GEMM-residual-RMSNorm-GEMM reparameterisation
+ * y = RMSNorm(xW0 + z, gamma) W1 = (r (xW0 + z) ⊙ gamma) W1, Fig. 4); the
+ * functional operator names linear_swiglu, linear_cross_entropy and
+ * linear_qknorm_rope come from the x-tip guide "CODA: 把 Transformer Block
+ * 重写成 GEMM-Epilogue 程序" (section 核验过程 / 使用 Functional API).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library never allocates or frees device memory.  Calls that need scratch
+ *    take a caller-allocated workspace `ws` of at least the size returned by
+ *    the matching *_workspace_size() query; its first 256 bytes hold the
+ *    device status word (zero it once, e.g. with coda_reset_status, before
+ *    first use).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  They return after enqueueing.
+ *  - Matrices are row-major with a leading dimension (row stride) given in
+ *    ELEMENTS.  Weights use the nn.Linear layout [out_features, in_features].
+ *  - bf16 tensors are passed as uint16_t bit patterns (coda_bf16).  All
+ *    fp32 -> bf16 conversions round to nearest even.  Accumulation is fp32.
+ *  - Alignment: every tensor pointer 16-byte aligned, every leading dimension
+ *    a multiple of 8 elements, feature dimensions (N, K, I, V, hidden) a
+ *    multiple of 8.  M (tokens) is arbitrary.
+ *  - Errors detected on the host are returned before anything is enqueued:
+ *    CODA_ERR_INVALID_ARG, CODA_ERR_ALIGNMENT, CODA_ERR_UNSUPPORTED,
+ *    CODA_ERR_WORKSPACE.  CODA_ERR_CUDA reports a failed launch.  Errors
+ *    found on the device (a bounded wait that ran out, a label or position
+ *    out of range) set bits of the workspace status word; read them with
+ *    coda_get_status().
+ *  - M == 0 (no rows) is a valid no-op.
+ */
+#ifndef CODA_H
+#define CODA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t coda_bf16;
+typedef void* coda_stream;
+
+typedef enum coda_status {
+  CODA_OK = 0,
+  CODA_ERR_INVALID_ARG = 1,    /* null required pointer, negative size, bad enum */
+  CODA_ERR_ALIGNMENT = 2,      /* pointer not 16-byte aligned or ld % 8 != 0 */
+  CODA_ERR_UNSUPPORTED = 3,    /* shape or option combination not implemented */
+  CODA_ERR_WORKSPACE = 4,      /* ws NULL or ws_bytes below the queried size */
+  CODA_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */
+  CODA_ERR_TIMEOUT = 6,        /* device: a bounded pipeline wait ran out */
+  CODA_ERR_LABEL_RANGE = 7,    /* device: label outside [0,V) and != ignore_index */
+  CODA_ERR_POSITION_RANGE = 8  /* device: RoPE position outside [0, max_pos) */
+} coda_status;
+
+/* Operand storage order of a GEMM operand. */
+enum { CODA_K_MAJOR = 0, CODA_MN_MAJOR = 1 };
+/* Output element type. */
+enum { CODA_BF16 = 0, CODA_F32 = 1 };
+
+/* Epilogue map selected in coda_epilogue_desc.map (§3.1 classes 1-5). */
+enum {
+  CODA_MAP_NONE = 0,         /* D = rs*cs*acc + aux_in[0] - row_coef*aux_in[1] (+D if beta); optional row sum-of-squares partials */
+  CODA_MAP_SWIGLU = 1,       /* H = silu(rs*X B^T) * (rs*X B2^T); aux_out[0], aux_out[1] save g, u */
+  CODA_MAP_DSWIGLU = 2,      /* acc = dH; aux_in = g, u; aux_out[0..2] = rs*dG, rs*dU, H; partials = row sum(dG g + dU u) */
+  CODA_MAP_QKNORM_ROPE = 3,  /* per-head RMSNorm + RoPE of q/k heads, v pass-through; aux_out[0] saves pre-norm q|k */
+  CODA_MAP_CE_LSE = 4,       /* online (max, sum-exp) per row over vocab tiles + target logit; D unused */
+  CODA_MAP_CE_DLOGITS = 5,   /* D = (softmax(acc) - onehot) * dloss / n_valid */
+  CODA_MAP_COLDOT = 6        /* D = cs*acc; partials = column sums of aux_in[0]*acc per 32-row group */
+};
+
+/*
+ * Epilogue descriptor: which primitives run on each output tile before it is
+ * written ("CODA" §3.1: element-wise/pairwise maps, rank-1 vector loads,
+ * rank-2 tile loads/stores, tile reductions to partials, running state).
+ * Unused pointers must be NULL, unused integers 0.
+ */
+typedef struct coda_epilogue_desc {
+  int32_t map;                   /* CODA_MAP_* */
+  const float* row_scale;        /* [M] fp32 per-row factor rs (e.g. 1/rms) or NULL */
+  const float* col_scale;        /* [N] fp32 per-column factor cs (e.g. gamma) or NULL */
+  const coda_bf16* aux_in[2];    /* rank-2 tile loads, [M, N] bf16 row-major */
+  int64_t ld_aux_in[2];
+  const float* row_coef;         /* [M] fp32: MAP_NONE subtracts row_coef[i]*aux_in[1][i,j] */
+  coda_bf16* aux_out[3];         /* rank-2 tile stores, [M, N] bf16 row-major */
+  int64_t ld_aux_out[3];
+  float* partials;               /* reduction partials (layout per map, see coda_gemm_epilogue) */
+  int64_t ld_partials;           /* elements between partial rows (>= M for row partials, >= N for column partials) */
+  int32_t beta;                  /* 1: accumulate into D (D += result) */
+  const coda_bf16* B2;           /* MAP_SWIGLU: second weight [N, K] (K-major) */
+  int64_t ldb2;
+  const coda_bf16* A2;           /* concatenated K: second (A2, B2) pair, same major-ness as A, B */
+  int64_t lda2;
+  int64_t K2;                    /* contraction length of the second pair (0 = none) */
+  /* cross-entropy */
+  const int32_t* labels;         /* [M] */
+  int32_t ignore_index;
+  const float* lse;              /* [M] saved log-sum-exp (CE_DLOGITS) */
+  const int32_t* n_valid;        /* device int32: number of non-ignored rows (CE_DLOGITS) */
+  float dloss;                   /* upstream gradient of the mean loss (CE_DLOGITS) */
+  float* target_logit;           /* [M] fp32 out (CE_LSE) */
+  int32_t vocab_tiles_per_unit;  /* CE_LSE: 256-wide vocab tiles per running-state chunk (0 = 16) */
+  /* QK-RMSNorm + RoPE */
+  const int32_t* positions;      /* [M] */
+  const float* cos_sin;          /* [max_pos, head_dim/2, 2] fp32 table from coda_rope_table */
+  int32_t max_pos;
+  int32_t n_q_heads, n_kv_heads, head_dim;
+  float eps;
+  const float* gamma_q;          /* [head_dim] */
+  const float* gamma_k;          /* [head_dim] */
+  coda_bf16* Q;                  /* [M, n_q*head_dim] */
+  coda_bf16* K;                  /* [M, n_kv*head_dim] */
+  coda_bf16* V;                  /* [M, n_kv*head_dim] */
+} coda_epilogue_desc;
+
+/* ------------------------------------------------------------------------
+ * Library / device status
+ * --------------------------------------------------------------------- */
+
+/* Version string of the library. */
+const char* coda_version(void);
+
+/* Human-readable name of a status code. */
+const char* coda_status_string(int status);
+
+/* Synchronises `stream`, then maps the device status word at the start of
+ * `ws` to a coda_status (CODA_OK if no device error bit is set).  The word is
+ * sticky: it keeps its bits until coda_reset_status(). */
+int coda_get_status(const void* ws, coda_stream stream);
+
+/* Enqueues a clear of the device status word (asynchronous). */
+int coda_reset_status(void* ws, coda_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Generic GEMM + epilogue ("CODA" §3.2: h = xW, y[i,j] = f_ij(h tile))
+ *
+ *   acc[m, n] = sum_k A(m, k) * B(n, k)   (+ the A2/B2 pair when K2 > 0)
+ *   D = epilogue(acc)                      (desc->map, see CODA_MAP_*)
+ *
+ * A: a_major == CODA_K_MAJOR -> A is [M, K] with row stride lda;
+ *    CODA_MN_MAJOR -> A is stored [K, M] with row stride lda.
+ * B: b_major == CODA_K_MAJOR -> B is [N, K] (nn.Linear weight);
+ *    CODA_MN_MAJOR -> B is stored [K, N].
+ * D: [M, N] row-major, d_dtype CODA_BF16 or CODA_F32 (F32 only for MAP_NONE).
+ * Partials layouts: MAP_NONE / MAP_DSWIGLU row partials [ceil(N/256), ld] fp32;
+ * MAP_CE_LSE (max, sumexp) float2 [ceil(ceil(N/256)/tiles_per_unit), ld];
+ * MAP_COLDOT column partials [4*ceil(M/128), ld].
+ * MAP_SWIGLU: N is the output width; B and B2 are the gate and up weights.
+ * Workspace: coda_gemm_epilogue_workspace_size() bytes (the status word).
+ * ---------------------------------------------------------------------- */
+size_t coda_gemm_epilogue_workspace_size(void);
+int coda_gemm_epilogue(const coda_epilogue_desc* desc,
+                       const coda_bf16* A, int64_t lda, int a_major,
+                       const coda_bf16* B, int64_t ldb, int b_major,
+                       void* D, int64_t ldd, int d_dtype,
+                       int64_t M, int64_t N, int64_t K,
+                       void* ws, size_t ws_bytes, coda_stream stream);
+
+/* ------------------------------------------------------------------------
+ * RMSNorm pieces ("CODA" §3.2.1)
+ * --------------------------------------------------------------------- */
+
+/* gamma fold: Wf[n, k] = bf16(gamma[k] * W[n, k]).  W, Wf: [N, K] bf16
+ * (may alias for an in-place fold); gamma: [K] fp32.  This is the
+ * "⊙ gamma moves into W1" step of the §3.2.1 equation; run once per weight
+ * version. */
+int coda_fold_gamma(const coda_bf16* W, const float* gamma, coda_bf16* Wf,
+                    int64_t N, int64_t K, coda_stream stream);
+
+/* r[i] = 1/sqrt(mean_k X[i,k]^2 + eps) for X [M, K] bf16 (row stride ldx):
+ * the per-row inverse RMS factor r of §3.2.1 for an input that no upstream
+ * GEMM epilogue produced. */
+int coda_rms_rstd(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, float eps,
+                  float* rstd, coda_stream stream);
+
+/* RoPE table: cos_sin[p, j] = (cos a, sin a), a = p * theta^(-2j/head_dim),
+ * j < head_dim/2, p < max_pos; computed in fp64, stored fp32.  Interleaved
+ * pair convention (2j, 2j+1). */
+int coda_rope_table(float theta, int32_t head_dim, int32_t max_pos, float* cos_sin,
+                    coda_stream stream);
+
+/* ------------------------------------------------------------------------
+ * RMSNorm-reparameterised projection + residual (§3.2.1, second GEMM)
+ *
+ *   Y = R + r ⊙ (X Wf^T),   Wf = W diag(gamma) (coda_fold_gamma),
+ *   which equals R + RMSNorm(X, gamma) W^T.
+ * X [M, K], Wf [N, K], R [M, N] (or NULL), Y [M, N] bf16.
+ * rstd_in: [M] fp32 r from an upstream epilogue, or NULL -> r is computed
+ * from X (eps) and also written to rstd_out (required then).
+ * ---------------------------------------------------------------------- */
+size_t coda_rmsnorm_linear_workspace_size(int64_t M, int64_t N, int64_t K);
+int coda_rmsnorm_linear(const coda_bf16* X, const float* rstd_in, const coda_bf16* Wf,
+                        const coda_bf16* R, float eps, float* rstd_out, coda_bf16* Y,
+                        int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* Backward of coda_rmsnorm_linear for upstream gradient dY [M, N]:
+ *   G' = r ⊙ dY,  c_i = r_i^2 sum_n dY_in (Y - R)_in / K,
+ *   dX = G' Wf - c ⊙ X,  dW' = G'^T X,  dW = dW' diag(gamma),
+ *   dgamma_k = sum_n W_nk dW'_nk.   (dR = dY: no copy is made.)
+ * Inputs: X [M,K], W and Wf [N,K], gamma [K], rstd [M], Y and R [M,N]
+ * (R may be NULL = zero).  Outputs: dX [M,K], dW [N,K] bf16, dgamma [K] fp32.
+ * The pages state only that this backward keeps the GEMM-epilogue form; the
+ * formulas are the chain rule of the §3.2.1 equation. */
+size_t coda_rmsnorm_linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K);
+int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W,
+                            const coda_bf16* Wf, const float* gamma, const float* rstd,
+                            const coda_bf16* Y, const coda_bf16* R,
+                            coda_bf16* dX, coda_bf16* dW, float* dgamma,
+                            int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Projection + residual (§3.2.1, first GEMM: "xW0 + z")
+ *
+ *   Y = R + X W^T    X [M, K], W [N, K], R [M, N] (NULL = 0), Y [M, N].
+ * rstd_out (optional, [M]): the epilogue also emits per-tile partial sums of
+ * squares of Y, merged by a small second kernel into
+ * rstd_out[i] = 1/sqrt(mean_n Y_in^2 + eps): the row factor r the next
+ * RMSNorm-reparameterised projection applies in its epilogue.
+ * ---------------------------------------------------------------------- */
+size_t coda_linear_residual_workspace_size(int64_t M, int64_t N, int64_t K);
+int coda_linear_residual(const coda_bf16* X, const coda_bf16* W, const coda_bf16* R,
+                         coda_bf16* Y, float eps, float* rstd_out,
+                         int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* Backward: dX = dY W [M, K], dW = dY^T X [N, K]; dR = dY (no copy). */
+size_t coda_linear_residual_bwd_workspace_size(int64_t M, int64_t N, int64_t K);
+int coda_linear_residual_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W,
+                             coda_bf16* dX, coda_bf16* dW,
+                             int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* ------------------------------------------------------------------------
+ * linear_swiglu (x-tip guide functional API; "CODA" §3.1 class 1 pairwise
+ * SwiGLU gate)
+ *
+ *   g = r ⊙ (X Wg^T),  u = r ⊙ (X Wu^T),  H = silu(g) ⊙ u
+ * X [M, K]; Wg, Wu [I, K] (pass gamma-folded weights with rstd for the
+ * RMSNorm-reparameterised MLP input); rstd [M] or NULL (r = 1);
+ * H [M, I]; g_save, u_save [M, I] or NULL.
+ * ---------------------------------------------------------------------- */
+size_t coda_linear_swiglu_workspace_size(int64_t M, int64_t I, int64_t K);
+int coda_linear_swiglu(const coda_bf16* X, const float* rstd, const coda_bf16* Wg, const coda_bf16* Wu,
+                       coda_bf16* H, coda_bf16* g_save, coda_bf16* u_save,
+                       int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* Backward of the SwiGLU MLP sublayer  Y = Xres + silu(g) u Wd^T  with
+ * g, u = linear_swiglu(X, rstd, Wgf, Wuf):
+ *   dH = dY Wd (GEMM) -> dSwiGLU epilogue -> G' = r ⊙ [dG | dU];
+ *   dX = G' [Wgf; Wuf] - c ⊙ X + dX_resid  (one GEMM over K = 2I);
+ *   dWd = dY^T H;  dWg = (G'_g^T X) diag(gamma), dWu likewise;
+ *   dgamma_k = sum_n (Wg_nk dWg'_nk + Wu_nk dWu'_nk).
+ * With rstd == NULL there is no RMSNorm (r = 1, c = 0, gamma ignored,
+ * Wgf/Wuf must equal Wg/Wu, dgamma untouched).
+ * Inputs: dY [M,K]; X [M,K]; rstd [M]|NULL; gamma [K]|NULL; Wg, Wu, Wgf, Wuf
+ * [I,K]; Wd [K,I]; g, u, H [M,I] saved by the forward; dX_resid [M,K]|NULL
+ * (gradient of the residual stream, added to dX).
+ * Outputs: dX [M,K], dWg, dWu [I,K], dWd [K,I] bf16; dgamma [K] fp32|NULL. */
+size_t coda_linear_swiglu_bwd_workspace_size(int64_t M, int64_t I, int64_t K);
+int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float* rstd, const float* gamma,
+                           const coda_bf16* Wg, const coda_bf16* Wu, const coda_bf16* Wgf, const coda_bf16* Wuf,
+                           const coda_bf16* Wd, const coda_bf16* g, const coda_bf16* u, const coda_bf16* H,
+                           const coda_bf16* dX_resid,
+                           coda_bf16* dX, coda_bf16* dWg, coda_bf16* dWu, coda_bf16* dWd, float* dgamma,
+                           int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* ------------------------------------------------------------------------
+ * linear_qknorm_rope (x-tip guide functional API): RMSNorm-reparameterised
+ * fused QKV projection with per-head QK-RMSNorm and RoPE in the epilogue.
+ *
+ *   [q | k | v] = r ⊙ (X Wf_qkv^T),  Wf_qkv = W_qkv diag(gamma_in),
+ *   Q_h = RoPE(RMSNorm_d(q_h) ⊙ gamma_q, pos),  K_h likewise, V = v.
+ * head_dim must be 128.  Column order of Wf_qkv rows: n_q q heads, then
+ * n_kv k heads, then n_kv v heads.  X [M, Kdim]; Wf_qkv [(n_q+2n_kv)*128, Kdim];
+ * rstd [M] (NULL: r = 1); gamma_q, gamma_k [128]; pos [M] int32 in
+ * [0, max_pos); cos_sin from coda_rope_table.  Outputs Q [M, n_q*128],
+ * K, V [M, n_kv*128]; qk_save [M, (n_q+n_kv)*128] pre-norm q|k or NULL.
+ * ---------------------------------------------------------------------- */
+size_t coda_linear_qknorm_rope_workspace_size(int64_t M, int64_t Kdim, int32_t n_q, int32_t n_kv, int32_t head_dim);
+int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf16* Wf_qkv,
+                            const float* gamma_q, const float* gamma_k, const int32_t* pos,
+                            const float* cos_sin, int32_t max_pos, float eps,
+                            int32_t n_q, int32_t n_kv, int32_t head_dim,
+                            coda_bf16* Q, coda_bf16* K, coda_bf16* V, coda_bf16* qk_save,
+                            int64_t M, int64_t Kdim, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* Backward: given dQ, dK, dV (gradients of the attention inputs), the saved
+ * pre-norm q|k (qk_save) and V:
+ *   per head  dn = RoPE^-1(dQ_h),  dq = rho (dn⊙gamma - n mean(n ⊙ dn⊙gamma)),
+ *   dgamma_q = sum dn ⊙ n;  dv = dV;  then the RMSNorm-reparameterised
+ *   projection backward with G = [dq | dk | dv]:
+ *   dX = r⊙G Wf_qkv - c ⊙ X + dX_resid, dW_qkv = ((r⊙G)^T X) diag(gamma_in),
+ *   dgamma_in.
+ * rstd/gamma_in may be NULL (no input RMSNorm; Wf_qkv == W_qkv then).
+ * Outputs: dX [M, Kdim], dW_qkv [(n_q+2n_kv)*128, Kdim] bf16; dgamma_in [Kdim],
+ * dgamma_q, dgamma_k [128] fp32. */
+size_t coda_linear_qknorm_rope_bwd_workspace_size(int64_t M, int64_t Kdim, int32_t n_q, int32_t n_kv,
+                                                  int32_t head_dim);
+int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const coda_bf16* dV,
+                                const coda_bf16* qk_save, const coda_bf16* V,
+                                const float* gamma_q, const float* gamma_k, const int32_t* pos,
+                                const float* cos_sin, int32_t max_pos, float eps,
+                                int32_t n_q, int32_t n_kv, int32_t head_dim,
+                                const coda_bf16* X, const float* rstd, const float* gamma_in,
+                                const coda_bf16* W_qkv, const coda_bf16* Wf_qkv, const coda_bf16* dX_resid,
+                                coda_bf16* dX, coda_bf16* dW_qkv, float* dgamma_in,
+                                float* dgamma_q, float* dgamma_k,
+                                int64_t M, int64_t Kdim, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* ------------------------------------------------------------------------
+ * linear_cross_entropy (x-tip guide functional API; "CODA" §3.1 class 5:
+ * running max / sum-exp state for online log-sum-exp and cross-entropy).
+ * Logits z = X W^T are never written to memory.
+ *
+ *   lse_i = log sum_j exp(z_ij),  loss_i = lse_i - z_{i,y_i},
+ *   loss_mean = sum over rows with y_i != ignore_index / n_valid
+ *   (NaN when n_valid == 0).
+ * X [M, K]; W [V, K]; labels [M] int32.  Outputs (device): loss_mean [1]
+ * fp32, lse [M] fp32 (saved for the backward), n_valid [1] int32.  A label
+ * outside [0, V) other than ignore_index sets CODA_ERR_LABEL_RANGE in the
+ * status word; the row is then treated as ignored.
+ * ---------------------------------------------------------------------- */
+size_t coda_linear_cross_entropy_workspace_size(int64_t M, int64_t V, int64_t K);
+int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int32_t* labels,
+                              int32_t ignore_index, float* loss_mean, float* lse, int32_t* n_valid,
+                              int64_t M, int64_t V, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* Backward for upstream gradient dloss of the mean loss:
+ *   dZ = (softmax(z) - onehot(y)) * dloss / n_valid (0 on ignored rows),
+ *   dX = dZ W [M, K], dW = dZ^T X [V, K] (bf16).
+ * lse and n_valid are the forward's outputs (device pointers).  dZ is
+ * recomputed tile by tile from X W^T and staged in the workspace. */
+size_t coda_linear_cross_entropy_bwd_workspace_size(int64_t M, int64_t V, int64_t K);
+int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const int32_t* labels,
+                                  int32_t ignore_index, const float* lse, const int32_t* n_valid,
+                                  float dloss, coda_bf16* dX, coda_bf16* dW,
+                                  int64_t M, int64_t V, int64_t K, void* ws, size_t ws_bytes,
+                                  coda_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CODA_H */

@@ -47,7 +47,33 @@ __all__ = [
     "rope_angles", "rope", "rope_inv", "qk_rmsnorm_rope_fwd", "qk_rmsnorm_rope_bwd",
     "linear_cross_entropy_fwd", "linear_cross_entropy_bwd",
     "block_fwd", "block_bwd", "block_flops", "mlp_flops", "ce_flops",
+    "gemm_epilogue_plain",
 ]
+
+
+# ---------------------------------------------------------------------------
+# the generic GEMM + element-wise / rank-1 / rank-2 epilogue
+# ---------------------------------------------------------------------------
+
+def gemm_epilogue_plain(A, B, row_scale=None, col_scale=None, aux0=None, row_coef=None, aux1=None,
+                        D_old=None):
+    """h = A B^T (A [M, K], B [N, K]); y_ij = rs_i cs_j h_ij + aux0_ij
+    - coef_i aux1_ij (+ D_old_ij).  [P1] §3.2: GEMM h = xW followed by a
+    tile-wise function y[i,j] = f_ij(h); the terms are the element-wise map,
+    rank-1 vector loads and rank-2 tile loads of §3.1 classes 1-3, and the
+    accumulation named in the abstract."""
+    y = A @ B.T
+    if row_scale is not None:
+        y = y * np.asarray(row_scale)[:, None]
+    if col_scale is not None:
+        y = y * np.asarray(col_scale)[None, :]
+    if aux0 is not None:
+        y = y + aux0
+    if row_coef is not None:
+        y = y - np.asarray(row_coef)[:, None] * aux1
+    if D_old is not None:
+        y = y + D_old
+    return y
 
 
 # ---------------------------------------------------------------------------

@@ -1,0 +1,49 @@
+"""Tolerances of the GPU-vs-oracle comparisons.
+
+  bf16 tensors          max |err| <= 3e-2 * RMS(ref)  and  ||err||_F / ||ref||_F <= 1e-2
+  fp32 reductions       relative error <= 1e-3   (rstd, lse, loss: computed from exact inputs)
+  integers              bit-exact
+
+Gain gradients (dgamma) are reductions over bf16-rounded intermediates, so
+they are held to the bf16 rule.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+BF16_MAX_REL_RMS = 3e-2
+BF16_FROB = 1e-2
+F32_REL = 1e-3
+
+
+def to_np(t):
+    if isinstance(t, torch.Tensor):
+        return t.detach().to("cpu").double().numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def bf16_metrics(got, ref):
+    g, r = to_np(got), to_np(ref)
+    assert g.shape == r.shape, f"shape {g.shape} != {r.shape}"
+    err = g - r
+    rms = float(np.sqrt(np.mean(r * r)))
+    fro = float(np.linalg.norm(err) / max(np.linalg.norm(r), 1e-300))
+    return float(np.max(np.abs(err))) / max(rms, 1e-300), fro
+
+
+def assert_bf16(got, ref, name):
+    g = to_np(got)
+    assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+    mx, fro = bf16_metrics(got, ref)
+    assert mx <= BF16_MAX_REL_RMS and fro <= BF16_FROB, \
+        f"{name}: max|err|/RMS = {mx:.3e} (<= {BF16_MAX_REL_RMS}), rel Frobenius = {fro:.3e} (<= {BF16_FROB})"
+    return mx, fro
+
+
+def assert_f32(got, ref, name, tol=F32_REL):
+    g, r = to_np(got), to_np(ref)
+    assert g.shape == r.shape, f"{name}: shape {g.shape} != {r.shape}"
+    rel = float(np.max(np.abs(g - r) / np.maximum(np.abs(r), 1e-30)))
+    assert rel <= tol, f"{name}: max relative error {rel:.3e} > {tol}"
+    return rel

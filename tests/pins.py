@@ -371,7 +371,29 @@ def check_block_grad(o):
     return max(_rel(b[g], _fd_grad(L, p[x])) for g, x in pairs)
 
 
+def check_gemm_epilogue_bruteforce(o):
+    """Triple loop over (i, j, k) in plain Python on a tiny problem."""
+    r = RNG(16)
+    M, N, K = 3, 4, 5
+    A, B = r.standard_normal((M, K)), r.standard_normal((N, K))
+    rs, cs = r.standard_normal(M), r.standard_normal(N)
+    a0, a1, d0 = r.standard_normal((M, N)), r.standard_normal((M, N)), r.standard_normal((M, N))
+    coef = r.standard_normal(M)
+    got = o.gemm_epilogue_plain(A, B, rs, cs, a0, coef, a1, d0)
+    ref = np.zeros((M, N))
+    for i in range(M):
+        for j in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += A[i, k] * B[j, k]
+            ref[i, j] = rs[i] * cs[j] * acc + a0[i, j] - coef[i] * a1[i, j] + d0[i, j]
+    plain = o.gemm_epilogue_plain(A, B)
+    ref2 = np.array([[sum(A[i, k] * B[j, k] for k in range(K)) for j in range(N)] for i in range(M)])
+    return max(_rel(got, ref), _rel(plain, ref2))
+
+
 ALL_CHECKS = {
+    "gemm_epilogue_bruteforce": (check_gemm_epilogue_bruteforce, 1e-13),
     "reparam_identity": (check_reparam_identity, 1e-13),
     "rmsnorm_library": (check_rmsnorm_library, 1e-13),
     "rmsnorm_scale_invariance": (check_rmsnorm_scale_invariance, 1e-13),

@@ -1,0 +1,168 @@
+"""GPU parity of the named operators (the hot-path rows) against the fp64
+oracle on seeded synthetic inputs: full size where the oracle finishes in
+seconds, scaled-down shapes with ragged tails otherwise."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import coda_oracle as O
+from parity import assert_bf16, assert_f32, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def coda():
+    import gemm_epilogue_transformer_bf16_gb300 as c
+    from gemm_epilogue_transformer_bf16_gb300 import _build
+    _build.build()
+    c.load()
+    return c
+
+
+def dev(d):
+    return {k: v.to(DEV) for k, v in d.items()}
+
+
+def f64(d):
+    return {k: to_np(v) for k, v in d.items()}
+
+
+# ---------------------------------------------------------------- workload 1
+@pytest.mark.parametrize("shape", [synth.SwigluShape(), synth.SwigluShape(200, 136, 264)])
+def test_linear_swiglu(coda, shape):
+    t = synth.make_swiglu(shape, seed=0)
+    d, o = dev(t), f64(t)
+    H, g, u = coda.linear_swiglu(d["X"], d["Wg"], d["Wu"])
+    Hr, gr, ur = O.swiglu_fwd(o["X"], o["Wg"], o["Wu"])
+    assert_bf16(H, Hr, "H")
+    assert_bf16(g, gr, "g")
+    assert_bf16(u, ur, "u")
+
+
+# ---------------------------------------------------------------- workload 2
+@pytest.mark.parametrize("shape", [synth.RmsLinearShape(), synth.RmsLinearShape(300, 264, 200)])
+def test_rmsnorm_linear_fwd_bwd(coda, shape):
+    t = synth.make_rms_linear(shape, seed=0)
+    d, o = dev(t), f64(t)
+    Wf = coda.fold_gamma(d["W"], d["gamma"])
+    Y, rstd = coda.rmsnorm_linear(d["X"], Wf, R=d["R"], eps=shape.eps)
+    yr, rr = O.rmsnorm_linear_fwd(o["X"], o["gamma"], o["W"], shape.eps, o["R"])
+    assert_bf16(Y, yr, "Y")
+    assert_f32(rstd, rr, "rstd")
+    g = coda.rmsnorm_linear_bwd(d["G"], d["X"], d["W"], Wf, d["gamma"], rstd, Y, d["R"])
+    b = O.rmsnorm_linear_bwd(o["X"], o["gamma"], o["W"], shape.eps, o["G"])
+    assert_bf16(g["dX"], b["dX"], "dX")
+    assert_bf16(g["dW"], b["dW"], "dW")
+    assert_bf16(g["dgamma"], b["dgamma"], "dgamma")
+
+
+def test_fold_gamma_and_rstd(coda):
+    t = synth.make_rms_linear(synth.RmsLinearShape(64, 128, 72), seed=3)
+    d, o = dev(t), f64(t)
+    Wf = coda.fold_gamma(d["W"], d["gamma"])
+    assert_bf16(Wf, o["W"] * o["gamma"][None, :], "Wf")
+    r = coda.rms_rstd(d["X"], 1e-6)
+    assert_f32(r, O.rms_inv(o["X"], 1e-6), "rstd")
+
+
+# ---------------------------------------------------------------- residual + partial RMS
+@pytest.mark.parametrize("M,N,K", [(256, 512, 384), (300, 776, 136)])
+def test_linear_residual_partial_rms(coda, M, N, K):
+    X = synth.randn_bf16((M, K), 1.0, 1)
+    W = synth.randn_bf16((N, K), 1 / math.sqrt(K), 2)
+    R = synth.randn_bf16((M, N), 1.0, 3)
+    Y, r = coda.linear_residual(X.to(DEV), W.to(DEV), R.to(DEV), eps=1e-6, want_rstd=True)
+    ur, rr = O.linear_residual_fwd(to_np(X), to_np(W), to_np(R), 1e-6)
+    assert_bf16(Y, ur, "u")
+    assert_f32(r, rr, "rstd from partials")
+    G = synth.randn_bf16((M, N), 1.0, 4)
+    g = coda.linear_residual_bwd(G.to(DEV), X.to(DEV), W.to(DEV))
+    b = O.linear_residual_bwd(to_np(X), to_np(W), to_np(G))
+    assert_bf16(g["dX"], b["dX"], "dX")
+    assert_bf16(g["dW"], b["dW"], "dW")
+
+
+# ---------------------------------------------------------------- workload 3 (scaled)
+@pytest.mark.parametrize("shape", [synth.MlpShape(512, 512, 1408), synth.MlpShape(200, 264, 392)])
+def test_swiglu_mlp_fwd_bwd(coda, shape):
+    t = synth.make_mlp(shape, seed=0)
+    d, o = dev(t), f64(t)
+    H, g, u = coda.linear_swiglu(d["X"], d["Wg"], d["Wu"])
+    Y = coda.linear_residual(H, d["Wd"], d["R"])
+    f = O.mlp_fwd(o["X"], o["Wg"], o["Wu"], o["Wd"], o["R"])
+    assert_bf16(H, f["H"], "H")
+    assert_bf16(Y, f["y"], "y")
+    gr = coda.linear_swiglu_bwd(d["dY"], d["X"], d["Wg"], d["Wu"], d["Wd"], g, u, H)
+    b = O.mlp_bwd(o["X"], o["Wg"], o["Wu"], o["Wd"], o["dY"])
+    for k in ("dX", "dWg", "dWu", "dWd"):
+        assert_bf16(gr[k], b[k], k)
+
+
+# ---------------------------------------------------------------- workload 4 (scaled)
+@pytest.mark.parametrize("shape", [synth.CeShape(512, 256, 4000), synth.CeShape(300, 136, 8192)])
+def test_linear_cross_entropy(coda, shape):
+    t = synth.make_ce(shape, seed=0)
+    lab = t["labels"].clone()
+    lab[1] = 0
+    lab[2] = shape.vocab - 1
+    t["labels"] = lab
+    d, o = dev(t), f64(t)
+    labels_np = t["labels"].numpy()
+    out = coda.linear_cross_entropy(d["X"], d["W"], d["labels"])
+    f = O.linear_cross_entropy_fwd(o["X"], o["W"], labels_np)
+    assert coda.get_status(out["ws"]) == 0
+    assert int(out["n_valid"].item()) == f["n_valid"]
+    assert_f32(out["lse"], f["lse"], "lse")
+    assert_f32(out["loss"], [f["loss"]], "loss")
+    g = coda.linear_cross_entropy_bwd(d["X"], d["W"], d["labels"], out["lse"], out["n_valid"], 1.0)
+    b = O.linear_cross_entropy_bwd(o["X"], o["W"], labels_np)
+    assert_bf16(g["dX"], b["dX"], "dX")
+    assert_bf16(g["dW"], b["dW"], "dW")
+
+
+def test_cross_entropy_all_ignored_and_bad_label(coda):
+    s = synth.CeShape(64, 128, 1024)
+    t = synth.make_ce(s, seed=5)
+    d = dev(t)
+    lab = torch.full((s.tokens,), -100, dtype=torch.int32, device=DEV)
+    out = coda.linear_cross_entropy(d["X"], d["W"], lab)
+    assert math.isnan(out["loss"].item()) and int(out["n_valid"].item()) == 0
+    g = coda.linear_cross_entropy_bwd(d["X"], d["W"], lab, out["lse"], out["n_valid"], 1.0)
+    assert not torch.any(g["dX"].float() != 0) and not torch.any(g["dW"].float() != 0)
+    assert coda.get_status(out["ws"]) == 0
+    lab2 = d["labels"].clone()
+    lab2[3] = s.vocab + 5
+    out2 = coda.linear_cross_entropy(d["X"], d["W"], lab2)
+    assert coda.get_status(out2["ws"]) == 7   # CODA_ERR_LABEL_RANGE
+    valid = (lab2 != -100) & (lab2 >= 0) & (lab2 < s.vocab)
+    assert int(out2["n_valid"].item()) == int(valid.sum().item())
+
+
+# ---------------------------------------------------------------- workload 5 (scaled)
+SMALL_BLOCK = synth.BlockShape(tokens=256, hidden=512, n_q=4, n_kv=2, head_dim=128, inter=1024, seq_len=128)
+RAGGED_BLOCK = synth.BlockShape(tokens=200, hidden=264, n_q=2, n_kv=1, head_dim=128, inter=392, seq_len=64)
+
+
+@pytest.mark.parametrize("shape", [SMALL_BLOCK, RAGGED_BLOCK])
+def test_block_fwd_bwd(coda, shape):
+    from gemm_epilogue_transformer_bf16_gb300.block import Block
+    t = synth.make_block(shape, seed=0)
+    d, o = dev(t), f64(t)
+    blk = Block(shape, d)
+    f = blk.forward(d["x0"], d["A"], d["pos"])
+    g = blk.backward(d["x0"], d["A"], d["pos"], d["dx2"], d["dQ"], d["dK"], d["dV"])
+    torch.cuda.synchronize()
+    assert coda.get_status(blk.ws) == 0
+    cfg = dict(n_q=shape.n_q, n_kv=shape.n_kv, head_dim=shape.head_dim, theta=shape.theta, eps=shape.eps)
+    rf = O.block_fwd(o, **cfg)
+    for k in ("Q", "K", "V", "x1", "x2"):
+        assert_bf16(f[k], rf[k], k)
+    rb = O.block_bwd(o, **cfg)
+    for k in ("dx0", "dA", "dx1", "dWqkv", "dWo", "dWg", "dWu", "dWd", "dgamma_attn", "dgamma_mlp",
+              "dgamma_q", "dgamma_k"):
+        assert_bf16(g[k], rb[k], k)

@@ -129,7 +129,17 @@ def _mut_mlp_bwd_transposed(m):
     m.mlp_bwd = bad
 
 
+def _mut_gemm_transposed_scale(m):
+    orig = m.gemm_epilogue_plain
+
+    def bad(A, B, row_scale=None, col_scale=None, aux0=None, row_coef=None, aux1=None, D_old=None):
+        return orig(A, B, row_scale, col_scale, aux0, None if row_coef is None else -np.asarray(row_coef),
+                    aux1, D_old)
+    m.gemm_epilogue_plain = bad
+
+
 MUTANTS = {
+    "gemm_coef_sign": _mut_gemm_transposed_scale,
     "rms_eps_outside_root": _mut_rms_eps_outside,
     "rmsnorm_bwd_drop_mean": _mut_rmsnorm_bwd_drop_mean,
     "rmsnorm_gamma_before_norm": _mut_rmsnorm_gamma_before,
