@@ -1,11 +1,19 @@
 """Tolerances of the GPU-vs-oracle comparisons.
 
-  bf16 tensors          max |err| <= 3e-2 * RMS(ref)  and  ||err||_F / ||ref||_F <= 1e-2
+  bf16 tensors          |err_i| <= 3e-2 * RMS(ref) + 2^-8 |ref_i|  for every element,
+                        and ||err||_F / ||ref||_F <= 1e-2
   fp32 reductions       relative error <= 1e-3   (rstd, lse, loss: computed from exact inputs)
   integers              bit-exact
 
 Gain gradients (dgamma) are reductions over bf16-rounded intermediates, so
 they are held to the bf16 rule.
+
+Reading of the max-error bound: a bf16 output cannot be closer to the exact
+value than its own storage rounding, half an ulp, i.e. up to 2^-8 |ref_i|.
+For heavy-tailed outputs (SwiGLU's H has max/RMS ~ 17) that alone exceeds
+3e-2 * RMS, so the literal bound would reject the correctly rounded exact
+result.  The per-element half-ulp term restores feasibility; the Frobenius
+bound is unchanged.
 """
 from __future__ import annotations
 
@@ -14,6 +22,7 @@ import torch
 
 BF16_MAX_REL_RMS = 3e-2
 BF16_FROB = 1e-2
+BF16_HALF_ULP = 2.0 ** -8
 F32_REL = 1e-3
 
 
@@ -24,12 +33,16 @@ def to_np(t):
 
 
 def bf16_metrics(got, ref):
+    """(max_i |err_i| / (3e-2 RMS + 2^-8 |ref_i|) * 3e-2, relative Frobenius).
+    The first value is compared with 3e-2: it equals max|err|/RMS when the
+    half-ulp allowance is zero."""
     g, r = to_np(got), to_np(ref)
     assert g.shape == r.shape, f"shape {g.shape} != {r.shape}"
     err = g - r
-    rms = float(np.sqrt(np.mean(r * r)))
+    rms = max(float(np.sqrt(np.mean(r * r))), 1e-300)
     fro = float(np.linalg.norm(err) / max(np.linalg.norm(r), 1e-300))
-    return float(np.max(np.abs(err))) / max(rms, 1e-300), fro
+    bound = BF16_MAX_REL_RMS * rms + BF16_HALF_ULP * np.abs(r)
+    return float(np.max(np.abs(err) / bound)) * BF16_MAX_REL_RMS, fro
 
 
 def assert_bf16(got, ref, name):
@@ -37,7 +50,8 @@ def assert_bf16(got, ref, name):
     assert np.all(np.isfinite(g)), f"{name}: non-finite values"
     mx, fro = bf16_metrics(got, ref)
     assert mx <= BF16_MAX_REL_RMS and fro <= BF16_FROB, \
-        f"{name}: max|err|/RMS = {mx:.3e} (<= {BF16_MAX_REL_RMS}), rel Frobenius = {fro:.3e} (<= {BF16_FROB})"
+        f"{name}: max|err|/(RMS + half-ulp) = {mx:.3e} (<= {BF16_MAX_REL_RMS}), " \
+        f"rel Frobenius = {fro:.3e} (<= {BF16_FROB})"
     return mx, fro
 
 
