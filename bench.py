@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused GEMM-epilogue transformer block (fwd + bwd).
+
+Workload (one step): the non-attention block at 70B-ish width -- tokens 8192
+(4 sequences of 2048), hidden 8192, 64 query / 8 KV heads of 128, SwiGLU
+intermediate 28672, bf16 weights ~N(0, 1/fan_in) -- forward and backward
+through libcoda.so: gamma folds, row RMS, QKV GEMM with QK-RMSNorm + RoPE
+epilogue, O-proj GEMM with residual + partial-RMS epilogue, gate/up GEMM with
+row-scale + SwiGLU epilogue, down-proj GEMM with residual epilogue, and the
+backward GEMMs with dSwiGLU, RMSNorm-backward and weight-gradient epilogues.
+The attention core is out of scope; its output and input gradients are seeded
+inputs.
+
+Prints one JSON line.  value = algorithmic TFLOP/s of the whole step (sum of
+2*M*N*K over its GEMMs, 42.06 TFLOP per step) with every input resident in
+HBM; e2e = the same with the step's activations copied host->device and the
+block output and input gradient copied back inside the timed region.
+
+--impl reference times the fp64 CPU oracle on a bounded token sample of the
+same workload instead (the reference arm: there is no runnable upstream).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM-epilogue TFLOP/s & % bf16 peak; block fwd+bwd ms vs unfused"
+WORKLOAD = ("non-attention transformer block fwd+bwd: tokens 8192 (4x2048), hidden 8192, 64 q / 8 kv heads x 128, "
+            "SwiGLU intermediate 28672; QKV+QK-RMSNorm+RoPE, O-proj+residual+partial RMS, gate/up+SwiGLU, "
+            "down+residual epilogues and their backward")
+DOMINANT = "gateup"   # the step's largest single GEMM-epilogue launch (row-scale + SwiGLU epilogue)
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gateup_swiglu_gemm_block8192.md")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="coda", choices=["coda", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-unfused", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-tokens", type=int, default=64, help="token sample of the CPU oracle timing")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(world):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("gloo")
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(x, world):
+    """Max of a host float over ranks (gloo; no data-path collective)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join("/tmp", f"coda_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- peaks / profile
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return d["bf16_tflops"], d["bf16_tflops_sustained"], d["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gemm_epilogue_transformer_bf16_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None if the kernel sources changed since it was taken."""
+    try:
+        txt = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    d = re.search(r"source_digest:\s*([0-9a-f]+)", txt)
+    if not m or not d or d.group(1) != source_digest():
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------------------- unfused comparison
+def unfused_step_fn(w, t, s):
+    """The same block fwd+bwd as eager torch.matmul (cuBLAS) plus unfused
+    element-wise ops, differentiated by autograd.  Comparison only."""
+    import torch
+    import torch.nn.functional as F
+
+    params = {k: w[k].detach().clone().requires_grad_(True)
+              for k in ("Wqkv", "Wo", "Wg", "Wu", "Wd", "gamma_attn", "gamma_mlp", "gamma_q", "gamma_k")}
+    T, d = s.tokens, s.head_dim
+    ang = t["pos"].double()[:, None] * (s.theta ** (-2.0 * torch.arange(d // 2, device=t["pos"].device,
+                                                                         dtype=torch.float64) / d))[None, :]
+    cos, sin = ang.cos().float(), ang.sin().float()
+
+    def rope(v):
+        a, b = v[..., 0::2], v[..., 1::2]
+        c, sn = cos[:, None, :], sin[:, None, :]
+        return torch.stack((a * c - b * sn, a * sn + b * c), dim=-1).flatten(-2)
+
+    def rms(x, g):
+        xf = x.float()
+        return (xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + s.eps) * g).to(torch.bfloat16)
+
+    def step():
+        p = params
+        x0 = t["x0"].detach().requires_grad_(True)
+        A = t["A"].detach().requires_grad_(True)
+        a0 = rms(x0, p["gamma_attn"])
+        qkv = a0 @ p["Wqkv"].t()
+        q = qkv[:, : s.n_q * d].view(T, s.n_q, d)
+        k = qkv[:, s.n_q * d: (s.n_q + s.n_kv) * d].view(T, s.n_kv, d)
+        v = qkv[:, (s.n_q + s.n_kv) * d:]
+        Q = rope(rms(q, p["gamma_q"]).float()).to(torch.bfloat16)
+        K = rope(rms(k, p["gamma_k"]).float()).to(torch.bfloat16)
+        x1 = x0 + A @ p["Wo"].t()
+        a1 = rms(x1, p["gamma_mlp"])
+        H = F.silu(a1 @ p["Wg"].t()) * (a1 @ p["Wu"].t())
+        x2 = x1 + H @ p["Wd"].t()
+        torch.autograd.backward([x2, Q, K, v], [t["dx2"], t["dQ"].view(T, s.n_q, d), t["dK"].view(T, s.n_kv, d),
+                                                t["dV"]])
+        for q_ in params.values():
+            q_.grad = None
+    return step
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_inputs(host, tokens):
+    """fp64 copies of the workload's weights and of its first `tokens` tokens."""
+    import numpy as np
+    sl = slice(0, tokens)
+    p = {}
+    for k, v in host.items():
+        if k in ("x0", "A", "dx2", "dQ", "dK", "dV", "pos"):
+            p[k] = v[sl].double().numpy() if k != "pos" else v[sl].numpy().astype(np.int64)
+        else:
+            p[k] = v.double().numpy()
+    return p
+
+
+def oracle_sample_timing(tokens, p):
+    """Time the fp64 oracle (as it stands) on the sample prepared by
+    oracle_inputs: block_fwd + block_bwd.  Returns (TFLOP/s, seconds, flops)."""
+    from oracle import coda_oracle as O
+    import synth
+    s = synth.FULL["c5"]
+    cfg = dict(n_q=s.n_q, n_kv=s.n_kv, head_dim=s.head_dim, theta=s.theta, eps=s.eps)
+    t0 = time.perf_counter()
+    O.block_fwd(p, **cfg)
+    O.block_bwd(p, **cfg)
+    dt = time.perf_counter() - t0
+    flops = O.block_flops(tokens, s.hidden, s.qkv_out, s.n_q * s.head_dim, s.inter)
+    return flops / dt / 1e12, dt, flops
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    import synth
+    s = synth.FULL["c5"]
+    host = synth.make_block(s, seed=0)
+    torch.set_num_threads(cores())
+    p = oracle_inputs(host, args.cpu_tokens)
+    vals, secs = [], []
+    for i in range(args.warmup + args.steps):
+        v, dt, flops = oracle_sample_timing(args.cpu_tokens, p)
+        if i >= args.warmup:
+            vals.append(v)
+            secs.append(dt)
+    val = statistics.median(vals)
+    sample = f"block fwd+bwd on the first {args.cpu_tokens} of 8192 tokens (full weights), fp64 NumPy"
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(secs) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens": s.tokens, "hidden": s.hidden, "inter": s.inter,
+                       "oracle_tokens_per_step": args.cpu_tokens},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- main arm
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import numpy as np
+    import torch
+    import synth
+    import gemm_epilogue_transformer_bf16_gb300 as coda
+    from gemm_epilogue_transformer_bf16_gb300.block import Block
+
+    rank, world, local = dist_env()
+    dist_init(world)
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    coda.load()
+    s = synth.FULL["c5"]
+    host = synth.make_block(s, seed=rank)          # replicas: each rank its own seeded batch
+    t = {k: v.to(dev) for k, v in host.items()}
+    blk = Block(s, t, device=dev)
+    flops_step = sum(blk.gemm_flops().values())
+    launches_step = sum(Block.LAUNCHES.values())
+    stream = torch.cuda.current_stream(dev)
+    args_step = (t["x0"], t["A"], t["pos"], t["dx2"], t["dQ"], t["dK"], t["dV"])
+
+    # ---------------------------------------------------------------- device-resident timing
+    names = list(Block.LAUNCHES)
+    for _ in range(args.warmup):
+        blk.step(*args_step)
+    torch.cuda.synchronize(dev)
+    st = coda.get_status(blk.ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {coda.status_string(st)}")
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
+    gpu_id = None
+    try:
+        gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        ev = marks[i]
+        ev[0].record(stream)
+        j = [1]
+
+        def mark(name, ev=ev, j=j):
+            ev[j[0]].record(stream)
+            j[0] += 1
+        blk.step(*args_step, mark=mark)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    dist_barrier(world)
+    ms_total = start.elapsed_time(stop)
+    ms_total = dist_max(ms_total, world)
+    ms_step = ms_total / args.steps
+    value = world * flops_step * args.steps / (ms_total / 1e3) / 1e12
+    stage_ms = {n: statistics.median(marks[i][k].elapsed_time(marks[i][k + 1]) for i in range(args.steps))
+                for k, n in enumerate(names)}
+    gf = blk.gemm_flops()
+    burst, sustained, hbm, peak_src = measured_peaks()
+    stages = {n: {"ms": round(stage_ms[n], 4), "launches": Block.LAUNCHES[n],
+                  "tflops": round(gf[n] / (stage_ms[n] / 1e3) / 1e12, 1) if gf[n] else None} for n in names}
+    ach = gf[DOMINANT] / (stage_ms[DOMINANT] / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": sustained, "unit": "TFLOP/s",
+                "frac": round(ach / sustained, 4), "traffic": profiled_traffic(),
+                "kernel": "coda_gemm_kernel<256, EpiSwiglu> (gate/up GEMM, 8192x57344x8192)",
+                "peak_kind": f"bf16 sustained ({peak_src})"}
+    torch.cuda.synchronize(dev)
+    if coda.get_status(blk.ws) != 0:
+        raise RuntimeError("device status error in timed region")
+
+    # ---------------------------------------------------------------- end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        in_keys = ("x0", "A", "pos", "dx2", "dQ", "dK", "dV")
+        hin = {k: host[k].pin_memory() for k in in_keys}
+        hx2 = torch.empty_like(host["x0"]).pin_memory()
+        hdx0 = torch.empty_like(host["x0"]).pin_memory()
+        dbuf = {k: torch.empty_like(t[k]) for k in in_keys}
+        h2d = sum(v.numel() * v.element_size() for v in hin.values())
+        d2h = hx2.numel() * hx2.element_size() + hdx0.numel() * hdx0.element_size()
+
+        def e2e_step():
+            for k in in_keys:
+                dbuf[k].copy_(hin[k], non_blocking=True)
+            f = blk.forward(dbuf["x0"], dbuf["A"], dbuf["pos"])
+            g = blk.backward(dbuf["x0"], dbuf["A"], dbuf["pos"], dbuf["dx2"], dbuf["dQ"], dbuf["dK"], dbuf["dV"])
+            hx2.copy_(f["x2"], non_blocking=True)
+            hdx0.copy_(g["dx0"], non_blocking=True)
+        for _ in range(max(1, args.warmup // 2)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        dist_barrier(world)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_e2e = dist_max(a.elapsed_time(b), world)
+        e2e = {"value": round(world * flops_step * args.steps / (ms_e2e / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e / args.steps, 3)}
+
+    # ---------------------------------------------------------------- unfused torch comparison
+    unfused_ms = None
+    if not args.no_unfused:
+        del blk
+        torch.cuda.empty_cache()
+        step = unfused_step_fn(t, t, s)
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        n_unf = max(3, args.steps // 3)
+        a.record(stream)
+        for _ in range(n_unf):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        unfused_ms = dist_max(a.elapsed_time(b) / n_unf, world)
+
+    # ---------------------------------------------------------------- CPU oracle baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        torch.set_num_threads(cores())
+        v, dt, fl = oracle_sample_timing(args.cpu_tokens, oracle_inputs(host, args.cpu_tokens))
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
+               "sample": f"fp64 NumPy block_fwd+block_bwd on the first {args.cpu_tokens} of 8192 tokens "
+                         f"(full weights): {fl / 1e12:.3f} TFLOP in {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens": s.tokens, "hidden": s.hidden, "n_q": s.n_q,
+                       "n_kv": s.n_kv, "head_dim": s.head_dim, "inter": s.inter, "tflop_per_step":
+                       round(flops_step / 1e12, 3), "l2": "inputs (1.7 GB of weights + activations) exceed the "
+                       "129 MB L2; no flush", "parallelism": f"replicas x{world}"},
+            "pct_bf16_peak": {"burst": round(value / world / burst, 4), "sustained": round(value / world / sustained, 4),
+                              "source": peak_src},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_step * args.steps,
+            "clocks": clk,
+            "unfused_ms_per_step": round(unfused_ms, 3) if unfused_ms else None,
+            "speedup_vs_unfused": round(unfused_ms / ms_step, 3) if unfused_ms else None,
+            "stages": stages,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -71,40 +71,64 @@ class Block:
         )
         self.ws = workspace(need, device)
 
+    # Kernels each stage launches (library calls are fixed sequences).
+    LAUNCHES = {"fold": 3, "rstd0": 1, "qkv": 1, "oproj": 2, "gateup": 1, "down": 1,
+                "mlp_bwd": 7, "oproj_bwd": 2, "qkv_bwd": 7}
+
+    def gemm_flops(self):
+        """Algorithmic GEMM FLOPs (2*M*N*K) of each stage of one step."""
+        s = self.s
+        T, Hd, I, a = s.tokens, s.hidden, s.inter, s.n_q * s.head_dim
+        q = s.qkv_out
+        return {"fold": 0, "rstd0": 0, "qkv": 2 * T * Hd * q, "oproj": 2 * T * a * Hd, "gateup": 4 * T * Hd * I,
+                "down": 2 * T * I * Hd, "mlp_bwd": 2 * (2 * T * Hd * I) + 2 * (4 * T * Hd * I),
+                "oproj_bwd": 4 * T * a * Hd, "qkv_bwd": 4 * T * Hd * q}
+
     # ------------------------------------------------------------------ forward
-    def forward(self, x0, A, pos):
+    def forward(self, x0, A, pos, mark=None):
         s, w = self.s, self.w
+        mark = mark or (lambda name: None)
         fold_gamma(w["Wqkv"], w["gamma_attn"], out=self.Wqkv_f)
         fold_gamma(w["Wg"], w["gamma_mlp"], out=self.Wg_f)
         fold_gamma(w["Wu"], w["gamma_mlp"], out=self.Wu_f)
+        mark("fold")
         rms_rstd(x0, s.eps, out=self.rstd0)
+        mark("rstd0")
         linear_qknorm_rope(x0, self.Wqkv_f, w["gamma_q"], w["gamma_k"], pos, self.cos_sin, s.n_q, s.n_kv,
                            rstd=self.rstd0, eps=s.eps, head_dim=s.head_dim, out=self.fwd, ws=self.ws)
+        mark("qkv")
         linear_residual(A, w["Wo"], x0, eps=s.eps, Y=self.x1, rstd_out=self.rstd1, ws=self.ws)
+        mark("oproj")
         linear_swiglu(self.x1, self.Wg_f, self.Wu_f, rstd=self.rstd1, H=self.H, g=self.g, u=self.u, ws=self.ws)
+        mark("gateup")
         linear_residual(self.H, w["Wd"], self.x1, Y=self.x2, ws=self.ws)
+        mark("down")
         return {"Q": self.fwd["Q"], "K": self.fwd["K"], "V": self.fwd["V"], "x1": self.x1, "x2": self.x2}
 
     # ------------------------------------------------------------------ backward
-    def backward(self, x0, A, pos, dx2, dQ, dK, dV):
+    def backward(self, x0, A, pos, dx2, dQ, dK, dV, mark=None):
         s, w = self.s, self.w
+        mark = mark or (lambda name: None)
         linear_swiglu_bwd(dx2, self.x1, w["Wg"], w["Wu"], w["Wd"], self.g, self.u, self.H, rstd=self.rstd1,
                           gamma=w["gamma_mlp"], Wgf=self.Wg_f, Wuf=self.Wu_f, dX_resid=dx2, ws=self.ws,
                           out=self.grads_mlp)
+        mark("mlp_bwd")
         linear_residual_bwd(self.dx1, A, w["Wo"], ws=self.ws, out=self.grads_o)
+        mark("oproj_bwd")
         linear_qknorm_rope_bwd(dQ, dK, dV, self.fwd["qk_save"], self.fwd["V"], w["gamma_q"], w["gamma_k"], pos,
                                self.cos_sin, s.n_q, s.n_kv, x0, w["Wqkv"], Wf_qkv=self.Wqkv_f, rstd=self.rstd0,
                                gamma_in=w["gamma_attn"], dX_resid=self.dx1, eps=s.eps, head_dim=s.head_dim,
                                ws=self.ws, out=self.grads_qkv)
+        mark("qkv_bwd")
         return {"dx0": self.grads_qkv["dX"], "dA": self.grads_o["dX"], "dx1": self.dx1,
                 "dWqkv": self.grads_qkv["dW"], "dWo": self.grads_o["dW"], "dWg": self.grads_mlp["dWg"],
                 "dWu": self.grads_mlp["dWu"], "dWd": self.grads_mlp["dWd"],
                 "dgamma_attn": self.grads_qkv["dgamma_in"], "dgamma_mlp": self.grads_mlp["dgamma"],
                 "dgamma_q": self.grads_qkv["dgamma_q"], "dgamma_k": self.grads_qkv["dgamma_k"]}
 
-    def step(self, x0, A, pos, dx2, dQ, dK, dV):
-        self.forward(x0, A, pos)
-        return self.backward(x0, A, pos, dx2, dQ, dK, dV)
+    def step(self, x0, A, pos, dx2, dQ, dK, dV, mark=None):
+        self.forward(x0, A, pos, mark)
+        return self.backward(x0, A, pos, dx2, dQ, dK, dV, mark)
 
 
 class LinearCE:

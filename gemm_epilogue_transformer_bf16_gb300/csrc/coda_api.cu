@@ -275,7 +275,13 @@ int coda_gemm_epilogue(const coda_epilogue_desc* d, const coda_bf16* A, int64_t 
   }
   for (int i = 0; i < 3; ++i) {
     CK(al(d->aux_out[i]));
-    if (d->aux_out[i]) CK(ldok(d->ld_aux_out[i], N));
+    if (!d->aux_out[i]) continue;
+    if (d->map == CODA_MAP_QKNORM_ROPE && i == 0) {
+      // the pre-norm save holds only the q and k heads
+      CK(ldok(d->ld_aux_out[0], static_cast<int64_t>(d->n_q_heads + d->n_kv_heads) * 128));
+    } else {
+      CK(ldok(d->ld_aux_out[i], N));
+    }
   }
   CK(al(d->row_scale));
   CK(al(d->col_scale));
@@ -388,6 +394,7 @@ int coda_gemm_epilogue(const coda_epilogue_desc* d, const coda_bf16* A, int64_t 
       e.lse = d->lse;
       e.n_valid = d->n_valid;
       e.dloss = d->dloss;
+      e.onehot = 1;
       break;
     case CODA_MAP_COLDOT:
       p.kind = coda::EpiKind::ColDot;
@@ -1017,7 +1024,13 @@ int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int3
 
 size_t coda_linear_cross_entropy_bwd_workspace_size(int64_t M, int64_t V, int64_t) {
   SizeCursor c;
-  c.take<__nv_bfloat16>(static_cast<size_t>(M) * V);  // dZ
+  c.take<__nv_bfloat16>(static_cast<size_t>(M) * V);  // dZ (softmax part)
+  c.take<float>(M);                                    // w_i
+  c.take<int32_t>(M);                                  // label of valid rows
+  c.take<int32_t>(V);                                  // counts per vocabulary row
+  c.take<int32_t>(V);                                  // scatter cursors
+  c.take<int32_t>(V + 1);                              // CSR offsets
+  c.take<int32_t>(M);                                  // CSR token indices
   return c.off;
 }
 
@@ -1038,9 +1051,17 @@ int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const 
   }
   WsCursor w(ws);
   __nv_bfloat16* dZ = w.take<__nv_bfloat16>(static_cast<size_t>(M) * V);
+  float* wrow = w.take<float>(M);
+  int32_t* lrow = w.take<int32_t>(M);
+  int32_t* counts = w.take<int32_t>(V);
+  int32_t* cursor = w.take<int32_t>(V);
+  int32_t* off = w.take<int32_t>(V + 1);
+  int32_t* idx = w.take<int32_t>(M);
   int* status = static_cast<int*>(ws);
   cudaStream_t s = S(stream);
-  {  // dZ = (softmax - onehot) * dloss / n_valid
+  CU(coda::launch_ce_onehot_prep(labels, ignore_index, M, V, n_valid, dloss, wrow, lrow, counts, cursor, off, idx,
+                                 s));
+  {  // dZ = softmax * dloss / n_valid (the one-hot part is applied exactly below)
     Plan p;
     p.kind = coda::EpiKind::CeDlogits;
     p.A = X;
@@ -1059,7 +1080,7 @@ int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const 
     p.e.dloss = dloss;
     CK(run(p, status, s));
   }
-  {  // dX = dZ W
+  {  // dX = dZ W - w_i W[y_i]
     Plan p;
     p.A = dZ;
     p.lda = V;
@@ -1071,9 +1092,13 @@ int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const 
     p.K = V;
     p.e.D = dX;
     p.e.ldd = K;
+    p.e.row_coef = wrow;
+    p.e.aux1 = BF(W);
+    p.e.ld_aux1 = K;
+    p.e.gather_rows = lrow;
     CK(run(p, status, s));
   }
-  {  // dW = dZ^T X
+  {  // dW = dZ^T X - sum over tokens labelled v of w_i X[i]
     Plan p;
     p.A = dZ;
     p.lda = V;
@@ -1086,6 +1111,11 @@ int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const 
     p.K = M;
     p.e.D = dW;
     p.e.ldd = K;
+    p.e.aux2 = BF(X);
+    p.e.ld_aux2 = K;
+    p.e.csr_off = off;
+    p.e.csr_idx = idx;
+    p.e.csr_w = wrow;
     CK(run(p, status, s));
   }
   return CODA_OK;

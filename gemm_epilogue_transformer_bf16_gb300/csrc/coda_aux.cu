@@ -234,6 +234,93 @@ cudaError_t launch_ce_combine(const float2* part, int64_t ld, int nchunks, const
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- CE backward one-hot terms
+// Per row: w_i = dloss / n_valid and its label for a valid row (else 0, -1);
+// and, for the dW GEMM, the tokens of every vocabulary row (counting sort by
+// label: histogram, exclusive scan, scatter, then each bucket sorted by token
+// index so that the epilogue's fp32 sums have a fixed order).
+__global__ void ce_prep_kernel(const int32_t* __restrict__ labels, int32_t ignore, int64_t M, int64_t V,
+                               const int32_t* __restrict__ n_valid, float dloss, float* wrow, int32_t* lrow,
+                               int32_t* counts) {
+  const int32_t nv = *n_valid;
+  const float w = nv > 0 ? dloss / static_cast<float>(nv) : 0.f;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int32_t y = labels[i];
+    const bool valid = y != ignore && y >= 0 && y < V && nv > 0;
+    wrow[i] = valid ? w : 0.f;
+    lrow[i] = valid ? y : -1;
+    if (valid) atomicAdd(&counts[y], 1);
+  }
+}
+
+// Exclusive scan of counts[0..V) into off[0..V] with one 1024-thread block.
+__global__ void __launch_bounds__(1024) scan_counts_kernel(const int32_t* __restrict__ counts, int64_t V,
+                                                           int32_t* off) {
+  __shared__ int32_t part[1024];
+  const int64_t per = (V + 1023) / 1024;
+  const int64_t b = threadIdx.x * per, e = (b + per < V) ? b + per : V;
+  int32_t s = 0;
+  for (int64_t i = b; i < e; ++i) s += counts[i];
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {  // Hillis-Steele inclusive scan of the 1024 partials
+    const int32_t v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0;
+  for (int64_t i = b; i < e; ++i) {
+    off[i] = run;
+    run += counts[i];
+  }
+  if (threadIdx.x == 1023) off[V] = part[1023];
+}
+
+__global__ void ce_fill_kernel(const int32_t* __restrict__ lrow, int64_t M, const int32_t* __restrict__ off,
+                               int32_t* cursor, int32_t* idx) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int32_t y = lrow[i];
+    if (y >= 0) idx[off[y] + atomicAdd(&cursor[y], 1)] = static_cast<int32_t>(i);
+  }
+}
+
+__global__ void ce_sort_buckets_kernel(const int32_t* __restrict__ off, int64_t V, int32_t* idx) {
+  for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < V;
+       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int32_t b = off[v], e = off[v + 1];
+    for (int32_t i = b + 1; i < e; ++i) {  // insertion sort; buckets hold a few tokens
+      const int32_t key = idx[i];
+      int32_t j = i - 1;
+      while (j >= b && idx[j] > key) {
+        idx[j + 1] = idx[j];
+        --j;
+      }
+      idx[j + 1] = key;
+    }
+  }
+}
+
+cudaError_t launch_ce_onehot_prep(const int32_t* labels, int32_t ignore, int64_t M, int64_t V,
+                                  const int32_t* n_valid, float dloss, float* wrow, int32_t* lrow,
+                                  int32_t* counts, int32_t* cursor, int32_t* off, int32_t* idx, cudaStream_t s) {
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * V, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(cursor, 0, sizeof(int32_t) * V, s)) != cudaSuccess) return e;
+  const unsigned mb = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((M + 255) / 256, 1024)));
+  ce_prep_kernel<<<mb, 256, 0, s>>>(labels, ignore, M, V, n_valid, dloss, wrow, lrow, counts);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  scan_counts_kernel<<<1, 1024, 0, s>>>(counts, V, off);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  ce_fill_kernel<<<mb, 256, 0, s>>>(lrow, M, off, cursor, idx);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const unsigned vb = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((V + 255) / 256, 1024)));
+  ce_sort_buckets_kernel<<<vb, 256, 0, s>>>(off, V, idx);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- RoPE table
 __global__ void rope_table_kernel(double theta, int head_dim, int max_pos, float2* cs) {
   const int half = head_dim / 2;

@@ -30,11 +30,13 @@ __device__ __forceinline__ void store_f32x8(float* p, const float* v) {
 }
 
 // ---------------------------------------------------------------------------
-// PLAIN:  D = rs_i * cs_j * acc + aux0 - coef_i * aux1 (+ D if beta)
+// PLAIN:  D = rs_i * cs_j * acc + aux0 - coef_i * aux1[g_i] (+ D if beta)
+//             - sum_{t in csr(i)} w_t * aux2[t]
 // optional row partial  sum_j D_ij^2  (of the stored, rounded values).
 // Covers: plain store, residual add, RMSNorm row-scale (+ residual),
-// accumulate, the residual + partial-RMS epilogue, and dX - c*X of the
-// RMSNorm-reparameterised backward.
+// accumulate, the residual + partial-RMS epilogue, dX - c*X of the
+// RMSNorm-reparameterised backward, and the exact one-hot terms of the
+// cross-entropy backward (g_i = label row gather; csr = tokens per label).
 // ---------------------------------------------------------------------------
 template <int BN>
 struct EpiPlain {
@@ -46,6 +48,12 @@ struct EpiPlain {
     const bool rv = row < t.M;
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
     const float rc = (e.row_coef && rv) ? e.row_coef[row] : 0.f;
+    const int64_t arow = e.gather_rows ? (rv ? e.gather_rows[row] : -1) : row;
+    int cb0 = 0, cb1 = 0;
+    if (e.csr_off && rv) {
+      cb0 = e.csr_off[row];
+      cb1 = e.csr_off[row + 1];
+    }
     float ss = 0.f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
@@ -74,11 +82,19 @@ struct EpiPlain {
 #pragma unroll
               for (int i = 0; i < 8; ++i) x[i] += r8[i];
             }
-            if (e.row_coef) {
+            if (e.row_coef && arow >= 0) {
               float r8[8];
-              load_bf16x8(e.aux1 + static_cast<int64_t>(row) * e.ld_aux1 + cc, r8);
+              load_bf16x8(e.aux1 + arow * e.ld_aux1 + cc, r8);
 #pragma unroll
               for (int i = 0; i < 8; ++i) x[i] -= rc * r8[i];
+            }
+            for (int j = cb0; j < cb1; ++j) {
+              const int32_t t2 = e.csr_idx[j];
+              const float w2 = e.csr_w[t2];
+              float r8[8];
+              load_bf16x8(e.aux2 + static_cast<int64_t>(t2) * e.ld_aux2 + cc, r8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[i] -= w2 * r8[i];
             }
             if (e.d_f32) {
               float* d = static_cast<float*>(e.D) + static_cast<int64_t>(row) * e.ldd + cc;
@@ -369,9 +385,13 @@ struct EpiCeLse {
 };
 
 // ---------------------------------------------------------------------------
-// CE_DLOGITS (softmax minus one-hot): recomputed logits z,
-//   dZ = (exp(z - lse_i) - [j == y_i]) * w_i,  w_i = dloss / n_valid for a
-//   valid row, 0 for an ignored (or out-of-range) label;  stored bf16.
+// CE_DLOGITS (softmax part of softmax minus one-hot): recomputed logits z,
+//   dZ = exp(z - lse_i) * w_i,  w_i = dloss / n_valid for a valid row, 0 for
+//   an ignored (or out-of-range) label;  stored bf16.  With `onehot` set the
+//   -w_i at the label column is included (the generic-descriptor form); the
+//   named cross-entropy backward instead applies it exactly in fp32 in the
+//   epilogues of the dX and dW GEMMs, so the large label element is never
+//   rounded to bf16.
 // ---------------------------------------------------------------------------
 template <int BN>
 struct EpiCeDlogits {
@@ -409,7 +429,7 @@ struct EpiCeDlogits {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float p = exp2f(fmaf(z[g * 8 + i], LOG2E, -lb));
-              x[i] = (p - (cc + i == lab ? 1.f : 0.f)) * w;
+              x[i] = (p - (e.onehot && cc + i == lab ? 1.f : 0.f)) * w;
             }
             store_bf16x8(d + cc, x);
           }

@@ -67,6 +67,12 @@ struct EpiArgs {
   const __nv_bfloat16* aux1;
   int64_t ld_aux1;
   const float* row_coef;
+  const int32_t* gather_rows;   // aux1 row read for output row i (skipped when < 0)
+  const __nv_bfloat16* aux2;    // rows subtracted through the CSR below
+  int64_t ld_aux2;
+  const int32_t* csr_off;       // [M+1] per output row: range of csr_idx
+  const int32_t* csr_idx;       // aux2 row indices
+  const float* csr_w;           // weight of each aux2 row
   __nv_bfloat16* out1;
   int64_t ld_out1;
   __nv_bfloat16* out2;
@@ -81,6 +87,7 @@ struct EpiArgs {
   const float* lse;
   const int32_t* n_valid;
   float dloss;
+  int onehot;                   // CE_DLOGITS: include -w at the label column
   float* target_logit;
   // QK-RMSNorm + RoPE
   const int32_t* pos;
