@@ -24,7 +24,7 @@ __all__ = [
     "fold_gamma", "rms_rstd", "rope_table", "gemm_epilogue", "EpilogueDesc",
     "rmsnorm_linear", "rmsnorm_linear_bwd", "linear_residual", "linear_residual_bwd",
     "linear_swiglu", "linear_swiglu_bwd", "linear_qknorm_rope", "linear_qknorm_rope_bwd",
-    "linear_cross_entropy", "linear_cross_entropy_bwd", "workspace",
+    "linear_cross_entropy", "linear_cross_entropy_bwd", "linear_cross_entropy_noalloc", "workspace",
     "MAP_NONE", "MAP_SWIGLU", "MAP_DSWIGLU", "MAP_QKNORM_ROPE", "MAP_CE_LSE",
     "MAP_CE_DLOGITS", "MAP_COLDOT", "K_MAJOR", "MN_MAJOR",
 ]
@@ -72,6 +72,8 @@ _SIGS = {
                                     + [_I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_cross_entropy_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_cross_entropy": ([_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_noalloc_scratch_bytes": ([], _SZ),
+    "coda_linear_cross_entropy_noalloc": ([_P, _P, _P, _I32, _P, _P, _P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
     "coda_linear_cross_entropy_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_cross_entropy_bwd": ([_P, _P, _P, _I32, _P, _P, _F, _P, _P, _I64, _I64, _I64, _P, _SZ, _P],
                                       ctypes.c_int),
@@ -383,6 +385,27 @@ def linear_cross_entropy(X, W, labels, ignore_index=-100, out=None, ws=None, str
         _f32(out["lse"], "lse"), _i32(out["n_valid"], "n_valid"), M, V, K, _ptr(ws), ws.numel(),
         _stream(stream)))
     out["ws"] = ws
+    return out
+
+
+def linear_cross_entropy_noalloc(X, W, labels, ignore_index=-100, out=None, stream=None):
+    """coda_linear_cross_entropy_noalloc: the forward with the library's fixed
+    device scratch instead of a workspace, for callers that cannot allocate
+    device memory (see include/coda.h).  Pass `out` (loss [1], lse [M],
+    n_valid [1], status [1] int32) so that nothing is allocated here either."""
+    lib = load()
+    M, K = X.shape
+    V = W.shape[0]
+    dev = X.device
+    if out is None:
+        out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
+               "lse": torch.empty(M, dtype=torch.float32, device=dev),
+               "n_valid": torch.empty(1, dtype=torch.int32, device=dev),
+               "status": torch.empty(1, dtype=torch.int32, device=dev)}
+    _check("coda_linear_cross_entropy_noalloc", lib.coda_linear_cross_entropy_noalloc(
+        _bf(X, "X"), _bf(W, "W"), _i32(labels, "labels"), int(ignore_index), _f32(out["loss"], "loss"),
+        _f32(out["lse"], "lse"), _i32(out["n_valid"], "n_valid"), _i32(out.get("status"), "status"),
+        M, V, K, _stream(stream)))
     return out
 
 

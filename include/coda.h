@@ -332,6 +332,32 @@ int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int3
                               int32_t ignore_index, float* loss_mean, float* lse, int32_t* n_valid,
                               int64_t M, int64_t V, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
 
+/* Variant of coda_linear_cross_entropy that allocates nothing and takes no
+ * workspace, for callers that cannot obtain device memory: a plugin or
+ * callback inside a host application that owns all device memory and passes
+ * it only input and output buffers, or a latency-critical loop that must not
+ * call cudaMalloc because it may synchronise the device.  The paper has no
+ * counterpart; this is an interface convenience of this library.
+ *
+ * Same arguments and results as coda_linear_cross_entropy, minus ws.  Its
+ * scratch is a fixed device array inside libcoda.so of
+ * coda_noalloc_scratch_bytes() bytes (8 MiB), held by every GPU that loads the
+ * library until the process exits; a problem whose
+ * coda_linear_cross_entropy_workspace_size(M, V, K) exceeds it is rejected
+ * with CODA_ERR_WORKSPACE before anything is enqueued (at V = 128256 that is
+ * M above about 32,000 tokens).  The first call on a device looks up the
+ * array's device address (set-up, once per device, with that device
+ * current); make that first call before any stream capture.  Every call
+ * shares the array, so calls that overlap on the GPU (different streams or
+ * threads) race and must be serialised by the caller.
+ * status_out (optional device int32) receives this call's device status word:
+ * 0 if no device error, otherwise the bits that coda_get_status maps (2 = a
+ * label out of range, 1 = a pipeline wait timed out). */
+size_t coda_noalloc_scratch_bytes(void);
+int coda_linear_cross_entropy_noalloc(const coda_bf16* X, const coda_bf16* W, const int32_t* labels,
+                                      int32_t ignore_index, float* loss_mean, float* lse, int32_t* n_valid,
+                                      int32_t* status_out, int64_t M, int64_t V, int64_t K, coda_stream stream);
+
 /* Backward for upstream gradient dloss of the mean loss:
  *   dZ = (softmax(z) - onehot(y)) * dloss / n_valid (0 on ignored rows),
  *   dX = dZ W [M, K], dW = dZ^T X [V, K] (bf16).
