@@ -53,6 +53,8 @@ def parse():
     p.add_argument("--no-unfused", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-tokens", type=int, default=64, help="token sample of the CPU oracle timing")
+    p.add_argument("--tokens", type=int, default=8192,
+                   help="tokens per step (8192 is the benchmark workload; smaller values only for profiling)")
     return p.parse_args()
 
 
@@ -296,7 +298,8 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     coda.load()
-    s = synth.FULL["c5"]
+    import dataclasses
+    s = dataclasses.replace(synth.FULL["c5"], tokens=args.tokens)
     host = synth.make_block(s, seed=rank)          # replicas: each rank its own seeded batch
     t = {k: v.to(dev) for k, v in host.items()}
     blk = Block(s, t, device=dev)
@@ -414,7 +417,7 @@ def main():
 
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.tokens == synth.FULL["c5"].tokens:
         torch.set_num_threads(cores())
         v, dt, fl = oracle_sample_timing(args.cpu_tokens, oracle_inputs(host, args.cpu_tokens))
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
