@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -108,11 +109,24 @@ struct Plan {
   EpiArgs e{};
 };
 
+// CTA pairs (cta_group::2, 256-row tiles) halve each SM's B traffic; a
+// problem of one 128-row block keeps single CTAs.  CODA_CTA_PAIR=0 in the
+// environment selects single CTAs everywhere (for comparisons).
+bool use_pairs(int64_t M) {
+  static const bool enabled = [] {
+    const char* v = std::getenv("CODA_CTA_PAIR");
+    return !(v && v[0] == '0');
+  }();
+  return enabled && M > coda::BM;
+}
+
 int run(const Plan& p, int* status, cudaStream_t s) {
   if (p.M == 0 || p.N == 0) return CODA_OK;
   if (!get_encoder()) return CODA_ERR_CUDA;
   const int sms = num_sms();
   if (sms <= 0) return CODA_ERR_CUDA;
+  const bool pair = use_pairs(p.M);
+  const uint32_t b_box_rows = pair ? BN / 2 : BN;  // K-major B rows one CTA stages
   CUtensorMap maps[4];
   std::memset(maps, 0, sizeof(maps));
   // A operands
@@ -120,7 +134,7 @@ int run(const Plan& p, int* status, cudaStream_t s) {
     return p.a_mn ? encode_map(m, ptr, Kc, p.M, ld, 64, 64) : encode_map(m, ptr, p.M, Kc, ld, 64, 128);
   };
   auto enc_b = [&](CUtensorMap* m, const void* ptr, int64_t ld, int64_t Kc) {
-    return p.b_mn ? encode_map(m, ptr, Kc, p.N, ld, 64, 64) : encode_map(m, ptr, p.N, Kc, ld, 64, BN);
+    return p.b_mn ? encode_map(m, ptr, Kc, p.N, ld, 64, 64) : encode_map(m, ptr, p.N, Kc, ld, 64, b_box_rows);
   };
   if (!enc_a(&maps[0], p.A, p.lda, p.K)) return CODA_ERR_CUDA;
   if (p.b_dual) {
@@ -140,7 +154,7 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   GemmArgs a{};
   a.M = static_cast<int>(p.M);
   a.N = static_cast<int>(p.N);
-  a.num_m = static_cast<int>(cdiv(p.M, coda::BM));
+  a.num_m = static_cast<int>(cdiv(p.M, pair ? 2 * coda::BM : coda::BM));
   a.num_n = static_cast<int>(cdiv(p.N, p.b_dual ? BN / 2 : BN));
   a.kb0 = static_cast<int>(cdiv(p.K, coda::BK));
   a.kb1 = p.K2 > 0 ? static_cast<int>(cdiv(p.K2, coda::BK)) : 0;
@@ -150,20 +164,20 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   a.n_per_unit = p.n_per_unit;
   a.num_units = p.n_per_unit > 1 ? a.num_m * static_cast<int>(cdiv(a.num_n, p.n_per_unit)) : a.num_m * a.num_n;
   a.group_m = 16;
-  a.idesc = coda::idesc_bf16(coda::BM, BN, p.a_mn, p.b_mn);
+  a.idesc = coda::idesc_bf16(pair ? 2 * coda::BM : coda::BM, BN, p.a_mn, p.b_mn);
   a.status = status;
   a.timeout_ns = TIMEOUT_NS;
   a.e = p.e;
-  const dim3 grid(static_cast<unsigned>(std::min(a.num_units, sms)));
+  const int nu = a.num_units;
   cudaError_t err;
   switch (p.kind) {
-    case coda::EpiKind::Plain: err = coda::launch_gemm_plain(grid, s, maps, a); break;
-    case coda::EpiKind::Swiglu: err = coda::launch_gemm_swiglu(grid, s, maps, a); break;
-    case coda::EpiKind::DSwiglu: err = coda::launch_gemm_dswiglu(grid, s, maps, a); break;
-    case coda::EpiKind::QkRope: err = coda::launch_gemm_qkrope(grid, s, maps, a); break;
-    case coda::EpiKind::CeLse: err = coda::launch_gemm_celse(grid, s, maps, a); break;
-    case coda::EpiKind::CeDlogits: err = coda::launch_gemm_cedlogits(grid, s, maps, a); break;
-    case coda::EpiKind::ColDot: err = coda::launch_gemm_coldot(grid, s, maps, a); break;
+    case coda::EpiKind::Plain: err = coda::launch_gemm_plain(nu, sms, pair, s, maps, a); break;
+    case coda::EpiKind::Swiglu: err = coda::launch_gemm_swiglu(nu, sms, pair, s, maps, a); break;
+    case coda::EpiKind::DSwiglu: err = coda::launch_gemm_dswiglu(nu, sms, pair, s, maps, a); break;
+    case coda::EpiKind::QkRope: err = coda::launch_gemm_qkrope(nu, sms, pair, s, maps, a); break;
+    case coda::EpiKind::CeLse: err = coda::launch_gemm_celse(nu, sms, pair, s, maps, a); break;
+    case coda::EpiKind::CeDlogits: err = coda::launch_gemm_cedlogits(nu, sms, pair, s, maps, a); break;
+    case coda::EpiKind::ColDot: err = coda::launch_gemm_coldot(nu, sms, pair, s, maps, a); break;
     default: return CODA_ERR_INVALID_ARG;
   }
   return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;

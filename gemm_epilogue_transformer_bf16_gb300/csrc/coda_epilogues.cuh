@@ -320,7 +320,8 @@ struct EpiColDot {
         const float send = hi ? p[0] : p[1];
         p[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
       }
-      if (e.partials && col0 + lane < t.N)
+      // (a CTA pair's second M block can lie wholly past M: no partial row for it)
+      if (e.partials && col0 + lane < t.N && t.mb * BM < t.M)
         e.partials[static_cast<int64_t>(t.mb * 4 + q) * e.ld_part + col0 + lane] = p[0];
     }
   }

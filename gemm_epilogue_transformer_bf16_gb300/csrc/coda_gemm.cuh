@@ -42,11 +42,15 @@ constexpr int BK = 64;
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARP0 = 2;
 
-template <int BN>
+// PAIR: a cluster of two CTAs on two SMs computes a 256 x BN tile with
+// tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of A and half of
+// B (BN/2 rows), so a stage is 32 KB and six of them fit.
+template <int BN, bool PAIR = false>
 struct GemmCfg {
-  static constexpr int STAGES = BN >= 256 ? 4 : 6;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows staged by one CTA
+  static constexpr int STAGES = PAIR ? 6 : (BN >= 256 ? 4 : 6);
   static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr uint32_t BAR_BYTES = 256;
@@ -153,12 +157,12 @@ __device__ __forceinline__ void epi_bar_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
-template <int BN, class Epi>
+template <int BN, class Epi, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     coda_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mB0,
                      const __grid_constant__ CUtensorMap mA1, const __grid_constant__ CUtensorMap mB1,
                      const GemmArgs args) {
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg<BN, PAIR>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -174,6 +178,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // In a pair, CTA rank 0 issues the MMAs and owns the "full" and
+  // "TMEM empty" barriers; both CTAs load, and both run epilogues.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int cluster_id = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int num_clusters = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -182,7 +192,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], PAIR ? 8 : 4);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -198,12 +208,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (args.b_dual) tma_prefetch_desc(&mB1);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<PAIR>(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish<PAIR>();
   }
   for (int i = threadIdx.x; i < BN; i += NUM_THREADS) epi_smem[i] = 0.f;
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // peer barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_kb = args.kb0 + args.kb1;
@@ -213,9 +224,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
-      for (int u = blockIdx.x; u < args.num_units && !aborted; u += gridDim.x) {
-        int mb, nb0, nlen, chunk;
-        unit_coords(args, u, mb, nb0, nlen, chunk);
+      for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters) {
+        int mb2, nb0, nlen, chunk;
+        unit_coords(args, u, mb2, nb0, nlen, chunk);
+        const int mb = PAIR ? mb2 * 2 + static_cast<int>(rank) : mb2;
         for (int j = 0; j < nlen && !aborted; ++j) {
           const int nb = nb0 + j;
           for (int kb = 0; kb < num_kb; ++kb, ++it) {
@@ -225,45 +237,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               aborted = true;
               break;
             }
-            mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+            if (leader) mbar_arrive_expect_tx(&full[s], PAIR ? 2 * Cfg::STAGE_BYTES : Cfg::STAGE_BYTES);
             const bool second = kb >= args.kb0;
             const CUtensorMap* ma = second ? &mA1 : &mA0;
             const CUtensorMap* mbp = second ? &mB1 : &mB0;
             const int k = (second ? kb - args.kb0 : kb) * BK;
             uint8_t* sa = tiles + s * Cfg::STAGE_BYTES;
             uint8_t* sb = sa + Cfg::A_BYTES;
-            if (!args.a_mn) {
-              tma_load_2d(sa, ma, &full[s], k, mb * BM);
-            } else {
+            if constexpr (PAIR) {
+              const uint32_t bar = mapa_shared(&full[s], 0);
+              if (!args.a_mn) {
+                tma_load_2d_pair(sa, ma, bar, k, mb * BM);
+              } else {
 #pragma unroll
-              for (int c = 0; c < BM / 64; ++c) tma_load_2d(sa + c * 8192, ma, &full[s], mb * BM + c * 64, k);
-            }
-            if (args.b_dual) {
-              tma_load_2d(sb, &mB0, &full[s], k, nb * (BN / 2));
-              tma_load_2d(sb + (BN / 2) * 128, &mB1, &full[s], k, nb * (BN / 2));
-            } else if (!args.b_mn) {
-              tma_load_2d(sb, mbp, &full[s], k, nb * BN);
-            } else {
+                for (int c = 0; c < BM / 64; ++c) tma_load_2d_pair(sa + c * 8192, ma, bar, mb * BM + c * 64, k);
+              }
+              if (args.b_dual) {
+                // the pair's N = [gate rows | up rows]: rank 0 stages the gate half, rank 1 the up half
+                tma_load_2d_pair(sb, rank ? &mB1 : &mB0, bar, k, nb * (BN / 2));
+              } else if (!args.b_mn) {
+                tma_load_2d_pair(sb, mbp, bar, k, nb * BN + static_cast<int>(rank) * Cfg::B_ROWS);
+              } else {
 #pragma unroll
-              for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * 8192, mbp, &full[s], nb * BN + c * 64, k);
+                for (int c = 0; c < Cfg::B_ROWS / 64; ++c)
+                  tma_load_2d_pair(sb + c * 8192, mbp, bar, nb * BN + static_cast<int>(rank) * Cfg::B_ROWS + c * 64,
+                                   k);
+              }
+            } else {
+              if (!args.a_mn) {
+                tma_load_2d(sa, ma, &full[s], k, mb * BM);
+              } else {
+#pragma unroll
+                for (int c = 0; c < BM / 64; ++c) tma_load_2d(sa + c * 8192, ma, &full[s], mb * BM + c * 64, k);
+              }
+              if (args.b_dual) {
+                tma_load_2d(sb, &mB0, &full[s], k, nb * (BN / 2));
+                tma_load_2d(sb + (BN / 2) * 128, &mB1, &full[s], k, nb * (BN / 2));
+              } else if (!args.b_mn) {
+                tma_load_2d(sb, mbp, &full[s], k, nb * BN);
+              } else {
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c)
+                  tma_load_2d(sb + c * 8192, mbp, &full[s], nb * BN + c * 64, k);
+              }
             }
           }
         }
       }
       if (aborted) {
-        // let every copy already issued land before the CTA's smem is reused
-        const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
-        for (uint32_t j = first; j < it; ++j) mbar_wait_drain(&full[j % S], (j / S) & 1, 200000000ull);
+        if (leader) {
+          // let every copy already issued land before the CTA's smem is reused
+          const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
+          for (uint32_t j = first; j < it; ++j) mbar_wait_drain(&full[j % S], (j / S) & 1, 200000000ull);
+        } else {
+          // the peer's copies complete on the leader's barrier; give them time
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 2000000ull) {
+          }
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       uint32_t it = 0, t = 0;
       bool issued = false;
-      for (int u = blockIdx.x; u < args.num_units && !aborted; u += gridDim.x) {
-        int mb, nb0, nlen, chunk;
-        unit_coords(args, u, mb, nb0, nlen, chunk);
+      const uint32_t idesc = args.idesc;
+      for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters) {
+        int mb2, nb0, nlen, chunk;
+        unit_coords(args, u, mb2, nb0, nlen, chunk);
         for (int j = 0; j < nlen && !aborted; ++j, ++t) {
           const uint32_t buf = t & 1;
           if (!mbar_wait_bounded(&tempty[buf], ((t >> 1) & 1) ^ 1, abort_flag, args.status, args.timeout_ns)) {
@@ -291,17 +333,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                             : sdesc_sw128(sa + k16 * 32, 16, 1024);
               const uint64_t bd = args.b_mn ? sdesc_sw128(sb + k16 * 2048, 8192, 1024)
                                             : sdesc_sw128(sb + k16 * 32, 16, 1024);
-              umma_bf16(d_tmem, ad, bd, args.idesc, (kb | k16) != 0);
+              if constexpr (PAIR)
+                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+              else
+                umma_bf16(d_tmem, ad, bd, idesc, (kb | k16) != 0);
             }
             issued = true;
-            umma_commit(&empty[s]);
+            if constexpr (PAIR)
+              umma_commit_pair_mc(&empty[s], 0x3);
+            else
+              umma_commit(&empty[s]);
           }
           if (aborted) break;
-          umma_commit(&tfull[buf]);
+          if constexpr (PAIR)
+            umma_commit_pair_mc(&tfull[buf], 0x3);
+          else
+            umma_commit(&tfull[buf]);
         }
       }
       if (aborted && issued) {
-        umma_commit(drain);
+        if constexpr (PAIR)
+          umma_commit_pair(drain);
+        else
+          umma_commit(drain);
         mbar_wait_drain(drain, 0, 200000000ull);
       }
     }
@@ -309,9 +363,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint32_t t = 0;
-    for (int u = blockIdx.x; u < args.num_units && !aborted; u += gridDim.x) {
-      int mb, nb0, nlen, chunk;
-      unit_coords(args, u, mb, nb0, nlen, chunk);
+    for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters) {
+      int mb2, nb0, nlen, chunk;
+      unit_coords(args, u, mb2, nb0, nlen, chunk);
+      const int mb = PAIR ? mb2 * 2 + static_cast<int>(rank) : mb2;
       TileInfo ti;
       ti.mb = mb;
       ti.unit_chunk = chunk;
@@ -334,7 +389,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         Epi::tile(st, args.e, ti, epi_smem);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster(mapa_shared(&tempty[buf], 0));
+          else
+            mbar_arrive(&tempty[buf]);
+        }
       }
       if (aborted) break;
       Epi::end(st, args.e, ti);
@@ -343,10 +403,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // no CTA leaves while its peer may still signal it
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    tmem_dealloc<PAIR>(tmem_base, Cfg::TMEM_COLS);
   }
 }
 

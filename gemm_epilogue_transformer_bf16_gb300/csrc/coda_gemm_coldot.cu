@@ -1,8 +1,10 @@
-// Instantiation of the persistent GEMM with the EpiColDot epilogue (BN = 256).
+// Instantiations of the persistent GEMM with the EpiColDot epilogue (BN = 256),
+// single-CTA and CTA-pair variants.
 #include "coda_launch.cuh"
 
 namespace coda {
-cudaError_t launch_gemm_coldot(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a) {
-  return launch_gemm_impl<256, EpiColDot<256>>(grid, s, m, a);
+cudaError_t launch_gemm_coldot(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                                const GemmArgs& a) {
+  return launch_gemm_impl<256, EpiColDot<256>>(num_units, sms, pair, s, m, a);
 }
 }  // namespace coda

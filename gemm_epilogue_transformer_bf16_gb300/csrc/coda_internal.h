@@ -12,14 +12,22 @@ namespace coda {
 
 enum class EpiKind : int { Plain = 0, Swiglu, DSwiglu, QkRope, CeLse, CeDlogits, ColDot };
 
-// Tensor maps in the order A0, B0, A1, B1.
-cudaError_t launch_gemm_plain(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
-cudaError_t launch_gemm_swiglu(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
-cudaError_t launch_gemm_dswiglu(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
-cudaError_t launch_gemm_qkrope(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
-cudaError_t launch_gemm_celse(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
-cudaError_t launch_gemm_cedlogits(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
-cudaError_t launch_gemm_coldot(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a);
+// Tensor maps in the order A0, B0, A1, B1.  `pair` selects the CTA-pair
+// (cta_group::2) variant; the launcher sizes the persistent grid.
+cudaError_t launch_gemm_plain(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                               const GemmArgs& a);
+cudaError_t launch_gemm_swiglu(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                               const GemmArgs& a);
+cudaError_t launch_gemm_dswiglu(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                               const GemmArgs& a);
+cudaError_t launch_gemm_qkrope(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                               const GemmArgs& a);
+cudaError_t launch_gemm_celse(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                               const GemmArgs& a);
+cudaError_t launch_gemm_cedlogits(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                               const GemmArgs& a);
+cudaError_t launch_gemm_coldot(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                               const GemmArgs& a);
 
 // auxiliary kernels (coda_aux.cu)
 cudaError_t launch_fold_gamma(const __nv_bfloat16* W, const float* gamma, __nv_bfloat16* Wf, int64_t N, int64_t K,

@@ -1,28 +1,63 @@
 // Launch helper for one (tile width, epilogue) instantiation of
 // coda_gemm_kernel: raises the dynamic shared-memory limit once per device and
-// launches one 192-thread CTA per SM-slot of the persistent grid.
+// launches the persistent grid -- one 192-thread CTA per SM, or, for the
+// CTA-pair variant, one 2-CTA cluster per SM pair (as many as can be resident
+// at once, which cudaOccupancyMaxActiveClusters reports).
 #pragma once
 #include "coda_epilogues.cuh"
 #include "coda_internal.h"
 
 namespace coda {
 
-template <int BN, class Epi>
-cudaError_t launch_gemm_impl(dim3 grid, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a) {
-  constexpr uint32_t smem = GemmCfg<BN>::SMEM_BYTES;
+template <int BN, class Epi, bool PAIR>
+cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a) {
+  constexpr uint32_t smem = GemmCfg<BN, PAIR>::SMEM_BYTES;
   static bool attr_done[64] = {};
+  static int max_clusters[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  auto kern = coda_gemm_kernel<BN, Epi, PAIR>;
   if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(coda_gemm_kernel<BN, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  coda_gemm_kernel<BN, Epi><<<grid, NUM_THREADS, smem, s>>>(m[0], m[1], m[2], m[3], a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if constexpr (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_clusters[dev] == 0) {
+      cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n <= 0) return cudaErrorInvalidConfiguration;
+      max_clusters[dev] = n;
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(num_units, max_clusters[dev])));
+  } else {
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min(num_units, sms)));
+  }
+  e = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int BN, class Epi>
+cudaError_t launch_gemm_impl(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                             const GemmArgs& a) {
+  return pair ? launch_gemm_variant<BN, Epi, true>(num_units, sms, s, m, a)
+              : launch_gemm_variant<BN, Epi, false>(num_units, sms, s, m, a);
 }
 
 }  // namespace coda
