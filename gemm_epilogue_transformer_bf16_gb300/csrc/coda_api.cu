@@ -120,6 +120,17 @@ bool use_pairs(int64_t M) {
   return enabled && M > coda::BM;
 }
 
+// Tile rows (units of the M tile) per raster group: concurrent tiles share
+// these rows' A panel in L2 while B streams.  CODA_GROUP_M overrides it.
+int group_m(bool pair) {
+  static const int env = [] {
+    const char* v = std::getenv("CODA_GROUP_M");
+    return v ? std::atoi(v) : 0;
+  }();
+  if (env > 0) return env;
+  return pair ? 8 : 16;
+}
+
 int run(const Plan& p, int* status, cudaStream_t s) {
   if (p.M == 0 || p.N == 0) return CODA_OK;
   if (!get_encoder()) return CODA_ERR_CUDA;
@@ -163,7 +174,7 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   a.b_dual = p.b_dual;
   a.n_per_unit = p.n_per_unit;
   a.num_units = p.n_per_unit > 1 ? a.num_m * static_cast<int>(cdiv(a.num_n, p.n_per_unit)) : a.num_m * a.num_n;
-  a.group_m = 16;
+  a.group_m = group_m(pair);
   a.idesc = coda::idesc_bf16(pair ? 2 * coda::BM : coda::BM, BN, p.a_mn, p.b_mn);
   a.status = status;
   a.timeout_ns = TIMEOUT_NS;
