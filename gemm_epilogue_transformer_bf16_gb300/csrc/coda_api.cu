@@ -131,6 +131,17 @@ int group_m(bool pair) {
   return pair ? 8 : 16;
 }
 
+// L2 cache-hint selection for the GEMM launches: bit 0 = A loads evict_last,
+// bit 1 = B loads evict_first, bit 2 = streaming epilogue stores.
+// CODA_L2_HINTS overrides the default.
+int l2_hints() {
+  static const int v = [] {
+    const char* e = std::getenv("CODA_L2_HINTS");
+    return e ? std::atoi(e) : 0;
+  }();
+  return v;
+}
+
 int run(const Plan& p, int* status, cudaStream_t s) {
   if (p.M == 0 || p.N == 0) return CODA_OK;
   if (!get_encoder()) return CODA_ERR_CUDA;
@@ -178,7 +189,9 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   a.idesc = coda::idesc_bf16(pair ? 2 * coda::BM : coda::BM, BN, p.a_mn, p.b_mn);
   a.status = status;
   a.timeout_ns = TIMEOUT_NS;
+  a.l2_hints = l2_hints() & 3;
   a.e = p.e;
+  a.e.st_stream = (l2_hints() & 4) ? 1 : 0;
   const int nu = a.num_units;
   cudaError_t err;
   switch (p.kind) {

@@ -117,7 +117,7 @@ struct EpiPlain {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) x[i] += o8[i];
               }
-              store_bf16x8(d, x);
+              store_bf16x8(d, x, e.st_stream);
               if (e.partials) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -171,9 +171,9 @@ struct EpiSwiglu {
               uu[i] = u[q * 8 + i] * rs;
               h[i] = gg[i] / (1.f + __expf(-gg[i])) * uu[i];
             }
-            store_bf16x8(static_cast<__nv_bfloat16*>(e.D) + off * e.ldd + cc, h);
-            if (e.out1) store_bf16x8(e.out1 + off * e.ld_out1 + cc, gg);
-            if (e.out2) store_bf16x8(e.out2 + off * e.ld_out2 + cc, uu);
+            store_bf16x8(static_cast<__nv_bfloat16*>(e.D) + off * e.ldd + cc, h, e.st_stream);
+            if (e.out1) store_bf16x8(e.out1 + off * e.ld_out1 + cc, gg, e.st_stream);
+            if (e.out2) store_bf16x8(e.out2 + off * e.ld_out2 + cc, uu, e.st_stream);
           }
         }
       }
@@ -227,9 +227,9 @@ struct EpiDSwiglu {
               dg[i] *= rs;
               du[i] *= rs;
             }
-            store_bf16x8(e.out1 + off * e.ld_out1 + cc, dg);
-            store_bf16x8(e.out2 + off * e.ld_out2 + cc, du);
-            if (e.out3) store_bf16x8(e.out3 + off * e.ld_out3 + cc, h);
+            store_bf16x8(e.out1 + off * e.ld_out1 + cc, dg, e.st_stream);
+            store_bf16x8(e.out2 + off * e.ld_out2 + cc, du, e.st_stream);
+            if (e.out3) store_bf16x8(e.out3 + off * e.ld_out3 + cc, h, e.st_stream);
           }
         }
       }
@@ -279,7 +279,7 @@ struct EpiColDot {
               p[g * 8 + i] = v[g * 8 + i] * w8[i];
               x[i] = e.col_scale ? v[g * 8 + i] * s8[i] : v[g * 8 + i];
             }
-            store_bf16x8(static_cast<__nv_bfloat16*>(e.D) + off * e.ldd + cc, x);
+            store_bf16x8(static_cast<__nv_bfloat16*>(e.D) + off * e.ldd + cc, x, e.st_stream);
           }
         }
       }
@@ -432,7 +432,7 @@ struct EpiCeDlogits {
               const float p = exp2f(fmaf(z[g * 8 + i], LOG2E, -lb));
               x[i] = (p - (e.onehot && cc + i == lab ? 1.f : 0.f)) * w;
             }
-            store_bf16x8(d + cc, x);
+            store_bf16x8(d + cc, x, e.st_stream);
           }
         }
       }
@@ -484,7 +484,7 @@ struct EpiQkRope {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= rs;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) store_bf16x8(vout + c + g * 8, v + g * 8);
+            for (int g = 0; g < 4; ++g) store_bf16x8(vout + c + g * 8, v + g * 8, e.st_stream);
           }
         }
         continue;
@@ -505,7 +505,7 @@ struct EpiQkRope {
         }
         if (rv && e.out1) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) store_bf16x8(e.out1 + off * e.ld_out1 + head * D + c + g * 8, v + g * 8);
+          for (int g = 0; g < 4; ++g) store_bf16x8(e.out1 + off * e.ld_out1 + head * D + c + g * 8, v + g * 8, e.st_stream);
         }
       }
       const float rho = rsqrtf(ss * (1.f / D) + e.eps);
@@ -528,7 +528,7 @@ struct EpiQkRope {
             o[2 * i + 1] = a * r.y + b * r.x;
           }
 #pragma unroll
-          for (int g = 0; g < 4; ++g) store_bf16x8(out + c + g * 8, o + g * 8);
+          for (int g = 0; g < 4; ++g) store_bf16x8(out + c + g * 8, o + g * 8, e.st_stream);
         }
       }
     }

@@ -92,6 +92,7 @@ struct EpiArgs {
   const int32_t* n_valid;
   float dloss;
   int onehot;                   // CE_DLOGITS: include -w at the label column
+  int st_stream;                // epilogue tile stores as streaming (.cs) stores
   float* target_logit;
   // QK-RMSNorm + RoPE
   const int32_t* pos;
@@ -122,6 +123,7 @@ struct GemmArgs {
   uint32_t idesc;
   int* status;
   uint64_t timeout_ns;
+  int l2_hints;      // bit 0: A loads evict_last, bit 1: B loads evict_first
   EpiArgs e;
 };
 
@@ -223,6 +225,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // A panels are shared by the raster group's successive waves; B tiles
+      // only by the tiles of one wave.
+      const bool hint_a = args.l2_hints & 1, hint_b = args.l2_hints & 2;
+      const uint64_t pol_a = l2_policy_evict_last();
+      const uint64_t pol_b = l2_policy_evict_first();
       uint32_t it = 0;
       for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters) {
         int mb2, nb0, nlen, chunk;
@@ -247,38 +254,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (PAIR) {
               const uint32_t bar = mapa_shared(&full[s], 0);
               if (!args.a_mn) {
-                tma_load_2d_pair(sa, ma, bar, k, mb * BM);
+                hint_a ? tma_load_2d_pair_hint(sa, ma, bar, k, mb * BM, pol_a) : tma_load_2d_pair(sa, ma, bar, k, mb * BM);
               } else {
 #pragma unroll
-                for (int c = 0; c < BM / 64; ++c) tma_load_2d_pair(sa + c * 8192, ma, bar, mb * BM + c * 64, k);
+                for (int c = 0; c < BM / 64; ++c)
+                  hint_a ? tma_load_2d_pair_hint(sa + c * 8192, ma, bar, mb * BM + c * 64, k, pol_a)
+                         : tma_load_2d_pair(sa + c * 8192, ma, bar, mb * BM + c * 64, k);
               }
               if (args.b_dual) {
                 // the pair's N = [gate rows | up rows]: rank 0 stages the gate half, rank 1 the up half
-                tma_load_2d_pair(sb, rank ? &mB1 : &mB0, bar, k, nb * (BN / 2));
+                hint_b ? tma_load_2d_pair_hint(sb, rank ? &mB1 : &mB0, bar, k, nb * (BN / 2), pol_b)
+                       : tma_load_2d_pair(sb, rank ? &mB1 : &mB0, bar, k, nb * (BN / 2));
               } else if (!args.b_mn) {
-                tma_load_2d_pair(sb, mbp, bar, k, nb * BN + static_cast<int>(rank) * Cfg::B_ROWS);
+                hint_b ? tma_load_2d_pair_hint(sb, mbp, bar, k, nb * BN + static_cast<int>(rank) * Cfg::B_ROWS, pol_b)
+                       : tma_load_2d_pair(sb, mbp, bar, k, nb * BN + static_cast<int>(rank) * Cfg::B_ROWS);
               } else {
 #pragma unroll
                 for (int c = 0; c < Cfg::B_ROWS / 64; ++c)
-                  tma_load_2d_pair(sb + c * 8192, mbp, bar, nb * BN + static_cast<int>(rank) * Cfg::B_ROWS + c * 64,
-                                   k);
+                  hint_b ? tma_load_2d_pair_hint(sb + c * 8192, mbp, bar,
+                                                 nb * BN + static_cast<int>(rank) * Cfg::B_ROWS + c * 64, k, pol_b)
+                         : tma_load_2d_pair(sb + c * 8192, mbp, bar,
+                                            nb * BN + static_cast<int>(rank) * Cfg::B_ROWS + c * 64, k);
               }
             } else {
               if (!args.a_mn) {
-                tma_load_2d(sa, ma, &full[s], k, mb * BM);
+                hint_a ? tma_load_2d_hint(sa, ma, &full[s], k, mb * BM, pol_a) : tma_load_2d(sa, ma, &full[s], k, mb * BM);
               } else {
 #pragma unroll
-                for (int c = 0; c < BM / 64; ++c) tma_load_2d(sa + c * 8192, ma, &full[s], mb * BM + c * 64, k);
+                for (int c = 0; c < BM / 64; ++c)
+                  hint_a ? tma_load_2d_hint(sa + c * 8192, ma, &full[s], mb * BM + c * 64, k, pol_a)
+                         : tma_load_2d(sa + c * 8192, ma, &full[s], mb * BM + c * 64, k);
               }
               if (args.b_dual) {
-                tma_load_2d(sb, &mB0, &full[s], k, nb * (BN / 2));
-                tma_load_2d(sb + (BN / 2) * 128, &mB1, &full[s], k, nb * (BN / 2));
+                hint_b ? tma_load_2d_hint(sb, &mB0, &full[s], k, nb * (BN / 2), pol_b)
+                       : tma_load_2d(sb, &mB0, &full[s], k, nb * (BN / 2));
+                hint_b ? tma_load_2d_hint(sb + (BN / 2) * 128, &mB1, &full[s], k, nb * (BN / 2), pol_b)
+                       : tma_load_2d(sb + (BN / 2) * 128, &mB1, &full[s], k, nb * (BN / 2));
               } else if (!args.b_mn) {
-                tma_load_2d(sb, mbp, &full[s], k, nb * BN);
+                hint_b ? tma_load_2d_hint(sb, mbp, &full[s], k, nb * BN, pol_b) : tma_load_2d(sb, mbp, &full[s], k, nb * BN);
               } else {
 #pragma unroll
                 for (int c = 0; c < BN / 64; ++c)
-                  tma_load_2d(sb + c * 8192, mbp, &full[s], nb * BN + c * 64, k);
+                  hint_b ? tma_load_2d_hint(sb + c * 8192, mbp, &full[s], nb * BN + c * 64, k, pol_b)
+                         : tma_load_2d(sb + c * 8192, mbp, &full[s], nb * BN + c * 64, k);
               }
             }
           }

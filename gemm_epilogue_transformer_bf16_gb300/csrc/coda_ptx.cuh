@@ -93,6 +93,28 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// L2 eviction-priority policies for the TMA loads below.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Same as tma_load_2d with an L2 cache-eviction policy.
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
 // 2-D tiled copy for a CTA pair (cta_group::2): the data lands in this CTA's
 // shared memory, the byte count is signalled on `bar_cluster`, a
 // shared::cluster address that may name the peer CTA's mbarrier.
@@ -102,6 +124,15 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x,
+                                                      int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
 
@@ -275,6 +306,17 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16* p, const float* v) {
   q.z = pack_bf16x2(v[4], v[5]);
   q.w = pack_bf16x2(v[6], v[7]);
   *reinterpret_cast<uint4*>(p) = q;
+}
+// Same, as a streaming store (.cs) when `stream` is set: an output tile is
+// written once and need not displace the L2-resident operand panel.
+__device__ __forceinline__ void store_bf16x8(__nv_bfloat16* p, const float* v, bool stream) {
+  const uint32_t x = pack_bf16x2(v[0], v[1]), y = pack_bf16x2(v[2], v[3]);
+  const uint32_t z = pack_bf16x2(v[4], v[5]), w = pack_bf16x2(v[6], v[7]);
+  if (stream)
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+  else
+    *reinterpret_cast<uint4*>(p) = make_uint4(x, y, z, w);
 }
 __device__ __forceinline__ float round_bf16(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
