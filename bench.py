@@ -52,6 +52,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-unfused", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-ce", action="store_true", help="skip the linear + cross-entropy side measurement")
     p.add_argument("--cpu-tokens", type=int, default=64, help="token sample of the CPU oracle timing")
     p.add_argument("--tokens", type=int, default=8192,
                    help="tokens per step (8192 is the benchmark workload; smaller values only for profiling)")
@@ -415,6 +416,46 @@ def main():
         torch.cuda.synchronize(dev)
         unfused_ms = dist_max(a.elapsed_time(b) / n_unf, world)
 
+    # ---------------------------------------------------------------- linear + CE (rows a8, a12)
+    # Not part of the block step: the 8192 x 2048 x 128256 linear + cross-entropy
+    # workload, forward and backward, timed the same way and reported beside it.
+    other = {}
+    if not args.no_ce:
+        from gemm_epilogue_transformer_bf16_gb300.block import LinearCE
+        from oracle.coda_oracle import ce_flops
+        cs_ = synth.FULL["c4"]
+        hc = synth.make_ce(cs_, seed=rank)
+        dc = {k: v.to(dev) for k, v in hc.items()}
+        ce = LinearCE(cs_.tokens, cs_.vocab, cs_.hidden, device=dev)
+        for _ in range(2):
+            ce.step(dc["X"], dc["W"], dc["labels"])
+        torch.cuda.synchronize(dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        n_ce = 3
+        fw, bw = [], []
+        for _ in range(n_ce):
+            ev[0].record(stream)
+            coda.linear_cross_entropy(dc["X"], dc["W"], dc["labels"], out=ce.out, ws=ce.ws)
+            ev[1].record(stream)
+            coda.linear_cross_entropy_bwd(dc["X"], dc["W"], dc["labels"], ce.out["lse"], ce.out["n_valid"], 1.0,
+                                          out=ce.grads, ws=ce.ws)
+            ev[2].record(stream)
+            torch.cuda.synchronize(dev)
+            fw.append(ev[0].elapsed_time(ev[1]))
+            bw.append(ev[1].elapsed_time(ev[2]))
+        if coda.get_status(ce.ws) != 0:
+            raise RuntimeError("device status error in the linear-CE measurement")
+        f_fwd = ce_flops(cs_.tokens, cs_.hidden, cs_.vocab, backward=False)
+        f_all = ce_flops(cs_.tokens, cs_.hidden, cs_.vocab)
+        mf, mb = statistics.median(fw), statistics.median(bw)
+        other["linear_cross_entropy"] = {
+            "workload": "tokens 8192, hidden 2048, vocab 128256, 5% ignored labels; fwd (online LSE epilogue + "
+                        "combine) and bwd (softmax-minus-onehot epilogue, dX, dW)",
+            "fwd_ms": round(mf, 3), "bwd_ms": round(mb, 3),
+            "fwd_tflops": round(f_fwd / (mf / 1e3) / 1e12, 1),
+            "fwd_bwd_tflops": round(f_all / ((mf + mb) / 1e3) / 1e12, 1)}
+        del ce, dc
+
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.tokens == synth.FULL["c5"].tokens:
@@ -443,6 +484,7 @@ def main():
             "unfused_ms_per_step": round(unfused_ms, 3) if unfused_ms else None,
             "speedup_vs_unfused": round(unfused_ms / ms_step, 3) if unfused_ms else None,
             "stages": stages,
+            "other_workloads": other or None,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

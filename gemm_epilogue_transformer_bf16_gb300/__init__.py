@@ -46,6 +46,7 @@ _SIGS = {
     "coda_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "coda_get_status": ([_P, _P], ctypes.c_int),
     "coda_reset_status": ([_P, _P], ctypes.c_int),
+    "coda_selftest_wait_timeout": ([ctypes.c_uint32, _P, _P], ctypes.c_int),
     "coda_gemm_epilogue_workspace_size": ([], _SZ),
     "coda_gemm_epilogue": ([_P, _P, _I64, ctypes.c_int, _P, _I64, ctypes.c_int, _P, _I64, ctypes.c_int,
                             _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),

@@ -277,6 +277,14 @@ int coda_reset_status(void* ws, coda_stream stream) {
   return CODA_OK;
 }
 
+int coda_selftest_wait_timeout(uint32_t limit_us, void* ws, coda_stream stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return CODA_ERR_INVALID_ARG;
+  CK(ws_ok(ws, WS_HEADER, WS_HEADER));
+  CU(coda::launch_selftest_wait_timeout(static_cast<uint64_t>(limit_us) * 1000ull, static_cast<int*>(ws),
+                                        S(stream)));
+  return CODA_OK;
+}
+
 // ------------------------------------------------------------------ generic
 size_t coda_gemm_epilogue_workspace_size(void) { return WS_HEADER; }
 
@@ -1023,9 +1031,10 @@ int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int3
                               void* ws, size_t ws_bytes, coda_stream stream) {
   CK(dims_ok(M, V, K));
   CK(ws_ok(ws, ws_bytes, coda_linear_cross_entropy_workspace_size(M, V, K)));
-  for (const void* q : {(const void*)X, (const void*)W, (const void*)labels, (const void*)loss_mean,
-                        (const void*)lse, (const void*)n_valid})
-    CK(req(q));
+  CK(req(loss_mean));
+  CK(req(n_valid));
+  if (M > 0)  // with no rows only the mean (NaN) and the count (0) are written
+    for (const void* q : {(const void*)X, (const void*)W, (const void*)labels, (const void*)lse}) CK(req(q));
   CK(al(X));
   CK(al(W));
   if (V == 0) return CODA_ERR_INVALID_ARG;
@@ -1078,9 +1087,11 @@ int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const 
                                   size_t ws_bytes, coda_stream stream) {
   CK(dims_ok(M, V, K));
   CK(ws_ok(ws, ws_bytes, coda_linear_cross_entropy_bwd_workspace_size(M, V, K)));
-  for (const void* q : {(const void*)X, (const void*)W, (const void*)labels, (const void*)lse,
-                        (const void*)n_valid, (const void*)dX, (const void*)dW})
-    CK(req(q));
+  CK(req(dW));
+  if (M > 0)  // with no rows dW is zero and nothing else is touched
+    for (const void* q : {(const void*)X, (const void*)W, (const void*)labels, (const void*)lse,
+                          (const void*)n_valid, (const void*)dX})
+      CK(req(q));
   for (const void* q : {(const void*)X, (const void*)W, (const void*)dX, (const void*)dW}) CK(al(q));
   if (V == 0) return CODA_ERR_INVALID_ARG;
   if (M == 0) {

@@ -321,6 +321,26 @@ cudaError_t launch_ce_onehot_prep(const int32_t* labels, int32_t ignore, int64_t
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- bounded-wait self-test
+// One thread waits on an mbarrier that nothing arrives on, through the same
+// bounded wait the GEMM pipeline uses; after `limit_ns` the wait gives up and
+// records CODA_DEV_TIMEOUT in the status word.  Shows on a live GPU that a
+// stuck pipeline stage turns into a host-readable error, not a hang.
+__global__ void selftest_wait_timeout_kernel(uint64_t limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  mbar_wait_bounded(&bar, 0, &abort_flag, status, limit_ns);
+}
+
+cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s) {
+  selftest_wait_timeout_kernel<<<1, 32, 0, s>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- RoPE table
 __global__ void rope_table_kernel(double theta, int head_dim, int max_pos, float2* cs) {
   const int half = head_dim / 2;

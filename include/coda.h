@@ -140,6 +140,14 @@ int coda_get_status(const void* ws, coda_stream stream);
 /* Enqueues a clear of the device status word (asynchronous). */
 int coda_reset_status(void* ws, coda_stream stream);
 
+/* Failure-path self-test: enqueues one thread that waits, through the same
+ * bounded mbarrier wait every GEMM pipeline stage uses, on a barrier that
+ * nothing arrives on.  After limit_us microseconds (1 .. 1e6) the wait gives
+ * up and sets the timeout bit of the status word in `ws` (256 bytes), so a
+ * following coda_get_status returns CODA_ERR_TIMEOUT and the CUDA context
+ * stays usable.  No kernel traps or spins without a limit. */
+int coda_selftest_wait_timeout(uint32_t limit_us, void* ws, coda_stream stream);
+
 /* ------------------------------------------------------------------------
  * Generic GEMM + epilogue ("CODA" §3.2: h = xW, y[i,j] = f_ij(h tile))
  *
