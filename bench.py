@@ -53,6 +53,7 @@ def parse():
     p.add_argument("--no-unfused", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-ce", action="store_true", help="skip the linear + cross-entropy side measurement")
+    p.add_argument("--serial", action="store_true", help="run the step's calls on one stream")
     p.add_argument("--cpu-tokens", type=int, default=64, help="token sample of the CPU oracle timing")
     p.add_argument("--tokens", type=int, default=8192,
                    help="tokens per step (8192 is the benchmark workload; smaller values only for profiling)")
@@ -303,7 +304,7 @@ def main():
     s = dataclasses.replace(synth.FULL["c5"], tokens=args.tokens)
     host = synth.make_block(s, seed=rank)          # replicas: each rank its own seeded batch
     t = {k: v.to(dev) for k, v in host.items()}
-    blk = Block(s, t, device=dev)
+    blk = Block(s, t, device=dev, concurrent=not args.serial)
     flops_step = sum(blk.gemm_flops().values())
     launches_step = sum(Block.LAUNCHES.values())
     stream = torch.cuda.current_stream(dev)

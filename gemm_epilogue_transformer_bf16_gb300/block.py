@@ -19,8 +19,13 @@ Backward (given dx2 and the attention-input gradients dQ, dK, dV):
   qkv    QK-norm+RoPE backward map, reparameterised RMSNorm backward,
          dx0 = dx1 + qkv branch; dWqkv, dgamma_attn, dgamma_q, dgamma_k
 
-Every step is a libcoda.so call on the current stream; buffers and one shared
-workspace are allocated once, so a step launches only the library's kernels.
+Every step is a libcoda.so call; buffers and workspaces are allocated once,
+so a step launches only the library's kernels.  With ``concurrent`` (the
+default) independent calls run on a second stream: in the forward the gamma
+folds, the row RMS of x0 and the QKV projection overlap the O-projection (the
+HBM-bound folds share SMs with the tensor-bound GEMM), and in the backward
+the O-projection backward overlaps the QKV backward, filling each other's
+last-wave tails.  The gate/up, down and MLP-backward GEMMs run alone.
 """
 from __future__ import annotations
 
@@ -32,9 +37,10 @@ from . import (fold_gamma, linear_cross_entropy, linear_cross_entropy_bwd, linea
 
 
 class Block:
-    def __init__(self, shape, weights, device="cuda"):
+    def __init__(self, shape, weights, device="cuda", concurrent=True):
         self.s = s = shape
         self.w = weights
+        self.concurrent = concurrent
         lib = load()
         T, Hd, I, d = s.tokens, s.hidden, s.inter, s.head_dim
         nqkv = s.qkv_out
@@ -70,35 +76,51 @@ class Block:
             lib.coda_linear_qknorm_rope_bwd_workspace_size(T, Hd, s.n_q, s.n_kv, d),
         )
         self.ws = workspace(need, device)
+        # second stream and its own workspace (calls on different streams must
+        # not share scratch)
+        self.s2 = torch.cuda.Stream(device=device) if concurrent else None
+        self.ws2 = workspace(need, device) if concurrent else self.ws
 
-    # Kernels each stage launches (library calls are fixed sequences).
-    LAUNCHES = {"fold": 3, "rstd0": 1, "qkv": 1, "oproj": 2, "gateup": 1, "down": 1,
-                "mlp_bwd": 7, "oproj_bwd": 2, "qkv_bwd": 7}
+    # Stages as the step's CUDA events delimit them on the main stream, and the
+    # kernels each launches (library calls are fixed sequences).  "pre" is the
+    # fold + row RMS + QKV branch overlapped with the O-projection; "attn_bwd"
+    # the O-projection backward overlapped with the QKV backward.
+    LAUNCHES = {"pre": 7, "gateup": 1, "down": 1, "mlp_bwd": 7, "attn_bwd": 9}
 
     def gemm_flops(self):
         """Algorithmic GEMM FLOPs (2*M*N*K) of each stage of one step."""
         s = self.s
         T, Hd, I, a = s.tokens, s.hidden, s.inter, s.n_q * s.head_dim
         q = s.qkv_out
-        return {"fold": 0, "rstd0": 0, "qkv": 2 * T * Hd * q, "oproj": 2 * T * a * Hd, "gateup": 4 * T * Hd * I,
-                "down": 2 * T * I * Hd, "mlp_bwd": 2 * (2 * T * Hd * I) + 2 * (4 * T * Hd * I),
-                "oproj_bwd": 4 * T * a * Hd, "qkv_bwd": 4 * T * Hd * q}
+        return {"pre": 2 * T * Hd * q + 2 * T * a * Hd, "gateup": 4 * T * Hd * I, "down": 2 * T * I * Hd,
+                "mlp_bwd": 2 * (2 * T * Hd * I) + 2 * (4 * T * Hd * I), "attn_bwd": 4 * T * a * Hd + 4 * T * Hd * q}
+
+    def _side(self):
+        """Context running calls on the second stream (or the main one)."""
+        if self.s2 is None:
+            return _NullCtx(), self.ws
+        self.s2.wait_stream(torch.cuda.current_stream(self.s2.device))
+        return torch.cuda.stream(self.s2), self.ws2
+
+    def _join(self):
+        if self.s2 is not None:
+            torch.cuda.current_stream(self.s2.device).wait_stream(self.s2)
 
     # ------------------------------------------------------------------ forward
     def forward(self, x0, A, pos, mark=None):
         s, w = self.s, self.w
         mark = mark or (lambda name: None)
-        fold_gamma(w["Wqkv"], w["gamma_attn"], out=self.Wqkv_f)
+        ctx, ws2 = self._side()
+        with ctx:   # QKV branch: independent of the O-projection
+            fold_gamma(w["Wqkv"], w["gamma_attn"], out=self.Wqkv_f)
+            rms_rstd(x0, s.eps, out=self.rstd0)
+            linear_qknorm_rope(x0, self.Wqkv_f, w["gamma_q"], w["gamma_k"], pos, self.cos_sin, s.n_q, s.n_kv,
+                               rstd=self.rstd0, eps=s.eps, head_dim=s.head_dim, out=self.fwd, ws=ws2)
         fold_gamma(w["Wg"], w["gamma_mlp"], out=self.Wg_f)
         fold_gamma(w["Wu"], w["gamma_mlp"], out=self.Wu_f)
-        mark("fold")
-        rms_rstd(x0, s.eps, out=self.rstd0)
-        mark("rstd0")
-        linear_qknorm_rope(x0, self.Wqkv_f, w["gamma_q"], w["gamma_k"], pos, self.cos_sin, s.n_q, s.n_kv,
-                           rstd=self.rstd0, eps=s.eps, head_dim=s.head_dim, out=self.fwd, ws=self.ws)
-        mark("qkv")
         linear_residual(A, w["Wo"], x0, eps=s.eps, Y=self.x1, rstd_out=self.rstd1, ws=self.ws)
-        mark("oproj")
+        self._join()
+        mark("pre")
         linear_swiglu(self.x1, self.Wg_f, self.Wu_f, rstd=self.rstd1, H=self.H, g=self.g, u=self.u, ws=self.ws)
         mark("gateup")
         linear_residual(self.H, w["Wd"], self.x1, Y=self.x2, ws=self.ws)
@@ -113,13 +135,15 @@ class Block:
                           gamma=w["gamma_mlp"], Wgf=self.Wg_f, Wuf=self.Wu_f, dX_resid=dx2, ws=self.ws,
                           out=self.grads_mlp)
         mark("mlp_bwd")
-        linear_residual_bwd(self.dx1, A, w["Wo"], ws=self.ws, out=self.grads_o)
-        mark("oproj_bwd")
+        ctx, ws2 = self._side()
+        with ctx:   # both need only dx1
+            linear_residual_bwd(self.dx1, A, w["Wo"], ws=ws2, out=self.grads_o)
         linear_qknorm_rope_bwd(dQ, dK, dV, self.fwd["qk_save"], self.fwd["V"], w["gamma_q"], w["gamma_k"], pos,
                                self.cos_sin, s.n_q, s.n_kv, x0, w["Wqkv"], Wf_qkv=self.Wqkv_f, rstd=self.rstd0,
                                gamma_in=w["gamma_attn"], dX_resid=self.dx1, eps=s.eps, head_dim=s.head_dim,
                                ws=self.ws, out=self.grads_qkv)
-        mark("qkv_bwd")
+        self._join()
+        mark("attn_bwd")
         return {"dx0": self.grads_qkv["dX"], "dA": self.grads_o["dX"], "dx1": self.dx1,
                 "dWqkv": self.grads_qkv["dW"], "dWo": self.grads_o["dW"], "dWg": self.grads_mlp["dWg"],
                 "dWu": self.grads_mlp["dWu"], "dWd": self.grads_mlp["dWd"],
@@ -129,6 +153,14 @@ class Block:
     def step(self, x0, A, pos, dx2, dQ, dK, dV, mark=None):
         self.forward(x0, A, pos, mark)
         return self.backward(x0, A, pos, dx2, dQ, dK, dV, mark)
+
+
+class _NullCtx:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *a):
+        return False
 
 
 class LinearCE:
