@@ -48,6 +48,7 @@ __all__ = [
     "linear_cross_entropy_fwd", "linear_cross_entropy_bwd",
     "block_fwd", "block_bwd", "block_flops", "mlp_flops", "ce_flops",
     "gemm_epilogue_plain",
+    "rmsnorm_linear_cross_entropy_fwd", "rmsnorm_linear_cross_entropy_bwd",
 ]
 
 
@@ -297,6 +298,29 @@ def linear_cross_entropy_bwd(X, W, labels, ignore_index=-100, dloss=1.0):
         dZ[rows, labels[rows]] -= 1.0
         dZ *= dloss / n_valid
     return {"dX": dZ @ W, "dW": dZ.T @ X, "dZ": dZ}
+
+
+# ---------------------------------------------------------------------------
+# final RMSNorm -> LM head -> cross-entropy (third site of the pattern)
+# ---------------------------------------------------------------------------
+
+def rmsnorm_linear_cross_entropy_fwd(X, gamma, W, labels, eps, ignore_index=-100):
+    """z = RMSNorm(X, gamma) W^T followed by the mean cross-entropy.
+    [P1] §3.2.1, third item of the pattern (final MLP down-projection ->
+    residual -> final RMSNorm -> language-model head).  Returns the dict of
+    linear_cross_entropy_fwd plus the row factor r."""
+    f = linear_cross_entropy_fwd(rmsnorm(X, gamma, eps), W, labels, ignore_index)
+    f["rstd"] = rms_inv(X, eps)
+    return f
+
+
+def rmsnorm_linear_cross_entropy_bwd(X, gamma, W, labels, eps, ignore_index=-100, dloss=1.0):
+    """Backward (chain rule): the cross-entropy backward on a = RMSNorm(X),
+    then the RMSNorm backward of its dX.  Returns dX, dW, dgamma."""
+    a = rmsnorm(X, gamma, eps)
+    b = linear_cross_entropy_bwd(a, W, labels, ignore_index, dloss)
+    dX, dgamma = rmsnorm_bwd(X, gamma, eps, b["dX"])
+    return {"dX": dX, "dW": b["dW"], "dgamma": dgamma}
 
 
 # ---------------------------------------------------------------------------

@@ -392,7 +392,36 @@ def check_gemm_epilogue_bruteforce(o):
     return max(_rel(got, ref), _rel(plain, ref2))
 
 
+def check_rmsnorm_ce_library(o):
+    """gamma = 1: the loss equals torch's cross_entropy of torch rms_norm's
+    output times W^T (float64), ignore_index = -100."""
+    r = RNG(17)
+    X = r.standard_normal((5, 8)) * 2
+    W = r.standard_normal((9, 8))
+    lab = np.array([0, 8, -100, 4, 2])
+    f = o.rmsnorm_linear_cross_entropy_fwd(X, np.ones(8), W, lab, 1e-6)
+    a = F.rms_norm(torch.from_numpy(X), (8,), eps=1e-6)
+    ref = F.cross_entropy(F.linear(a, torch.from_numpy(W)), torch.from_numpy(lab).long(), ignore_index=-100).item()
+    return max(abs(f["loss"] - ref) / abs(ref), _rel(f["rstd"], 1 / np.sqrt((X ** 2).mean(axis=1) + 1e-6)))
+
+
+def check_rmsnorm_ce_grad(o):
+    """FD gradients of the mean loss w.r.t. X, W and gamma."""
+    r = RNG(18)
+    X = r.standard_normal((4, 6))
+    W = r.standard_normal((7, 6))
+    g = 1 + 0.1 * r.standard_normal(6)
+    lab = np.array([1, -100, 6, 0])
+    b = o.rmsnorm_linear_cross_entropy_bwd(X, g, W, lab, 1e-6)
+
+    def L():
+        return o.rmsnorm_linear_cross_entropy_fwd(X, g, W, lab, 1e-6)["loss"]
+    return max(_rel(b["dX"], _fd_grad(L, X)), _rel(b["dW"], _fd_grad(L, W)), _rel(b["dgamma"], _fd_grad(L, g)))
+
+
 ALL_CHECKS = {
+    "rmsnorm_ce_library": (check_rmsnorm_ce_library, 1e-12),
+    "rmsnorm_ce_grad": (check_rmsnorm_ce_grad, 1e-7),
     "gemm_epilogue_bruteforce": (check_gemm_epilogue_bruteforce, 1e-13),
     "reparam_identity": (check_reparam_identity, 1e-13),
     "rmsnorm_library": (check_rmsnorm_library, 1e-13),

@@ -138,7 +138,16 @@ def _mut_gemm_transposed_scale(m):
     m.gemm_epilogue_plain = bad
 
 
+def _mut_rmsnorm_ce_skip_norm_bwd(m):
+    def bad(X, gamma, W, labels, eps, ignore_index=-100, dloss=1.0):
+        a = m.rmsnorm(X, gamma, eps)
+        b = m.linear_cross_entropy_bwd(a, W, labels, ignore_index, dloss)
+        return {"dX": b["dX"] * gamma, "dW": b["dW"], "dgamma": (b["dX"] * a).sum(axis=0)}
+    m.rmsnorm_linear_cross_entropy_bwd = bad
+
+
 MUTANTS = {
+    "rmsnorm_ce_skips_norm_backward": _mut_rmsnorm_ce_skip_norm_bwd,
     "gemm_coef_sign": _mut_gemm_transposed_scale,
     "rms_eps_outside_root": _mut_rms_eps_outside,
     "rmsnorm_bwd_drop_mean": _mut_rmsnorm_bwd_drop_mean,
