@@ -25,6 +25,7 @@ __all__ = [
     "rmsnorm_linear", "rmsnorm_linear_bwd", "linear_residual", "linear_residual_bwd",
     "linear_swiglu", "linear_swiglu_bwd", "linear_qknorm_rope", "linear_qknorm_rope_bwd",
     "linear_cross_entropy", "linear_cross_entropy_bwd", "linear_cross_entropy_noalloc", "workspace",
+    "rmsnorm_linear_cross_entropy", "rmsnorm_linear_cross_entropy_bwd", "rms_rstd",
     "MAP_NONE", "MAP_SWIGLU", "MAP_DSWIGLU", "MAP_QKNORM_ROPE", "MAP_CE_LSE",
     "MAP_CE_DLOGITS", "MAP_COLDOT", "K_MAJOR", "MN_MAJOR",
 ]
@@ -73,6 +74,12 @@ _SIGS = {
                                     + [_I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_cross_entropy_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_cross_entropy": ([_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_rmsnorm_linear_cross_entropy_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_rmsnorm_linear_cross_entropy": ([_P, _P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P],
+                                          ctypes.c_int),
+    "coda_rmsnorm_linear_cross_entropy_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_rmsnorm_linear_cross_entropy_bwd": ([_P, _P, _P, _P, _P, _P, _I32, _P, _P, _F, _P, _P, _P, _P,
+                                               _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_noalloc_scratch_bytes": ([], _SZ),
     "coda_linear_cross_entropy_noalloc": ([_P, _P, _P, _I32, _P, _P, _P, _P, _I64, _I64, _I64, _P], ctypes.c_int),
     "coda_linear_cross_entropy_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
@@ -385,6 +392,44 @@ def linear_cross_entropy(X, W, labels, ignore_index=-100, out=None, ws=None, str
         _bf(X, "X"), _bf(W, "W"), _i32(labels, "labels"), int(ignore_index), _f32(out["loss"], "loss"),
         _f32(out["lse"], "lse"), _i32(out["n_valid"], "n_valid"), M, V, K, _ptr(ws), ws.numel(),
         _stream(stream)))
+    out["ws"] = ws
+    return out
+
+
+def rmsnorm_linear_cross_entropy(X, rstd, Wf, labels, ignore_index=-100, out=None, ws=None, stream=None):
+    """Final RMSNorm folded into the LM head: CE of z = rstd ⊙ (X Wf^T)."""
+    lib = load()
+    M, K = X.shape
+    V = Wf.shape[0]
+    dev = X.device
+    if out is None:
+        out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
+               "lse": torch.empty(M, dtype=torch.float32, device=dev),
+               "n_valid": torch.empty(1, dtype=torch.int32, device=dev)}
+    ws = _ws(ws, lib.coda_rmsnorm_linear_cross_entropy_workspace_size(M, V, K), dev)
+    _check("coda_rmsnorm_linear_cross_entropy", lib.coda_rmsnorm_linear_cross_entropy(
+        _bf(X, "X"), _f32(rstd, "rstd"), _bf(Wf, "Wf"), _i32(labels, "labels"), int(ignore_index),
+        _f32(out["loss"], "loss"), _f32(out["lse"], "lse"), _i32(out["n_valid"], "n_valid"), M, V, K,
+        _ptr(ws), ws.numel(), _stream(stream)))
+    out["ws"] = ws
+    return out
+
+
+def rmsnorm_linear_cross_entropy_bwd(X, rstd, gamma, W, Wf, labels, lse, n_valid, dloss=1.0, ignore_index=-100,
+                                     dX_resid=None, out=None, ws=None, stream=None):
+    lib = load()
+    M, K = X.shape
+    V = W.shape[0]
+    dev = X.device
+    if out is None:
+        out = {"dX": torch.empty_like(X), "dW": torch.empty_like(W),
+               "dgamma": torch.empty(K, dtype=torch.float32, device=dev)}
+    ws = _ws(ws, lib.coda_rmsnorm_linear_cross_entropy_bwd_workspace_size(M, V, K), dev)
+    _check("coda_rmsnorm_linear_cross_entropy_bwd", lib.coda_rmsnorm_linear_cross_entropy_bwd(
+        _bf(X, "X"), _f32(rstd, "rstd"), _f32(gamma, "gamma"), _bf(W, "W"), _bf(Wf, "Wf"),
+        _i32(labels, "labels"), int(ignore_index), _f32(lse, "lse"), _i32(n_valid, "n_valid"), float(dloss),
+        _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"), _bf(out["dW"], "dW"), _f32(out["dgamma"], "dgamma"),
+        M, V, K, _ptr(ws), ws.numel(), _stream(stream)))
     out["ws"] = ws
     return out
 

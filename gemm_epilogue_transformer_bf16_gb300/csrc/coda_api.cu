@@ -1026,9 +1026,13 @@ size_t coda_linear_cross_entropy_workspace_size(int64_t M, int64_t V, int64_t) {
   return c.off;
 }
 
-int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int32_t* labels, int32_t ignore_index,
-                              float* loss_mean, float* lse, int32_t* n_valid, int64_t M, int64_t V, int64_t K,
-                              void* ws, size_t ws_bytes, coda_stream stream) {
+}  // extern "C"
+
+// Linear + cross-entropy forward; `rstd` (optional) scales each row's logits
+// (the final RMSNorm folded into the head).
+static int ce_forward(const coda_bf16* X, const coda_bf16* W, const int32_t* labels, int32_t ignore_index,
+                      const float* rstd, float* loss_mean, float* lse, int32_t* n_valid, int64_t M, int64_t V,
+                      int64_t K, void* ws, size_t ws_bytes, coda_stream stream) {
   CK(dims_ok(M, V, K));
   CK(ws_ok(ws, ws_bytes, coda_linear_cross_entropy_workspace_size(M, V, K)));
   CK(req(loss_mean));
@@ -1058,6 +1062,7 @@ int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int3
     p.N = V;
     p.K = K;
     p.n_per_unit = CE_TILES_PER_UNIT;
+    p.e.row_scale = rstd;
     p.e.labels = labels;
     p.e.target_logit = target;
     p.e.partials = reinterpret_cast<float*>(part);
@@ -1067,6 +1072,14 @@ int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int3
   CU(coda::launch_ce_combine(part, M, nch, target, labels, ignore_index, M, V, lse, bl, bc, nblk, loss_mean, n_valid,
                              status, s));
   return CODA_OK;
+}
+
+extern "C" {
+
+int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int32_t* labels, int32_t ignore_index,
+                              float* loss_mean, float* lse, int32_t* n_valid, int64_t M, int64_t V, int64_t K,
+                              void* ws, size_t ws_bytes, coda_stream stream) {
+  return ce_forward(X, W, labels, ignore_index, nullptr, loss_mean, lse, n_valid, M, V, K, ws, ws_bytes, stream);
 }
 
 size_t coda_linear_cross_entropy_bwd_workspace_size(int64_t M, int64_t V, int64_t) {
@@ -1108,8 +1121,8 @@ int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const 
   int32_t* idx = w.take<int32_t>(M);
   int* status = static_cast<int*>(ws);
   cudaStream_t s = S(stream);
-  CU(coda::launch_ce_onehot_prep(labels, ignore_index, M, V, n_valid, dloss, wrow, lrow, counts, cursor, off, idx,
-                                 s));
+  CU(coda::launch_ce_onehot_prep(labels, ignore_index, M, V, n_valid, dloss, nullptr, wrow, lrow, counts, cursor,
+                                 off, idx, s));
   {  // dZ = softmax * dloss / n_valid (the one-hot part is applied exactly below)
     Plan p;
     p.kind = coda::EpiKind::CeDlogits;
@@ -1167,6 +1180,148 @@ int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const 
     p.e.csr_w = wrow;
     CK(run(p, status, s));
   }
+  return CODA_OK;
+}
+
+
+// ------------------------------------------------------------------ final RMSNorm -> LM head -> CE
+size_t coda_rmsnorm_linear_cross_entropy_workspace_size(int64_t M, int64_t V, int64_t K) {
+  return coda_linear_cross_entropy_workspace_size(M, V, K);
+}
+
+int coda_rmsnorm_linear_cross_entropy(const coda_bf16* X, const float* rstd, const coda_bf16* Wf,
+                                      const int32_t* labels, int32_t ignore_index, float* loss_mean, float* lse,
+                                      int32_t* n_valid, int64_t M, int64_t V, int64_t K, void* ws, size_t ws_bytes,
+                                      coda_stream stream) {
+  if (M > 0) CK(req(rstd));
+  return ce_forward(X, Wf, labels, ignore_index, rstd, loss_mean, lse, n_valid, M, V, K, ws, ws_bytes, stream);
+}
+
+size_t coda_rmsnorm_linear_cross_entropy_bwd_workspace_size(int64_t M, int64_t V, int64_t K) {
+  SizeCursor c;
+  c.take<__nv_bfloat16>(static_cast<size_t>(M) * V);           // G' = r * softmax * w
+  c.take<float>(M);                                             // r_i w_i
+  c.take<int32_t>(M);                                           // label of valid rows
+  c.take<int32_t>(V);                                           // counts
+  c.take<int32_t>(V);                                           // cursors
+  c.take<int32_t>(V + 1);                                       // CSR offsets
+  c.take<int32_t>(M);                                           // CSR token indices
+  c.take<float>(static_cast<size_t>(cdiv(V, BN)) * M);          // row partials sum p z
+  c.take<float>(M);                                             // target logits
+  c.take<float>(M);                                             // RMSNorm coefficient c
+  c.take<float>(static_cast<size_t>(4 * cdiv(V, 128)) * K);     // dgamma partials
+  return c.off;
+}
+
+int coda_rmsnorm_linear_cross_entropy_bwd(const coda_bf16* X, const float* rstd, const float* gamma,
+                                          const coda_bf16* W, const coda_bf16* Wf, const int32_t* labels,
+                                          int32_t ignore_index, const float* lse, const int32_t* n_valid, float dloss,
+                                          const coda_bf16* dX_resid, coda_bf16* dX, coda_bf16* dW, float* dgamma,
+                                          int64_t M, int64_t V, int64_t K, void* ws, size_t ws_bytes,
+                                          coda_stream stream) {
+  CK(dims_ok(M, V, K));
+  CK(ws_ok(ws, ws_bytes, coda_rmsnorm_linear_cross_entropy_bwd_workspace_size(M, V, K)));
+  if (V == 0) return CODA_ERR_INVALID_ARG;
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)X, (const void*)rstd, (const void*)gamma, (const void*)W, (const void*)Wf,
+                        (const void*)labels, (const void*)lse, (const void*)n_valid, (const void*)dX,
+                        (const void*)dW, (const void*)dgamma})
+    CK(req(q));
+  for (const void* q : {(const void*)X, (const void*)gamma, (const void*)W, (const void*)Wf, (const void*)dX_resid,
+                        (const void*)dX, (const void*)dW})
+    CK(al(q));
+  WsCursor w(ws);
+  __nv_bfloat16* Gp = w.take<__nv_bfloat16>(static_cast<size_t>(M) * V);
+  float* rw = w.take<float>(M);
+  int32_t* lrow = w.take<int32_t>(M);
+  int32_t* counts = w.take<int32_t>(V);
+  int32_t* cursor = w.take<int32_t>(V);
+  int32_t* off = w.take<int32_t>(V + 1);
+  int32_t* idx = w.take<int32_t>(M);
+  const int ntile = static_cast<int>(cdiv(V, BN));
+  float* pz = w.take<float>(static_cast<size_t>(ntile) * M);
+  float* target = w.take<float>(M);
+  float* coef = w.take<float>(M);
+  const int64_t nmb = cdiv(V, 128);
+  float* dgp = w.take<float>(static_cast<size_t>(4 * nmb) * K);
+  int* status = static_cast<int*>(ws);
+  cudaStream_t s = S(stream);
+  CU(coda::launch_ce_onehot_prep(labels, ignore_index, M, V, n_valid, dloss, rstd, rw, lrow, counts, cursor, off,
+                                 idx, s));
+  {  // G' = r * softmax(r * X Wf^T) * w; row partials sum p z; target logits
+    Plan p;
+    p.kind = coda::EpiKind::CeDlogits;
+    p.A = X;
+    p.lda = K;
+    p.B = Wf;
+    p.ldb = K;
+    p.M = M;
+    p.N = V;
+    p.K = K;
+    p.e.D = Gp;
+    p.e.ldd = V;
+    p.e.row_scale = rstd;
+    p.e.labels = labels;
+    p.e.ignore_index = ignore_index;
+    p.e.lse = lse;
+    p.e.n_valid = n_valid;
+    p.e.dloss = dloss;
+    p.e.partials = pz;
+    p.e.ld_part = M;
+    p.e.target_logit = target;
+    CK(run(p, status, s));
+  }
+  CU(coda::launch_ce_norm_coef(pz, M, ntile, target, rstd, rw, M, 1.f / static_cast<float>(K), coef, s));
+  {  // dX = G' Wf - r_i w_i Wf[y_i] - c_i X_i (+ dX_resid)
+    Plan p;
+    p.A = Gp;
+    p.lda = V;
+    p.B = Wf;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.M = M;
+    p.N = K;
+    p.K = V;
+    p.e.D = dX;
+    p.e.ldd = K;
+    p.e.aux0 = BF(dX_resid);
+    p.e.ld_aux0 = K;
+    p.e.row_coef = rw;
+    p.e.aux1 = BF(Wf);
+    p.e.ld_aux1 = K;
+    p.e.gather_rows = lrow;
+    p.e.row_coef2 = coef;
+    p.e.aux3 = BF(X);
+    p.e.ld_aux3 = K;
+    CK(run(p, status, s));
+  }
+  {  // dW = (G'^T X - one-hot rows) diag(gamma); dgamma partials
+    Plan p;
+    p.kind = coda::EpiKind::ColDot;
+    p.A = Gp;
+    p.lda = V;
+    p.a_mn = 1;
+    p.B = X;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.M = V;
+    p.N = K;
+    p.K = M;
+    p.e.D = dW;
+    p.e.ldd = K;
+    p.e.col_scale = gamma;
+    p.e.aux0 = BF(W);
+    p.e.ld_aux0 = K;
+    p.e.partials = dgp;
+    p.e.ld_part = K;
+    p.e.aux2 = BF(X);
+    p.e.ld_aux2 = K;
+    p.e.csr_off = off;
+    p.e.csr_idx = idx;
+    p.e.csr_w = rw;
+    CK(run(p, status, s));
+  }
+  CU(coda::launch_colsum(dgp, 4 * nmb, K, K, dgamma, s));
   return CODA_OK;
 }
 

@@ -240,15 +240,15 @@ cudaError_t launch_ce_combine(const float2* part, int64_t ld, int nchunks, const
 // label: histogram, exclusive scan, scatter, then each bucket sorted by token
 // index so that the epilogue's fp32 sums have a fixed order).
 __global__ void ce_prep_kernel(const int32_t* __restrict__ labels, int32_t ignore, int64_t M, int64_t V,
-                               const int32_t* __restrict__ n_valid, float dloss, float* wrow, int32_t* lrow,
-                               int32_t* counts) {
+                               const int32_t* __restrict__ n_valid, float dloss, const float* __restrict__ rstd,
+                               float* wrow, int32_t* lrow, int32_t* counts) {
   const int32_t nv = *n_valid;
   const float w = nv > 0 ? dloss / static_cast<float>(nv) : 0.f;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int32_t y = labels[i];
     const bool valid = y != ignore && y >= 0 && y < V && nv > 0;
-    wrow[i] = valid ? w : 0.f;
+    wrow[i] = valid ? (rstd ? w * rstd[i] : w) : 0.f;
     lrow[i] = valid ? y : -1;
     if (valid) atomicAdd(&counts[y], 1);
   }
@@ -304,13 +304,13 @@ __global__ void ce_sort_buckets_kernel(const int32_t* __restrict__ off, int64_t 
 }
 
 cudaError_t launch_ce_onehot_prep(const int32_t* labels, int32_t ignore, int64_t M, int64_t V,
-                                  const int32_t* n_valid, float dloss, float* wrow, int32_t* lrow,
+                                  const int32_t* n_valid, float dloss, const float* rstd, float* wrow, int32_t* lrow,
                                   int32_t* counts, int32_t* cursor, int32_t* off, int32_t* idx, cudaStream_t s) {
   cudaError_t e;
   if ((e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * V, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(cursor, 0, sizeof(int32_t) * V, s)) != cudaSuccess) return e;
   const unsigned mb = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((M + 255) / 256, 1024)));
-  ce_prep_kernel<<<mb, 256, 0, s>>>(labels, ignore, M, V, n_valid, dloss, wrow, lrow, counts);
+  ce_prep_kernel<<<mb, 256, 0, s>>>(labels, ignore, M, V, n_valid, dloss, rstd, wrow, lrow, counts);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   scan_counts_kernel<<<1, 1024, 0, s>>>(counts, V, off);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -318,6 +318,34 @@ cudaError_t launch_ce_onehot_prep(const int32_t* labels, int32_t ignore, int64_t
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const unsigned vb = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((V + 255) / 256, 1024)));
   ce_sort_buckets_kernel<<<vb, 256, 0, s>>>(off, V, idx);
+  return cudaGetLastError();
+}
+
+// RMSNorm-backward coefficient of a row-scaled cross-entropy head:
+//   c_i = r_i * (r_i w_i) * (sum_t pz[t][i] - z_{i,y_i}) / K,
+// i.e. r_i^2 * sum_j dZ_ij z_ij / K with dZ = (softmax - onehot) * w_i.
+// Rows with w_i = 0 (ignored labels) get 0 without reading their target.
+__global__ void ce_norm_coef_kernel(const float* __restrict__ pz, int64_t ld, int nparts,
+                                    const float* __restrict__ target, const float* __restrict__ rstd,
+                                    const float* __restrict__ rw, int64_t M, float inv_k, float* coef) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float w = rw[i];
+    if (w == 0.f) {
+      coef[i] = 0.f;
+      continue;
+    }
+    float s = 0.f;
+    for (int t = 0; t < nparts; ++t) s += pz[t * ld + i];
+    coef[i] = rstd[i] * w * (s - target[i]) * inv_k;
+  }
+}
+
+cudaError_t launch_ce_norm_coef(const float* pz, int64_t ld, int nparts, const float* target, const float* rstd,
+                                const float* rw, int64_t M, float inv_k, float* coef, cudaStream_t s) {
+  const int64_t blocks = std::min<int64_t>((M + 255) / 256, 4096);
+  ce_norm_coef_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(pz, ld, nparts, target,
+                                                                                          rstd, rw, M, inv_k, coef);
   return cudaGetLastError();
 }
 

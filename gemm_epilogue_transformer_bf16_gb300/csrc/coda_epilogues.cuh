@@ -30,8 +30,8 @@ __device__ __forceinline__ void store_f32x8(float* p, const float* v) {
 }
 
 // ---------------------------------------------------------------------------
-// PLAIN:  D = rs_i * cs_j * acc + aux0 - coef_i * aux1[g_i] (+ D if beta)
-//             - sum_{t in csr(i)} w_t * aux2[t]
+// PLAIN:  D = rs_i * cs_j * acc + aux0 - coef_i * aux1[g_i] - coef2_i * aux3
+//             - sum_{t in csr(i)} w_t * aux2[t]  (+ D if beta)
 // optional row partial  sum_j D_ij^2  (of the stored, rounded values).
 // Covers: plain store, residual add, RMSNorm row-scale (+ residual),
 // accumulate, the residual + partial-RMS epilogue, dX - c*X of the
@@ -48,6 +48,7 @@ struct EpiPlain {
     const bool rv = row < t.M;
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
     const float rc = (e.row_coef && rv) ? e.row_coef[row] : 0.f;
+    const float rc2 = (e.row_coef2 && rv) ? e.row_coef2[row] : 0.f;
     const int64_t arow = e.gather_rows ? (rv ? e.gather_rows[row] : -1) : row;
     int cb0 = 0, cb1 = 0;
     if (e.csr_off && rv) {
@@ -87,6 +88,12 @@ struct EpiPlain {
               load_bf16x8(e.aux1 + arow * e.ld_aux1 + cc, r8);
 #pragma unroll
               for (int i = 0; i < 8; ++i) x[i] -= rc * r8[i];
+            }
+            if (e.row_coef2) {
+              float r8[8];
+              load_bf16x8(e.aux3 + static_cast<int64_t>(row) * e.ld_aux3 + cc, r8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[i] -= rc2 * r8[i];
             }
             for (int j = cb0; j < cb1; ++j) {
               const int32_t t2 = e.csr_idx[j];
@@ -240,9 +247,11 @@ struct EpiDSwiglu {
 
 // ---------------------------------------------------------------------------
 // COLDOT (weight-gradient epilogue of the RMSNorm-reparameterised backward):
-// the accumulator is dW'[n, k] (rows = weight output features);
-//   D = cs_k * acc                (dW = dW' diag(gamma))
-//   column partial  sum_n aux0[n, k] * acc[n, k]   (dgamma contribution)
+// the accumulator is dW'[n, k] (rows = weight output features), optionally
+// minus the rows of aux2 listed for row n in the CSR (the exact one-hot term
+// of a cross-entropy head):  v = acc - sum_{t in csr(n)} w_t aux2[t, k];
+//   D = cs_k * v                  (dW = dW' diag(gamma))
+//   column partial  sum_n aux0[n, k] * v[n, k]     (dgamma contribution)
 // written per (m block, warp) to partials[(mb*4 + warp) * ld_part + k].
 // ---------------------------------------------------------------------------
 template <int BN>
@@ -255,6 +264,11 @@ struct EpiColDot {
     const bool rv = row < t.M;
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;
+    int cb0 = 0, cb1 = 0;
+    if (e.csr_off && rv) {
+      cb0 = e.csr_off[row];
+      cb1 = e.csr_off[row + 1];
+    }
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int col0 = t.nb * BN + c;
@@ -272,6 +286,14 @@ struct EpiColDot {
           const int cc = col0 + g * 8;
           if (cc < t.N) {
             float w8[8], s8[8], x[8];
+            for (int j = cb0; j < cb1; ++j) {
+              const int32_t t2 = e.csr_idx[j];
+              const float w2 = e.csr_w[t2];
+              float r8[8];
+              load_bf16x8(e.aux2 + static_cast<int64_t>(t2) * e.ld_aux2 + cc, r8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[g * 8 + i] -= w2 * r8[i];
+            }
             load_bf16x8(e.aux0 + off * e.ld_aux0 + cc, w8);
             if (e.col_scale) load_f32x8(e.col_scale + cc, s8);
 #pragma unroll
@@ -351,6 +373,7 @@ struct EpiCeLse {
   }
   static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t, float*) {
     const bool rv = t.row < t.M;
+    const float rs = (e.row_scale && rv) ? e.row_scale[t.row] : 1.f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int col0 = t.nb * BN + c;
@@ -359,6 +382,10 @@ struct EpiCeLse {
       __syncwarp();
       tmem_ld32(t.taddr + c, z);
       if (rv) {
+        if (e.row_scale) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] *= rs;
+        }
         const int nvalid = min(32, t.N - col0);
         float mc = -INFINITY;
 #pragma unroll
@@ -393,6 +420,11 @@ struct EpiCeLse {
 //   named cross-entropy backward instead applies it exactly in fp32 in the
 //   epilogues of the dX and dW GEMMs, so the large label element is never
 //   rounded to bf16.
+// With a row scale rs (the final RMSNorm folded into the LM head, z = rs*acc)
+// the stored value is rs * dZ (the row-scaled gradient G' of the
+// reparameterised backward), and for the RMSNorm backward coefficient the
+// epilogue also emits row partials sum_j p_ij z_ij (partials[nb][row]) and
+// the target logit z_{i,y_i} (target_logit).
 // ---------------------------------------------------------------------------
 template <int BN>
 struct EpiCeDlogits {
@@ -412,7 +444,10 @@ struct EpiCeDlogits {
       if (!valid) lab = -1;
       lse = e.lse[row];
     }
+    const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
+    const float ws = w * rs;
     const float lb = lse * LOG2E;
+    float pz = 0.f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int col0 = t.nb * BN + c;
@@ -429,14 +464,18 @@ struct EpiCeDlogits {
             float x[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float p = exp2f(fmaf(z[g * 8 + i], LOG2E, -lb));
-              x[i] = (p - (e.onehot && cc + i == lab ? 1.f : 0.f)) * w;
+              const float zz = z[g * 8 + i] * rs;
+              const float p = exp2f(fmaf(zz, LOG2E, -lb));
+              x[i] = (p - (e.onehot && cc + i == lab ? 1.f : 0.f)) * ws;
+              pz += p * zz;
+              if (e.target_logit && cc + i == lab) e.target_logit[row] = zz;
             }
             store_bf16x8(d + cc, x, e.st_stream);
           }
         }
       }
     }
+    if (e.partials && rv) e.partials[static_cast<int64_t>(t.nb) * e.ld_part + row] = pz;
   }
 };
 

@@ -77,6 +77,9 @@ struct EpiArgs {
   const int32_t* csr_off;       // [M+1] per output row: range of csr_idx
   const int32_t* csr_idx;       // aux2 row indices
   const float* csr_w;           // weight of each aux2 row
+  const float* row_coef2;       // PLAIN: D -= row_coef2_i * aux3[i, j]
+  const __nv_bfloat16* aux3;
+  int64_t ld_aux3;
   __nv_bfloat16* out1;
   int64_t ld_out1;
   __nv_bfloat16* out2;

@@ -340,6 +340,40 @@ int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int3
                               int32_t ignore_index, float* loss_mean, float* lse, int32_t* n_valid,
                               int64_t M, int64_t V, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
 
+/* ------------------------------------------------------------------------
+ * Final RMSNorm -> LM head -> cross-entropy ("CODA" §3.2.1, third site of
+ * the GEMM-residual-RMSNorm-GEMM pattern: final down-projection -> residual
+ * -> final RMSNorm -> language-model head)
+ *
+ *   z = r ⊙ (X Wf^T),  Wf = W diag(gamma) (coda_fold_gamma),
+ *   which equals RMSNorm(X, gamma) W^T; then the cross-entropy of
+ *   coda_linear_cross_entropy.  rstd [M] comes from the producing epilogue
+ *   (coda_linear_residual's rstd_out) or coda_rms_rstd.  The workspace and the
+ *   outputs are those of coda_linear_cross_entropy (lse is that of z).
+ * ---------------------------------------------------------------------- */
+size_t coda_rmsnorm_linear_cross_entropy_workspace_size(int64_t M, int64_t V, int64_t K);
+int coda_rmsnorm_linear_cross_entropy(const coda_bf16* X, const float* rstd, const coda_bf16* Wf,
+                                      const int32_t* labels, int32_t ignore_index, float* loss_mean, float* lse,
+                                      int32_t* n_valid, int64_t M, int64_t V, int64_t K, void* ws, size_t ws_bytes,
+                                      coda_stream stream);
+
+/* Backward for upstream gradient dloss of the mean loss.  With
+ * G = dZ = (softmax(z) - onehot) * dloss / n_valid and G' = r ⊙ G:
+ *   dX = G' Wf - c ⊙ X (+ dX_resid),  c_i = r_i^2 sum_v G_iv z_iv / K,
+ *   dW = (G'^T X) diag(gamma),  dgamma_k = sum_v W_vk (G'^T X)_vk.
+ * The one-hot part of G' is applied exactly in fp32 (row gather of Wf for dX,
+ * a label -> token list for dW); only r * softmax * w is staged in bf16.
+ * Inputs: X [M,K] (the un-normalised residual stream), rstd [M], gamma [K],
+ * W and Wf [V,K], labels [M], lse [M] and n_valid from the forward,
+ * dX_resid [M,K] or NULL.  Outputs: dX [M,K], dW [V,K] bf16, dgamma [K] fp32. */
+size_t coda_rmsnorm_linear_cross_entropy_bwd_workspace_size(int64_t M, int64_t V, int64_t K);
+int coda_rmsnorm_linear_cross_entropy_bwd(const coda_bf16* X, const float* rstd, const float* gamma,
+                                          const coda_bf16* W, const coda_bf16* Wf, const int32_t* labels,
+                                          int32_t ignore_index, const float* lse, const int32_t* n_valid, float dloss,
+                                          const coda_bf16* dX_resid, coda_bf16* dX, coda_bf16* dW, float* dgamma,
+                                          int64_t M, int64_t V, int64_t K, void* ws, size_t ws_bytes,
+                                          coda_stream stream);
+
 /* Variant of coda_linear_cross_entropy that allocates nothing and takes no
  * workspace, for callers that cannot obtain device memory: a plugin or
  * callback inside a host application that owns all device memory and passes

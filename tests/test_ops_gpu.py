@@ -166,3 +166,34 @@ def test_block_fwd_bwd(coda, shape):
     for k in ("dx0", "dA", "dx1", "dWqkv", "dWo", "dWg", "dWu", "dWd", "dgamma_attn", "dgamma_mlp",
               "dgamma_q", "dgamma_k"):
         assert_bf16(g[k], rb[k], k)
+
+
+# ---------------------------------------------------------------- final RMSNorm -> LM head -> CE
+@pytest.mark.parametrize("shape", [synth.CeShape(512, 256, 4000), synth.CeShape(300, 136, 8200)])
+def test_rmsnorm_linear_cross_entropy(coda, shape):
+    t = synth.make_ce(shape, seed=0)
+    lab = t["labels"].clone()
+    lab[1] = 0
+    lab[2] = shape.vocab - 1
+    t["labels"] = lab
+    t["gamma"] = synth.gain_f32(shape.hidden, 9)
+    t["R"] = synth.randn_bf16((shape.tokens, shape.hidden), 1.0, 10)
+    d, o = dev(t), f64(t)
+    labels_np = t["labels"].numpy()
+    eps = 1e-6
+    Wf = coda.fold_gamma(d["W"], d["gamma"])
+    r = coda.rms_rstd(d["X"], eps)
+    out = coda.rmsnorm_linear_cross_entropy(d["X"], r, Wf, d["labels"])
+    f = O.rmsnorm_linear_cross_entropy_fwd(o["X"], o["gamma"], o["W"], labels_np, eps)
+    assert coda.get_status(out["ws"]) == 0
+    assert int(out["n_valid"].item()) == f["n_valid"]
+    assert_f32(r, f["rstd"], "rstd")
+    assert_f32(out["lse"], f["lse"], "lse")
+    assert_f32(out["loss"], [f["loss"]], "loss")
+    g = coda.rmsnorm_linear_cross_entropy_bwd(d["X"], r, d["gamma"], d["W"], Wf, d["labels"], out["lse"],
+                                              out["n_valid"], 1.0, dX_resid=d["R"])
+    b = O.rmsnorm_linear_cross_entropy_bwd(o["X"], o["gamma"], o["W"], labels_np, eps)
+    assert coda.get_status(g["ws"]) == 0
+    assert_bf16(g["dX"], b["dX"] + o["R"], "dX (+ residual gradient)")
+    assert_bf16(g["dW"], b["dW"], "dW")
+    assert_bf16(g["dgamma"], b["dgamma"], "dgamma")
