@@ -49,6 +49,7 @@ __all__ = [
     "block_fwd", "block_bwd", "block_flops", "mlp_flops", "ce_flops",
     "gemm_epilogue_plain",
     "rmsnorm_linear_cross_entropy_fwd", "rmsnorm_linear_cross_entropy_bwd",
+    "sigmoid", "linear_sigmoid_fwd", "linear_sigmoid_bwd",
 ]
 
 
@@ -298,6 +299,36 @@ def linear_cross_entropy_bwd(X, W, labels, ignore_index=-100, dloss=1.0):
         dZ[rows, labels[rows]] -= 1.0
         dZ *= dloss / n_valid
     return {"dX": dZ @ W, "dW": dZ.T @ X, "dZ": dZ}
+
+
+# ---------------------------------------------------------------------------
+# linear + sigmoid (gate)
+# ---------------------------------------------------------------------------
+
+def sigmoid(a):
+    """1 / (1 + exp(-a))."""
+    return 1.0 / (1.0 + np.exp(-np.asarray(a, dtype=np.float64)))
+
+
+def linear_sigmoid_fwd(X, W, Z=None):
+    """y = sigmoid(X W^T), or sigmoid(X W^T) ⊙ Z when a gated tensor Z is given.
+    [P3] names linear_sigmoid among the functional operators; reading: a
+    linear layer with an element-wise sigmoid, optionally gating Z (the
+    §3.1 class-1 element-wise / pairwise map)."""
+    s = sigmoid(X @ W.T)
+    return s if Z is None else s * Z
+
+
+def linear_sigmoid_bwd(X, W, dY, Z=None):
+    """Chain rule: dz = dY ⊙ (Z) ⊙ s (1 - s), dX = dz W, dW = dz^T X, and
+    dZ = dY ⊙ s when Z is given."""
+    s = sigmoid(X @ W.T)
+    g = dY if Z is None else dY * Z
+    dz = g * s * (1.0 - s)
+    out = {"dX": dz @ W, "dW": dz.T @ X}
+    if Z is not None:
+        out["dZ"] = dY * s
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -419,7 +419,32 @@ def check_rmsnorm_ce_grad(o):
     return max(_rel(b["dX"], _fd_grad(L, X)), _rel(b["dW"], _fd_grad(L, W)), _rel(b["dgamma"], _fd_grad(L, g)))
 
 
+def check_linear_sigmoid(o):
+    """sigmoid(0) = 1/2, sigmoid(a) + sigmoid(-a) = 1, vs torch sigmoid/linear
+    in float64, and FD gradients (with and without the gated tensor)."""
+    r = RNG(19)
+    X = r.standard_normal((4, 6))
+    W = r.standard_normal((5, 6))
+    Z = r.standard_normal((4, 5))
+    dY = r.standard_normal((4, 5))
+    a = np.linspace(-6, 6, 13)
+    e = [abs(o.sigmoid(0.0) - 0.5), float(np.max(np.abs(o.sigmoid(a) + o.sigmoid(-a) - 1.0)))]
+    ref = torch.sigmoid(F.linear(torch.from_numpy(X), torch.from_numpy(W))).numpy()
+    e += [_rel(o.linear_sigmoid_fwd(X, W), ref), _rel(o.linear_sigmoid_fwd(X, W, Z), ref * Z)]
+    for gated in (False, True):
+        zz = Z if gated else None
+        b = o.linear_sigmoid_bwd(X, W, dY, zz)
+
+        def L():
+            return float((dY * o.linear_sigmoid_fwd(X, W, zz)).sum())
+        e += [_rel(b["dX"], _fd_grad(L, X)), _rel(b["dW"], _fd_grad(L, W))]
+        if gated:
+            e.append(_rel(b["dZ"], _fd_grad(L, Z)))
+    return max(e)
+
+
 ALL_CHECKS = {
+    "linear_sigmoid": (check_linear_sigmoid, 1e-7),
     "rmsnorm_ce_library": (check_rmsnorm_ce_library, 1e-12),
     "rmsnorm_ce_grad": (check_rmsnorm_ce_grad, 1e-7),
     "gemm_epilogue_bruteforce": (check_gemm_epilogue_bruteforce, 1e-13),

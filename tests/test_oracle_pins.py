@@ -146,7 +146,20 @@ def _mut_rmsnorm_ce_skip_norm_bwd(m):
     m.rmsnorm_linear_cross_entropy_bwd = bad
 
 
+def _mut_sigmoid_bwd_missing_factor(m):
+    def bad(X, W, dY, Z=None):
+        s = m.sigmoid(X @ W.T)
+        g = dY if Z is None else dY * Z
+        dz = g * s
+        out = {"dX": dz @ W, "dW": dz.T @ X}
+        if Z is not None:
+            out["dZ"] = dY * s
+        return out
+    m.linear_sigmoid_bwd = bad
+
+
 MUTANTS = {
+    "sigmoid_bwd_missing_derivative": _mut_sigmoid_bwd_missing_factor,
     "rmsnorm_ce_skips_norm_backward": _mut_rmsnorm_ce_skip_norm_bwd,
     "gemm_coef_sign": _mut_gemm_transposed_scale,
     "rms_eps_outside_root": _mut_rms_eps_outside,
