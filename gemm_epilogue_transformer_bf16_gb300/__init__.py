@@ -26,14 +26,15 @@ __all__ = [
     "linear_swiglu", "linear_swiglu_bwd", "linear_qknorm_rope", "linear_qknorm_rope_bwd",
     "linear_cross_entropy", "linear_cross_entropy_bwd", "linear_cross_entropy_noalloc", "workspace",
     "rmsnorm_linear_cross_entropy", "rmsnorm_linear_cross_entropy_bwd", "rms_rstd",
+    "linear_sigmoid", "linear_sigmoid_bwd",
     "MAP_NONE", "MAP_SWIGLU", "MAP_DSWIGLU", "MAP_QKNORM_ROPE", "MAP_CE_LSE",
-    "MAP_CE_DLOGITS", "MAP_COLDOT", "K_MAJOR", "MN_MAJOR",
+    "MAP_CE_DLOGITS", "MAP_COLDOT", "MAP_SIGMOID", "MAP_DSIGMOID", "K_MAJOR", "MN_MAJOR",
 ]
 
 K_MAJOR, MN_MAJOR = 0, 1
 BF16, F32 = 0, 1
 (MAP_NONE, MAP_SWIGLU, MAP_DSWIGLU, MAP_QKNORM_ROPE, MAP_CE_LSE, MAP_CE_DLOGITS,
- MAP_COLDOT) = range(7)
+ MAP_COLDOT, MAP_SIGMOID, MAP_DSIGMOID) = range(9)
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -74,6 +75,10 @@ _SIGS = {
                                     + [_I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_cross_entropy_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_cross_entropy": ([_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_sigmoid_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_sigmoid": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_sigmoid_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_sigmoid_bwd": ([_P] * 7 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_rmsnorm_linear_cross_entropy_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_rmsnorm_linear_cross_entropy": ([_P, _P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P],
                                           ctypes.c_int),
@@ -393,6 +398,32 @@ def linear_cross_entropy(X, W, labels, ignore_index=-100, out=None, ws=None, str
         _f32(out["lse"], "lse"), _i32(out["n_valid"], "n_valid"), M, V, K, _ptr(ws), ws.numel(),
         _stream(stream)))
     out["ws"] = ws
+    return out
+
+
+def linear_sigmoid(X, W, Z=None, Y=None, ws=None, stream=None):
+    """sigmoid(X W^T), gating Z when given."""
+    lib = load()
+    M, K = X.shape
+    N = W.shape[0]
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    ws = _ws(ws, lib.coda_linear_sigmoid_workspace_size(M, N, K), X.device)
+    _check("coda_linear_sigmoid", lib.coda_linear_sigmoid(_bf(X, "X"), _bf(W, "W"), _bf(Z, "Z"), _bf(Y, "Y"),
+                                                          M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
+    return Y
+
+
+def linear_sigmoid_bwd(dY, X, W, Z=None, out=None, ws=None, stream=None):
+    lib = load()
+    M, K = X.shape
+    N = W.shape[0]
+    if out is None:
+        out = {"dX": torch.empty_like(X), "dW": torch.empty_like(W),
+               "dZ": torch.empty_like(dY) if Z is not None else None}
+    ws = _ws(ws, lib.coda_linear_sigmoid_bwd_workspace_size(M, N, K), X.device)
+    _check("coda_linear_sigmoid_bwd", lib.coda_linear_sigmoid_bwd(
+        _bf(dY, "dY"), _bf(X, "X"), _bf(W, "W"), _bf(Z, "Z"), _bf(out["dX"], "dX"), _bf(out["dW"], "dW"),
+        _bf(out.get("dZ"), "dZ"), M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

@@ -202,6 +202,7 @@ int run(const Plan& p, int* status, cudaStream_t s) {
     case coda::EpiKind::CeLse: err = coda::launch_gemm_celse(nu, sms, pair, s, maps, a); break;
     case coda::EpiKind::CeDlogits: err = coda::launch_gemm_cedlogits(nu, sms, pair, s, maps, a); break;
     case coda::EpiKind::ColDot: err = coda::launch_gemm_coldot(nu, sms, pair, s, maps, a); break;
+    case coda::EpiKind::Sigmoid: err = coda::launch_gemm_sigmoid(nu, sms, pair, s, maps, a); break;
     default: return CODA_ERR_INVALID_ARG;
   }
   return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
@@ -297,7 +298,7 @@ int coda_gemm_epilogue(const coda_epilogue_desc* d, const coda_bf16* A, int64_t 
   if (a_major != CODA_K_MAJOR && a_major != CODA_MN_MAJOR) return CODA_ERR_INVALID_ARG;
   if (b_major != CODA_K_MAJOR && b_major != CODA_MN_MAJOR) return CODA_ERR_INVALID_ARG;
   if (d_dtype != CODA_BF16 && d_dtype != CODA_F32) return CODA_ERR_INVALID_ARG;
-  if (d->map < CODA_MAP_NONE || d->map > CODA_MAP_COLDOT) return CODA_ERR_INVALID_ARG;
+  if (d->map < CODA_MAP_NONE || d->map > CODA_MAP_DSIGMOID) return CODA_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return CODA_OK;
   CK(req(A));
   CK(req(B));
@@ -311,7 +312,7 @@ int coda_gemm_epilogue(const coda_epilogue_desc* d, const coda_bf16* A, int64_t 
     CK(ldok(ldb, b_major == CODA_K_MAJOR ? K : N));
   }
   if (d_dtype == CODA_F32 && d->map != CODA_MAP_NONE) return CODA_ERR_UNSUPPORTED;
-  if (d->map != CODA_MAP_CE_LSE && d->map != CODA_MAP_QKNORM_ROPE) {
+  if (d->map != CODA_MAP_CE_LSE && d->map != CODA_MAP_QKNORM_ROPE && d->map != CODA_MAP_DSIGMOID) {
     CK(req(D));
     CK(ldok(ldd, N));
   }
@@ -446,6 +447,16 @@ int coda_gemm_epilogue(const coda_epilogue_desc* d, const coda_bf16* A, int64_t 
       p.kind = coda::EpiKind::ColDot;
       if (!d->aux_in[0]) return CODA_ERR_INVALID_ARG;
       if (e.partials && e.ld_part < N) return CODA_ERR_INVALID_ARG;
+      break;
+    case CODA_MAP_SIGMOID:
+      p.kind = coda::EpiKind::Sigmoid;
+      e.mode = 0;
+      break;
+    case CODA_MAP_DSIGMOID:
+      p.kind = coda::EpiKind::Sigmoid;
+      if (!d->aux_in[1] || !d->aux_out[0]) return CODA_ERR_INVALID_ARG;
+      if (d->aux_out[1] && !d->aux_in[0]) return CODA_ERR_INVALID_ARG;
+      e.mode = 1;
       break;
   }
   return run(p, static_cast<int*>(ws), S(stream));
@@ -1322,6 +1333,109 @@ int coda_rmsnorm_linear_cross_entropy_bwd(const coda_bf16* X, const float* rstd,
     CK(run(p, status, s));
   }
   CU(coda::launch_colsum(dgp, 4 * nmb, K, K, dgamma, s));
+  return CODA_OK;
+}
+
+
+// ------------------------------------------------------------------ linear_sigmoid
+size_t coda_linear_sigmoid_workspace_size(int64_t, int64_t, int64_t) { return WS_HEADER; }
+
+int coda_linear_sigmoid(const coda_bf16* X, const coda_bf16* W, const coda_bf16* Z, coda_bf16* Y, int64_t M,
+                        int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream) {
+  CK(dims_ok(M, N, K));
+  CK(ws_ok(ws, ws_bytes, WS_HEADER));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)X, (const void*)W, (const void*)Y}) CK(req(q));
+  for (const void* q : {(const void*)X, (const void*)W, (const void*)Z, (const void*)Y}) CK(al(q));
+  Plan p;
+  p.kind = coda::EpiKind::Sigmoid;
+  p.A = X;
+  p.lda = K;
+  p.B = W;
+  p.ldb = K;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.e.D = Y;
+  p.e.ldd = N;
+  p.e.aux0 = BF(Z);
+  p.e.ld_aux0 = N;
+  p.e.mode = 0;
+  return run(p, static_cast<int*>(ws), S(stream));
+}
+
+size_t coda_linear_sigmoid_bwd_workspace_size(int64_t M, int64_t N, int64_t) {
+  SizeCursor c;
+  c.take<__nv_bfloat16>(static_cast<size_t>(M) * N);  // dz
+  return c.off;
+}
+
+int coda_linear_sigmoid_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W, const coda_bf16* Z,
+                            coda_bf16* dX, coda_bf16* dW, coda_bf16* dZ, int64_t M, int64_t N, int64_t K, void* ws,
+                            size_t ws_bytes, coda_stream stream) {
+  CK(dims_ok(M, N, K));
+  CK(ws_ok(ws, ws_bytes, coda_linear_sigmoid_bwd_workspace_size(M, N, K)));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)dY, (const void*)X, (const void*)W, (const void*)dX, (const void*)dW})
+    CK(req(q));
+  if (Z && !dZ) return CODA_ERR_INVALID_ARG;
+  for (const void* q : {(const void*)dY, (const void*)X, (const void*)W, (const void*)Z, (const void*)dX,
+                        (const void*)dW, (const void*)dZ})
+    CK(al(q));
+  WsCursor w(ws);
+  __nv_bfloat16* dz = w.take<__nv_bfloat16>(static_cast<size_t>(M) * N);
+  int* status = static_cast<int*>(ws);
+  cudaStream_t s = S(stream);
+  {  // recompute z = X W^T; dz = dY (* Z) * s (1 - s); dZ = dY * s
+    Plan p;
+    p.kind = coda::EpiKind::Sigmoid;
+    p.A = X;
+    p.lda = K;
+    p.B = W;
+    p.ldb = K;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.e.aux0 = BF(Z);
+    p.e.ld_aux0 = N;
+    p.e.aux1 = BF(dY);
+    p.e.ld_aux1 = N;
+    p.e.out1 = dz;
+    p.e.ld_out1 = N;
+    p.e.out2 = Z ? BF(dZ) : nullptr;
+    p.e.ld_out2 = N;
+    p.e.mode = 1;
+    CK(run(p, status, s));
+  }
+  {  // dX = dz W
+    Plan p;
+    p.A = dz;
+    p.lda = N;
+    p.B = W;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.M = M;
+    p.N = K;
+    p.K = N;
+    p.e.D = dX;
+    p.e.ldd = K;
+    CK(run(p, status, s));
+  }
+  {  // dW = dz^T X
+    Plan p;
+    p.A = dz;
+    p.lda = N;
+    p.a_mn = 1;
+    p.B = X;
+    p.ldb = K;
+    p.b_mn = 1;
+    p.M = N;
+    p.N = K;
+    p.K = M;
+    p.e.D = dW;
+    p.e.ldd = K;
+    CK(run(p, status, s));
+  }
   return CODA_OK;
 }
 

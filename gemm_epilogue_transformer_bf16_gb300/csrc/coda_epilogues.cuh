@@ -480,6 +480,62 @@ struct EpiCeDlogits {
 };
 
 // ---------------------------------------------------------------------------
+// SIGMOID (element-wise gate): z = rs * acc, s = sigmoid(z).
+//   mode 0:  D = s, or s * aux0 when a gated tensor Z = aux0 is given.
+//   mode 1 (backward on recomputed z, dY = aux1):
+//            out1 = dz = dY (* Z) * s (1 - s);   out2 = dZ = dY * s (if Z).
+// ---------------------------------------------------------------------------
+template <int BN>
+struct EpiSigmoid {
+  struct State {};
+  static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+    const int row = t.row;
+    const bool rv = row < t.M;
+    const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
+    const int64_t off = static_cast<int64_t>(row);
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      const int col0 = t.nb * BN + c;
+      if (col0 >= t.N) break;
+      float v[32];
+      __syncwarp();
+      tmem_ld32(t.taddr + c, v);
+      if (rv) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int cc = col0 + g * 8;
+          if (cc < t.N) {
+            float sg[8], z8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sg[i] = 1.f / (1.f + __expf(-v[g * 8 + i] * rs));
+            if (e.aux0) load_bf16x8(e.aux0 + off * e.ld_aux0 + cc, z8);
+            if (e.mode == 0) {
+              float y[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) y[i] = e.aux0 ? sg[i] * z8[i] : sg[i];
+              store_bf16x8(static_cast<__nv_bfloat16*>(e.D) + off * e.ldd + cc, y, e.st_stream);
+            } else {
+              float dy[8], dz[8], dg[8];
+              load_bf16x8(e.aux1 + off * e.ld_aux1 + cc, dy);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float gg = e.aux0 ? dy[i] * z8[i] : dy[i];
+                dz[i] = gg * sg[i] * (1.f - sg[i]);
+                dg[i] = dy[i] * sg[i];
+              }
+              store_bf16x8(e.out1 + off * e.ld_out1 + cc, dz, e.st_stream);
+              if (e.out2) store_bf16x8(e.out2 + off * e.ld_out2 + cc, dg, e.st_stream);
+            }
+          }
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
 // QKNORM_ROPE (row scale + per-head RMSNorm + RoPE rotation, pairwise map):
 // a BN = 256 tile holds two 128-wide heads of the fused [q | k | v]
 // projection.  q/k heads: x = rs*acc, n = x * rsqrt(mean(x^2) + eps) * gamma,

@@ -10,7 +10,7 @@
 
 namespace coda {
 
-enum class EpiKind : int { Plain = 0, Swiglu, DSwiglu, QkRope, CeLse, CeDlogits, ColDot };
+enum class EpiKind : int { Plain = 0, Swiglu, DSwiglu, QkRope, CeLse, CeDlogits, ColDot, Sigmoid };
 
 // Tensor maps in the order A0, B0, A1, B1.  `pair` selects the CTA-pair
 // (cta_group::2) variant; the launcher sizes the persistent grid.
@@ -26,6 +26,8 @@ cudaError_t launch_gemm_celse(int num_units, int sms, bool pair, cudaStream_t s,
                                const GemmArgs& a);
 cudaError_t launch_gemm_cedlogits(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
+cudaError_t launch_gemm_sigmoid(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                                const GemmArgs& a);
 cudaError_t launch_gemm_coldot(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
 

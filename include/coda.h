@@ -75,7 +75,9 @@ enum {
   CODA_MAP_QKNORM_ROPE = 3,  /* per-head RMSNorm + RoPE of q/k heads, v pass-through; aux_out[0] saves pre-norm q|k */
   CODA_MAP_CE_LSE = 4,       /* online (max, sum-exp) per row over vocab tiles + target logit; D unused */
   CODA_MAP_CE_DLOGITS = 5,   /* D = (softmax(acc) - onehot) * dloss / n_valid */
-  CODA_MAP_COLDOT = 6        /* D = cs*acc; partials = column sums of aux_in[0]*acc per 32-row group */
+  CODA_MAP_COLDOT = 6,       /* D = cs*acc; partials = column sums of aux_in[0]*acc per 32-row group */
+  CODA_MAP_SIGMOID = 7,      /* D = sigmoid(rs*acc) (* aux_in[0] when given) */
+  CODA_MAP_DSIGMOID = 8      /* recomputed z = rs*acc, dY = aux_in[1]: aux_out[0] = dY (*aux_in[0]) s(1-s), aux_out[1] = dY s */
 };
 
 /*
@@ -339,6 +341,27 @@ size_t coda_linear_cross_entropy_workspace_size(int64_t M, int64_t V, int64_t K)
 int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int32_t* labels,
                               int32_t ignore_index, float* loss_mean, float* lse, int32_t* n_valid,
                               int64_t M, int64_t V, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* ------------------------------------------------------------------------
+ * linear_sigmoid (x-tip guide functional API; the pages give only the name).
+ * Reading: a linear layer with an element-wise sigmoid ("CODA" §3.1 class 1),
+ * optionally gating a second tensor:
+ *   Y = sigmoid(X W^T)            (Z == NULL)
+ *   Y = sigmoid(X W^T) ⊙ Z        (Z [M, N] bf16)
+ * X [M, K], W [N, K], Y [M, N] bf16.
+ * ---------------------------------------------------------------------- */
+size_t coda_linear_sigmoid_workspace_size(int64_t M, int64_t N, int64_t K);
+int coda_linear_sigmoid(const coda_bf16* X, const coda_bf16* W, const coda_bf16* Z, coda_bf16* Y, int64_t M,
+                        int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* Backward for upstream gradient dY [M, N]: the logits are recomputed by the
+ * GEMM and the epilogue forms dz = dY (⊙ Z) ⊙ s (1 - s) (staged bf16 in the
+ * workspace) and dZ = dY ⊙ s; then dX = dz W [M, K] and dW = dz^T X [N, K].
+ * dZ is required when Z is given, ignored otherwise. */
+size_t coda_linear_sigmoid_bwd_workspace_size(int64_t M, int64_t N, int64_t K);
+int coda_linear_sigmoid_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W, const coda_bf16* Z,
+                            coda_bf16* dX, coda_bf16* dW, coda_bf16* dZ, int64_t M, int64_t N, int64_t K, void* ws,
+                            size_t ws_bytes, coda_stream stream);
 
 /* ------------------------------------------------------------------------
  * Final RMSNorm -> LM head -> cross-entropy ("CODA" §3.2.1, third site of

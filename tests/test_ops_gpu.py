@@ -197,3 +197,23 @@ def test_rmsnorm_linear_cross_entropy(coda, shape):
     assert_bf16(g["dX"], b["dX"] + o["R"], "dX (+ residual gradient)")
     assert_bf16(g["dW"], b["dW"], "dW")
     assert_bf16(g["dgamma"], b["dgamma"], "dgamma")
+
+
+# ---------------------------------------------------------------- linear_sigmoid
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("M,N,K", [(512, 768, 384), (300, 264, 200)])
+def test_linear_sigmoid(coda, gated, M, N, K):
+    X = synth.randn_bf16((M, K), 1.0, 1)
+    W = synth.randn_bf16((N, K), 1 / math.sqrt(K), 2)
+    Z = synth.randn_bf16((M, N), 1.0, 3) if gated else None
+    dY = synth.randn_bf16((M, N), 1.0, 4)
+    Zd = Z.to(DEV) if gated else None
+    Y = coda.linear_sigmoid(X.to(DEV), W.to(DEV), Zd)
+    Zo = to_np(Z) if gated else None
+    assert_bf16(Y, O.linear_sigmoid_fwd(to_np(X), to_np(W), Zo), "Y")
+    g = coda.linear_sigmoid_bwd(dY.to(DEV), X.to(DEV), W.to(DEV), Zd)
+    b = O.linear_sigmoid_bwd(to_np(X), to_np(W), to_np(dY), Zo)
+    assert_bf16(g["dX"], b["dX"], "dX")
+    assert_bf16(g["dW"], b["dW"], "dW")
+    if gated:
+        assert_bf16(g["dZ"], b["dZ"], "dZ")
