@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libcoda.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
-                     "-I" + INCLUDE, "-I" + CSRC]
+                     "-I" + INCLUDE, "-I" + CSRC] + os.environ.get("CODA_NVCC_FLAGS", "").split()
 
 
 def _nvcc():

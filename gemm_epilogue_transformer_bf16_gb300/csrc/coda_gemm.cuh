@@ -45,17 +45,21 @@ constexpr int EPI_WARP0 = 2;
 // PAIR: a cluster of two CTAs on two SMs computes a 256 x BN tile with
 // tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of A and half of
 // B (BN/2 rows), so a stage is 32 KB and six of them fit.
+#ifndef CODA_PAIR_STAGES
+#define CODA_PAIR_STAGES 6
+#endif
 template <int BN, bool PAIR = false>
 struct GemmCfg {
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows staged by one CTA
-  static constexpr int STAGES = PAIR ? 6 : (BN >= 256 ? 4 : 6);
+  static constexpr int STAGES = PAIR ? CODA_PAIR_STAGES : (BN >= 256 ? 4 : 6);
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr uint32_t BAR_BYTES = 256;
-  static constexpr uint32_t EPI_SMEM_BYTES = BN * 4;
+  static constexpr uint32_t EPI_SMEM_BYTES = 0;
   static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + EPI_SMEM_BYTES;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
 // Everything an epilogue may read or write.  Unused fields are null/zero.
@@ -217,7 +221,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc<PAIR>(tmem_slot, Cfg::TMEM_COLS);
     tmem_relinquish<PAIR>();
   }
-  for (int i = threadIdx.x; i < BN; i += NUM_THREADS) epi_smem[i] = 0.f;
   tc_fence_before();
   __syncthreads();
   if constexpr (PAIR) cluster_sync();  // peer barriers initialised before any remote arrive
