@@ -50,6 +50,7 @@ __all__ = [
     "gemm_epilogue_plain",
     "rmsnorm_linear_cross_entropy_fwd", "rmsnorm_linear_cross_entropy_bwd",
     "sigmoid", "linear_sigmoid_fwd", "linear_sigmoid_bwd",
+    "E4M3_MAX", "quantize_fp8_rows", "linear_fp8_fwd", "swiglu_fp8_fwd",
 ]
 
 
@@ -329,6 +330,50 @@ def linear_sigmoid_bwd(X, W, dY, Z=None):
     if Z is not None:
         out["dZ"] = dY * s
     return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) operands with per-row scales
+# ---------------------------------------------------------------------------
+# The pages motivate fusion by low-precision GEMMs (FP8 / FP4, [P1] §1 and
+# [P2]); they give no quantisation recipe.  Reading: per-row (per token, per
+# output channel) scales s = amax / 448 in fp32, codes q = e4m3(x / s) with
+# the division in fp32, round to nearest even, saturating at +-448.  These
+# are the decisions the kernel takes, in the kernel's precision (fp32), so
+# the codes must match bit for bit.
+
+E4M3_MAX = 448.0
+
+
+def quantize_fp8_rows(X):
+    """Returns (codes uint8 [M, K], values float64 [M, K] = e4m3(codes),
+    scales float32 [M]); x ~= values * scale."""
+    import torch
+    x32 = np.asarray(X, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=1) if x32.shape[1] else np.zeros(x32.shape[0], np.float32)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    v = np.clip((x32 / scale[:, None]).astype(np.float32), -E4M3_MAX, E4M3_MAX)
+    q = torch.from_numpy(v).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).numpy(), q.double().numpy(), scale
+
+
+def linear_fp8_fwd(Xv, sx, Wv, sw, R=None, row_scale=None):
+    """y = R + rs_i * (Xv_i sx_i) . (Wv_n sw_n): the plain linear of
+    gemm_epilogue_plain on the dequantised operands."""
+    A = Xv * np.asarray(sx, dtype=np.float64)[:, None]
+    B = Wv * np.asarray(sw, dtype=np.float64)[:, None]
+    return gemm_epilogue_plain(A, B, row_scale=row_scale, aux0=R)
+
+
+def swiglu_fp8_fwd(Xv, sx, Wgv, sg, Wuv, su, row_scale=None):
+    """swiglu_fwd on the dequantised operands, with the optional row factor r
+    applied to g and u before the gate (as the RMSNorm-reparameterised
+    gate/up projection does).  Returns (H, g, u)."""
+    A = Xv * np.asarray(sx, dtype=np.float64)[:, None]
+    if row_scale is not None:
+        A = A * np.asarray(row_scale, dtype=np.float64)[:, None]
+    return swiglu_fwd(A, Wgv * np.asarray(sg, dtype=np.float64)[:, None],
+                      Wuv * np.asarray(su, dtype=np.float64)[:, None])
 
 
 # ---------------------------------------------------------------------------

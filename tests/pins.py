@@ -443,7 +443,71 @@ def check_linear_sigmoid(o):
     return max(e)
 
 
+def _e4m3_table():
+    """All finite e4m3 codes and their values, decoded from the format's
+    definition (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+    subnormals at exponent 0, code 0x7f / 0xff = NaN)."""
+    codes, vals = [], []
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        sgn = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 0x7
+        v = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        codes.append(c)
+        vals.append(sgn * v)
+    return np.array(codes, dtype=np.uint8), np.array(vals)
+
+
+def check_fp8_quantizer(o):
+    """(1) every finite e4m3 value, in a row whose max is 448 (scale 1),
+    quantises to its own code; (2) |q s - x| <= 2^-4 |x| in the normal range
+    and <= 2^-10 s below it; (3) each row's max maps to +-448 exactly;
+    (4) a zero row gives zero codes and scale 1; (5) monotone."""
+    codes, vals = _e4m3_table()
+    row = np.concatenate([vals, [448.0]])[None, :]
+    qc, qv, sc = o.quantize_fp8_rows(row)
+    e = [float(np.any(qc[0, :-1] != codes)), abs(float(sc[0]) - 1.0), _rel(qv[0, :-1], vals)]
+    r = RNG(20)
+    X = r.standard_normal((6, 300)) * np.array([1e-3, 1, 30, 1e4, 0.5, 7])[:, None]
+    qc, qv, sc = o.quantize_fp8_rows(X)
+    deq = qv * sc[:, None].astype(np.float64)
+    ax = np.abs(X)
+    normal = ax / sc[:, None] >= 2.0 ** -6
+    err = np.abs(deq - X)
+    rel_normal = float(np.max(np.where(normal, err / np.maximum(ax, 1e-300), 0.0)))
+    abs_sub = float(np.max(np.where(normal, 0.0, err / sc[:, None])))
+    e.append(0.0 if rel_normal <= 2.0 ** -4 * (1 + 1e-6) else 1.0)   # half an ulp of a 3-bit mantissa
+    e.append(0.0 if abs_sub <= 2.0 ** -10 * (1 + 1e-6) else 1.0)     # half the subnormal spacing 2^-9
+    e.append(float(np.max(np.abs(np.abs(qv).max(axis=1) - 448.0))))
+    qc0, qv0, sc0 = o.quantize_fp8_rows(np.zeros((1, 5)))
+    e.append(float(np.any(qv0 != 0)) + abs(float(sc0[0]) - 1.0))
+    xs = np.sort(r.standard_normal(500))[None, :]
+    e.append(float(np.any(np.diff(o.quantize_fp8_rows(xs)[1][0]) < 0)))
+    return max(e)
+
+
+def check_fp8_linear(o):
+    """With operands already e4m3 values and row maxima 448 (scales 1), the
+    FP8 linear and SwiGLU equal the bf16 definitions exactly."""
+    codes, vals = _e4m3_table()
+    r = RNG(21)
+    pick = lambda shape: vals[r.integers(0, len(vals), size=shape)] * (2.0 ** -6)
+    X = pick((4, 16))
+    Wg, Wu = pick((6, 16)), pick((6, 16))
+    X[:, 0], Wg[:, 0], Wu[:, 0] = 448.0 * 2.0 ** -6, 448.0 * 2.0 ** -6, 448.0 * 2.0 ** -6
+    _, xv, sx = o.quantize_fp8_rows(X)
+    _, gv, sg = o.quantize_fp8_rows(Wg)
+    _, uv, su = o.quantize_fp8_rows(Wu)
+    H, g, u = o.swiglu_fp8_fwd(xv, sx, gv, sg, uv, su)
+    H0, g0, u0 = o.swiglu_fwd(X, Wg, Wu)
+    y = o.linear_fp8_fwd(xv, sx, gv, sg)
+    return max(_rel(H, H0), _rel(g, g0), _rel(u, u0), _rel(y, X @ Wg.T))
+
+
 ALL_CHECKS = {
+    "fp8_quantizer": (check_fp8_quantizer, 1e-12),
+    "fp8_linear": (check_fp8_linear, 1e-14),
     "linear_sigmoid": (check_linear_sigmoid, 1e-7),
     "rmsnorm_ce_library": (check_rmsnorm_ce_library, 1e-12),
     "rmsnorm_ce_grad": (check_rmsnorm_ce_grad, 1e-7),

@@ -158,7 +158,22 @@ def _mut_sigmoid_bwd_missing_factor(m):
     m.linear_sigmoid_bwd = bad
 
 
+def _mut_fp8_truncate(m):
+    import torch
+
+    def bad(X):
+        x32 = np.asarray(X, dtype=np.float32)
+        amax = np.max(np.abs(x32), axis=1)
+        scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+        v = np.clip(x32 / scale[:, None], -448, 448)
+        v = np.sign(v) * np.floor(np.abs(v) * 8) / 8       # truncation instead of rounding
+        q = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn)
+        return q.view(torch.uint8).numpy(), q.double().numpy(), scale
+    m.quantize_fp8_rows = bad
+
+
 MUTANTS = {
+    "fp8_truncates": _mut_fp8_truncate,
     "sigmoid_bwd_missing_derivative": _mut_sigmoid_bwd_missing_factor,
     "rmsnorm_ce_skips_norm_backward": _mut_rmsnorm_ce_skip_norm_bwd,
     "gemm_coef_sign": _mut_gemm_transposed_scale,
