@@ -26,7 +26,7 @@ __all__ = [
     "linear_swiglu", "linear_swiglu_bwd", "linear_qknorm_rope", "linear_qknorm_rope_bwd",
     "linear_cross_entropy", "linear_cross_entropy_bwd", "linear_cross_entropy_noalloc", "workspace",
     "rmsnorm_linear_cross_entropy", "rmsnorm_linear_cross_entropy_bwd", "rms_rstd",
-    "linear_sigmoid", "linear_sigmoid_bwd",
+    "linear_sigmoid", "linear_sigmoid_bwd", "quantize_fp8_rows", "linear_fp8", "linear_swiglu_fp8",
     "MAP_NONE", "MAP_SWIGLU", "MAP_DSWIGLU", "MAP_QKNORM_ROPE", "MAP_CE_LSE",
     "MAP_CE_DLOGITS", "MAP_COLDOT", "MAP_SIGMOID", "MAP_DSIGMOID", "K_MAJOR", "MN_MAJOR",
 ]
@@ -75,6 +75,11 @@ _SIGS = {
                                     + [_I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_cross_entropy_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_cross_entropy": ([_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_quantize_fp8_rows": ([_P, _I64, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "coda_linear_fp8_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_fp8": ([_P] * 6 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_swiglu_fp8_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_swiglu_fp8": ([_P] * 10 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_sigmoid_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_sigmoid": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_sigmoid_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
@@ -399,6 +404,49 @@ def linear_cross_entropy(X, W, labels, ignore_index=-100, out=None, ws=None, str
         _stream(stream)))
     out["ws"] = ws
     return out
+
+
+def _u8(t, name="tensor"):
+    return _ptr(t, torch.uint8, name)
+
+
+def quantize_fp8_rows(X, Xq=None, scale=None, stream=None):
+    """Per-row e4m3 quantisation: returns (codes uint8 [M, K], scale fp32 [M])."""
+    M, K = X.shape
+    Xq = torch.empty(M, K, dtype=torch.uint8, device=X.device) if Xq is None else Xq
+    scale = torch.empty(M, dtype=torch.float32, device=X.device) if scale is None else scale
+    _check("coda_quantize_fp8_rows", load().coda_quantize_fp8_rows(_bf(X, "X"), K, M, K, _u8(Xq, "Xq"),
+                                                                   _f32(scale, "scale"), _stream(stream)))
+    return Xq, scale
+
+
+def linear_fp8(Xq, sx, Wq, sw, R=None, Y=None, ws=None, stream=None):
+    lib = load()
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=Xq.device) if Y is None else Y
+    ws = _ws(ws, lib.coda_linear_fp8_workspace_size(M, N, K), Xq.device)
+    _check("coda_linear_fp8", lib.coda_linear_fp8(_u8(Xq, "Xq"), _f32(sx, "sx"), _u8(Wq, "Wq"), _f32(sw, "sw"),
+                                                  _bf(R, "R"), _bf(Y, "Y"), M, N, K, _ptr(ws), ws.numel(),
+                                                  _stream(stream)))
+    return Y
+
+
+def linear_swiglu_fp8(Xq, sx, Wgq, sg, Wuq, su, rstd=None, save=True, H=None, g=None, u=None, ws=None,
+                      stream=None):
+    lib = load()
+    M, K = Xq.shape
+    I = Wgq.shape[0]
+    dev = Xq.device
+    H = torch.empty(M, I, dtype=torch.bfloat16, device=dev) if H is None else H
+    if save:
+        g = torch.empty(M, I, dtype=torch.bfloat16, device=dev) if g is None else g
+        u = torch.empty(M, I, dtype=torch.bfloat16, device=dev) if u is None else u
+    ws = _ws(ws, lib.coda_linear_swiglu_fp8_workspace_size(M, I, K), dev)
+    _check("coda_linear_swiglu_fp8", lib.coda_linear_swiglu_fp8(
+        _u8(Xq, "Xq"), _f32(sx, "sx"), _f32(rstd, "rstd"), _u8(Wgq, "Wgq"), _f32(sg, "sg"), _u8(Wuq, "Wuq"),
+        _f32(su, "su"), _bf(H, "H"), _bf(g, "g"), _bf(u, "u"), M, I, K, _ptr(ws), ws.numel(), _stream(stream)))
+    return H, g, u
 
 
 def linear_sigmoid(X, W, Z=None, Y=None, ws=None, stream=None):

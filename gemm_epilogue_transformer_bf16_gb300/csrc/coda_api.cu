@@ -78,12 +78,13 @@ int num_sms() {
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride
 // `ld` elements; box = box_cols x box_rows, 128-byte swizzle, zero fill.
 bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_cols,
-                uint32_t box_rows) {
+                uint32_t box_rows, int elem_bytes = 2) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * elem_bytes};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -104,6 +105,7 @@ struct Plan {
   int64_t ldb2 = 0;
   int64_t K2 = 0;
   int b_dual = 0;
+  int fp8 = 0;  // e4m3 operands (K-major only)
   int64_t M = 0, N = 0, K = 0;
   int n_per_unit = 1;
   EpiArgs e{};
@@ -152,16 +154,21 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   CUtensorMap maps[4];
   std::memset(maps, 0, sizeof(maps));
   // A operands
+  // a k-slice is 128 bytes: 64 bf16 or 128 e4m3 elements
+  const int esz = p.fp8 ? 1 : 2;
+  const uint32_t kbox = p.fp8 ? 2 * coda::BK : coda::BK;
+  if (p.fp8 && (p.a_mn || p.b_mn)) return CODA_ERR_UNSUPPORTED;
   auto enc_a = [&](CUtensorMap* m, const void* ptr, int64_t ld, int64_t Kc) {
-    return p.a_mn ? encode_map(m, ptr, Kc, p.M, ld, 64, 64) : encode_map(m, ptr, p.M, Kc, ld, 64, 128);
+    return p.a_mn ? encode_map(m, ptr, Kc, p.M, ld, 64, 64) : encode_map(m, ptr, p.M, Kc, ld, kbox, 128, esz);
   };
   auto enc_b = [&](CUtensorMap* m, const void* ptr, int64_t ld, int64_t Kc) {
-    return p.b_mn ? encode_map(m, ptr, Kc, p.N, ld, 64, 64) : encode_map(m, ptr, p.N, Kc, ld, 64, b_box_rows);
+    return p.b_mn ? encode_map(m, ptr, Kc, p.N, ld, 64, 64)
+                  : encode_map(m, ptr, p.N, Kc, ld, kbox, b_box_rows, esz);
   };
   if (!enc_a(&maps[0], p.A, p.lda, p.K)) return CODA_ERR_CUDA;
   if (p.b_dual) {
-    if (!encode_map(&maps[1], p.B, p.N, p.K, p.ldb, 64, BN / 2)) return CODA_ERR_CUDA;
-    if (!encode_map(&maps[3], p.B2, p.N, p.K, p.ldb2, 64, BN / 2)) return CODA_ERR_CUDA;
+    if (!encode_map(&maps[1], p.B, p.N, p.K, p.ldb, kbox, BN / 2, esz)) return CODA_ERR_CUDA;
+    if (!encode_map(&maps[3], p.B2, p.N, p.K, p.ldb2, kbox, BN / 2, esz)) return CODA_ERR_CUDA;
     maps[2] = maps[0];
   } else {
     if (!enc_b(&maps[1], p.B, p.ldb, p.K)) return CODA_ERR_CUDA;
@@ -178,15 +185,17 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   a.N = static_cast<int>(p.N);
   a.num_m = static_cast<int>(cdiv(p.M, pair ? 2 * coda::BM : coda::BM));
   a.num_n = static_cast<int>(cdiv(p.N, p.b_dual ? BN / 2 : BN));
-  a.kb0 = static_cast<int>(cdiv(p.K, coda::BK));
-  a.kb1 = p.K2 > 0 ? static_cast<int>(cdiv(p.K2, coda::BK)) : 0;
+  a.kb0 = static_cast<int>(cdiv(p.K, kbox));
+  a.kb1 = p.K2 > 0 ? static_cast<int>(cdiv(p.K2, kbox)) : 0;
+  a.fp8 = p.fp8;
   a.a_mn = p.a_mn;
   a.b_mn = p.b_mn;
   a.b_dual = p.b_dual;
   a.n_per_unit = p.n_per_unit;
   a.num_units = p.n_per_unit > 1 ? a.num_m * static_cast<int>(cdiv(a.num_n, p.n_per_unit)) : a.num_m * a.num_n;
   a.group_m = group_m(pair);
-  a.idesc = coda::idesc_bf16(pair ? 2 * coda::BM : coda::BM, BN, p.a_mn, p.b_mn);
+  a.idesc = p.fp8 ? coda::idesc_e4m3(pair ? 2 * coda::BM : coda::BM, BN)
+                  : coda::idesc_bf16(pair ? 2 * coda::BM : coda::BM, BN, p.a_mn, p.b_mn);
   a.status = status;
   a.timeout_ns = TIMEOUT_NS;
   a.l2_hints = l2_hints() & 3;
@@ -1437,6 +1446,95 @@ int coda_linear_sigmoid_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_
     CK(run(p, status, s));
   }
   return CODA_OK;
+}
+
+
+// ------------------------------------------------------------------ FP8 (e4m3) operands
+int coda_quantize_fp8_rows(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq, float* scale,
+                           coda_stream stream) {
+  if (M < 0 || K < 0) return CODA_ERR_INVALID_ARG;
+  if (K % 16) return CODA_ERR_UNSUPPORTED;  // 16-byte rows for the e4m3 tensor maps
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)X, (const void*)Xq, (const void*)scale}) CK(req(q));
+  CK(al(X));
+  CK(al(Xq));
+  CK(ldok(ldx, K));
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  CU(coda::launch_quantize_fp8_rows(BF(X), ldx, M, K, Xq, K, scale, sms, S(stream)));
+  return CODA_OK;
+}
+
+size_t coda_linear_fp8_workspace_size(int64_t, int64_t, int64_t) { return WS_HEADER; }
+
+int coda_linear_fp8(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, const coda_bf16* R,
+                    coda_bf16* Y, int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream) {
+  CK(dims_ok(M, N, K));
+  if (K % 16) return CODA_ERR_UNSUPPORTED;
+  CK(ws_ok(ws, ws_bytes, WS_HEADER));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)Xq, (const void*)sx, (const void*)Wq, (const void*)sw, (const void*)Y})
+    CK(req(q));
+  for (const void* q : {(const void*)Xq, (const void*)Wq, (const void*)sw, (const void*)R, (const void*)Y})
+    CK(al(q));
+  Plan p;
+  p.fp8 = 1;
+  p.A = Xq;
+  p.lda = K;
+  p.B = Wq;
+  p.ldb = K;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.e.D = Y;
+  p.e.ldd = N;
+  p.e.row_scale = sx;
+  p.e.col_scale = sw;
+  p.e.aux0 = BF(R);
+  p.e.ld_aux0 = N;
+  return run(p, static_cast<int*>(ws), S(stream));
+}
+
+size_t coda_linear_swiglu_fp8_workspace_size(int64_t, int64_t, int64_t) { return WS_HEADER; }
+
+int coda_linear_swiglu_fp8(const uint8_t* Xq, const float* sx, const float* rstd, const uint8_t* Wgq,
+                           const float* sg, const uint8_t* Wuq, const float* su, coda_bf16* H, coda_bf16* g_save,
+                           coda_bf16* u_save, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
+                           coda_stream stream) {
+  CK(dims_ok(M, I, K));
+  if (K % 16) return CODA_ERR_UNSUPPORTED;
+  CK(ws_ok(ws, ws_bytes, WS_HEADER));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)Xq, (const void*)sx, (const void*)Wgq, (const void*)sg, (const void*)Wuq,
+                        (const void*)su, (const void*)H})
+    CK(req(q));
+  for (const void* q : {(const void*)Xq, (const void*)Wgq, (const void*)Wuq, (const void*)sg, (const void*)su,
+                        (const void*)H, (const void*)g_save, (const void*)u_save})
+    CK(al(q));
+  Plan p;
+  p.kind = coda::EpiKind::Swiglu;
+  p.fp8 = 1;
+  p.A = Xq;
+  p.lda = K;
+  p.B = Wgq;
+  p.ldb = K;
+  p.B2 = Wuq;
+  p.ldb2 = K;
+  p.b_dual = 1;
+  p.M = M;
+  p.N = I;
+  p.K = K;
+  p.e.D = H;
+  p.e.ldd = I;
+  p.e.row_scale = sx;
+  p.e.row_scale2 = rstd;
+  p.e.col_scale = sg;
+  p.e.col_scale2 = su;
+  p.e.out1 = BF(g_save);
+  p.e.ld_out1 = I;
+  p.e.out2 = BF(u_save);
+  p.e.ld_out2 = I;
+  return run(p, static_cast<int*>(ws), S(stream));
 }
 
 }  // extern "C"

@@ -7,6 +7,8 @@
 // warp-per-row for row work, grids sized to the SM count.
 #include <cmath>
 
+#include <cuda_fp8.h>
+
 #include "coda_epilogues.cuh"
 #include "coda_internal.h"
 
@@ -346,6 +348,50 @@ cudaError_t launch_ce_norm_coef(const float* pz, int64_t ld, int nparts, const f
   const int64_t blocks = std::min<int64_t>((M + 255) / 256, 4096);
   ce_norm_coef_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(pz, ld, nparts, target,
                                                                                           rstd, rw, M, inv_k, coef);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- FP8 (e4m3) row quantisation
+// Warp per row: scale = amax / 448 (fp32; 1 for an all-zero row), codes =
+// e4m3(x / scale), fp32 division, round to nearest even, saturating.
+__global__ void quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int64_t M, int64_t K,
+                                         uint8_t* Xq, int64_t ldq, float* scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; row < M; row += warps) {
+    const __nv_bfloat16* x = X + row * ldx;
+    float amax = 0.f;
+    for (int64_t k = lane * 8; k < K; k += 256) {
+      float v[8];
+      load_bf16x8(x + k, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = amax > 0.f ? amax / 448.f : 1.f;
+    if (lane == 0) scale[row] = s;
+    uint8_t* q = Xq + row * ldq;
+    for (int64_t k = lane * 8; k < K; k += 256) {
+      float v[8];
+      load_bf16x8(x + k, v);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        lo |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(v[j] / s, __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        hi |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(v[4 + j] / s, __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+      *reinterpret_cast<uint2*>(q + k) = make_uint2(lo, hi);
+    }
+  }
+}
+
+cudaError_t launch_quantize_fp8_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq,
+                                     int64_t ldq, float* scale, int num_sms, cudaStream_t s) {
+  const int64_t blocks = std::min<int64_t>((M + 7) / 8, static_cast<int64_t>(num_sms) * 8);
+  quantize_fp8_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(X, ldx, M, K, Xq,
+                                                                                               ldq, scale);
   return cudaGetLastError();
 }
 

@@ -144,7 +144,9 @@ struct EpiPlain {
 // ---------------------------------------------------------------------------
 // SWIGLU (pairwise map on co-resident gate/up accumulators):
 //   accumulator columns [0, BN/2) = X Wg^T, [BN/2, BN) = X Wu^T for the same
-//   output columns;  g = rs*acc_g, u = rs*acc_u, H = silu(g) * u.
+//   output columns;  g = rs*acc_g, u = rs*acc_u, H = silu(g) * u.  With FP8
+//   operands rs also carries the token scale and g, u the per-column weight
+//   scales (col_scale, col_scale2).
 //   Optionally stores g and u (bf16) for the backward.
 // ---------------------------------------------------------------------------
 template <int BN>
@@ -156,7 +158,7 @@ struct EpiSwiglu {
   static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
     const int row = t.row;
     const bool rv = row < t.M;
-    const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
+    const float rs = ((e.row_scale && rv) ? e.row_scale[row] : 1.f) * ((e.row_scale2 && rv) ? e.row_scale2[row] : 1.f);
 #pragma unroll 1
     for (int c = 0; c < HALF; c += 32) {
       const int col0 = t.nb * HALF + c;
@@ -171,11 +173,19 @@ struct EpiSwiglu {
         for (int q = 0; q < 4; ++q) {
           const int cc = col0 + q * 8;
           if (cc < t.N) {
-            float gg[8], uu[8], h[8];
+            float gg[8], uu[8], h[8], cg[8], cu[8];
+            if (e.col_scale) {
+              load_f32x8(e.col_scale + cc, cg);
+              load_f32x8(e.col_scale2 + cc, cu);
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               gg[i] = g[q * 8 + i] * rs;
               uu[i] = u[q * 8 + i] * rs;
+              if (e.col_scale) {
+                gg[i] *= cg[i];
+                uu[i] *= cu[i];
+              }
               h[i] = gg[i] / (1.f + __expf(-gg[i])) * uu[i];
             }
             store_bf16x8(static_cast<__nv_bfloat16*>(e.D) + off * e.ldd + cc, h, e.st_stream);

@@ -81,6 +81,8 @@ struct EpiArgs {
   const int32_t* csr_off;       // [M+1] per output row: range of csr_idx
   const int32_t* csr_idx;       // aux2 row indices
   const float* csr_w;           // weight of each aux2 row
+  const float* row_scale2;      // SWIGLU: second per-row factor (FP8 token scale)
+  const float* col_scale2;      // SWIGLU: per-column factor of the up half (col_scale: gate half)
   const float* row_coef2;       // PLAIN: D -= row_coef2_i * aux3[i, j]
   const __nv_bfloat16* aux3;
   int64_t ld_aux3;
@@ -132,6 +134,7 @@ struct GemmArgs {
   int* status;
   uint64_t timeout_ns;
   int l2_hints;      // bit 0: A loads evict_last, bit 1: B loads evict_first
+  int fp8;           // e4m3 operands: 128 elements per 128-byte k-slice, kind::f8f6f4
   EpiArgs e;
 };
 
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool second = kb >= args.kb0;
             const CUtensorMap* ma = second ? &mA1 : &mA0;
             const CUtensorMap* mbp = second ? &mB1 : &mB0;
-            const int k = (second ? kb - args.kb0 : kb) * BK;
+            const int k = (second ? kb - args.kb0 : kb) * (args.fp8 ? 2 * BK : BK);
             uint8_t* sa = tiles + s * Cfg::STAGE_BYTES;
             uint8_t* sb = sa + Cfg::A_BYTES;
             if constexpr (PAIR) {
@@ -358,10 +361,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                             : sdesc_sw128(sa + k16 * 32, 16, 1024);
               const uint64_t bd = args.b_mn ? sdesc_sw128(sb + k16 * 2048, 8192, 1024)
                                             : sdesc_sw128(sb + k16 * 32, 16, 1024);
-              if constexpr (PAIR)
-                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k16) != 0);
-              else
-                umma_bf16(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+              if constexpr (PAIR) {
+                if (args.fp8)
+                  umma_f8_pair(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+                else
+                  umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+              } else {
+                if (args.fp8)
+                  umma_f8(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+                else
+                  umma_bf16(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+              }
             }
             issued = true;
             if constexpr (PAIR)

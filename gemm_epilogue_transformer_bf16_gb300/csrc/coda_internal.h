@@ -52,6 +52,8 @@ cudaError_t launch_ce_onehot_prep(const int32_t* labels, int32_t ignore, int64_t
                                   int32_t* counts, int32_t* cursor, int32_t* off, int32_t* idx, cudaStream_t s);
 cudaError_t launch_ce_norm_coef(const float* pz, int64_t ld, int nparts, const float* target, const float* rstd,
                                 const float* rw, int64_t M, float inv_k, float* coef, cudaStream_t s);
+cudaError_t launch_quantize_fp8_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq,
+                                     int64_t ldq, float* scale, int num_sms, cudaStream_t s);
 cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 cudaError_t launch_rope_table(double theta, int head_dim, int max_pos, float2* cs, cudaStream_t s);
 cudaError_t launch_qk_bwd(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, const __nv_bfloat16* dV,

@@ -364,6 +364,39 @@ int coda_linear_sigmoid_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_
                             size_t ws_bytes, coda_stream stream);
 
 /* ------------------------------------------------------------------------
+ * FP8 (e4m3) operands: the same mainloop with tcgen05 kind::f8f6f4 and the
+ * same epilogues.  The pages motivate fusion by low-precision GEMMs ("CODA"
+ * §1: FP8 / FP4 make the materialised tensors' cost more important) but give
+ * no quantisation recipe; this library uses per-row scales:
+ *   scale_i = max_k |x_ik| / 448 (fp32; 1 for an all-zero row),
+ *   q_ik = e4m3(x_ik / scale_i)  (fp32 division, round to nearest even,
+ *   saturating), x ~= q * scale.
+ * Activations are scaled per token, weights per output channel.  FP8
+ * operands are K-major with K a multiple of 16 (16-byte rows).
+ * ---------------------------------------------------------------------- */
+
+/* X [M, K] bf16 (row stride ldx) -> Xq [M, K] e4m3 bytes (row stride K),
+ * scale [M] fp32. */
+int coda_quantize_fp8_rows(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq, float* scale,
+                           coda_stream stream);
+
+/* Y = R + (sx ⊙ Xq)(sw ⊙ Wq)^T: Xq [M, K], sx [M], Wq [N, K], sw [N],
+ * R [M, N] bf16 or NULL, Y [M, N] bf16. */
+size_t coda_linear_fp8_workspace_size(int64_t M, int64_t N, int64_t K);
+int coda_linear_fp8(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw, const coda_bf16* R,
+                    coda_bf16* Y, int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+
+/* linear_swiglu on e4m3 operands: g = r ⊙ (sx ⊙ Xq)(sg ⊙ Wgq)^T,
+ * u = r ⊙ (sx ⊙ Xq)(su ⊙ Wuq)^T, H = silu(g) ⊙ u.  rstd [M] or NULL (r = 1,
+ * the RMSNorm-reparameterised input when given with gamma-folded weights);
+ * Wgq, Wuq [I, K]; sg, su [I]; H, g_save, u_save [M, I] bf16. */
+size_t coda_linear_swiglu_fp8_workspace_size(int64_t M, int64_t I, int64_t K);
+int coda_linear_swiglu_fp8(const uint8_t* Xq, const float* sx, const float* rstd, const uint8_t* Wgq,
+                           const float* sg, const uint8_t* Wuq, const float* su, coda_bf16* H, coda_bf16* g_save,
+                           coda_bf16* u_save, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
+                           coda_stream stream);
+
+/* ------------------------------------------------------------------------
  * Final RMSNorm -> LM head -> cross-entropy ("CODA" §3.2.1, third site of
  * the GEMM-residual-RMSNorm-GEMM pattern: final down-projection -> residual
  * -> final RMSNorm -> language-model head)

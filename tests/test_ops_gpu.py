@@ -217,3 +217,38 @@ def test_linear_sigmoid(coda, gated, M, N, K):
     assert_bf16(g["dW"], b["dW"], "dW")
     if gated:
         assert_bf16(g["dZ"], b["dZ"], "dZ")
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) operands
+@pytest.mark.parametrize("M,N,K", [(512, 768, 512), (300, 264, 208)])
+def test_fp8_quantize_and_linear(coda, M, N, K):
+    X = synth.randn_bf16((M, K), 1.0, 1)
+    W = synth.randn_bf16((N, K), 1 / math.sqrt(K), 2)
+    R = synth.randn_bf16((M, N), 1.0, 3)
+    xq, sx = coda.quantize_fp8_rows(X.to(DEV))
+    wq, sw = coda.quantize_fp8_rows(W.to(DEV))
+    ocx, ovx, osx = O.quantize_fp8_rows(to_np(X))
+    ocw, ovw, osw = O.quantize_fp8_rows(to_np(W))
+    # the quantised codes and scales are decisions: bit-exact
+    assert np.array_equal(xq.cpu().numpy(), ocx) and np.array_equal(wq.cpu().numpy(), ocw)
+    assert np.array_equal(sx.cpu().numpy(), osx) and np.array_equal(sw.cpu().numpy(), osw)
+    Y = coda.linear_fp8(xq, sx, wq, sw, R.to(DEV))
+    assert_bf16(Y, O.linear_fp8_fwd(ovx, osx, ovw, osw, R=to_np(R)), "Y fp8")
+
+
+@pytest.mark.parametrize("shape", [synth.MlpShape(512, 512, 1408), synth.MlpShape(300, 272, 392)])
+def test_fp8_linear_swiglu(coda, shape):
+    t = synth.make_mlp(shape, seed=0)
+    d = dev(t)
+    r = coda.rms_rstd(d["X"], 1e-6)
+    xq, sx = coda.quantize_fp8_rows(d["X"])
+    gq, sg = coda.quantize_fp8_rows(d["Wg"])
+    uq, su = coda.quantize_fp8_rows(d["Wu"])
+    H, g, u = coda.linear_swiglu_fp8(xq, sx, gq, sg, uq, su, rstd=r)
+    _, ovx, osx = O.quantize_fp8_rows(to_np(t["X"]))
+    _, ovg, osg = O.quantize_fp8_rows(to_np(t["Wg"]))
+    _, ovu, osu = O.quantize_fp8_rows(to_np(t["Wu"]))
+    Hr, gr, ur = O.swiglu_fp8_fwd(ovx, osx, ovg, osg, ovu, osu, row_scale=O.rms_inv(to_np(t["X"]), 1e-6))
+    assert_bf16(H, Hr, "H fp8")
+    assert_bf16(g, gr, "g fp8")
+    assert_bf16(u, ur, "u fp8")
