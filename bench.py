@@ -503,6 +503,35 @@ def main():
             "fwd_bwd_tflops": round(f_all / ((mf + mb) / 1e3) / 1e12, 1)}
         del ce, dc
 
+        # FP8 (e4m3) gate/up + SwiGLU at the block's shape (NEXT row: the same
+        # mainloop with kind::f8f6f4), beside the bf16 launch timed above.
+        T_, H_, I_ = s.tokens, s.hidden, s.inter
+        r_ = coda.rms_rstd(t["x0"], s.eps)
+        xq, sx = coda.quantize_fp8_rows(t["x0"])
+        gq, sg = coda.quantize_fp8_rows(t["Wg"])
+        uq, su = coda.quantize_fp8_rows(t["Wu"])
+        Hq = torch.empty(T_, I_, dtype=torch.bfloat16, device=dev)
+        gq8, uq8 = torch.empty_like(Hq), torch.empty_like(Hq)
+        ws8 = coda.workspace(256, dev)
+        f8 = []
+        for i in range(5):
+            ev[0].record(stream)
+            coda.linear_swiglu_fp8(xq, sx, gq, sg, uq, su, rstd=r_, H=Hq, g=gq8, u=uq8, ws=ws8)
+            ev[1].record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 2:
+                f8.append(ev[0].elapsed_time(ev[1]))
+        if coda.get_status(ws8) != 0:
+            raise RuntimeError("device status error in the FP8 measurement")
+        m8 = statistics.median(f8)
+        fp8_peak = 2 * burst
+        other["fp8_gateup_swiglu"] = {
+            "workload": "e4m3 gate/up GEMM with row-scale + SwiGLU epilogue, 8192 x 2x28672 x 8192, per-row scales",
+            "ms": round(m8, 3), "tflops": round(gf[DOMINANT] / (m8 / 1e3) / 1e12, 1),
+            "peak": round(fp8_peak, 1), "peak_kind": f"fp8 = 2 x bf16 burst ({peak_src}, nominal ratio)",
+            "frac": round(gf[DOMINANT] / (m8 / 1e3) / 1e12 / fp8_peak, 4)}
+        del xq, gq, uq, Hq, gq8, uq8
+
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.tokens == synth.FULL["c5"].tokens:

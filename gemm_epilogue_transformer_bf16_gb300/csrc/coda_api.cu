@@ -187,7 +187,6 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   a.num_n = static_cast<int>(cdiv(p.N, p.b_dual ? BN / 2 : BN));
   a.kb0 = static_cast<int>(cdiv(p.K, kbox));
   a.kb1 = p.K2 > 0 ? static_cast<int>(cdiv(p.K2, kbox)) : 0;
-  a.fp8 = p.fp8;
   a.a_mn = p.a_mn;
   a.b_mn = p.b_mn;
   a.b_dual = p.b_dual;
@@ -203,6 +202,15 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   a.e.st_stream = (l2_hints() & 4) ? 1 : 0;
   const int nu = a.num_units;
   cudaError_t err;
+  if (p.fp8) {
+    if (p.kind == coda::EpiKind::Plain)
+      err = coda::launch_gemm_plain_fp8(nu, sms, pair, s, maps, a);
+    else if (p.kind == coda::EpiKind::Swiglu)
+      err = coda::launch_gemm_swiglu_fp8(nu, sms, pair, s, maps, a);
+    else
+      return CODA_ERR_UNSUPPORTED;
+    return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
+  }
   switch (p.kind) {
     case coda::EpiKind::Plain: err = coda::launch_gemm_plain(nu, sms, pair, s, maps, a); break;
     case coda::EpiKind::Swiglu: err = coda::launch_gemm_swiglu(nu, sms, pair, s, maps, a); break;

@@ -43,7 +43,7 @@ struct EpiPlain {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
@@ -155,7 +155,7 @@ struct EpiSwiglu {
   static constexpr int HALF = BN / 2;
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     const float rs = ((e.row_scale && rv) ? e.row_scale[row] : 1.f) * ((e.row_scale2 && rv) ? e.row_scale2[row] : 1.f);
@@ -211,7 +211,7 @@ struct EpiDSwiglu {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
@@ -269,7 +269,7 @@ struct EpiColDot {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     const int lane = threadIdx.x & 31;
@@ -381,7 +381,7 @@ struct EpiCeLse {
       reinterpret_cast<float2*>(e.partials)[static_cast<int64_t>(t.unit_chunk) * e.ld_part + t.row] =
           make_float2(st.m, st.s);
   }
-  static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t, float*) {
+  static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t) {
     const bool rv = t.row < t.M;
     const float rs = (e.row_scale && rv) ? e.row_scale[t.row] : 1.f;
 #pragma unroll 1
@@ -441,7 +441,7 @@ struct EpiCeDlogits {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     int lab = -1;
@@ -500,7 +500,7 @@ struct EpiSigmoid {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
@@ -558,7 +558,7 @@ struct EpiQkRope {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t, float*) {
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     constexpr int D = 128;
     const int row = t.row;
     const bool rv = row < t.M;

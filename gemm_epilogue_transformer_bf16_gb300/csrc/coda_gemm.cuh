@@ -40,7 +40,6 @@ namespace coda {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int NUM_THREADS = 192;
-constexpr int EPI_WARP0 = 2;
 
 // PAIR: a cluster of two CTAs on two SMs computes a 256 x BN tile with
 // tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of A and half of
@@ -57,8 +56,7 @@ struct GemmCfg {
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr uint32_t BAR_BYTES = 256;
-  static constexpr uint32_t EPI_SMEM_BYTES = 0;
-  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + EPI_SMEM_BYTES;
+  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
@@ -134,7 +132,6 @@ struct GemmArgs {
   int* status;
   uint64_t timeout_ns;
   int l2_hints;      // bit 0: A loads evict_last, bit 1: B loads evict_first
-  int fp8;           // e4m3 operands: 128 elements per 128-byte k-slice, kind::f8f6f4
   EpiArgs e;
 };
 
@@ -166,11 +163,9 @@ __device__ __forceinline__ void unit_coords(const GemmArgs& a, int u, int& mb, i
   }
 }
 
-__device__ __forceinline__ void epi_bar_sync() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
-template <int BN, class Epi, bool PAIR>
+// FP8: e4m3 operands, tcgen05.mma kind::f8f6f4, 128 elements per 128-byte
+// k-slice (a compile-time variant, so the bf16 kernels hold only kind::f16).
+template <int BN, class Epi, bool PAIR, bool FP8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     coda_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mB0,
                      const __grid_constant__ CUtensorMap mA1, const __grid_constant__ CUtensorMap mB1,
@@ -187,7 +182,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* epi_smem = reinterpret_cast<float*>(smem + S * Cfg::STAGE_BYTES + Cfg::BAR_BYTES);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -258,7 +252,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool second = kb >= args.kb0;
             const CUtensorMap* ma = second ? &mA1 : &mA0;
             const CUtensorMap* mbp = second ? &mB1 : &mB0;
-            const int k = (second ? kb - args.kb0 : kb) * (args.fp8 ? 2 * BK : BK);
+            const int k = (second ? kb - args.kb0 : kb) * (FP8 ? 2 * BK : BK);
             uint8_t* sa = tiles + s * Cfg::STAGE_BYTES;
             uint8_t* sb = sa + Cfg::A_BYTES;
             if constexpr (PAIR) {
@@ -361,17 +355,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                             : sdesc_sw128(sa + k16 * 32, 16, 1024);
               const uint64_t bd = args.b_mn ? sdesc_sw128(sb + k16 * 2048, 8192, 1024)
                                             : sdesc_sw128(sb + k16 * 32, 16, 1024);
-              if constexpr (PAIR) {
-                if (args.fp8)
-                  umma_f8_pair(d_tmem, ad, bd, idesc, (kb | k16) != 0);
-                else
-                  umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k16) != 0);
-              } else {
-                if (args.fp8)
-                  umma_f8(d_tmem, ad, bd, idesc, (kb | k16) != 0);
-                else
-                  umma_bf16(d_tmem, ad, bd, idesc, (kb | k16) != 0);
-              }
+              if constexpr (PAIR && FP8)
+                umma_f8_pair(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+              else if constexpr (PAIR)
+                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+              else if constexpr (FP8)
+                umma_f8(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+              else
+                umma_bf16(d_tmem, ad, bd, idesc, (kb | k16) != 0);
             }
             issued = true;
             if constexpr (PAIR)
@@ -421,7 +412,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         ti.nb = nb0 + j;
         ti.taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
-        Epi::tile(st, args.e, ti, epi_smem);
+        Epi::tile(st, args.e, ti);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {

@@ -28,6 +28,10 @@ cudaError_t launch_gemm_cedlogits(int num_units, int sms, bool pair, cudaStream_
                                const GemmArgs& a);
 cudaError_t launch_gemm_sigmoid(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
                                 const GemmArgs& a);
+cudaError_t launch_gemm_plain_fp8(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                                  const GemmArgs& a);
+cudaError_t launch_gemm_swiglu_fp8(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+                                   const GemmArgs& a);
 cudaError_t launch_gemm_coldot(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
 

@@ -9,7 +9,7 @@
 
 namespace coda {
 
-template <int BN, class Epi, bool PAIR>
+template <int BN, class Epi, bool PAIR, bool FP8>
 cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a) {
   constexpr uint32_t smem = GemmCfg<BN, PAIR>::SMEM_BYTES;
   static bool attr_done[64] = {};
@@ -18,7 +18,7 @@ cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CU
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  auto kern = coda_gemm_kernel<BN, Epi, PAIR>;
+  auto kern = coda_gemm_kernel<BN, Epi, PAIR, FP8>;
   if (!attr_done[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -53,11 +53,11 @@ cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CU
   return cudaGetLastError();
 }
 
-template <int BN, class Epi>
+template <int BN, class Epi, bool FP8 = false>
 cudaError_t launch_gemm_impl(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
                              const GemmArgs& a) {
-  return pair ? launch_gemm_variant<BN, Epi, true>(num_units, sms, s, m, a)
-              : launch_gemm_variant<BN, Epi, false>(num_units, sms, s, m, a);
+  return pair ? launch_gemm_variant<BN, Epi, true, FP8>(num_units, sms, s, m, a)
+              : launch_gemm_variant<BN, Epi, false, FP8>(num_units, sms, s, m, a);
 }
 
 }  // namespace coda
