@@ -111,26 +111,35 @@ struct Plan {
   EpiArgs e{};
 };
 
-// CTA pairs (cta_group::2, 256-row tiles) halve each SM's B traffic; a
-// problem of one 128-row block keeps single CTAs.  CODA_CTA_PAIR=0 in the
-// environment selects single CTAs everywhere (for comparisons).
-bool use_pairs(int64_t M) {
-  static const bool enabled = [] {
+// Cluster size of a GEMM launch.  CTA pairs (cta_group::2, 256-row tiles)
+// halve each SM's B traffic; two pairs on adjacent 256-row blocks that share
+// the B tile through TMA multicast cut each SM's operand traffic by another
+// quarter.  A problem of one 128-row block keeps single CTAs.  In the
+// environment, CODA_CTA_PAIR=0 selects single CTAs everywhere and
+// CODA_CTA_QUAD=0 stops at pairs (for comparisons).
+int cluster_ctas(int64_t M) {
+  static const bool pairs = [] {
     const char* v = std::getenv("CODA_CTA_PAIR");
     return !(v && v[0] == '0');
   }();
-  return enabled && M > coda::BM;
+  static const bool quads = [] {
+    const char* v = std::getenv("CODA_CTA_QUAD");
+    return !(v && v[0] == '0');
+  }();
+  if (!pairs || M <= coda::BM) return 1;
+  return (quads && M > 2 * coda::BM) ? 4 : 2;
 }
 
-// Tile rows (units of the M tile) per raster group: concurrent tiles share
-// these rows' A panel in L2 while B streams.  CODA_GROUP_M overrides it.
-int group_m(bool pair) {
+// Units of the M tile per raster group (2048 rows by default): concurrent
+// tiles share these rows' A panel in L2 while B streams.  CODA_GROUP_M
+// overrides it.
+int group_m(int cg) {
   static const int env = [] {
     const char* v = std::getenv("CODA_GROUP_M");
     return v ? std::atoi(v) : 0;
   }();
   if (env > 0) return env;
-  return pair ? 8 : 16;
+  return 16 / cg;
 }
 
 // L2 cache-hint selection for the GEMM launches: bit 0 = A loads evict_last,
@@ -149,8 +158,11 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   if (!get_encoder()) return CODA_ERR_CUDA;
   const int sms = num_sms();
   if (sms <= 0) return CODA_ERR_CUDA;
-  const bool pair = use_pairs(p.M);
-  const uint32_t b_box_rows = pair ? BN / 2 : BN;  // K-major B rows one CTA stages
+  const int cg = cluster_ctas(p.M);
+  const bool pair = cg >= 2;
+  // K-major B rows one TMA copy stages: the tile's N, its half per pair CTA,
+  // a quarter per CTA with two pairs (each copy multicast to both pairs)
+  const uint32_t b_box_rows = static_cast<uint32_t>(BN / cg);
   CUtensorMap maps[4];
   std::memset(maps, 0, sizeof(maps));
   // A operands
@@ -167,8 +179,9 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   };
   if (!enc_a(&maps[0], p.A, p.lda, p.K)) return CODA_ERR_CUDA;
   if (p.b_dual) {
-    if (!encode_map(&maps[1], p.B, p.N, p.K, p.ldb, kbox, BN / 2, esz)) return CODA_ERR_CUDA;
-    if (!encode_map(&maps[3], p.B2, p.N, p.K, p.ldb2, kbox, BN / 2, esz)) return CODA_ERR_CUDA;
+    const uint32_t rows = cg == 4 ? BN / 4 : BN / 2;
+    if (!encode_map(&maps[1], p.B, p.N, p.K, p.ldb, kbox, rows, esz)) return CODA_ERR_CUDA;
+    if (!encode_map(&maps[3], p.B2, p.N, p.K, p.ldb2, kbox, rows, esz)) return CODA_ERR_CUDA;
     maps[2] = maps[0];
   } else {
     if (!enc_b(&maps[1], p.B, p.ldb, p.K)) return CODA_ERR_CUDA;
@@ -183,7 +196,7 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   GemmArgs a{};
   a.M = static_cast<int>(p.M);
   a.N = static_cast<int>(p.N);
-  a.num_m = static_cast<int>(cdiv(p.M, pair ? 2 * coda::BM : coda::BM));
+  a.num_m = static_cast<int>(cdiv(p.M, cg * coda::BM));
   a.num_n = static_cast<int>(cdiv(p.N, p.b_dual ? BN / 2 : BN));
   a.kb0 = static_cast<int>(cdiv(p.K, kbox));
   a.kb1 = p.K2 > 0 ? static_cast<int>(cdiv(p.K2, kbox)) : 0;
@@ -192,7 +205,7 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   a.b_dual = p.b_dual;
   a.n_per_unit = p.n_per_unit;
   a.num_units = p.n_per_unit > 1 ? a.num_m * static_cast<int>(cdiv(a.num_n, p.n_per_unit)) : a.num_m * a.num_n;
-  a.group_m = group_m(pair);
+  a.group_m = group_m(cg);
   a.idesc = p.fp8 ? coda::idesc_e4m3(pair ? 2 * coda::BM : coda::BM, BN)
                   : coda::idesc_bf16(pair ? 2 * coda::BM : coda::BM, BN, p.a_mn, p.b_mn);
   a.status = status;
@@ -204,22 +217,22 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   cudaError_t err;
   if (p.fp8) {
     if (p.kind == coda::EpiKind::Plain)
-      err = coda::launch_gemm_plain_fp8(nu, sms, pair, s, maps, a);
+      err = coda::launch_gemm_plain_fp8(nu, sms, cg, s, maps, a);
     else if (p.kind == coda::EpiKind::Swiglu)
-      err = coda::launch_gemm_swiglu_fp8(nu, sms, pair, s, maps, a);
+      err = coda::launch_gemm_swiglu_fp8(nu, sms, cg, s, maps, a);
     else
       return CODA_ERR_UNSUPPORTED;
     return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
   }
   switch (p.kind) {
-    case coda::EpiKind::Plain: err = coda::launch_gemm_plain(nu, sms, pair, s, maps, a); break;
-    case coda::EpiKind::Swiglu: err = coda::launch_gemm_swiglu(nu, sms, pair, s, maps, a); break;
-    case coda::EpiKind::DSwiglu: err = coda::launch_gemm_dswiglu(nu, sms, pair, s, maps, a); break;
-    case coda::EpiKind::QkRope: err = coda::launch_gemm_qkrope(nu, sms, pair, s, maps, a); break;
-    case coda::EpiKind::CeLse: err = coda::launch_gemm_celse(nu, sms, pair, s, maps, a); break;
-    case coda::EpiKind::CeDlogits: err = coda::launch_gemm_cedlogits(nu, sms, pair, s, maps, a); break;
-    case coda::EpiKind::ColDot: err = coda::launch_gemm_coldot(nu, sms, pair, s, maps, a); break;
-    case coda::EpiKind::Sigmoid: err = coda::launch_gemm_sigmoid(nu, sms, pair, s, maps, a); break;
+    case coda::EpiKind::Plain: err = coda::launch_gemm_plain(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::Swiglu: err = coda::launch_gemm_swiglu(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::DSwiglu: err = coda::launch_gemm_dswiglu(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::QkRope: err = coda::launch_gemm_qkrope(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::CeLse: err = coda::launch_gemm_celse(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::CeDlogits: err = coda::launch_gemm_cedlogits(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::ColDot: err = coda::launch_gemm_coldot(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::Sigmoid: err = coda::launch_gemm_sigmoid(nu, sms, cg, s, maps, a); break;
     default: return CODA_ERR_INVALID_ARG;
   }
   return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;

@@ -163,13 +163,21 @@ __device__ __forceinline__ void unit_coords(const GemmArgs& a, int u, int& mb, i
   }
 }
 
+// CG: CTAs per cluster.  1 = single CTAs (M = 128 tiles); 2 = a CTA pair
+// (cta_group::2, M = 256); 4 = two CTA pairs on adjacent 256-row blocks that
+// share the B tile: each CTA loads half of its B rows and multicasts them to
+// the CTA at the same position in the other pair, so every SM stages 24 KB
+// per k-slice instead of 32 KB.
 // FP8: e4m3 operands, tcgen05.mma kind::f8f6f4, 128 elements per 128-byte
 // k-slice (a compile-time variant, so the bf16 kernels hold only kind::f16).
-template <int BN, class Epi, bool PAIR, bool FP8 = false>
+template <int BN, class Epi, int CG, bool FP8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     coda_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mB0,
                      const __grid_constant__ CUtensorMap mA1, const __grid_constant__ CUtensorMap mB1,
                      const GemmArgs args) {
+  constexpr bool PAIR = CG >= 2;
+  constexpr bool QUAD = CG == 4;
+  static_assert(CG == 1 || CG == 2 || CG == 4, "cluster size");
   using Cfg = GemmCfg<BN, PAIR>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -185,17 +193,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // In a pair, CTA rank 0 issues the MMAs and owns the "full" and
+  // In a pair, the even CTA issues the MMAs and owns the "full" and
   // "TMEM empty" barriers; both CTAs load, and both run epilogues.
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  const bool leader = rank == 0;
-  const int cluster_id = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int num_clusters = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const uint32_t pair_lead = rank & ~1u;
+  const bool leader = (rank & 1u) == 0;
+  const int cluster_id = static_cast<int>(blockIdx.x) / CG;
+  const int num_clusters = static_cast<int>(gridDim.x) / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], QUAD ? 2 : 1);  // one commit per pair reading the stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -228,7 +237,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues the copies.
+    const uint32_t el = elect_one();
+    {
       // A panels are shared by the raster group's successive waves; B tiles
       // only by the tiles of one wave.
       const bool hint_a = args.l2_hints & 1, hint_b = args.l2_hints & 2;
@@ -238,7 +249,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters) {
         int mb2, nb0, nlen, chunk;
         unit_coords(args, u, mb2, nb0, nlen, chunk);
-        const int mb = PAIR ? mb2 * 2 + static_cast<int>(rank) : mb2;
+        const int mb = mb2 * CG + static_cast<int>(rank);
         for (int j = 0; j < nlen && !aborted; ++j) {
           const int nb = nb0 + j;
           for (int kb = 0; kb < num_kb; ++kb, ++it) {
@@ -248,7 +259,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               aborted = true;
               break;
             }
-            if (leader) mbar_arrive_expect_tx(&full[s], PAIR ? 2 * Cfg::STAGE_BYTES : Cfg::STAGE_BYTES);
+            if (leader) mbar_arrive_expect_tx(&full[s], PAIR ? 2 * Cfg::STAGE_BYTES : Cfg::STAGE_BYTES, el);
             const bool second = kb >= args.kb0;
             const CUtensorMap* ma = second ? &mA1 : &mA0;
             const CUtensorMap* mbp = second ? &mB1 : &mB0;
@@ -256,51 +267,67 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint8_t* sa = tiles + s * Cfg::STAGE_BYTES;
             uint8_t* sb = sa + Cfg::A_BYTES;
             if constexpr (PAIR) {
-              const uint32_t bar = mapa_shared(&full[s], 0);
+              const uint32_t bar = mapa_shared(&full[s], pair_lead);
               if (!args.a_mn) {
-                hint_a ? tma_load_2d_pair_hint(sa, ma, bar, k, mb * BM, pol_a) : tma_load_2d_pair(sa, ma, bar, k, mb * BM);
+                hint_a ? tma_load_2d_pair_hint(sa, ma, bar, k, mb * BM, pol_a, el)
+                       : tma_load_2d_pair(sa, ma, bar, k, mb * BM, el);
               } else {
 #pragma unroll
                 for (int c = 0; c < BM / 64; ++c)
-                  hint_a ? tma_load_2d_pair_hint(sa + c * 8192, ma, bar, mb * BM + c * 64, k, pol_a)
-                         : tma_load_2d_pair(sa + c * 8192, ma, bar, mb * BM + c * 64, k);
+                  hint_a ? tma_load_2d_pair_hint(sa + c * 8192, ma, bar, mb * BM + c * 64, k, pol_a, el)
+                         : tma_load_2d_pair(sa + c * 8192, ma, bar, mb * BM + c * 64, k, el);
               }
-              if (args.b_dual) {
+              if constexpr (QUAD) {
+                // this CTA's B rows (as in a pair) split in two 64-row halves:
+                // half h is loaded by the CTA of pair h and lands in both pairs
+                const int h = static_cast<int>(rank >> 1);
+                const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ 2u)));
+                const int odd = static_cast<int>(rank & 1u);
+                if (args.b_dual)
+                  tma_load_2d_pair_mc(sb + h * 8192, odd ? &mB1 : &mB0, bar, k, nb * (BN / 2) + h * 64, mask, el);
+                else if (!args.b_mn)
+                  tma_load_2d_pair_mc(sb + h * 8192, mbp, bar, k, nb * BN + odd * Cfg::B_ROWS + h * 64, mask, el);
+                else
+                  tma_load_2d_pair_mc(sb + h * 8192, mbp, bar, nb * BN + odd * Cfg::B_ROWS + h * 64, k, mask, el);
+              } else if (args.b_dual) {
                 // the pair's N = [gate rows | up rows]: rank 0 stages the gate half, rank 1 the up half
-                hint_b ? tma_load_2d_pair_hint(sb, rank ? &mB1 : &mB0, bar, k, nb * (BN / 2), pol_b)
-                       : tma_load_2d_pair(sb, rank ? &mB1 : &mB0, bar, k, nb * (BN / 2));
+                hint_b ? tma_load_2d_pair_hint(sb, rank ? &mB1 : &mB0, bar, k, nb * (BN / 2), pol_b, el)
+                       : tma_load_2d_pair(sb, rank ? &mB1 : &mB0, bar, k, nb * (BN / 2), el);
               } else if (!args.b_mn) {
-                hint_b ? tma_load_2d_pair_hint(sb, mbp, bar, k, nb * BN + static_cast<int>(rank) * Cfg::B_ROWS, pol_b)
-                       : tma_load_2d_pair(sb, mbp, bar, k, nb * BN + static_cast<int>(rank) * Cfg::B_ROWS);
+                hint_b ? tma_load_2d_pair_hint(sb, mbp, bar, k, nb * BN + static_cast<int>(rank) * Cfg::B_ROWS, pol_b,
+                                               el)
+                       : tma_load_2d_pair(sb, mbp, bar, k, nb * BN + static_cast<int>(rank) * Cfg::B_ROWS, el);
               } else {
 #pragma unroll
                 for (int c = 0; c < Cfg::B_ROWS / 64; ++c)
                   hint_b ? tma_load_2d_pair_hint(sb + c * 8192, mbp, bar,
-                                                 nb * BN + static_cast<int>(rank) * Cfg::B_ROWS + c * 64, k, pol_b)
+                                                 nb * BN + static_cast<int>(rank) * Cfg::B_ROWS + c * 64, k, pol_b, el)
                          : tma_load_2d_pair(sb + c * 8192, mbp, bar,
-                                            nb * BN + static_cast<int>(rank) * Cfg::B_ROWS + c * 64, k);
+                                            nb * BN + static_cast<int>(rank) * Cfg::B_ROWS + c * 64, k, el);
               }
             } else {
               if (!args.a_mn) {
-                hint_a ? tma_load_2d_hint(sa, ma, &full[s], k, mb * BM, pol_a) : tma_load_2d(sa, ma, &full[s], k, mb * BM);
+                hint_a ? tma_load_2d_hint(sa, ma, &full[s], k, mb * BM, pol_a, el)
+                       : tma_load_2d(sa, ma, &full[s], k, mb * BM, el);
               } else {
 #pragma unroll
                 for (int c = 0; c < BM / 64; ++c)
-                  hint_a ? tma_load_2d_hint(sa + c * 8192, ma, &full[s], mb * BM + c * 64, k, pol_a)
-                         : tma_load_2d(sa + c * 8192, ma, &full[s], mb * BM + c * 64, k);
+                  hint_a ? tma_load_2d_hint(sa + c * 8192, ma, &full[s], mb * BM + c * 64, k, pol_a, el)
+                         : tma_load_2d(sa + c * 8192, ma, &full[s], mb * BM + c * 64, k, el);
               }
               if (args.b_dual) {
-                hint_b ? tma_load_2d_hint(sb, &mB0, &full[s], k, nb * (BN / 2), pol_b)
-                       : tma_load_2d(sb, &mB0, &full[s], k, nb * (BN / 2));
-                hint_b ? tma_load_2d_hint(sb + (BN / 2) * 128, &mB1, &full[s], k, nb * (BN / 2), pol_b)
-                       : tma_load_2d(sb + (BN / 2) * 128, &mB1, &full[s], k, nb * (BN / 2));
+                hint_b ? tma_load_2d_hint(sb, &mB0, &full[s], k, nb * (BN / 2), pol_b, el)
+                       : tma_load_2d(sb, &mB0, &full[s], k, nb * (BN / 2), el);
+                hint_b ? tma_load_2d_hint(sb + (BN / 2) * 128, &mB1, &full[s], k, nb * (BN / 2), pol_b, el)
+                       : tma_load_2d(sb + (BN / 2) * 128, &mB1, &full[s], k, nb * (BN / 2), el);
               } else if (!args.b_mn) {
-                hint_b ? tma_load_2d_hint(sb, mbp, &full[s], k, nb * BN, pol_b) : tma_load_2d(sb, mbp, &full[s], k, nb * BN);
+                hint_b ? tma_load_2d_hint(sb, mbp, &full[s], k, nb * BN, pol_b, el)
+                       : tma_load_2d(sb, mbp, &full[s], k, nb * BN, el);
               } else {
 #pragma unroll
                 for (int c = 0; c < BN / 64; ++c)
-                  hint_b ? tma_load_2d_hint(sb + c * 8192, mbp, &full[s], nb * BN + c * 64, k, pol_b)
-                         : tma_load_2d(sb + c * 8192, mbp, &full[s], nb * BN + c * 64, k);
+                  hint_b ? tma_load_2d_hint(sb + c * 8192, mbp, &full[s], nb * BN + c * 64, k, pol_b, el)
+                         : tma_load_2d(sb + c * 8192, mbp, &full[s], nb * BN + c * 64, k, el);
               }
             }
           }
@@ -321,7 +348,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
-    if (lane == 0 && leader) {
+    // The whole warp of the pair's even CTA runs the loop; one elected lane
+    // issues the MMAs and commits.
+    if (leader) {
+      const uint32_t el = elect_one();
       uint32_t it = 0, t = 0;
       bool issued = false;
       const uint32_t idesc = args.idesc;
@@ -355,33 +385,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                             : sdesc_sw128(sa + k16 * 32, 16, 1024);
               const uint64_t bd = args.b_mn ? sdesc_sw128(sb + k16 * 2048, 8192, 1024)
                                             : sdesc_sw128(sb + k16 * 32, 16, 1024);
+              const uint32_t acc = (kb | k16) != 0;
               if constexpr (PAIR && FP8)
-                umma_f8_pair(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+                umma_f8_pair(d_tmem, ad, bd, idesc, acc, el);
               else if constexpr (PAIR)
-                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+                umma_bf16_pair(d_tmem, ad, bd, idesc, acc, el);
               else if constexpr (FP8)
-                umma_f8(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+                umma_f8(d_tmem, ad, bd, idesc, acc, el);
               else
-                umma_bf16(d_tmem, ad, bd, idesc, (kb | k16) != 0);
+                umma_bf16(d_tmem, ad, bd, idesc, acc, el);
             }
             issued = true;
-            if constexpr (PAIR)
-              umma_commit_pair_mc(&empty[s], 0x3);
+            if constexpr (QUAD)
+              umma_commit_pair_mc(&empty[s], 0xF, el);  // the stage's B halves live in all four CTAs
+            else if constexpr (PAIR)
+              umma_commit_pair_mc(&empty[s], 0x3, el);
             else
-              umma_commit(&empty[s]);
+              umma_commit(&empty[s], el);
           }
           if (aborted) break;
           if constexpr (PAIR)
-            umma_commit_pair_mc(&tfull[buf], 0x3);
+            umma_commit_pair_mc(&tfull[buf], static_cast<uint16_t>(0x3u << pair_lead), el);
           else
-            umma_commit(&tfull[buf]);
+            umma_commit(&tfull[buf], el);
         }
       }
       if (aborted && issued) {
         if constexpr (PAIR)
-          umma_commit_pair(drain);
+          umma_commit_pair(drain, el);
         else
-          umma_commit(drain);
+          umma_commit(drain, el);
         mbar_wait_drain(drain, 0, 200000000ull);
       }
     }
@@ -392,7 +425,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters) {
       int mb2, nb0, nlen, chunk;
       unit_coords(args, u, mb2, nb0, nlen, chunk);
-      const int mb = PAIR ? mb2 * 2 + static_cast<int>(rank) : mb2;
+      const int mb = mb2 * CG + static_cast<int>(rank);
       TileInfo ti;
       ti.mb = mb;
       ti.unit_chunk = chunk;
@@ -417,7 +450,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           if constexpr (PAIR)
-            mbar_arrive_cluster(mapa_shared(&tempty[buf], 0));
+            mbar_arrive_cluster(mapa_shared(&tempty[buf], pair_lead));
           else
             mbar_arrive(&tempty[buf]);
         }

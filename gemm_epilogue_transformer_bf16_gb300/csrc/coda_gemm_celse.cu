@@ -1,10 +1,10 @@
 // Instantiations of the persistent GEMM with the EpiCeLse epilogue (BN = 256),
-// single-CTA and CTA-pair variants.
+// single-CTA, CTA-pair and two-pair (shared B) variants.
 #include "coda_launch.cuh"
 
 namespace coda {
-cudaError_t launch_gemm_celse(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_celse(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                 const GemmArgs& a) {
-  return launch_gemm_impl<256, EpiCeLse<256>>(num_units, sms, pair, s, m, a);
+  return launch_gemm_impl<256, EpiCeLse<256>>(num_units, sms, cg, s, m, a);
 }
 }  // namespace coda

@@ -1,14 +1,14 @@
 // Instantiations of the persistent GEMM on e4m3 operands (kind::f8f6f4) with
-// the EpiPlain and EpiSwiglu epilogues (BN = 256), single-CTA and CTA-pair.
+// the EpiPlain and EpiSwiglu epilogues (BN = 256), single-CTA, CTA-pair and two-pair variants.
 #include "coda_launch.cuh"
 
 namespace coda {
-cudaError_t launch_gemm_plain_fp8(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_plain_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                   const GemmArgs& a) {
-  return launch_gemm_impl<256, EpiPlain<256>, true>(num_units, sms, pair, s, m, a);
+  return launch_gemm_impl<256, EpiPlain<256>, true>(num_units, sms, cg, s, m, a);
 }
-cudaError_t launch_gemm_swiglu_fp8(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_swiglu_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                    const GemmArgs& a) {
-  return launch_gemm_impl<256, EpiSwiglu<256>, true>(num_units, sms, pair, s, m, a);
+  return launch_gemm_impl<256, EpiSwiglu<256>, true>(num_units, sms, cg, s, m, a);
 }
 }  // namespace coda

@@ -12,27 +12,28 @@ namespace coda {
 
 enum class EpiKind : int { Plain = 0, Swiglu, DSwiglu, QkRope, CeLse, CeDlogits, ColDot, Sigmoid };
 
-// Tensor maps in the order A0, B0, A1, B1.  `pair` selects the CTA-pair
-// (cta_group::2) variant; the launcher sizes the persistent grid.
-cudaError_t launch_gemm_plain(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+// Tensor maps in the order A0, B0, A1, B1.  `cg` is the cluster size: 1
+// (single CTAs), 2 (a cta_group::2 pair) or 4 (two pairs sharing B by TMA
+// multicast); the launcher sizes the persistent grid.
+cudaError_t launch_gemm_plain(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
-cudaError_t launch_gemm_swiglu(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_swiglu(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
-cudaError_t launch_gemm_dswiglu(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_dswiglu(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
-cudaError_t launch_gemm_qkrope(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_qkrope(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
-cudaError_t launch_gemm_celse(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_celse(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
-cudaError_t launch_gemm_cedlogits(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_cedlogits(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
-cudaError_t launch_gemm_sigmoid(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_sigmoid(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                 const GemmArgs& a);
-cudaError_t launch_gemm_plain_fp8(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_plain_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                   const GemmArgs& a);
-cudaError_t launch_gemm_swiglu_fp8(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_swiglu_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                    const GemmArgs& a);
-cudaError_t launch_gemm_coldot(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_coldot(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
 
 // auxiliary kernels (coda_aux.cu)

@@ -1,24 +1,25 @@
 // Launch helper for one (tile width, epilogue) instantiation of
 // coda_gemm_kernel: raises the dynamic shared-memory limit once per device and
 // launches the persistent grid -- one 192-thread CTA per SM, or, for the
-// CTA-pair variant, one 2-CTA cluster per SM pair (as many as can be resident
-// at once, which cudaOccupancyMaxActiveClusters reports).
+// clustered variants (CTA pairs, two pairs sharing B), as many 2- or 4-CTA
+// clusters as can be resident at once (cudaOccupancyMaxActiveClusters).
 #pragma once
+#include <cstdio>
 #include "coda_epilogues.cuh"
 #include "coda_internal.h"
 
 namespace coda {
 
-template <int BN, class Epi, bool PAIR, bool FP8>
+template <int BN, class Epi, int CG, bool FP8>
 cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a) {
-  constexpr uint32_t smem = GemmCfg<BN, PAIR>::SMEM_BYTES;
+  constexpr uint32_t smem = GemmCfg<BN, (CG >= 2)>::SMEM_BYTES;
   static bool attr_done[64] = {};
   static int max_clusters[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  auto kern = coda_gemm_kernel<BN, Epi, PAIR, FP8>;
+  auto kern = coda_gemm_kernel<BN, Epi, CG, FP8>;
   if (!attr_done[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -29,22 +30,25 @@ cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CU
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  if constexpr (PAIR) {
+  if constexpr (CG >= 2) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (max_clusters[dev] == 0) {
-      cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+      cfg.gridDim = dim3(static_cast<unsigned>(sms - sms % CG));
       int n = 0;
       e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
       if (e != cudaSuccess) return e;
       if (n <= 0) return cudaErrorInvalidConfiguration;
       max_clusters[dev] = n;
+#ifdef CODA_DEBUG_LAUNCH
+      fprintf(stderr, "coda: cluster size %d, %d resident clusters\n", CG, n);
+#endif
     }
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(num_units, max_clusters[dev])));
+    cfg.gridDim = dim3(static_cast<unsigned>(CG * std::min(num_units, max_clusters[dev])));
   } else {
     cfg.gridDim = dim3(static_cast<unsigned>(std::min(num_units, sms)));
   }
@@ -54,10 +58,14 @@ cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CU
 }
 
 template <int BN, class Epi, bool FP8 = false>
-cudaError_t launch_gemm_impl(int num_units, int sms, bool pair, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_impl(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                              const GemmArgs& a) {
-  return pair ? launch_gemm_variant<BN, Epi, true, FP8>(num_units, sms, s, m, a)
-              : launch_gemm_variant<BN, Epi, false, FP8>(num_units, sms, s, m, a);
+  switch (cg) {
+    case 1: return launch_gemm_variant<BN, Epi, 1, FP8>(num_units, sms, s, m, a);
+    case 2: return launch_gemm_variant<BN, Epi, 2, FP8>(num_units, sms, s, m, a);
+    case 4: return launch_gemm_variant<BN, Epi, 4, FP8>(num_units, sms, s, m, a);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace coda

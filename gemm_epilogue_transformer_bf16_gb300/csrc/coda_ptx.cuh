@@ -30,9 +30,11 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %2, 0;\n\t"
+      "@P mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)), "r"(bytes), "r"(p)
+      : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -85,55 +87,87 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
 
 // 2-D tiled bulk tensor copy global -> shared, completion counted in bytes
 // on `bar`.  x is the innermost (contiguous) coordinate in elements.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y) {
+// The copy and MMA helpers below take an issue predicate `p`: the whole warp
+// executes them with the same (warp-uniform) operands and only the lane with
+// p != 0 issues the instruction (see elect_one), so the operands stay in
+// uniform registers and the loop around them runs without divergence.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
+                                            uint32_t p) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %5, 0;\n\t"
+      "@P cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(p)
       : "memory");
 }
 
 // L2 eviction-priority policies for the TMA loads below.
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 
 // Same as tma_load_2d with an L2 cache-eviction policy.
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
-                                                 uint64_t policy) {
+                                                 uint64_t policy, uint32_t p) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %6, 0;\n\t"
+      "@P cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy), "r"(p)
       : "memory");
 }
 
 // 2-D tiled copy for a CTA pair (cta_group::2): the data lands in this CTA's
 // shared memory, the byte count is signalled on `bar_cluster`, a
 // shared::cluster address that may name the peer CTA's mbarrier.
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x,
-                                                 int y) {
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x, int y,
+                                                 uint32_t p) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y)
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %5, 0;\n\t"
+      "@P cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(p)
       : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x,
-                                                      int y, uint64_t policy) {
+                                                      int y, uint64_t policy, uint32_t p) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %6, 0;\n\t"
+      "@P cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy), "r"(p)
       : "memory");
+}
+
+// The same copy multicast to every CTA in `cta_mask` (same shared-memory
+// offset in each).  With cta_group::2 the byte count of each destination is
+// signalled on the mbarrier at `bar_cluster`'s offset in the even CTA of that
+// destination's pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x,
+                                                    int y, uint16_t cta_mask, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %6, 0;\n\t"
+      "@P cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "h"(cta_mask), "r"(p)
+      : "memory");
+}
+
+// 1 in exactly one active lane of the warp, 0 in the others.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(e));
+  return e;
 }
 
 // ---------------------------------------------------------------- clusters
@@ -192,12 +226,13 @@ __device__ __forceinline__ void tc_fence_after() {
 // D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulator, issued by
 // one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
+                                          uint32_t accumulate, uint32_t p) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred A, P;\n\t"
+      "setp.ne.b32 A, %4, 0;\n\t"
+      "setp.ne.b32 P, %5, 0;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, A;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(p)
       : "memory");
 }
 
@@ -206,56 +241,63 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
 // each CTA's TMEM receiving its own 128 rows.  Issued by one thread of the
 // even CTA.
 __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                               uint32_t accumulate) {
+                                               uint32_t accumulate, uint32_t p) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred A, P;\n\t"
+      "setp.ne.b32 A, %4, 0;\n\t"
+      "setp.ne.b32 P, %5, 0;\n\t"
+      "@P tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, A;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(p)
       : "memory");
 }
 
 // The same with e4m3 operands (kind::f8f6f4, K = 32 elements per
 // instruction = the same 32 bytes as a bf16 K = 16 step).
 __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t accumulate) {
+                                        uint32_t accumulate, uint32_t p) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred A, P;\n\t"
+      "setp.ne.b32 A, %4, 0;\n\t"
+      "setp.ne.b32 P, %5, 0;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, A;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(p)
       : "memory");
 }
 __device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                             uint32_t accumulate) {
+                                             uint32_t accumulate, uint32_t p) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred A, P;\n\t"
+      "setp.ne.b32 A, %4, 0;\n\t"
+      "setp.ne.b32 P, %5, 0;\n\t"
+      "@P tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, A;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(p)
       : "memory");
 }
 
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
+__device__ __forceinline__ void umma_commit(uint64_t* bar, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %1, 0;\n\t"
+      "@P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)),
+      "r"(p)
+      : "memory");
 }
 // CTA-pair form: arrive on the mbarrier at `bar`'s offset in every CTA of
 // `cta_mask`.
-__device__ __forceinline__ void umma_commit_pair_mc(uint64_t* bar, uint16_t cta_mask) {
+__device__ __forceinline__ void umma_commit_pair_mc(uint64_t* bar, uint16_t cta_mask, uint32_t p) {
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %2, 0;\n\t"
+      "@P tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
+      ::"r"(smem_u32(bar)), "h"(cta_mask), "r"(p)
       : "memory");
 }
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %1, 0;\n\t"
+      "@P tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)),
+      "r"(p)
+      : "memory");
 }
 
 // 32 consecutive fp32 columns of one TMEM lane per thread (warp w reads lanes
