@@ -7,7 +7,9 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
+#include <cstdio>
 #include <cstring>
+#include <utility>
 #include <mutex>
 
 #include "coda.h"
@@ -153,6 +155,27 @@ int l2_hints() {
   return v;
 }
 
+// Back-off (ns) of the GEMM's waiting warps: the producer between stages
+// (0: it must refill a stage as soon as the MMAs release it) and the epilogue
+// while the accumulator fills (its polling otherwise spends power the tensor
+// cores could use under the power cap).  CODA_WAIT_SLEEP="producer,epilogue"
+// overrides the defaults.
+void wait_sleep(uint32_t& producer, uint32_t& epilogue) {
+  static const std::pair<uint32_t, uint32_t> v = [] {
+    uint32_t a = 0, b = 512;
+    if (const char* e = std::getenv("CODA_WAIT_SLEEP")) {
+      unsigned x = 0, y = 0;
+      if (std::sscanf(e, "%u,%u", &x, &y) == 2) {
+        a = x;
+        b = y;
+      }
+    }
+    return std::make_pair(a, b);
+  }();
+  producer = v.first;
+  epilogue = v.second;
+}
+
 int run(const Plan& p, int* status, cudaStream_t s) {
   if (p.M == 0 || p.N == 0) return CODA_OK;
   if (!get_encoder()) return CODA_ERR_CUDA;
@@ -211,6 +234,7 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   a.status = status;
   a.timeout_ns = TIMEOUT_NS;
   a.l2_hints = l2_hints() & 3;
+  wait_sleep(a.producer_sleep_ns, a.epilogue_sleep_ns);
   a.e = p.e;
   a.e.st_stream = (l2_hints() & 4) ? 1 : 0;
   const int nu = a.num_units;

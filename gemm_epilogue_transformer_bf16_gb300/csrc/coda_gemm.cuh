@@ -131,7 +131,9 @@ struct GemmArgs {
   uint32_t idesc;
   int* status;
   uint64_t timeout_ns;
-  int l2_hints;      // bit 0: A loads evict_last, bit 1: B loads evict_first
+  int l2_hints;                // bit 0: A loads evict_last, bit 1: B loads evict_first
+  uint32_t producer_sleep_ns;  // back-off of the producer's and the epilogue's
+  uint32_t epilogue_sleep_ns;  // barrier waits (0 = spin)
   EpiArgs e;
 };
 
@@ -255,7 +257,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kb = 0; kb < num_kb; ++kb, ++it) {
             const int s = it % S;
             const uint32_t ph = (it / S) & 1;
-            if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, args.status, args.timeout_ns)) {
+            if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, args.status, args.timeout_ns,
+                                   args.producer_sleep_ns)) {
               aborted = true;
               break;
             }
@@ -437,7 +440,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       Epi::begin(st, args.e, ti);
       for (int j = 0; j < nlen; ++j, ++t) {
         const uint32_t buf = t & 1;
-        if (!mbar_wait_bounded(&tfull[buf], (t >> 1) & 1, abort_flag, args.status, args.timeout_ns)) {
+        if (!mbar_wait_bounded(&tfull[buf], (t >> 1) & 1, abort_flag, args.status, args.timeout_ns,
+                               args.epilogue_sleep_ns)) {
           aborted = true;
           break;
         }

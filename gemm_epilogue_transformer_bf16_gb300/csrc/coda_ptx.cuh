@@ -53,14 +53,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // of the CTA gave up) or after `limit_ns` of wall time, in which case it sets
 // `*abort`, records CODA_DEV_TIMEOUT in the status word and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                  int* status, uint64_t limit_ns) {
+                                                  int* status, uint64_t limit_ns, uint32_t sleep_ns = 0) {
   const uint32_t b = smem_u32(bar);
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 32; ++i) {
       if (mbar_try_wait(b, parity)) return true;
+      if (sleep_ns) __nanosleep(sleep_ns);  // a waiter with slack backs off
+    }
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
