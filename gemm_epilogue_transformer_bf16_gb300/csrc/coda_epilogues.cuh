@@ -10,7 +10,8 @@
 // (its TMEM lane); it walks the tile's columns 32 at a time.  Row reductions
 // are therefore thread-local; column reductions use a warp reduce-scatter.
 // All TMEM loads are executed by full warps (rows past M only mask their
-// global accesses).
+// global accesses).  The large bf16 outputs leave through warp_store_bf16x32,
+// which turns the warp's 32 rows x 32 columns into row-contiguous stores.
 #pragma once
 #include "coda_gemm.cuh"
 
@@ -27,6 +28,42 @@ __device__ __forceinline__ void load_f32x8(const float* p, float* o) {
 __device__ __forceinline__ void store_f32x8(float* p, const float* v) {
   *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// Stores a warp's 32 rows x 32 columns as bf16: thread `lane` passes the 32
+// values of row row0 + lane, columns col0 .. col0 + 31.  The fragment goes
+// through the warp's 2 KB shared-memory buffer -- 16-byte chunk p of row r
+// sits at r * 64 + ((p ^ ((r >> 1) & 3)) * 16), so the row-wise writes and
+// the column-wise reads are both free of bank conflicts -- and leaves as
+// 16-byte stores that each cover 8 rows x 64 contiguous bytes (whole 32-byte
+// sectors) instead of 32 rows x 16 bytes.  Rows >= M and columns >= N are
+// not written (N is a multiple of 8).  Called by all 32 lanes.
+__device__ __forceinline__ void warp_store_bf16x32(uint8_t* stage, __nv_bfloat16* base, int64_t ld, int row0,
+                                                   int M, int col0, int N, const float* v, bool stream) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint4 w = make_uint4(pack_bf16x2(v[p * 8 + 0], v[p * 8 + 1]), pack_bf16x2(v[p * 8 + 2], v[p * 8 + 3]),
+                               pack_bf16x2(v[p * 8 + 4], v[p * 8 + 5]), pack_bf16x2(v[p * 8 + 6], v[p * 8 + 7]));
+    *reinterpret_cast<uint4*>(stage + lane * 64 + ((p ^ ((lane >> 1) & 3)) * 16)) = w;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 8 + (lane >> 2), p = lane & 3;
+    const uint4 w = *reinterpret_cast<const uint4*>(stage + r * 64 + ((p ^ ((r >> 1) & 3)) * 16));
+    const int row = row0 + r, col = col0 + p * 8;
+    if (row < M && col < N) {
+      __nv_bfloat16* dst = base + static_cast<int64_t>(row) * ld + col;
+      if (stream)
+        asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(w.x), "r"(w.y), "r"(w.z),
+                     "r"(w.w)
+                     : "memory");
+      else
+        *reinterpret_cast<uint4*>(dst) = w;
+    }
+  }
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -56,6 +93,7 @@ struct EpiPlain {
       cb1 = e.csr_off[row + 1];
     }
     float ss = 0.f;
+    const int row0 = row - static_cast<int>(threadIdx.x & 31);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int col0 = t.nb * BN + c;
@@ -67,10 +105,10 @@ struct EpiPlain {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int cc = col0 + g * 8;
+          float* x = v + g * 8;
           if (cc < t.N) {
-            float x[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = v[g * 8 + i] * rs;
+            for (int i = 0; i < 8; ++i) x[i] *= rs;
             if (e.col_scale) {
               float s8[8];
               load_f32x8(e.col_scale + cc, s8);
@@ -117,14 +155,12 @@ struct EpiPlain {
                 for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
               }
             } else {
-              __nv_bfloat16* d = static_cast<__nv_bfloat16*>(e.D) + static_cast<int64_t>(row) * e.ldd + cc;
               if (e.beta) {
                 float o8[8];
-                load_bf16x8(d, o8);
+                load_bf16x8(static_cast<const __nv_bfloat16*>(e.D) + static_cast<int64_t>(row) * e.ldd + cc, o8);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) x[i] += o8[i];
               }
-              store_bf16x8(d, x, e.st_stream);
               if (e.partials) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -136,6 +172,8 @@ struct EpiPlain {
           }
         }
       }
+      if (!e.d_f32)
+        warp_store_bf16x32(t.stage, static_cast<__nv_bfloat16*>(e.D), e.ldd, row0, t.M, col0, t.N, v, e.st_stream);
     }
     if (e.partials && rv) e.partials[static_cast<int64_t>(t.nb) * e.ld_part + row] = ss;
   }
@@ -159,6 +197,7 @@ struct EpiSwiglu {
     const int row = t.row;
     const bool rv = row < t.M;
     const float rs = ((e.row_scale && rv) ? e.row_scale[row] : 1.f) * ((e.row_scale2 && rv) ? e.row_scale2[row] : 1.f);
+    const int row0 = row - static_cast<int>(threadIdx.x & 31);
 #pragma unroll 1
     for (int c = 0; c < HALF; c += 32) {
       const int col0 = t.nb * HALF + c;
@@ -168,32 +207,32 @@ struct EpiSwiglu {
       tmem_ld32(t.taddr + c, g);
       tmem_ld32(t.taddr + HALF + c, u);
       if (rv) {
-        const int64_t off = static_cast<int64_t>(row);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int cc = col0 + q * 8;
-          if (cc < t.N) {
-            float gg[8], uu[8], h[8], cg[8], cu[8];
-            if (e.col_scale) {
-              load_f32x8(e.col_scale + cc, cg);
-              load_f32x8(e.col_scale2 + cc, cu);
-            }
+          float cg[8], cu[8];
+          if (e.col_scale && cc < t.N) {
+            load_f32x8(e.col_scale + cc, cg);
+            load_f32x8(e.col_scale2 + cc, cu);
+          }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              gg[i] = g[q * 8 + i] * rs;
-              uu[i] = u[q * 8 + i] * rs;
-              if (e.col_scale) {
-                gg[i] *= cg[i];
-                uu[i] *= cu[i];
-              }
-              h[i] = gg[i] / (1.f + __expf(-gg[i])) * uu[i];
+          for (int i = 0; i < 8; ++i) {
+            g[q * 8 + i] *= rs;
+            u[q * 8 + i] *= rs;
+            if (e.col_scale && cc < t.N) {
+              g[q * 8 + i] *= cg[i];
+              u[q * 8 + i] *= cu[i];
             }
-            store_bf16x8(static_cast<__nv_bfloat16*>(e.D) + off * e.ldd + cc, h, e.st_stream);
-            if (e.out1) store_bf16x8(e.out1 + off * e.ld_out1 + cc, gg, e.st_stream);
-            if (e.out2) store_bf16x8(e.out2 + off * e.ld_out2 + cc, uu, e.st_stream);
           }
         }
       }
+      float h[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) h[i] = g[i] / (1.f + __expf(-g[i])) * u[i];
+      auto* D = static_cast<__nv_bfloat16*>(e.D);
+      warp_store_bf16x32(t.stage, D, e.ldd, row0, t.M, col0, t.N, h, e.st_stream);
+      if (e.out1) warp_store_bf16x32(t.stage, e.out1, e.ld_out1, row0, t.M, col0, t.N, g, e.st_stream);
+      if (e.out2) warp_store_bf16x32(t.stage, e.out2, e.ld_out2, row0, t.M, col0, t.N, u, e.st_stream);
     }
   }
 };
@@ -216,11 +255,12 @@ struct EpiDSwiglu {
     const bool rv = row < t.M;
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
     float dot = 0.f;
+    const int row0 = row - static_cast<int>(threadIdx.x & 31);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int col0 = t.nb * BN + c;
       if (col0 >= t.N) break;
-      float dh[32];
+      float dh[32], du[32] = {}, h[32] = {};  // rows past M keep zeros (never stored)
       __syncwarp();
       tmem_ld32(t.taddr + c, dh);
       if (rv) {
@@ -229,7 +269,7 @@ struct EpiDSwiglu {
         for (int q = 0; q < 4; ++q) {
           const int cc = col0 + q * 8;
           if (cc < t.N) {
-            float g8[8], u8[8], dg[8], du[8], h[8];
+            float g8[8], u8[8];
             load_bf16x8(e.aux0 + off * e.ld_aux0 + cc, g8);
             load_bf16x8(e.aux1 + off * e.ld_aux1 + cc, u8);
 #pragma unroll
@@ -237,19 +277,19 @@ struct EpiDSwiglu {
               const float s = 1.f / (1.f + __expf(-g8[i]));
               const float sg = g8[i] * s;
               const float d = dh[q * 8 + i];
-              dg[i] = d * u8[i] * s * (1.f + g8[i] * (1.f - s));
-              du[i] = d * sg;
-              h[i] = sg * u8[i];
-              dot += dg[i] * g8[i] + du[i] * u8[i];
-              dg[i] *= rs;
-              du[i] *= rs;
+              const float dg = d * u8[i] * s * (1.f + g8[i] * (1.f - s));
+              const float dui = d * sg;
+              h[q * 8 + i] = sg * u8[i];
+              dot += dg * g8[i] + dui * u8[i];
+              dh[q * 8 + i] = dg * rs;   // G'_g
+              du[q * 8 + i] = dui * rs;  // G'_u
             }
-            store_bf16x8(e.out1 + off * e.ld_out1 + cc, dg, e.st_stream);
-            store_bf16x8(e.out2 + off * e.ld_out2 + cc, du, e.st_stream);
-            if (e.out3) store_bf16x8(e.out3 + off * e.ld_out3 + cc, h, e.st_stream);
           }
         }
       }
+      warp_store_bf16x32(t.stage, e.out1, e.ld_out1, row0, t.M, col0, t.N, dh, e.st_stream);
+      warp_store_bf16x32(t.stage, e.out2, e.ld_out2, row0, t.M, col0, t.N, du, e.st_stream);
+      if (e.out3) warp_store_bf16x32(t.stage, e.out3, e.ld_out3, row0, t.M, col0, t.N, h, e.st_stream);
     }
     if (e.partials && rv) e.partials[static_cast<int64_t>(t.nb) * e.ld_part + row] = dot;
   }
@@ -295,7 +335,7 @@ struct EpiColDot {
         for (int g = 0; g < 4; ++g) {
           const int cc = col0 + g * 8;
           if (cc < t.N) {
-            float w8[8], s8[8], x[8];
+            float w8[8], s8[8];
             for (int j = cb0; j < cb1; ++j) {
               const int32_t t2 = e.csr_idx[j];
               const float w2 = e.csr_w[t2];
@@ -309,12 +349,13 @@ struct EpiColDot {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               p[g * 8 + i] = v[g * 8 + i] * w8[i];
-              x[i] = e.col_scale ? v[g * 8 + i] * s8[i] : v[g * 8 + i];
+              if (e.col_scale) v[g * 8 + i] *= s8[i];
             }
-            store_bf16x8(static_cast<__nv_bfloat16*>(e.D) + off * e.ldd + cc, x, e.st_stream);
           }
         }
       }
+      warp_store_bf16x32(t.stage, static_cast<__nv_bfloat16*>(e.D), e.ldd, row - lane, t.M, col0, t.N, v,
+                         e.st_stream);
       // reduce-scatter over the warp: afterwards lane L holds the column
       // sum of column col0 + L over this warp's 32 rows.
       __syncwarp();

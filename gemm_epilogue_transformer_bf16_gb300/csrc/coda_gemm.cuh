@@ -56,7 +56,8 @@ struct GemmCfg {
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr uint32_t BAR_BYTES = 256;
-  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr uint32_t EPI_STAGE_BYTES = 4 * 2048;  // 2 KB store-transpose buffer per epilogue warp
+  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + EPI_STAGE_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
@@ -143,6 +144,7 @@ struct TileInfo {
   int M, N;
   uint32_t taddr;   // TMEM address of this warp's lane quarter, column 0
   int* status;
+  uint8_t* stage;   // this warp's 2 KB shared-memory store-transpose buffer
 };
 
 // Unit -> (m block, first n block, number of n blocks).
@@ -192,6 +194,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* epi_stage = smem + S * Cfg::STAGE_BYTES + Cfg::BAR_BYTES;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -436,6 +439,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ti.M = args.M;
       ti.N = args.N;
       ti.status = args.status;
+      ti.stage = epi_stage + q * 2048;
       typename Epi::State st;
       Epi::begin(st, args.e, ti);
       for (int j = 0; j < nlen; ++j, ++t) {
