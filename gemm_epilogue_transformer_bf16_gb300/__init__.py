@@ -66,7 +66,7 @@ _SIGS = {
     "coda_linear_swiglu_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_swiglu": ([_P] * 7 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_swiglu_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
-    "coda_linear_swiglu_bwd": ([_P] * 18 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_swiglu_bwd": ([_P] * 18 + [_I64, _I64, _I64, _P, _SZ, _P, _P], ctypes.c_int),
     "coda_linear_qknorm_rope_workspace_size": ([_I64, _I64, _I32, _I32, _I32], _SZ),
     "coda_linear_qknorm_rope": ([_P] * 7 + [_I32, _F, _I32, _I32, _I32] + [_P] * 4 + [_I64, _I64, _P, _SZ, _P],
                                 ctypes.c_int),
@@ -322,7 +322,9 @@ def linear_swiglu(X, Wg, Wu, rstd=None, save=True, H=None, g=None, u=None, ws=No
 
 
 def linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=None, gamma=None, Wgf=None, Wuf=None, dX_resid=None,
-                      ws=None, out=None, stream=None):
+                      ws=None, out=None, stream=None, side_stream=None):
+    """SwiGLU MLP backward (coda_linear_swiglu_bwd).  `side_stream`: optional
+    second torch.cuda.Stream for the weight-gradient GEMMs."""
     lib = load()
     M, K = X.shape
     I = Wg.shape[0]
@@ -339,7 +341,7 @@ def linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=None, gamma=None, Wgf=Non
         _bf(Wgf, "Wgf"), _bf(Wuf, "Wuf"), _bf(Wd, "Wd"), _bf(g, "g"), _bf(u, "u"), _bf(H, "H"),
         _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"), _bf(out["dWg"], "dWg"), _bf(out["dWu"], "dWu"),
         _bf(out["dWd"], "dWd"), _f32(out.get("dgamma"), "dgamma"), M, I, K, _ptr(ws), ws.numel(),
-        _stream(stream)))
+        _stream(stream), side_stream.cuda_stream if side_stream is not None else None))
     return out
 
 

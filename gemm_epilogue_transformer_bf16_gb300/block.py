@@ -24,8 +24,10 @@ so a step launches only the library's kernels.  With ``concurrent`` (the
 default) independent calls run on a second stream: in the forward the gamma
 folds, the row RMS of x0 and the QKV projection overlap the O-projection (the
 HBM-bound folds share SMs with the tensor-bound GEMM), and in the backward
-the O-projection backward overlaps the QKV backward, filling each other's
-last-wave tails.  The gate/up, down and MLP-backward GEMMs run alone.
+the O-projection backward overlaps the QKV backward, and inside the MLP
+backward the weight-gradient GEMMs run on the second stream beside the
+dH -> dX chain, filling each other's last-wave tails.  The gate/up and down
+GEMMs run alone.
 """
 from __future__ import annotations
 
@@ -133,7 +135,7 @@ class Block:
         mark = mark or (lambda name: None)
         linear_swiglu_bwd(dx2, self.x1, w["Wg"], w["Wu"], w["Wd"], self.g, self.u, self.H, rstd=self.rstd1,
                           gamma=w["gamma_mlp"], Wgf=self.Wg_f, Wuf=self.Wu_f, dX_resid=dx2, ws=self.ws,
-                          out=self.grads_mlp)
+                          out=self.grads_mlp, side_stream=self.s2)
         mark("mlp_bwd")
         ctx, ws2 = self._side()
         with ctx:   # both need only dx1

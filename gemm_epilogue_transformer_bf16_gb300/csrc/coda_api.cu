@@ -291,6 +291,30 @@ int ws_ok(const void* ws, size_t have, size_t need) {
 }
 
 cudaStream_t S(coda_stream s) { return static_cast<cudaStream_t>(s); }
+
+// Events that order work across two streams within one call; destroyed when
+// the call returns (destruction of a recorded event is deferred by the
+// runtime until the work it tracks has completed).
+class EventSet {
+ public:
+  explicit EventSet(int n) : n_(n) {
+    for (int i = 0; i < n_; ++i)
+      if (cudaEventCreateWithFlags(&e_[i], cudaEventDisableTiming) != cudaSuccess) ok_ = false;
+  }
+  ~EventSet() {
+    for (int i = 0; i < n_; ++i)
+      if (e_[i]) cudaEventDestroy(e_[i]);
+  }
+  EventSet(const EventSet&) = delete;
+  EventSet& operator=(const EventSet&) = delete;
+  bool ok() const { return ok_; }
+  cudaEvent_t operator[](int i) const { return e_[i]; }
+
+ private:
+  int n_;
+  bool ok_ = true;
+  cudaEvent_t e_[4] = {};
+};
 const __nv_bfloat16* BF(const coda_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
 __nv_bfloat16* BF(coda_bf16* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
 
@@ -807,7 +831,7 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
                            const coda_bf16* Wd, const coda_bf16* g, const coda_bf16* u, const coda_bf16* H,
                            const coda_bf16* dX_resid, coda_bf16* dX, coda_bf16* dWg, coda_bf16* dWu, coda_bf16* dWd,
                            float* dgamma, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
-                           coda_stream stream) {
+                           coda_stream stream, coda_stream side_stream) {
   CK(dims_ok(M, I, K));
   CK(ws_ok(ws, ws_bytes, coda_linear_swiglu_bwd_workspace_size(M, I, K)));
   if (M == 0) return CODA_OK;
@@ -830,6 +854,18 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
   float* dgp = w.take<float>(static_cast<size_t>(8 * nmb) * K);
   int* status = static_cast<int*>(ws);
   cudaStream_t s = S(stream);
+  // With a side stream the weight gradients run beside the dX chain:
+  //   stream:  dH -> dSwiGLU (G') -> c -> dX
+  //   side:    dWd,  then (after G') dWg, dWu
+  // so each persistent GEMM's last, partly filled wave overlaps the other
+  // chain's next GEMM.  They share only the status word (atomic OR).
+  cudaStream_t s2 = side_stream ? S(side_stream) : s;
+  EventSet ev(s2 != s ? 3 : 0);
+  if (!ev.ok()) return CODA_ERR_CUDA;
+  if (s2 != s) {
+    CU(cudaEventRecord(ev[0], s));
+    CU(cudaStreamWaitEvent(s2, ev[0], 0));
+  }
   {  // dH = dY Wd  ->  dSwiGLU  ->  G' (+ row partials)
     Plan p;
     p.kind = coda::EpiKind::DSwiglu;
@@ -855,6 +891,22 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
       p.e.ld_part = M;
     }
     CK(run(p, status, s));
+  }
+  if (s2 != s) CU(cudaEventRecord(ev[1], s));
+  {  // dWd = dY^T H (needs neither G' nor c)
+    Plan p;
+    p.A = dY;
+    p.lda = K;
+    p.a_mn = 1;
+    p.B = H;
+    p.ldb = I;
+    p.b_mn = 1;
+    p.M = K;
+    p.N = I;
+    p.K = M;
+    p.e.D = dWd;
+    p.e.ldd = I;
+    CK(run(p, status, s2));
   }
   if (norm)
     CU(coda::launch_combine_rows(spart, M, static_cast<int>(cdiv(I, BN)), M, 1.f / static_cast<float>(K), 0.f,
@@ -885,21 +937,7 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
     }
     CK(run(p, status, s));
   }
-  {  // dWd = dY^T H
-    Plan p;
-    p.A = dY;
-    p.lda = K;
-    p.a_mn = 1;
-    p.B = H;
-    p.ldb = I;
-    p.b_mn = 1;
-    p.M = K;
-    p.N = I;
-    p.K = M;
-    p.e.D = dWd;
-    p.e.ldd = I;
-    CK(run(p, status, s));
-  }
+  if (s2 != s) CU(cudaStreamWaitEvent(s2, ev[1], 0));
   for (int which = 0; which < 2; ++which) {  // dWg, dWu = (G'^T X) diag(gamma)
     Plan p;
     p.kind = norm ? coda::EpiKind::ColDot : coda::EpiKind::Plain;
@@ -921,7 +959,11 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
       p.e.partials = dgp + static_cast<size_t>(which) * 4 * nmb * K;
       p.e.ld_part = K;
     }
-    CK(run(p, status, s));
+    CK(run(p, status, s2));
+  }
+  if (s2 != s) {
+    CU(cudaEventRecord(ev[2], s2));
+    CU(cudaStreamWaitEvent(s, ev[2], 0));
   }
   if (norm) CU(coda::launch_colsum(dgp, 8 * nmb, K, K, dgamma, s));
   return CODA_OK;

@@ -272,14 +272,19 @@ int coda_linear_swiglu(const coda_bf16* X, const float* rstd, const coda_bf16* W
  * Inputs: dY [M,K]; X [M,K]; rstd [M]|NULL; gamma [K]|NULL; Wg, Wu, Wgf, Wuf
  * [I,K]; Wd [K,I]; g, u, H [M,I] saved by the forward; dX_resid [M,K]|NULL
  * (gradient of the residual stream, added to dX).
- * Outputs: dX [M,K], dWg, dWu [I,K], dWd [K,I] bf16; dgamma [K] fp32|NULL. */
+ * Outputs: dX [M,K], dWg, dWu [I,K], dWd [K,I] bf16; dgamma [K] fp32|NULL.
+ * side_stream (optional, may be NULL): a second stream on which dWd, dWg
+ * and dWu run beside the dH -> dX chain (ordered by events the call
+ * records; the call returns with `stream` waiting for both chains).  The
+ * call's kernels on either stream use the one workspace. */
 size_t coda_linear_swiglu_bwd_workspace_size(int64_t M, int64_t I, int64_t K);
 int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float* rstd, const float* gamma,
                            const coda_bf16* Wg, const coda_bf16* Wu, const coda_bf16* Wgf, const coda_bf16* Wuf,
                            const coda_bf16* Wd, const coda_bf16* g, const coda_bf16* u, const coda_bf16* H,
                            const coda_bf16* dX_resid,
                            coda_bf16* dX, coda_bf16* dWg, coda_bf16* dWu, coda_bf16* dWd, float* dgamma,
-                           int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+                           int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes, coda_stream stream,
+                           coda_stream side_stream);
 
 /* ------------------------------------------------------------------------
  * linear_qknorm_rope (x-tip guide functional API): RMSNorm-reparameterised

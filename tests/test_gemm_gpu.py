@@ -122,3 +122,47 @@ def test_large_k_many_tiles(coda):
     ws = coda.gemm_epilogue(coda.EpilogueDesc(), A.to(dev), B.to(dev), D, M, N, K)
     assert coda.get_status(ws) == 0
     assert_bf16(D, O.gemm_epilogue_plain(to_np(A), to_np(B)), "D 1024x2048x2048")
+
+
+@pytest.mark.parametrize("a_major,b_major", [(0, 0), (1, 1), (0, 1)])
+@pytest.mark.parametrize("M", [129, 255, 257, 383, 511, 513, 700])
+def test_cluster_boundaries_and_no_stray_writes(coda, a_major, b_major, M):
+    """M around the single-CTA / CTA-pair / two-pair switch points (128, 256,
+    512 rows), where the second pair of a 4-CTA cluster can lie partly or
+    wholly past M.  D is a window of a larger buffer (row stride N + 24):
+    every element outside the M x N window must keep its sentinel."""
+    N, K = 264, 200
+    dev = "cuda"
+    A = randn_bf16((M, K), 1.0, 51)
+    B = randn_bf16((N, K), 1.0 / np.sqrt(K), 52)
+    full = torch.full((M + 40, N + 24), 7.0, dtype=torch.bfloat16, device=dev)
+    # an MN-major A is [K, M] with its row stride padded to a multiple of 8
+    # elements (16 bytes, the tensor-map stride rule)
+    lda = None
+    Ad = _operand(A, a_major)
+    if a_major == 1:
+        lda = (M + 7) // 8 * 8
+        Ad = torch.zeros(K, lda, dtype=torch.bfloat16)
+        Ad[:, :M] = A.t()
+    # the output starts at full[0, 0] with row stride N + 24
+    ws = coda.gemm_epilogue(coda.EpilogueDesc(), Ad.to(dev), _operand(B, b_major).to(dev), full,
+                            M, N, K, a_major=a_major, b_major=b_major, lda=lda, ldd=N + 24)
+    torch.cuda.synchronize()
+    assert coda.get_status(ws) == 0
+    assert_bf16(full[:M, :N], O.gemm_epilogue_plain(to_np(A), to_np(B)), f"D M={M}")
+    assert bool((full[M:] == 7.0).all()), "write below row M"
+    assert bool((full[:, N:] == 7.0).all()), "write right of column N"
+
+
+@pytest.mark.parametrize("M", [257, 513, 700])
+def test_swiglu_cluster_boundaries(coda, M):
+    """The gate/up pair split across the CTAs of 2- and 4-CTA clusters."""
+    I, K = 264, 200
+    dev = "cuda"
+    X = randn_bf16((M, K), 1.0, 61)
+    Wg = randn_bf16((I, K), 1.0 / np.sqrt(K), 62)
+    Wu = randn_bf16((I, K), 1.0 / np.sqrt(K), 63)
+    H, g, u = coda.linear_swiglu(X.to(dev), Wg.to(dev), Wu.to(dev))
+    torch.cuda.synchronize()
+    ref = O.swiglu_fwd(to_np(X), to_np(Wg), to_np(Wu))
+    assert_bf16(H, ref[0], f"H M={M}")
