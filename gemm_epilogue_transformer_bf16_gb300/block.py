@@ -21,9 +21,10 @@ Backward (given dx2 and the attention-input gradients dQ, dK, dV):
 
 Every step is a libcoda.so call; buffers and workspaces are allocated once,
 so a step launches only the library's kernels.  With ``concurrent`` (the
-default) independent calls run on a second stream: in the forward the gamma
-folds, the row RMS of x0 and the QKV projection overlap the O-projection (the
-HBM-bound folds share SMs with the tensor-bound GEMM), and in the backward
+default) independent calls run on a second stream: in the forward the QKV
+branch (its gamma fold, the row RMS of x0, the QKV projection) runs beside
+the O-projection and the MLP weights' folds that follow it (the HBM-bound
+folds share SMs with the tensor-bound GEMMs), and in the backward
 the O-projection backward overlaps the QKV backward, and inside the MLP
 backward the weight-gradient GEMMs run on the second stream beside the
 dH -> dX chain, filling each other's last-wave tails.  The gate/up and down
@@ -118,9 +119,11 @@ class Block:
             rms_rstd(x0, s.eps, out=self.rstd0)
             linear_qknorm_rope(x0, self.Wqkv_f, w["gamma_q"], w["gamma_k"], pos, self.cos_sin, s.n_q, s.n_kv,
                                rstd=self.rstd0, eps=s.eps, head_dim=s.head_dim, out=self.fwd, ws=ws2)
+        linear_residual(A, w["Wo"], x0, eps=s.eps, Y=self.x1, rstd_out=self.rstd1, ws=self.ws)
+        # HBM-bound folds after the O-projection: they run beside the QKV GEMM
+        # (their blocks use no shared memory and fit next to its CTAs)
         fold_gamma(w["Wg"], w["gamma_mlp"], out=self.Wg_f)
         fold_gamma(w["Wu"], w["gamma_mlp"], out=self.Wu_f)
-        linear_residual(A, w["Wo"], x0, eps=s.eps, Y=self.x1, rstd_out=self.rstd1, ws=self.ws)
         self._join()
         mark("pre")
         linear_swiglu(self.x1, self.Wg_f, self.Wu_f, rstd=self.rstd1, H=self.H, g=self.g, u=self.u, ws=self.ws)
