@@ -54,6 +54,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-ce", action="store_true", help="skip the linear + cross-entropy side measurement")
     p.add_argument("--serial", action="store_true", help="run the step's calls on one stream")
+    p.add_argument("--fold-weights", action="store_true",
+                   help="fold the RMSNorm gains into the weights each step instead of applying them in the "
+                        "producing epilogues")
     p.add_argument("--cpu-tokens", type=int, default=64, help="token sample of the CPU oracle timing")
     p.add_argument("--tokens", type=int, default=8192,
                    help="tokens per step (8192 is the benchmark workload; smaller values only for profiling)")
@@ -304,14 +307,14 @@ def main():
     s = dataclasses.replace(synth.FULL["c5"], tokens=args.tokens)
     host = synth.make_block(s, seed=rank)          # replicas: each rank its own seeded batch
     t = {k: v.to(dev) for k, v in host.items()}
-    blk = Block(s, t, device=dev, concurrent=not args.serial)
+    blk = Block(s, t, device=dev, concurrent=not args.serial, fold_weights=args.fold_weights)
     flops_step = sum(blk.gemm_flops().values())
-    launches_step = sum(Block.LAUNCHES.values())
+    launches_step = sum(blk.launches().values())
     stream = torch.cuda.current_stream(dev)
     args_step = (t["x0"], t["A"], t["pos"], t["dx2"], t["dQ"], t["dK"], t["dV"])
 
     # ---------------------------------------------------------------- device-resident timing
-    names = list(Block.LAUNCHES)
+    names = list(blk.launches())
     for _ in range(args.warmup):
         blk.step(*args_step)
     torch.cuda.synchronize(dev)
@@ -354,7 +357,7 @@ def main():
                 for k, n in enumerate(names)}
     gf = blk.gemm_flops()
     burst, sustained, hbm, peak_src = measured_peaks()
-    stages = {n: {"ms": round(stage_ms[n], 4), "launches": Block.LAUNCHES[n],
+    stages = {n: {"ms": round(stage_ms[n], 4), "launches": blk.launches()[n],
                   "tflops": round(gf[n] / (stage_ms[n] / 1e3) / 1e12, 1) if gf[n] else None} for n in names}
     ach = gf[DOMINANT] / (stage_ms[DOMINANT] / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": sustained, "unit": "TFLOP/s",
@@ -549,7 +552,9 @@ def main():
             "config": {"workload": WORKLOAD, "tokens": s.tokens, "hidden": s.hidden, "n_q": s.n_q,
                        "n_kv": s.n_kv, "head_dim": s.head_dim, "inter": s.inter, "tflop_per_step":
                        round(flops_step / 1e12, 3), "l2": "inputs (1.7 GB of weights + activations) exceed the "
-                       "129 MB L2; no flush", "parallelism": f"replicas x{world}"},
+                       "129 MB L2; no flush", "parallelism": f"replicas x{world}",
+                       "rmsnorm_gain": "folded into the weights each step" if args.fold_weights
+                       else "applied by the producing epilogue (u = x ⊙ gamma)"},
             "pct_bf16_peak": {"burst": round(value / world / burst, 4), "sustained": round(value / world / sustained, 4),
                               "source": peak_src},
             "roofline": roofline,

@@ -21,7 +21,7 @@ from ._build import LIB as _LIB_PATH
 
 __all__ = [
     "load", "CodaError", "lib_path", "status_string", "get_status", "reset_status",
-    "fold_gamma", "rms_rstd", "rope_table", "gemm_epilogue", "EpilogueDesc",
+    "fold_gamma", "rms_rstd", "rmsnorm_scale", "rope_table", "gemm_epilogue", "EpilogueDesc",
     "rmsnorm_linear", "rmsnorm_linear_bwd", "linear_residual", "linear_residual_bwd",
     "linear_swiglu", "linear_swiglu_bwd", "linear_qknorm_rope", "linear_qknorm_rope_bwd",
     "linear_cross_entropy", "linear_cross_entropy_bwd", "linear_cross_entropy_noalloc", "workspace",
@@ -54,24 +54,25 @@ _SIGS = {
                             _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_fold_gamma": ([_P, _P, _P, _I64, _I64, _P], ctypes.c_int),
     "coda_rms_rstd": ([_P, _I64, _I64, _I64, _F, _P, _P], ctypes.c_int),
+    "coda_rmsnorm_scale": ([_P, _I64, _I64, _I64, _F, _P, _P, _P, _I64, _P], ctypes.c_int),
     "coda_rope_table": ([_F, _I32, _I32, _P, _P], ctypes.c_int),
     "coda_rmsnorm_linear_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_rmsnorm_linear": ([_P, _P, _P, _P, _F, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_rmsnorm_linear_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
-    "coda_rmsnorm_linear_bwd": ([_P] * 11 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_rmsnorm_linear_bwd": ([_P] * 10 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_residual_workspace_size": ([_I64, _I64, _I64], _SZ),
-    "coda_linear_residual": ([_P, _P, _P, _P, _F, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_residual": ([_P, _P, _P, _P, _F, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_residual_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_residual_bwd": ([_P] * 5 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_swiglu_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_swiglu": ([_P] * 7 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_swiglu_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
-    "coda_linear_swiglu_bwd": ([_P] * 18 + [_I64, _I64, _I64, _P, _SZ, _P, _P], ctypes.c_int),
+    "coda_linear_swiglu_bwd": ([_P] * 16 + [_I64, _I64, _I64, _P, _SZ, _P, _P], ctypes.c_int),
     "coda_linear_qknorm_rope_workspace_size": ([_I64, _I64, _I32, _I32, _I32], _SZ),
     "coda_linear_qknorm_rope": ([_P] * 7 + [_I32, _F, _I32, _I32, _I32] + [_P] * 4 + [_I64, _I64, _P, _SZ, _P],
                                 ctypes.c_int),
     "coda_linear_qknorm_rope_bwd_workspace_size": ([_I64, _I64, _I32, _I32, _I32], _SZ),
-    "coda_linear_qknorm_rope_bwd": ([_P] * 9 + [_I32, _F, _I32, _I32, _I32] + [_P] * 11
+    "coda_linear_qknorm_rope_bwd": ([_P] * 9 + [_I32, _F, _I32, _I32, _I32] + [_P] * 10
                                     + [_I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_cross_entropy_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_cross_entropy": ([_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
@@ -226,6 +227,16 @@ def rms_rstd(X, eps, out=None, stream=None):
     return out
 
 
+def rmsnorm_scale(X, gamma, eps, rstd=None, U=None, stream=None):
+    """rstd = 1/rms(X) per row and U = X ⊙ gamma in one pass (coda_rmsnorm_scale)."""
+    M, K = X.shape
+    rstd = torch.empty(M, dtype=torch.float32, device=X.device) if rstd is None else rstd
+    U = torch.empty_like(X) if U is None else U
+    _check("coda_rmsnorm_scale", load().coda_rmsnorm_scale(_bf(X, "X"), K, M, K, float(eps), _f32(gamma, "gamma"),
+                                                           _f32(rstd, "rstd"), _bf(U, "U"), K, _stream(stream)))
+    return rstd, U
+
+
 def rope_table(theta, head_dim, max_pos, device="cuda", out=None, stream=None):
     out = torch.empty(max_pos, head_dim // 2, 2, dtype=torch.float32, device=device) if out is None else out
     _check("coda_rope_table", load().coda_rope_table(float(theta), int(head_dim), int(max_pos),
@@ -263,7 +274,7 @@ def rmsnorm_linear(X, Wf, R=None, rstd_in=None, eps=1e-6, rstd_out=None, Y=None,
     return Y, (rstd_in if rstd_in is not None else rstd_out)
 
 
-def rmsnorm_linear_bwd(dY, X, W, Wf, gamma, rstd, Y, R=None, ws=None, out=None, stream=None):
+def rmsnorm_linear_bwd(dY, X, W, gamma, rstd, Y, R=None, ws=None, out=None, stream=None):
     lib = load()
     M, K = X.shape
     N = W.shape[0]
@@ -272,13 +283,16 @@ def rmsnorm_linear_bwd(dY, X, W, Wf, gamma, rstd, Y, R=None, ws=None, out=None, 
                "dgamma": torch.empty(K, dtype=torch.float32, device=X.device)}
     ws = _ws(ws, lib.coda_rmsnorm_linear_bwd_workspace_size(M, N, K), X.device)
     _check("coda_rmsnorm_linear_bwd", lib.coda_rmsnorm_linear_bwd(
-        _bf(dY, "dY"), _bf(X, "X"), _bf(W, "W"), _bf(Wf, "Wf"), _f32(gamma, "gamma"), _f32(rstd, "rstd"),
+        _bf(dY, "dY"), _bf(X, "X"), _bf(W, "W"), _f32(gamma, "gamma"), _f32(rstd, "rstd"),
         _bf(Y, "Y"), _bf(R, "R"), _bf(out["dX"], "dX"), _bf(out["dW"], "dW"), _f32(out["dgamma"], "dgamma"),
         M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 
-def linear_residual(X, W, R=None, eps=1e-6, want_rstd=False, Y=None, rstd_out=None, ws=None, stream=None):
+def linear_residual(X, W, R=None, eps=1e-6, want_rstd=False, Y=None, rstd_out=None, gamma_next=None, U_out=None,
+                    ws=None, stream=None):
+    """Y = R + X W^T (coda_linear_residual); optionally the row factor of the
+    next RMSNorm (rstd_out / want_rstd) and U_out = Y ⊙ gamma_next."""
     lib = load()
     M, K = X.shape
     N = W.shape[0]
@@ -288,7 +302,7 @@ def linear_residual(X, W, R=None, eps=1e-6, want_rstd=False, Y=None, rstd_out=No
     ws = _ws(ws, lib.coda_linear_residual_workspace_size(M, N, K), X.device)
     _check("coda_linear_residual", lib.coda_linear_residual(
         _bf(X, "X"), _bf(W, "W"), _bf(R, "R"), _bf(Y, "Y"), float(eps), _f32(rstd_out, "rstd_out"),
-        M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
+        _f32(gamma_next, "gamma_next"), _bf(U_out, "U_out"), M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
     return (Y, rstd_out) if want_rstd or rstd_out is not None else Y
 
 
@@ -321,16 +335,15 @@ def linear_swiglu(X, Wg, Wu, rstd=None, save=True, H=None, g=None, u=None, ws=No
     return H, g, u
 
 
-def linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=None, gamma=None, Wgf=None, Wuf=None, dX_resid=None,
-                      ws=None, out=None, stream=None, side_stream=None):
-    """SwiGLU MLP backward (coda_linear_swiglu_bwd).  `side_stream`: optional
-    second torch.cuda.Stream for the weight-gradient GEMMs."""
+def linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=None, gamma=None, dX_resid=None, ws=None, out=None,
+                      stream=None, side_stream=None):
+    """SwiGLU MLP backward (coda_linear_swiglu_bwd); Wg, Wu not folded.
+    `side_stream`: optional second torch.cuda.Stream for the weight-gradient
+    GEMMs."""
     lib = load()
     M, K = X.shape
     I = Wg.shape[0]
     dev = X.device
-    Wgf = Wg if Wgf is None else Wgf
-    Wuf = Wu if Wuf is None else Wuf
     if out is None:
         out = {"dX": torch.empty_like(X), "dWg": torch.empty_like(Wg), "dWu": torch.empty_like(Wu),
                "dWd": torch.empty_like(Wd),
@@ -338,10 +351,10 @@ def linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=None, gamma=None, Wgf=Non
     ws = _ws(ws, lib.coda_linear_swiglu_bwd_workspace_size(M, I, K), dev)
     _check("coda_linear_swiglu_bwd", lib.coda_linear_swiglu_bwd(
         _bf(dY, "dY"), _bf(X, "X"), _f32(rstd, "rstd"), _f32(gamma, "gamma"), _bf(Wg, "Wg"), _bf(Wu, "Wu"),
-        _bf(Wgf, "Wgf"), _bf(Wuf, "Wuf"), _bf(Wd, "Wd"), _bf(g, "g"), _bf(u, "u"), _bf(H, "H"),
-        _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"), _bf(out["dWg"], "dWg"), _bf(out["dWu"], "dWu"),
-        _bf(out["dWd"], "dWd"), _f32(out.get("dgamma"), "dgamma"), M, I, K, _ptr(ws), ws.numel(),
-        _stream(stream), side_stream.cuda_stream if side_stream is not None else None))
+        _bf(Wd, "Wd"), _bf(g, "g"), _bf(u, "u"), _bf(H, "H"), _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"),
+        _bf(out["dWg"], "dWg"), _bf(out["dWu"], "dWu"), _bf(out["dWd"], "dWd"), _f32(out.get("dgamma"), "dgamma"),
+        M, I, K, _ptr(ws), ws.numel(), _stream(stream),
+        side_stream.cuda_stream if side_stream is not None else None))
     return out
 
 
@@ -367,12 +380,13 @@ def linear_qknorm_rope(X, Wf_qkv, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, rst
 
 
 def linear_qknorm_rope_bwd(dQ, dK, dV, qk_save, V, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, X, W_qkv,
-                           Wf_qkv=None, rstd=None, gamma_in=None, dX_resid=None, eps=1e-6, head_dim=128,
-                           ws=None, out=None, stream=None):
+                           rstd=None, gamma_in=None, dX_resid=None, eps=1e-6, head_dim=128, ws=None, out=None,
+                           stream=None):
+    """QK-RMSNorm + RoPE projection backward (coda_linear_qknorm_rope_bwd);
+    W_qkv not folded."""
     lib = load()
     M, Kd = X.shape
     dev = X.device
-    Wf_qkv = W_qkv if Wf_qkv is None else Wf_qkv
     if out is None:
         out = {"dX": torch.empty_like(X), "dW": torch.empty_like(W_qkv),
                "dgamma_in": torch.empty(Kd, dtype=torch.float32, device=dev) if rstd is not None else None,
@@ -384,9 +398,9 @@ def linear_qknorm_rope_bwd(dQ, dK, dV, qk_save, V, gamma_q, gamma_k, pos, cos_si
         _bf(dQ, "dQ"), _bf(dK, "dK"), _bf(dV, "dV"), _bf(qk_save, "qk_save"), _bf(V, "V"),
         _f32(gamma_q, "gamma_q"), _f32(gamma_k, "gamma_k"), _i32(pos, "pos"), _f32(cos_sin, "cos_sin"),
         max_pos, float(eps), n_q, n_kv, head_dim, _bf(X, "X"), _f32(rstd, "rstd"), _f32(gamma_in, "gamma_in"),
-        _bf(W_qkv, "W_qkv"), _bf(Wf_qkv, "Wf_qkv"), _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"),
-        _bf(out["dW"], "dW"), _f32(out.get("dgamma_in"), "dgamma_in"), _f32(out["dgamma_q"], "dgamma_q"),
-        _f32(out["dgamma_k"], "dgamma_k"), M, Kd, _ptr(ws), ws.numel(), _stream(stream)))
+        _bf(W_qkv, "W_qkv"), _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"), _bf(out["dW"], "dW"),
+        _f32(out.get("dgamma_in"), "dgamma_in"), _f32(out["dgamma_q"], "dgamma_q"), _f32(out["dgamma_k"], "dgamma_k"),
+        M, Kd, _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

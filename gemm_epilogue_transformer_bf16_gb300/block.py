@@ -1,30 +1,39 @@
 """The non-attention transformer block as a sequence of GEMM-epilogue calls.
 
 Forward ("CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
-§3.2.1, sites 1 and 2 of the GEMM-residual-RMSNorm-GEMM pattern):
+§3.2.1, sites 1 and 2 of the GEMM-residual-RMSNorm-GEMM pattern).  The
+residual add and the "⊙ gamma" of RMSNorm(y, gamma) are block-local, so the
+epilogue that produces y applies them; the row factor r = 1/rms(y) needs a
+whole row and moves to the epilogue of the next GEMM:
 
-  fold   Wqkv' = Wqkv diag(gamma_attn), Wg' / Wu' = W diag(gamma_mlp)
-  rstd0  r0 = 1/rms(x0)                        (x0 has no producing GEMM here)
-  qkv    Q, K, V = QKnorm+RoPE epilogue of r0 ⊙ (x0 Wqkv'^T)
+  rms0   r0 = 1/rms(x0), u0 = x0 ⊙ gamma_attn  (x0 has no producing GEMM here)
+  qkv    Q, K, V = QKnorm+RoPE epilogue of r0 ⊙ (u0 Wqkv^T)
          [attention itself is out of scope: its output A is an input]
-  oproj  x1 = x0 + A Wo^T, epilogue partial sums of squares -> r1
-  gateup H = silu(r1 ⊙ x1 Wg'^T) ⊙ (r1 ⊙ x1 Wu'^T)       (SwiGLU epilogue)
+  oproj  x1 = x0 + A Wo^T; the epilogue also writes u1 = x1 ⊙ gamma_mlp and
+         partial sums of squares -> r1
+  gateup H = silu(r1 ⊙ u1 Wg^T) ⊙ (r1 ⊙ u1 Wu^T)         (SwiGLU epilogue)
   down   x2 = x1 + H Wd^T                                  (residual epilogue)
 
 Backward (given dx2 and the attention-input gradients dQ, dK, dV):
 
-  mlp    dSwiGLU epilogue on dH = dx2 Wd, reparameterised RMSNorm backward,
-         dx1 = dx2 + mlp branch; dWg, dWu, dWd, dgamma_mlp
+  mlp    dSwiGLU epilogue on dH = dx2 Wd -> G'; dx1 = gamma ⊙ (G' [Wg; Wu])
+         - c ⊙ x1 + dx2 with the dgamma_mlp column partials in its epilogue;
+         dWg, dWu = (G'^T x1) diag(gamma) (column-scale epilogue); dWd = dx2^T H
   oproj  dA = dx1 Wo, dWo = dx1^T A
-  qkv    QK-norm+RoPE backward map, reparameterised RMSNorm backward,
-         dx0 = dx1 + qkv branch; dWqkv, dgamma_attn, dgamma_q, dgamma_k
+  qkv    QK-norm+RoPE backward map, then the same RMSNorm-reparameterised
+         backward for dx0 = dx1 + qkv branch, dWqkv, dgamma_attn;
+         dgamma_q, dgamma_k
+
+With ``fold_weights=True`` the forward instead folds gamma into the weights
+(W' = W diag(gamma), once per step since the weights change every step) and
+its GEMMs read x; the backward is the same either way.
 
 Every step is a libcoda.so call; buffers and workspaces are allocated once,
 so a step launches only the library's kernels.  With ``concurrent`` (the
 default) independent calls run on a second stream: in the forward the QKV
-branch (its gamma fold, the row RMS of x0, the QKV projection) runs beside
-the O-projection and the MLP weights' folds that follow it (the HBM-bound
-folds share SMs with the tensor-bound GEMMs), and in the backward
+branch (row RMS of x0, QKV projection; with folded weights also the Wqkv
+fold) runs beside the O-projection (and the MLP weights' folds that follow
+it, which share SMs with the tensor-bound GEMM), and in the backward
 the O-projection backward overlaps the QKV backward, and inside the MLP
 backward the weight-gradient GEMMs run on the second stream beside the
 dH -> dX chain, filling each other's last-wave tails.  The gate/up and down
@@ -36,23 +45,28 @@ import torch
 
 from . import (fold_gamma, linear_cross_entropy, linear_cross_entropy_bwd, linear_qknorm_rope,
                linear_qknorm_rope_bwd, linear_residual, linear_residual_bwd, linear_swiglu, linear_swiglu_bwd,
-               load, rms_rstd, rope_table, workspace)
+               load, rms_rstd, rmsnorm_scale, rope_table, workspace)
 
 
 class Block:
-    def __init__(self, shape, weights, device="cuda", concurrent=True):
+    def __init__(self, shape, weights, device="cuda", concurrent=True, fold_weights=False):
         self.s = s = shape
         self.w = weights
         self.concurrent = concurrent
+        self.fold_weights = fold_weights
         lib = load()
         T, Hd, I, d = s.tokens, s.hidden, s.inter, s.head_dim
         nqkv = s.qkv_out
         bf = dict(dtype=torch.bfloat16, device=device)
         f32 = dict(dtype=torch.float32, device=device)
         e = torch.empty
-        self.Wqkv_f = e(nqkv, Hd, **bf)
-        self.Wg_f = e(I, Hd, **bf)
-        self.Wu_f = e(I, Hd, **bf)
+        if fold_weights:
+            self.Wqkv_f = e(nqkv, Hd, **bf)
+            self.Wg_f = e(I, Hd, **bf)
+            self.Wu_f = e(I, Hd, **bf)
+        else:
+            self.U0 = e(T, Hd, **bf)
+            self.U1 = e(T, Hd, **bf)
         self.cos_sin = rope_table(s.theta, d, s.seq_len, device=device)
         self.rstd0 = e(T, **f32)
         self.rstd1 = e(T, **f32)
@@ -86,9 +100,14 @@ class Block:
 
     # Stages as the step's CUDA events delimit them on the main stream, and the
     # kernels each launches (library calls are fixed sequences).  "pre" is the
-    # fold + row RMS + QKV branch overlapped with the O-projection; "attn_bwd"
-    # the O-projection backward overlapped with the QKV backward.
-    LAUNCHES = {"pre": 7, "gateup": 1, "down": 1, "mlp_bwd": 7, "attn_bwd": 9}
+    # row RMS + QKV branch beside the O-projection (with the folds when the
+    # weights are folded); "attn_bwd" the O-projection backward beside the
+    # QKV backward.
+    LAUNCHES = {"pre": 4, "gateup": 1, "down": 1, "mlp_bwd": 7, "attn_bwd": 9}
+    LAUNCHES_FOLDED = {"pre": 7, "gateup": 1, "down": 1, "mlp_bwd": 7, "attn_bwd": 9}
+
+    def launches(self):
+        return self.LAUNCHES_FOLDED if self.fold_weights else self.LAUNCHES
 
     def gemm_flops(self):
         """Algorithmic GEMM FLOPs (2*M*N*K) of each stage of one step."""
@@ -114,19 +133,29 @@ class Block:
         s, w = self.s, self.w
         mark = mark or (lambda name: None)
         ctx, ws2 = self._side()
-        with ctx:   # QKV branch: independent of the O-projection
-            fold_gamma(w["Wqkv"], w["gamma_attn"], out=self.Wqkv_f)
-            rms_rstd(x0, s.eps, out=self.rstd0)
-            linear_qknorm_rope(x0, self.Wqkv_f, w["gamma_q"], w["gamma_k"], pos, self.cos_sin, s.n_q, s.n_kv,
-                               rstd=self.rstd0, eps=s.eps, head_dim=s.head_dim, out=self.fwd, ws=ws2)
-        linear_residual(A, w["Wo"], x0, eps=s.eps, Y=self.x1, rstd_out=self.rstd1, ws=self.ws)
-        # HBM-bound folds after the O-projection: they run beside the QKV GEMM
-        # (their blocks use no shared memory and fit next to its CTAs)
-        fold_gamma(w["Wg"], w["gamma_mlp"], out=self.Wg_f)
-        fold_gamma(w["Wu"], w["gamma_mlp"], out=self.Wu_f)
+        if self.fold_weights:
+            with ctx:   # QKV branch: independent of the O-projection
+                fold_gamma(w["Wqkv"], w["gamma_attn"], out=self.Wqkv_f)
+                rms_rstd(x0, s.eps, out=self.rstd0)
+                linear_qknorm_rope(x0, self.Wqkv_f, w["gamma_q"], w["gamma_k"], pos, self.cos_sin, s.n_q, s.n_kv,
+                                   rstd=self.rstd0, eps=s.eps, head_dim=s.head_dim, out=self.fwd, ws=ws2)
+            linear_residual(A, w["Wo"], x0, eps=s.eps, Y=self.x1, rstd_out=self.rstd1, ws=self.ws)
+            # HBM-bound folds after the O-projection: they run beside the QKV
+            # GEMM (their blocks use no shared memory and fit next to its CTAs)
+            fold_gamma(w["Wg"], w["gamma_mlp"], out=self.Wg_f)
+            fold_gamma(w["Wu"], w["gamma_mlp"], out=self.Wu_f)
+            xin, Wg, Wu = self.x1, self.Wg_f, self.Wu_f
+        else:
+            with ctx:   # QKV branch: independent of the O-projection
+                rmsnorm_scale(x0, w["gamma_attn"], s.eps, rstd=self.rstd0, U=self.U0)
+                linear_qknorm_rope(self.U0, w["Wqkv"], w["gamma_q"], w["gamma_k"], pos, self.cos_sin, s.n_q,
+                                   s.n_kv, rstd=self.rstd0, eps=s.eps, head_dim=s.head_dim, out=self.fwd, ws=ws2)
+            linear_residual(A, w["Wo"], x0, eps=s.eps, Y=self.x1, rstd_out=self.rstd1, gamma_next=w["gamma_mlp"],
+                            U_out=self.U1, ws=self.ws)
+            xin, Wg, Wu = self.U1, w["Wg"], w["Wu"]
         self._join()
         mark("pre")
-        linear_swiglu(self.x1, self.Wg_f, self.Wu_f, rstd=self.rstd1, H=self.H, g=self.g, u=self.u, ws=self.ws)
+        linear_swiglu(xin, Wg, Wu, rstd=self.rstd1, H=self.H, g=self.g, u=self.u, ws=self.ws)
         mark("gateup")
         linear_residual(self.H, w["Wd"], self.x1, Y=self.x2, ws=self.ws)
         mark("down")
@@ -137,14 +166,13 @@ class Block:
         s, w = self.s, self.w
         mark = mark or (lambda name: None)
         linear_swiglu_bwd(dx2, self.x1, w["Wg"], w["Wu"], w["Wd"], self.g, self.u, self.H, rstd=self.rstd1,
-                          gamma=w["gamma_mlp"], Wgf=self.Wg_f, Wuf=self.Wu_f, dX_resid=dx2, ws=self.ws,
-                          out=self.grads_mlp, side_stream=self.s2)
+                          gamma=w["gamma_mlp"], dX_resid=dx2, ws=self.ws, out=self.grads_mlp, side_stream=self.s2)
         mark("mlp_bwd")
         ctx, ws2 = self._side()
         with ctx:   # both need only dx1
             linear_residual_bwd(self.dx1, A, w["Wo"], ws=ws2, out=self.grads_o)
         linear_qknorm_rope_bwd(dQ, dK, dV, self.fwd["qk_save"], self.fwd["V"], w["gamma_q"], w["gamma_k"], pos,
-                               self.cos_sin, s.n_q, s.n_kv, x0, w["Wqkv"], Wf_qkv=self.Wqkv_f, rstd=self.rstd0,
+                               self.cos_sin, s.n_q, s.n_kv, x0, w["Wqkv"], rstd=self.rstd0,
                                gamma_in=w["gamma_attn"], dX_resid=self.dx1, eps=s.eps, head_dim=s.head_dim,
                                ws=self.ws, out=self.grads_qkv)
         self._join()

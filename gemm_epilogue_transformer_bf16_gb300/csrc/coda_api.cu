@@ -257,6 +257,7 @@ int run(const Plan& p, int* status, cudaStream_t s) {
     case coda::EpiKind::CeDlogits: err = coda::launch_gemm_cedlogits(nu, sms, cg, s, maps, a); break;
     case coda::EpiKind::ColDot: err = coda::launch_gemm_coldot(nu, sms, cg, s, maps, a); break;
     case coda::EpiKind::Sigmoid: err = coda::launch_gemm_sigmoid(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::RmsDx: err = coda::launch_gemm_rmsdx(nu, sms, cg, s, maps, a); break;
     default: return CODA_ERR_INVALID_ARG;
   }
   return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
@@ -571,6 +572,22 @@ int coda_rms_rstd(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, float e
   return CODA_OK;
 }
 
+int coda_rmsnorm_scale(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, float eps, const float* gamma,
+                       float* rstd, coda_bf16* U, int64_t ldu, coda_stream stream) {
+  CK(dims_ok(M, 8, K));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)X, (const void*)gamma, (const void*)rstd, (const void*)U}) {
+    CK(req(q));
+    CK(al(q));
+  }
+  CK(ldok(ldx, K));
+  CK(ldok(ldu, K));
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  CU(coda::launch_row_rstd(BF(X), ldx, M, K, eps, rstd, sms, S(stream), gamma, BF(U), ldu));
+  return CODA_OK;
+}
+
 int coda_rope_table(float theta, int32_t head_dim, int32_t max_pos, float* cos_sin, coda_stream stream) {
   if (head_dim <= 0 || head_dim % 2 || max_pos <= 0 || !(theta > 0.f)) return CODA_ERR_INVALID_ARG;
   CK(req(cos_sin));
@@ -622,23 +639,21 @@ size_t coda_rmsnorm_linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K) {
   c.take<__nv_bfloat16>(static_cast<size_t>(M) * N);  // G'
   c.take<float>(M);                                    // s
   c.take<float>(M);                                    // coef
-  c.take<float>(static_cast<size_t>(4 * cdiv(N, 128)) * K);  // dgamma partials
+  c.take<float>(static_cast<size_t>(4 * cdiv(M, 128)) * K);  // dgamma partials per (token block, warp)
   return c.off;
 }
 
-int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W, const coda_bf16* Wf,
-                            const float* gamma, const float* rstd, const coda_bf16* Y, const coda_bf16* R,
+int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W, const float* gamma, const float* rstd, const coda_bf16* Y, const coda_bf16* R,
                             coda_bf16* dX, coda_bf16* dW, float* dgamma, int64_t M, int64_t N, int64_t K, void* ws,
                             size_t ws_bytes, coda_stream stream) {
   CK(dims_ok(M, N, K));
   CK(ws_ok(ws, ws_bytes, coda_rmsnorm_linear_bwd_workspace_size(M, N, K)));
   if (M == 0) return CODA_OK;
-  for (const void* q : {(const void*)dY, (const void*)X, (const void*)W, (const void*)Wf, (const void*)gamma,
-                        (const void*)rstd, (const void*)Y, (const void*)dX, (const void*)dW, (const void*)dgamma})
+  for (const void* q : {(const void*)dY, (const void*)X, (const void*)W, (const void*)gamma, (const void*)rstd,
+                        (const void*)Y, (const void*)dX, (const void*)dW, (const void*)dgamma})
     CK(req(q));
-  for (const void* q : {(const void*)dY, (const void*)X, (const void*)W, (const void*)Wf, (const void*)gamma,
-                        (const void*)rstd, (const void*)Y, (const void*)R, (const void*)dX, (const void*)dW,
-                        (const void*)dgamma})
+  for (const void* q : {(const void*)dY, (const void*)X, (const void*)W, (const void*)gamma, (const void*)rstd,
+                        (const void*)Y, (const void*)R, (const void*)dX, (const void*)dW, (const void*)dgamma})
     CK(al(q));
   const int sms = num_sms();
   if (sms <= 0) return CODA_ERR_CUDA;
@@ -646,17 +661,18 @@ int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_
   __nv_bfloat16* Gp = w.take<__nv_bfloat16>(static_cast<size_t>(M) * N);
   float* srow = w.take<float>(M);
   float* coef = w.take<float>(M);
-  const int64_t nmb = cdiv(N, 128);
-  float* dgp = w.take<float>(static_cast<size_t>(4 * nmb) * K);
+  const int64_t ntb = cdiv(M, 128);
+  float* dgp = w.take<float>(static_cast<size_t>(4 * ntb) * K);
   int* status = static_cast<int*>(ws);
   cudaStream_t s = S(stream);
   CU(coda::launch_rms_bwd_prepass(BF(dY), BF(Y), BF(R), rstd, M, N, Gp, srow, sms, s));
   CU(coda::launch_combine_rows(srow, M, 1, M, 1.f / static_cast<float>(K), 0.f, rstd, coef, 1, s));
-  {  // dX = G' Wf - c * X
+  {  // D = G' W;  dX = gamma D - c X, dgamma column partials sum_i X_ik D_ik
     Plan p;
+    p.kind = coda::EpiKind::RmsDx;
     p.A = Gp;
     p.lda = N;
-    p.B = Wf;
+    p.B = W;
     p.ldb = K;
     p.b_mn = 1;
     p.M = M;
@@ -667,11 +683,13 @@ int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_
     p.e.row_coef = coef;
     p.e.aux1 = BF(X);
     p.e.ld_aux1 = K;
+    p.e.col_scale = gamma;
+    p.e.partials = dgp;
+    p.e.ld_part = K;
     CK(run(p, status, s));
   }
-  {  // dW = (G'^T X) diag(gamma), dgamma partials
+  {  // dW = (G'^T X) diag(gamma)
     Plan p;
-    p.kind = coda::EpiKind::ColDot;
     p.A = Gp;
     p.lda = N;
     p.a_mn = 1;
@@ -684,13 +702,9 @@ int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_
     p.e.D = dW;
     p.e.ldd = K;
     p.e.col_scale = gamma;
-    p.e.aux0 = BF(W);
-    p.e.ld_aux0 = K;
-    p.e.partials = dgp;
-    p.e.ld_part = K;
     CK(run(p, status, s));
   }
-  CU(coda::launch_colsum(dgp, 4 * nmb, K, K, dgamma, s));
+  CU(coda::launch_colsum(dgp, 4 * ntb, K, K, dgamma, s));
   return CODA_OK;
 }
 
@@ -702,15 +716,17 @@ size_t coda_linear_residual_workspace_size(int64_t M, int64_t N, int64_t) {
 }
 
 int coda_linear_residual(const coda_bf16* X, const coda_bf16* W, const coda_bf16* R, coda_bf16* Y, float eps,
-                         float* rstd_out, int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
-                         coda_stream stream) {
+                         float* rstd_out, const float* gamma_next, coda_bf16* U_out, int64_t M, int64_t N, int64_t K,
+                         void* ws, size_t ws_bytes, coda_stream stream) {
   CK(dims_ok(M, N, K));
   CK(ws_ok(ws, ws_bytes, coda_linear_residual_workspace_size(M, N, K)));
   if (M == 0) return CODA_OK;
   CK(req(X));
   CK(req(W));
   CK(req(Y));
-  for (const void* q : {(const void*)X, (const void*)W, (const void*)R, (const void*)Y, (const void*)rstd_out})
+  if ((gamma_next == nullptr) != (U_out == nullptr)) return CODA_ERR_INVALID_ARG;
+  for (const void* q : {(const void*)X, (const void*)W, (const void*)R, (const void*)Y, (const void*)rstd_out,
+                        (const void*)gamma_next, (const void*)U_out})
     CK(al(q));
   WsCursor w(ws);
   float* part = w.take<float>(static_cast<size_t>(cdiv(N, BN)) * M);
@@ -729,6 +745,11 @@ int coda_linear_residual(const coda_bf16* X, const coda_bf16* W, const coda_bf16
   if (rstd_out) {
     p.e.partials = part;
     p.e.ld_part = M;
+  }
+  if (U_out) {  // U = Y ⊙ gamma_next: the next RMSNorm-reparameterised GEMM's input
+    p.e.out1 = BF(U_out);
+    p.e.ld_out1 = N;
+    p.e.col_scale2 = gamma_next;
   }
   CK(run(p, static_cast<int*>(ws), S(stream)));
   if (rstd_out)
@@ -822,12 +843,12 @@ size_t coda_linear_swiglu_bwd_workspace_size(int64_t M, int64_t I, int64_t K) {
   c.take<__nv_bfloat16>(static_cast<size_t>(M) * 2 * I);      // G' = [r dG | r dU]
   c.take<float>(static_cast<size_t>(cdiv(I, BN)) * M);        // row partials of sum(dG g + dU u)
   c.take<float>(M);                                            // coef
-  c.take<float>(static_cast<size_t>(8 * cdiv(I, 128)) * K);   // dgamma partials (gate, up)
+  c.take<float>(static_cast<size_t>(4 * cdiv(M, 128)) * K);   // dgamma partials per (token block, warp)
   return c.off;
 }
 
 int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float* rstd, const float* gamma,
-                           const coda_bf16* Wg, const coda_bf16* Wu, const coda_bf16* Wgf, const coda_bf16* Wuf,
+                           const coda_bf16* Wg, const coda_bf16* Wu,
                            const coda_bf16* Wd, const coda_bf16* g, const coda_bf16* u, const coda_bf16* H,
                            const coda_bf16* dX_resid, coda_bf16* dX, coda_bf16* dWg, coda_bf16* dWu, coda_bf16* dWd,
                            float* dgamma, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
@@ -835,14 +856,14 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
   CK(dims_ok(M, I, K));
   CK(ws_ok(ws, ws_bytes, coda_linear_swiglu_bwd_workspace_size(M, I, K)));
   if (M == 0) return CODA_OK;
-  for (const void* q : {(const void*)dY, (const void*)X, (const void*)Wg, (const void*)Wu, (const void*)Wgf,
-                        (const void*)Wuf, (const void*)Wd, (const void*)g, (const void*)u, (const void*)H,
-                        (const void*)dX, (const void*)dWg, (const void*)dWu, (const void*)dWd})
+  for (const void* q : {(const void*)dY, (const void*)X, (const void*)Wg, (const void*)Wu, (const void*)Wd,
+                        (const void*)g, (const void*)u, (const void*)H, (const void*)dX, (const void*)dWg,
+                        (const void*)dWu, (const void*)dWd})
     CK(req(q));
   for (const void* q : {(const void*)dY, (const void*)X, (const void*)rstd, (const void*)gamma, (const void*)Wg,
-                        (const void*)Wu, (const void*)Wgf, (const void*)Wuf, (const void*)Wd, (const void*)g,
-                        (const void*)u, (const void*)H, (const void*)dX_resid, (const void*)dX, (const void*)dWg,
-                        (const void*)dWu, (const void*)dWd, (const void*)dgamma})
+                        (const void*)Wu, (const void*)Wd, (const void*)g, (const void*)u, (const void*)H,
+                        (const void*)dX_resid, (const void*)dX, (const void*)dWg, (const void*)dWu, (const void*)dWd,
+                        (const void*)dgamma})
     CK(al(q));
   const bool norm = rstd != nullptr;
   if (norm && (!gamma || !dgamma)) return CODA_ERR_INVALID_ARG;
@@ -850,8 +871,8 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
   __nv_bfloat16* Gp = w.take<__nv_bfloat16>(static_cast<size_t>(M) * 2 * I);
   float* spart = w.take<float>(static_cast<size_t>(cdiv(I, BN)) * M);
   float* coef = w.take<float>(M);
-  const int64_t nmb = cdiv(I, 128);
-  float* dgp = w.take<float>(static_cast<size_t>(8 * nmb) * K);
+  const int64_t ntb = cdiv(M, 128);
+  float* dgp = w.take<float>(static_cast<size_t>(4 * ntb) * K);
   int* status = static_cast<int*>(ws);
   cudaStream_t s = S(stream);
   // With a side stream the weight gradients run beside the dX chain:
@@ -911,16 +932,18 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
   if (norm)
     CU(coda::launch_combine_rows(spart, M, static_cast<int>(cdiv(I, BN)), M, 1.f / static_cast<float>(K), 0.f,
                                  rstd, coef, 1, s));
-  {  // dX = G'_g Wgf + G'_u Wuf (- c X) (+ dX_resid): one GEMM over K = 2I
+  {  // D = G'_g Wg + G'_u Wu (one GEMM over K = 2I);  dX = gamma D - c X + dX_resid
+     // with the dgamma column partials sum_i X_ik D_ik  (without RMSNorm: D + dX_resid)
     Plan p;
+    p.kind = norm ? coda::EpiKind::RmsDx : coda::EpiKind::Plain;
     p.A = Gp;
     p.lda = 2 * I;
-    p.B = Wgf;
+    p.B = Wg;
     p.ldb = K;
     p.b_mn = 1;
     p.A2 = Gp + I;
     p.lda2 = 2 * I;
-    p.B2 = Wuf;
+    p.B2 = Wu;
     p.ldb2 = K;
     p.K2 = I;
     p.M = M;
@@ -934,13 +957,15 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
       p.e.row_coef = coef;
       p.e.aux1 = BF(X);
       p.e.ld_aux1 = K;
+      p.e.col_scale = gamma;
+      p.e.partials = dgp;
+      p.e.ld_part = K;
     }
     CK(run(p, status, s));
   }
   if (s2 != s) CU(cudaStreamWaitEvent(s2, ev[1], 0));
   for (int which = 0; which < 2; ++which) {  // dWg, dWu = (G'^T X) diag(gamma)
     Plan p;
-    p.kind = norm ? coda::EpiKind::ColDot : coda::EpiKind::Plain;
     p.A = Gp + which * I;
     p.lda = 2 * I;
     p.a_mn = 1;
@@ -952,20 +977,14 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
     p.K = M;
     p.e.D = which ? dWu : dWg;
     p.e.ldd = K;
-    if (norm) {
-      p.e.col_scale = gamma;
-      p.e.aux0 = BF(which ? Wu : Wg);
-      p.e.ld_aux0 = K;
-      p.e.partials = dgp + static_cast<size_t>(which) * 4 * nmb * K;
-      p.e.ld_part = K;
-    }
+    p.e.col_scale = gamma;  // NULL without RMSNorm
     CK(run(p, status, s2));
   }
   if (s2 != s) {
     CU(cudaEventRecord(ev[2], s2));
     CU(cudaStreamWaitEvent(s, ev[2], 0));
   }
-  if (norm) CU(coda::launch_colsum(dgp, 8 * nmb, K, K, dgamma, s));
+  if (norm) CU(coda::launch_colsum(dgp, 4 * ntb, K, K, dgamma, s));
   return CODA_OK;
 }
 
@@ -1020,7 +1039,7 @@ size_t coda_linear_qknorm_rope_bwd_workspace_size(int64_t M, int64_t Kdim, int32
   c.take<float>(M);                                           // s
   c.take<float>(M);                                           // coef
   c.take<float>(static_cast<size_t>(qk_bwd_blocks(M)) * 256);  // dgamma_q|k partials
-  c.take<float>(static_cast<size_t>(4 * cdiv(N, 128)) * Kdim);  // dgamma_in partials
+  c.take<float>(static_cast<size_t>(4 * cdiv(M, 128)) * Kdim);  // dgamma_in partials per (token block, warp)
   return c.off;
 }
 
@@ -1029,7 +1048,7 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
                                 const float* gamma_k, const int32_t* pos, const float* cos_sin, int32_t max_pos,
                                 float eps, int32_t n_q, int32_t n_kv, int32_t head_dim, const coda_bf16* X,
                                 const float* rstd, const float* gamma_in, const coda_bf16* W_qkv,
-                                const coda_bf16* Wf_qkv, const coda_bf16* dX_resid, coda_bf16* dX, coda_bf16* dW_qkv,
+                                const coda_bf16* dX_resid, coda_bf16* dX, coda_bf16* dW_qkv,
                                 float* dgamma_in, float* dgamma_q, float* dgamma_k, int64_t M, int64_t Kdim, void* ws,
                                 size_t ws_bytes, coda_stream stream) {
   if (head_dim != 128) return CODA_ERR_UNSUPPORTED;
@@ -1040,14 +1059,14 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
   if (M == 0) return CODA_OK;
   for (const void* q : {(const void*)dQ, (const void*)dK, (const void*)dV, (const void*)qk_save, (const void*)V,
                         (const void*)gamma_q, (const void*)gamma_k, (const void*)pos, (const void*)cos_sin,
-                        (const void*)X, (const void*)W_qkv, (const void*)Wf_qkv, (const void*)dX,
-                        (const void*)dW_qkv, (const void*)dgamma_q, (const void*)dgamma_k})
+                        (const void*)X, (const void*)W_qkv, (const void*)dX, (const void*)dW_qkv,
+                        (const void*)dgamma_q, (const void*)dgamma_k})
     CK(req(q));
   for (const void* q : {(const void*)dQ, (const void*)dK, (const void*)dV, (const void*)qk_save, (const void*)V,
                         (const void*)gamma_q, (const void*)gamma_k, (const void*)cos_sin, (const void*)X,
-                        (const void*)rstd, (const void*)gamma_in, (const void*)W_qkv, (const void*)Wf_qkv,
-                        (const void*)dX_resid, (const void*)dX, (const void*)dW_qkv, (const void*)dgamma_in,
-                        (const void*)dgamma_q, (const void*)dgamma_k})
+                        (const void*)rstd, (const void*)gamma_in, (const void*)W_qkv, (const void*)dX_resid,
+                        (const void*)dX, (const void*)dW_qkv, (const void*)dgamma_in, (const void*)dgamma_q,
+                        (const void*)dgamma_k})
     CK(al(q));
   const bool norm = rstd != nullptr;
   if (norm && (!gamma_in || !dgamma_in)) return CODA_ERR_INVALID_ARG;
@@ -1059,8 +1078,8 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
   float* coef = w.take<float>(M);
   const int nblk = qk_bwd_blocks(M);
   float* dgqk = w.take<float>(static_cast<size_t>(nblk) * 256);
-  const int64_t nmb = cdiv(N, 128);
-  float* dgp = w.take<float>(static_cast<size_t>(4 * nmb) * Kdim);
+  const int64_t ntb = cdiv(M, 128);
+  float* dgp = w.take<float>(static_cast<size_t>(4 * ntb) * Kdim);
   int* status = static_cast<int*>(ws);
   cudaStream_t s = S(stream);
   CU(coda::launch_qk_bwd(BF(dQ), BF(dK), BF(dV), BF(qk_save), BF(V), gamma_q, gamma_k, pos,
@@ -1070,11 +1089,13 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
   CU(coda::launch_colsum(dgqk + 128, nblk, 128, 256, dgamma_k, s));
   if (norm)
     CU(coda::launch_combine_rows(srow, M, 1, M, 1.f / static_cast<float>(Kdim), 0.f, rstd, coef, 1, s));
-  {  // dX = G' Wf_qkv (- c X) (+ dX_resid)
+  {  // D = G' W_qkv;  dX = gamma_in D - c X + dX_resid with the dgamma_in column
+     // partials sum_i X_ik D_ik  (without RMSNorm: D + dX_resid)
     Plan p;
+    p.kind = norm ? coda::EpiKind::RmsDx : coda::EpiKind::Plain;
     p.A = Gp;
     p.lda = N;
-    p.B = Wf_qkv;
+    p.B = W_qkv;
     p.ldb = Kdim;
     p.b_mn = 1;
     p.M = M;
@@ -1088,12 +1109,14 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
       p.e.row_coef = coef;
       p.e.aux1 = BF(X);
       p.e.ld_aux1 = Kdim;
+      p.e.col_scale = gamma_in;
+      p.e.partials = dgp;
+      p.e.ld_part = Kdim;
     }
     CK(run(p, status, s));
   }
-  {  // dW_qkv = (G'^T X) diag(gamma_in), dgamma_in partials
+  {  // dW_qkv = (G'^T X) diag(gamma_in)
     Plan p;
-    p.kind = norm ? coda::EpiKind::ColDot : coda::EpiKind::Plain;
     p.A = Gp;
     p.lda = N;
     p.a_mn = 1;
@@ -1105,16 +1128,10 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
     p.K = M;
     p.e.D = dW_qkv;
     p.e.ldd = Kdim;
-    if (norm) {
-      p.e.col_scale = gamma_in;
-      p.e.aux0 = BF(W_qkv);
-      p.e.ld_aux0 = Kdim;
-      p.e.partials = dgp;
-      p.e.ld_part = Kdim;
-    }
+    p.e.col_scale = gamma_in;  // NULL without RMSNorm
     CK(run(p, status, s));
   }
-  if (norm) CU(coda::launch_colsum(dgp, 4 * nmb, Kdim, Kdim, dgamma_in, s));
+  if (norm) CU(coda::launch_colsum(dgp, 4 * ntb, Kdim, Kdim, dgamma_in, s));
   return CODA_OK;
 }
 

@@ -46,8 +46,12 @@ cudaError_t launch_fold_gamma(const __nv_bfloat16* W, const float* gamma, __nv_b
 }
 
 // ---------------------------------------------------------------- row rstd
+// One warp per row: r = 1/sqrt(mean_k X^2 + eps); with gamma, in the same
+// read, U = bf16(X ⊙ gamma) (the input of an RMSNorm-reparameterised GEMM
+// whose row scale r is applied in its epilogue).
 __global__ void row_rstd_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int64_t M, int64_t K, float eps,
-                                float* rstd) {
+                                float* rstd, const float* __restrict__ gamma, __nv_bfloat16* __restrict__ U,
+                                int64_t ldu) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; row < M; row += warps) {
@@ -58,6 +62,13 @@ __global__ void row_rstd_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx
       load_bf16x8(x + k, v);
 #pragma unroll
       for (int j = 0; j < 8; ++j) s += v[j] * v[j];
+      if (U) {
+        float g[8];
+        load_f32x8(gamma + k, g);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] *= g[j];
+        store_bf16x8(U + row * ldu + k, v);
+      }
     }
     s = warp_sum(s);
     if (lane == 0) rstd[row] = 1.f / sqrtf(s / static_cast<float>(K) + eps);
@@ -65,9 +76,10 @@ __global__ void row_rstd_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx
 }
 
 cudaError_t launch_row_rstd(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, float eps, float* rstd,
-                            int num_sms, cudaStream_t s) {
+                            int num_sms, cudaStream_t s, const float* gamma, __nv_bfloat16* U, int64_t ldu) {
   const int64_t blocks = std::min<int64_t>((M + 7) / 8, static_cast<int64_t>(num_sms) * 8);
-  row_rstd_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(X, ldx, M, K, eps, rstd);
+  row_rstd_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(X, ldx, M, K, eps, rstd, gamma,
+                                                                                       U, ldu);
   return cudaGetLastError();
 }
 

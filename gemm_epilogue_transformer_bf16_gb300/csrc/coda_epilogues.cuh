@@ -66,10 +66,54 @@ __device__ __forceinline__ void warp_store_bf16x32(uint8_t* stage, __nv_bfloat16
   __syncwarp();
 }
 
+// Reduce-scatter over the warp: on entry thread `lane` holds p[0..31] of its
+// row; afterwards p[0] of lane L is the sum over the warp's 32 rows of column
+// L.  Fixed order, so bitwise reproducible.
+__device__ __forceinline__ void warp_colsum_partial(float* p, int lane) {
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const bool hi = lane & 16;
+    const float keep = hi ? p[i + 16] : p[i];
+    const float send = hi ? p[i] : p[i + 16];
+    p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool hi = lane & 8;
+    const float keep = hi ? p[i + 8] : p[i];
+    const float send = hi ? p[i] : p[i + 8];
+    p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool hi = lane & 4;
+    const float keep = hi ? p[i + 4] : p[i];
+    const float send = hi ? p[i] : p[i + 4];
+    p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool hi = lane & 2;
+    const float keep = hi ? p[i + 2] : p[i];
+    const float send = hi ? p[i] : p[i + 2];
+    p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  {
+    const bool hi = lane & 1;
+    const float keep = hi ? p[1] : p[0];
+    const float send = hi ? p[0] : p[1];
+    p[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // PLAIN:  D = rs_i * cs_j * acc + aux0 - coef_i * aux1[g_i] - coef2_i * aux3
 //             - sum_{t in csr(i)} w_t * aux2[t]  (+ D if beta)
-// optional row partial  sum_j D_ij^2  (of the stored, rounded values).
+// optional row partial  sum_j D_ij^2  (of the stored, rounded values), and
+// optional second output  out1 = bf16(D_ij * cs2_j)  (D as stored: the
+// input of the next RMSNorm-reparameterised GEMM, x ⊙ gamma, written by the
+// epilogue that produces x).
 // Covers: plain store, residual add, RMSNorm row-scale (+ residual),
 // accumulate, the residual + partial-RMS epilogue, dX - c*X of the
 // RMSNorm-reparameterised backward, and the exact one-hot terms of the
@@ -172,8 +216,23 @@ struct EpiPlain {
           }
         }
       }
-      if (!e.d_f32)
+      if (!e.d_f32) {
         warp_store_bf16x32(t.stage, static_cast<__nv_bfloat16*>(e.D), e.ldd, row0, t.M, col0, t.N, v, e.st_stream);
+        if (e.out1) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            float s8[8];
+            if (col0 + g * 8 < t.N)
+              load_f32x8(e.col_scale2 + col0 + g * 8, s8);
+            else
+#pragma unroll
+              for (int i = 0; i < 8; ++i) s8[i] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[g * 8 + i] = round_bf16(v[g * 8 + i]) * s8[i];
+          }
+          warp_store_bf16x32(t.stage, e.out1, e.ld_out1, row0, t.M, col0, t.N, v, e.st_stream);
+        }
+      }
     }
     if (e.partials && rv) e.partials[static_cast<int64_t>(t.nb) * e.ld_part + row] = ss;
   }
@@ -356,44 +415,67 @@ struct EpiColDot {
       }
       warp_store_bf16x32(t.stage, static_cast<__nv_bfloat16*>(e.D), e.ldd, row - lane, t.M, col0, t.N, v,
                          e.st_stream);
-      // reduce-scatter over the warp: afterwards lane L holds the column
-      // sum of column col0 + L over this warp's 32 rows.
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const bool hi = lane & 16;
-        const float keep = hi ? p[i + 16] : p[i];
-        const float send = hi ? p[i] : p[i + 16];
-        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const bool hi = lane & 8;
-        const float keep = hi ? p[i + 8] : p[i];
-        const float send = hi ? p[i] : p[i + 8];
-        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const bool hi = lane & 4;
-        const float keep = hi ? p[i + 4] : p[i];
-        const float send = hi ? p[i] : p[i + 4];
-        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const bool hi = lane & 2;
-        const float keep = hi ? p[i + 2] : p[i];
-        const float send = hi ? p[i] : p[i + 2];
-        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-      }
-      {
-        const bool hi = lane & 1;
-        const float keep = hi ? p[1] : p[0];
-        const float send = hi ? p[0] : p[1];
-        p[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-      }
+      warp_colsum_partial(p, lane);
       // (a CTA pair's second M block can lie wholly past M: no partial row for it)
+      if (e.partials && col0 + lane < t.N && t.mb * BM < t.M)
+        e.partials[static_cast<int64_t>(t.mb * 4 + q) * e.ld_part + col0 + lane] = p[0];
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// RMSDX (input gradient of an RMSNorm-reparameterised projection whose GEMM
+// read u = x ⊙ gamma, gamma applied by the producing epilogue): the
+// accumulator is D = G' W with the weight not folded, and
+//   out = cs_k * D + aux0 - coef_i * aux1     (gamma D + dX_resid - c x)
+//   column partial  sum_i aux1[i, k] * D[i, k]  (dgamma contribution)
+// written per (m block, warp) to partials[(mb*4 + warp) * ld_part + k].
+// ---------------------------------------------------------------------------
+template <int BN>
+struct EpiRmsDx {
+  struct State {};
+  static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
+    const int row = t.row;
+    const bool rv = row < t.M;
+    const int lane = threadIdx.x & 31;
+    const int q = (threadIdx.x >> 5) & 3;
+    const float rc = (e.row_coef && rv) ? e.row_coef[row] : 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      const int col0 = t.nb * BN + c;
+      if (col0 >= t.N) break;
+      float v[32];
+      __syncwarp();
+      tmem_ld32(t.taddr + c, v);
+      float p[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) p[i] = 0.f;
+      if (rv) {
+        const int64_t off = static_cast<int64_t>(row);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int cc = col0 + g * 8;
+          if (cc < t.N) {
+            float x8[8], s8[8], r8[8];
+            load_bf16x8(e.aux1 + off * e.ld_aux1 + cc, x8);
+            load_f32x8(e.col_scale + cc, s8);
+            if (e.aux0) load_bf16x8(e.aux0 + off * e.ld_aux0 + cc, r8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float d = v[g * 8 + i];
+              p[g * 8 + i] = x8[i] * d;
+              float o = d * s8[i];
+              if (e.aux0) o += r8[i];
+              v[g * 8 + i] = o - rc * x8[i];
+            }
+          }
+        }
+      }
+      warp_store_bf16x32(t.stage, static_cast<__nv_bfloat16*>(e.D), e.ldd, row - lane, t.M, col0, t.N, v,
+                         e.st_stream);
+      warp_colsum_partial(p, lane);
       if (e.partials && col0 + lane < t.N && t.mb * BM < t.M)
         e.partials[static_cast<int64_t>(t.mb * 4 + q) * e.ld_part + col0 + lane] = p[0];
     }

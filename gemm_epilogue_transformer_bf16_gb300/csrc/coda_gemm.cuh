@@ -81,7 +81,7 @@ struct EpiArgs {
   const int32_t* csr_idx;       // aux2 row indices
   const float* csr_w;           // weight of each aux2 row
   const float* row_scale2;      // SWIGLU: second per-row factor (FP8 token scale)
-  const float* col_scale2;      // SWIGLU: per-column factor of the up half (col_scale: gate half)
+  const float* col_scale2;      // SWIGLU: per-column factor of the up half (col_scale: gate half); PLAIN: gamma of out1
   const float* row_coef2;       // PLAIN: D -= row_coef2_i * aux3[i, j]
   const __nv_bfloat16* aux3;
   int64_t ld_aux3;

@@ -10,7 +10,7 @@
 
 namespace coda {
 
-enum class EpiKind : int { Plain = 0, Swiglu, DSwiglu, QkRope, CeLse, CeDlogits, ColDot, Sigmoid };
+enum class EpiKind : int { Plain = 0, Swiglu, DSwiglu, QkRope, CeLse, CeDlogits, ColDot, Sigmoid, RmsDx };
 
 // Tensor maps in the order A0, B0, A1, B1.  `cg` is the cluster size: 1
 // (single CTAs), 2 (a cta_group::2 pair) or 4 (two pairs sharing B by TMA
@@ -33,6 +33,8 @@ cudaError_t launch_gemm_plain_fp8(int num_units, int sms, int cg, cudaStream_t s
                                   const GemmArgs& a);
 cudaError_t launch_gemm_swiglu_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                    const GemmArgs& a);
+cudaError_t launch_gemm_rmsdx(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
+                              const GemmArgs& a);
 cudaError_t launch_gemm_coldot(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
 
@@ -40,7 +42,8 @@ cudaError_t launch_gemm_coldot(int num_units, int sms, int cg, cudaStream_t s, c
 cudaError_t launch_fold_gamma(const __nv_bfloat16* W, const float* gamma, __nv_bfloat16* Wf, int64_t N, int64_t K,
                               int num_sms, cudaStream_t s);
 cudaError_t launch_row_rstd(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, float eps, float* rstd,
-                            int num_sms, cudaStream_t s);
+                            int num_sms, cudaStream_t s, const float* gamma = nullptr, __nv_bfloat16* U = nullptr,
+                            int64_t ldu = 0);
 // mode 0: out = 1/sqrt(sum_t p[t] * inv_k + eps);  mode 1: out = r^2 * sum_t p[t] * inv_k
 cudaError_t launch_combine_rows(const float* p, int64_t ld, int nparts, int64_t M, float inv_k, float eps,
                                 const float* r, float* out, int mode, cudaStream_t s);

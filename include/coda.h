@@ -192,6 +192,16 @@ int coda_fold_gamma(const coda_bf16* W, const float* gamma, coda_bf16* Wf,
 int coda_rms_rstd(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, float eps,
                   float* rstd, coda_stream stream);
 
+/* RMSNorm prepass for an input no upstream GEMM epilogue produced:
+ *   rstd[i] = 1/sqrt(mean_k X[i,k]^2 + eps),   U[i, k] = bf16(X[i,k] * gamma[k])
+ * in one read of X [M, K] bf16 (row stride ldx).  U [M, K] bf16 (row stride
+ * ldu) is the input of the RMSNorm-reparameterised GEMM that applies rstd in
+ * its epilogue (§3.2.1: the gamma multiply is block-local and the row factor
+ * r moves to the end of the next GEMM).  gamma [K] fp32.  All pointers
+ * required, 16-byte aligned. */
+int coda_rmsnorm_scale(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, float eps, const float* gamma,
+                       float* rstd, coda_bf16* U, int64_t ldu, coda_stream stream);
+
 /* RoPE table: cos_sin[p, j] = (cos a, sin a), a = p * theta^(-2j/head_dim),
  * j < head_dim/2, p < max_pos; computed in fp64, stored fp32.  Interleaved
  * pair convention (2j, 2j+1). */
@@ -213,17 +223,18 @@ int coda_rmsnorm_linear(const coda_bf16* X, const float* rstd_in, const coda_bf1
                         int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
 
 /* Backward of coda_rmsnorm_linear for upstream gradient dY [M, N]:
- *   G' = r ⊙ dY,  c_i = r_i^2 sum_n dY_in (Y - R)_in / K,
- *   dX = G' Wf - c ⊙ X,  dW' = G'^T X,  dW = dW' diag(gamma),
- *   dgamma_k = sum_n W_nk dW'_nk.   (dR = dY: no copy is made.)
- * Inputs: X [M,K], W and Wf [N,K], gamma [K], rstd [M], Y and R [M,N]
+ *   G' = r ⊙ dY,  c_i = r_i^2 sum_n dY_in (Y - R)_in / K,  D = G' W,
+ *   dX = gamma ⊙ D - c ⊙ X,  dW = (G'^T X) diag(gamma),
+ *   dgamma_k = sum_i X_ik D_ik   (column partials of the dX epilogue).
+ *   (dR = dY: no copy is made.)
+ * Inputs: X [M,K], W [N,K] (not folded), gamma [K], rstd [M], Y and R [M,N]
  * (R may be NULL = zero).  Outputs: dX [M,K], dW [N,K] bf16, dgamma [K] fp32.
  * The pages state only that this backward keeps the GEMM-epilogue form; the
- * formulas are the chain rule of the §3.2.1 equation. */
+ * formulas are the chain rule of the §3.2.1 equation, and they hold whether
+ * the forward folded gamma into W or applied it to the GEMM input. */
 size_t coda_rmsnorm_linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K);
-int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W,
-                            const coda_bf16* Wf, const float* gamma, const float* rstd,
-                            const coda_bf16* Y, const coda_bf16* R,
+int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W, const float* gamma,
+                            const float* rstd, const coda_bf16* Y, const coda_bf16* R,
                             coda_bf16* dX, coda_bf16* dW, float* dgamma,
                             int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
 
@@ -235,10 +246,14 @@ int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_
  * squares of Y, merged by a small second kernel into
  * rstd_out[i] = 1/sqrt(mean_n Y_in^2 + eps): the row factor r the next
  * RMSNorm-reparameterised projection applies in its epilogue.
+ * gamma_next [N] fp32 and U_out [M, N] bf16 (optional, both or neither): the
+ * epilogue also writes U_out = bf16(Y ⊙ gamma_next), Y as stored -- the
+ * "⊙ gamma" of §3.2.1 applied where it is block-local, so the next GEMM
+ * reads U with its weight unfolded.
  * ---------------------------------------------------------------------- */
 size_t coda_linear_residual_workspace_size(int64_t M, int64_t N, int64_t K);
 int coda_linear_residual(const coda_bf16* X, const coda_bf16* W, const coda_bf16* R,
-                         coda_bf16* Y, float eps, float* rstd_out,
+                         coda_bf16* Y, float eps, float* rstd_out, const float* gamma_next, coda_bf16* U_out,
                          int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
 
 /* Backward: dX = dY W [M, K], dW = dY^T X [N, K]; dR = dY (no copy). */
@@ -262,16 +277,18 @@ int coda_linear_swiglu(const coda_bf16* X, const float* rstd, const coda_bf16* W
                        int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
 
 /* Backward of the SwiGLU MLP sublayer  Y = Xres + silu(g) u Wd^T  with
- * g, u = linear_swiglu(X, rstd, Wgf, Wuf):
+ * g, u = r ⊙ (X ⊙ gamma) [Wg; Wu]^T (linear_swiglu on the gain-scaled input,
+ * or on X with gamma folded into Wg, Wu -- the gradients are the same):
  *   dH = dY Wd (GEMM) -> dSwiGLU epilogue -> G' = r ⊙ [dG | dU];
- *   dX = G' [Wgf; Wuf] - c ⊙ X + dX_resid  (one GEMM over K = 2I);
- *   dWd = dY^T H;  dWg = (G'_g^T X) diag(gamma), dWu likewise;
- *   dgamma_k = sum_n (Wg_nk dWg'_nk + Wu_nk dWu'_nk).
+ *   D = G' [Wg; Wu]  (one GEMM over K = 2I),
+ *   dX = gamma ⊙ D - c ⊙ X + dX_resid  with the dgamma_k = sum_i X_ik D_ik
+ *   column partials in its epilogue;
+ *   dWd = dY^T H;  dWg = (G'_g^T X) diag(gamma), dWu likewise.
  * With rstd == NULL there is no RMSNorm (r = 1, c = 0, gamma ignored,
- * Wgf/Wuf must equal Wg/Wu, dgamma untouched).
- * Inputs: dY [M,K]; X [M,K]; rstd [M]|NULL; gamma [K]|NULL; Wg, Wu, Wgf, Wuf
- * [I,K]; Wd [K,I]; g, u, H [M,I] saved by the forward; dX_resid [M,K]|NULL
- * (gradient of the residual stream, added to dX).
+ * dX = D + dX_resid, dgamma untouched).
+ * Inputs: dY [M,K]; X [M,K]; rstd [M]|NULL; gamma [K]|NULL; Wg, Wu [I,K]
+ * (not folded); Wd [K,I]; g, u, H [M,I] saved by the forward; dX_resid
+ * [M,K]|NULL (gradient of the residual stream, added to dX).
  * Outputs: dX [M,K], dWg, dWu [I,K], dWd [K,I] bf16; dgamma [K] fp32|NULL.
  * side_stream (optional, may be NULL): a second stream on which dWd, dWg
  * and dWu run beside the dH -> dX chain (ordered by events the call
@@ -279,9 +296,8 @@ int coda_linear_swiglu(const coda_bf16* X, const float* rstd, const coda_bf16* W
  * call's kernels on either stream use the one workspace. */
 size_t coda_linear_swiglu_bwd_workspace_size(int64_t M, int64_t I, int64_t K);
 int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float* rstd, const float* gamma,
-                           const coda_bf16* Wg, const coda_bf16* Wu, const coda_bf16* Wgf, const coda_bf16* Wuf,
-                           const coda_bf16* Wd, const coda_bf16* g, const coda_bf16* u, const coda_bf16* H,
-                           const coda_bf16* dX_resid,
+                           const coda_bf16* Wg, const coda_bf16* Wu, const coda_bf16* Wd, const coda_bf16* g,
+                           const coda_bf16* u, const coda_bf16* H, const coda_bf16* dX_resid,
                            coda_bf16* dX, coda_bf16* dWg, coda_bf16* dWu, coda_bf16* dWd, float* dgamma,
                            int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes, coda_stream stream,
                            coda_stream side_stream);
@@ -310,10 +326,11 @@ int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf
  * pre-norm q|k (qk_save) and V:
  *   per head  dn = RoPE^-1(dQ_h),  dq = rho (dn⊙gamma - n mean(n ⊙ dn⊙gamma)),
  *   dgamma_q = sum dn ⊙ n;  dv = dV;  then the RMSNorm-reparameterised
- *   projection backward with G = [dq | dk | dv]:
- *   dX = r⊙G Wf_qkv - c ⊙ X + dX_resid, dW_qkv = ((r⊙G)^T X) diag(gamma_in),
- *   dgamma_in.
- * rstd/gamma_in may be NULL (no input RMSNorm; Wf_qkv == W_qkv then).
+ *   projection backward with G' = r ⊙ [dq | dk | dv] and D = G' W_qkv:
+ *   dX = gamma_in ⊙ D - c ⊙ X + dX_resid with the dgamma_in_k =
+ *   sum_i X_ik D_ik column partials in its epilogue,
+ *   dW_qkv = (G'^T X) diag(gamma_in).  W_qkv is not folded.
+ * rstd/gamma_in may be NULL (no input RMSNorm: dX = D + dX_resid).
  * Outputs: dX [M, Kdim], dW_qkv [(n_q+2n_kv)*128, Kdim] bf16; dgamma_in [Kdim],
  * dgamma_q, dgamma_k [128] fp32. */
 size_t coda_linear_qknorm_rope_bwd_workspace_size(int64_t M, int64_t Kdim, int32_t n_q, int32_t n_kv,
@@ -324,7 +341,7 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
                                 const float* cos_sin, int32_t max_pos, float eps,
                                 int32_t n_q, int32_t n_kv, int32_t head_dim,
                                 const coda_bf16* X, const float* rstd, const float* gamma_in,
-                                const coda_bf16* W_qkv, const coda_bf16* Wf_qkv, const coda_bf16* dX_resid,
+                                const coda_bf16* W_qkv, const coda_bf16* dX_resid,
                                 coda_bf16* dX, coda_bf16* dW_qkv, float* dgamma_in,
                                 float* dgamma_q, float* dgamma_k,
                                 int64_t M, int64_t Kdim, void* ws, size_t ws_bytes, coda_stream stream);

@@ -93,12 +93,12 @@ def test_rejects_bad_arguments_on_host(lib):
     # feature dims must be multiples of 8
     assert lib.coda_linear_swiglu(FAKE, None, FAKE, FAKE, FAKE, None, None, 16, 60, 64, ws, 4096, None) == 3
     # negative size
-    assert lib.coda_linear_residual(FAKE, FAKE, None, FAKE, 1e-6, None, -1, 64, 64, ws, 4096, None) == 1
+    assert lib.coda_linear_residual(FAKE, FAKE, None, FAKE, 1e-6, None, None, None, -1, 64, 64, ws, 4096, None) == 1
     # workspace too small
     need = lib.coda_rmsnorm_linear_bwd_workspace_size(128, 64, 64)
-    assert lib.coda_rmsnorm_linear_bwd(*([FAKE] * 11), 128, 64, 64, ws, need - 1, None) == 4
+    assert lib.coda_rmsnorm_linear_bwd(*([FAKE] * 10), 128, 64, 64, ws, need - 1, None) == 4
     # null workspace
-    assert lib.coda_linear_residual(FAKE, FAKE, None, FAKE, 1e-6, None, 16, 64, 64, None, 4096, None) == 4
+    assert lib.coda_linear_residual(FAKE, FAKE, None, FAKE, 1e-6, None, None, None, 16, 64, 64, None, 4096, None) == 4
     # head_dim other than 128 is unsupported
     assert lib.coda_linear_qknorm_rope(*([FAKE] * 7), 16, 1e-6, 2, 1, 64, *([FAKE] * 4), 16, 64, ws, 4096,
                                        None) == 3
@@ -110,7 +110,7 @@ def test_empty_problem_is_a_noop(lib):
     ws = FAKE
     # M == 0: nothing to do, nothing enqueued, OK
     assert lib.coda_linear_swiglu(FAKE, None, FAKE, FAKE, FAKE, None, None, 0, 64, 64, ws, 4096, None) == 0
-    assert lib.coda_linear_residual(FAKE, FAKE, None, FAKE, 1e-6, None, 0, 64, 64, ws, 4096, None) == 0
+    assert lib.coda_linear_residual(FAKE, FAKE, None, FAKE, 1e-6, None, None, None, 0, 64, 64, ws, 4096, None) == 0
 
 
 def test_generic_rejects_bad_descriptor(lib):

@@ -54,7 +54,7 @@ def test_rmsnorm_linear_fwd_bwd(coda, shape):
     yr, rr = O.rmsnorm_linear_fwd(o["X"], o["gamma"], o["W"], shape.eps, o["R"])
     assert_bf16(Y, yr, "Y")
     assert_f32(rstd, rr, "rstd")
-    g = coda.rmsnorm_linear_bwd(d["G"], d["X"], d["W"], Wf, d["gamma"], rstd, Y, d["R"])
+    g = coda.rmsnorm_linear_bwd(d["G"], d["X"], d["W"], d["gamma"], rstd, Y, d["R"])
     b = O.rmsnorm_linear_bwd(o["X"], o["gamma"], o["W"], shape.eps, o["G"])
     assert_bf16(g["dX"], b["dX"], "dX")
     assert_bf16(g["dW"], b["dW"], "dW")
@@ -68,6 +68,54 @@ def test_fold_gamma_and_rstd(coda):
     assert_bf16(Wf, o["W"] * o["gamma"][None, :], "Wf")
     r = coda.rms_rstd(d["X"], 1e-6)
     assert_f32(r, O.rms_inv(o["X"], 1e-6), "rstd")
+
+
+def test_rmsnorm_scale(coda):
+    """One pass: r = 1/rms(X) and U = X ⊙ gamma (bit-exact: one bf16 rounding
+    of an fp32 product of two exact values)."""
+    t = synth.make_rms_linear(synth.RmsLinearShape(200, 128, 264), seed=5)
+    d, o = dev(t), f64(t)
+    r, U = coda.rmsnorm_scale(d["X"], d["gamma"], 1e-6)
+    assert_f32(r, O.rms_inv(o["X"], 1e-6), "rstd")
+    assert torch.equal(U, (d["X"].float() * d["gamma"][None, :]).to(torch.bfloat16)), "U = X * gamma"
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 384), (300, 776, 136)])
+def test_linear_residual_gamma_output(coda, M, N, K):
+    """The producing epilogue's second output U = Y ⊙ gamma (Y as stored)."""
+    X = synth.randn_bf16((M, K), 1.0, 1)
+    W = synth.randn_bf16((N, K), 1 / math.sqrt(K), 2)
+    R = synth.randn_bf16((M, N), 1.0, 3)
+    gamma = synth.gain_f32(N, 4).to(DEV)
+    U = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    Y, r = coda.linear_residual(X.to(DEV), W.to(DEV), R.to(DEV), eps=1e-6, want_rstd=True, gamma_next=gamma,
+                                U_out=U)
+    ur, rr = O.linear_residual_fwd(to_np(X), to_np(W), to_np(R), 1e-6)
+    assert_bf16(Y, ur, "Y")
+    assert_f32(r, rr, "rstd from partials")
+    assert torch.equal(U, (Y.float() * gamma[None, :]).to(torch.bfloat16)), "U = Y * gamma"
+
+
+@pytest.mark.parametrize("shape", [synth.MlpShape(512, 512, 1408), synth.MlpShape(200, 264, 392)])
+def test_mlp_bwd_gamma_in_epilogue(coda, shape):
+    """RMSNorm -> SwiGLU MLP with the gain applied to the GEMM input
+    (U = X ⊙ gamma, weights unfolded): forward and the backward whose dX
+    epilogue emits the dgamma column partials."""
+    t = synth.make_mlp(shape, seed=1)
+    t["gamma"] = synth.gain_f32(shape.hidden, 8)
+    d, o = dev(t), f64(t)
+    eps = 1e-6
+    r, U = coda.rmsnorm_scale(d["X"], d["gamma"], eps)
+    H, g, u = coda.linear_swiglu(U, d["Wg"], d["Wu"], rstd=r)
+    f = O.mlp_fwd(o["X"], o["Wg"], o["Wu"], o["Wd"], o["R"], o["gamma"], eps)
+    assert_bf16(H, f["H"], "H")
+    gr = coda.linear_swiglu_bwd(d["dY"], d["X"], d["Wg"], d["Wu"], d["Wd"], g, u, H, rstd=r, gamma=d["gamma"],
+                                dX_resid=d["dY"])
+    torch.cuda.synchronize()
+    b = O.mlp_bwd(o["X"], o["Wg"], o["Wu"], o["Wd"], o["dY"], o["gamma"], eps)
+    assert_bf16(gr["dX"], b["dX"] + o["dY"], "dX")
+    for k in ("dWg", "dWu", "dWd", "dgamma"):
+        assert_bf16(gr[k], b[k], k)
 
 
 # ---------------------------------------------------------------- residual + partial RMS
@@ -148,12 +196,15 @@ SMALL_BLOCK = synth.BlockShape(tokens=256, hidden=512, n_q=4, n_kv=2, head_dim=1
 RAGGED_BLOCK = synth.BlockShape(tokens=200, hidden=264, n_q=2, n_kv=1, head_dim=128, inter=392, seq_len=64)
 
 
+@pytest.mark.parametrize("fold_weights", [False, True])
 @pytest.mark.parametrize("shape", [SMALL_BLOCK, RAGGED_BLOCK])
-def test_block_fwd_bwd(coda, shape):
+def test_block_fwd_bwd(coda, shape, fold_weights):
+    """Both ways of applying the RMSNorm gains: in the producing epilogue
+    (u = x ⊙ gamma, the default) and folded into the weights."""
     from gemm_epilogue_transformer_bf16_gb300.block import Block
     t = synth.make_block(shape, seed=0)
     d, o = dev(t), f64(t)
-    blk = Block(shape, d)
+    blk = Block(shape, d, fold_weights=fold_weights)
     f = blk.forward(d["x0"], d["A"], d["pos"])
     g = blk.backward(d["x0"], d["A"], d["pos"], d["dx2"], d["dQ"], d["dK"], d["dV"])
     torch.cuda.synchronize()

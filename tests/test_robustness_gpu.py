@@ -108,9 +108,9 @@ def test_mlp_backward_side_stream_matches_single_stream(coda):
     Wgf = coda.fold_gamma(Wg, gamma)
     Wuf = coda.fold_gamma(Wu, gamma)
     H, g, u = coda.linear_swiglu(X, Wgf, Wuf, rstd=rstd)
-    one = coda.linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=rstd, gamma=gamma, Wgf=Wgf, Wuf=Wuf, dX_resid=dY)
+    one = coda.linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=rstd, gamma=gamma, dX_resid=dY)
     side = torch.cuda.Stream()
-    two = coda.linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=rstd, gamma=gamma, Wgf=Wgf, Wuf=Wuf, dX_resid=dY,
+    two = coda.linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=rstd, gamma=gamma, dX_resid=dY,
                                  side_stream=side)
     torch.cuda.synchronize()
     for k in ("dX", "dWg", "dWu", "dWd", "dgamma"):
