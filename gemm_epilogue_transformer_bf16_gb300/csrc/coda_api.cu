@@ -118,18 +118,21 @@ struct Plan {
 // the B tile through TMA multicast cut each SM's operand traffic by another
 // quarter.  A problem of one 128-row block keeps single CTAs.  In the
 // environment, CODA_CTA_PAIR=0 selects single CTAs everywhere and
-// CODA_CTA_QUAD=0 stops at pairs (for comparisons).
-int cluster_ctas(int64_t M) {
+// CODA_CTA_QUAD=0 stops at pairs (for comparisons); CODA_CTA_QUAD=2 keeps
+// two-pair clusters for GEMMs with an MN-major operand or K <= 4096 only.
+int cluster_ctas(int64_t M, int a_mn, int b_mn, int64_t K) {
   static const bool pairs = [] {
     const char* v = std::getenv("CODA_CTA_PAIR");
     return !(v && v[0] == '0');
   }();
-  static const bool quads = [] {
+  static const int quads = [] {
     const char* v = std::getenv("CODA_CTA_QUAD");
-    return !(v && v[0] == '0');
+    return v ? std::atoi(v) : 1;
   }();
   if (!pairs || M <= coda::BM) return 1;
-  return (quads && M > 2 * coda::BM) ? 4 : 2;
+  if (M <= 2 * coda::BM || quads == 0) return 2;
+  if (quads == 2 && !a_mn && !b_mn && K > 4096) return 2;
+  return 4;
 }
 
 // Units of the M tile per raster group (2048 rows by default): concurrent
@@ -181,7 +184,7 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   if (!get_encoder()) return CODA_ERR_CUDA;
   const int sms = num_sms();
   if (sms <= 0) return CODA_ERR_CUDA;
-  const int cg = cluster_ctas(p.M);
+  const int cg = cluster_ctas(p.M, p.a_mn, p.b_mn, p.K + p.K2);
   const bool pair = cg >= 2;
   // K-major B rows one TMA copy stages: the tile's N, its half per pair CTA,
   // a quarter per CTA with two pairs (each copy multicast to both pairs)
