@@ -104,6 +104,14 @@ def test_rejects_bad_arguments_on_host(lib):
                                        None) == 3
     # K == 0 with work to do
     assert lib.coda_linear_residual_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, 16, 64, 0, ws, 4096, None) == 3
+    # gain output: gamma_next and U_out come together
+    assert lib.coda_linear_residual(FAKE, FAKE, None, FAKE, 1e-6, None, FAKE, None, 16, 64, 64, ws, 4096,
+                                    None) == 1
+    # RMSNorm prepass: every pointer required and aligned, row strides >= K and multiples of 8
+    assert lib.coda_rmsnorm_scale(FAKE, 64, 16, 64, 1e-6, None, FAKE, FAKE, 64, None) == 1
+    assert lib.coda_rmsnorm_scale(FAKE, 64, 16, 64, 1e-6, FAKE, FAKE, FAKE_UNALIGNED, 64, None) == 2
+    assert lib.coda_rmsnorm_scale(FAKE, 64, 16, 64, 1e-6, FAKE, FAKE, FAKE, 60, None) == 1
+    assert lib.coda_rmsnorm_scale(FAKE, 64, 0, 64, 1e-6, FAKE, FAKE, FAKE, 64, None) == 0
 
 
 def test_empty_problem_is_a_noop(lib):

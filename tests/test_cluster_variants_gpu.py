@@ -1,0 +1,22 @@
+"""The GEMM kernel in each cluster size: single CTAs (CODA_CTA_PAIR=0), CTA
+pairs only (CODA_CTA_QUAD=0), and the per-GEMM policy CODA_CTA_QUAD=2.  The
+switches are read once per process, so each variant runs
+cluster_variant_check.py (block forward/backward, FP8 linear, against the
+fp64 oracle) in a fresh process."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.mark.parametrize("env", [{"CODA_CTA_PAIR": "0"}, {"CODA_CTA_QUAD": "0"}, {"CODA_CTA_QUAD": "2"}])
+def test_cluster_variant(env):
+    e = dict(os.environ)
+    e.update(env)
+    r = subprocess.run([sys.executable, os.path.join(HERE, "cluster_variant_check.py")], env=e,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), f"{env}:\n{r.stdout[-2000:]}\n{r.stderr[-4000:]}"
