@@ -358,7 +358,7 @@ def linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=None, gamma=None, dX_resi
     return out
 
 
-def linear_qknorm_rope(X, Wf_qkv, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, rstd=None, eps=1e-6,
+def linear_qknorm_rope(X, W, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, rstd=None, eps=1e-6,
                        head_dim=128, save=True, out=None, ws=None, stream=None):
     lib = load()
     M, Kd = X.shape
@@ -372,7 +372,7 @@ def linear_qknorm_rope(X, Wf_qkv, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, rst
     max_pos = cos_sin.shape[0]
     ws = _ws(ws, lib.coda_linear_qknorm_rope_workspace_size(M, Kd, n_q, n_kv, head_dim), dev)
     _check("coda_linear_qknorm_rope", lib.coda_linear_qknorm_rope(
-        _bf(X, "X"), _f32(rstd, "rstd"), _bf(Wf_qkv, "Wf_qkv"), _f32(gamma_q, "gamma_q"),
+        _bf(X, "X"), _f32(rstd, "rstd"), _bf(W, "W"), _f32(gamma_q, "gamma_q"),
         _f32(gamma_k, "gamma_k"), _i32(pos, "pos"), _f32(cos_sin, "cos_sin"), max_pos, float(eps),
         n_q, n_kv, head_dim, _bf(out["Q"], "Q"), _bf(out["K"], "K"), _bf(out["V"], "V"),
         _bf(out.get("qk_save"), "qk_save"), M, Kd, _ptr(ws), ws.numel(), _stream(stream)))

@@ -994,7 +994,7 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
 // ------------------------------------------------------------------ linear_qknorm_rope
 size_t coda_linear_qknorm_rope_workspace_size(int64_t, int64_t, int32_t, int32_t, int32_t) { return WS_HEADER; }
 
-int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf16* Wf_qkv, const float* gamma_q,
+int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf16* W, const float* gamma_q,
                             const float* gamma_k, const int32_t* pos, const float* cos_sin, int32_t max_pos,
                             float eps, int32_t n_q, int32_t n_kv, int32_t head_dim, coda_bf16* Q, coda_bf16* K,
                             coda_bf16* V, coda_bf16* qk_save, int64_t M, int64_t Kdim, void* ws, size_t ws_bytes,
@@ -1024,9 +1024,9 @@ int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf
   d.K = K;
   d.V = V;
   CK(req(X));
-  CK(req(Wf_qkv));
+  CK(req(W));
   CK(al(rstd));
-  return coda_gemm_epilogue(&d, X, Kdim, CODA_K_MAJOR, Wf_qkv, Kdim, CODA_K_MAJOR, nullptr, N, CODA_BF16, M, N,
+  return coda_gemm_epilogue(&d, X, Kdim, CODA_K_MAJOR, W, Kdim, CODA_K_MAJOR, nullptr, N, CODA_BF16, M, N,
                             Kdim, ws, ws_bytes, stream);
 }
 

@@ -306,16 +306,18 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
  * linear_qknorm_rope (x-tip guide functional API): RMSNorm-reparameterised
  * fused QKV projection with per-head QK-RMSNorm and RoPE in the epilogue.
  *
- *   [q | k | v] = r ⊙ (X Wf_qkv^T),  Wf_qkv = W_qkv diag(gamma_in),
+ *   [q | k | v] = r ⊙ (X W^T),   which is RMSNorm(x, gamma_in) W_qkv^T when
+ *   either X = x ⊙ gamma_in (coda_rmsnorm_scale) and W = W_qkv, or X = x and
+ *   W = W_qkv diag(gamma_in) (coda_fold_gamma);
  *   Q_h = RoPE(RMSNorm_d(q_h) ⊙ gamma_q, pos),  K_h likewise, V = v.
- * head_dim must be 128.  Column order of Wf_qkv rows: n_q q heads, then
- * n_kv k heads, then n_kv v heads.  X [M, Kdim]; Wf_qkv [(n_q+2n_kv)*128, Kdim];
+ * head_dim must be 128.  Column order of W rows: n_q q heads, then
+ * n_kv k heads, then n_kv v heads.  X [M, Kdim]; W [(n_q+2n_kv)*128, Kdim];
  * rstd [M] (NULL: r = 1); gamma_q, gamma_k [128]; pos [M] int32 in
  * [0, max_pos); cos_sin from coda_rope_table.  Outputs Q [M, n_q*128],
  * K, V [M, n_kv*128]; qk_save [M, (n_q+n_kv)*128] pre-norm q|k or NULL.
  * ---------------------------------------------------------------------- */
 size_t coda_linear_qknorm_rope_workspace_size(int64_t M, int64_t Kdim, int32_t n_q, int32_t n_kv, int32_t head_dim);
-int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf16* Wf_qkv,
+int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf16* W,
                             const float* gamma_q, const float* gamma_k, const int32_t* pos,
                             const float* cos_sin, int32_t max_pos, float eps,
                             int32_t n_q, int32_t n_kv, int32_t head_dim,
