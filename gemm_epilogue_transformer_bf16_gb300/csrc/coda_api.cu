@@ -179,19 +179,75 @@ void wait_sleep(uint32_t& producer, uint32_t& epilogue) {
   epilogue = v.second;
 }
 
-int run(const Plan& p, int* status, cudaStream_t s) {
-  if (p.M == 0 || p.N == 0) return CODA_OK;
-  if (!get_encoder()) return CODA_ERR_CUDA;
-  const int sms = num_sms();
-  if (sms <= 0) return CODA_ERR_CUDA;
-  const int cg = cluster_ctas(p.M, p.a_mn, p.b_mn, p.K + p.K2);
+#define CK(x)                  \
+  do {                         \
+    int _r = (x);              \
+    if (_r != CODA_OK) return _r; \
+  } while (0)
+#define CU(x) \
+  do { if ((x) != cudaSuccess) return CODA_ERR_CUDA; } while (0)
+
+// Events that order work across two streams within one call; destroyed when
+// the call returns (destruction of a recorded event is deferred by the
+// runtime until the work it tracks has completed).
+class EventSet {
+ public:
+  explicit EventSet(int n) : n_(n) {
+    for (int i = 0; i < n_; ++i)
+      if (cudaEventCreateWithFlags(&e_[i], cudaEventDisableTiming) != cudaSuccess) ok_ = false;
+  }
+  ~EventSet() {
+    for (int i = 0; i < n_; ++i)
+      if (e_[i]) cudaEventDestroy(e_[i]);
+  }
+  EventSet(const EventSet&) = delete;
+  EventSet& operator=(const EventSet&) = delete;
+  bool ok() const { return ok_; }
+  cudaEvent_t operator[](int i) const { return e_[i]; }
+
+ private:
+  int n_;
+  bool ok_ = true;
+  cudaEvent_t e_[4] = {};
+};
+
+// Kernel dispatch by epilogue kind and operand type.  With a.query_clusters
+// set, reports the resident-cluster limit of that kernel instead of launching.
+int dispatch(const Plan& p, int sms, int cg, cudaStream_t s, const CUtensorMap* maps, const GemmArgs& a) {
+  const int nu = a.num_units;
+  cudaError_t err;
+  if (p.fp8) {
+    if (p.kind == coda::EpiKind::Plain)
+      err = coda::launch_gemm_plain_fp8(nu, sms, cg, s, maps, a);
+    else if (p.kind == coda::EpiKind::Swiglu)
+      err = coda::launch_gemm_swiglu_fp8(nu, sms, cg, s, maps, a);
+    else
+      return CODA_ERR_UNSUPPORTED;
+    return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
+  }
+  switch (p.kind) {
+    case coda::EpiKind::Plain: err = coda::launch_gemm_plain(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::Swiglu: err = coda::launch_gemm_swiglu(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::DSwiglu: err = coda::launch_gemm_dswiglu(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::QkRope: err = coda::launch_gemm_qkrope(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::CeLse: err = coda::launch_gemm_celse(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::CeDlogits: err = coda::launch_gemm_cedlogits(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::ColDot: err = coda::launch_gemm_coldot(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::Sigmoid: err = coda::launch_gemm_sigmoid(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::RmsDx: err = coda::launch_gemm_rmsdx(nu, sms, cg, s, maps, a); break;
+    default: return CODA_ERR_INVALID_ARG;
+  }
+  return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
+}
+
+// Tensor maps and kernel arguments of one launch with cluster size `cg` over
+// the N tiles [nb_base, nb_base + n_tiles).
+int prepare(const Plan& p, int* status, int cg, int nb_base, int n_tiles, CUtensorMap* maps, GemmArgs& a) {
   const bool pair = cg >= 2;
   // K-major B rows one TMA copy stages: the tile's N, its half per pair CTA,
   // a quarter per CTA with two pairs (each copy multicast to both pairs)
   const uint32_t b_box_rows = static_cast<uint32_t>(BN / cg);
-  CUtensorMap maps[4];
-  std::memset(maps, 0, sizeof(maps));
-  // A operands
+  std::memset(maps, 0, 4 * sizeof(CUtensorMap));
   // a k-slice is 128 bytes: 64 bf16 or 128 e4m3 elements
   const int esz = p.fp8 ? 1 : 2;
   const uint32_t kbox = p.fp8 ? 2 * coda::BK : coda::BK;
@@ -219,11 +275,12 @@ int run(const Plan& p, int* status, cudaStream_t s) {
       maps[3] = maps[1];
     }
   }
-  GemmArgs a{};
+  a = GemmArgs{};
   a.M = static_cast<int>(p.M);
   a.N = static_cast<int>(p.N);
   a.num_m = static_cast<int>(cdiv(p.M, cg * coda::BM));
-  a.num_n = static_cast<int>(cdiv(p.N, p.b_dual ? BN / 2 : BN));
+  a.num_n = n_tiles;
+  a.nb_base = nb_base;
   a.kb0 = static_cast<int>(cdiv(p.K, kbox));
   a.kb1 = p.K2 > 0 ? static_cast<int>(cdiv(p.K2, kbox)) : 0;
   a.a_mn = p.a_mn;
@@ -240,39 +297,103 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   wait_sleep(a.producer_sleep_ns, a.epilogue_sleep_ns);
   a.e = p.e;
   a.e.st_stream = (l2_hints() & 4) ? 1 : 0;
-  const int nu = a.num_units;
-  cudaError_t err;
-  if (p.fp8) {
-    if (p.kind == coda::EpiKind::Plain)
-      err = coda::launch_gemm_plain_fp8(nu, sms, cg, s, maps, a);
-    else if (p.kind == coda::EpiKind::Swiglu)
-      err = coda::launch_gemm_swiglu_fp8(nu, sms, cg, s, maps, a);
-    else
-      return CODA_ERR_UNSUPPORTED;
-    return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
-  }
-  switch (p.kind) {
-    case coda::EpiKind::Plain: err = coda::launch_gemm_plain(nu, sms, cg, s, maps, a); break;
-    case coda::EpiKind::Swiglu: err = coda::launch_gemm_swiglu(nu, sms, cg, s, maps, a); break;
-    case coda::EpiKind::DSwiglu: err = coda::launch_gemm_dswiglu(nu, sms, cg, s, maps, a); break;
-    case coda::EpiKind::QkRope: err = coda::launch_gemm_qkrope(nu, sms, cg, s, maps, a); break;
-    case coda::EpiKind::CeLse: err = coda::launch_gemm_celse(nu, sms, cg, s, maps, a); break;
-    case coda::EpiKind::CeDlogits: err = coda::launch_gemm_cedlogits(nu, sms, cg, s, maps, a); break;
-    case coda::EpiKind::ColDot: err = coda::launch_gemm_coldot(nu, sms, cg, s, maps, a); break;
-    case coda::EpiKind::Sigmoid: err = coda::launch_gemm_sigmoid(nu, sms, cg, s, maps, a); break;
-    case coda::EpiKind::RmsDx: err = coda::launch_gemm_rmsdx(nu, sms, cg, s, maps, a); break;
-    default: return CODA_ERR_INVALID_ARG;
-  }
-  return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
+  return CODA_OK;
 }
 
-#define CK(x)                  \
-  do {                         \
-    int _r = (x);              \
-    if (_r != CODA_OK) return _r; \
-  } while (0)
-#define CU(x) \
-  do { if ((x) != cudaSuccess) return CODA_ERR_CUDA; } while (0)
+// The stream that carries the CTA-pair slice of a split launch issued on
+// `s`: one non-blocking stream per (device, caller stream), created once and
+// kept for the process, so that GEMMs the caller runs concurrently on
+// different streams do not queue behind each other's slices.
+cudaStream_t side_stream(cudaStream_t s) {
+  static std::mutex mu;
+  constexpr int kSlots = 64;
+  static int dev_of[kSlots];
+  static cudaStream_t key[kSlots];
+  static cudaStream_t val[kSlots];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (dev_of[i] == dev && key[i] == s) return val[i];
+  if (used == kSlots) return nullptr;  // no more slots: the caller launches unsplit
+  cudaStream_t t = nullptr;
+  if (cudaStreamCreateWithFlags(&t, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+  dev_of[used] = dev;
+  key[used] = s;
+  val[used] = t;
+  ++used;
+  return t;
+}
+
+// Split launches: the two-pair kernel leaves the SMs its 4-CTA clusters
+// cannot use (GPCs whose SM count is not a multiple of 4) idle.  A CTA-pair
+// kernel sized to those SMs takes the last N tiles, on a second stream, and
+// the split point balances the two kernels' waves (a two-pair unit and a
+// pair unit take the same time).  CODA_SPLIT=0 in the environment turns it
+// off (for comparisons).
+bool split_enabled() {
+  static const bool v = [] {
+    const char* e = std::getenv("CODA_SPLIT");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
+
+int run(const Plan& p, int* status, cudaStream_t s) {
+  if (p.M == 0 || p.N == 0) return CODA_OK;
+  if (!get_encoder()) return CODA_ERR_CUDA;
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  const int cg = cluster_ctas(p.M, p.a_mn, p.b_mn, p.K + p.K2);
+  const int num_n = static_cast<int>(cdiv(p.N, p.b_dual ? BN / 2 : BN));
+  CUtensorMap maps[4];
+  GemmArgs a;
+  if (cg == 4 && p.n_per_unit <= 1 && num_n >= 4 && split_enabled()) {
+    // resident clusters of the two-pair and the pair kernel
+    int q_max = 0, p_max = 0;
+    CK(prepare(p, status, 4, 0, num_n, maps, a));
+    a.query_clusters = &q_max;
+    CK(dispatch(p, sms, 4, s, maps, a));
+    CK(prepare(p, status, 2, 0, num_n, maps, a));
+    a.query_clusters = &p_max;
+    CK(dispatch(p, sms, 2, s, maps, a));
+    const int extra = p_max - 2 * q_max;  // pairs that fit beside a full two-pair grid
+    if (q_max > 0 && extra > 0) {
+      const int64_t mq = cdiv(p.M, 4 * coda::BM), mp = cdiv(p.M, 2 * coda::BM);
+      const int64_t t0 = cdiv(mq * num_n, q_max);
+      int best = 0;
+      int64_t tbest = t0;
+      for (int np = 1; np <= num_n / 4; ++np) {
+        const int64_t t = std::max(cdiv(mq * (num_n - np), q_max), cdiv(mp * np, extra));
+        if (t < tbest) {
+          tbest = t;
+          best = np;
+        }
+      }
+      cudaStream_t s2 = best > 0 ? side_stream(s) : nullptr;
+      if (s2) {
+        EventSet ev(2);
+        if (!ev.ok()) return CODA_ERR_CUDA;
+        CU(cudaEventRecord(ev[0], s));
+        CU(cudaStreamWaitEvent(s2, ev[0], 0));
+        CK(prepare(p, status, 4, 0, num_n - best, maps, a));
+        CK(dispatch(p, sms, 4, s, maps, a));
+        CUtensorMap maps2[4];
+        GemmArgs a2;
+        CK(prepare(p, status, 2, num_n - best, best, maps2, a2));
+        a2.max_clusters = extra;
+        CK(dispatch(p, sms, 2, s2, maps2, a2));
+        CU(cudaEventRecord(ev[1], s2));
+        CU(cudaStreamWaitEvent(s, ev[1], 0));
+        return CODA_OK;
+      }
+    }
+  }
+  CK(prepare(p, status, cg, 0, num_n, maps, a));
+  return dispatch(p, sms, cg, s, maps, a);
+}
+
 
 // Argument checks.  `need` pointers must be non-null; every non-null pointer
 // must be 16-byte aligned.
@@ -295,30 +416,6 @@ int ws_ok(const void* ws, size_t have, size_t need) {
 }
 
 cudaStream_t S(coda_stream s) { return static_cast<cudaStream_t>(s); }
-
-// Events that order work across two streams within one call; destroyed when
-// the call returns (destruction of a recorded event is deferred by the
-// runtime until the work it tracks has completed).
-class EventSet {
- public:
-  explicit EventSet(int n) : n_(n) {
-    for (int i = 0; i < n_; ++i)
-      if (cudaEventCreateWithFlags(&e_[i], cudaEventDisableTiming) != cudaSuccess) ok_ = false;
-  }
-  ~EventSet() {
-    for (int i = 0; i < n_; ++i)
-      if (e_[i]) cudaEventDestroy(e_[i]);
-  }
-  EventSet(const EventSet&) = delete;
-  EventSet& operator=(const EventSet&) = delete;
-  bool ok() const { return ok_; }
-  cudaEvent_t operator[](int i) const { return e_[i]; }
-
- private:
-  int n_;
-  bool ok_ = true;
-  cudaEvent_t e_[4] = {};
-};
 const __nv_bfloat16* BF(const coda_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
 __nv_bfloat16* BF(coda_bf16* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
 

@@ -129,6 +129,7 @@ struct GemmArgs {
   int n_per_unit;    // consecutive N tiles handled as one unit (running state)
   int num_units;
   int group_m;       // raster: M blocks per group
+  int nb_base;       // first N tile of this launch (a launch may cover a slice of N)
   uint32_t idesc;
   int* status;
   uint64_t timeout_ns;
@@ -136,6 +137,9 @@ struct GemmArgs {
   uint32_t producer_sleep_ns;  // back-off of the producer's and the epilogue's
   uint32_t epilogue_sleep_ns;  // barrier waits (0 = spin)
   EpiArgs e;
+  // host side only (the kernel ignores them)
+  int max_clusters;     // > 0: launch at most this many clusters
+  int* query_clusters;  // non-null: report the resident-cluster limit and launch nothing
 };
 
 struct TileInfo {
@@ -156,7 +160,7 @@ __device__ __forceinline__ void unit_coords(const GemmArgs& a, int u, int& mb, i
     const int gm = min(a.group_m, a.num_m - first_m);
     const int r = u - g * per_group;
     mb = first_m + r % gm;
-    nb0 = r / gm;
+    nb0 = a.nb_base + r / gm;
     nlen = 1;
     chunk = nb0;
   } else {

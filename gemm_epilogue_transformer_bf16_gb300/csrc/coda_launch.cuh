@@ -48,9 +48,19 @@ cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CU
       fprintf(stderr, "coda: cluster size %d, %d resident clusters\n", CG, n);
 #endif
     }
-    cfg.gridDim = dim3(static_cast<unsigned>(CG * std::min(num_units, max_clusters[dev])));
+    if (a.query_clusters) {
+      *a.query_clusters = max_clusters[dev];
+      return cudaSuccess;
+    }
+    const int cap = a.max_clusters > 0 ? std::min(a.max_clusters, max_clusters[dev]) : max_clusters[dev];
+    cfg.gridDim = dim3(static_cast<unsigned>(CG * std::min(num_units, cap)));
   } else {
-    cfg.gridDim = dim3(static_cast<unsigned>(std::min(num_units, sms)));
+    if (a.query_clusters) {
+      *a.query_clusters = sms;
+      return cudaSuccess;
+    }
+    const int cap = a.max_clusters > 0 ? std::min(a.max_clusters, sms) : sms;
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min(num_units, cap)));
   }
   e = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], a);
   if (e != cudaSuccess) return e;

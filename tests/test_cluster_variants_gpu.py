@@ -1,5 +1,7 @@
 """The GEMM kernel in each cluster size: single CTAs (CODA_CTA_PAIR=0), CTA
-pairs only (CODA_CTA_QUAD=0), and the per-GEMM policy CODA_CTA_QUAD=2.  The
+pairs only (CODA_CTA_QUAD=0), the per-GEMM policy CODA_CTA_QUAD=2 and split
+launches turned off (CODA_SPLIT=0; by default a two-pair kernel and a pair
+kernel share the GPU).  The
 switches are read once per process, so each variant runs
 cluster_variant_check.py (block forward/backward, FP8 linear, against the
 fp64 oracle) in a fresh process."""
@@ -13,7 +15,8 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-@pytest.mark.parametrize("env", [{"CODA_CTA_PAIR": "0"}, {"CODA_CTA_QUAD": "0"}, {"CODA_CTA_QUAD": "2"}])
+@pytest.mark.parametrize("env", [{"CODA_CTA_PAIR": "0"}, {"CODA_CTA_QUAD": "0"}, {"CODA_CTA_QUAD": "2"},
+                                 {"CODA_SPLIT": "0"}])
 def test_cluster_variant(env):
     e = dict(os.environ)
     e.update(env)
