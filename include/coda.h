@@ -21,7 +21,11 @@
  *    device status word (zero it once, e.g. with coda_reset_status, before
  *    first use).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
- *    default stream).  They return after enqueueing.
+ *    default stream).  They return after enqueueing.  A GEMM may run part of
+ *    its tiles on a second, library-created non-blocking stream (one per
+ *    device and caller stream, kept for the process), forked from and joined
+ *    back to `stream` with events inside the call: work the caller enqueues
+ *    on `stream` afterwards is ordered after all of it.
  *  - Matrices are row-major with a leading dimension (row stride) given in
  *    ELEMENTS.  Weights use the nn.Linear layout [out_features, in_features].
  *  - bf16 tensors are passed as uint16_t bit patterns (coda_bf16).  All
