@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstdio>
@@ -64,17 +65,17 @@ bool get_encoder() {
   return g_encode != nullptr;
 }
 
-int g_num_sms[64] = {0};
+std::atomic<int> g_num_sms[64];  // per device, cached on first use
 
 int num_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (g_num_sms[dev] == 0) {
-    int n = 0;
+  int n = g_num_sms[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    g_num_sms[dev] = n;
+    g_num_sms[dev].store(n, std::memory_order_relaxed);  // every thread stores the same value
   }
-  return g_num_sms[dev];
+  return n;
 }
 
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride

@@ -4,7 +4,9 @@
 // clustered variants (CTA pairs, two pairs sharing B), as many 2- or 4-CTA
 // clusters as can be resident at once (cudaOccupancyMaxActiveClusters).
 #pragma once
+#include <atomic>
 #include <cstdio>
+#include <mutex>
 #include "coda_epilogues.cuh"
 #include "coda_internal.h"
 
@@ -13,17 +15,24 @@ namespace coda {
 template <int BN, class Epi, int CG, bool FP8>
 cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a) {
   constexpr uint32_t smem = GemmCfg<BN, (CG >= 2)>::SMEM_BYTES;
-  static bool attr_done[64] = {};
-  static int max_clusters[64] = {};
+  // per device, set up once (first calls from several host threads are
+  // serialised on `init`): the shared-memory limit and the resident-cluster
+  // count; afterwards read without the lock
+  static std::mutex init;
+  static std::atomic<bool> attr_done[64];
+  static std::atomic<int> max_clusters[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   auto kern = coda_gemm_kernel<BN, Epi, CG, FP8>;
-  if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(init);
+    if (!attr_done[dev].load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      attr_done[dev].store(true, std::memory_order_release);
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS);
@@ -37,22 +46,26 @@ cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CU
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (max_clusters[dev] == 0) {
-      cfg.gridDim = dim3(static_cast<unsigned>(sms - sms % CG));
-      int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-      if (e != cudaSuccess) return e;
-      if (n <= 0) return cudaErrorInvalidConfiguration;
-      max_clusters[dev] = n;
+    if (max_clusters[dev].load(std::memory_order_acquire) == 0) {
+      std::lock_guard<std::mutex> lock(init);
+      if (max_clusters[dev].load(std::memory_order_relaxed) == 0) {
+        cfg.gridDim = dim3(static_cast<unsigned>(sms - sms % CG));
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n <= 0) return cudaErrorInvalidConfiguration;
+        max_clusters[dev].store(n, std::memory_order_release);
 #ifdef CODA_DEBUG_LAUNCH
-      fprintf(stderr, "coda: cluster size %d, %d resident clusters\n", CG, n);
+        fprintf(stderr, "coda: cluster size %d, %d resident clusters\n", CG, n);
 #endif
+      }
     }
+    const int resident = max_clusters[dev].load(std::memory_order_acquire);
     if (a.query_clusters) {
-      *a.query_clusters = max_clusters[dev];
+      *a.query_clusters = resident;
       return cudaSuccess;
     }
-    const int cap = a.max_clusters > 0 ? std::min(a.max_clusters, max_clusters[dev]) : max_clusters[dev];
+    const int cap = a.max_clusters > 0 ? std::min(a.max_clusters, resident) : resident;
     cfg.gridDim = dim3(static_cast<unsigned>(CG * std::min(num_units, cap)));
   } else {
     if (a.query_clusters) {
