@@ -166,3 +166,53 @@ def test_swiglu_cluster_boundaries(coda, M):
     torch.cuda.synchronize()
     ref = O.swiglu_fwd(to_np(X), to_np(Wg), to_np(Wu))
     assert_bf16(H, ref[0], f"H M={M}")
+
+
+@pytest.mark.parametrize("a_major,b_major", [(0, 0), (1, 1), (0, 1)])
+@pytest.mark.parametrize("M,N", [(500, 36 * 256 + 200), (300, 36 * 256 + 8)])
+def test_split_launch_ragged(coda, a_major, b_major, M, N):
+    """A GEMM that takes a split launch on a 152-SM GB300: one two-pair tile
+    row and 37 N tiles -- 36 for the 36 resident 4-CTA clusters, the last,
+    ragged tile for a CTA-pair kernel beside them (one wave instead of two).
+    Parity, and nothing written outside the M x N window of a larger
+    buffer."""
+    K = 136
+    dev = "cuda"
+    A = randn_bf16((M, K), 1.0, 81)
+    B = randn_bf16((N, K), 1.0 / np.sqrt(K), 82)
+    full = torch.full((M + 24, N + 40), 7.0, dtype=torch.bfloat16, device=dev)
+    lda = None
+    Ad = _operand(A, a_major)
+    if a_major == 1:
+        lda = (M + 7) // 8 * 8
+        Ad = torch.zeros(K, lda, dtype=torch.bfloat16)
+        Ad[:, :M] = A.t()
+    ws = coda.gemm_epilogue(coda.EpilogueDesc(), Ad.to(dev), _operand(B, b_major).to(dev), full, M, N, K,
+                            a_major=a_major, b_major=b_major, lda=lda, ldd=N + 40)
+    torch.cuda.synchronize()
+    assert coda.get_status(ws) == 0
+    assert_bf16(full[:M, :N], O.gemm_epilogue_plain(to_np(A), to_np(B)), f"D {M}x{N}")
+    assert bool((full[M:] == 7.0).all()), "write below row M"
+    assert bool((full[:, N:] == 7.0).all()), "write right of column N"
+
+
+def test_split_launch_swiglu_and_partials(coda):
+    """Split launches on the gate/up dual-B tile (I = 36 * 128 + 72: 37
+    half-tiles) and on a residual epilogue whose row partials (the next
+    RMSNorm's r) come from both slices."""
+    M, I, K = 500, 36 * 128 + 72, 136
+    dev = "cuda"
+    X = randn_bf16((M, K), 1.0, 91)
+    Wg = randn_bf16((I, K), 1.0 / np.sqrt(K), 92)
+    Wu = randn_bf16((I, K), 1.0 / np.sqrt(K), 93)
+    H, g, u = coda.linear_swiglu(X.to(dev), Wg.to(dev), Wu.to(dev))
+    N = 36 * 256 + 200
+    R = randn_bf16((M, N), 1.0, 94)
+    W = randn_bf16((N, K), 1.0 / np.sqrt(K), 95)
+    Y, r = coda.linear_residual(X.to(dev), W.to(dev), R.to(dev), eps=1e-6, want_rstd=True)
+    torch.cuda.synchronize()
+    ref = O.swiglu_fwd(to_np(X), to_np(Wg), to_np(Wu))
+    assert_bf16(H, ref[0], "H")
+    yr, rr = O.linear_residual_fwd(to_np(X), to_np(W), to_np(R), 1e-6)
+    assert_bf16(Y, yr, "Y")
+    assert_f32(r, rr, "rstd from both slices' partials")
