@@ -52,7 +52,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-unfused", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--no-ce", action="store_true", help="skip the linear + cross-entropy side measurement")
+    p.add_argument("--no-ce", action="store_true",
+                   help="skip the side measurements (linear + cross-entropy, FP8 gate/up, MLP, RMSNorm-linear)")
     p.add_argument("--serial", action="store_true", help="run the step's calls on one stream")
     p.add_argument("--fold-weights", action="store_true",
                    help="fold the RMSNorm gains into the weights each step instead of applying them in the "
@@ -472,7 +473,6 @@ def main():
     other = {}
     if not args.no_ce:
         from gemm_epilogue_transformer_bf16_gb300.block import LinearCE
-        from oracle.coda_oracle import ce_flops
         cs_ = synth.FULL["c4"]
         hc = synth.make_ce(cs_, seed=rank)
         dc = {k: v.to(dev) for k, v in hc.items()}
@@ -495,8 +495,9 @@ def main():
             bw.append(ev[1].elapsed_time(ev[2]))
         if coda.get_status(ce.ws) != 0:
             raise RuntimeError("device status error in the linear-CE measurement")
-        f_fwd = ce_flops(cs_.tokens, cs_.hidden, cs_.vocab, backward=False)
-        f_all = ce_flops(cs_.tokens, cs_.hidden, cs_.vocab)
+        # 2*M*N*K: the logits GEMM forward; the backward recomputes them, then dX and dW
+        f_fwd = 2 * cs_.tokens * cs_.hidden * cs_.vocab
+        f_all = 4 * f_fwd
         mf, mb = statistics.median(fw), statistics.median(bw)
         other["linear_cross_entropy"] = {
             "workload": "tokens 8192, hidden 2048, vocab 128256, 5% ignored labels; fwd (online LSE epilogue + "
@@ -534,6 +535,54 @@ def main():
             "peak": round(fp8_peak, 1), "peak_kind": f"fp8 = 2 x bf16 burst ({peak_src}, nominal ratio)",
             "frac": round(gf[DOMINANT] / (m8 / 1e3) / 1e12 / fp8_peak, 4)}
         del xq, gq, uq, Hq, gq8, uq8
+
+        # Configs 3 and 2 (also parity workloads), forward + backward, timed the
+        # same way: the SwiGLU MLP at hidden 4096 and the RMSNorm-reparameterised
+        # projection + residual of config 2 (gain folded into W: the standalone
+        # operator's form).  FLOPs 2*M*N*K per GEMM.
+        def time_calls(fn, n=5, warm=2):
+            for _ in range(warm):
+                fn()
+            torch.cuda.synchronize(dev)
+            ev[0].record(stream)
+            for _ in range(n):
+                fn()
+            ev[1].record(stream)
+            torch.cuda.synchronize(dev)
+            return ev[0].elapsed_time(ev[1]) / n
+
+        s3 = synth.FULL["c3"]
+        d3 = {k: v.to(dev) for k, v in synth.make_mlp(s3, seed=rank).items()}
+        ws3 = coda.workspace(max(coda.load().coda_linear_swiglu_bwd_workspace_size(s3.tokens, s3.inter, s3.hidden),
+                                 coda.load().coda_linear_residual_workspace_size(s3.tokens, s3.hidden, s3.inter)), dev)
+        o3 = {}
+
+        def mlp_step():
+            H3, g3, u3 = coda.linear_swiglu(d3["X"], d3["Wg"], d3["Wu"], ws=ws3)
+            coda.linear_residual(H3, d3["Wd"], d3["R"], ws=ws3)
+            o3["g"] = coda.linear_swiglu_bwd(d3["dY"], d3["X"], d3["Wg"], d3["Wu"], d3["Wd"], g3, u3, H3, ws=ws3)
+        m3 = time_calls(mlp_step)
+        f3 = 2 * s3.tokens * s3.hidden * s3.inter * 3 * 3       # fwd 3 GEMMs, bwd 6
+        other["mlp_swiglu"] = {
+            "workload": f"SwiGLU MLP fwd+bwd, tokens {s3.tokens}, hidden {s3.hidden}, intermediate {s3.inter}",
+            "ms": round(m3, 3), "tflops": round(f3 / (m3 / 1e3) / 1e12, 1),
+            "frac_of_sustained": round(f3 / (m3 / 1e3) / 1e12 / sustained, 4)}
+        del d3, o3, ws3
+        s2 = synth.FULL["c2"]
+        d2 = {k: v.to(dev) for k, v in synth.make_rms_linear(s2, seed=rank).items()}
+
+        def rms_step():
+            Wf = coda.fold_gamma(d2["W"], d2["gamma"])
+            Y2, r2 = coda.rmsnorm_linear(d2["X"], Wf, d2["R"], eps=s2.eps)
+            coda.rmsnorm_linear_bwd(d2["G"], d2["X"], d2["W"], d2["gamma"], r2, Y2, d2["R"])
+        m2 = time_calls(rms_step, n=20, warm=3)
+        f2 = 2 * s2.tokens * s2.hidden * s2.out * 3               # fwd 1 GEMM, bwd 2
+        other["rmsnorm_linear"] = {
+            "workload": f"RMSNorm-reparameterised projection + residual fwd+bwd, tokens {s2.tokens}, "
+                        f"hidden {s2.hidden}, out {s2.out} (gain fold, row RMS, prepass and combines included)",
+            "ms": round(m2, 3), "tflops": round(f2 / (m2 / 1e3) / 1e12, 1),
+            "frac_of_sustained": round(f2 / (m2 / 1e3) / 1e12 / sustained, 4)}
+        del d2
 
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None
