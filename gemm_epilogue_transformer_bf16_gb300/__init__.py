@@ -199,6 +199,28 @@ def _ws(ws, need, device):
     return ws
 
 
+def _rows(t):
+    """[..., F] -> ([M, F], leading shape) for the token-major operands of the
+    forward calls; 2-D tensors and None pass through (leading shape None)."""
+    if t is None or t.dim() == 2:
+        return t, None
+    if not t.is_contiguous():          # a copy would drop what the kernel writes
+        raise ValueError("tensors with leading dimensions must be contiguous")
+    return t.view(-1, t.shape[-1]), tuple(t.shape[:-1])
+
+
+def _lead(t, lead):
+    """Back to the caller's leading shape: [M, F] -> [*lead, F], [M] -> lead."""
+    if t is None or lead is None:
+        return t
+    return t.view(*lead, t.shape[-1]) if t.dim() == 2 else t.view(lead)
+
+
+def _vec(t, lead):
+    """A per-token vector given in the caller's leading shape, as [M]."""
+    return t if (t is None or lead is None) else t.view(-1)
+
+
 def get_status(ws, stream=None):
     return load().coda_get_status(_ptr(ws), _stream(stream))
 
@@ -228,13 +250,17 @@ def rms_rstd(X, eps, out=None, stream=None):
 
 
 def rmsnorm_scale(X, gamma, eps, rstd=None, U=None, stream=None):
-    """rstd = 1/rms(X) per row and U = X ⊙ gamma in one pass (coda_rmsnorm_scale)."""
+    """rstd = 1/rms(X) per row and U = X ⊙ gamma in one pass (coda_rmsnorm_scale).
+    X may have leading dimensions ([..., K]); the outputs keep them."""
+    X, lead = _rows(X)
+    U, _ = _rows(U)
+    rstd = _vec(rstd, lead)
     M, K = X.shape
     rstd = torch.empty(M, dtype=torch.float32, device=X.device) if rstd is None else rstd
     U = torch.empty_like(X) if U is None else U
     _check("coda_rmsnorm_scale", load().coda_rmsnorm_scale(_bf(X, "X"), K, M, K, float(eps), _f32(gamma, "gamma"),
                                                            _f32(rstd, "rstd"), _bf(U, "U"), K, _stream(stream)))
-    return rstd, U
+    return _lead(rstd, lead), _lead(U, lead)
 
 
 def rope_table(theta, head_dim, max_pos, device="cuda", out=None, stream=None):
@@ -292,8 +318,14 @@ def rmsnorm_linear_bwd(dY, X, W, gamma, rstd, Y, R=None, ws=None, out=None, stre
 def linear_residual(X, W, R=None, eps=1e-6, want_rstd=False, Y=None, rstd_out=None, gamma_next=None, U_out=None,
                     ws=None, stream=None):
     """Y = R + X W^T (coda_linear_residual); optionally the row factor of the
-    next RMSNorm (rstd_out / want_rstd) and U_out = Y ⊙ gamma_next."""
+    next RMSNorm (rstd_out / want_rstd) and U_out = Y ⊙ gamma_next.  X, R, Y,
+    U_out may have leading dimensions ([..., features]); outputs keep them."""
     lib = load()
+    X, lead = _rows(X)
+    R, _ = _rows(R)
+    Y, _ = _rows(Y)
+    U_out, _ = _rows(U_out)
+    rstd_out = _vec(rstd_out, lead)
     M, K = X.shape
     N = W.shape[0]
     Y = torch.empty(M, N, dtype=torch.bfloat16, device=X.device) if Y is None else Y
@@ -303,6 +335,7 @@ def linear_residual(X, W, R=None, eps=1e-6, want_rstd=False, Y=None, rstd_out=No
     _check("coda_linear_residual", lib.coda_linear_residual(
         _bf(X, "X"), _bf(W, "W"), _bf(R, "R"), _bf(Y, "Y"), float(eps), _f32(rstd_out, "rstd_out"),
         _f32(gamma_next, "gamma_next"), _bf(U_out, "U_out"), M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
+    Y, rstd_out = _lead(Y, lead), _lead(rstd_out, lead)
     return (Y, rstd_out) if want_rstd or rstd_out is not None else Y
 
 
@@ -320,7 +353,14 @@ def linear_residual_bwd(dY, X, W, ws=None, out=None, stream=None):
 
 
 def linear_swiglu(X, Wg, Wu, rstd=None, save=True, H=None, g=None, u=None, ws=None, stream=None):
+    """H = silu(r ⊙ X Wg^T) ⊙ (r ⊙ X Wu^T) (coda_linear_swiglu), and g, u when
+    `save`.  X may have leading dimensions ([..., K]); the outputs keep them."""
     lib = load()
+    X, lead = _rows(X)
+    H, _ = _rows(H)
+    g, _ = _rows(g)
+    u, _ = _rows(u)
+    rstd = _vec(rstd, lead)
     M, K = X.shape
     I = Wg.shape[0]
     dev = X.device
@@ -332,7 +372,7 @@ def linear_swiglu(X, Wg, Wu, rstd=None, save=True, H=None, g=None, u=None, ws=No
     _check("coda_linear_swiglu", lib.coda_linear_swiglu(
         _bf(X, "X"), _f32(rstd, "rstd"), _bf(Wg, "Wg"), _bf(Wu, "Wu"), _bf(H, "H"), _bf(g, "g"), _bf(u, "u"),
         M, I, K, _ptr(ws), ws.numel(), _stream(stream)))
-    return H, g, u
+    return _lead(H, lead), _lead(g, lead), _lead(u, lead)
 
 
 def linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=None, gamma=None, dX_resid=None, ws=None, out=None,
@@ -360,9 +400,17 @@ def linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=None, gamma=None, dX_resi
 
 def linear_qknorm_rope(X, W, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, rstd=None, eps=1e-6,
                        head_dim=128, save=True, out=None, ws=None, stream=None):
+    """QKV projection with per-head QK-RMSNorm and RoPE in the epilogue
+    (coda_linear_qknorm_rope).  X may have leading dimensions ([..., Kdim],
+    pos [...]); when it does and `out` is not given, Q, K, V, qk_save keep
+    them."""
     lib = load()
+    X, lead = _rows(X)
+    pos = _vec(pos, lead)
+    rstd = _vec(rstd, lead)
     M, Kd = X.shape
     dev = X.device
+    shaped = out is None and lead is not None
     if out is None:
         out = {"Q": torch.empty(M, n_q * head_dim, dtype=torch.bfloat16, device=dev),
                "K": torch.empty(M, n_kv * head_dim, dtype=torch.bfloat16, device=dev),
@@ -376,6 +424,8 @@ def linear_qknorm_rope(X, W, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, rstd=Non
         _f32(gamma_k, "gamma_k"), _i32(pos, "pos"), _f32(cos_sin, "cos_sin"), max_pos, float(eps),
         n_q, n_kv, head_dim, _bf(out["Q"], "Q"), _bf(out["K"], "K"), _bf(out["V"], "V"),
         _bf(out.get("qk_save"), "qk_save"), M, Kd, _ptr(ws), ws.numel(), _stream(stream)))
+    if shaped:
+        out = {k: _lead(v, lead) for k, v in out.items()}
     return out
 
 
@@ -405,8 +455,15 @@ def linear_qknorm_rope_bwd(dQ, dK, dV, qk_save, V, gamma_q, gamma_k, pos, cos_si
 
 
 def linear_cross_entropy(X, W, labels, ignore_index=-100, out=None, ws=None, stream=None):
+    """Mean token cross-entropy of softmax(X W^T) against `labels` with an
+    online log-sum-exp; logits never reach HBM (coda_linear_cross_entropy).
+    X may have leading dimensions ([..., K], labels [...]); when it does and
+    `out` is not given, lse keeps them."""
     lib = load()
+    X, lead = _rows(X)
+    labels = _vec(labels, lead)
     M, K = X.shape
+    shaped = out is None and lead is not None
     V = W.shape[0]
     dev = X.device
     if out is None:
@@ -419,6 +476,8 @@ def linear_cross_entropy(X, W, labels, ignore_index=-100, out=None, ws=None, str
         _f32(out["lse"], "lse"), _i32(out["n_valid"], "n_valid"), M, V, K, _ptr(ws), ws.numel(),
         _stream(stream)))
     out["ws"] = ws
+    if shaped:
+        out["lse"] = out["lse"].reshape(lead)
     return out
 
 
@@ -466,15 +525,19 @@ def linear_swiglu_fp8(Xq, sx, Wgq, sg, Wuq, su, rstd=None, save=True, H=None, g=
 
 
 def linear_sigmoid(X, W, Z=None, Y=None, ws=None, stream=None):
-    """sigmoid(X W^T), gating Z when given."""
+    """sigmoid(X W^T), gating Z when given.  X, Z, Y may have leading
+    dimensions ([..., features]); Y keeps them."""
     lib = load()
+    X, lead = _rows(X)
+    Z, _ = _rows(Z)
+    Y, _ = _rows(Y)
     M, K = X.shape
     N = W.shape[0]
     Y = torch.empty(M, N, dtype=torch.bfloat16, device=X.device) if Y is None else Y
     ws = _ws(ws, lib.coda_linear_sigmoid_workspace_size(M, N, K), X.device)
     _check("coda_linear_sigmoid", lib.coda_linear_sigmoid(_bf(X, "X"), _bf(W, "W"), _bf(Z, "Z"), _bf(Y, "Y"),
                                                           M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
-    return Y
+    return _lead(Y, lead)
 
 
 def linear_sigmoid_bwd(dY, X, W, Z=None, out=None, ws=None, stream=None):

@@ -303,3 +303,63 @@ def test_fp8_linear_swiglu(coda, shape):
     assert_bf16(H, Hr, "H fp8")
     assert_bf16(g, gr, "g fp8")
     assert_bf16(u, ur, "u fp8")
+
+
+# ---------------------------------------------------------------- leading dimensions
+def test_leading_dims_match_flat_calls(coda):
+    """[batch, seq, features] operands give, bit for bit, the flat [tokens,
+    features] results, reshaped to the caller's leading shape (the wrappers
+    only change views; the kernels see the same rows)."""
+    s = RAGGED_BLOCK
+    B, S = 2, s.tokens // 2
+    t = dev(synth.make_block(s, seed=11))
+    x = t["x0"]
+    x3 = x.view(B, S, -1)
+    pos3 = t["pos"].view(B, S)
+    cs = coda.rope_table(s.theta, s.head_dim, s.seq_len)
+
+    def same(a, b, name):
+        assert torch.equal(a.reshape(b.shape), b), f"{name}: the 3-D call differs from the flat one"
+
+    r2, U2 = coda.rmsnorm_scale(x, t["gamma_attn"], s.eps)
+    r3, U3 = coda.rmsnorm_scale(x3, t["gamma_attn"], s.eps)
+    assert r3.shape == (B, S) and U3.shape == x3.shape
+    same(r3, r2, "rstd")
+    same(U3, U2, "U")
+
+    q2 = coda.linear_qknorm_rope(U2, t["Wqkv"], t["gamma_q"], t["gamma_k"], t["pos"], cs, s.n_q, s.n_kv, rstd=r2)
+    q3 = coda.linear_qknorm_rope(U3, t["Wqkv"], t["gamma_q"], t["gamma_k"], pos3, cs, s.n_q, s.n_kv, rstd=r3)
+    for k in ("Q", "K", "V", "qk_save"):
+        assert q3[k].shape[:2] == (B, S)
+        same(q3[k], q2[k], k)
+
+    A = t["A"]
+    y2, ry2 = coda.linear_residual(A, t["Wo"], x, eps=s.eps, want_rstd=True)
+    y3, ry3 = coda.linear_residual(A.view(B, S, -1), t["Wo"], x3, eps=s.eps, want_rstd=True)
+    assert y3.shape == x3.shape and ry3.shape == (B, S)
+    same(y3, y2, "Y")
+    same(ry3, ry2, "rstd_out")
+
+    H2, g2, u2 = coda.linear_swiglu(y2, t["Wg"], t["Wu"], rstd=ry2)
+    H3, g3, u3 = coda.linear_swiglu(y3, t["Wg"], t["Wu"], rstd=ry3)
+    assert H3.shape == (B, S, s.inter)
+    for a, b, n in ((H3, H2, "H"), (g3, g2, "g"), (u3, u2, "u")):
+        same(a, b, n)
+
+    Z = H2[:, : s.hidden].contiguous()
+    sg2 = coda.linear_sigmoid(H2, t["Wd"], Z)
+    sg3 = coda.linear_sigmoid(H3, t["Wd"], Z.view(B, S, -1))
+    assert sg3.shape == (B, S, s.hidden)
+    same(sg3, sg2, "sigmoid")
+
+    labels = (torch.arange(s.tokens, device=DEV, dtype=torch.int32) * 7) % s.inter
+    labels[3] = -100
+    W_head = t["Wg"]                                       # [inter, hidden]: a small vocabulary
+    c2 = coda.linear_cross_entropy(x, W_head, labels)
+    c3 = coda.linear_cross_entropy(x3, W_head, labels.view(B, S))
+    assert c3["lse"].shape == (B, S)
+    same(c3["lse"], c2["lse"], "lse")
+    same(c3["loss"], c2["loss"], "loss")
+
+    with pytest.raises(ValueError):
+        coda.linear_swiglu(y3.transpose(0, 1), t["Wg"], t["Wu"])
