@@ -51,6 +51,8 @@ __all__ = [
     "rmsnorm_linear_cross_entropy_fwd", "rmsnorm_linear_cross_entropy_bwd",
     "sigmoid", "linear_sigmoid_fwd", "linear_sigmoid_bwd",
     "E4M3_MAX", "quantize_fp8_rows", "linear_fp8_fwd", "swiglu_fp8_fwd",
+    "E2M1_MAX", "E2M1_GRID", "NVFP4_BLOCK", "e2m1_round", "e2m1_value", "quantize_nvfp4_rows",
+    "linear_nvfp4_fwd", "swiglu_nvfp4_fwd",
 ]
 
 
@@ -374,6 +376,92 @@ def swiglu_fp8_fwd(Xv, sx, Wgv, sg, Wuv, su, row_scale=None):
         A = A * np.asarray(row_scale, dtype=np.float64)[:, None]
     return swiglu_fwd(A, Wgv * np.asarray(sg, dtype=np.float64)[:, None],
                       Wuv * np.asarray(su, dtype=np.float64)[:, None])
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 operands: e2m1 elements, an e4m3 scale per 16 elements, fp32 row scale
+# ---------------------------------------------------------------------------
+# [P1] §1 and [P2] name FP4 beside FP8 as the formats that make the GEMMs
+# fast and the data movement around them dominant; the pages give no recipe.
+# Reading: NVIDIA's NVFP4 block format (4-bit e2m1 values, one e4m3 scale
+# per 16 consecutive elements along K), with the second-level fp32 scale
+# taken per row (token or output channel) as in the FP8 path.  Per row:
+#
+#   s      = amax(row) / (6 * 448)            (1 for an all-zero row)
+#   for each block of 16 elements along K, with bmax = max |x| over it:
+#   sf     = e4m3(bmax / (6 * s))             nearest even, saturating at 448
+#   code_k = e2m1(x_k / (sf * s))             nearest even, saturating at +-6;
+#            0 for the whole block when sf = 0
+#   x_k   ~= e2m1(code_k) * sf * s
+#
+# Each quotient and product is a single fp32 operation: the codes and scales
+# are integer decisions taken in the kernel's precision, so they must match
+# bit for bit.  A code of magnitude 0 carries no sign (-0 is written as +0).
+
+E2M1_MAX = 6.0
+# magnitudes of the e2m1 codes 0..7 (1 sign bit, 2 exponent bits with bias 1,
+# 1 mantissa bit; exponent 0 holds 0 and the subnormal 0.5)
+E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+NVFP4_BLOCK = 16
+_NVFP4_SCALE_DIV = np.float32(E2M1_MAX * E4M3_MAX)   # 2688
+
+
+def e2m1_round(v):
+    """Values -> e2m1 codes (uint8: bit 3 sign, bits 0-2 magnitude index):
+    the nearest grid magnitude, ties to the even index, |v| >= 6 -> 6."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    lo = np.clip(np.searchsorted(E2M1_GRID, a, side="right") - 1, 0, 7)
+    hi = np.minimum(lo + 1, 7)
+    d_lo = a - E2M1_GRID[lo]
+    d_hi = E2M1_GRID[hi] - a
+    up = (hi != lo) & ((d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0)))
+    idx = np.where(up, hi, lo).astype(np.uint8)
+    neg = (np.asarray(v) < 0) & (idx > 0)
+    return (idx | np.where(neg, 8, 0)).astype(np.uint8)
+
+
+def e2m1_value(codes):
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.where(c & 8, -1.0, 1.0) * E2M1_GRID[c & 7]
+
+
+def quantize_nvfp4_rows(X):
+    """Returns (codes uint8 [M, K], one e2m1 code per element; sf uint8
+    [M, K/16], e4m3 block-scale codes; s float32 [M]; values float64 [M, K] =
+    e2m1(code) * e4m3(sf), so that x ~= values * s).  K % 16 == 0."""
+    import torch
+    x32 = np.asarray(X, dtype=np.float32)
+    M, K = x32.shape
+    assert K % NVFP4_BLOCK == 0
+    nb = K // NVFP4_BLOCK
+    ax = np.abs(x32)
+    amax = ax.max(axis=1) if K else np.zeros(M, np.float32)
+    s = np.where(amax > 0, amax / _NVFP4_SCALE_DIV, np.float32(1.0)).astype(np.float32)
+    bmax = ax.reshape(M, nb, NVFP4_BLOCK).max(axis=2) if K else np.zeros((M, 0), np.float32)
+    t = (np.float32(E2M1_MAX) * s).astype(np.float32)
+    sf_f = np.minimum((bmax / t[:, None]).astype(np.float32), np.float32(E4M3_MAX))
+    sfq = torch.from_numpy(np.ascontiguousarray(sf_f)).to(torch.float8_e4m3fn)
+    sf = sfq.view(torch.uint8).numpy().copy()
+    sf_val = sfq.float().numpy()
+    denom = np.repeat((sf_val * s[:, None]).astype(np.float32), NVFP4_BLOCK, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = (x32 / denom).astype(np.float32)
+    zero_block = np.repeat(sf_val == 0, NVFP4_BLOCK, axis=1)
+    codes = np.where(zero_block, 0, e2m1_round(np.where(zero_block, 0, v))).astype(np.uint8)
+    values = e2m1_value(codes) * np.repeat(sf_val.astype(np.float64), NVFP4_BLOCK, axis=1)
+    return codes, sf, s, values
+
+
+def linear_nvfp4_fwd(Xv, sx, Wv, sw, R=None, row_scale=None):
+    """The plain linear on dequantised NVFP4 operands: y = R + rs_i *
+    (Xv_i sx_i) . (Wv_n sw_n), values from quantize_nvfp4_rows."""
+    return linear_fp8_fwd(Xv, sx, Wv, sw, R=R, row_scale=row_scale)
+
+
+def swiglu_nvfp4_fwd(Xv, sx, Wgv, sg, Wuv, su, row_scale=None):
+    """swiglu_fwd on dequantised NVFP4 operands (row factor r applied to g
+    and u before the gate).  Returns (H, g, u)."""
+    return swiglu_fp8_fwd(Xv, sx, Wgv, sg, Wuv, su, row_scale=row_scale)
 
 
 # ---------------------------------------------------------------------------

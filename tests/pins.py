@@ -505,7 +505,135 @@ def check_fp8_linear(o):
     return max(_rel(H, H0), _rel(g, g0), _rel(u, u0), _rel(y, X @ Wg.T))
 
 
+def _e2m1_decode_table():
+    """The 16 e2m1 codes decoded from the format's definition: bit 3 sign,
+    bits 1-2 exponent with bias 1, bit 0 mantissa; exponent 0 is subnormal
+    (mantissa x 0.5)."""
+    out = []
+    for c in range(16):
+        sgn = -1.0 if c & 8 else 1.0
+        e, m = (c >> 1) & 3, c & 1
+        out.append(sgn * (m * 0.5 if e == 0 else (1 + m / 2.0) * 2.0 ** (e - 1)))
+    return np.array(out)
+
+
+def _e2m1_nearest_even(v):
+    """Round to the e2m1 grid binade by binade: spacing 0.5 below 2, 1 in
+    [2, 4), 2 in [4, 6]; np.round rounds halves to even multiples, which
+    are the even codes; saturate at 6."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    sp = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))
+    return np.sign(v) * np.minimum(np.round(a / sp) * sp, 6.0)
+
+
+def check_e2m1(o):
+    """(1) the oracle's decode of every code equals the format definition;
+    (2) rounding equals the binade-wise nearest-even reference on random
+    values and on every tie point, with saturation at +-6 and no negative
+    zero codes."""
+    e = [_rel(o.e2m1_value(np.arange(16)), _e2m1_decode_table())]
+    r = RNG(30)
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    v = np.concatenate([r.uniform(-8, 8, 4000), ties, -ties, [0.0, 6.0, -6.0, 7.5, -1e9, 1e-9, -1e-9]])
+    v = v.astype(np.float32)
+    c = o.e2m1_round(v)
+    e.append(float(np.max(np.abs(o.e2m1_value(c) - _e2m1_nearest_even(v)))))
+    e.append(float(np.any((c & 7) == 0) and np.any(c[(c & 7) == 0] != 0)))
+    return max(e)
+
+
+def _nvfp4_exact_rows(r, rows, nblocks, row_pow2):
+    """Rows whose NVFP4 quantisation is exact: each block is grid magnitudes
+    (random signs, one entry at 6) times an e4m3 scale; block 0 carries
+    6 * 448 so s = 1, times 2^row_pow2[i] per row.  Returns (X, codes,
+    sf codes, s)."""
+    ecodes, evals = _e4m3_table()
+    pos = evals > 0
+    ecodes, evals = ecodes[pos], evals[pos]
+    grid = _e2m1_decode_table()[:8]
+    X = np.zeros((rows, nblocks * 16))
+    codes = np.zeros((rows, nblocks * 16), np.uint8)
+    sfc = np.zeros((rows, nblocks), np.uint8)
+    for i in range(rows):
+        for b in range(nblocks):
+            j = len(ecodes) - 1 if b == 0 else r.integers(0, len(ecodes))   # 448 in block 0
+            idx = r.integers(0, 8, 16)
+            idx[r.integers(0, 16)] = 7
+            sgn = np.where(r.random(16) < 0.5, 8, 0) * (idx > 0)
+            codes[i, b * 16:(b + 1) * 16] = idx | sgn
+            X[i, b * 16:(b + 1) * 16] = np.where(sgn, -1.0, 1.0) * grid[idx] * evals[j]
+            sfc[i, b] = ecodes[j]
+    X *= (2.0 ** np.asarray(row_pow2, dtype=np.float64))[:, None]
+    return X, codes, sfc, 2.0 ** np.asarray(row_pow2, dtype=np.float64)
+
+
+def check_nvfp4_quantizer(o):
+    """(1) rows built from grid values and e4m3 scales (s a power of two)
+    quantise to exactly those codes, scales and s; (2) s = amax / 2688;
+    every block scale is within half an e4m3 ulp of bmax / (6 s) (normal
+    range); the largest element of each such block gets magnitude code 7;
+    every element is within half a grid step of x / (sf s), times sf s;
+    (3) a zero row gives s = 1 and zero scales and codes; (4) a block whose
+    scale underflows e4m3 gets zero codes."""
+    r = RNG(31)
+    X, codes, sfc, s_exp = _nvfp4_exact_rows(r, 5, 6, [0, -6, 3, -20, 10])
+    c, sf, s, vals = o.quantize_nvfp4_rows(X)
+    e = [float(np.any(c != codes)), float(np.any(sf != sfc)), _rel(s, s_exp),
+         _rel(vals * s[:, None], X)]
+    Y = (r.standard_normal((6, 256)) * np.array([1e-3, 1, 30, 1e4, 0.5, 7])[:, None]).astype(np.float32)
+    Y[2, 16:32] *= 1e-3                                     # a quiet block among loud ones
+    c, sf, s, vals = o.quantize_nvfp4_rows(Y)
+    amax = np.abs(Y).max(axis=1)
+    q = amax.astype(np.float64) / 2688.0                     # s is this quotient rounded to fp32
+    e.append(0.0 if np.all(np.abs(s - q) <= 2.0 ** -24 * q) else 1.0)
+    ecodes, evals = _e4m3_table()
+    lut = np.zeros(256)
+    lut[ecodes] = evals
+    sfv = lut[sf]
+    bmax = np.abs(Y.astype(np.float64)).reshape(6, 16, 16).max(axis=2)
+    target = bmax / (6.0 * s.astype(np.float64)[:, None])
+    normal = target >= 2.0 ** -6
+    e.append(0.0 if np.all(np.abs(sfv - target)[normal] <= 2.0 ** -4 * target[normal] * (1 + 1e-6)) else 1.0)
+    mag = (c & 7).reshape(6, 16, 16)
+    arg = np.abs(Y).reshape(6, 16, 16).argmax(axis=2)
+    top = np.take_along_axis(mag, arg[..., None], axis=2)[..., 0]
+    e.append(float(np.any(top[normal] != 7)))
+    denom = np.repeat(sfv * s.astype(np.float64)[:, None], 16, axis=1)
+    ok = denom > 0
+    v = np.abs(Y.astype(np.float64))[ok] / denom[ok]
+    half = np.where(v < 2, 0.25, np.where(v < 4, 0.5, 1.0))
+    err = np.abs(vals * s[:, None] - Y)[ok]
+    e.append(0.0 if np.all(err <= denom[ok] * np.maximum(half, v - 6.0) * (1 + 1e-6)) else 1.0)
+    c0, sf0, s0, v0 = o.quantize_nvfp4_rows(np.zeros((1, 32)))
+    e.append(float(np.any(c0) or np.any(sf0) or np.any(v0)) + abs(float(s0[0]) - 1.0))
+    Z = np.zeros((1, 32), np.float32)
+    Z[0, 0] = 2688.0
+    Z[0, 16:] = 1e-7                                        # 1e-7 / 6 far below e4m3's 2^-9
+    cz, sfz, _, _ = o.quantize_nvfp4_rows(Z)
+    e.append(float(sfz[0, 1] != 0 or np.any(cz[0, 16:])))
+    return max(e)
+
+
+def check_nvfp4_linear(o):
+    """With exactly representable operands, the NVFP4 linear and SwiGLU
+    equal the bf16 definitions exactly."""
+    r = RNG(32)
+    X, *_ = _nvfp4_exact_rows(r, 4, 2, [-10, -13, -8, -18])
+    Wg, *_ = _nvfp4_exact_rows(r, 5, 2, [-11, -10, -12, -11, -13])
+    Wu, *_ = _nvfp4_exact_rows(r, 5, 2, [-12, -11, -10, -12, -11])
+    _, _, sx, xv = o.quantize_nvfp4_rows(X)
+    _, _, sg, gv = o.quantize_nvfp4_rows(Wg)
+    _, _, su, uv = o.quantize_nvfp4_rows(Wu)
+    H, g, u = o.swiglu_nvfp4_fwd(xv, sx, gv, sg, uv, su)
+    H0, g0, u0 = o.swiglu_fwd(X, Wg, Wu)
+    y = o.linear_nvfp4_fwd(xv, sx, gv, sg)
+    return max(_rel(H, H0), _rel(g, g0), _rel(u, u0), _rel(y, X @ Wg.T))
+
+
 ALL_CHECKS = {
+    "e2m1": (check_e2m1, 0.0),
+    "nvfp4_quantizer": (check_nvfp4_quantizer, 1e-12),
+    "nvfp4_linear": (check_nvfp4_linear, 1e-14),
     "fp8_quantizer": (check_fp8_quantizer, 1e-12),
     "fp8_linear": (check_fp8_linear, 1e-14),
     "linear_sigmoid": (check_linear_sigmoid, 1e-7),

@@ -172,7 +172,21 @@ def _mut_fp8_truncate(m):
     m.quantize_fp8_rows = bad
 
 
+def _source_mutant(old, new):
+    """A mutant that re-executes the oracle's source with one phrase replaced."""
+    def apply(m):
+        src = open(ORACLE_SRC).read()
+        assert src.count(old) == 1, old
+        exec(compile(src.replace(old, new), ORACLE_SRC, "exec"), m.__dict__)
+    return apply
+
+
 MUTANTS = {
+    "e2m1_ties_away_from_zero": _source_mutant("((d_hi == d_lo) & (hi % 2 == 0))", "(d_hi == d_lo)"),
+    "nvfp4_block_scale_from_row_max": _source_mutant("ax.reshape(M, nb, NVFP4_BLOCK).max(axis=2)",
+                                                     "np.repeat(amax[:, None], nb, axis=1)"),
+    "nvfp4_codes_without_row_scale": _source_mutant("(sf_val * s[:, None]).astype(np.float32)",
+                                                    "sf_val.astype(np.float32)"),
     "fp8_truncates": _mut_fp8_truncate,
     "sigmoid_bwd_missing_derivative": _mut_sigmoid_bwd_missing_factor,
     "rmsnorm_ce_skips_norm_backward": _mut_rmsnorm_ce_skip_norm_bwd,
