@@ -26,7 +26,8 @@ __all__ = [
     "linear_swiglu", "linear_swiglu_bwd", "linear_qknorm_rope", "linear_qknorm_rope_bwd",
     "linear_cross_entropy", "linear_cross_entropy_bwd", "linear_cross_entropy_noalloc", "workspace",
     "rmsnorm_linear_cross_entropy", "rmsnorm_linear_cross_entropy_bwd", "rms_rstd",
-    "linear_sigmoid", "linear_sigmoid_bwd", "quantize_fp8_rows", "linear_fp8", "linear_swiglu_fp8",
+    "linear_sigmoid", "linear_sigmoid_bwd", "quantize_fp8_rows", "linear_fp8", "linear_swiglu_fp8", "quantize_nvfp4_rows", "linear_nvfp4",
+    "linear_swiglu_nvfp4",
     "MAP_NONE", "MAP_SWIGLU", "MAP_DSWIGLU", "MAP_QKNORM_ROPE", "MAP_CE_LSE",
     "MAP_CE_DLOGITS", "MAP_COLDOT", "MAP_SIGMOID", "MAP_DSIGMOID", "K_MAJOR", "MN_MAJOR",
 ]
@@ -81,6 +82,12 @@ _SIGS = {
     "coda_linear_fp8": ([_P] * 6 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_swiglu_fp8_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_swiglu_fp8": ([_P] * 10 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_nvfp4_scale_bytes": ([_I64, _I64], _SZ),
+    "coda_quantize_nvfp4_rows": ([_P, _I64, _I64, _I64, _P, _P, _P, _P], ctypes.c_int),
+    "coda_linear_nvfp4_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_nvfp4": ([_P] * 8 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_swiglu_nvfp4_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_swiglu_nvfp4": ([_P] * 13 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_sigmoid_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_sigmoid": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_sigmoid_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
@@ -521,6 +528,53 @@ def linear_swiglu_fp8(Xq, sx, Wgq, sg, Wuq, su, rstd=None, save=True, H=None, g=
     _check("coda_linear_swiglu_fp8", lib.coda_linear_swiglu_fp8(
         _u8(Xq, "Xq"), _f32(sx, "sx"), _f32(rstd, "rstd"), _u8(Wgq, "Wgq"), _f32(sg, "sg"), _u8(Wuq, "Wuq"),
         _f32(su, "su"), _bf(H, "H"), _bf(g, "g"), _bf(u, "u"), M, I, K, _ptr(ws), ws.numel(), _stream(stream)))
+    return H, g, u
+
+
+def quantize_nvfp4_rows(X, stream=None):
+    """Per-row NVFP4 quantisation (coda_quantize_nvfp4_rows): returns (codes
+    uint8 [M, K/2], two e2m1 codes per byte; block scales uint8 in the
+    tensor-core order of include/coda.h; row scales fp32 [M])."""
+    lib = load()
+    M, K = X.shape
+    dev = X.device
+    Xq = torch.empty(M, K // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(max(lib.coda_nvfp4_scale_bytes(M, K), 16), dtype=torch.uint8, device=dev)
+    scale = torch.empty(M, dtype=torch.float32, device=dev)
+    _check("coda_quantize_nvfp4_rows", lib.coda_quantize_nvfp4_rows(
+        _bf(X, "X"), X.stride(0), M, K, _u8(Xq, "Xq"), _u8(sf, "sf"), _f32(scale, "scale"), _stream(stream)))
+    return Xq, sf, scale
+
+
+def linear_nvfp4(Xq, sfx, sx, Wq, sfw, sw, R=None, Y=None, ws=None, stream=None):
+    """Y = R + X̂ Ŵᵀ on NVFP4 operands (coda_linear_nvfp4)."""
+    lib = load()
+    M, K = Xq.shape[0], 2 * Xq.shape[1]
+    N = Wq.shape[0]
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=Xq.device) if Y is None else Y
+    ws = _ws(ws, lib.coda_linear_nvfp4_workspace_size(M, N, K), Xq.device)
+    _check("coda_linear_nvfp4", lib.coda_linear_nvfp4(
+        _u8(Xq, "Xq"), _u8(sfx, "sfx"), _f32(sx, "sx"), _u8(Wq, "Wq"), _u8(sfw, "sfw"), _f32(sw, "sw"),
+        _bf(R, "R"), _bf(Y, "Y"), M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
+    return Y
+
+
+def linear_swiglu_nvfp4(Xq, sfx, sx, Wgq, sfg, sg, Wuq, sfu, su, rstd=None, save=True, H=None, g=None, u=None,
+                        ws=None, stream=None):
+    """SwiGLU gate/up projection on NVFP4 operands (coda_linear_swiglu_nvfp4)."""
+    lib = load()
+    M, K = Xq.shape[0], 2 * Xq.shape[1]
+    I = Wgq.shape[0]
+    dev = Xq.device
+    H = torch.empty(M, I, dtype=torch.bfloat16, device=dev) if H is None else H
+    if save:
+        g = torch.empty(M, I, dtype=torch.bfloat16, device=dev) if g is None else g
+        u = torch.empty(M, I, dtype=torch.bfloat16, device=dev) if u is None else u
+    ws = _ws(ws, lib.coda_linear_swiglu_nvfp4_workspace_size(M, I, K), dev)
+    _check("coda_linear_swiglu_nvfp4", lib.coda_linear_swiglu_nvfp4(
+        _u8(Xq, "Xq"), _u8(sfx, "sfx"), _f32(sx, "sx"), _f32(rstd, "rstd"), _u8(Wgq, "Wgq"), _u8(sfg, "sfg"),
+        _f32(sg, "sg"), _u8(Wuq, "Wuq"), _u8(sfu, "sfu"), _f32(su, "su"), _bf(H, "H"), _bf(g, "g"), _bf(u, "u"),
+        M, I, K, _ptr(ws), ws.numel(), _stream(stream)))
     return H, g, u
 
 

@@ -1299,6 +1299,47 @@ static int ce_forward(const coda_bf16* X, const coda_bf16* W, const int32_t* lab
   return CODA_OK;
 }
 
+// One NVFP4 GEMM launch: single CTAs, 128 x 256 tiles (b_dual: 128 gate +
+// 128 up columns), k-slices of 256 elements.
+int run_nvfp4(coda::EpiKind kind, const uint8_t* A, const uint8_t* B0, const uint8_t* B1, coda::Nvfp4Scales sc,
+              int64_t M, int64_t N, int64_t K, int b_dual, const EpiArgs& e, int* status, cudaStream_t s) {
+  if (M == 0 || N == 0) return CODA_OK;
+  if (!get_encoder()) return CODA_ERR_CUDA;
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  CUtensorMap maps[3];
+  std::memset(maps, 0, sizeof(maps));
+  const int64_t kb = K / 2;  // bytes of codes per row
+  if (!encode_map(&maps[0], A, M, kb, kb, 128, coda::BM, 1)) return CODA_ERR_CUDA;
+  if (b_dual) {
+    if (!encode_map(&maps[1], B0, N, kb, kb, 128, BN / 2, 1)) return CODA_ERR_CUDA;
+    if (!encode_map(&maps[2], B1, N, kb, kb, 128, BN / 2, 1)) return CODA_ERR_CUDA;
+  } else {
+    if (!encode_map(&maps[1], B0, N, kb, kb, 128, BN, 1)) return CODA_ERR_CUDA;
+    maps[2] = maps[1];
+  }
+  GemmArgs a{};
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.num_m = static_cast<int>(cdiv(M, coda::BM));
+  a.num_n = static_cast<int>(cdiv(N, b_dual ? BN / 2 : BN));
+  a.kb0 = static_cast<int>(cdiv(K, 256));
+  a.b_dual = b_dual;
+  a.n_per_unit = 1;
+  a.num_units = a.num_m * a.num_n;
+  a.group_m = group_m(1);
+  a.idesc = coda::nvfp4_idesc();
+  a.status = status;
+  a.timeout_ns = TIMEOUT_NS;
+  wait_sleep(a.producer_sleep_ns, a.epilogue_sleep_ns);
+  a.e = e;
+  a.e.st_stream = (l2_hints() & 4) ? 1 : 0;
+  sc.kt = cdiv(K, 256);
+  cudaError_t err = kind == coda::EpiKind::Swiglu ? coda::launch_gemm_swiglu_nvfp4(a.num_units, sms, s, maps, a, sc)
+                                                  : coda::launch_gemm_plain_nvfp4(a.num_units, sms, s, maps, a, sc);
+  return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
+}
+
 extern "C" {
 
 int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int32_t* labels, int32_t ignore_index,
@@ -1740,6 +1781,87 @@ int coda_linear_swiglu_fp8(const uint8_t* Xq, const float* sx, const float* rstd
   p.e.out2 = BF(u_save);
   p.e.ld_out2 = I;
   return run(p, static_cast<int*>(ws), S(stream));
+}
+
+// ------------------------------------------------------------------ NVFP4 operands
+size_t coda_nvfp4_scale_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0) return 0;
+  return static_cast<size_t>(cdiv(rows, 256) * 2 * cdiv(K, 256) * 2048);
+}
+
+int coda_quantize_nvfp4_rows(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq, uint8_t* sf,
+                             float* scale, coda_stream stream) {
+  if (M < 0 || K < 0) return CODA_ERR_INVALID_ARG;
+  if (K % 32) return CODA_ERR_UNSUPPORTED;  // 16-byte rows of packed codes for the tensor maps
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)X, (const void*)Xq, (const void*)sf, (const void*)scale}) CK(req(q));
+  CK(al(X));
+  CK(al(Xq));
+  CK(al(sf));
+  CK(ldok(ldx, K));
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  CU(coda::launch_quantize_nvfp4_rows(BF(X), ldx, M, K, Xq, sf, scale, sms, S(stream)));
+  return CODA_OK;
+}
+
+size_t coda_linear_nvfp4_workspace_size(int64_t, int64_t, int64_t) { return WS_HEADER; }
+
+int coda_linear_nvfp4(const uint8_t* Xq, const uint8_t* sfx, const float* sx, const uint8_t* Wq, const uint8_t* sfw,
+                      const float* sw, const coda_bf16* R, coda_bf16* Y, int64_t M, int64_t N, int64_t K, void* ws,
+                      size_t ws_bytes, coda_stream stream) {
+  CK(dims_ok(M, N, K));
+  if (K % 32) return CODA_ERR_UNSUPPORTED;
+  CK(ws_ok(ws, ws_bytes, WS_HEADER));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)Xq, (const void*)sfx, (const void*)sx, (const void*)Wq, (const void*)sfw,
+                        (const void*)sw, (const void*)Y})
+    CK(req(q));
+  for (const void* q : {(const void*)Xq, (const void*)sfx, (const void*)Wq, (const void*)sfw, (const void*)R,
+                        (const void*)Y})
+    CK(al(q));
+  EpiArgs e{};
+  e.D = Y;
+  e.ldd = N;
+  e.row_scale = sx;
+  e.col_scale = sw;
+  e.aux0 = BF(R);
+  e.ld_aux0 = N;
+  coda::Nvfp4Scales sc{sfx, sfw, sfw, 0};
+  return run_nvfp4(coda::EpiKind::Plain, Xq, Wq, Wq, sc, M, N, K, 0, e, static_cast<int*>(ws), S(stream));
+}
+
+size_t coda_linear_swiglu_nvfp4_workspace_size(int64_t, int64_t, int64_t) { return WS_HEADER; }
+
+int coda_linear_swiglu_nvfp4(const uint8_t* Xq, const uint8_t* sfx, const float* sx, const float* rstd,
+                             const uint8_t* Wgq, const uint8_t* sfg, const float* sg, const uint8_t* Wuq,
+                             const uint8_t* sfu, const float* su, coda_bf16* H, coda_bf16* g_save,
+                             coda_bf16* u_save, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
+                             coda_stream stream) {
+  CK(dims_ok(M, I, K));
+  if (K % 32) return CODA_ERR_UNSUPPORTED;
+  CK(ws_ok(ws, ws_bytes, WS_HEADER));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)Xq, (const void*)sfx, (const void*)sx, (const void*)Wgq, (const void*)sfg,
+                        (const void*)sg, (const void*)Wuq, (const void*)sfu, (const void*)su, (const void*)H})
+    CK(req(q));
+  for (const void* q : {(const void*)Xq, (const void*)sfx, (const void*)Wgq, (const void*)sfg, (const void*)Wuq,
+                        (const void*)sfu, (const void*)sg, (const void*)su, (const void*)H, (const void*)g_save,
+                        (const void*)u_save})
+    CK(al(q));
+  EpiArgs e{};
+  e.D = H;
+  e.ldd = I;
+  e.row_scale = sx;
+  e.row_scale2 = rstd;
+  e.col_scale = sg;
+  e.col_scale2 = su;
+  e.out1 = BF(g_save);
+  e.ld_out1 = I;
+  e.out2 = BF(u_save);
+  e.ld_out2 = I;
+  coda::Nvfp4Scales sc{sfx, sfg, sfu, 0};
+  return run_nvfp4(coda::EpiKind::Swiglu, Xq, Wgq, Wuq, sc, M, I, K, 1, e, static_cast<int*>(ws), S(stream));
 }
 
 }  // extern "C"

@@ -38,6 +38,23 @@ cudaError_t launch_gemm_rmsdx(int num_units, int sms, int cg, cudaStream_t s, co
 cudaError_t launch_gemm_coldot(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
 
+// NVFP4 operands (coda_nvfp4.cu): e2m1 codes in tensor maps m[0] (A), m[1]
+// (B, or the gate half when a.b_dual), m[2] (the up half); the e4m3 block
+// scales in the tensor-core order described there.
+struct Nvfp4Scales {
+  const uint8_t* a;   // A's block scales
+  const uint8_t* b0;  // B's (gate weight's) block scales
+  const uint8_t* b1;  // up weight's block scales (b_dual)
+  int64_t kt;         // k tiles of 256 elements
+};
+uint32_t nvfp4_idesc();
+cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Q,
+                                       uint8_t* SF, float* scale, int num_sms, cudaStream_t s);
+cudaError_t launch_gemm_plain_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a,
+                                    const Nvfp4Scales& sc);
+cudaError_t launch_gemm_swiglu_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
+                                     const GemmArgs& a, const Nvfp4Scales& sc);
+
 // auxiliary kernels (coda_aux.cu)
 cudaError_t launch_fold_gamma(const __nv_bfloat16* W, const float* gamma, __nv_bfloat16* Wf, int64_t N, int64_t K,
                               int num_sms, cudaStream_t s);

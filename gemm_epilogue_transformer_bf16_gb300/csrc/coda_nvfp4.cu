@@ -1,0 +1,423 @@
+// NVFP4 operands: 4-bit e2m1 elements with one e4m3 scale per 16 elements
+// along K and an fp32 scale per row, and the persistent GEMM that consumes
+// them with tcgen05.mma kind::mxf4nvf4 (block-scaled, scale vector 4X).
+//
+// "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs" (§1) and
+// the news flash on it name FP4 beside FP8 as the formats that make the
+// matrix multiplications fast and the data movement around them dominant;
+// the epilogues are the ones of the bf16 and e4m3 kernels.
+//
+// Quantised operand layout (what coda_quantize_nvfp4_rows writes):
+//   codes  [rows, K/2] bytes: element 2j in the low nibble of byte j, 2j+1 in
+//          the high nibble (e2m1: bit 3 sign, bits 0-2 magnitude index);
+//   scale  [rows] fp32: s = amax(row) / (6 * 448), 1 for a zero row;
+//   sf     e4m3 block scales in the order the tensor core reads them: rows in
+//          blocks of 128, K in tiles of 256 elements (16 scales per row);
+//          the 2 KB of one (row block, k tile) are contiguous, four 512-byte
+//          groups of 64 elements, each holding row r's 4 scales at byte
+//          (r % 32) * 16 + ((r % 128) / 32) * 4.  Rows are padded to a
+//          multiple of 256 and K to a multiple of 256 with zero scales.
+//
+// GEMM structure: the single-CTA form of the bf16 kernel (warp 0 TMA
+// producer, warp 1 TMEM owner and MMA issuer, warps 2-5 epilogue), M = 128,
+// N = 256, k-slices of 256 elements (128 bytes of codes per row, the same
+// 128-byte swizzled rows), four stages.  Per stage the producer also copies
+// the k-slice's block scales (2 KB for A, 4 KB for B) to shared memory;
+// the MMA thread moves them into TMEM with tcgen05.cp (32 lanes x 128 bits,
+// replicated to the four lane quarters) before the four MMAs (K = 64 each)
+// that read them.  TMEM: the accumulator in columns 0-255 and, per stage,
+// 64 columns of scales (A at +0, B at +16); one accumulator, so the
+// epilogue of a tile does not overlap the next tile's mainloop.
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+
+#include "coda_epilogues.cuh"
+#include "coda_internal.h"
+
+namespace coda {
+
+namespace {
+
+constexpr int F4_BN = 256;
+constexpr int F4_STAGES = 4;
+constexpr uint32_t F4_A_BYTES = BM * 128;
+constexpr uint32_t F4_B_BYTES = F4_BN * 128;
+constexpr uint32_t F4_SFA_BYTES = 2048;
+constexpr uint32_t F4_SFB_BYTES = 4096;
+constexpr uint32_t F4_STAGE_BYTES = F4_A_BYTES + F4_B_BYTES + F4_SFA_BYTES + F4_SFB_BYTES;
+constexpr uint32_t F4_BAR_BYTES = 256;
+constexpr uint32_t F4_EPI_BYTES = 4 * 2048;
+constexpr uint32_t F4_SMEM = 1024 + F4_STAGES * F4_STAGE_BYTES + F4_BAR_BYTES + F4_EPI_BYTES;
+constexpr uint32_t F4_TMEM_COLS = 512;
+constexpr uint32_t F4_SF_COL0 = 256;     // first TMEM column of the scale slots
+constexpr uint32_t F4_SF_SLOT_COLS = 64;
+static_assert(F4_STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
+static_assert(F4_SMEM <= 232448, "shared memory per CTA");
+static_assert(F4_SF_COL0 + F4_STAGES * F4_SF_SLOT_COLS <= F4_TMEM_COLS, "TMEM columns");
+
+// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of
+// 16), completion counted in bytes on `bar`; issued when p != 0.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %3, 0;\n\t"
+      "@P cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%4];\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(p), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory descriptor without swizzling: 8-row x 16-byte core
+// matrices, `sbo` bytes between consecutive 8-row groups.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;  // layout type 0 (no swizzle) at bits 61-63
+}
+
+// 32 rows x 128 bits from shared memory into TMEM lanes 0-31, replicated to
+// the four 32-lane quarters (4 columns).
+__device__ __forceinline__ void tmem_cp_32x128_x4(uint32_t taddr, uint64_t sdesc, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %2, 0;\n\t"
+      "@P tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(sdesc), "r"(p)
+      : "memory");
+}
+
+// D[tmem] (+)= (A . sfA) * (B . sfB)^T: e2m1 operands, e4m3 scale per 16
+// elements (scale vector 4X), K = 64 per instruction, fp32 accumulator.
+__device__ __forceinline__ void umma_nvfp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate,
+                                           uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred A, P;\n\t"
+      "setp.ne.b32 A, %6, 0;\n\t"
+      "setp.ne.b32 P, %7, 0;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], A;\n\t}" ::
+          "r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(p)
+      : "memory");
+}
+
+// Instruction descriptor of the block-scaled kinds: B scale-factor id 0
+// (bits 4-5), A and B e2m1 (type 1 at bits 7-9 and 10-12), K-major, N>>3 at
+// bits 17-22, scale type e4m3 (bit 23 = 0), M>>4 at bits 24-28, A
+// scale-factor id 0 (bits 29-30), K = 64 (bit 31 = 0).
+constexpr uint32_t idesc_nvfp4(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// e4m3 code -> value (1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
+// exponent 0 subnormal); scale codes are never NaN (<= 448 by construction).
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  const float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0.001953125f;
+  return (b & 0x80u) ? -v : v;
+}
+
+__device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t j, int64_t kt_count) {
+  return ((r >> 7) * kt_count + (j >> 4)) * 2048 + ((j >> 2) & 3) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 +
+         (j & 3);
+}
+
+// One warp per row (rows up to the padded count; padding rows only write
+// zero scales).  Pass 1: the row's amax.  Pass 2, lane per 16-element block:
+// the block's e4m3 scale and sixteen e2m1 codes.
+__global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx,
+                                                                  int64_t M, int64_t K, uint8_t* __restrict__ Q,
+                                                                  uint8_t* __restrict__ SF,
+                                                                  float* __restrict__ scale, int64_t rows_pad,
+                                                                  int64_t kt_count) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t nb = K / 16, nb_pad = kt_count * 16;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows_pad;
+       r += warps) {
+    if (r >= M) {
+      for (int64_t j = lane; j < nb_pad; j += 32) SF[sf_offset(r, j, kt_count)] = 0;
+      continue;
+    }
+    const __nv_bfloat16* row = X + r * ldx;
+    float amax = 0.f;
+    for (int64_t j = lane; j < nb; j += 32) {
+      const uint4* p = reinterpret_cast<const uint4*>(row + j * 16);
+      const uint4 w[2] = {p[0], p[1]};
+      const uint32_t* u = reinterpret_cast<const uint32_t*>(w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[i])), fabsf(bf16_hi(u[i]))));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+    if (lane == 0) scale[r] = s;
+    const float t = __fmul_rn(6.0f, s);
+    for (int64_t j = lane; j < nb_pad; j += 32) {
+      uint32_t sfb = 0;
+      if (j < nb) {
+        const uint4* p = reinterpret_cast<const uint4*>(row + j * 16);
+        const uint4 w[2] = {p[0], p[1]};
+        const uint32_t* u = reinterpret_cast<const uint32_t*>(w);
+        float x[16];
+        float bmax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          x[2 * i] = bf16_lo(u[i]);
+          x[2 * i + 1] = bf16_hi(u[i]);
+          bmax = fmaxf(bmax, fmaxf(fabsf(x[2 * i]), fabsf(x[2 * i + 1])));
+        }
+        const float sf_f = fminf(__fdiv_rn(bmax, t), 448.0f);
+        sfb = __nv_cvt_float_to_fp8(sf_f, __NV_SATFINITE, __NV_E4M3);
+        const float denom = __fmul_rn(e4m3_value(sfb), s);
+        uint32_t lo = 0, hi = 0;
+        if (denom > 0.f) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            uint32_t c = __nv_cvt_float_to_fp4(__fdiv_rn(x[i], denom), __NV_E2M1, cudaRoundNearest) & 0xFu;
+            if ((c & 7u) == 0) c = 0;  // no negative zero
+            if (i < 8)
+              lo |= c << (4 * i);
+            else
+              hi |= c << (4 * (i - 8));
+          }
+        }
+        *reinterpret_cast<uint2*>(Q + r * (K / 2) + j * 8) = make_uint2(lo, hi);
+      }
+      SF[sf_offset(r, j, kt_count)] = static_cast<uint8_t>(sfb);
+    }
+  }
+}
+
+template <class Epi>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    coda_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
+                           const __grid_constant__ CUtensorMap mB1, const GemmArgs args, const Nvfp4Scales sc) {
+  constexpr int S = F4_STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * F4_STAGE_BYTES);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* epi_stage = smem + S * F4_STAGE_BYTES + F4_BAR_BYTES;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mA);
+    tma_prefetch_desc(&mB0);
+    if (args.b_dual) tma_prefetch_desc(&mB1);
+  }
+  if (warp == 1) {
+    tmem_alloc<false>(tmem_slot, F4_TMEM_COLS);
+    tmem_relinquish<false>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_kb = args.kb0;
+  const int cluster_id = static_cast<int>(blockIdx.x);
+  const int num_clusters = static_cast<int>(gridDim.x);
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint32_t el = elect_one();
+    uint32_t it = 0;
+    for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters) {
+      int mb, nb, nlen, chunk;
+      unit_coords(args, u, mb, nb, nlen, chunk);
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % S;
+        if (!mbar_wait_bounded(&empty[s], ((it / S) & 1) ^ 1, abort_flag, args.status, args.timeout_ns,
+                               args.producer_sleep_ns)) {
+          aborted = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], F4_STAGE_BYTES, el);
+        uint8_t* sa = tiles + s * F4_STAGE_BYTES;
+        uint8_t* sb = sa + F4_A_BYTES;
+        uint8_t* sfa = sb + F4_B_BYTES;
+        uint8_t* sfb = sfa + F4_SFA_BYTES;
+        const int x = kb * 128;  // bytes of codes = 256 elements
+        tma_load_2d(sa, &mA, &full[s], x, mb * BM, el);
+        bulk_load(sfa, sc.a + (static_cast<int64_t>(mb) * sc.kt + kb) * 2048, 2048, &full[s], el);
+        if (args.b_dual) {
+          // N = [128 gate rows | 128 up rows]: row block nb of each weight
+          tma_load_2d(sb, &mB0, &full[s], x, nb * (F4_BN / 2), el);
+          tma_load_2d(sb + (F4_BN / 2) * 128, &mB1, &full[s], x, nb * (F4_BN / 2), el);
+          bulk_load(sfb, sc.b0 + (static_cast<int64_t>(nb) * sc.kt + kb) * 2048, 2048, &full[s], el);
+          bulk_load(sfb + 2048, sc.b1 + (static_cast<int64_t>(nb) * sc.kt + kb) * 2048, 2048, &full[s], el);
+        } else {
+          // row blocks 2nb and 2nb + 1 (scale rows are padded to 256)
+          tma_load_2d(sb, &mB0, &full[s], x, nb * F4_BN, el);
+          bulk_load(sfb, sc.b0 + (static_cast<int64_t>(2 * nb) * sc.kt + kb) * 2048, 2048, &full[s], el);
+          bulk_load(sfb + 2048, sc.b0 + (static_cast<int64_t>(2 * nb + 1) * sc.kt + kb) * 2048, 2048, &full[s],
+                    el);
+        }
+      }
+    }
+    if (aborted) {
+      const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
+      for (uint32_t j = first; j < it; ++j) mbar_wait_drain(&full[j % S], (j / S) & 1, 200000000ull);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ scale copies + MMA issuer
+    const uint32_t el = elect_one();
+    uint32_t it = 0, t = 0;
+    bool issued = false;
+    const uint32_t idesc = args.idesc;
+    for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters, ++t) {
+      if (!mbar_wait_bounded(tempty, (t & 1) ^ 1, abort_flag, args.status, args.timeout_ns)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % S;
+        if (!mbar_wait_bounded(&full[s], (it / S) & 1, abort_flag, args.status, args.timeout_ns)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(tiles + s * F4_STAGE_BYTES);
+        const uint32_t sb = sa + F4_A_BYTES;
+        const uint32_t sfa = sb + F4_B_BYTES;
+        const uint32_t sfb = sfa + F4_SFA_BYTES;
+        const uint32_t slot = tmem_base + F4_SF_COL0 + static_cast<uint32_t>(s) * F4_SF_SLOT_COLS;
+        // A: one 512-byte group per 64-element step -> 4 columns each;
+        // B: two 128-row halves per step -> 8 columns each (rows 0-127, then 128-255)
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          tmem_cp_32x128_x4(slot + g * 4, sdesc_plain(sfa + g * 512, 128, 128), el);
+          tmem_cp_32x128_x4(slot + 16 + g * 8, sdesc_plain(sfb + g * 512, 128, 128), el);
+          tmem_cp_32x128_x4(slot + 16 + g * 8 + 4, sdesc_plain(sfb + 2048 + g * 512, 128, 128), el);
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          // 64 e2m1 elements = 32 bytes of each 128-byte swizzled row
+          const uint64_t ad = sdesc_sw128(sa + g * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sb + g * 32, 16, 1024);
+          umma_nvfp4(tmem_base, ad, bd, idesc, slot + g * 4, slot + 16 + g * 8, (kb | g) != 0, el);
+        }
+        issued = true;
+        umma_commit(&empty[s], el);
+      }
+      if (aborted) break;
+      umma_commit(tfull, el);
+    }
+    if (aborted && issued) {
+      umma_commit(drain, el);
+      mbar_wait_drain(drain, 0, 200000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    uint32_t t = 0;
+    for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters, ++t) {
+      int mb, nb, nlen, chunk;
+      unit_coords(args, u, mb, nb, nlen, chunk);
+      TileInfo ti;
+      ti.mb = mb;
+      ti.unit_chunk = chunk;
+      ti.row = mb * BM + q * 32 + lane;
+      ti.M = args.M;
+      ti.N = args.N;
+      ti.status = args.status;
+      ti.stage = epi_stage + q * 2048;
+      typename Epi::State st;
+      Epi::begin(st, args.e, ti);
+      if (!mbar_wait_bounded(tfull, t & 1, abort_flag, args.status, args.timeout_ns, args.epilogue_sleep_ns)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      __syncwarp();
+      ti.nb = nb;
+      ti.taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      Epi::tile(st, args.e, ti);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+      Epi::end(st, args.e, ti);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc<false>(tmem_base, F4_TMEM_COLS);
+  }
+}
+
+template <class Epi>
+cudaError_t launch_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a,
+                         const Nvfp4Scales& sc) {
+  static std::mutex init;
+  static std::atomic<bool> attr_done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  auto kern = coda_gemm_nvfp4_kernel<Epi>;
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(init);
+    if (!attr_done[dev].load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(F4_SMEM));
+      if (e != cudaSuccess) return e;
+      attr_done[dev].store(true, std::memory_order_release);
+    }
+  }
+  const int grid = std::min(num_units, sms);
+  kern<<<grid, NUM_THREADS, F4_SMEM, s>>>(m[0], m[1], m[2], a, sc);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+uint32_t nvfp4_idesc() { return idesc_nvfp4(BM, F4_BN); }
+
+cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Q,
+                                       uint8_t* SF, float* scale, int num_sms, cudaStream_t s) {
+  const int64_t rows_pad = (M + 255) / 256 * 256;
+  const int64_t kt = (K + 255) / 256;
+  const int64_t blocks = std::min<int64_t>((rows_pad + 7) / 8, static_cast<int64_t>(num_sms) * 8);
+  quantize_nvfp4_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(
+      X, ldx, M, K, Q, SF, scale, rows_pad, kt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_plain_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a,
+                                    const Nvfp4Scales& sc) {
+  return launch_nvfp4<EpiPlain<256>>(num_units, sms, s, m, a, sc);
+}
+cudaError_t launch_gemm_swiglu_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
+                                     const GemmArgs& a, const Nvfp4Scales& sc) {
+  return launch_nvfp4<EpiSwiglu<256>>(num_units, sms, s, m, a, sc);
+}
+
+}  // namespace coda

@@ -425,6 +425,55 @@ int coda_linear_swiglu_fp8(const uint8_t* Xq, const float* sx, const float* rstd
                            coda_stream stream);
 
 /* ------------------------------------------------------------------------
+ * NVFP4 operands: 4-bit e2m1 elements, one e4m3 scale per 16 consecutive
+ * elements along K, an fp32 scale per row; the GEMM runs on tcgen05.mma
+ * kind::mxf4nvf4 (block-scaled) with the same epilogues.  The pages name
+ * FP4 beside FP8 as the formats that make the GEMMs fast and the data
+ * movement around them dominant ("CODA: Rewriting Transformer Blocks as
+ * GEMM-Epilogue Programs", §1; the news flash on it) and give no recipe:
+ * this is NVIDIA's NVFP4 block format with the second-level scale per row.
+ *
+ * Quantisation of row x (each step one fp32 operation):
+ *   s = amax(x) / 2688 (= 6 * 448; 1 for a zero row);
+ *   per block of 16: sf = e4m3(bmax / (6 s)), nearest even, <= 448;
+ *   code = e2m1(x / (sf s)), nearest even, saturating at +-6; 0 when sf = 0;
+ *   x ~= e2m1(code) * sf * s.
+ * Layouts:
+ *   Xq     [rows, K/2] bytes, contiguous: element 2j in the low nibble of byte
+ *          j, 2j+1 in the high nibble; e2m1 = bit 3 sign, bits 0-2 index of
+ *          the magnitude in {0, 0.5, 1, 1.5, 2, 3, 4, 6}; no negative zero.
+ *   scale  [rows] fp32.
+ *   sf     coda_nvfp4_scale_bytes(rows, K) bytes, the order the tensor core
+ *          reads: the scale of row r, 16-element block j sits at byte
+ *            ((r/128) * KT + j/16) * 2048 + ((j/4) % 4) * 512
+ *            + (r % 32) * 16 + ((r % 128) / 32) * 4 + j % 4
+ *          with KT = ceil(K / 256); rows are padded to a multiple of 256 and
+ *          blocks to KT * 16, the padding holding zero scales.
+ * Requirements: K % 32 == 0; Xq, sf 16-byte aligned; N (I) % 8 == 0.  */
+size_t coda_nvfp4_scale_bytes(int64_t rows, int64_t K);
+int coda_quantize_nvfp4_rows(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq, uint8_t* sf,
+                             float* scale, coda_stream stream);
+
+/* Y = R + (sx ⊙ deq(Xq, sfx))(sw ⊙ deq(Wq, sfw))^T: X side [M, K], W side
+ * [N, K] (as quantised by coda_quantize_nvfp4_rows), R [M, N] bf16 or NULL,
+ * Y [M, N] bf16. */
+size_t coda_linear_nvfp4_workspace_size(int64_t M, int64_t N, int64_t K);
+int coda_linear_nvfp4(const uint8_t* Xq, const uint8_t* sfx, const float* sx, const uint8_t* Wq, const uint8_t* sfw,
+                      const float* sw, const coda_bf16* R, coda_bf16* Y, int64_t M, int64_t N, int64_t K, void* ws,
+                      size_t ws_bytes, coda_stream stream);
+
+/* linear_swiglu on NVFP4 operands: g = r ⊙ X̂ Ŵgᵀ, u = r ⊙ X̂ Ŵuᵀ,
+ * H = silu(g) ⊙ u with X̂ = sx ⊙ deq(Xq, sfx) and likewise for the weights
+ * ([I, K] each); rstd [M] or NULL (r = 1); H, g_save, u_save [M, I] bf16
+ * (g_save, u_save may be NULL). */
+size_t coda_linear_swiglu_nvfp4_workspace_size(int64_t M, int64_t I, int64_t K);
+int coda_linear_swiglu_nvfp4(const uint8_t* Xq, const uint8_t* sfx, const float* sx, const float* rstd,
+                             const uint8_t* Wgq, const uint8_t* sfg, const float* sg, const uint8_t* Wuq,
+                             const uint8_t* sfu, const float* su, coda_bf16* H, coda_bf16* g_save,
+                             coda_bf16* u_save, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
+                             coda_stream stream);
+
+/* ------------------------------------------------------------------------
  * Final RMSNorm -> LM head -> cross-entropy ("CODA" §3.2.1, third site of
  * the GEMM-residual-RMSNorm-GEMM pattern: final down-projection -> residual
  * -> final RMSNorm -> language-model head)

@@ -112,6 +112,16 @@ def test_rejects_bad_arguments_on_host(lib):
     assert lib.coda_rmsnorm_scale(FAKE, 64, 16, 64, 1e-6, FAKE, FAKE, FAKE_UNALIGNED, 64, None) == 2
     assert lib.coda_rmsnorm_scale(FAKE, 64, 16, 64, 1e-6, FAKE, FAKE, FAKE, 60, None) == 1
     assert lib.coda_rmsnorm_scale(FAKE, 64, 0, 64, 1e-6, FAKE, FAKE, FAKE, 64, None) == 0
+    # NVFP4: K a multiple of 32; block scales required and aligned
+    assert lib.coda_quantize_nvfp4_rows(FAKE, 48, 16, 48, FAKE, FAKE, FAKE, None) == 3
+    assert lib.coda_quantize_nvfp4_rows(FAKE, 64, 16, 64, FAKE, None, FAKE, None) == 1
+    assert lib.coda_quantize_nvfp4_rows(FAKE, 64, 16, 64, FAKE, FAKE_UNALIGNED, FAKE, None) == 2
+    assert lib.coda_linear_nvfp4(*([FAKE] * 6), None, FAKE, 16, 64, 48, ws, 4096, None) == 3
+    assert lib.coda_linear_nvfp4(FAKE, None, *([FAKE] * 4), None, FAKE, 16, 64, 64, ws, 4096, None) == 1
+    assert lib.coda_linear_swiglu_nvfp4(*([FAKE] * 9), None, FAKE, None, None, 16, 64, 64, ws, 4096, None) == 1
+    assert lib.coda_linear_swiglu_nvfp4(*([FAKE] * 10), FAKE, None, None, 0, 64, 64, ws, 4096, None) == 0
+    assert lib.coda_nvfp4_scale_bytes(300, 224) == 2 * 2 * 1 * 2048
+    assert lib.coda_nvfp4_scale_bytes(256, 512) == 2 * 2 * 2048
 
 
 def test_empty_problem_is_a_noop(lib):
