@@ -534,7 +534,37 @@ def main():
             "ms": round(m8, 3), "tflops": round(gf[DOMINANT] / (m8 / 1e3) / 1e12, 1),
             "peak": round(fp8_peak, 1), "peak_kind": f"fp8 = 2 x bf16 burst ({peak_src}, nominal ratio)",
             "frac": round(gf[DOMINANT] / (m8 / 1e3) / 1e12 / fp8_peak, 4)}
-        del xq, gq, uq, Hq, gq8, uq8
+        del xq, gq, uq
+
+        # NVFP4 (e2m1 + e4m3 block scales) gate/up + SwiGLU at the same shape:
+        # the block-scaled kind::mxf4nvf4 mainloop, single CTAs.
+        fq = []
+        xq4, sfx4, sx4 = coda.quantize_nvfp4_rows(t["x0"])
+        gq4, sfg4, sg4 = coda.quantize_nvfp4_rows(t["Wg"])
+        uq4, sfu4, su4 = coda.quantize_nvfp4_rows(t["Wu"])
+        for i in range(5):
+            ev[0].record(stream)
+            coda.quantize_nvfp4_rows(t["x0"])
+            ev[1].record(stream)
+            coda.linear_swiglu_nvfp4(xq4, sfx4, sx4, gq4, sfg4, sg4, uq4, sfu4, su4, rstd=r_, H=Hq, g=gq8, u=uq8,
+                                     ws=ws8)
+            ev[2].record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 2:
+                fq.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
+        if coda.get_status(ws8) != 0:
+            raise RuntimeError("device status error in the NVFP4 measurement")
+        mq4 = statistics.median(q for q, _ in fq)
+        m4 = statistics.median(g for _, g in fq)
+        fp4_peak = 6 * burst
+        other["nvfp4_gateup_swiglu"] = {
+            "workload": "NVFP4 gate/up GEMM (e2m1, e4m3 scale per 16, fp32 row scale) with row-scale + SwiGLU "
+                        "epilogue, 8192 x 2x28672 x 8192, single-CTA tiles",
+            "ms": round(m4, 3), "tflops": round(gf[DOMINANT] / (m4 / 1e3) / 1e12, 1),
+            "peak": round(fp4_peak, 1), "peak_kind": f"fp4 = 6 x bf16 burst ({peak_src}, nominal ratio)",
+            "frac": round(gf[DOMINANT] / (m4 / 1e3) / 1e12 / fp4_peak, 4),
+            "quantize_x_ms": round(mq4, 3)}
+        del xq4, gq4, uq4, sfx4, sfg4, sfu4, Hq, gq8, uq8
 
         # Configs 3 and 2 (also parity workloads), forward + backward, timed the
         # same way: the SwiGLU MLP at hidden 4096 and the RMSNorm-reparameterised

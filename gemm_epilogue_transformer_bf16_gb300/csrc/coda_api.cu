@@ -1299,35 +1299,39 @@ static int ce_forward(const coda_bf16* X, const coda_bf16* W, const int32_t* lab
   return CODA_OK;
 }
 
-// One NVFP4 GEMM launch: single CTAs, 128 x 256 tiles (b_dual: 128 gate +
-// 128 up columns), k-slices of 256 elements.
+// One NVFP4 GEMM launch: 128 x 256 tiles (b_dual: 128 gate + 128 up
+// columns), k-slices of 256 elements; single CTAs, or clusters of four CTAs
+// on adjacent row blocks that each copy a 64-row quarter of the B tile.
 int run_nvfp4(coda::EpiKind kind, const uint8_t* A, const uint8_t* B0, const uint8_t* B1, coda::Nvfp4Scales sc,
               int64_t M, int64_t N, int64_t K, int b_dual, const EpiArgs& e, int* status, cudaStream_t s) {
   if (M == 0 || N == 0) return CODA_OK;
   if (!get_encoder()) return CODA_ERR_CUDA;
   const int sms = num_sms();
   if (sms <= 0) return CODA_ERR_CUDA;
+  const int cg = coda::nvfp4_cluster_size(M);
+  // rows of one B copy: the whole tile (256, or 128 per weight when dual),
+  // or a quarter of it when four CTAs share the tile
+  const uint32_t b_rows = cg == 4 ? BN / 4 : (b_dual ? BN / 2 : BN);
   CUtensorMap maps[3];
   std::memset(maps, 0, sizeof(maps));
   const int64_t kb = K / 2;  // bytes of codes per row
   if (!encode_map(&maps[0], A, M, kb, kb, 128, coda::BM, 1)) return CODA_ERR_CUDA;
+  if (!encode_map(&maps[1], B0, N, kb, kb, 128, b_rows, 1)) return CODA_ERR_CUDA;
   if (b_dual) {
-    if (!encode_map(&maps[1], B0, N, kb, kb, 128, BN / 2, 1)) return CODA_ERR_CUDA;
-    if (!encode_map(&maps[2], B1, N, kb, kb, 128, BN / 2, 1)) return CODA_ERR_CUDA;
+    if (!encode_map(&maps[2], B1, N, kb, kb, 128, b_rows, 1)) return CODA_ERR_CUDA;
   } else {
-    if (!encode_map(&maps[1], B0, N, kb, kb, 128, BN, 1)) return CODA_ERR_CUDA;
     maps[2] = maps[1];
   }
   GemmArgs a{};
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
-  a.num_m = static_cast<int>(cdiv(M, coda::BM));
+  a.num_m = static_cast<int>(cdiv(M, static_cast<int64_t>(cg) * coda::BM));
   a.num_n = static_cast<int>(cdiv(N, b_dual ? BN / 2 : BN));
   a.kb0 = static_cast<int>(cdiv(K, 256));
   a.b_dual = b_dual;
   a.n_per_unit = 1;
   a.num_units = a.num_m * a.num_n;
-  a.group_m = group_m(1);
+  a.group_m = group_m(cg);
   a.idesc = coda::nvfp4_idesc();
   a.status = status;
   a.timeout_ns = TIMEOUT_NS;
@@ -1335,8 +1339,9 @@ int run_nvfp4(coda::EpiKind kind, const uint8_t* A, const uint8_t* B0, const uin
   a.e = e;
   a.e.st_stream = (l2_hints() & 4) ? 1 : 0;
   sc.kt = cdiv(K, 256);
-  cudaError_t err = kind == coda::EpiKind::Swiglu ? coda::launch_gemm_swiglu_nvfp4(a.num_units, sms, s, maps, a, sc)
-                                                  : coda::launch_gemm_plain_nvfp4(a.num_units, sms, s, maps, a, sc);
+  cudaError_t err = kind == coda::EpiKind::Swiglu
+                        ? coda::launch_gemm_swiglu_nvfp4(cg, a.num_units, sms, s, maps, a, sc)
+                        : coda::launch_gemm_plain_nvfp4(cg, a.num_units, sms, s, maps, a, sc);
   return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
 }
 
@@ -1786,7 +1791,7 @@ int coda_linear_swiglu_fp8(const uint8_t* Xq, const float* sx, const float* rstd
 // ------------------------------------------------------------------ NVFP4 operands
 size_t coda_nvfp4_scale_bytes(int64_t rows, int64_t K) {
   if (rows < 0 || K < 0) return 0;
-  return static_cast<size_t>(cdiv(rows, 256) * 2 * cdiv(K, 256) * 2048);
+  return static_cast<size_t>(cdiv(rows, 512) * 4 * cdiv(K, 256) * 2048);
 }
 
 int coda_quantize_nvfp4_rows(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq, uint8_t* sf,

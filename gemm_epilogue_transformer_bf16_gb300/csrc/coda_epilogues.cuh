@@ -246,7 +246,10 @@ struct EpiPlain {
 //   scales (col_scale, col_scale2).
 //   Optionally stores g and u (bf16) for the backward.
 // ---------------------------------------------------------------------------
-template <int BN>
+// UP: TMEM column offset of the up half from the gate half (BN / 2 when the
+// tile is [gate | up]; a kernel that hands each epilogue warp a column range
+// of a wider tile passes the wider tile's half).
+template <int BN, int UP = BN / 2>
 struct EpiSwiglu {
   struct State {};
   static constexpr int HALF = BN / 2;
@@ -264,7 +267,7 @@ struct EpiSwiglu {
       float g[32], u[32];
       __syncwarp();
       tmem_ld32(t.taddr + c, g);
-      tmem_ld32(t.taddr + HALF + c, u);
+      tmem_ld32(t.taddr + UP + c, u);
       if (rv) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {

@@ -48,11 +48,15 @@ struct Nvfp4Scales {
   int64_t kt;         // k tiles of 256 elements
 };
 uint32_t nvfp4_idesc();
+// Cluster size of the NVFP4 kernel for M rows: 1 (single CTAs) or 4 (four
+// CTAs sharing B; each copies a 64-row quarter of the B tile, so the B
+// tensor maps must have 64-row boxes).
+int nvfp4_cluster_size(int64_t M);
 cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Q,
                                        uint8_t* SF, float* scale, int num_sms, cudaStream_t s);
-cudaError_t launch_gemm_plain_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a,
-                                    const Nvfp4Scales& sc);
-cudaError_t launch_gemm_swiglu_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_plain_nvfp4(int cg, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
+                                    const GemmArgs& a, const Nvfp4Scales& sc);
+cudaError_t launch_gemm_swiglu_nvfp4(int cg, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
                                      const GemmArgs& a, const Nvfp4Scales& sc);
 
 // auxiliary kernels (coda_aux.cu)

@@ -16,7 +16,8 @@
 //          the 2 KB of one (row block, k tile) are contiguous, four 512-byte
 //          groups of 64 elements, each holding row r's 4 scales at byte
 //          (r % 32) * 16 + ((r % 128) / 32) * 4.  Rows are padded to a
-//          multiple of 256 and K to a multiple of 256 with zero scales.
+//          multiple of 512 (a cluster of four 128-row blocks) and K to a
+//          multiple of 256 with zero scales.
 //
 // GEMM structure: the single-CTA form of the bf16 kernel (warp 0 TMA
 // producer, warp 1 TMEM owner and MMA issuer, warps 2-5 epilogue), M = 128,
@@ -30,7 +31,11 @@
 // epilogue of a tile does not overlap the next tile's mainloop.
 #include <algorithm>
 #include <atomic>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
+#include <type_traits>
+#include <utility>
 
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
@@ -43,19 +48,24 @@ namespace coda {
 namespace {
 
 constexpr int F4_BN = 256;
-constexpr int F4_STAGES = 4;
 constexpr uint32_t F4_A_BYTES = BM * 128;
 constexpr uint32_t F4_B_BYTES = F4_BN * 128;
 constexpr uint32_t F4_SFA_BYTES = 2048;
 constexpr uint32_t F4_SFB_BYTES = 4096;
 constexpr uint32_t F4_STAGE_BYTES = F4_A_BYTES + F4_B_BYTES + F4_SFA_BYTES + F4_SFB_BYTES;
 constexpr uint32_t F4_BAR_BYTES = 256;
-constexpr uint32_t F4_EPI_BYTES = 4 * 2048;
-constexpr uint32_t F4_SMEM = 1024 + F4_STAGES * F4_STAGE_BYTES + F4_BAR_BYTES + F4_EPI_BYTES;
 constexpr uint32_t F4_TMEM_COLS = 512;
 constexpr uint32_t F4_SF_COL0 = 256;     // first TMEM column of the scale slots
 constexpr uint32_t F4_SF_SLOT_COLS = 64;
 static_assert(F4_STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
+
+// Eight epilogue warps, two per TMEM lane quarter, each on half of the
+// tile's columns; three stages.
+constexpr int F4_EW = 8;
+constexpr int F4_STAGES = 3;
+constexpr int F4_THREADS = 64 + 32 * F4_EW;
+constexpr uint32_t F4_EPI_BYTES = F4_EW * 2048;
+constexpr uint32_t F4_SMEM = 1024 + F4_STAGES * F4_STAGE_BYTES + F4_BAR_BYTES + F4_EPI_BYTES;
 static_assert(F4_SMEM <= 232448, "shared memory per CTA");
 static_assert(F4_SF_COL0 + F4_STAGES * F4_SF_SLOT_COLS <= F4_TMEM_COLS, "TMEM columns");
 
@@ -67,6 +77,42 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "@P cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%4];\n\t}" ::"r"(
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(p), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// The same, written to the same offset in every CTA of `mask` in the
+// cluster, completion counted on each destination CTA's barrier at `bar`'s
+// offset.
+__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                             uint16_t mask, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %3, 0;\n\t"
+      "@P cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1], %2, [%4], %5;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(p), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+// Tiled tensor copy multicast to the CTAs of `mask` (same smem offset and
+// barrier offset in each).
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
+                                               uint16_t mask, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %5, 0;\n\t"
+      "@P cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %6;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(p), "h"(mask)
+      : "memory");
+}
+
+// Arrive once on the barrier at `bar`'s offset in every CTA of `mask` when
+// the tcgen05 operations issued so far by this thread have completed.
+__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %2, 0;\n\t"
+      "@P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::
+          "r"(smem_u32(bar)),
+      "h"(mask), "r"(p)
       : "memory");
 }
 
@@ -194,11 +240,125 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const __nv_bfl
   }
 }
 
-template <class Epi>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// The epilogue, one warp's share: 32 rows (TMEM lane quarter q) x 128
+// accumulator columns (half h of the tile).  With one accumulator in TMEM
+// the next tile's MMAs wait for it, so the warp first pulls its columns
+// into registers and frees the accumulator, then scales, applies the map
+// and stores while the next tile's mainloop runs.
+//   KIND 0: y = rs_i * cs_j * acc (+ R), columns nb*256 + h*128 + [0, 128);
+//   KIND 1: g = rs_i * cg_j * acc_gate, u = rs_i * cu_j * acc_up,
+//           H = silu(g) * u, columns nb*128 + h*64 + [0, 64)
+//   (rs = token scale x optional RMSNorm row factor; cs, cg, cu the
+//   weights' row scales), as EpiPlain / EpiSwiglu do for the other kernels.
+template <int KIND>
+__device__ __forceinline__ void f4_epilogue(const EpiArgs& e, const TileInfo& t, int h, uint64_t* tfull,
+                                            uint32_t parity, uint64_t* tempty, volatile int* abort_flag,
+                                            uint64_t timeout_ns, uint32_t sleep_ns, bool& aborted) {
+  const int lane = threadIdx.x & 31;
+  const int row = t.row;
+  const bool rv = row < t.M;
+  const int row0 = row - lane;
+  float v[128];
+  if (!mbar_wait_bounded(tfull, parity, abort_flag, t.status, timeout_ns, sleep_ns)) {
+    aborted = true;
+    return;
+  }
+  tc_fence_after();
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    // KIND 0: columns h*128 + 32c; KIND 1: gate h*64 + 32c (c < 2), up 128 + h*64 + 32(c-2)
+    const uint32_t col = KIND == 0 ? h * 128 + 32 * c : (c < 2 ? h * 64 + 32 * c : 128 + h * 64 + 32 * (c - 2));
+    tmem_ld32(t.taddr + col, *reinterpret_cast<float(*)[32]>(v + 32 * c));
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(tempty);
+  auto* D = static_cast<__nv_bfloat16*>(e.D);
+  if constexpr (KIND == 0) {
+    const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int col0 = t.nb * 256 + h * 128 + 32 * c;
+      if (col0 >= t.N) break;
+      float* x = v + 32 * c;
+      if (rv) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int cc = col0 + g * 8;
+          if (cc < t.N) {
+            float s8[8];
+            if (e.col_scale) {
+              load_f32x8(e.col_scale + cc, s8);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) s8[i] = 1.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[g * 8 + i] = x[g * 8 + i] * rs * s8[i];
+            if (e.aux0) {
+              float r8[8];
+              load_bf16x8(e.aux0 + static_cast<int64_t>(row) * e.ld_aux0 + cc, r8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[g * 8 + i] += r8[i];
+            }
+          }
+        }
+      }
+      warp_store_bf16x32(t.stage, D, e.ldd, row0, t.M, col0, t.N, x, e.st_stream);
+    }
+  } else {
+    const float rs =
+        ((e.row_scale && rv) ? e.row_scale[row] : 1.f) * ((e.row_scale2 && rv) ? e.row_scale2[row] : 1.f);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int col0 = t.nb * 128 + h * 64 + 32 * c;
+      if (col0 >= t.N) break;
+      float* g = v + 32 * c;
+      float* u = v + 64 + 32 * c;
+      if (rv) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cc = col0 + q * 8;
+          float cg[8], cu[8];
+          if (e.col_scale && cc < t.N) {
+            load_f32x8(e.col_scale + cc, cg);
+            load_f32x8(e.col_scale2 + cc, cu);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            g[q * 8 + i] *= rs;
+            u[q * 8 + i] *= rs;
+            if (e.col_scale && cc < t.N) {
+              g[q * 8 + i] *= cg[i];
+              u[q * 8 + i] *= cu[i];
+            }
+          }
+        }
+      }
+      if (e.out1) warp_store_bf16x32(t.stage, e.out1, e.ld_out1, row0, t.M, col0, t.N, g, e.st_stream);
+      if (e.out2) warp_store_bf16x32(t.stage, e.out2, e.ld_out2, row0, t.M, col0, t.N, u, e.st_stream);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.f + __expf(-g[i])) * u[i];
+      warp_store_bf16x32(t.stage, D, e.ldd, row0, t.M, col0, t.N, g, e.st_stream);
+    }
+  }
+}
+
+// KIND 0: EpiPlain (B = one weight, 256 columns); 1: EpiSwiglu (B = 128 gate
+// + 128 up rows of two weights).  CG: 1, or 4 CTAs on four adjacent 128-row
+// blocks sharing the B tile: each loads a 64-row quarter of B and a quarter
+// of its block scales and multicasts them to all four, so every SM stages
+// 27 KB of its own per k-slice instead of 54 KB.  The MMAs stay per CTA
+// (cta_group::1); a stage is released when all four CTAs' MMAs are done
+// with it (each commit arrives on the stage barrier of every CTA).
+template <int KIND, int CG>
+__global__ void __launch_bounds__(F4_THREADS, 1)
     coda_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
                            const __grid_constant__ CUtensorMap mB1, const GemmArgs args, const Nvfp4Scales sc) {
+  static_assert(CG == 1 || CG == 4, "cluster size");
   constexpr int S = F4_STAGES;
+  constexpr bool MC = CG == 4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
@@ -213,13 +373,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = MC ? cluster_ctarank() : 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CG);  // one commit from each CTA reading the stage's B quarters
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 4);
+    mbar_init(tempty, F4_EW);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -235,11 +396,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (MC) cluster_sync();  // peer barriers initialised before any multicast lands
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_kb = args.kb0;
-  const int cluster_id = static_cast<int>(blockIdx.x);
-  const int num_clusters = static_cast<int>(gridDim.x);
+  const int cluster_id = static_cast<int>(blockIdx.x) / CG;
+  const int num_clusters = static_cast<int>(gridDim.x) / CG;
   bool aborted = false;
 
   if (warp == 0) {
@@ -247,8 +409,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t el = elect_one();
     uint32_t it = 0;
     for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters) {
-      int mb, nb, nlen, chunk;
-      unit_coords(args, u, mb, nb, nlen, chunk);
+      int mbc, nb, nlen, chunk;
+      unit_coords(args, u, mbc, nb, nlen, chunk);
+      const int mb = mbc * CG + static_cast<int>(rank);
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const int s = it % S;
         if (!mbar_wait_bounded(&empty[s], ((it / S) & 1) ^ 1, abort_flag, args.status, args.timeout_ns,
@@ -264,18 +427,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int x = kb * 128;  // bytes of codes = 256 elements
         tma_load_2d(sa, &mA, &full[s], x, mb * BM, el);
         bulk_load(sfa, sc.a + (static_cast<int64_t>(mb) * sc.kt + kb) * 2048, 2048, &full[s], el);
-        if (args.b_dual) {
-          // N = [128 gate rows | 128 up rows]: row block nb of each weight
-          tma_load_2d(sb, &mB0, &full[s], x, nb * (F4_BN / 2), el);
-          tma_load_2d(sb + (F4_BN / 2) * 128, &mB1, &full[s], x, nb * (F4_BN / 2), el);
-          bulk_load(sfb, sc.b0 + (static_cast<int64_t>(nb) * sc.kt + kb) * 2048, 2048, &full[s], el);
-          bulk_load(sfb + 2048, sc.b1 + (static_cast<int64_t>(nb) * sc.kt + kb) * 2048, 2048, &full[s], el);
+        // B rows of the tile: [256 rows of B] or [128 gate | 128 up]; their
+        // scales: two 2 KB groups (row blocks 2nb, 2nb + 1, or gate nb, up nb)
+        const uint8_t* sf0 = args.b_dual ? sc.b0 + (static_cast<int64_t>(nb) * sc.kt + kb) * 2048
+                                         : sc.b0 + (static_cast<int64_t>(2 * nb) * sc.kt + kb) * 2048;
+        const uint8_t* sf1 = args.b_dual ? sc.b1 + (static_cast<int64_t>(nb) * sc.kt + kb) * 2048
+                                         : sc.b0 + (static_cast<int64_t>(2 * nb + 1) * sc.kt + kb) * 2048;
+        if constexpr (MC) {
+          // quarter r of the B rows and of their 4 KB of scales, to all four CTAs
+          const int r = static_cast<int>(rank);
+          const CUtensorMap* mb_map = (args.b_dual && r >= 2) ? &mB1 : &mB0;
+          const int row = args.b_dual ? nb * (F4_BN / 2) + (r & 1) * 64 : nb * F4_BN + r * 64;
+          tma_load_2d_mc(sb + r * 8192, mb_map, &full[s], x, row, 0xF, el);
+          bulk_load_mc(sfb + r * 1024, (r >> 1 ? sf1 : sf0) + (r & 1) * 1024, 1024, &full[s], 0xF, el);
         } else {
-          // row blocks 2nb and 2nb + 1 (scale rows are padded to 256)
-          tma_load_2d(sb, &mB0, &full[s], x, nb * F4_BN, el);
-          bulk_load(sfb, sc.b0 + (static_cast<int64_t>(2 * nb) * sc.kt + kb) * 2048, 2048, &full[s], el);
-          bulk_load(sfb + 2048, sc.b0 + (static_cast<int64_t>(2 * nb + 1) * sc.kt + kb) * 2048, 2048, &full[s],
-                    el);
+          if (args.b_dual) {
+            tma_load_2d(sb, &mB0, &full[s], x, nb * (F4_BN / 2), el);
+            tma_load_2d(sb + (F4_BN / 2) * 128, &mB1, &full[s], x, nb * (F4_BN / 2), el);
+          } else {
+            tma_load_2d(sb, &mB0, &full[s], x, nb * F4_BN, el);
+          }
+          bulk_load(sfb, sf0, 2048, &full[s], el);
+          bulk_load(sfb + 2048, sf1, 2048, &full[s], el);
         }
       }
     }
@@ -323,7 +496,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           umma_nvfp4(tmem_base, ad, bd, idesc, slot + g * 4, slot + 16 + g * 8, (kb | g) != 0, el);
         }
         issued = true;
-        umma_commit(&empty[s], el);
+        if constexpr (MC)
+          umma_commit_mc(&empty[s], 0xF, el);
+        else
+          umma_commit(&empty[s], el);
       }
       if (aborted) break;
       umma_commit(tfull, el);
@@ -334,39 +510,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // warps 2-5 take the first half of the tile's columns, 6-9 the second
     const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
     uint32_t t = 0;
     for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters, ++t) {
-      int mb, nb, nlen, chunk;
-      unit_coords(args, u, mb, nb, nlen, chunk);
+      int mbc, nb, nlen, chunk;
+      unit_coords(args, u, mbc, nb, nlen, chunk);
+      const int mb = mbc * CG + static_cast<int>(rank);
       TileInfo ti;
       ti.mb = mb;
+      ti.nb = nb;
       ti.unit_chunk = chunk;
       ti.row = mb * BM + q * 32 + lane;
       ti.M = args.M;
       ti.N = args.N;
       ti.status = args.status;
-      ti.stage = epi_stage + q * 2048;
-      typename Epi::State st;
-      Epi::begin(st, args.e, ti);
-      if (!mbar_wait_bounded(tfull, t & 1, abort_flag, args.status, args.timeout_ns, args.epilogue_sleep_ns)) {
-        aborted = true;
-        break;
-      }
-      tc_fence_after();
-      __syncwarp();
-      ti.nb = nb;
+      ti.stage = epi_stage + (warp - 2) * 2048;
       ti.taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      Epi::tile(st, args.e, ti);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
-      Epi::end(st, args.e, ti);
+      f4_epilogue<KIND>(args.e, ti, h, tfull, t & 1, tempty, abort_flag, args.timeout_ns, args.epilogue_sleep_ns,
+                        aborted);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (MC) cluster_sync();  // no CTA leaves while a peer may still write or signal it
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -374,26 +543,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <class Epi>
+// Grid: one CTA (CG = 1) or one 4-CTA cluster per unit up to the resident
+// limit; the first call on a device sets the shared-memory limit and looks
+// up the resident-cluster count.
+template <int KIND, int CG>
 cudaError_t launch_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a,
                          const Nvfp4Scales& sc) {
   static std::mutex init;
   static std::atomic<bool> attr_done[64];
+  static std::atomic<int> max_clusters[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  auto kern = coda_gemm_nvfp4_kernel<Epi>;
+  auto kern = coda_gemm_nvfp4_kernel<KIND, CG>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(F4_THREADS);
+  cfg.dynamicSmemBytes = F4_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(init);
     if (!attr_done[dev].load(std::memory_order_relaxed)) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(F4_SMEM));
       if (e != cudaSuccess) return e;
+      int n = sms;
+      if (CG > 1) {
+        cfg.gridDim = dim3(static_cast<unsigned>(sms - sms % CG));
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n <= 0) return cudaErrorInvalidConfiguration;
+      }
+      max_clusters[dev].store(n, std::memory_order_relaxed);
       attr_done[dev].store(true, std::memory_order_release);
     }
   }
-  const int grid = std::min(num_units, sms);
-  kern<<<grid, NUM_THREADS, F4_SMEM, s>>>(m[0], m[1], m[2], a, sc);
+  const int resident = max_clusters[dev].load(std::memory_order_relaxed);
+  cfg.gridDim = dim3(static_cast<unsigned>(CG * std::min(num_units, resident)));
+  e = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], a, sc);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -401,9 +595,20 @@ cudaError_t launch_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorM
 
 uint32_t nvfp4_idesc() { return idesc_nvfp4(BM, F4_BN); }
 
+// Variant: single CTAs by default; CODA_NVFP4=4 in the environment selects
+// clusters of four CTAs sharing the B tile (for comparisons) when there are
+// at least four 128-row blocks.
+int nvfp4_cluster_size(int64_t M) {
+  static const int env = [] {
+    const char* v = std::getenv("CODA_NVFP4");
+    return v ? std::atoi(v) : 1;
+  }();
+  return env == 4 && M > 3 * BM ? 4 : 1;
+}
+
 cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Q,
                                        uint8_t* SF, float* scale, int num_sms, cudaStream_t s) {
-  const int64_t rows_pad = (M + 255) / 256 * 256;
+  const int64_t rows_pad = (M + 511) / 512 * 512;
   const int64_t kt = (K + 255) / 256;
   const int64_t blocks = std::min<int64_t>((rows_pad + 7) / 8, static_cast<int64_t>(num_sms) * 8);
   quantize_nvfp4_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(
@@ -411,13 +616,13 @@ cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int6
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_plain_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a,
-                                    const Nvfp4Scales& sc) {
-  return launch_nvfp4<EpiPlain<256>>(num_units, sms, s, m, a, sc);
+cudaError_t launch_gemm_plain_nvfp4(int cg, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
+                                    const GemmArgs& a, const Nvfp4Scales& sc) {
+  return cg == 4 ? launch_nvfp4<0, 4>(num_units, sms, s, m, a, sc) : launch_nvfp4<0, 1>(num_units, sms, s, m, a, sc);
 }
-cudaError_t launch_gemm_swiglu_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
+cudaError_t launch_gemm_swiglu_nvfp4(int cg, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
                                      const GemmArgs& a, const Nvfp4Scales& sc) {
-  return launch_nvfp4<EpiSwiglu<256>>(num_units, sms, s, m, a, sc);
+  return cg == 4 ? launch_nvfp4<1, 4>(num_units, sms, s, m, a, sc) : launch_nvfp4<1, 1>(num_units, sms, s, m, a, sc);
 }
 
 }  // namespace coda

@@ -447,7 +447,7 @@ int coda_linear_swiglu_fp8(const uint8_t* Xq, const float* sx, const float* rstd
  *          reads: the scale of row r, 16-element block j sits at byte
  *            ((r/128) * KT + j/16) * 2048 + ((j/4) % 4) * 512
  *            + (r % 32) * 16 + ((r % 128) / 32) * 4 + j % 4
- *          with KT = ceil(K / 256); rows are padded to a multiple of 256 and
+ *          with KT = ceil(K / 256); rows are padded to a multiple of 512 and
  *          blocks to KT * 16, the padding holding zero scales.
  * Requirements: K % 32 == 0; Xq, sf 16-byte aligned; N (I) % 8 == 0.  */
 size_t coda_nvfp4_scale_bytes(int64_t rows, int64_t K);

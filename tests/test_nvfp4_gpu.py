@@ -50,7 +50,7 @@ def check_quantised(coda, X, q, sf, s):
     assert np.array_equal(unpack_codes(q), oc), "e2m1 codes"
     assert np.array_equal(s.cpu().numpy(), os_), "row scales"
     buf = sf.cpu().numpy()
-    assert buf.size == coda.load().coda_nvfp4_scale_bytes(M, K) == -(-M // 256) * 2 * -(-K // 256) * 2048
+    assert buf.size == coda.load().coda_nvfp4_scale_bytes(M, K) == -(-M // 512) * 4 * -(-K // 256) * 2048
     off = scale_offsets(M, K)
     assert np.array_equal(buf[off], osf), "block scales"
     pad = np.ones(buf.size, bool)
@@ -106,3 +106,17 @@ def test_nvfp4_special_rows(coda):
     X[1, 5] = 3000.0
     xq, sfx, sx = coda.quantize_nvfp4_rows(X.to(DEV))
     check_quantised(coda, X, xq, sfx, sx)
+
+
+@pytest.mark.parametrize("variant", ["1", "4"])
+def test_nvfp4_kernel_variants(variant):
+    """Each kernel variant (single CTAs, or four-CTA clusters sharing the B
+    tile by multicast) in a fresh process."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, CODA_NVFP4=variant)
+    r = subprocess.run([sys.executable, os.path.join(here, "nvfp4_variant_check.py")], env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), f"{variant}:\n{r.stdout[-2000:]}\n{r.stderr[-4000:]}"
