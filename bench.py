@@ -153,10 +153,17 @@ def measured_peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+# The sources the dominant kernel (gate/up GEMM + SwiGLU epilogue) and its
+# host-side launch are built from; a change to any of them invalidates the
+# committed DRAM-traffic figure.
+DOMINANT_SOURCES = ["coda_api.cu", "coda_epilogues.cuh", "coda_gemm.cuh", "coda_gemm_swiglu.cu", "coda_internal.h",
+                    "coda_launch.cuh", "coda_ptx.cuh", "coda_status.h"]
+
+
 def source_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_epilogue_transformer_bf16_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in DOMINANT_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 

@@ -1300,8 +1300,8 @@ static int ce_forward(const coda_bf16* X, const coda_bf16* W, const int32_t* lab
 }
 
 // One NVFP4 GEMM launch: 128 x 256 tiles (b_dual: 128 gate + 128 up
-// columns), k-slices of 256 elements; single CTAs, or clusters of four CTAs
-// on adjacent row blocks that each copy a 64-row quarter of the B tile.
+// columns), k-slices of 256 elements; single CTAs, or clusters of cg CTAs
+// on adjacent row blocks that each copy 256 / cg rows of the B tile.
 int run_nvfp4(coda::EpiKind kind, const uint8_t* A, const uint8_t* B0, const uint8_t* B1, coda::Nvfp4Scales sc,
               int64_t M, int64_t N, int64_t K, int b_dual, const EpiArgs& e, int* status, cudaStream_t s) {
   if (M == 0 || N == 0) return CODA_OK;
@@ -1311,7 +1311,7 @@ int run_nvfp4(coda::EpiKind kind, const uint8_t* A, const uint8_t* B0, const uin
   const int cg = coda::nvfp4_cluster_size(M);
   // rows of one B copy: the whole tile (256, or 128 per weight when dual),
   // or a quarter of it when four CTAs share the tile
-  const uint32_t b_rows = cg == 4 ? BN / 4 : (b_dual ? BN / 2 : BN);
+  const uint32_t b_rows = cg > 1 ? BN / cg : (b_dual ? BN / 2 : BN);
   CUtensorMap maps[3];
   std::memset(maps, 0, sizeof(maps));
   const int64_t kb = K / 2;  // bytes of codes per row

@@ -48,9 +48,9 @@ struct Nvfp4Scales {
   int64_t kt;         // k tiles of 256 elements
 };
 uint32_t nvfp4_idesc();
-// Cluster size of the NVFP4 kernel for M rows: 1 (single CTAs) or 4 (four
-// CTAs sharing B; each copies a 64-row quarter of the B tile, so the B
-// tensor maps must have 64-row boxes).
+// Cluster size of the NVFP4 kernel for M rows: 1 (single CTAs), 2 or 4
+// (CTAs sharing B; each copies 256 / cg rows of the B tile, so the B tensor
+// maps must have boxes of that many rows).
 int nvfp4_cluster_size(int64_t M);
 cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Q,
                                        uint8_t* SF, float* scale, int num_sms, cudaStream_t s);

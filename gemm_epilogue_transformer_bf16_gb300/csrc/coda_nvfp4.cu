@@ -60,11 +60,12 @@ constexpr uint32_t F4_SF_SLOT_COLS = 64;
 static_assert(F4_STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
 
 // Eight epilogue warps, two per TMEM lane quarter, each on half of the
-// tile's columns; three stages.
+// tile's columns, with 1 KB store buffers; four stages.
 constexpr int F4_EW = 8;
-constexpr int F4_STAGES = 3;
+constexpr int F4_STAGES = 4;
 constexpr int F4_THREADS = 64 + 32 * F4_EW;
-constexpr uint32_t F4_EPI_BYTES = F4_EW * 2048;
+constexpr uint32_t F4_EPI_WARP_BYTES = 1024;
+constexpr uint32_t F4_EPI_BYTES = F4_EW * F4_EPI_WARP_BYTES;
 constexpr uint32_t F4_SMEM = 1024 + F4_STAGES * F4_STAGE_BYTES + F4_BAR_BYTES + F4_EPI_BYTES;
 static_assert(F4_SMEM <= 232448, "shared memory per CTA");
 static_assert(F4_SF_COL0 + F4_STAGES * F4_SF_SLOT_COLS <= F4_TMEM_COLS, "TMEM columns");
@@ -240,6 +241,46 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const __nv_bfl
   }
 }
 
+// Stores a warp's 32 rows x 16 columns as bf16 (thread `lane` passes the 16
+// values of row row0 + lane, columns col0 ..) through the warp's 1 KB buffer:
+// 16-byte chunk p of row r sits at r * 32 + ((p ^ ((r >> 2) & 1)) * 16), so
+// the row-wise writes cover all banks once per 8 lanes and the reads take a
+// contiguous 512 bytes; each global store then covers 16 rows x 32
+// contiguous bytes.  Rows >= M and columns >= N are not written (N is a
+// multiple of 8).  Called by all 32 lanes.
+__device__ __forceinline__ void f4_store_bf16x16(uint8_t* stage, __nv_bfloat16* base, int64_t ld, int row0, int M,
+                                                 int col0, int N, const float* v, bool stream) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const uint4 w = make_uint4(pack_bf16x2(v[p * 8 + 0], v[p * 8 + 1]), pack_bf16x2(v[p * 8 + 2], v[p * 8 + 3]),
+                               pack_bf16x2(v[p * 8 + 4], v[p * 8 + 5]), pack_bf16x2(v[p * 8 + 6], v[p * 8 + 7]));
+    *reinterpret_cast<uint4*>(stage + lane * 32 + ((p ^ ((lane >> 2) & 1)) * 16)) = w;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = i * 16 + (lane >> 1), p = lane & 1;
+    const uint4 w = *reinterpret_cast<const uint4*>(stage + r * 32 + ((p ^ ((r >> 2) & 1)) * 16));
+    const int row = row0 + r, col = col0 + p * 8;
+    if (row < M && col < N) {
+      __nv_bfloat16* dst = base + static_cast<int64_t>(row) * ld + col;
+      if (stream)
+        asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(w.x), "r"(w.y), "r"(w.z),
+                     "r"(w.w)
+                     : "memory");
+      else
+        *reinterpret_cast<uint4*>(dst) = w;
+    }
+  }
+  __syncwarp();
+}
+__device__ __forceinline__ void f4_store_bf16x32(uint8_t* stage, __nv_bfloat16* base, int64_t ld, int row0, int M,
+                                                 int col0, int N, const float* v, bool stream) {
+  f4_store_bf16x16(stage, base, ld, row0, M, col0, N, v, stream);
+  f4_store_bf16x16(stage, base, ld, row0, M, col0 + 16, N, v + 16, stream);
+}
+
 // The epilogue, one warp's share: 32 rows (TMEM lane quarter q) x 128
 // accumulator columns (half h of the tile).  With one accumulator in TMEM
 // the next tile's MMAs wait for it, so the warp first pulls its columns
@@ -305,7 +346,7 @@ __device__ __forceinline__ void f4_epilogue(const EpiArgs& e, const TileInfo& t,
           }
         }
       }
-      warp_store_bf16x32(t.stage, D, e.ldd, row0, t.M, col0, t.N, x, e.st_stream);
+      f4_store_bf16x32(t.stage, D, e.ldd, row0, t.M, col0, t.N, x, e.st_stream);
     }
   } else {
     const float rs =
@@ -336,11 +377,11 @@ __device__ __forceinline__ void f4_epilogue(const EpiArgs& e, const TileInfo& t,
           }
         }
       }
-      if (e.out1) warp_store_bf16x32(t.stage, e.out1, e.ld_out1, row0, t.M, col0, t.N, g, e.st_stream);
-      if (e.out2) warp_store_bf16x32(t.stage, e.out2, e.ld_out2, row0, t.M, col0, t.N, u, e.st_stream);
+      if (e.out1) f4_store_bf16x32(t.stage, e.out1, e.ld_out1, row0, t.M, col0, t.N, g, e.st_stream);
+      if (e.out2) f4_store_bf16x32(t.stage, e.out2, e.ld_out2, row0, t.M, col0, t.N, u, e.st_stream);
 #pragma unroll
       for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.f + __expf(-g[i])) * u[i];
-      warp_store_bf16x32(t.stage, D, e.ldd, row0, t.M, col0, t.N, g, e.st_stream);
+      f4_store_bf16x32(t.stage, D, e.ldd, row0, t.M, col0, t.N, g, e.st_stream);
     }
   }
 }
@@ -356,9 +397,9 @@ template <int KIND, int CG>
 __global__ void __launch_bounds__(F4_THREADS, 1)
     coda_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
                            const __grid_constant__ CUtensorMap mB1, const GemmArgs args, const Nvfp4Scales sc) {
-  static_assert(CG == 1 || CG == 4, "cluster size");
+  static_assert(CG == 1 || CG == 2 || CG == 4, "cluster size");
   constexpr int S = F4_STAGES;
-  constexpr bool MC = CG == 4;
+  constexpr bool MC = CG > 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
@@ -434,12 +475,18 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
         const uint8_t* sf1 = args.b_dual ? sc.b1 + (static_cast<int64_t>(nb) * sc.kt + kb) * 2048
                                          : sc.b0 + (static_cast<int64_t>(2 * nb + 1) * sc.kt + kb) * 2048;
         if constexpr (MC) {
-          // quarter r of the B rows and of their 4 KB of scales, to all four CTAs
+          // piece r (of CG) of the tile's B rows and of their 4 KB of
+          // scales, to every CTA of the cluster
+          constexpr int P = F4_BN / CG;               // rows per piece
+          constexpr uint32_t PS = F4_SFB_BYTES / CG;  // scale bytes per piece
+          constexpr uint16_t ALL = (1u << CG) - 1;
           const int r = static_cast<int>(rank);
-          const CUtensorMap* mb_map = (args.b_dual && r >= 2) ? &mB1 : &mB0;
-          const int row = args.b_dual ? nb * (F4_BN / 2) + (r & 1) * 64 : nb * F4_BN + r * 64;
-          tma_load_2d_mc(sb + r * 8192, mb_map, &full[s], x, row, 0xF, el);
-          bulk_load_mc(sfb + r * 1024, (r >> 1 ? sf1 : sf0) + (r & 1) * 1024, 1024, &full[s], 0xF, el);
+          const int tr = r * P;                       // first tile row of the piece
+          const CUtensorMap* mb_map = (args.b_dual && tr >= F4_BN / 2) ? &mB1 : &mB0;
+          const int row = args.b_dual ? nb * (F4_BN / 2) + tr % (F4_BN / 2) : nb * F4_BN + tr;
+          tma_load_2d_mc(sb + tr * 128, mb_map, &full[s], x, row, ALL, el);
+          const uint32_t so = r * PS;
+          bulk_load_mc(sfb + so, (so >= 2048 ? sf1 : sf0) + so % 2048, PS, &full[s], ALL, el);
         } else {
           if (args.b_dual) {
             tma_load_2d(sb, &mB0, &full[s], x, nb * (F4_BN / 2), el);
@@ -497,7 +544,7 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
         }
         issued = true;
         if constexpr (MC)
-          umma_commit_mc(&empty[s], 0xF, el);
+          umma_commit_mc(&empty[s], static_cast<uint16_t>((1u << CG) - 1), el);
         else
           umma_commit(&empty[s], el);
       }
@@ -526,7 +573,7 @@ __global__ void __launch_bounds__(F4_THREADS, 1)
       ti.M = args.M;
       ti.N = args.N;
       ti.status = args.status;
-      ti.stage = epi_stage + (warp - 2) * 2048;
+      ti.stage = epi_stage + (warp - 2) * F4_EPI_WARP_BYTES;
       ti.taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       f4_epilogue<KIND>(args.e, ti, h, tfull, t & 1, tempty, abort_flag, args.timeout_ns, args.epilogue_sleep_ns,
                         aborted);
@@ -595,15 +642,16 @@ cudaError_t launch_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorM
 
 uint32_t nvfp4_idesc() { return idesc_nvfp4(BM, F4_BN); }
 
-// Variant: single CTAs by default; CODA_NVFP4=4 in the environment selects
-// clusters of four CTAs sharing the B tile (for comparisons) when there are
-// at least four 128-row blocks.
+// Variant: single CTAs by default; CODA_NVFP4=2 or 4 in the environment
+// selects clusters of that many CTAs sharing the B tile (for comparisons)
+// when there are at least as many 128-row blocks.
 int nvfp4_cluster_size(int64_t M) {
   static const int env = [] {
     const char* v = std::getenv("CODA_NVFP4");
-    return v ? std::atoi(v) : 1;
+    const int c = v ? std::atoi(v) : 1;
+    return c == 2 || c == 4 ? c : 1;
   }();
-  return env == 4 && M > 3 * BM ? 4 : 1;
+  return M > (env - 1) * BM ? env : 1;
 }
 
 cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Q,
@@ -618,11 +666,21 @@ cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int6
 
 cudaError_t launch_gemm_plain_nvfp4(int cg, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
                                     const GemmArgs& a, const Nvfp4Scales& sc) {
-  return cg == 4 ? launch_nvfp4<0, 4>(num_units, sms, s, m, a, sc) : launch_nvfp4<0, 1>(num_units, sms, s, m, a, sc);
+  switch (cg) {
+    case 1: return launch_nvfp4<0, 1>(num_units, sms, s, m, a, sc);
+    case 2: return launch_nvfp4<0, 2>(num_units, sms, s, m, a, sc);
+    case 4: return launch_nvfp4<0, 4>(num_units, sms, s, m, a, sc);
+    default: return cudaErrorInvalidValue;
+  }
 }
 cudaError_t launch_gemm_swiglu_nvfp4(int cg, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
                                      const GemmArgs& a, const Nvfp4Scales& sc) {
-  return cg == 4 ? launch_nvfp4<1, 4>(num_units, sms, s, m, a, sc) : launch_nvfp4<1, 1>(num_units, sms, s, m, a, sc);
+  switch (cg) {
+    case 1: return launch_nvfp4<1, 1>(num_units, sms, s, m, a, sc);
+    case 2: return launch_nvfp4<1, 2>(num_units, sms, s, m, a, sc);
+    case 4: return launch_nvfp4<1, 4>(num_units, sms, s, m, a, sc);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace coda

@@ -108,7 +108,7 @@ def test_nvfp4_special_rows(coda):
     check_quantised(coda, X, xq, sfx, sx)
 
 
-@pytest.mark.parametrize("variant", ["1", "4"])
+@pytest.mark.parametrize("variant", ["1", "2", "4"])
 def test_nvfp4_kernel_variants(variant):
     """Each kernel variant (single CTAs, or four-CTA clusters sharing the B
     tile by multicast) in a fresh process."""
