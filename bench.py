@@ -54,6 +54,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-ce", action="store_true",
                    help="skip the side measurements (linear + cross-entropy, FP8 gate/up, MLP, RMSNorm-linear)")
+    p.add_argument("--legs", default="ce,fp8,nvfp4,mlp,rms",
+                   help="side measurements to run (comma list of ce, fp8, nvfp4, mlp, rms)")
     p.add_argument("--serial", action="store_true", help="run the step's calls on one stream")
     p.add_argument("--fold-weights", action="store_true",
                    help="fold the RMSNorm gains into the weights each step instead of applying them in the "
@@ -478,7 +480,9 @@ def main():
     # Not part of the block step: the 8192 x 2048 x 128256 linear + cross-entropy
     # workload, forward and backward, timed the same way and reported beside it.
     other = {}
-    if not args.no_ce:
+    legs = set(args.legs.split(","))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    if not args.no_ce and "ce" in legs:
         from gemm_epilogue_transformer_bf16_gb300.block import LinearCE
         cs_ = synth.FULL["c4"]
         hc = synth.make_ce(cs_, seed=rank)
@@ -487,7 +491,6 @@ def main():
         for _ in range(2):
             ce.step(dc["X"], dc["W"], dc["labels"])
         torch.cuda.synchronize(dev)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         n_ce = 3
         fw, bw = [], []
         for _ in range(n_ce):
@@ -514,16 +517,18 @@ def main():
             "fwd_bwd_tflops": round(f_all / ((mf + mb) / 1e3) / 1e12, 1)}
         del ce, dc
 
-        # FP8 (e4m3) gate/up + SwiGLU at the block's shape (NEXT row: the same
-        # mainloop with kind::f8f6f4), beside the bf16 launch timed above.
+    if not args.no_ce and ("fp8" in legs or "nvfp4" in legs):
         T_, H_, I_ = s.tokens, s.hidden, s.inter
         r_ = coda.rms_rstd(t["x0"], s.eps)
-        xq, sx = coda.quantize_fp8_rows(t["x0"])
-        gq, sg = coda.quantize_fp8_rows(t["Wg"])
-        uq, su = coda.quantize_fp8_rows(t["Wu"])
         Hq = torch.empty(T_, I_, dtype=torch.bfloat16, device=dev)
         gq8, uq8 = torch.empty_like(Hq), torch.empty_like(Hq)
         ws8 = coda.workspace(256, dev)
+    if not args.no_ce and "fp8" in legs:
+        # FP8 (e4m3) gate/up + SwiGLU at the block's shape (NEXT row: the same
+        # mainloop with kind::f8f6f4), beside the bf16 launch timed above.
+        xq, sx = coda.quantize_fp8_rows(t["x0"])
+        gq, sg = coda.quantize_fp8_rows(t["Wg"])
+        uq, su = coda.quantize_fp8_rows(t["Wu"])
         f8 = []
         for i in range(5):
             ev[0].record(stream)
@@ -537,12 +542,12 @@ def main():
         m8 = statistics.median(f8)
         fp8_peak = 2 * burst
         other["fp8_gateup_swiglu"] = {
-            "workload": "e4m3 gate/up GEMM with row-scale + SwiGLU epilogue, 8192 x 2x28672 x 8192, per-row scales",
+            "workload": f"e4m3 gate/up GEMM with row-scale + SwiGLU epilogue, {T_} x 2x{I_} x {H_}, per-row scales",
             "ms": round(m8, 3), "tflops": round(gf[DOMINANT] / (m8 / 1e3) / 1e12, 1),
             "peak": round(fp8_peak, 1), "peak_kind": f"fp8 = 2 x bf16 burst ({peak_src}, nominal ratio)",
             "frac": round(gf[DOMINANT] / (m8 / 1e3) / 1e12 / fp8_peak, 4)}
         del xq, gq, uq
-
+    if not args.no_ce and "nvfp4" in legs:
         # NVFP4 (e2m1 + e4m3 block scales) gate/up + SwiGLU at the same shape:
         # the block-scaled kind::mxf4nvf4 mainloop, single CTAs.
         fq = []
@@ -565,29 +570,32 @@ def main():
         m4 = statistics.median(g for _, g in fq)
         fp4_peak = 6 * burst
         other["nvfp4_gateup_swiglu"] = {
-            "workload": "NVFP4 gate/up GEMM (e2m1, e4m3 scale per 16, fp32 row scale) with row-scale + SwiGLU "
-                        "epilogue, 8192 x 2x28672 x 8192, single-CTA tiles",
+            "workload": f"NVFP4 gate/up GEMM (e2m1, e4m3 scale per 16, fp32 row scale) with row-scale + SwiGLU "
+                        f"epilogue, {T_} x 2x{I_} x {H_}, single-CTA tiles",
             "ms": round(m4, 3), "tflops": round(gf[DOMINANT] / (m4 / 1e3) / 1e12, 1),
             "peak": round(fp4_peak, 1), "peak_kind": f"fp4 = 6 x bf16 burst ({peak_src}, nominal ratio)",
             "frac": round(gf[DOMINANT] / (m4 / 1e3) / 1e12 / fp4_peak, 4),
             "quantize_x_ms": round(mq4, 3)}
-        del xq4, gq4, uq4, sfx4, sfg4, sfu4, Hq, gq8, uq8
+        del xq4, gq4, uq4, sfx4, sfg4, sfu4
+    if not args.no_ce and ("fp8" in legs or "nvfp4" in legs):
+        del Hq, gq8, uq8
 
-        # Configs 3 and 2 (also parity workloads), forward + backward, timed the
-        # same way: the SwiGLU MLP at hidden 4096 and the RMSNorm-reparameterised
-        # projection + residual of config 2 (gain folded into W: the standalone
-        # operator's form).  FLOPs 2*M*N*K per GEMM.
-        def time_calls(fn, n=5, warm=2):
-            for _ in range(warm):
-                fn()
-            torch.cuda.synchronize(dev)
-            ev[0].record(stream)
-            for _ in range(n):
-                fn()
-            ev[1].record(stream)
-            torch.cuda.synchronize(dev)
-            return ev[0].elapsed_time(ev[1]) / n
+    # Configs 3 and 2 (also parity workloads), forward + backward, timed the
+    # same way: the SwiGLU MLP at hidden 4096 and the RMSNorm-reparameterised
+    # projection + residual of config 2 (gain folded into W: the standalone
+    # operator's form).  FLOPs 2*M*N*K per GEMM.
+    def time_calls(fn, n=5, warm=2):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize(dev)
+        ev[0].record(stream)
+        for _ in range(n):
+            fn()
+        ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        return ev[0].elapsed_time(ev[1]) / n
 
+    if not args.no_ce and "mlp" in legs:
         s3 = synth.FULL["c3"]
         d3 = {k: v.to(dev) for k, v in synth.make_mlp(s3, seed=rank).items()}
         ws3 = coda.workspace(max(coda.load().coda_linear_swiglu_bwd_workspace_size(s3.tokens, s3.inter, s3.hidden),
@@ -605,6 +613,7 @@ def main():
             "ms": round(m3, 3), "tflops": round(f3 / (m3 / 1e3) / 1e12, 1),
             "frac_of_sustained": round(f3 / (m3 / 1e3) / 1e12 / sustained, 4)}
         del d3, o3, ws3
+    if not args.no_ce and "rms" in legs:
         s2 = synth.FULL["c2"]
         d2 = {k: v.to(dev) for k, v in synth.make_rms_linear(s2, seed=rank).items()}
 
