@@ -93,6 +93,20 @@ bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int
   return r == CUDA_SUCCESS;
 }
 
+// A 2-D byte tensor map without swizzling (rows of `cols` bytes), for data
+// that is not a matrix operand (the NVFP4 block scales).
+bool encode_map_plain(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, uint32_t box_cols,
+                      uint32_t box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // One GEMM + epilogue launch.
 struct Plan {
   coda::EpiKind kind = coda::EpiKind::Plain;
@@ -1308,6 +1322,43 @@ int run_nvfp4(coda::EpiKind kind, const uint8_t* A, const uint8_t* B0, const uin
   if (!get_encoder()) return CODA_ERR_CUDA;
   const int sms = num_sms();
   if (sms <= 0) return CODA_ERR_CUDA;
+  if (coda::nvfp4_pairs(M)) {
+    // CTA pairs: each CTA copies its own 128 rows of A and of B; the block
+    // scales through byte maps of 256-byte rows (an 8-row box = one 2 KB group)
+    CUtensorMap maps[6];
+    std::memset(maps, 0, sizeof(maps));
+    const int64_t kbytes = K / 2;
+    auto sf_map = [&](CUtensorMap* m, const uint8_t* sf, int64_t rows) {
+      const int64_t bytes = static_cast<int64_t>(coda_nvfp4_scale_bytes(rows, K));
+      return encode_map_plain(m, sf, bytes / 256, 256, 256, 8);
+    };
+    if (!encode_map(&maps[0], A, M, kbytes, kbytes, 128, coda::BM, 1)) return CODA_ERR_CUDA;
+    if (!encode_map(&maps[1], B0, N, kbytes, kbytes, 128, BN / 2, 1)) return CODA_ERR_CUDA;
+    if (!encode_map(&maps[2], b_dual ? B1 : B0, N, kbytes, kbytes, 128, BN / 2, 1)) return CODA_ERR_CUDA;
+    if (!sf_map(&maps[3], sc.a, M)) return CODA_ERR_CUDA;
+    if (!sf_map(&maps[4], sc.b0, N)) return CODA_ERR_CUDA;
+    if (!sf_map(&maps[5], b_dual ? sc.b1 : sc.b0, N)) return CODA_ERR_CUDA;
+    GemmArgs a{};
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.num_m = static_cast<int>(cdiv(M, 2 * coda::BM));
+    a.num_n = static_cast<int>(cdiv(N, b_dual ? BN / 2 : BN));
+    a.kb0 = static_cast<int>(cdiv(K, 256));
+    a.b_dual = b_dual;
+    a.n_per_unit = 1;
+    a.num_units = a.num_m * a.num_n;
+    a.group_m = group_m(2);
+    a.idesc = coda::nvfp4_idesc_pair();
+    a.status = status;
+    a.timeout_ns = TIMEOUT_NS;
+    wait_sleep(a.producer_sleep_ns, a.epilogue_sleep_ns);
+    a.e = e;
+    a.e.st_stream = (l2_hints() & 4) ? 1 : 0;
+    sc.kt = cdiv(K, 256);
+    const cudaError_t err = coda::launch_gemm_nvfp4_pair(kind == coda::EpiKind::Swiglu ? 1 : 0, a.num_units, sms,
+                                                         s, maps, a, sc);
+    return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
+  }
   const int cg = coda::nvfp4_cluster_size(M);
   // rows of one B copy: the whole tile (256, or 128 per weight when dual),
   // or a quarter of it when four CTAs share the tile

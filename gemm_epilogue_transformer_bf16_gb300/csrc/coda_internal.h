@@ -52,6 +52,13 @@ uint32_t nvfp4_idesc();
 // (CTAs sharing B; each copies 256 / cg rows of the B tile, so the B tensor
 // maps must have boxes of that many rows).
 int nvfp4_cluster_size(int64_t M);
+// CTA pairs (cta_group::2, 256 x 256 tiles) for M rows; then the tensor maps
+// are A, B0, B1 with 128-row boxes and the block scales of A, B0, B1 as 2-D
+// byte maps [bytes / 256, 256] with 8-row boxes (one 2 KB group).
+bool nvfp4_pairs(int64_t M);
+uint32_t nvfp4_idesc_pair();
+cudaError_t launch_gemm_nvfp4_pair(int kind, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
+                                   const GemmArgs& a, const Nvfp4Scales& sc);
 cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Q,
                                        uint8_t* SF, float* scale, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm_plain_nvfp4(int cg, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,

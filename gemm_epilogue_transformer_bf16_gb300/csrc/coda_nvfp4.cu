@@ -33,6 +33,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 #include <utility>
@@ -291,7 +292,7 @@ __device__ __forceinline__ void f4_store_bf16x32(uint8_t* stage, __nv_bfloat16* 
 //           H = silu(g) * u, columns nb*128 + h*64 + [0, 64)
 //   (rs = token scale x optional RMSNorm row factor; cs, cg, cu the
 //   weights' row scales), as EpiPlain / EpiSwiglu do for the other kernels.
-template <int KIND>
+template <int KIND, bool PAIR = false>
 __device__ __forceinline__ void f4_epilogue(const EpiArgs& e, const TileInfo& t, int h, uint64_t* tfull,
                                             uint32_t parity, uint64_t* tempty, volatile int* abort_flag,
                                             uint64_t timeout_ns, uint32_t sleep_ns, bool& aborted) {
@@ -314,7 +315,12 @@ __device__ __forceinline__ void f4_epilogue(const EpiArgs& e, const TileInfo& t,
   }
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive(tempty);
+  if (lane == 0) {
+    if constexpr (PAIR)
+      mbar_arrive_cluster(mapa_shared(tempty, 0));  // the pair's accumulator barrier is in the even CTA
+    else
+      mbar_arrive(tempty);
+  }
   auto* D = static_cast<__nv_bfloat16*>(e.D);
   if constexpr (KIND == 0) {
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
@@ -638,9 +644,302 @@ cudaError_t launch_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorM
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ CTA pairs
+// The same GEMM on CTA pairs (tcgen05 cta_group::2): a cluster of two CTAs on
+// adjacent 128-row blocks computes a 256 x 256 tile; each CTA stages its own
+// 128 rows of A and its own 128 of the 256 B rows (the MMA reads the other
+// half from the peer), its rows' block scales, and the scales of all 256 B
+// rows (each CTA loads one half and multicasts it to both).  The scales
+// travel through 2-D tensor maps (rows of 256 bytes, 8-row boxes = one 2 KB
+// group), so that both CTAs' copies complete on the leader's barrier.  The
+// leader (even CTA) moves the scales into TMEM with tcgen05.cp.cta_group::2
+// (each CTA from its own shared memory into its own TMEM) and issues the
+// MMAs; both CTAs run the epilogue on their own 128 rows.  A stage is 38 KB
+// (five fit) for the same tensor work per CTA as a 54 KB single-CTA stage.
+constexpr uint32_t P4_A_BYTES = BM * 128;
+constexpr uint32_t P4_B_BYTES = (F4_BN / 2) * 128;
+constexpr uint32_t P4_SFA_BYTES = 2048;
+constexpr uint32_t P4_SFB_BYTES = 4096;
+constexpr uint32_t P4_STAGE_BYTES = P4_A_BYTES + P4_B_BYTES + P4_SFA_BYTES + P4_SFB_BYTES;
+constexpr int P4_STAGES = 5;
+constexpr uint32_t P4_SF_SLOT_COLS = 48;
+constexpr uint32_t P4_SMEM = 1024 + P4_STAGES * P4_STAGE_BYTES + F4_BAR_BYTES + F4_EPI_BYTES;
+// bytes landing per stage, counted on the leader's barrier: A, B and A's
+// scales from both CTAs, and both 2 KB halves of B's scales in both CTAs
+constexpr uint32_t P4_TX = 2 * (P4_A_BYTES + P4_B_BYTES + P4_SFA_BYTES) + 2 * P4_SFB_BYTES;
+static_assert(P4_STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
+static_assert(P4_SMEM <= 232448, "shared memory per CTA");
+static_assert(F4_SF_COL0 + P4_STAGES * P4_SF_SLOT_COLS <= F4_TMEM_COLS, "TMEM columns");
+
+__device__ __forceinline__ void tmem_cp_32x128_x4_pair(uint32_t taddr, uint64_t sdesc, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %2, 0;\n\t"
+      "@P tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(sdesc), "r"(p)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_nvfp4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate,
+                                                uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred A, P;\n\t"
+      "setp.ne.b32 A, %6, 0;\n\t"
+      "setp.ne.b32 P, %7, 0;\n\t"
+      "@P tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], A;\n\t}" ::
+          "r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(p)
+      : "memory");
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(F4_THREADS, 1)
+    coda_gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
+                                const __grid_constant__ CUtensorMap mB1, const __grid_constant__ CUtensorMap mSA,
+                                const __grid_constant__ CUtensorMap mSB0, const __grid_constant__ CUtensorMap mSB1,
+                                const GemmArgs args, const Nvfp4Scales sc) {
+  constexpr int S = P4_STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * P4_STAGE_BYTES);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* epi_stage = smem + S * P4_STAGE_BYTES + F4_BAR_BYTES;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 2 * F4_EW);  // every epilogue warp of both CTAs
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mA);
+    tma_prefetch_desc(&mB0);
+    tma_prefetch_desc(&mSA);
+    tma_prefetch_desc(&mSB0);
+    if (args.b_dual) {
+      tma_prefetch_desc(&mB1);
+      tma_prefetch_desc(&mSB1);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc<true>(tmem_slot, F4_TMEM_COLS);
+    tmem_relinquish<true>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the leader's barriers are initialised before the peer signals them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_kb = args.kb0;
+  const int cluster_id = static_cast<int>(blockIdx.x) / 2;
+  const int num_clusters = static_cast<int>(gridDim.x) / 2;
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    const uint32_t el = elect_one();
+    uint32_t it = 0;
+    for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters) {
+      int mbc, nb, nlen, chunk;
+      unit_coords(args, u, mbc, nb, nlen, chunk);
+      const int mb = mbc * 2 + static_cast<int>(rank);
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % S;
+        if (!mbar_wait_bounded(&empty[s], ((it / S) & 1) ^ 1, abort_flag, args.status, args.timeout_ns,
+                               args.producer_sleep_ns)) {
+          aborted = true;
+          break;
+        }
+        if (leader) mbar_arrive_expect_tx(&full[s], P4_TX, el);
+        const uint32_t bar = mapa_shared(&full[s], 0);
+        uint8_t* sa = tiles + s * P4_STAGE_BYTES;
+        uint8_t* sb = sa + P4_A_BYTES;
+        uint8_t* sfa = sb + P4_B_BYTES;
+        uint8_t* sfb = sfa + P4_SFA_BYTES;
+        const int x = kb * 128;
+        tma_load_2d_pair(sa, &mA, bar, x, mb * BM, el);
+        if (args.b_dual)
+          tma_load_2d_pair(sb, rank ? &mB1 : &mB0, bar, x, nb * (F4_BN / 2), el);
+        else
+          tma_load_2d_pair(sb, &mB0, bar, x, nb * F4_BN + static_cast<int>(rank) * (F4_BN / 2), el);
+        tma_load_2d_pair(sfa, &mSA, bar, 0, 8 * (mb * static_cast<int>(sc.kt) + kb), el);
+        // B's scales: this CTA loads the group of its own B rows into slot
+        // `rank` of both CTAs' scale area
+        const int cb = args.b_dual ? nb * static_cast<int>(sc.kt) + kb
+                                   : (2 * nb + static_cast<int>(rank)) * static_cast<int>(sc.kt) + kb;
+        tma_load_2d_pair_mc(sfb + rank * 2048, (args.b_dual && rank) ? &mSB1 : &mSB0, bar, 0, 8 * cb, 0x3, el);
+      }
+    }
+    if (aborted) {
+      if (leader) {
+        const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
+        for (uint32_t j = first; j < it; ++j) mbar_wait_drain(&full[j % S], (j / S) & 1, 200000000ull);
+      } else {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ scale copies + MMA issuer (leader)
+    if (leader) {
+      const uint32_t el = elect_one();
+      uint32_t it = 0, t = 0;
+      bool issued = false;
+      const uint32_t idesc = args.idesc;
+      for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters, ++t) {
+        if (!mbar_wait_bounded(tempty, (t & 1) ^ 1, abort_flag, args.status, args.timeout_ns)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % S;
+          if (!mbar_wait_bounded(&full[s], (it / S) & 1, abort_flag, args.status, args.timeout_ns)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(tiles + s * P4_STAGE_BYTES);
+          const uint32_t sb = sa + P4_A_BYTES;
+          const uint32_t sfa = sb + P4_B_BYTES;
+          const uint32_t sfb = sfa + P4_SFA_BYTES;
+          const uint32_t slot = tmem_base + F4_SF_COL0 + static_cast<uint32_t>(s) * P4_SF_SLOT_COLS;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            tmem_cp_32x128_x4_pair(slot + g * 4, sdesc_plain(sfa + g * 512, 128, 128), el);
+            tmem_cp_32x128_x4_pair(slot + 16 + g * 8, sdesc_plain(sfb + g * 512, 128, 128), el);
+            tmem_cp_32x128_x4_pair(slot + 16 + g * 8 + 4, sdesc_plain(sfb + 2048 + g * 512, 128, 128), el);
+          }
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint64_t ad = sdesc_sw128(sa + g * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sb + g * 32, 16, 1024);
+            umma_nvfp4_pair(tmem_base, ad, bd, idesc, slot + g * 4, slot + 16 + g * 8, (kb | g) != 0, el);
+          }
+          issued = true;
+          umma_commit_pair_mc(&empty[s], 0x3, el);
+        }
+        if (aborted) break;
+        umma_commit_pair_mc(tfull, 0x3, el);
+      }
+      if (aborted && issued) {
+        umma_commit_pair(drain, el);
+        mbar_wait_drain(drain, 0, 200000000ull);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    uint32_t t = 0;
+    for (int u = cluster_id; u < args.num_units && !aborted; u += num_clusters, ++t) {
+      int mbc, nb, nlen, chunk;
+      unit_coords(args, u, mbc, nb, nlen, chunk);
+      const int mb = mbc * 2 + static_cast<int>(rank);
+      TileInfo ti;
+      ti.mb = mb;
+      ti.nb = nb;
+      ti.unit_chunk = chunk;
+      ti.row = mb * BM + q * 32 + lane;
+      ti.M = args.M;
+      ti.N = args.N;
+      ti.status = args.status;
+      ti.stage = epi_stage + (warp - 2) * F4_EPI_WARP_BYTES;
+      ti.taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      f4_epilogue<KIND, true>(args.e, ti, h, tfull, t & 1, tempty, abort_flag, args.timeout_ns,
+                              args.epilogue_sleep_ns, aborted);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still write or signal it
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc<true>(tmem_base, F4_TMEM_COLS);
+  }
+}
+
+template <int KIND>
+cudaError_t launch_nvfp4_pair(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a,
+                              const Nvfp4Scales& sc) {
+  static std::mutex init;
+  static std::atomic<bool> attr_done[64];
+  static std::atomic<int> max_clusters[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  auto kern = coda_gemm_nvfp4_pair_kernel<KIND>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(F4_THREADS);
+  cfg.dynamicSmemBytes = P4_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(init);
+    if (!attr_done[dev].load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P4_SMEM));
+      if (e != cudaSuccess) return e;
+      cfg.gridDim = dim3(static_cast<unsigned>(sms - sms % 2));
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n <= 0) return cudaErrorInvalidConfiguration;
+      max_clusters[dev].store(n, std::memory_order_relaxed);
+      attr_done[dev].store(true, std::memory_order_release);
+    }
+  }
+  const int resident = max_clusters[dev].load(std::memory_order_relaxed);
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(num_units, resident)));
+  e = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], m[4], m[5], a, sc);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 uint32_t nvfp4_idesc() { return idesc_nvfp4(BM, F4_BN); }
+uint32_t nvfp4_idesc_pair() { return idesc_nvfp4(2 * BM, F4_BN); }
+
+// CTA pairs: CODA_NVFP4=pair in the environment selects them when there are
+// at least two 128-row blocks.
+bool nvfp4_pairs(int64_t M) {
+  static const bool env = [] {
+    const char* v = std::getenv("CODA_NVFP4");
+    return v && std::strcmp(v, "pair") == 0;
+  }();
+  return env && M > BM;
+}
+
+cudaError_t launch_gemm_nvfp4_pair(int kind, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
+                                   const GemmArgs& a, const Nvfp4Scales& sc) {
+  return kind == 1 ? launch_nvfp4_pair<1>(num_units, sms, s, m, a, sc)
+                   : launch_nvfp4_pair<0>(num_units, sms, s, m, a, sc);
+}
 
 // Variant: single CTAs by default; CODA_NVFP4=2 or 4 in the environment
 // selects clusters of that many CTAs sharing the B tile (for comparisons)

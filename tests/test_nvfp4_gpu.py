@@ -108,10 +108,10 @@ def test_nvfp4_special_rows(coda):
     check_quantised(coda, X, xq, sfx, sx)
 
 
-@pytest.mark.parametrize("variant", ["1", "2", "4"])
+@pytest.mark.parametrize("variant", ["1", "2", "4", "pair"])
 def test_nvfp4_kernel_variants(variant):
-    """Each kernel variant (single CTAs, or four-CTA clusters sharing the B
-    tile by multicast) in a fresh process."""
+    """Each kernel variant (single CTAs, clusters of 2 or 4 CTAs sharing the
+    B tile by multicast, CTA pairs) in a fresh process."""
     import os
     import subprocess
     import sys
