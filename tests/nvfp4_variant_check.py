@@ -38,6 +38,16 @@ def main():
     torch.cuda.synchronize()
     assert coda.get_status(ws) == 0
     assert_bf16(Y, O.linear_nvfp4_fwd(*xo, *wo, R=to_np(R)), "nvfp4 Y")
+    # more tiles than resident CTAs or clusters: each works through several
+    M, N, K = 4096, 2048, 256
+    X = synth.randn_bf16((M, K), 1.0, 27)
+    W = synth.randn_bf16((N, K), 1 / math.sqrt(K), 28)
+    xd, xo = quant(X)
+    wd, wo = quant(W)
+    Y = coda.linear_nvfp4(*xd, *wd, ws=ws)
+    torch.cuda.synchronize()
+    assert coda.get_status(ws) == 0
+    assert_bf16(Y, O.linear_nvfp4_fwd(*xo, *wo), "nvfp4 Y, several tiles per CTA")
     M, I, K = 700, 392, 512
     X = synth.randn_bf16((M, K), 1.0, 24)
     Wg = synth.randn_bf16((I, K), 1 / math.sqrt(K), 25)
