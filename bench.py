@@ -248,7 +248,7 @@ def oracle_sample_timing(tokens, p):
     oracle_inputs: block_fwd + block_bwd.  Returns (TFLOP/s, seconds, flops)."""
     from oracle import coda_oracle as O
     import synth
-    s = synth.FULL["c5"]
+    s = synth.FULL["block"]
     cfg = dict(n_q=s.n_q, n_kv=s.n_kv, head_dim=s.head_dim, theta=s.theta, eps=s.eps)
     t0 = time.perf_counter()
     O.block_fwd(p, **cfg)
@@ -272,7 +272,7 @@ def run_reference(args):
         return 0
     import torch
     import synth
-    s = synth.FULL["c5"]
+    s = synth.FULL["block"]
     host = synth.make_block(s, seed=0)
     torch.set_num_threads(cores())
     p = oracle_inputs(host, args.cpu_tokens)
@@ -314,7 +314,7 @@ def main():
     dev = torch.device("cuda", local)
     coda.load()
     import dataclasses
-    s = dataclasses.replace(synth.FULL["c5"], tokens=args.tokens)
+    s = dataclasses.replace(synth.FULL["block"], tokens=args.tokens)
     host = synth.make_block(s, seed=rank)          # replicas: each rank its own seeded batch
     t = {k: v.to(dev) for k, v in host.items()}
     blk = Block(s, t, device=dev, concurrent=not args.serial, fold_weights=args.fold_weights)
@@ -484,7 +484,7 @@ def main():
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     if not args.no_ce and "ce" in legs:
         from gemm_epilogue_transformer_bf16_gb300.block import LinearCE
-        cs_ = synth.FULL["c4"]
+        cs_ = synth.FULL["linear_ce"]
         hc = synth.make_ce(cs_, seed=rank)
         dc = {k: v.to(dev) for k, v in hc.items()}
         ce = LinearCE(cs_.tokens, cs_.vocab, cs_.hidden, device=dev)
@@ -580,9 +580,9 @@ def main():
     if not args.no_ce and ("fp8" in legs or "nvfp4" in legs):
         del Hq, gq8, uq8
 
-    # Configs 3 and 2 (also parity workloads), forward + backward, timed the
+    # Two more workloads (also parity workloads), forward + backward, timed the
     # same way: the SwiGLU MLP at hidden 4096 and the RMSNorm-reparameterised
-    # projection + residual of config 2 (gain folded into W: the standalone
+    # projection + residual at 4096 x 2048 (gain folded into W: the standalone
     # operator's form).  FLOPs 2*M*N*K per GEMM.
     def time_calls(fn, n=5, warm=2):
         for _ in range(warm):
@@ -596,7 +596,7 @@ def main():
         return ev[0].elapsed_time(ev[1]) / n
 
     if not args.no_ce and "mlp" in legs:
-        s3 = synth.FULL["c3"]
+        s3 = synth.FULL["mlp"]
         d3 = {k: v.to(dev) for k, v in synth.make_mlp(s3, seed=rank).items()}
         ws3 = coda.workspace(max(coda.load().coda_linear_swiglu_bwd_workspace_size(s3.tokens, s3.inter, s3.hidden),
                                  coda.load().coda_linear_residual_workspace_size(s3.tokens, s3.hidden, s3.inter)), dev)
@@ -614,7 +614,7 @@ def main():
             "frac_of_sustained": round(f3 / (m3 / 1e3) / 1e12 / sustained, 4)}
         del d3, o3, ws3
     if not args.no_ce and "rms" in legs:
-        s2 = synth.FULL["c2"]
+        s2 = synth.FULL["rmsnorm_linear"]
         d2 = {k: v.to(dev) for k, v in synth.make_rms_linear(s2, seed=rank).items()}
 
         def rms_step():
@@ -632,7 +632,7 @@ def main():
 
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.tokens == synth.FULL["c5"].tokens:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.tokens == synth.FULL["block"].tokens:
         torch.set_num_threads(cores())
         v, dt, fl = oracle_sample_timing(args.cpu_tokens, oracle_inputs(host, args.cpu_tokens))
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",

@@ -118,7 +118,7 @@ def rmsnorm_bwd(x, gamma, eps, dy):
 
 
 # ---------------------------------------------------------------------------
-# RMSNorm followed by a projection (+ residual), workload 2
+# RMSNorm followed by a projection (+ residual)
 # ---------------------------------------------------------------------------
 
 def rmsnorm_linear_fwd(X, gamma, W, eps, R=None):
@@ -217,7 +217,7 @@ def mlp_bwd(X, Wg, Wu, Wd, dY, gamma=None, eps=1e-6):
 
 
 # ---------------------------------------------------------------------------
-# QK-RMSNorm + RoPE, workload 5
+# QK-RMSNorm + RoPE
 # ---------------------------------------------------------------------------
 
 def rope_angles(pos, head_dim, theta):
@@ -260,7 +260,7 @@ def qk_rmsnorm_rope_bwd(q, gamma, pos, theta, eps, dout):
 
 
 # ---------------------------------------------------------------------------
-# linear + cross-entropy, workload 4
+# linear + cross-entropy
 # ---------------------------------------------------------------------------
 
 def _lse(z):
@@ -488,7 +488,7 @@ def rmsnorm_linear_cross_entropy_bwd(X, gamma, W, labels, eps, ignore_index=-100
 
 
 # ---------------------------------------------------------------------------
-# the non-attention transformer block, workload 5
+# the non-attention transformer block
 # ---------------------------------------------------------------------------
 
 def _heads(t, n, d):

@@ -66,14 +66,14 @@ def positions_i32(tokens, seq_len):
 # --------------------------------------------------------------------------
 
 @dataclass(frozen=True)
-class SwigluShape:            # workload 1: linear + SwiGLU forward
+class SwigluShape:            # linear + SwiGLU forward, 256 x 512 -> 1024
     tokens: int = 256
     hidden: int = 512
     inter: int = 1024
 
 
 @dataclass(frozen=True)
-class RmsLinearShape:         # workload 2: RMSNorm-reparam projection + residual
+class RmsLinearShape:         # RMSNorm-reparameterised projection + residual, 4096 x 2048 -> 2048
     tokens: int = 4096
     hidden: int = 2048
     out: int = 2048
@@ -81,14 +81,14 @@ class RmsLinearShape:         # workload 2: RMSNorm-reparam projection + residua
 
 
 @dataclass(frozen=True)
-class MlpShape:               # workload 3: SwiGLU MLP fwd+bwd
+class MlpShape:               # SwiGLU MLP fwd+bwd, 8192 x 4096, intermediate 11008
     tokens: int = 8192
     hidden: int = 4096
     inter: int = 11008
 
 
 @dataclass(frozen=True)
-class CeShape:                # workload 4: linear + cross-entropy
+class CeShape:                # linear + cross-entropy, 8192 x 2048, vocabulary 128256
     tokens: int = 8192
     hidden: int = 2048
     vocab: int = 128256
@@ -97,7 +97,7 @@ class CeShape:                # workload 4: linear + cross-entropy
 
 
 @dataclass(frozen=True)
-class BlockShape:             # workload 5: non-attention block fwd+bwd
+class BlockShape:             # non-attention block fwd+bwd, 8192 tokens, hidden 8192
     tokens: int = 8192
     hidden: int = 8192
     n_q: int = 64
@@ -114,11 +114,11 @@ class BlockShape:             # workload 5: non-attention block fwd+bwd
 
 
 FULL = {
-    "c1": SwigluShape(),
-    "c2": RmsLinearShape(),
-    "c3": MlpShape(),
-    "c4": CeShape(),
-    "c5": BlockShape(),
+    "swiglu": SwigluShape(),
+    "rmsnorm_linear": RmsLinearShape(),
+    "mlp": MlpShape(),
+    "linear_ce": CeShape(),
+    "block": BlockShape(),
 }
 
 

@@ -1,5 +1,7 @@
-"""Full-size parity on the BASELINE workloads (configs 3, 4 and 5; config 2
-runs in full in test_ops_gpu.py), in the launch configuration bench.py times.
+"""Full-size parity on the benchmark workloads (the SwiGLU MLP at hidden 4096,
+linear + cross-entropy at vocabulary 128256, the block at hidden 8192 and the
+FP8 / NVFP4 gate/up legs at its shape; the RMSNorm-linear workload runs in
+full in test_ops_gpu.py), in the launch configuration bench.py times.
 
 The fp64 oracle cannot evaluate these workloads whole in a test's time, so it
 is evaluated exactly on samples:
@@ -58,9 +60,9 @@ def _gamma_property(dgamma, gamma, pairs, name):
     assert_bf16(lhs, rhs, name)
 
 
-# ---------------------------------------------------------------- config 3
+# ---------------------------------------------------------------- SwiGLU MLP, hidden 4096
 def test_mlp_fullsize(coda):
-    s = synth.FULL["c3"]
+    s = synth.FULL["mlp"]
     t = synth.make_mlp(s, seed=0)
     d = {k: v.to(DEV) for k, v in t.items()}
     H, g, u = coda.linear_swiglu(d["X"], d["Wg"], d["Wu"])
@@ -81,9 +83,9 @@ def test_mlp_fullsize(coda):
     assert_bf16(_at(gr["dWd"], iu, 1), bu["dWd"], "dWd sampled units")
 
 
-# ---------------------------------------------------------------- config 4
+# ---------------------------------------------------------------- linear + cross-entropy, vocabulary 128256
 def test_cross_entropy_fullsize(coda):
-    s = synth.FULL["c4"]
+    s = synth.FULL["linear_ce"]
     t = synth.make_ce(s, seed=0)
     d = {k: v.to(DEV) for k, v in t.items()}
     out = coda.linear_cross_entropy(d["X"], d["W"], d["labels"])
@@ -112,10 +114,10 @@ def test_cross_entropy_fullsize(coda):
     assert float(np.max(np.abs(colsum) / scale)) < 3e-2, "columns of dW do not sum to ~0"
 
 
-# ---------------------------------------------------------------- config 5 (bench workload)
+# ---------------------------------------------------------------- block, hidden 8192 (the bench workload)
 def test_block_fullsize(coda):
     from gemm_epilogue_transformer_bf16_gb300.block import Block
-    s = synth.FULL["c5"]
+    s = synth.FULL["block"]
     t = synth.make_block(s, seed=0)
     d = {k: v.to(DEV) for k, v in t.items()}
     blk = Block(s, d)
@@ -146,3 +148,60 @@ def test_block_fullsize(coda):
                     "dgamma_mlp * gamma vs sum W dW")
     _gamma_property(gr["dgamma_attn"], t["gamma_attn"], [(t["Wqkv"], gr["dWqkv"])],
                     "dgamma_attn * gamma vs sum W dW")
+
+
+# ---------------------------------------------------------------- low-precision gate/up legs (bench shape)
+def _gateup_inputs():
+    s = synth.FULL["block"]
+    t = synth.make_block(s, seed=0)
+    return s, t["x0"], t["Wg"], t["Wu"]
+
+
+def test_fp8_gateup_fullsize(coda):
+    """e4m3 gate/up + SwiGLU at the bench's shape (8192 x 2x28672 x 8192):
+    quantisation is per row, so the oracle's codes for sampled token rows and
+    sampled weight rows are exact, and so are the outputs at those entries."""
+    s, x, Wg, Wu = _gateup_inputs()
+    xq, sx = coda.quantize_fp8_rows(x.to(DEV))
+    gq, sg = coda.quantize_fp8_rows(Wg.to(DEV))
+    uq, su = coda.quantize_fp8_rows(Wu.to(DEV))
+    H, g, u = coda.linear_swiglu_fp8(xq, sx, gq, sg, uq, su)
+    torch.cuda.synchronize()
+    rows = synth.sample_rows(s.tokens, N_ROWS).numpy()
+    iu = _units(s.inter, 8 * N_UNITS, 11)
+    ocx, ovx, osx = O.quantize_fp8_rows(to_np(x)[rows])
+    ocg, ovg, osg = O.quantize_fp8_rows(to_np(Wg)[iu])
+    ocu, ovu, osu = O.quantize_fp8_rows(to_np(Wu)[iu])
+    assert np.array_equal(_at(xq, rows).numpy(), ocx) and np.array_equal(_at(gq, iu).numpy(), ocg)
+    assert np.array_equal(_at(uq, iu).numpy(), ocu) and np.array_equal(_at(sx, rows).numpy(), osx)
+    Hr, gr, ur = O.swiglu_fp8_fwd(ovx, osx, ovg, osg, ovu, osu)
+    for name, got, ref in (("H", H, Hr), ("g", g, gr), ("u", u, ur)):
+        assert_bf16(_at(_at(got, rows), iu, 1), ref, f"fp8 {name} sampled rows x units")
+
+
+def test_nvfp4_gateup_fullsize(coda):
+    """NVFP4 gate/up + SwiGLU at the bench's shape, checked the same way:
+    codes and row scales of sampled rows bit for bit, outputs at sampled
+    (token, unit) entries against the oracle on the dequantised operands."""
+    s, x, Wg, Wu = _gateup_inputs()
+    xq, sfx, sx = coda.quantize_nvfp4_rows(x.to(DEV))
+    gq, sfg, sg = coda.quantize_nvfp4_rows(Wg.to(DEV))
+    uq, sfu, su = coda.quantize_nvfp4_rows(Wu.to(DEV))
+    H, g, u = coda.linear_swiglu_nvfp4(xq, sfx, sx, gq, sfg, sg, uq, sfu, su)
+    torch.cuda.synchronize()
+    rows = synth.sample_rows(s.tokens, N_ROWS).numpy()
+    iu = _units(s.inter, 8 * N_UNITS, 12)
+
+    def unpack(q):
+        q = q.numpy()
+        out = np.empty((q.shape[0], 2 * q.shape[1]), np.uint8)
+        out[:, 0::2], out[:, 1::2] = q & 0xF, q >> 4
+        return out
+    cx, _, osx, ovx = O.quantize_nvfp4_rows(to_np(x)[rows])
+    cg, _, osg, ovg = O.quantize_nvfp4_rows(to_np(Wg)[iu])
+    cu, _, osu, ovu = O.quantize_nvfp4_rows(to_np(Wu)[iu])
+    assert np.array_equal(unpack(_at(xq, rows)), cx) and np.array_equal(unpack(_at(gq, iu)), cg)
+    assert np.array_equal(unpack(_at(uq, iu)), cu) and np.array_equal(_at(sx, rows).numpy(), osx)
+    Hr, gr, ur = O.swiglu_nvfp4_fwd(ovx, osx, ovg, osg, ovu, osu)
+    for name, got, ref in (("H", H, Hr), ("g", g, gr), ("u", u, ur)):
+        assert_bf16(_at(_at(got, rows), iu, 1), ref, f"nvfp4 {name} sampled rows x units")

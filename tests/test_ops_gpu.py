@@ -32,7 +32,7 @@ def f64(d):
     return {k: to_np(v) for k, v in d.items()}
 
 
-# ---------------------------------------------------------------- workload 1
+# ---------------------------------------------------------------- linear + SwiGLU
 @pytest.mark.parametrize("shape", [synth.SwigluShape(), synth.SwigluShape(200, 136, 264)])
 def test_linear_swiglu(coda, shape):
     t = synth.make_swiglu(shape, seed=0)
@@ -44,7 +44,7 @@ def test_linear_swiglu(coda, shape):
     assert_bf16(u, ur, "u")
 
 
-# ---------------------------------------------------------------- workload 2
+# ---------------------------------------------------------------- RMSNorm-reparameterised projection
 @pytest.mark.parametrize("shape", [synth.RmsLinearShape(), synth.RmsLinearShape(300, 264, 200)])
 def test_rmsnorm_linear_fwd_bwd(coda, shape):
     t = synth.make_rms_linear(shape, seed=0)
@@ -135,7 +135,7 @@ def test_linear_residual_partial_rms(coda, M, N, K):
     assert_bf16(g["dW"], b["dW"], "dW")
 
 
-# ---------------------------------------------------------------- workload 3 (scaled)
+# ---------------------------------------------------------------- SwiGLU MLP (scaled)
 @pytest.mark.parametrize("shape", [synth.MlpShape(512, 512, 1408), synth.MlpShape(200, 264, 392)])
 def test_swiglu_mlp_fwd_bwd(coda, shape):
     t = synth.make_mlp(shape, seed=0)
@@ -151,7 +151,7 @@ def test_swiglu_mlp_fwd_bwd(coda, shape):
         assert_bf16(gr[k], b[k], k)
 
 
-# ---------------------------------------------------------------- workload 4 (scaled)
+# ---------------------------------------------------------------- linear + cross-entropy (scaled)
 @pytest.mark.parametrize("shape", [synth.CeShape(512, 256, 4000), synth.CeShape(300, 136, 8192)])
 def test_linear_cross_entropy(coda, shape):
     t = synth.make_ce(shape, seed=0)
@@ -191,7 +191,7 @@ def test_cross_entropy_all_ignored_and_bad_label(coda):
     assert int(out2["n_valid"].item()) == int(valid.sum().item())
 
 
-# ---------------------------------------------------------------- workload 5 (scaled)
+# ---------------------------------------------------------------- transformer block (scaled)
 SMALL_BLOCK = synth.BlockShape(tokens=256, hidden=512, n_q=4, n_kv=2, head_dim=128, inter=1024, seq_len=128)
 RAGGED_BLOCK = synth.BlockShape(tokens=200, hidden=264, n_q=2, n_kv=1, head_dim=128, inter=392, seq_len=64)
 
