@@ -616,19 +616,46 @@ def main():
     if not args.no_ce and "rms" in legs:
         s2 = synth.FULL["rmsnorm_linear"]
         d2 = {k: v.to(dev) for k, v in synth.make_rms_linear(s2, seed=rank).items()}
+        # outputs and workspaces allocated once, as a training loop holds them;
+        # dW on a second stream beside c -> dX
+        M2, N2, K2 = s2.tokens, s2.out, s2.hidden
+        lib = coda.load()
+        Wf2 = torch.empty_like(d2["W"])
+        Y2 = torch.empty(M2, N2, dtype=torch.bfloat16, device=dev)
+        r2 = torch.empty(M2, dtype=torch.float32, device=dev)
+        ws2a = coda.workspace(lib.coda_rmsnorm_linear_workspace_size(M2, N2, K2), dev)
+        ws2b = coda.workspace(lib.coda_rmsnorm_linear_bwd_workspace_size(M2, N2, K2), dev)
+        g2 = {"dX": torch.empty_like(d2["X"]), "dW": torch.empty_like(d2["W"]),
+              "dgamma": torch.empty(K2, dtype=torch.float32, device=dev)}
+        side2 = torch.cuda.Stream(device=dev)
 
         def rms_step():
-            Wf = coda.fold_gamma(d2["W"], d2["gamma"])
-            Y2, r2 = coda.rmsnorm_linear(d2["X"], Wf, d2["R"], eps=s2.eps)
-            coda.rmsnorm_linear_bwd(d2["G"], d2["X"], d2["W"], d2["gamma"], r2, Y2, d2["R"])
+            coda.fold_gamma(d2["W"], d2["gamma"], out=Wf2)
+            coda.rmsnorm_linear(d2["X"], Wf2, d2["R"], eps=s2.eps, rstd_out=r2, Y=Y2, ws=ws2a)
+            coda.rmsnorm_linear_bwd(d2["G"], d2["X"], d2["W"], d2["gamma"], r2, Y2, d2["R"], ws=ws2b, out=g2,
+                                    side_stream=side2)
         m2 = time_calls(rms_step, n=20, warm=3)
+        # the same calls captured once into a CUDA graph (on a capture stream
+        # that has run them once outside the capture) and replayed
+        cap2 = torch.cuda.Stream(device=dev)
+        cap2.wait_stream(stream)
+        with torch.cuda.stream(cap2):
+            rms_step()
+        stream.wait_stream(cap2)
+        graph2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph2, stream=cap2):
+            rms_step()
+        mg2 = time_calls(graph2.replay, n=20, warm=3)
+        if coda.get_status(ws2a) != 0 or coda.get_status(ws2b) != 0:
+            raise RuntimeError("device status error in the RMSNorm-linear measurement")
         f2 = 2 * s2.tokens * s2.hidden * s2.out * 3               # fwd 1 GEMM, bwd 2
         other["rmsnorm_linear"] = {
             "workload": f"RMSNorm-reparameterised projection + residual fwd+bwd, tokens {s2.tokens}, "
                         f"hidden {s2.hidden}, out {s2.out} (gain fold, row RMS, prepass and combines included)",
             "ms": round(m2, 3), "tflops": round(f2 / (m2 / 1e3) / 1e12, 1),
-            "frac_of_sustained": round(f2 / (m2 / 1e3) / 1e12 / sustained, 4)}
-        del d2
+            "frac_of_sustained": round(f2 / (m2 / 1e3) / 1e12 / sustained, 4),
+            "graph_ms": round(mg2, 3), "graph_tflops": round(f2 / (mg2 / 1e3) / 1e12, 1)}
+        del d2, graph2
 
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None

@@ -60,7 +60,7 @@ _SIGS = {
     "coda_rmsnorm_linear_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_rmsnorm_linear": ([_P, _P, _P, _P, _F, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_rmsnorm_linear_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
-    "coda_rmsnorm_linear_bwd": ([_P] * 10 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_rmsnorm_linear_bwd": ([_P] * 10 + [_I64, _I64, _I64, _P, _SZ, _P, _P], ctypes.c_int),
     "coda_linear_residual_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_residual": ([_P, _P, _P, _P, _F, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_residual_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
@@ -307,7 +307,9 @@ def rmsnorm_linear(X, Wf, R=None, rstd_in=None, eps=1e-6, rstd_out=None, Y=None,
     return Y, (rstd_in if rstd_in is not None else rstd_out)
 
 
-def rmsnorm_linear_bwd(dY, X, W, gamma, rstd, Y, R=None, ws=None, out=None, stream=None):
+def rmsnorm_linear_bwd(dY, X, W, gamma, rstd, Y, R=None, ws=None, out=None, stream=None, side_stream=None):
+    """RMSNorm-reparameterised projection backward (coda_rmsnorm_linear_bwd);
+    `side_stream`: optional second torch.cuda.Stream for the dW GEMM."""
     lib = load()
     M, K = X.shape
     N = W.shape[0]
@@ -318,7 +320,8 @@ def rmsnorm_linear_bwd(dY, X, W, gamma, rstd, Y, R=None, ws=None, out=None, stre
     _check("coda_rmsnorm_linear_bwd", lib.coda_rmsnorm_linear_bwd(
         _bf(dY, "dY"), _bf(X, "X"), _bf(W, "W"), _f32(gamma, "gamma"), _f32(rstd, "rstd"),
         _bf(Y, "Y"), _bf(R, "R"), _bf(out["dX"], "dX"), _bf(out["dW"], "dW"), _f32(out["dgamma"], "dgamma"),
-        M, N, K, _ptr(ws), ws.numel(), _stream(stream)))
+        M, N, K, _ptr(ws), ws.numel(), _stream(stream),
+        side_stream.cuda_stream if side_stream is not None else None))
     return out
 
 

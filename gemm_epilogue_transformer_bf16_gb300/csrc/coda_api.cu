@@ -760,7 +760,7 @@ size_t coda_rmsnorm_linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K) {
 
 int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W, const float* gamma, const float* rstd, const coda_bf16* Y, const coda_bf16* R,
                             coda_bf16* dX, coda_bf16* dW, float* dgamma, int64_t M, int64_t N, int64_t K, void* ws,
-                            size_t ws_bytes, coda_stream stream) {
+                            size_t ws_bytes, coda_stream stream, coda_stream side_stream) {
   CK(dims_ok(M, N, K));
   CK(ws_ok(ws, ws_bytes, coda_rmsnorm_linear_bwd_workspace_size(M, N, K)));
   if (M == 0) return CODA_OK;
@@ -781,6 +781,16 @@ int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_
   int* status = static_cast<int*>(ws);
   cudaStream_t s = S(stream);
   CU(coda::launch_rms_bwd_prepass(BF(dY), BF(Y), BF(R), rstd, M, N, Gp, srow, sms, s));
+  // With a side stream, dW runs beside c -> dX (both read only G', X, W), so
+  // each GEMM's partly filled last wave overlaps the other; they share only
+  // the status word (atomic OR).
+  cudaStream_t s2 = side_stream ? S(side_stream) : s;
+  EventSet ev(s2 != s ? 2 : 0);
+  if (!ev.ok()) return CODA_ERR_CUDA;
+  if (s2 != s) {
+    CU(cudaEventRecord(ev[0], s));
+    CU(cudaStreamWaitEvent(s2, ev[0], 0));
+  }
   CU(coda::launch_combine_rows(srow, M, 1, M, 1.f / static_cast<float>(K), 0.f, rstd, coef, 1, s));
   {  // D = G' W;  dX = gamma D - c X, dgamma column partials sum_i X_ik D_ik
     Plan p;
@@ -817,9 +827,13 @@ int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_
     p.e.D = dW;
     p.e.ldd = K;
     p.e.col_scale = gamma;
-    CK(run(p, status, s));
+    CK(run(p, status, s2));
   }
   CU(coda::launch_colsum(dgp, 4 * ntb, K, K, dgamma, s));
+  if (s2 != s) {
+    CU(cudaEventRecord(ev[1], s2));
+    CU(cudaStreamWaitEvent(s, ev[1], 0));
+  }
   return CODA_OK;
 }
 

@@ -235,12 +235,16 @@ int coda_rmsnorm_linear(const coda_bf16* X, const float* rstd_in, const coda_bf1
  * (R may be NULL = zero).  Outputs: dX [M,K], dW [N,K] bf16, dgamma [K] fp32.
  * The pages state only that this backward keeps the GEMM-epilogue form; the
  * formulas are the chain rule of the §3.2.1 equation, and they hold whether
- * the forward folded gamma into W or applied it to the GEMM input. */
+ * the forward folded gamma into W or applied it to the GEMM input.
+ * side_stream (optional, may be NULL): a second stream on which the dW GEMM
+ * runs beside c -> dX (ordered by events the call records; the call returns
+ * with `stream` waiting for both).  Both use the one workspace. */
 size_t coda_rmsnorm_linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K);
 int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_bf16* W, const float* gamma,
                             const float* rstd, const coda_bf16* Y, const coda_bf16* R,
                             coda_bf16* dX, coda_bf16* dW, float* dgamma,
-                            int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream);
+                            int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes, coda_stream stream,
+                            coda_stream side_stream);
 
 /* ------------------------------------------------------------------------
  * Projection + residual (§3.2.1, first GEMM: "xW0 + z")

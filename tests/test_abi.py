@@ -96,7 +96,7 @@ def test_rejects_bad_arguments_on_host(lib):
     assert lib.coda_linear_residual(FAKE, FAKE, None, FAKE, 1e-6, None, None, None, -1, 64, 64, ws, 4096, None) == 1
     # workspace too small
     need = lib.coda_rmsnorm_linear_bwd_workspace_size(128, 64, 64)
-    assert lib.coda_rmsnorm_linear_bwd(*([FAKE] * 10), 128, 64, 64, ws, need - 1, None) == 4
+    assert lib.coda_rmsnorm_linear_bwd(*([FAKE] * 10), 128, 64, 64, ws, need - 1, None, None) == 4
     # null workspace
     assert lib.coda_linear_residual(FAKE, FAKE, None, FAKE, 1e-6, None, None, None, 16, 64, 64, None, 4096, None) == 4
     # head_dim other than 128 is unsupported

@@ -115,3 +115,46 @@ def test_mlp_backward_side_stream_matches_single_stream(coda):
     torch.cuda.synchronize()
     for k in ("dX", "dWg", "dWu", "dWd", "dgamma"):
         assert torch.equal(one[k], two[k]), f"{k} differs with a side stream"
+
+
+def test_rmsnorm_linear_backward_side_stream_matches_single_stream(coda):
+    """dW on a second stream beside c -> dX gives the same bits, and so does a
+    CUDA-graph replay of the forward + backward captured with that side stream
+    (the call's fork and join become graph edges)."""
+    M, N, K = 4096, 2048, 2048            # the RMSNorm-linear benchmark shape
+    dev = "cuda"
+    t = {k: v.to(dev) for k, v in synth.make_rms_linear(synth.RmsLinearShape(M, K, N), seed=9).items()}
+    Wf = coda.fold_gamma(t["W"], t["gamma"])
+    Y, r = coda.rmsnorm_linear(t["X"], Wf, t["R"], eps=1e-6)
+    one = coda.rmsnorm_linear_bwd(t["G"], t["X"], t["W"], t["gamma"], r, Y, t["R"])
+    side = torch.cuda.Stream()
+    two = coda.rmsnorm_linear_bwd(t["G"], t["X"], t["W"], t["gamma"], r, Y, t["R"], side_stream=side)
+    torch.cuda.synchronize()
+    for k in ("dX", "dW", "dgamma"):
+        assert torch.equal(one[k], two[k]), f"{k} differs with a side stream"
+    lib = coda.load()
+    ws1 = coda.workspace(lib.coda_rmsnorm_linear_workspace_size(M, N, K))
+    ws2 = coda.workspace(lib.coda_rmsnorm_linear_bwd_workspace_size(M, N, K))
+    Y2, r2 = torch.empty_like(Y), torch.empty_like(r)
+    out = {k: torch.empty_like(v) for k, v in one.items()}
+
+    def step():
+        coda.fold_gamma(t["W"], t["gamma"], out=Wf)
+        coda.rmsnorm_linear(t["X"], Wf, t["R"], eps=1e-6, rstd_out=r2, Y=Y2, ws=ws1)
+        coda.rmsnorm_linear_bwd(t["G"], t["X"], t["W"], t["gamma"], r2, Y2, t["R"], ws=ws2, out=out,
+                                side_stream=side)
+    cap = torch.cuda.Stream()
+    with torch.cuda.stream(cap):
+        step()                              # first calls set up kernels and streams outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        step()
+    for v in out.values():
+        v.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(Y2, Y) and torch.equal(r2, r)
+    for k in ("dX", "dW", "dgamma"):
+        assert torch.equal(out[k], one[k]), f"{k} differs in the graph replay"
+    assert coda.get_status(ws1) == 0 and coda.get_status(ws2) == 0
