@@ -601,11 +601,13 @@ def main():
         ws3 = coda.workspace(max(coda.load().coda_linear_swiglu_bwd_workspace_size(s3.tokens, s3.inter, s3.hidden),
                                  coda.load().coda_linear_residual_workspace_size(s3.tokens, s3.hidden, s3.inter)), dev)
         o3 = {}
+        side3 = torch.cuda.Stream(device=dev)
 
         def mlp_step():
             H3, g3, u3 = coda.linear_swiglu(d3["X"], d3["Wg"], d3["Wu"], ws=ws3)
             coda.linear_residual(H3, d3["Wd"], d3["R"], ws=ws3)
-            o3["g"] = coda.linear_swiglu_bwd(d3["dY"], d3["X"], d3["Wg"], d3["Wu"], d3["Wd"], g3, u3, H3, ws=ws3)
+            o3["g"] = coda.linear_swiglu_bwd(d3["dY"], d3["X"], d3["Wg"], d3["Wu"], d3["Wd"], g3, u3, H3, ws=ws3,
+                                             side_stream=side3)
         m3 = time_calls(mlp_step)
         f3 = 2 * s3.tokens * s3.hidden * s3.inter * 3 * 3       # fwd 3 GEMMs, bwd 6
         other["mlp_swiglu"] = {
