@@ -26,6 +26,11 @@
  *    device and caller stream, kept for the process), forked from and joined
  *    back to `stream` with events inside the call: work the caller enqueues
  *    on `stream` afterwards is ordered after all of it.
+ *  - Calls can be captured into a CUDA graph (stream capture); the forks and
+ *    joins above, and those of the optional side streams, become graph
+ *    edges.  The first call of each kind on a device (which sets kernel
+ *    attributes and creates the library's streams) and the first call on
+ *    each capture stream must run outside a capture.
  *  - Matrices are row-major with a leading dimension (row stride) given in
  *    ELEMENTS.  Weights use the nn.Linear layout [out_features, in_features].
  *  - bf16 tensors are passed as uint16_t bit patterns (coda_bf16).  All
