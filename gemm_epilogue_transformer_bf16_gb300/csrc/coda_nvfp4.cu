@@ -19,16 +19,19 @@
 //          multiple of 512 (a cluster of four 128-row blocks) and K to a
 //          multiple of 256 with zero scales.
 //
-// GEMM structure: the single-CTA form of the bf16 kernel (warp 0 TMA
-// producer, warp 1 TMEM owner and MMA issuer, warps 2-5 epilogue), M = 128,
-// N = 256, k-slices of 256 elements (128 bytes of codes per row, the same
-// 128-byte swizzled rows), four stages.  Per stage the producer also copies
-// the k-slice's block scales (2 KB for A, 4 KB for B) to shared memory;
-// the MMA thread moves them into TMEM with tcgen05.cp (32 lanes x 128 bits,
+// GEMM structure: warp 0 TMA producer, warp 1 TMEM owner and MMA issuer,
+// warps 2-9 epilogue (two per TMEM lane quarter); M = 128, N = 256, k-slices
+// of 256 elements (128 bytes of codes per row, the same 128-byte swizzled
+// rows as the bf16 kernel), four stages.  Per stage the producer also copies
+// the k-slice's block scales (2 KB for A, 4 KB for B) to shared memory; the
+// MMA thread moves them into TMEM with tcgen05.cp (32 lanes x 128 bits,
 // replicated to the four lane quarters) before the four MMAs (K = 64 each)
 // that read them.  TMEM: the accumulator in columns 0-255 and, per stage,
-// 64 columns of scales (A at +0, B at +16); one accumulator, so the
-// epilogue of a tile does not overlap the next tile's mainloop.
+// 64 columns of scales (A at +0, B at +16).  With a single accumulator the
+// epilogue warps pull their columns into registers and free it before their
+// math and stores, which then overlap the next tile's mainloop.  Variants:
+// clusters of 2 or 4 CTAs sharing the B tile by multicast, and CTA pairs
+// (cta_group::2, 256 x 256 tiles) further down.
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
@@ -170,6 +173,13 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
   return (b & 0x80u) ? -v : v;
 }
 
+// Eight e2m1 codes in a word: a code of magnitude 0 loses its sign bit.
+__device__ __forceinline__ uint32_t clear_negative_zero(uint32_t w) {
+  const uint32_t m = w & 0x77777777u;
+  const uint32_t nz = (m | (m >> 1) | (m >> 2)) & 0x11111111u;  // bit 0 of each nibble: magnitude != 0
+  return m | (w & (nz << 3));
+}
+
 __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t j, int64_t kt_count) {
   return ((r >> 7) * kt_count + (j >> 4)) * 2048 + ((j >> 2) & 3) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 +
          (j & 3);
@@ -194,6 +204,7 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const __nv_bfl
     }
     const __nv_bfloat16* row = X + r * ldx;
     float amax = 0.f;
+#pragma unroll 4
     for (int64_t j = lane; j < nb; j += 32) {
       const uint4* p = reinterpret_cast<const uint4*>(row + j * 16);
       const uint4 w[2] = {p[0], p[1]};
@@ -206,6 +217,7 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const __nv_bfl
     const float s = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
     if (lane == 0) scale[r] = s;
     const float t = __fmul_rn(6.0f, s);
+#pragma unroll 2
     for (int64_t j = lane; j < nb_pad; j += 32) {
       uint32_t sfb = 0;
       if (j < nb) {
@@ -225,15 +237,20 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const __nv_bfl
         const float denom = __fmul_rn(e4m3_value(sfb), s);
         uint32_t lo = 0, hi = 0;
         if (denom > 0.f) {
+          // one division per block: the elements are scaled by its reciprocal
+          const float inv = fminf(__fdiv_rn(1.0f, denom), 3.40282347e38f);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            uint32_t c = __nv_cvt_float_to_fp4(__fdiv_rn(x[i], denom), __NV_E2M1, cudaRoundNearest) & 0xFu;
-            if ((c & 7u) == 0) c = 0;  // no negative zero
-            if (i < 8)
-              lo |= c << (4 * i);
+          for (int i = 0; i < 8; ++i) {
+            // element 2i in the low nibble, 2i + 1 in the high nibble
+            const uint32_t c2 = __nv_cvt_float2_to_fp4x2(
+                make_float2(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv)), __NV_E2M1, cudaRoundNearest);
+            if (i < 4)
+              lo |= (c2 & 0xFFu) << (8 * i);
             else
-              hi |= c << (4 * (i - 8));
+              hi |= (c2 & 0xFFu) << (8 * (i - 4));
           }
+          lo = clear_negative_zero(lo);
+          hi = clear_negative_zero(hi);
         }
         *reinterpret_cast<uint2*>(Q + r * (K / 2) + j * 8) = make_uint2(lo, hi);
       }

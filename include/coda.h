@@ -445,7 +445,8 @@ int coda_linear_swiglu_fp8(const uint8_t* Xq, const float* sx, const float* rstd
  * Quantisation of row x (each step one fp32 operation):
  *   s = amax(x) / 2688 (= 6 * 448; 1 for a zero row);
  *   per block of 16: sf = e4m3(bmax / (6 s)), nearest even, <= 448;
- *   code = e2m1(x / (sf s)), nearest even, saturating at +-6; 0 when sf = 0;
+ *   inv = min(1 / (sf s), FLT_MAX), one per block;
+ *   code = e2m1(x inv), nearest even, saturating at +-6; 0 when sf s = 0;
  *   x ~= e2m1(code) * sf * s.
  * Layouts:
  *   Xq     [rows, K/2] bytes, contiguous: element 2j in the low nibble of byte

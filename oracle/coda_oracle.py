@@ -390,13 +390,17 @@ def swiglu_fp8_fwd(Xv, sx, Wgv, sg, Wuv, su, row_scale=None):
 #   s      = amax(row) / (6 * 448)            (1 for an all-zero row)
 #   for each block of 16 elements along K, with bmax = max |x| over it:
 #   sf     = e4m3(bmax / (6 * s))             nearest even, saturating at 448
-#   code_k = e2m1(x_k / (sf * s))             nearest even, saturating at +-6;
-#            0 for the whole block when sf = 0
+#   inv    = min(1 / (sf * s), FLT_MAX)       the block's reciprocal divisor
+#   code_k = e2m1(x_k * inv)                  nearest even, saturating at +-6;
+#            0 for the whole block when sf * s = 0
 #   x_k   ~= e2m1(code_k) * sf * s
 #
 # Each quotient and product is a single fp32 operation: the codes and scales
 # are integer decisions taken in the kernel's precision, so they must match
-# bit for bit.  A code of magnitude 0 carries no sign (-0 is written as +0).
+# bit for bit.  The elements are scaled by the block's reciprocal (one
+# division per 16 elements); the cap keeps rows whose scales are far below
+# the fp32 normal range finite.  A code of magnitude 0 carries no sign (-0 is
+# written as +0).
 
 E2M1_MAX = 6.0
 # magnitudes of the e2m1 codes 0..7 (1 sign bit, 2 exponent bits with bias 1,
@@ -443,10 +447,11 @@ def quantize_nvfp4_rows(X):
     sfq = torch.from_numpy(np.ascontiguousarray(sf_f)).to(torch.float8_e4m3fn)
     sf = sfq.view(torch.uint8).numpy().copy()
     sf_val = sfq.float().numpy()
-    denom = np.repeat((sf_val * s[:, None]).astype(np.float32), NVFP4_BLOCK, axis=1)
-    with np.errstate(divide="ignore", invalid="ignore"):
-        v = (x32 / denom).astype(np.float32)
-    zero_block = np.repeat(sf_val == 0, NVFP4_BLOCK, axis=1)
+    denom = (sf_val * s[:, None]).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        inv = np.minimum(np.float32(1.0) / denom, np.finfo(np.float32).max).astype(np.float32)
+        v = (x32 * np.repeat(inv, NVFP4_BLOCK, axis=1)).astype(np.float32)
+    zero_block = np.repeat(denom == 0, NVFP4_BLOCK, axis=1)
     codes = np.where(zero_block, 0, e2m1_round(np.where(zero_block, 0, v))).astype(np.uint8)
     values = e2m1_value(codes) * np.repeat(sf_val.astype(np.float64), NVFP4_BLOCK, axis=1)
     return codes, sf, s, values
