@@ -26,7 +26,7 @@ __all__ = [
     "linear_swiglu", "linear_swiglu_bwd", "linear_qknorm_rope", "linear_qknorm_rope_bwd",
     "linear_cross_entropy", "linear_cross_entropy_bwd", "linear_cross_entropy_noalloc", "workspace",
     "rmsnorm_linear_cross_entropy", "rmsnorm_linear_cross_entropy_bwd", "rms_rstd",
-    "linear_sigmoid", "linear_sigmoid_bwd", "quantize_fp8_rows", "linear_fp8", "linear_swiglu_fp8", "quantize_nvfp4_rows", "linear_nvfp4",
+    "linear_sigmoid", "linear_sigmoid_bwd", "quantize_fp8_rows", "linear_fp8", "linear_swiglu_fp8", "quantize_nvfp4_rows", "rmsnorm_scale_nvfp4", "linear_nvfp4",
     "linear_swiglu_nvfp4",
     "MAP_NONE", "MAP_SWIGLU", "MAP_DSWIGLU", "MAP_QKNORM_ROPE", "MAP_CE_LSE",
     "MAP_CE_DLOGITS", "MAP_COLDOT", "MAP_SIGMOID", "MAP_DSIGMOID", "K_MAJOR", "MN_MAJOR",
@@ -84,6 +84,7 @@ _SIGS = {
     "coda_linear_swiglu_fp8": ([_P] * 10 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_nvfp4_scale_bytes": ([_I64, _I64], _SZ),
     "coda_quantize_nvfp4_rows": ([_P, _I64, _I64, _I64, _P, _P, _P, _P], ctypes.c_int),
+    "coda_rmsnorm_scale_nvfp4": ([_P, _I64, _I64, _I64, _F, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "coda_linear_nvfp4_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_nvfp4": ([_P] * 8 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_swiglu_nvfp4_workspace_size": ([_I64, _I64, _I64], _SZ),
@@ -547,6 +548,23 @@ def quantize_nvfp4_rows(X, stream=None):
     _check("coda_quantize_nvfp4_rows", lib.coda_quantize_nvfp4_rows(
         _bf(X, "X"), X.stride(0), M, K, _u8(Xq, "Xq"), _u8(sf, "sf"), _f32(scale, "scale"), _stream(stream)))
     return Xq, sf, scale
+
+
+def rmsnorm_scale_nvfp4(X, gamma, eps, stream=None):
+    """One pass over X (coda_rmsnorm_scale_nvfp4): the NVFP4 codes, block
+    scales and row scales of u = X ⊙ gamma, and rstd = 1/rms(X).  Returns
+    (codes, block scales, row scales, rstd)."""
+    lib = load()
+    M, K = X.shape
+    dev = X.device
+    Xq = torch.empty(M, K // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(max(lib.coda_nvfp4_scale_bytes(M, K), 16), dtype=torch.uint8, device=dev)
+    scale = torch.empty(M, dtype=torch.float32, device=dev)
+    rstd = torch.empty(M, dtype=torch.float32, device=dev)
+    _check("coda_rmsnorm_scale_nvfp4", lib.coda_rmsnorm_scale_nvfp4(
+        _bf(X, "X"), X.stride(0), M, K, float(eps), _f32(gamma, "gamma"), _f32(rstd, "rstd"), _u8(Xq, "Xq"),
+        _u8(sf, "sf"), _f32(scale, "scale"), _stream(stream)))
+    return Xq, sf, scale, rstd
 
 
 def linear_nvfp4(Xq, sfx, sx, Wq, sfw, sw, R=None, Y=None, ws=None, stream=None):

@@ -1875,6 +1875,21 @@ int coda_quantize_nvfp4_rows(const coda_bf16* X, int64_t ldx, int64_t M, int64_t
   return CODA_OK;
 }
 
+int coda_rmsnorm_scale_nvfp4(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, float eps, const float* gamma,
+                             float* rstd, uint8_t* Xq, uint8_t* sf, float* scale, coda_stream stream) {
+  if (M < 0 || K < 0) return CODA_ERR_INVALID_ARG;
+  if (K % 32) return CODA_ERR_UNSUPPORTED;
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)X, (const void*)gamma, (const void*)Xq, (const void*)sf, (const void*)scale})
+    CK(req(q));
+  for (const void* q : {(const void*)X, (const void*)gamma, (const void*)Xq, (const void*)sf}) CK(al(q));
+  CK(ldok(ldx, K));
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  CU(coda::launch_quantize_nvfp4_rows(BF(X), ldx, M, K, Xq, sf, scale, sms, S(stream), gamma, rstd, eps));
+  return CODA_OK;
+}
+
 size_t coda_linear_nvfp4_workspace_size(int64_t, int64_t, int64_t) { return WS_HEADER; }
 
 int coda_linear_nvfp4(const uint8_t* Xq, const uint8_t* sfx, const float* sx, const uint8_t* Wq, const uint8_t* sfw,

@@ -59,8 +59,11 @@ bool nvfp4_pairs(int64_t M);
 uint32_t nvfp4_idesc_pair();
 cudaError_t launch_gemm_nvfp4_pair(int kind, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
                                    const GemmArgs& a, const Nvfp4Scales& sc);
+// gamma (optional): quantise x * gamma (fp32 products); rstd (optional):
+// also write 1 / sqrt(mean(x^2) + eps) per row.
 cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Q,
-                                       uint8_t* SF, float* scale, int num_sms, cudaStream_t s);
+                                       uint8_t* SF, float* scale, int num_sms, cudaStream_t s,
+                                       const float* gamma = nullptr, float* rstd = nullptr, float eps = 0.f);
 cudaError_t launch_gemm_plain_nvfp4(int cg, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,
                                     const GemmArgs& a, const Nvfp4Scales& sc);
 cudaError_t launch_gemm_swiglu_nvfp4(int cg, int num_units, int sms, cudaStream_t s, const CUtensorMap* m,

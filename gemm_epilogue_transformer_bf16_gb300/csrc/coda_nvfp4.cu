@@ -173,6 +173,31 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
   return (b & 0x80u) ? -v : v;
 }
 
+// x[0..15] *= gamma[16j ..] (one fp32 product each).
+__device__ __forceinline__ void apply_gamma(const float* gamma, int64_t j, float* x) {
+  const float4* gp = reinterpret_cast<const float4*>(gamma + j * 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 g = gp[i];
+    x[4 * i] = __fmul_rn(x[4 * i], g.x);
+    x[4 * i + 1] = __fmul_rn(x[4 * i + 1], g.y);
+    x[4 * i + 2] = __fmul_rn(x[4 * i + 2], g.z);
+    x[4 * i + 3] = __fmul_rn(x[4 * i + 3], g.w);
+  }
+}
+
+// Block j (16 elements) of a bf16 row as fp32.
+__device__ __forceinline__ void load_block16(const __nv_bfloat16* row, const float*, int64_t j, float* x) {
+  const uint4* p = reinterpret_cast<const uint4*>(row + j * 16);
+  const uint4 w[2] = {p[0], p[1]};
+  const uint32_t* u = reinterpret_cast<const uint32_t*>(w);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = bf16_lo(u[i]);
+    x[2 * i + 1] = bf16_hi(u[i]);
+  }
+}
+
 // Eight e2m1 codes in a word: a code of magnitude 0 loses its sign bit.
 __device__ __forceinline__ uint32_t clear_negative_zero(uint32_t w) {
   const uint32_t m = w & 0x77777777u;
@@ -186,13 +211,17 @@ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t j, int64_t kt_co
 }
 
 // One warp per row (rows up to the padded count; padding rows only write
-// zero scales).  Pass 1: the row's amax.  Pass 2, lane per 16-element block:
-// the block's e4m3 scale and sixteen e2m1 codes.
+// zero scales).  The quantised row is x, or u = x * gamma when a gain vector
+// is given (the RMSNorm gain, applied without rounding u to bf16).  Pass 1:
+// the row's amax (and, when rstd is given, sum x^2 for 1 / rms(x)).  Pass 2,
+// lane per 16-element block: the block's e4m3 scale and sixteen e2m1 codes.
+template <bool GAMMA, bool RSTD>
 __global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx,
                                                                   int64_t M, int64_t K, uint8_t* __restrict__ Q,
                                                                   uint8_t* __restrict__ SF,
                                                                   float* __restrict__ scale, int64_t rows_pad,
-                                                                  int64_t kt_count) {
+                                                                  int64_t kt_count, const float* __restrict__ gamma,
+                                                                  float* __restrict__ rstd, float eps) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int64_t nb = K / 16, nb_pad = kt_count * 16;
@@ -203,17 +232,26 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const __nv_bfl
       continue;
     }
     const __nv_bfloat16* row = X + r * ldx;
-    float amax = 0.f;
+    float amax = 0.f, ss = 0.f;
 #pragma unroll 4
     for (int64_t j = lane; j < nb; j += 32) {
-      const uint4* p = reinterpret_cast<const uint4*>(row + j * 16);
-      const uint4 w[2] = {p[0], p[1]};
-      const uint32_t* u = reinterpret_cast<const uint32_t*>(w);
+      float x[16];
+      load_block16(row, nullptr, j, x);
+      if constexpr (RSTD) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[i])), fabsf(bf16_hi(u[i]))));
+        for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
+      }
+      if constexpr (GAMMA) apply_gamma(gamma, j, x);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if constexpr (RSTD) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) rstd[r] = 1.f / sqrtf(ss / static_cast<float>(K) + eps);
+    }
     const float s = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
     if (lane == 0) scale[r] = s;
     const float t = __fmul_rn(6.0f, s);
@@ -221,17 +259,12 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const __nv_bfl
     for (int64_t j = lane; j < nb_pad; j += 32) {
       uint32_t sfb = 0;
       if (j < nb) {
-        const uint4* p = reinterpret_cast<const uint4*>(row + j * 16);
-        const uint4 w[2] = {p[0], p[1]};
-        const uint32_t* u = reinterpret_cast<const uint32_t*>(w);
         float x[16];
+        load_block16(row, nullptr, j, x);
+        if constexpr (GAMMA) apply_gamma(gamma, j, x);
         float bmax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          x[2 * i] = bf16_lo(u[i]);
-          x[2 * i + 1] = bf16_hi(u[i]);
-          bmax = fmaxf(bmax, fmaxf(fabsf(x[2 * i]), fabsf(x[2 * i + 1])));
-        }
+        for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(x[i]));
         const float sf_f = fminf(__fdiv_rn(bmax, t), 448.0f);
         sfb = __nv_cvt_float_to_fp8(sf_f, __NV_SATFINITE, __NV_E4M3);
         const float denom = __fmul_rn(e4m3_value(sfb), s);
@@ -971,12 +1004,24 @@ int nvfp4_cluster_size(int64_t M) {
 }
 
 cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Q,
-                                       uint8_t* SF, float* scale, int num_sms, cudaStream_t s) {
+                                       uint8_t* SF, float* scale, int num_sms, cudaStream_t s, const float* gamma,
+                                       float* rstd, float eps) {
   const int64_t rows_pad = (M + 511) / 512 * 512;
   const int64_t kt = (K + 255) / 256;
   const int64_t blocks = std::min<int64_t>((rows_pad + 7) / 8, static_cast<int64_t>(num_sms) * 8);
-  quantize_nvfp4_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(
-      X, ldx, M, K, Q, SF, scale, rows_pad, kt);
+  const unsigned grid = static_cast<unsigned>(std::max<int64_t>(blocks, 1));
+  if (gamma && rstd)
+    quantize_nvfp4_rows_kernel<true, true><<<grid, 256, 0, s>>>(X, ldx, M, K, Q, SF, scale, rows_pad, kt, gamma,
+                                                                  rstd, eps);
+  else if (gamma)
+    quantize_nvfp4_rows_kernel<true, false><<<grid, 256, 0, s>>>(X, ldx, M, K, Q, SF, scale, rows_pad, kt, gamma,
+                                                                   rstd, eps);
+  else if (rstd)
+    quantize_nvfp4_rows_kernel<false, true><<<grid, 256, 0, s>>>(X, ldx, M, K, Q, SF, scale, rows_pad, kt, gamma,
+                                                                   rstd, eps);
+  else
+    quantize_nvfp4_rows_kernel<false, false><<<grid, 256, 0, s>>>(X, ldx, M, K, Q, SF, scale, rows_pad, kt, gamma,
+                                                                    rstd, eps);
   return cudaGetLastError();
 }
 

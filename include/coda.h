@@ -464,6 +464,16 @@ size_t coda_nvfp4_scale_bytes(int64_t rows, int64_t K);
 int coda_quantize_nvfp4_rows(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq, uint8_t* sf,
                              float* scale, coda_stream stream);
 
+/* The RMSNorm input stage of an NVFP4 projection in one pass over X: the
+ * codes, block scales and row scales of u = x ⊙ gamma (fp32 products, not
+ * rounded to bf16) as coda_quantize_nvfp4_rows writes them, and, when rstd
+ * is not NULL, rstd = 1 / sqrt(mean(x^2) + eps) per row — the row factor r
+ * of the RMSNorm reparameterisation ("CODA: Rewriting Transformer Blocks as
+ * GEMM-Epilogue Programs", §3.2.1), applied by the next GEMM's epilogue
+ * (coda_linear_swiglu_nvfp4's rstd).  gamma [K] fp32, 16-byte aligned. */
+int coda_rmsnorm_scale_nvfp4(const coda_bf16* X, int64_t ldx, int64_t M, int64_t K, float eps, const float* gamma,
+                             float* rstd, uint8_t* Xq, uint8_t* sf, float* scale, coda_stream stream);
+
 /* Y = R + (sx ⊙ deq(Xq, sfx))(sw ⊙ deq(Wq, sfw))^T: X side [M, K], W side
  * [N, K] (as quantised by coda_quantize_nvfp4_rows), R [M, N] bf16 or NULL,
  * Y [M, N] bf16. */

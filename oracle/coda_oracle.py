@@ -52,6 +52,7 @@ __all__ = [
     "sigmoid", "linear_sigmoid_fwd", "linear_sigmoid_bwd",
     "E4M3_MAX", "quantize_fp8_rows", "linear_fp8_fwd", "swiglu_fp8_fwd",
     "E2M1_MAX", "E2M1_GRID", "NVFP4_BLOCK", "e2m1_round", "e2m1_value", "quantize_nvfp4_rows",
+    "rmsnorm_scale_nvfp4",
     "linear_nvfp4_fwd", "swiglu_nvfp4_fwd",
 ]
 
@@ -455,6 +456,15 @@ def quantize_nvfp4_rows(X):
     codes = np.where(zero_block, 0, e2m1_round(np.where(zero_block, 0, v))).astype(np.uint8)
     values = e2m1_value(codes) * np.repeat(sf_val.astype(np.float64), NVFP4_BLOCK, axis=1)
     return codes, sf, s, values
+
+
+def rmsnorm_scale_nvfp4(X, gamma, eps):
+    """The RMSNorm input stage of an NVFP4 projection ([P1] §3.2.1: the
+    projection applies r to the product of x ⊙ gamma and W): the NVFP4
+    quantisation of u = x ⊙ gamma, the products taken in fp32 and not
+    rounded to bf16, and r = 1/rms(x).  Returns quantize_nvfp4_rows(u) + (r,)."""
+    u = (np.asarray(X, dtype=np.float32) * np.asarray(gamma, dtype=np.float32)[None, :]).astype(np.float32)
+    return quantize_nvfp4_rows(u) + (rms_inv(X, eps),)
 
 
 def linear_nvfp4_fwd(Xv, sx, Wv, sw, R=None, row_scale=None):

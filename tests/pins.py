@@ -630,7 +630,28 @@ def check_nvfp4_linear(o):
     return max(_rel(H, H0), _rel(g, g0), _rel(u, u0), _rel(y, X @ Wg.T))
 
 
+def check_rmsnorm_scale_nvfp4(o):
+    """(1) gamma = 2^k per column block: codes and block scales equal those
+    of x alone and the row scales carry the factor exactly (products by a
+    power of two are exact); (2) r is the RMSNorm of x, not of x ⊙ gamma,
+    written out here: 1 / sqrt(mean(x^2) + eps)."""
+    r = RNG(33)
+    X = (r.standard_normal((5, 64)) * np.array([1e-2, 1, 3, 50, 0.2])[:, None]).astype(np.float32)
+    e = []
+    for k in (-3, 0, 5):
+        g = np.full(64, 2.0 ** k)
+        c, sf, s, v, rr = o.rmsnorm_scale_nvfp4(X, g, 1e-6)
+        c0, sf0, s0, v0 = o.quantize_nvfp4_rows(X)
+        e += [float(np.any(c != c0)), float(np.any(sf != sf0)), _rel(s, s0 * 2.0 ** k)]
+    g = 1 + 0.3 * r.standard_normal(64)
+    *_, rr = o.rmsnorm_scale_nvfp4(X, g, 1e-6)
+    x64 = X.astype(np.float64)
+    e.append(_rel(rr, 1.0 / np.sqrt((x64 * x64).mean(axis=1) + 1e-6)))
+    return max(e)
+
+
 ALL_CHECKS = {
+    "rmsnorm_scale_nvfp4": (check_rmsnorm_scale_nvfp4, 1e-12),
     "e2m1": (check_e2m1, 0.0),
     "nvfp4_quantizer": (check_nvfp4_quantizer, 1e-12),
     "nvfp4_linear": (check_nvfp4_linear, 1e-14),

@@ -120,6 +120,8 @@ def test_rejects_bad_arguments_on_host(lib):
     assert lib.coda_linear_nvfp4(FAKE, None, *([FAKE] * 4), None, FAKE, 16, 64, 64, ws, 4096, None) == 1
     assert lib.coda_linear_swiglu_nvfp4(*([FAKE] * 9), None, FAKE, None, None, 16, 64, 64, ws, 4096, None) == 1
     assert lib.coda_linear_swiglu_nvfp4(*([FAKE] * 10), FAKE, None, None, 0, 64, 64, ws, 4096, None) == 0
+    assert lib.coda_rmsnorm_scale_nvfp4(FAKE, 64, 16, 64, 1e-6, None, None, FAKE, FAKE, FAKE, None) == 1
+    assert lib.coda_rmsnorm_scale_nvfp4(FAKE, 48, 16, 48, 1e-6, FAKE, None, FAKE, FAKE, FAKE, None) == 3
     assert lib.coda_nvfp4_scale_bytes(300, 224) == 4 * 1 * 2048
     assert lib.coda_nvfp4_scale_bytes(600, 512) == 8 * 2 * 2048
 

@@ -120,3 +120,29 @@ def test_nvfp4_kernel_variants(variant):
     r = subprocess.run([sys.executable, os.path.join(here, "nvfp4_variant_check.py")], env=env,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), f"{variant}:\n{r.stdout[-2000:]}\n{r.stderr[-4000:]}"
+
+
+@pytest.mark.parametrize("shape", [synth.MlpShape(512, 512, 1408), synth.MlpShape(300, 288, 392)])
+def test_rmsnorm_scale_nvfp4_into_swiglu(coda, shape):
+    """The fused RMSNorm input stage (r = 1/rms(x) and the NVFP4 codes of
+    x ⊙ gamma in one pass) bit for bit against the oracle, then the NVFP4
+    SwiGLU projection with r as its row factor."""
+    t = synth.make_mlp(shape, seed=4)
+    d = {k: v.to(DEV) for k, v in t.items()}
+    gamma = synth.gain_f32(shape.hidden, 5)
+    xq, sfx, sx, r = coda.rmsnorm_scale_nvfp4(d["X"], gamma.to(DEV), 1e-6)
+    oc, osf, osx, ov, orr = O.rmsnorm_scale_nvfp4(to_np(t["X"]), gamma.numpy(), 1e-6)
+    assert np.array_equal(unpack_codes(xq), oc), "codes of x * gamma"
+    assert np.array_equal(sx.cpu().numpy(), osx), "row scales"
+    assert np.array_equal(sfx.cpu().numpy()[scale_offsets(*t["X"].shape)], osf), "block scales"
+    from parity import assert_f32
+    assert_f32(r, orr, "rstd")
+    gq, sfg, sg = coda.quantize_nvfp4_rows(d["Wg"])
+    uq, sfu, su = coda.quantize_nvfp4_rows(d["Wu"])
+    gv, osg = check_quantised(coda, t["Wg"], gq, sfg, sg)
+    uv, osu = check_quantised(coda, t["Wu"], uq, sfu, su)
+    H, g, u = coda.linear_swiglu_nvfp4(xq, sfx, sx, gq, sfg, sg, uq, sfu, su, rstd=r)
+    Hr, gr, ur = O.swiglu_nvfp4_fwd(ov, osx, gv, osg, uv, osu, row_scale=orr)
+    assert_bf16(H, Hr, "H (fused input stage)")
+    assert_bf16(g, gr, "g (fused input stage)")
+    assert_bf16(u, ur, "u (fused input stage)")
