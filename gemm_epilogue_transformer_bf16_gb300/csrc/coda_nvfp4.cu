@@ -187,7 +187,7 @@ __device__ __forceinline__ void apply_gamma(const float* gamma, int64_t j, float
 }
 
 // Block j (16 elements) of a bf16 row as fp32.
-__device__ __forceinline__ void load_block16(const __nv_bfloat16* row, const float*, int64_t j, float* x) {
+__device__ __forceinline__ void load_block16(const __nv_bfloat16* row, int64_t j, float* x) {
   const uint4* p = reinterpret_cast<const uint4*>(row + j * 16);
   const uint4 w[2] = {p[0], p[1]};
   const uint32_t* u = reinterpret_cast<const uint32_t*>(w);
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const __nv_bfl
 #pragma unroll 4
     for (int64_t j = lane; j < nb; j += 32) {
       float x[16];
-      load_block16(row, nullptr, j, x);
+      load_block16(row, j, x);
       if constexpr (RSTD) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(256) quantize_nvfp4_rows_kernel(const __nv_bfl
       uint32_t sfb = 0;
       if (j < nb) {
         float x[16];
-        load_block16(row, nullptr, j, x);
+        load_block16(row, j, x);
         if constexpr (GAMMA) apply_gamma(gamma, j, x);
         float bmax = 0.f;
 #pragma unroll
