@@ -1,7 +1,7 @@
 """Builds libcoda.so in-tree with nvcc for sm_103a (no CMake, no torch
 extension machinery): every .cu under csrc/ is compiled in parallel to an
 object file under _build/, then linked into a shared library next to this
-file.  The CUDA runtime is linked statically; the driver's tensor-map encoder
+file.  The CUDA runtime is linked statically; the CUDA driver library's tensor-map encoder (libcuda)
 is resolved at run time, so the library loads on machines without a GPU.
 """
 from __future__ import annotations
