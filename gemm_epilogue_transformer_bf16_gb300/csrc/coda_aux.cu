@@ -23,6 +23,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // ---------------------------------------------------------------- gamma fold
 __global__ void fold_gamma_kernel(const __nv_bfloat16* __restrict__ W, const float* __restrict__ gamma,
                                   __nv_bfloat16* Wf, int64_t N, int64_t K) {
+  griddep_launch_dependents();
   const int64_t total8 = N * K / 8;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -52,6 +53,7 @@ cudaError_t launch_fold_gamma(const __nv_bfloat16* W, const float* gamma, __nv_b
 __global__ void row_rstd_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int64_t M, int64_t K, float eps,
                                 float* rstd, const float* __restrict__ gamma, __nv_bfloat16* __restrict__ U,
                                 int64_t ldu) {
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; row < M; row += warps) {
@@ -86,6 +88,7 @@ cudaError_t launch_row_rstd(const __nv_bfloat16* X, int64_t ldx, int64_t M, int6
 // ---------------------------------------------------------------- combine row partials
 __global__ void combine_rows_kernel(const float* __restrict__ p, int64_t ld, int nparts, int64_t M, float inv_k,
                                     float eps, const float* __restrict__ r, float* out, int mode) {
+  griddep_launch_dependents();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float s = 0.f;
@@ -112,6 +115,7 @@ cudaError_t launch_combine_rows(const float* p, int64_t ld, int nparts, int64_t 
 __global__ void rms_bwd_prepass_kernel(const __nv_bfloat16* __restrict__ G, const __nv_bfloat16* __restrict__ Y,
                                        const __nv_bfloat16* __restrict__ R, const float* __restrict__ rstd,
                                        int64_t M, int64_t N, __nv_bfloat16* Gp, float* srow) {
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; row < M; row += warps) {
@@ -154,6 +158,7 @@ cudaError_t launch_rms_bwd_prepass(const __nv_bfloat16* G, const __nv_bfloat16* 
 // Block = 32 columns x 32 row groups; row group g sums rows g, g+32, ...;
 // the 32 group sums are then added in order.
 __global__ void colsum_kernel(const float* __restrict__ p, int64_t nrows, int64_t ncols, int64_t ld, float* out) {
+  griddep_launch_dependents();
   __shared__ float part[32][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int64_t col = blockIdx.x * 32 + tx;
@@ -182,6 +187,7 @@ __global__ void ce_combine_kernel(const float2* __restrict__ part, int64_t ld, i
                                   const float* __restrict__ target, const int32_t* __restrict__ labels,
                                   int32_t ignore, int64_t M, int64_t V, float* lse_out, double* blk_loss,
                                   int* blk_cnt, int* status) {
+  griddep_launch_dependents();
   __shared__ double sl[CE_COMBINE_THREADS];
   __shared__ int sc[CE_COMBINE_THREADS];
   double acc = 0.0;
@@ -225,6 +231,7 @@ __global__ void ce_combine_kernel(const float2* __restrict__ part, int64_t ld, i
 
 __global__ void ce_finalize_kernel(const double* blk_loss, const int* blk_cnt, int nblk, float* loss_mean,
                                    int32_t* n_valid) {
+  griddep_launch_dependents();
   if (threadIdx.x != 0) return;
   double s = 0.0;
   long long c = 0;
@@ -256,6 +263,7 @@ cudaError_t launch_ce_combine(const float2* part, int64_t ld, int nchunks, const
 __global__ void ce_prep_kernel(const int32_t* __restrict__ labels, int32_t ignore, int64_t M, int64_t V,
                                const int32_t* __restrict__ n_valid, float dloss, const float* __restrict__ rstd,
                                float* wrow, int32_t* lrow, int32_t* counts) {
+  griddep_launch_dependents();
   const int32_t nv = *n_valid;
   const float w = nv > 0 ? dloss / static_cast<float>(nv) : 0.f;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M;
@@ -294,6 +302,7 @@ __global__ void __launch_bounds__(1024) scan_counts_kernel(const int32_t* __rest
 
 __global__ void ce_fill_kernel(const int32_t* __restrict__ lrow, int64_t M, const int32_t* __restrict__ off,
                                int32_t* cursor, int32_t* idx) {
+  griddep_launch_dependents();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int32_t y = lrow[i];
@@ -302,6 +311,7 @@ __global__ void ce_fill_kernel(const int32_t* __restrict__ lrow, int64_t M, cons
 }
 
 __global__ void ce_sort_buckets_kernel(const int32_t* __restrict__ off, int64_t V, int32_t* idx) {
+  griddep_launch_dependents();
   for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < V;
        v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int32_t b = off[v], e = off[v + 1];
@@ -342,6 +352,7 @@ cudaError_t launch_ce_onehot_prep(const int32_t* labels, int32_t ignore, int64_t
 __global__ void ce_norm_coef_kernel(const float* __restrict__ pz, int64_t ld, int nparts,
                                     const float* __restrict__ target, const float* __restrict__ rstd,
                                     const float* __restrict__ rw, int64_t M, float inv_k, float* coef) {
+  griddep_launch_dependents();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float w = rw[i];
@@ -368,6 +379,7 @@ cudaError_t launch_ce_norm_coef(const float* pz, int64_t ld, int nparts, const f
 // e4m3(x / scale), fp32 division, round to nearest even, saturating.
 __global__ void quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int64_t M, int64_t K,
                                          uint8_t* Xq, int64_t ldq, float* scale) {
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; row < M; row += warps) {
@@ -429,6 +441,7 @@ cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, int* status, cudaStr
 
 // ---------------------------------------------------------------- RoPE table
 __global__ void rope_table_kernel(double theta, int head_dim, int max_pos, float2* cs) {
+  griddep_launch_dependents();
   const int half = head_dim / 2;
   const int64_t total = static_cast<int64_t>(max_pos) * half;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -478,6 +491,7 @@ __global__ void __launch_bounds__(QK_BWD_WARPS * 32)
                   const int32_t* __restrict__ pos, const float2* __restrict__ cs, int max_pos, float eps, int n_q,
                   int n_kv, const float* __restrict__ rstd, int64_t M, __nv_bfloat16* Gp, float* srow,
                   float* dgam_part, int* status) {
+  griddep_launch_dependents();
   constexpr int D = 128;
   __shared__ float red[QK_BWD_WARPS][2 * D];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;

@@ -243,6 +243,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int num_kb = args.kb0 + args.kb1;
   bool aborted = false;
+  // Everything above touched only shared memory, TMEM and the kernel
+  // parameters: with programmatic launch it overlaps the previous kernel's
+  // tail.  From here on global memory is read and written.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

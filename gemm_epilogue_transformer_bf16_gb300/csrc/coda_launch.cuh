@@ -6,11 +6,22 @@
 #pragma once
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 #include "coda_epilogues.cuh"
 #include "coda_internal.h"
 
 namespace coda {
+
+// GEMM launches use programmatic dependent launch (CODA_PDL=0 in the
+// environment turns it off, for comparisons).
+inline bool programmatic_launch() {
+  static const bool v = [] {
+    const char* e = std::getenv("CODA_PDL");
+    return e ? e[0] != '0' : true;
+  }();
+  return v;
+}
 
 template <int BN, class Epi, int CG, bool FP8>
 cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a) {
@@ -38,7 +49,7 @@ cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CU
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   if constexpr (CG >= 2) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CG;
@@ -74,6 +85,14 @@ cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CU
     }
     const int cap = a.max_clusters > 0 ? std::min(a.max_clusters, sms) : sms;
     cfg.gridDim = dim3(static_cast<unsigned>(std::min(num_units, cap)));
+  }
+  if (programmatic_launch()) {
+    // may start before the previous kernel in the stream has finished: the
+    // kernel runs its prologue, then waits for it (griddep_wait)
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    ++cfg.numAttrs;
   }
   e = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], a);
   if (e != cudaSuccess) return e;

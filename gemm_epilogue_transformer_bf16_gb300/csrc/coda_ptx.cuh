@@ -172,6 +172,18 @@ __device__ __forceinline__ uint32_t elect_one() {
   return e;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel in its stream is still running; griddep_wait blocks
+// until that kernel has completed and its memory operations are visible, so
+// it must precede every global-memory access of such a kernel.
+// griddep_launch_dependents lets the next such kernel start its own
+// prologue early (it still waits for this one to complete).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
