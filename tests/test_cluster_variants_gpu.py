@@ -1,7 +1,9 @@
 """The GEMM kernel in each cluster size: single CTAs (CODA_CTA_PAIR=0), CTA
 pairs only (CODA_CTA_QUAD=0), the per-GEMM policy CODA_CTA_QUAD=2 and split
 launches turned off (CODA_SPLIT=0; by default a two-pair kernel and a pair
-kernel share the GPU).  The
+kernel share the GPU); and the launch options turned off: programmatic
+dependent launch (CODA_PDL=0) and streaming epilogue stores for large
+outputs (CODA_L2_HINTS=0).  The
 switches are read once per process, so each variant runs
 cluster_variant_check.py (block forward/backward, FP8 linear, against the
 fp64 oracle) in a fresh process."""
@@ -16,7 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 @pytest.mark.parametrize("env", [{"CODA_CTA_PAIR": "0"}, {"CODA_CTA_QUAD": "0"}, {"CODA_CTA_QUAD": "2"},
-                                 {"CODA_SPLIT": "0"}])
+                                 {"CODA_SPLIT": "0"}, {"CODA_PDL": "0"}, {"CODA_L2_HINTS": "0"}])
 def test_cluster_variant(env):
     e = dict(os.environ)
     e.update(env)
