@@ -228,35 +228,44 @@ def rope_angles(pos, head_dim, theta):
     return np.asarray(pos, dtype=np.float64)[:, None] * inv_freq[None, :]
 
 
-def rope(v, pos, theta):
-    """Rotate interleaved pairs (2j, 2j+1) of v[t, head, d] by angle[t, j].
-    [P1] §3.1 class 1 names RoPE-style rotations as a pairwise map; the
-    convention (interleaved pairs) is a reading."""
+def rope(v, pos, theta, pairing="interleaved"):
+    """Rotate pairs of v[t, head, d] by angle[t, j] = pos[t] * theta^(-2j/d):
+    [a, b] -> [a cos - b sin, a sin + b cos].  pairing "interleaved": pair j
+    is (2j, 2j+1); "half": pair j is (j, j + d/2) (the two halves of the
+    head).  [P1] §3.1 class 1 names RoPE-style rotations as a pairwise map;
+    the pairing convention is a reading, and both are supported."""
     d = v.shape[-1]
     ang = rope_angles(pos, d, theta)[:, None, :]
     c, s = np.cos(ang), np.sin(ang)
-    a, b = v[..., 0::2], v[..., 1::2]
     out = np.empty_like(v)
-    out[..., 0::2] = a * c - b * s
-    out[..., 1::2] = a * s + b * c
+    if pairing == "interleaved":
+        a, b = v[..., 0::2], v[..., 1::2]
+        out[..., 0::2] = a * c - b * s
+        out[..., 1::2] = a * s + b * c
+    elif pairing == "half":
+        a, b = v[..., : d // 2], v[..., d // 2:]
+        out[..., : d // 2] = a * c - b * s
+        out[..., d // 2:] = a * s + b * c
+    else:
+        raise ValueError(pairing)
     return out
 
 
-def rope_inv(v, pos, theta):
+def rope_inv(v, pos, theta, pairing="interleaved"):
     """Rotation by the negative angle: the inverse (and transpose) of rope."""
-    return rope(v, -np.asarray(pos, dtype=np.float64), theta)
+    return rope(v, -np.asarray(pos, dtype=np.float64), theta, pairing)
 
 
-def qk_rmsnorm_rope_fwd(q, gamma, pos, theta, eps):
+def qk_rmsnorm_rope_fwd(q, gamma, pos, theta, eps, pairing="interleaved"):
     """q[t, head, d] -> RoPE(RMSNorm_d(q) ⊙ gamma, pos).  [P3]'s
     linear_qknorm_rope names the fused operator: per-head RMSNorm, then RoPE."""
-    return rope(rmsnorm(q, gamma, eps), pos, theta)
+    return rope(rmsnorm(q, gamma, eps), pos, theta, pairing)
 
 
-def qk_rmsnorm_rope_bwd(q, gamma, pos, theta, eps, dout):
+def qk_rmsnorm_rope_bwd(q, gamma, pos, theta, eps, dout, pairing="interleaved"):
     """Backward: inverse rotation of the gradient, then per-head RMSNorm
     backward.  Returns (dq, dgamma)."""
-    dn = rope_inv(dout, pos, theta)
+    dn = rope_inv(dout, pos, theta, pairing)
     return rmsnorm_bwd(q, gamma, eps, dn)
 
 

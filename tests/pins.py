@@ -222,6 +222,37 @@ def check_rope_invariants(o):
     return max(e)
 
 
+def check_rope_half(o):
+    """Half-split pairing: (1) equals the interleaved rotation after moving
+    element j to 2j and j + d/2 to 2j + 1 (and back); (2) pair j = 1 of
+    head_dim 8 at pos 3 rotates elements 1 and 5 by 0.3 rad, nothing else
+    moves; (3) pair norms are preserved and rope_inv undoes it; (4) the
+    pairing name is checked."""
+    r = RNG(13)
+    d, theta = 8, 10000.0
+    v = r.standard_normal((4, 3, d))
+    pos = np.array([0, 1, 5, 17])
+    perm = np.empty(d, dtype=int)                 # interleaved position of each half-split element
+    perm[: d // 2] = 2 * np.arange(d // 2)
+    perm[d // 2:] = 2 * np.arange(d // 2) + 1
+    vi = np.empty_like(v)
+    vi[..., perm] = v
+    w = o.rope(v, pos, theta, "half")
+    e = [_rel(w, o.rope(vi, pos, theta)[..., perm])]
+    unit = np.zeros((1, 1, d))
+    unit[0, 0, 1] = 1.0
+    w1 = o.rope(unit, [3], theta, "half")[0, 0]
+    e.append(abs(w1[1] - math.cos(0.3)) + abs(w1[5] - math.sin(0.3)) + np.abs(np.delete(w1, [1, 5])).sum())
+    e.append(_rel(np.hypot(w[..., : d // 2], w[..., d // 2:]), np.hypot(v[..., : d // 2], v[..., d // 2:])))
+    e.append(_rel(o.rope_inv(w, pos, theta, "half"), v))
+    try:
+        o.rope(v, pos, theta, "other")
+        e.append(1.0)
+    except ValueError:
+        pass
+    return max(e)
+
+
 def check_qknorm_closed_form(o):
     """gamma = 1 and pos = 0: each head of the output has mean square
     ms / (ms + eps) where ms is the head's input mean square."""
@@ -233,16 +264,16 @@ def check_qknorm_closed_form(o):
     return _rel(np.mean(out * out, axis=-1), ms / (ms + eps))
 
 
-def check_qknorm_grad(o):
+def check_qknorm_grad(o, pairing="interleaved"):
     r = RNG(12)
     q = r.standard_normal((3, 2, 8))
     g = 1 + 0.1 * r.standard_normal(8)
     pos = np.array([0, 7, 300])
     dout = r.standard_normal(q.shape)
-    dq, dg = o.qk_rmsnorm_rope_bwd(q, g, pos, 500000.0, 1e-6, dout)
+    dq, dg = o.qk_rmsnorm_rope_bwd(q, g, pos, 500000.0, 1e-6, dout, pairing)
 
     def L():
-        return float((dout * o.qk_rmsnorm_rope_fwd(q, g, pos, 500000.0, 1e-6)).sum())
+        return float((dout * o.qk_rmsnorm_rope_fwd(q, g, pos, 500000.0, 1e-6, pairing)).sum())
     return max(_rel(dq, _fd_grad(L, q)), _rel(dg, _fd_grad(L, g)))
 
 
@@ -674,6 +705,8 @@ ALL_CHECKS = {
     "rope_invariants": (check_rope_invariants, 1e-12),
     "qknorm_closed_form": (check_qknorm_closed_form, 1e-12),
     "qknorm_grad": (check_qknorm_grad, 1e-7),
+    "qknorm_grad_half_pairing": (lambda o: check_qknorm_grad(o, "half"), 1e-7),
+    "rope_half": (check_rope_half, 1e-12),
     "ce_uniform": (check_ce_uniform, 1e-14),
     "ce_library": (check_ce_library, 1e-7),
     "ce_all_ignored": (check_ce_all_ignored, 0.5),

@@ -182,6 +182,8 @@ def _source_mutant(old, new):
 
 
 MUTANTS = {
+    "rope_half_swapped_halves": _source_mutant("a, b = v[..., : d // 2], v[..., d // 2:]",
+                                               "a, b = v[..., d // 2:], v[..., : d // 2]"),
     "rmsnorm_nvfp4_rms_of_scaled_input": _source_mutant("(rms_inv(X, eps),)", "(rms_inv(u, eps),)"),
     "e2m1_ties_away_from_zero": _source_mutant("((d_hi == d_lo) & (hi % 2 == 0))", "(d_hi == d_lo)"),
     "nvfp4_block_scale_from_row_max": _source_mutant("ax.reshape(M, nb, NVFP4_BLOCK).max(axis=2)",
