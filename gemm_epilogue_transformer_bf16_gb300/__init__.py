@@ -24,6 +24,7 @@ __all__ = [
     "fold_gamma", "rms_rstd", "rmsnorm_scale", "rope_table", "gemm_epilogue", "EpilogueDesc",
     "rmsnorm_linear", "rmsnorm_linear_bwd", "linear_residual", "linear_residual_bwd",
     "linear_swiglu", "linear_swiglu_bwd", "linear_qknorm_rope", "linear_qknorm_rope_bwd",
+    "ROPE_INTERLEAVED", "ROPE_HALF",
     "linear_cross_entropy", "linear_cross_entropy_bwd", "linear_cross_entropy_noalloc", "workspace",
     "rmsnorm_linear_cross_entropy", "rmsnorm_linear_cross_entropy_bwd", "rms_rstd",
     "linear_sigmoid", "linear_sigmoid_bwd", "quantize_fp8_rows", "linear_fp8", "linear_swiglu_fp8", "quantize_nvfp4_rows", "rmsnorm_scale_nvfp4", "linear_nvfp4",
@@ -70,10 +71,10 @@ _SIGS = {
     "coda_linear_swiglu_bwd_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_swiglu_bwd": ([_P] * 16 + [_I64, _I64, _I64, _P, _SZ, _P, _P], ctypes.c_int),
     "coda_linear_qknorm_rope_workspace_size": ([_I64, _I64, _I32, _I32, _I32], _SZ),
-    "coda_linear_qknorm_rope": ([_P] * 7 + [_I32, _F, _I32, _I32, _I32] + [_P] * 4 + [_I64, _I64, _P, _SZ, _P],
+    "coda_linear_qknorm_rope": ([_P] * 7 + [_I32, _F, _I32, _I32, _I32, _I32] + [_P] * 4 + [_I64, _I64, _P, _SZ, _P],
                                 ctypes.c_int),
     "coda_linear_qknorm_rope_bwd_workspace_size": ([_I64, _I64, _I32, _I32, _I32], _SZ),
-    "coda_linear_qknorm_rope_bwd": ([_P] * 9 + [_I32, _F, _I32, _I32, _I32] + [_P] * 10
+    "coda_linear_qknorm_rope_bwd": ([_P] * 9 + [_I32, _F, _I32, _I32, _I32, _I32] + [_P] * 10
                                     + [_I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_cross_entropy_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_cross_entropy": ([_P, _P, _P, _I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
@@ -150,7 +151,7 @@ class EpilogueDesc(ctypes.Structure):
         ("target_logit", _P), ("vocab_tiles_per_unit", _I32),
         ("positions", _P), ("cos_sin", _P), ("max_pos", _I32), ("n_q_heads", _I32),
         ("n_kv_heads", _I32), ("head_dim", _I32), ("eps", _F), ("gamma_q", _P), ("gamma_k", _P),
-        ("Q", _P), ("K", _P), ("V", _P),
+        ("Q", _P), ("K", _P), ("V", _P), ("rope_pairing", _I32),
     ]
 
 
@@ -227,6 +228,18 @@ def _lead(t, lead):
 def _vec(t, lead):
     """A per-token vector given in the caller's leading shape, as [M]."""
     return t if (t is None or lead is None) else t.view(-1)
+
+
+ROPE_INTERLEAVED, ROPE_HALF = 0, 1
+
+
+def _pairing(p):
+    """RoPE pairing name -> coda_rope_pairing: "interleaved" pairs (2j, 2j+1),
+    "half" pairs (j, j + head_dim/2)."""
+    try:
+        return {"interleaved": ROPE_INTERLEAVED, "half": ROPE_HALF}[p]
+    except KeyError:
+        raise ValueError(f"RoPE pairing must be 'interleaved' or 'half', not {p!r}") from None
 
 
 def get_status(ws, stream=None):
@@ -410,7 +423,7 @@ def linear_swiglu_bwd(dY, X, Wg, Wu, Wd, g, u, H, rstd=None, gamma=None, dX_resi
 
 
 def linear_qknorm_rope(X, W, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, rstd=None, eps=1e-6,
-                       head_dim=128, save=True, out=None, ws=None, stream=None):
+                       head_dim=128, save=True, out=None, ws=None, stream=None, pairing="interleaved"):
     """QKV projection with per-head QK-RMSNorm and RoPE in the epilogue
     (coda_linear_qknorm_rope).  X may have leading dimensions ([..., Kdim],
     pos [...]); when it does and `out` is not given, Q, K, V, qk_save keep
@@ -433,7 +446,7 @@ def linear_qknorm_rope(X, W, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, rstd=Non
     _check("coda_linear_qknorm_rope", lib.coda_linear_qknorm_rope(
         _bf(X, "X"), _f32(rstd, "rstd"), _bf(W, "W"), _f32(gamma_q, "gamma_q"),
         _f32(gamma_k, "gamma_k"), _i32(pos, "pos"), _f32(cos_sin, "cos_sin"), max_pos, float(eps),
-        n_q, n_kv, head_dim, _bf(out["Q"], "Q"), _bf(out["K"], "K"), _bf(out["V"], "V"),
+        n_q, n_kv, head_dim, _pairing(pairing), _bf(out["Q"], "Q"), _bf(out["K"], "K"), _bf(out["V"], "V"),
         _bf(out.get("qk_save"), "qk_save"), M, Kd, _ptr(ws), ws.numel(), _stream(stream)))
     if shaped:
         out = {k: _lead(v, lead) for k, v in out.items()}
@@ -442,7 +455,7 @@ def linear_qknorm_rope(X, W, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, rstd=Non
 
 def linear_qknorm_rope_bwd(dQ, dK, dV, qk_save, V, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, X, W_qkv,
                            rstd=None, gamma_in=None, dX_resid=None, eps=1e-6, head_dim=128, ws=None, out=None,
-                           stream=None):
+                           stream=None, pairing="interleaved"):
     """QK-RMSNorm + RoPE projection backward (coda_linear_qknorm_rope_bwd);
     W_qkv not folded."""
     lib = load()
@@ -458,7 +471,8 @@ def linear_qknorm_rope_bwd(dQ, dK, dV, qk_save, V, gamma_q, gamma_k, pos, cos_si
     _check("coda_linear_qknorm_rope_bwd", lib.coda_linear_qknorm_rope_bwd(
         _bf(dQ, "dQ"), _bf(dK, "dK"), _bf(dV, "dV"), _bf(qk_save, "qk_save"), _bf(V, "V"),
         _f32(gamma_q, "gamma_q"), _f32(gamma_k, "gamma_k"), _i32(pos, "pos"), _f32(cos_sin, "cos_sin"),
-        max_pos, float(eps), n_q, n_kv, head_dim, _bf(X, "X"), _f32(rstd, "rstd"), _f32(gamma_in, "gamma_in"),
+        max_pos, float(eps), n_q, n_kv, head_dim, _pairing(pairing), _bf(X, "X"), _f32(rstd, "rstd"),
+        _f32(gamma_in, "gamma_in"),
         _bf(W_qkv, "W_qkv"), _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"), _bf(out["dW"], "dW"),
         _f32(out.get("dgamma_in"), "dgamma_in"), _f32(out["dgamma_q"], "dgamma_q"), _f32(out["dgamma_k"], "dgamma_k"),
         M, Kd, _ptr(ws), ws.numel(), _stream(stream)))

@@ -125,6 +125,7 @@ struct Plan {
   int fp8 = 0;  // e4m3 operands (K-major only)
   int64_t M = 0, N = 0, K = 0;
   int n_per_unit = 1;
+  int rope_half = 0;  // QkRope: half-split RoPE pairs
   EpiArgs e{};
 };
 
@@ -259,7 +260,10 @@ int dispatch(const Plan& p, int sms, int cg, cudaStream_t s, const CUtensorMap* 
     case coda::EpiKind::Plain: err = coda::launch_gemm_plain(nu, sms, cg, s, maps, a); break;
     case coda::EpiKind::Swiglu: err = coda::launch_gemm_swiglu(nu, sms, cg, s, maps, a); break;
     case coda::EpiKind::DSwiglu: err = coda::launch_gemm_dswiglu(nu, sms, cg, s, maps, a); break;
-    case coda::EpiKind::QkRope: err = coda::launch_gemm_qkrope(nu, sms, cg, s, maps, a); break;
+    case coda::EpiKind::QkRope:
+      err = p.rope_half ? coda::launch_gemm_qkrope_half(nu, sms, cg, s, maps, a)
+                        : coda::launch_gemm_qkrope(nu, sms, cg, s, maps, a);
+      break;
     case coda::EpiKind::CeLse: err = coda::launch_gemm_celse(nu, sms, cg, s, maps, a); break;
     case coda::EpiKind::CeDlogits: err = coda::launch_gemm_cedlogits(nu, sms, cg, s, maps, a); break;
     case coda::EpiKind::ColDot: err = coda::launch_gemm_coldot(nu, sms, cg, s, maps, a); break;
@@ -617,6 +621,8 @@ int coda_gemm_epilogue(const coda_epilogue_desc* d, const coda_bf16* A, int64_t 
     case CODA_MAP_QKNORM_ROPE:
       p.kind = coda::EpiKind::QkRope;
       if (d->head_dim != 128) return CODA_ERR_UNSUPPORTED;
+      if (d->rope_pairing != CODA_ROPE_INTERLEAVED && d->rope_pairing != CODA_ROPE_HALF) return CODA_ERR_INVALID_ARG;
+      p.rope_half = d->rope_pairing == CODA_ROPE_HALF;
       if (d->n_q_heads <= 0 || d->n_kv_heads < 0) return CODA_ERR_INVALID_ARG;
       if (N != static_cast<int64_t>(d->n_q_heads + 2 * d->n_kv_heads) * 128) return CODA_ERR_INVALID_ARG;
       if (!d->positions || !d->cos_sin || d->max_pos <= 0 || !d->gamma_q || !d->Q) return CODA_ERR_INVALID_ARG;
@@ -1144,7 +1150,8 @@ size_t coda_linear_qknorm_rope_workspace_size(int64_t, int64_t, int32_t, int32_t
 
 int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf16* W, const float* gamma_q,
                             const float* gamma_k, const int32_t* pos, const float* cos_sin, int32_t max_pos,
-                            float eps, int32_t n_q, int32_t n_kv, int32_t head_dim, coda_bf16* Q, coda_bf16* K,
+                            float eps, int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t rope_pairing,
+                            coda_bf16* Q, coda_bf16* K,
                             coda_bf16* V, coda_bf16* qk_save, int64_t M, int64_t Kdim, void* ws, size_t ws_bytes,
                             coda_stream stream) {
   if (head_dim != 128) return CODA_ERR_UNSUPPORTED;
@@ -1165,6 +1172,7 @@ int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf
   d.n_q_heads = n_q;
   d.n_kv_heads = n_kv;
   d.head_dim = head_dim;
+  d.rope_pairing = rope_pairing;
   d.eps = eps;
   d.gamma_q = gamma_q;
   d.gamma_k = gamma_k;
@@ -1197,13 +1205,15 @@ size_t coda_linear_qknorm_rope_bwd_workspace_size(int64_t M, int64_t Kdim, int32
 int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const coda_bf16* dV,
                                 const coda_bf16* qk_save, const coda_bf16* V, const float* gamma_q,
                                 const float* gamma_k, const int32_t* pos, const float* cos_sin, int32_t max_pos,
-                                float eps, int32_t n_q, int32_t n_kv, int32_t head_dim, const coda_bf16* X,
+                                float eps, int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t rope_pairing,
+                                const coda_bf16* X,
                                 const float* rstd, const float* gamma_in, const coda_bf16* W_qkv,
                                 const coda_bf16* dX_resid, coda_bf16* dX, coda_bf16* dW_qkv,
                                 float* dgamma_in, float* dgamma_q, float* dgamma_k, int64_t M, int64_t Kdim, void* ws,
                                 size_t ws_bytes, coda_stream stream) {
   if (head_dim != 128) return CODA_ERR_UNSUPPORTED;
   if (n_q <= 0 || n_kv <= 0 || max_pos <= 0) return CODA_ERR_INVALID_ARG;
+  if (rope_pairing != CODA_ROPE_INTERLEAVED && rope_pairing != CODA_ROPE_HALF) return CODA_ERR_INVALID_ARG;
   const int64_t N = static_cast<int64_t>(n_q + 2 * n_kv) * head_dim;
   CK(dims_ok(M, N, Kdim));
   CK(ws_ok(ws, ws_bytes, coda_linear_qknorm_rope_bwd_workspace_size(M, Kdim, n_q, n_kv, head_dim)));
@@ -1235,7 +1245,7 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
   cudaStream_t s = S(stream);
   CU(coda::launch_qk_bwd(BF(dQ), BF(dK), BF(dV), BF(qk_save), BF(V), gamma_q, gamma_k, pos,
                          reinterpret_cast<const float2*>(cos_sin), max_pos, eps, n_q, n_kv, rstd, M, Gp, srow, dgqk,
-                         nblk, status, s));
+                         nblk, status, s, rope_pairing == CODA_ROPE_HALF));
   CU(coda::launch_colsum(dgqk, nblk, 128, 256, dgamma_q, s));
   CU(coda::launch_colsum(dgqk + 128, nblk, 128, 256, dgamma_k, s));
   if (norm)

@@ -484,6 +484,9 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* p, const float* v) {
   *reinterpret_cast<uint2*>(p) = q;
 }
 
+// HALF: RoPE pairs (j, j + 64) of each head (lanes l and l + 16 hold the
+// two elements of a pair) instead of interleaved pairs (2j, 2j + 1).
+template <bool HALF>
 __global__ void __launch_bounds__(QK_BWD_WARPS * 32)
     qk_bwd_kernel(const __nv_bfloat16* __restrict__ dQ, const __nv_bfloat16* __restrict__ dK,
                   const __nv_bfloat16* __restrict__ dV, const __nv_bfloat16* __restrict__ qk_save,
@@ -514,6 +517,12 @@ __global__ void __launch_bounds__(QK_BWD_WARPS * 32)
     }
     const float2 c0 = cs[static_cast<int64_t>(p) * (D / 2) + 2 * lane];
     const float2 c1 = cs[static_cast<int64_t>(p) * (D / 2) + 2 * lane + 1];
+    // half-split: this lane's elements 4 (lane % 16) + i of a half, angles j = 4 (lane % 16) + i
+    float2 ch[4];
+    if constexpr (HALF) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ch[i] = cs[static_cast<int64_t>(p) * (D / 2) + 4 * (lane & 15) + i];
+    }
     const float r = rstd ? rstd[row] : 1.f;
     float s = 0.f;
     for (int h = 0; h < n_q + n_kv; ++h) {
@@ -527,11 +536,22 @@ __global__ void __launch_bounds__(QK_BWD_WARPS * 32)
       float n[4], dn[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) n[i] = x[i] * rho;
-      // inverse rotation of pairs (0,1) with c0 and (2,3) with c1
-      dn[0] = d[0] * c0.x + d[1] * c0.y;
-      dn[1] = -d[0] * c0.y + d[1] * c0.x;
-      dn[2] = d[2] * c1.x + d[3] * c1.y;
-      dn[3] = -d[2] * c1.y + d[3] * c1.x;
+      if constexpr (HALF) {
+        // inverse rotation of (first half, second half) element pairs; the
+        // partner sits in lane l ^ 16 at the same index
+        const bool second = lane >= 16;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float dp = __shfl_xor_sync(0xffffffffu, d[i], 16);
+          dn[i] = second ? -dp * ch[i].y + d[i] * ch[i].x : d[i] * ch[i].x + dp * ch[i].y;
+        }
+      } else {
+        // inverse rotation of pairs (0,1) with c0 and (2,3) with c1
+        dn[0] = d[0] * c0.x + d[1] * c0.y;
+        dn[1] = -d[0] * c0.y + d[1] * c0.x;
+        dn[2] = d[2] * c1.x + d[3] * c1.y;
+        dn[3] = -d[2] * c1.y + d[3] * c1.x;
+      }
       const float* g = is_q ? g_q : g_k;
       float* acc = is_q ? aq : ak;
       float dng[4];
@@ -583,9 +603,13 @@ cudaError_t launch_qk_bwd(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, cons
                           const __nv_bfloat16* qk_save, const __nv_bfloat16* V, const float* gq, const float* gk,
                           const int32_t* pos, const float2* cs, int max_pos, float eps, int n_q, int n_kv,
                           const float* rstd, int64_t M, __nv_bfloat16* Gp, float* srow, float* dgam_part,
-                          int nblk, int* status, cudaStream_t s) {
-  qk_bwd_kernel<<<nblk, QK_BWD_WARPS * 32, 0, s>>>(dQ, dK, dV, qk_save, V, gq, gk, pos, cs, max_pos, eps, n_q, n_kv,
-                                                   rstd, M, Gp, srow, dgam_part, status);
+                          int nblk, int* status, cudaStream_t s, bool rope_half) {
+  if (rope_half)
+    qk_bwd_kernel<true><<<nblk, QK_BWD_WARPS * 32, 0, s>>>(dQ, dK, dV, qk_save, V, gq, gk, pos, cs, max_pos, eps,
+                                                           n_q, n_kv, rstd, M, Gp, srow, dgam_part, status);
+  else
+    qk_bwd_kernel<false><<<nblk, QK_BWD_WARPS * 32, 0, s>>>(dQ, dK, dV, qk_save, V, gq, gk, pos, cs, max_pos, eps,
+                                                            n_q, n_kv, rstd, M, Gp, srow, dgam_part, status);
   return cudaGetLastError();
 }
 

@@ -678,7 +678,9 @@ struct EpiSigmoid {
 // pairs (2i, 2i+1) rotated by the (cos, sin) of (pos, i); optional save of x
 // (pre-norm, out1).  v heads: rs*acc stored as is.
 // ---------------------------------------------------------------------------
-template <int BN>
+// HALF: RoPE pairs (j, j + 64) of each head instead of interleaved pairs
+// (2j, 2j + 1); the angle of pair j is the same in both.
+template <int BN, bool HALF = false>
 struct EpiQkRope {
   static_assert(BN % 128 == 0, "heads are 128 wide");
   struct State {};
@@ -740,26 +742,58 @@ struct EpiQkRope {
         }
       }
       const float rho = rsqrtf(ss * (1.f / D) + e.eps);
+      if constexpr (HALF) {
+        // pair j = c + i of the first half with j + 64 of the second half
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        float v[32];
-        __syncwarp();
-        tmem_ld32(tcol + c, v);
-        if (rv) {
-          float gm[32];
+        for (int c = 0; c < D / 2; c += 32) {
+          float v1[32], v2[32];
+          __syncwarp();
+          tmem_ld32(tcol + c, v1);
+          tmem_ld32(tcol + D / 2 + c, v2);
+          if (rv) {
+            float g1[32], g2[32];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) load_f32x8(gamma + c + g * 8, gm + g * 8);
-          float o[32];
+            for (int g = 0; g < 4; ++g) {
+              load_f32x8(gamma + c + g * 8, g1 + g * 8);
+              load_f32x8(gamma + D / 2 + c + g * 8, g2 + g * 8);
+            }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 r = cs[c / 2 + i];
-            const float a = v[2 * i] * rs * rho * gm[2 * i];
-            const float b = v[2 * i + 1] * rs * rho * gm[2 * i + 1];
-            o[2 * i] = a * r.x - b * r.y;
-            o[2 * i + 1] = a * r.y + b * r.x;
+            for (int i = 0; i < 32; ++i) {
+              const float2 r = cs[c + i];
+              const float a = v1[i] * rs * rho * g1[i];
+              const float b = v2[i] * rs * rho * g2[i];
+              v1[i] = a * r.x - b * r.y;
+              v2[i] = a * r.y + b * r.x;
+            }
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              store_bf16x8(out + c + g * 8, v1 + g * 8, e.st_stream);
+              store_bf16x8(out + D / 2 + c + g * 8, v2 + g * 8, e.st_stream);
+            }
           }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          float v[32];
+          __syncwarp();
+          tmem_ld32(tcol + c, v);
+          if (rv) {
+            float gm[32];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) store_bf16x8(out + c + g * 8, o + g * 8, e.st_stream);
+            for (int g = 0; g < 4; ++g) load_f32x8(gamma + c + g * 8, gm + g * 8);
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 r = cs[c / 2 + i];
+              const float a = v[2 * i] * rs * rho * gm[2 * i];
+              const float b = v[2 * i + 1] * rs * rho * gm[2 * i + 1];
+              o[2 * i] = a * r.x - b * r.y;
+              o[2 * i + 1] = a * r.y + b * r.x;
+            }
+#pragma unroll
+            for (int g = 0; g < 4; ++g) store_bf16x8(out + c + g * 8, o + g * 8, e.st_stream);
+          }
         }
       }
     }

@@ -23,6 +23,8 @@ cudaError_t launch_gemm_dswiglu(int num_units, int sms, int cg, cudaStream_t s, 
                                const GemmArgs& a);
 cudaError_t launch_gemm_qkrope(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
+cudaError_t launch_gemm_qkrope_half(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
+                                    const GemmArgs& a);
 cudaError_t launch_gemm_celse(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                const GemmArgs& a);
 cudaError_t launch_gemm_cedlogits(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
@@ -99,7 +101,7 @@ cudaError_t launch_qk_bwd(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, cons
                           const __nv_bfloat16* qk_save, const __nv_bfloat16* V, const float* gq, const float* gk,
                           const int32_t* pos, const float2* cs, int max_pos, float eps, int n_q, int n_kv,
                           const float* rstd, int64_t M, __nv_bfloat16* Gp, float* srow, float* dgam_part,
-                          int nblk, int* status, cudaStream_t s);
+                          int nblk, int* status, cudaStream_t s, bool rope_half = false);
 
 constexpr int QK_BWD_WARPS = 8;
 constexpr int CE_COMBINE_THREADS = 256;

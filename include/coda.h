@@ -89,6 +89,12 @@ enum {
   CODA_MAP_DSIGMOID = 8      /* recomputed z = rs*acc, dY = aux_in[1]: aux_out[0] = dY (*aux_in[0]) s(1-s), aux_out[1] = dY s */
 };
 
+/* RoPE pairing of a head's elements (the pages leave the convention open;
+ * both are supported): CODA_ROPE_INTERLEAVED rotates pairs (2j, 2j+1),
+ * CODA_ROPE_HALF rotates pairs (j, j + head_dim/2); pair j's angle is
+ * pos * theta^(-2j/head_dim) in both. */
+typedef enum coda_rope_pairing { CODA_ROPE_INTERLEAVED = 0, CODA_ROPE_HALF = 1 } coda_rope_pairing;
+
 /*
  * Epilogue descriptor: which primitives run on each output tile before it is
  * written ("CODA" §3.1: element-wise/pairwise maps, rank-1 vector loads,
@@ -131,6 +137,7 @@ typedef struct coda_epilogue_desc {
   coda_bf16* Q;                  /* [M, n_q*head_dim] */
   coda_bf16* K;                  /* [M, n_kv*head_dim] */
   coda_bf16* V;                  /* [M, n_kv*head_dim] */
+  int32_t rope_pairing;          /* coda_rope_pairing (0 = interleaved) */
 } coda_epilogue_desc;
 
 /* ------------------------------------------------------------------------
@@ -326,14 +333,15 @@ int coda_linear_swiglu_bwd(const coda_bf16* dY, const coda_bf16* X, const float*
  * head_dim must be 128.  Column order of W rows: n_q q heads, then
  * n_kv k heads, then n_kv v heads.  X [M, Kdim]; W [(n_q+2n_kv)*128, Kdim];
  * rstd [M] (NULL: r = 1); gamma_q, gamma_k [128]; pos [M] int32 in
- * [0, max_pos); cos_sin from coda_rope_table.  Outputs Q [M, n_q*128],
+ * [0, max_pos); cos_sin from coda_rope_table; rope_pairing a
+ * coda_rope_pairing (the kernel is compiled for each).  Outputs Q [M, n_q*128],
  * K, V [M, n_kv*128]; qk_save [M, (n_q+n_kv)*128] pre-norm q|k or NULL.
  * ---------------------------------------------------------------------- */
 size_t coda_linear_qknorm_rope_workspace_size(int64_t M, int64_t Kdim, int32_t n_q, int32_t n_kv, int32_t head_dim);
 int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf16* W,
                             const float* gamma_q, const float* gamma_k, const int32_t* pos,
                             const float* cos_sin, int32_t max_pos, float eps,
-                            int32_t n_q, int32_t n_kv, int32_t head_dim,
+                            int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t rope_pairing,
                             coda_bf16* Q, coda_bf16* K, coda_bf16* V, coda_bf16* qk_save,
                             int64_t M, int64_t Kdim, void* ws, size_t ws_bytes, coda_stream stream);
 
@@ -354,7 +362,7 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
                                 const coda_bf16* qk_save, const coda_bf16* V,
                                 const float* gamma_q, const float* gamma_k, const int32_t* pos,
                                 const float* cos_sin, int32_t max_pos, float eps,
-                                int32_t n_q, int32_t n_kv, int32_t head_dim,
+                                int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t rope_pairing,
                                 const coda_bf16* X, const float* rstd, const float* gamma_in,
                                 const coda_bf16* W_qkv, const coda_bf16* dX_resid,
                                 coda_bf16* dX, coda_bf16* dW_qkv, float* dgamma_in,

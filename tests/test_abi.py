@@ -61,9 +61,10 @@ def test_epilogue_desc_layout_matches_header():
 #include <stddef.h>
 #include "coda.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(coda_epilogue_desc), offsetof(coda_epilogue_desc, partials),
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(coda_epilogue_desc), offsetof(coda_epilogue_desc, partials),
          offsetof(coda_epilogue_desc, K2), offsetof(coda_epilogue_desc, dloss),
-         offsetof(coda_epilogue_desc, eps), offsetof(coda_epilogue_desc, V));
+         offsetof(coda_epilogue_desc, eps), offsetof(coda_epilogue_desc, V),
+         offsetof(coda_epilogue_desc, rope_pairing));
   return 0;
 }
 '''
@@ -74,7 +75,8 @@ int main(void) {
         subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe])
         got = [int(x) for x in subprocess.check_output([exe]).split()]
     D = coda.EpilogueDesc
-    want = [ctypes.sizeof(D), D.partials.offset, D.K2.offset, D.dloss.offset, D.eps.offset, D.V.offset]
+    want = [ctypes.sizeof(D), D.partials.offset, D.K2.offset, D.dloss.offset, D.eps.offset, D.V.offset,
+            D.rope_pairing.offset]
     assert got == want
 
 
@@ -100,8 +102,11 @@ def test_rejects_bad_arguments_on_host(lib):
     # null workspace
     assert lib.coda_linear_residual(FAKE, FAKE, None, FAKE, 1e-6, None, None, None, 16, 64, 64, None, 4096, None) == 4
     # head_dim other than 128 is unsupported
-    assert lib.coda_linear_qknorm_rope(*([FAKE] * 7), 16, 1e-6, 2, 1, 64, *([FAKE] * 4), 16, 64, ws, 4096,
+    assert lib.coda_linear_qknorm_rope(*([FAKE] * 7), 16, 1e-6, 2, 1, 64, 0, *([FAKE] * 4), 16, 64, ws, 4096,
                                        None) == 3
+    # unknown RoPE pairing
+    assert lib.coda_linear_qknorm_rope_bwd(*([FAKE] * 9), 16, 1e-6, 2, 1, 128, 7, *([FAKE] * 10), 16, 64, ws,
+                                           1 << 30, None) == 1
     # K == 0 with work to do
     assert lib.coda_linear_residual_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, 16, 64, 0, ws, 4096, None) == 3
     # gain output: gamma_next and U_out come together

@@ -363,3 +363,44 @@ def test_leading_dims_match_flat_calls(coda):
 
     with pytest.raises(ValueError):
         coda.linear_swiglu(y3.transpose(0, 1), t["Wg"], t["Wu"])
+
+
+# ---------------------------------------------------------------- QK-RMSNorm + RoPE, both pairings
+@pytest.mark.parametrize("pairing", ["interleaved", "half"])
+def test_linear_qknorm_rope_pairings(coda, pairing):
+    """The fused QKV projection with per-head QK-RMSNorm and RoPE, forward and
+    backward, for interleaved pairs (2j, 2j+1) and half-split pairs
+    (j, j + 64), against the oracle composed from its RMSNorm, per-head
+    QK-norm + RoPE and their backward passes (ragged token count)."""
+    s = RAGGED_BLOCK
+    t = synth.make_block(s, seed=21)
+    d = dev(t)
+    o = {k: to_np(v) for k, v in t.items()}
+    cs = coda.rope_table(s.theta, s.head_dim, s.seq_len)
+    r, U = coda.rmsnorm_scale(d["x0"], d["gamma_attn"], s.eps)
+    out = coda.linear_qknorm_rope(U, d["Wqkv"], d["gamma_q"], d["gamma_k"], d["pos"], cs, s.n_q, s.n_kv, rstd=r,
+                                  eps=s.eps, pairing=pairing)
+    g = coda.linear_qknorm_rope_bwd(d["dQ"], d["dK"], d["dV"], out["qk_save"], out["V"], d["gamma_q"], d["gamma_k"],
+                                    d["pos"], cs, s.n_q, s.n_kv, d["x0"], d["Wqkv"], rstd=r, gamma_in=d["gamma_attn"],
+                                    eps=s.eps, pairing=pairing)
+    M, D = s.tokens, s.head_dim
+    xn = O.rmsnorm(o["x0"], o["gamma_attn"], s.eps)
+    qkv = xn @ o["Wqkv"].T
+    q = qkv[:, : s.n_q * D].reshape(M, s.n_q, D)
+    k = qkv[:, s.n_q * D:(s.n_q + s.n_kv) * D].reshape(M, s.n_kv, D)
+    pos = t["pos"].numpy()
+    Qr = O.qk_rmsnorm_rope_fwd(q, o["gamma_q"], pos, s.theta, s.eps, pairing).reshape(M, -1)
+    Kr = O.qk_rmsnorm_rope_fwd(k, o["gamma_k"], pos, s.theta, s.eps, pairing).reshape(M, -1)
+    assert_bf16(out["Q"], Qr, f"Q ({pairing})")
+    assert_bf16(out["K"], Kr, f"K ({pairing})")
+    assert_bf16(out["V"], qkv[:, (s.n_q + s.n_kv) * D:], f"V ({pairing})")
+    dq, dgq = O.qk_rmsnorm_rope_bwd(q, o["gamma_q"], pos, s.theta, s.eps, o["dQ"].reshape(M, s.n_q, D), pairing)
+    dk, dgk = O.qk_rmsnorm_rope_bwd(k, o["gamma_k"], pos, s.theta, s.eps, o["dK"].reshape(M, s.n_kv, D), pairing)
+    dqkv = np.concatenate([dq.reshape(M, -1), dk.reshape(M, -1), o["dV"]], axis=1)
+    dx, dgin = O.rmsnorm_bwd(o["x0"], o["gamma_attn"], s.eps, dqkv @ o["Wqkv"])
+    assert_bf16(g["dX"], dx, f"dX ({pairing})")
+    assert_bf16(g["dW"], dqkv.T @ xn, f"dWqkv ({pairing})")
+    # gain gradients are sums over tokens with cancellation: the RMS-relative rule, as for the block
+    assert_bf16(g["dgamma_in"], dgin, f"dgamma_in ({pairing})")
+    assert_bf16(g["dgamma_q"], dgq, f"dgamma_q ({pairing})")
+    assert_bf16(g["dgamma_k"], dgk, f"dgamma_k ({pairing})")
