@@ -321,6 +321,32 @@ def check_ce_library(o):
     return max(e)
 
 
+def check_ce_lse_merge(o):
+    """Per-chunk (max, sum-exp) states over any split of the vocabulary,
+    merged as m = max_c m_c, s = sum_c s_c exp(m_c - m), give the full-row
+    lse = m + log s of the oracle: the state the online-LSE epilogue carries
+    and its combine pass merges."""
+    r = RNG(16)
+    M, K, V = 4, 6, 23
+    X = r.standard_normal((M, K)) * 3
+    W = r.standard_normal((V, K))
+    lab = np.array([0, 5, 22, 11])
+    full = o.linear_cross_entropy_fwd(X, W, lab)["lse"]
+    e = []
+    for cuts in ([7, 15], [1, 2, 3, 20], [11]):
+        m = np.full(M, -np.inf)
+        acc = np.zeros(M)
+        for lo, hi in zip([0] + cuts, cuts + [V]):
+            z = X @ W[lo:hi].T                      # the chunk's logits
+            mc = z.max(axis=1)
+            sc = np.exp(z - mc[:, None]).sum(axis=1)
+            mn = np.maximum(m, mc)
+            acc = acc * np.exp(m - mn) + sc * np.exp(mc - mn)
+            m = mn
+        e.append(_rel(m + np.log(acc), full))
+    return max(e)
+
+
 def check_ce_all_ignored(o):
     """Every row ignored: loss = 0/0 = NaN (torch's mean reduction), zero grad."""
     r = RNG(14)
@@ -710,6 +736,7 @@ ALL_CHECKS = {
     "ce_uniform": (check_ce_uniform, 1e-14),
     "ce_library": (check_ce_library, 1e-7),
     "ce_all_ignored": (check_ce_all_ignored, 0.5),
+    "ce_lse_merge": (check_ce_lse_merge, 1e-14),
     "block_special_cases": (check_block_special_cases, 1e-12),
     "block_grad": (check_block_grad, 1e-7),
 }
