@@ -482,6 +482,27 @@ def main():
     other = {}
     legs = set(args.legs.split(","))
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def time_calls(fn, n=5, warm=2):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize(dev)
+        ev[0].record(stream)
+        for _ in range(n):
+            fn()
+        ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        return ev[0].elapsed_time(ev[1]) / n
+
+    def unfused_leg(entry, fn, ours_ms, n=3):
+        """Time the same workload as eager torch (cuBLAS matmuls, unfused
+        element-wise ops, autograd backward) and add it to the leg's entry."""
+        if args.no_unfused:
+            return
+        ms = time_calls(fn, n=n, warm=1)
+        entry["unfused_ms"] = round(ms, 3)
+        entry["speedup_vs_unfused"] = round(ms / ours_ms, 3)
+
     if not args.no_ce and "ce" in legs:
         from gemm_epilogue_transformer_bf16_gb300.block import LinearCE
         cs_ = synth.FULL["linear_ce"]
@@ -515,7 +536,19 @@ def main():
             "fwd_ms": round(mf, 3), "bwd_ms": round(mb, 3),
             "fwd_tflops": round(f_fwd / (mf / 1e3) / 1e12, 1),
             "fwd_bwd_tflops": round(f_all / ((mf + mb) / 1e3) / 1e12, 1)}
-        del ce, dc
+        del ce
+        Xr = dc["X"].detach().requires_grad_(True)
+        Wr = dc["W"].detach().requires_grad_(True)
+        lab_long = dc["labels"].long()
+
+        def ce_unfused():
+            # bf16 logits from cuBLAS (2.1 GB, they fit), fp32 cross-entropy, autograd backward
+            z = Xr @ Wr.t()
+            torch.nn.functional.cross_entropy(z.float(), lab_long, ignore_index=cs_.ignore_index).backward()
+            Xr.grad = None
+            Wr.grad = None
+        unfused_leg(other["linear_cross_entropy"], ce_unfused, mf + mb)
+        del dc, Xr, Wr
 
     if not args.no_ce and ("fp8" in legs or "nvfp4" in legs):
         T_, H_, I_ = s.tokens, s.hidden, s.inter
@@ -584,17 +617,6 @@ def main():
     # same way: the SwiGLU MLP at hidden 4096 and the RMSNorm-reparameterised
     # projection + residual at 4096 x 2048 (gain folded into W: the standalone
     # operator's form).  FLOPs 2*M*N*K per GEMM.
-    def time_calls(fn, n=5, warm=2):
-        for _ in range(warm):
-            fn()
-        torch.cuda.synchronize(dev)
-        ev[0].record(stream)
-        for _ in range(n):
-            fn()
-        ev[1].record(stream)
-        torch.cuda.synchronize(dev)
-        return ev[0].elapsed_time(ev[1]) / n
-
     if not args.no_ce and "mlp" in legs:
         s3 = synth.FULL["mlp"]
         d3 = {k: v.to(dev) for k, v in synth.make_mlp(s3, seed=rank).items()}
@@ -614,7 +636,17 @@ def main():
             "workload": f"SwiGLU MLP fwd+bwd, tokens {s3.tokens}, hidden {s3.hidden}, intermediate {s3.inter}",
             "ms": round(m3, 3), "tflops": round(f3 / (m3 / 1e3) / 1e12, 1),
             "frac_of_sustained": round(f3 / (m3 / 1e3) / 1e12 / sustained, 4)}
-        del d3, o3, ws3
+        del o3, ws3
+        p3 = {k: d3[k].detach().requires_grad_(True) for k in ("X", "Wg", "Wu", "Wd")}
+
+        def mlp_unfused():
+            p = p3
+            H = torch.nn.functional.silu(p["X"] @ p["Wg"].t()) * (p["X"] @ p["Wu"].t())
+            (d3["R"] + H @ p["Wd"].t()).backward(d3["dY"])
+            for v in p.values():
+                v.grad = None
+        unfused_leg(other["mlp_swiglu"], mlp_unfused, m3)
+        del d3, p3
     if not args.no_ce and "rms" in legs:
         s2 = synth.FULL["rmsnorm_linear"]
         d2 = {k: v.to(dev) for k, v in synth.make_rms_linear(s2, seed=rank).items()}
@@ -657,7 +689,19 @@ def main():
             "ms": round(m2, 3), "tflops": round(f2 / (m2 / 1e3) / 1e12, 1),
             "frac_of_sustained": round(f2 / (m2 / 1e3) / 1e12 / sustained, 4),
             "graph_ms": round(mg2, 3), "graph_tflops": round(f2 / (mg2 / 1e3) / 1e12, 1)}
-        del d2, graph2
+        del graph2
+        p2 = {"X": d2["X"].detach().requires_grad_(True), "W": d2["W"].detach().requires_grad_(True),
+              "gamma": d2["gamma"].detach().requires_grad_(True)}
+
+        def rms_unfused():
+            p = p2
+            xf = p["X"].float()
+            xn = (xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + s2.eps) * p["gamma"]).to(torch.bfloat16)
+            (d2["R"] + xn @ p["W"].t()).backward(d2["G"])
+            for v in p.values():
+                v.grad = None
+        unfused_leg(other["rmsnorm_linear"], rms_unfused, m2, n=20)
+        del d2, p2
 
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None
