@@ -172,6 +172,29 @@ int group_m(int cg) {
 // the same speed); smaller outputs stay in L2 for the kernel that reads them
 // next.  CODA_L2_HINTS overrides with a fixed bit set.
 constexpr int64_t STREAM_STORE_BYTES = 64ll << 20;
+
+// The dSwiGLU epilogue requests its tile's rows of g and u into L2 before its
+// chunk loop (on by default; CODA_AUX_PREFETCH=0 turns it off, for
+// comparisons).
+int aux_prefetch() {
+  static const int v = [] {
+    const char* e = std::getenv("CODA_AUX_PREFETCH");
+    return (e && e[0] == '0') ? 0 : 1;
+  }();
+  return v;
+}
+
+// A two-pair GEMM whose units fill the grid's last wave poorly runs as CTA
+// pairs when that takes at least 7 % fewer waves (a pair and a two-pair unit
+// take the same time per CTA; pairs lose the B multicast between pairs,
+// worth about 3 %).  On by default; CODA_PAIR_WAVES=0 turns it off.
+bool pair_waves_enabled() {
+  static const bool v = [] {
+    const char* e = std::getenv("CODA_PAIR_WAVES");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
 int l2_hints() {
   static const int v = [] {
     const char* e = std::getenv("CODA_L2_HINTS");
@@ -338,6 +361,7 @@ int prepare(const Plan& p, int* status, int cg, int nb_base, int n_tiles, CUtens
     const int64_t esz = p.e.d_f32 ? 4 : 2;
     a.e.st_stream = stream_stores(p.M * cols * esz * n_out);
   }
+  a.e.aux_prefetch = aux_prefetch();
   return CODA_OK;
 }
 
@@ -390,7 +414,8 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   const int num_n = static_cast<int>(cdiv(p.N, p.b_dual ? BN / 2 : BN));
   CUtensorMap maps[4];
   GemmArgs a;
-  if (cg == 4 && p.n_per_unit <= 1 && num_n >= 4 && split_enabled()) {
+  int cg_run = cg;
+  if (cg == 4 && p.n_per_unit <= 1 && (split_enabled() || pair_waves_enabled())) {
     // resident clusters of the two-pair and the pair kernel
     int q_max = 0, p_max = 0;
     CK(prepare(p, status, 4, 0, num_n, maps, a));
@@ -400,11 +425,10 @@ int run(const Plan& p, int* status, cudaStream_t s) {
     a.query_clusters = &p_max;
     CK(dispatch(p, sms, 2, s, maps, a));
     const int extra = p_max - 2 * q_max;  // pairs that fit beside a full two-pair grid
-    if (q_max > 0 && extra > 0) {
-      const int64_t mq = cdiv(p.M, 4 * coda::BM), mp = cdiv(p.M, 2 * coda::BM);
-      const int64_t t0 = cdiv(mq * num_n, q_max);
-      int best = 0;
-      int64_t tbest = t0;
+    const int64_t mq = cdiv(p.M, 4 * coda::BM), mp = cdiv(p.M, 2 * coda::BM);
+    int best = 0;
+    int64_t tbest = q_max > 0 ? cdiv(mq * num_n, q_max) : 0;
+    if (q_max > 0 && extra > 0 && num_n >= 4 && split_enabled()) {
       for (int np = 1; np <= num_n / 4; ++np) {
         const int64_t t = std::max(cdiv(mq * (num_n - np), q_max), cdiv(mp * np, extra));
         if (t < tbest) {
@@ -412,7 +436,13 @@ int run(const Plan& p, int* status, cudaStream_t s) {
           best = np;
         }
       }
-      cudaStream_t s2 = best > 0 ? side_stream(s) : nullptr;
+    }
+    if (q_max > 0 && p_max > 0 && pair_waves_enabled() && cdiv(mp * num_n, p_max) * 100 <= tbest * 93) {
+      cg_run = 2;
+      best = 0;
+    }
+    if (best > 0) {
+      cudaStream_t s2 = side_stream(s);
       if (s2) {
         EventSet ev(2);
         if (!ev.ok()) return CODA_ERR_CUDA;
@@ -431,8 +461,8 @@ int run(const Plan& p, int* status, cudaStream_t s) {
       }
     }
   }
-  CK(prepare(p, status, cg, 0, num_n, maps, a));
-  return dispatch(p, sms, cg, s, maps, a);
+  CK(prepare(p, status, cg_run, 0, num_n, maps, a));
+  return dispatch(p, sms, cg_run, s, maps, a);
 }
 
 

@@ -318,25 +318,58 @@ struct EpiDSwiglu {
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
     float dot = 0.f;
     const int row0 = row - static_cast<int>(threadIdx.x & 31);
+    // The thread's row segments of g and u for the whole tile are requested
+    // into L2 first, and each 32-column chunk's g and u are loaded into
+    // registers one chunk ahead, so that their latency overlaps the previous
+    // chunk's math and stores (at K = 4096 one round trip per chunk made
+    // this epilogue longer than the next tile's mainloop).
+    const int cbase = t.nb * BN;
+    const int64_t goff = static_cast<int64_t>(row) * e.ld_aux0;
+    const int64_t uoff = static_cast<int64_t>(row) * e.ld_aux1;
+    if (e.aux_prefetch && rv && cbase < t.N) {
+      const int bytes = min(BN, t.N - cbase) * 2;
+      prefetch_l2_span(e.aux0 + goff + cbase, bytes);
+      prefetch_l2_span(e.aux1 + uoff + cbase, bytes);
+    }
+    uint4 gn[4], un[4];  // the next chunk's g and u, raw bf16
+    auto fetch = [&](int col0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cc = col0 + q * 8;
+        if (rv && cc < t.N) {
+          gn[q] = *reinterpret_cast<const uint4*>(e.aux0 + goff + cc);
+          un[q] = *reinterpret_cast<const uint4*>(e.aux1 + uoff + cc);
+        } else {
+          gn[q] = make_uint4(0u, 0u, 0u, 0u);
+          un[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    };
+    fetch(cbase);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
-      const int col0 = t.nb * BN + c;
+      const int col0 = cbase + c;
       if (col0 >= t.N) break;
+      uint4 gc[4], uc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        gc[q] = gn[q];
+        uc[q] = un[q];
+      }
+      if (c + 32 < BN) fetch(col0 + 32);
       float dh[32], du[32] = {}, h[32] = {};  // rows past M keep zeros (never stored)
       __syncwarp();
       tmem_ld32(t.taddr + c, dh);
       if (rv) {
-        const int64_t off = static_cast<int64_t>(row);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int cc = col0 + q * 8;
-          if (cc < t.N) {
+          if (col0 + q * 8 < t.N) {
             float g8[8], u8[8];
-            load_bf16x8(e.aux0 + off * e.ld_aux0 + cc, g8);
-            load_bf16x8(e.aux1 + off * e.ld_aux1 + cc, u8);
+            bf16x8_to_f32(gc[q], g8);
+            bf16x8_to_f32(uc[q], u8);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float s = 1.f / (1.f + __expf(-g8[i]));
+              const float s = __fdividef(1.f, 1.f + __expf(-g8[i]));  // sigmoid(g); 0 once exp overflows
               const float sg = g8[i] * s;
               const float d = dh[q * 8 + i];
               const float dg = d * u8[i] * s * (1.f + g8[i] * (1.f - s));

@@ -101,6 +101,7 @@ struct EpiArgs {
   float dloss;
   int onehot;                   // CE_DLOGITS: include -w at the label column
   int st_stream;                // epilogue tile stores as streaming (.cs) stores
+  int aux_prefetch;             // DSWIGLU: request the tile's g/u rows into L2 before the chunk loop
   int mode;                     // SIGMOID: 0 forward, 1 backward on the recomputed logits
   float* target_logit;
   // QK-RMSNorm + RoPE

@@ -372,6 +372,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Request the bytes [p, p + bytes) into L2 (a hint: nothing is returned and
+// nothing waits on it).  One prefetch per 128-byte line, plus the line that
+// holds the last byte when p is not line-aligned; every address issued lies
+// inside the span.
+__device__ __forceinline__ void prefetch_l2_span(const void* p, int bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (int o = 0; o < bytes; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(c + o));
+  if (bytes > 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(c + bytes - 1));
+}
+
+// 8 bf16 packed in 16 bytes, widened to fp32.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float* out) {
+  out[0] = bf16_lo(q.x); out[1] = bf16_hi(q.x);
+  out[2] = bf16_lo(q.y); out[3] = bf16_hi(q.y);
+  out[4] = bf16_lo(q.z); out[5] = bf16_hi(q.z);
+  out[6] = bf16_lo(q.w); out[7] = bf16_hi(q.w);
+}
+
 // Load 8 consecutive bf16 (16 bytes) as fp32.
 __device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* p, float* out) {
   uint4 q = *reinterpret_cast<const uint4*>(p);

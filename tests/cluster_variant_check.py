@@ -1,6 +1,7 @@
 """Run by test_cluster_variants_gpu.py in a fresh process (the cluster-size
 switches are read once per process): a ragged transformer block forward and
-backward, a SwiGLU MLP backward and an FP8 linear, against the fp64 oracle.
+backward, a SwiGLU MLP backward, an FP8 linear and a linear + residual whose
+shape the launch policy runs as CTA pairs, against the fp64 oracle.
 Exits non-zero on the first mismatch."""
 import os
 import sys
@@ -12,7 +13,7 @@ sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 
 import synth  # noqa: E402
 from oracle import coda_oracle as O  # noqa: E402
-from parity import assert_bf16, to_np  # noqa: E402
+from parity import assert_bf16, assert_f32, to_np  # noqa: E402
 
 import gemm_epilogue_transformer_bf16_gb300 as coda  # noqa: E402
 from gemm_epilogue_transformer_bf16_gb300.block import Block  # noqa: E402
@@ -50,6 +51,17 @@ def main():
     _, ovx, osx = O.quantize_fp8_rows(to_np(X))
     _, ovw, osw = O.quantize_fp8_rows(to_np(W))
     assert_bf16(Y, O.linear_fp8_fwd(ovx, osx, ovw, osw), "fp8 Y")
+    # linear + residual at 8192 x 4096: eight waves of two-pair units but
+    # seven of CTA pairs, so the default launch policy runs it as pairs
+    M, N, K = 8192, 4096, 128
+    X = synth.randn_bf16((M, K), 1.0, 21)
+    W = synth.randn_bf16((N, K), 1 / 12, 22)
+    R = synth.randn_bf16((M, N), 1.0, 23)
+    Y, r = coda.linear_residual(X.to(dev), W.to(dev), R.to(dev), eps=1e-6, want_rstd=True)
+    torch.cuda.synchronize()
+    ur, rr = O.linear_residual_fwd(to_np(X), to_np(W), to_np(R), 1e-6)
+    assert_bf16(Y, ur, "8192x4096 Y")
+    assert_f32(r, rr, "8192x4096 rstd")
     print("ok")
 
 
