@@ -190,6 +190,13 @@ MUTANTS = {
                                                      "np.repeat(amax[:, None], nb, axis=1)"),
     "nvfp4_codes_without_row_scale": _source_mutant("(sf_val * s[:, None]).astype(np.float32)",
                                                     "sf_val.astype(np.float32)"),
+    "qknorm_bwd_forward_rotation": _source_mutant("dn = rope_inv(dout, pos, theta, pairing)",
+                                                  "dn = rope(dout, pos, theta, pairing)"),
+    "residual_rms_of_input": _source_mutant("return u, rms_inv(u, eps)", "return u, rms_inv(X, eps)"),
+    "quantised_linear_drops_weight_scale": _source_mutant("B = Wv * np.asarray(sw, dtype=np.float64)[:, None]",
+                                                          "B = Wv"),
+    "lse_mean_instead_of_sum": _source_mutant("np.log(np.exp(z - m).sum(axis=-1, keepdims=True))",
+                                              "np.log(np.exp(z - m).mean(axis=-1, keepdims=True))"),
     "fp8_truncates": _mut_fp8_truncate,
     "sigmoid_bwd_missing_derivative": _mut_sigmoid_bwd_missing_factor,
     "rmsnorm_ce_skips_norm_backward": _mut_rmsnorm_ce_skip_norm_bwd,
