@@ -707,6 +707,37 @@ def check_rmsnorm_scale_nvfp4(o):
     return max(e)
 
 
+def check_quantised_swiglu_row_factor(o):
+    """The row factor of the quantised SwiGLU forward is the RMSNorm row
+    factor, applied to the input before the gate: with exactly representable
+    operands and r = 1/rms(X), swiglu_fp8_fwd and swiglu_nvfp4_fwd with
+    row_scale r equal the SwiGLU-MLP forward with unit gain (RMSNorm first,
+    then the gate) on the same operands."""
+    codes, vals = _e4m3_table()
+    r = RNG(41)
+    pick = lambda shape: vals[r.integers(0, len(vals), size=shape)] * (2.0 ** -6)
+    e = []
+    X, Wg, Wu = pick((4, 16)), pick((6, 16)), pick((6, 16))
+    X[:, 0], Wg[:, 0], Wu[:, 0] = 448.0 * 2.0 ** -6, 448.0 * 2.0 ** -6, 448.0 * 2.0 ** -6
+    _, xv, sx = o.quantize_fp8_rows(X)
+    _, gv, sg = o.quantize_fp8_rows(Wg)
+    _, uv, su = o.quantize_fp8_rows(Wu)
+    ref = o.mlp_fwd(X, Wg, Wu, np.zeros((16, 6)), np.zeros((4, 16)), gamma=np.ones(16), eps=1e-6)
+    H, g, u = o.swiglu_fp8_fwd(xv, sx, gv, sg, uv, su, row_scale=o.rms_inv(X, 1e-6))
+    e += [_rel(H, ref["H"]), _rel(g, ref["g"]), _rel(u, ref["u"])]
+    X, *_ = _nvfp4_exact_rows(r, 4, 2, [-10, -13, -8, -18])
+    Wg, *_ = _nvfp4_exact_rows(r, 5, 2, [-11, -10, -12, -11, -13])
+    Wu, *_ = _nvfp4_exact_rows(r, 5, 2, [-12, -11, -10, -12, -11])
+    _, _, sx, xv = o.quantize_nvfp4_rows(X)
+    _, _, sg, gv = o.quantize_nvfp4_rows(Wg)
+    _, _, su, uv = o.quantize_nvfp4_rows(Wu)
+    K = X.shape[1]
+    ref = o.mlp_fwd(X, Wg, Wu, np.zeros((K, 5)), np.zeros((4, K)), gamma=np.ones(K), eps=1e-6)
+    H, g, u = o.swiglu_nvfp4_fwd(xv, sx, gv, sg, uv, su, row_scale=o.rms_inv(X, 1e-6))
+    e += [_rel(H, ref["H"]), _rel(g, ref["g"]), _rel(u, ref["u"])]
+    return max(e)
+
+
 ALL_CHECKS = {
     "rmsnorm_scale_nvfp4": (check_rmsnorm_scale_nvfp4, 1e-12),
     "e2m1": (check_e2m1, 0.0),
@@ -714,6 +745,7 @@ ALL_CHECKS = {
     "nvfp4_linear": (check_nvfp4_linear, 1e-14),
     "fp8_quantizer": (check_fp8_quantizer, 1e-12),
     "fp8_linear": (check_fp8_linear, 1e-14),
+    "quantised_swiglu_row_factor": (check_quantised_swiglu_row_factor, 1e-12),
     "linear_sigmoid": (check_linear_sigmoid, 1e-7),
     "rmsnorm_ce_library": (check_rmsnorm_ce_library, 1e-12),
     "rmsnorm_ce_grad": (check_rmsnorm_ce_grad, 1e-7),

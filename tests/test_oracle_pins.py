@@ -197,6 +197,11 @@ MUTANTS = {
                                                           "B = Wv"),
     "lse_mean_instead_of_sum": _source_mutant("np.log(np.exp(z - m).sum(axis=-1, keepdims=True))",
                                               "np.log(np.exp(z - m).mean(axis=-1, keepdims=True))"),
+    "swiglu_quantised_drops_row_factor": _source_mutant(
+        "A = A * np.asarray(row_scale, dtype=np.float64)[:, None]", "A = A"),
+    "e2m1_wrong_grid": _source_mutant("np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])",
+                                      "np.array([0.0, 0.5, 1.0, 1.5, 2.0, 2.5, 4.0, 6.0])"),
+    "sigmoid_gate_grad_without_s": _source_mutant('out["dZ"] = dY * s', 'out["dZ"] = dY'),
     "fp8_truncates": _mut_fp8_truncate,
     "sigmoid_bwd_missing_derivative": _mut_sigmoid_bwd_missing_factor,
     "rmsnorm_ce_skips_norm_backward": _mut_rmsnorm_ce_skip_norm_bwd,
