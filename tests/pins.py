@@ -295,7 +295,8 @@ def check_ce_uniform(o):
 def check_ce_library(o):
     """Against torch cross_entropy(ignore_index=-100) in float64; one dominant
     logit gives loss -> 0; gradient rows sum to zero; ignored rows have zero
-    gradient; n_valid is an exact count; FD gradients of the mean loss."""
+    gradient; n_valid is an exact count; FD gradients of the mean loss, and
+    of dloss times it for an upstream gradient dloss = -1.75."""
     r = RNG(13)
     M, K, V = 6, 5, 11
     X = r.standard_normal((M, K))
@@ -314,6 +315,9 @@ def check_ce_library(o):
     def L():
         return o.linear_cross_entropy_fwd(X, W, lab)["loss"]
     e += [_rel(b["dX"], _fd_grad(L, X)), _rel(b["dW"], _fd_grad(L, W))]
+    # an upstream gradient dloss != 1 scales the gradient of the mean loss
+    b2 = o.linear_cross_entropy_bwd(X, W, lab, dloss=-1.75)
+    e += [_rel(b2["dX"], _fd_grad(lambda: -1.75 * L(), X)), _rel(b2["dW"], _fd_grad(lambda: -1.75 * L(), W))]
     Wd = np.zeros((V, K))
     Wd[3] = 100.0
     Xd = np.ones((1, K))
@@ -384,7 +388,8 @@ def check_block_special_cases(o):
     output is x0 + A Wo^T (torch linear); with A = 0 the MLP sees x0 and
     x2 - x0 equals the MLP branch computed from torch rms_norm/linear/silu;
     V is the plain projection of RMSNorm(x0); with gamma_q = 1 and pos = 0
-    every Q head has mean square ms/(ms+eps)."""
+    every Q head has mean square ms/(ms+eps); Q and K are RoPE of the q and
+    k slices normalised per head by torch rms_norm with their own gains."""
     p, cfg = tiny_block()
     e = []
     q = dict(p)
@@ -410,6 +415,14 @@ def check_block_special_cases(o):
     qh = qkv[:, :8].reshape(3, 2, 4)
     ms = np.mean(qh ** 2, axis=-1)
     e.append(_rel(np.mean(f["Q"].reshape(3, 2, 4) ** 2, axis=-1), ms / (ms + cfg["eps"])))
+    # Q and K at general gains and positions: the q and k column slices of
+    # the projection, each head normalised by torch rms_norm with its own
+    # gain (gamma_q for Q, gamma_k for K), then the (separately pinned) RoPE
+    f = o.block_fwd(p, **cfg)
+    for name, cols, heads, gain in (("Q", slice(0, 8), 2, "gamma_q"), ("K", slice(8, 12), 1, "gamma_k")):
+        hn = F.rms_norm(t(qkv[:, cols].reshape(3, heads, 4)), (4,), weight=t(p[gain]), eps=cfg["eps"]).numpy()
+        ref = o.rope(hn, p["pos"], cfg["theta"]).reshape(3, -1)
+        e.append(_rel(f[name], ref))
     return max(e)
 
 
@@ -463,16 +476,17 @@ def check_rmsnorm_ce_library(o):
 
 
 def check_rmsnorm_ce_grad(o):
-    """FD gradients of the mean loss w.r.t. X, W and gamma."""
+    """FD gradients of dloss times the mean loss (dloss = 0.6, the upstream
+    gradient) w.r.t. X, W and gamma."""
     r = RNG(18)
     X = r.standard_normal((4, 6))
     W = r.standard_normal((7, 6))
     g = 1 + 0.1 * r.standard_normal(6)
     lab = np.array([1, -100, 6, 0])
-    b = o.rmsnorm_linear_cross_entropy_bwd(X, g, W, lab, 1e-6)
+    b = o.rmsnorm_linear_cross_entropy_bwd(X, g, W, lab, 1e-6, dloss=0.6)
 
     def L():
-        return o.rmsnorm_linear_cross_entropy_fwd(X, g, W, lab, 1e-6)["loss"]
+        return 0.6 * o.rmsnorm_linear_cross_entropy_fwd(X, g, W, lab, 1e-6)["loss"]
     return max(_rel(b["dX"], _fd_grad(L, X)), _rel(b["dW"], _fd_grad(L, W)), _rel(b["dgamma"], _fd_grad(L, g)))
 
 

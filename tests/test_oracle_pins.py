@@ -172,12 +172,17 @@ def _mut_fp8_truncate(m):
     m.quantize_fp8_rows = bad
 
 
-def _source_mutant(old, new):
-    """A mutant that re-executes the oracle's source with one phrase replaced."""
+def _source_mutant(old, new, *more):
+    """A mutant that re-executes the oracle's source with one phrase replaced
+    (or several: further (old, new) pairs)."""
+    pairs = [(old, new)] + list(more)
+
     def apply(m):
         src = open(ORACLE_SRC).read()
-        assert src.count(old) == 1, old
-        exec(compile(src.replace(old, new), ORACLE_SRC, "exec"), m.__dict__)
+        for a, b in pairs:
+            assert src.count(a) == 1, a
+            src = src.replace(a, b)
+        exec(compile(src, ORACLE_SRC, "exec"), m.__dict__)
     return apply
 
 
@@ -202,6 +207,13 @@ MUTANTS = {
     "e2m1_wrong_grid": _source_mutant("np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])",
                                       "np.array([0.0, 0.5, 1.0, 1.5, 2.0, 2.5, 4.0, 6.0])"),
     "sigmoid_gate_grad_without_s": _source_mutant('out["dZ"] = dY * s', 'out["dZ"] = dY'),
+    "ce_grad_ignores_dloss": _source_mutant("dZ *= dloss / n_valid", "dZ *= 1.0 / n_valid"),
+    # the same wrong gain in the forward and the backward: the gradients stay
+    # consistent, so only a forward pin can see it
+    "block_k_uses_gamma_q": _source_mutant(
+        'K = qk_rmsnorm_rope_fwd(k, p["gamma_k"], p["pos"], theta, eps)',
+        'K = qk_rmsnorm_rope_fwd(k, p["gamma_q"], p["pos"], theta, eps)',
+        ('dk, dgk = qk_rmsnorm_rope_bwd(k, p["gamma_k"]', 'dk, dgk = qk_rmsnorm_rope_bwd(k, p["gamma_q"]')),
     "fp8_truncates": _mut_fp8_truncate,
     "sigmoid_bwd_missing_derivative": _mut_sigmoid_bwd_missing_factor,
     "rmsnorm_ce_skips_norm_backward": _mut_rmsnorm_ce_skip_norm_bwd,
