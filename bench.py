@@ -66,33 +66,13 @@ def parse():
     return p.parse_args()
 
 
-# ----------------------------------------------------------------------------- distributed plumbing
-def dist_env():
-    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
-
-
-def dist_init(world):
-    if world > 1:
-        import torch.distributed as dist
-        if not dist.is_initialized():
-            dist.init_process_group("gloo")
-
-
-def dist_barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def dist_max(x, world):
-    """Max of a host float over ranks (gloo; no data-path collective)."""
-    if world <= 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([float(x)], dtype=torch.float64)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+# ----------------------------------------------------------------------------- one GPU only
+def world_size(args):
+    """The benchmark runs on one GPU.  The default GEMM shares B tiles between
+    the CTAs of a cluster with TMA multicast, and this library is built for a
+    single device; a multi-process launch is refused instead of running
+    replicas."""
+    return max(int(os.environ.get("WORLD_SIZE", 1)), args.gpus)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -267,8 +247,7 @@ def cores():
 
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args):
-    rank, world, _ = dist_env()
-    if rank != 0:
+    if int(os.environ.get("RANK", 0)) != 0:
         return 0
     import torch
     import synth
@@ -301,21 +280,23 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if world_size(args) > 1:
+        print("bench.py runs on one GPU only: the library is single-device and its cluster GEMMs share tiles by "
+              "TMA multicast; launch it without --gpus > 1 / WORLD_SIZE > 1", file=sys.stderr)
+        return 2
     import numpy as np
     import torch
     import synth
     import gemm_epilogue_transformer_bf16_gb300 as coda
     from gemm_epilogue_transformer_bf16_gb300.block import Block
 
-    rank, world, local = dist_env()
-    dist_init(world)
     assert torch.cuda.is_available(), "bench.py needs a CUDA device"
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
     coda.load()
     import dataclasses
     s = dataclasses.replace(synth.FULL["block"], tokens=args.tokens)
-    host = synth.make_block(s, seed=rank)          # replicas: each rank its own seeded batch
+    host = synth.make_block(s, seed=0)
     t = {k: v.to(dev) for k, v in host.items()}
     blk = Block(s, t, device=dev, concurrent=not args.serial, fold_weights=args.fold_weights)
     flops_step = sum(blk.gemm_flops().values())
@@ -339,7 +320,6 @@ def main():
     except Exception:
         gpu_id = None
     clocks = ClockSampler(gpu_id)
-    dist_barrier(world)
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)
@@ -358,11 +338,9 @@ def main():
     stop.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
-    dist_barrier(world)
     ms_total = start.elapsed_time(stop)
-    ms_total = dist_max(ms_total, world)
     ms_step = ms_total / args.steps
-    value = world * flops_step * args.steps / (ms_total / 1e3) / 1e12
+    value = flops_step * args.steps / (ms_total / 1e3) / 1e12
     stage_ms = {n: statistics.median(marks[i][k].elapsed_time(marks[i][k + 1]) for i in range(args.steps))
                 for k, n in enumerate(names)}
     gf = blk.gemm_flops()
@@ -442,17 +420,16 @@ def main():
 
         e2e_run(max(2, args.warmup // 2))
         torch.cuda.synchronize(dev)
-        dist_barrier(world)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         e2e_run(args.steps, a)
         b.record(stream)
         torch.cuda.synchronize(dev)
-        ms_e2e = dist_max(a.elapsed_time(b), world)
+        ms_e2e = a.elapsed_time(b)
         if not (torch.equal(hx2, blk.x2.cpu()) and torch.equal(hdx0, blk.grads_qkv["dX"].cpu())):
             raise RuntimeError("e2e results read back do not match the device buffers")
-        e2e = {"value": round(world * flops_step * args.steps / (ms_e2e / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+        e2e = {"value": round(flops_step * args.steps / (ms_e2e / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e / args.steps, 3),
                "copies": "pinned host buffers; next step's inputs prefetched on a copy stream, results read back "
                          "on another"}
@@ -474,7 +451,7 @@ def main():
             step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        unfused_ms = dist_max(a.elapsed_time(b) / n_unf, world)
+        unfused_ms = a.elapsed_time(b) / n_unf
 
     # ---------------------------------------------------------------- linear + CE (rows a8, a12)
     # Not part of the block step: the 8192 x 2048 x 128256 linear + cross-entropy
@@ -506,7 +483,7 @@ def main():
     if not args.no_ce and "ce" in legs:
         from gemm_epilogue_transformer_bf16_gb300.block import LinearCE
         cs_ = synth.FULL["linear_ce"]
-        hc = synth.make_ce(cs_, seed=rank)
+        hc = synth.make_ce(cs_, seed=0)
         dc = {k: v.to(dev) for k, v in hc.items()}
         ce = LinearCE(cs_.tokens, cs_.vocab, cs_.hidden, device=dev)
         for _ in range(2):
@@ -619,7 +596,7 @@ def main():
     # operator's form).  FLOPs 2*M*N*K per GEMM.
     if not args.no_ce and "mlp" in legs:
         s3 = synth.FULL["mlp"]
-        d3 = {k: v.to(dev) for k, v in synth.make_mlp(s3, seed=rank).items()}
+        d3 = {k: v.to(dev) for k, v in synth.make_mlp(s3, seed=0).items()}
         ws3 = coda.workspace(max(coda.load().coda_linear_swiglu_bwd_workspace_size(s3.tokens, s3.inter, s3.hidden),
                                  coda.load().coda_linear_residual_workspace_size(s3.tokens, s3.hidden, s3.inter)), dev)
         o3 = {}
@@ -649,7 +626,7 @@ def main():
         del d3, p3
     if not args.no_ce and "rms" in legs:
         s2 = synth.FULL["rmsnorm_linear"]
-        d2 = {k: v.to(dev) for k, v in synth.make_rms_linear(s2, seed=rank).items()}
+        d2 = {k: v.to(dev) for k, v in synth.make_rms_linear(s2, seed=0).items()}
         # outputs and workspaces allocated once, as a training loop holds them;
         # dW on a second stream beside c -> dX
         M2, N2, K2 = s2.tokens, s2.out, s2.hidden
@@ -705,40 +682,36 @@ def main():
 
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.tokens == synth.FULL["block"].tokens:
+    if not args.no_cpu_baseline and args.tokens == synth.FULL["block"].tokens:
         torch.set_num_threads(cores())
         v, dt, fl = oracle_sample_timing(args.cpu_tokens, oracle_inputs(host, args.cpu_tokens))
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
                "sample": f"fp64 NumPy block_fwd+block_bwd on the first {args.cpu_tokens} of 8192 tokens "
                          f"(full weights): {fl / 1e12:.3f} TFLOP in {dt:.1f} s"}
 
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "tokens": s.tokens, "hidden": s.hidden, "n_q": s.n_q,
-                       "n_kv": s.n_kv, "head_dim": s.head_dim, "inter": s.inter, "tflop_per_step":
-                       round(flops_step / 1e12, 3), "l2": "inputs (1.7 GB of weights + activations) exceed the "
-                       "129 MB L2; no flush", "parallelism": f"replicas x{world}",
-                       "rmsnorm_gain": "folded into the weights each step" if args.fold_weights
-                       else "applied by the producing epilogue (u = x ⊙ gamma)"},
-            "pct_bf16_peak": {"burst": round(value / world / burst, 4), "sustained": round(value / world / sustained, 4),
-                              "source": peak_src},
-            "roofline": roofline,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": launches_step * args.steps,
-            "clocks": clk,
-            "unfused_ms_per_step": round(unfused_ms, 3) if unfused_ms else None,
-            "speedup_vs_unfused": round(unfused_ms / ms_step, 3) if unfused_ms else None,
-            "stages": stages,
-            "other_workloads": other or None,
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": s.tokens, "hidden": s.hidden, "n_q": s.n_q,
+                   "n_kv": s.n_kv, "head_dim": s.head_dim, "inter": s.inter, "tflop_per_step":
+                   round(flops_step / 1e12, 3), "l2": "inputs (1.7 GB of weights + activations) exceed the "
+                   "129 MB L2; no flush", "parallelism": "single GPU",
+                   "rmsnorm_gain": "folded into the weights each step" if args.fold_weights
+                   else "applied by the producing epilogue (u = x ⊙ gamma)"},
+        "pct_bf16_peak": {"burst": round(value / burst, 4), "sustained": round(value / sustained, 4),
+                          "source": peak_src},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_step * args.steps,
+        "clocks": clk,
+        "unfused_ms_per_step": round(unfused_ms, 3) if unfused_ms else None,
+        "speedup_vs_unfused": round(unfused_ms / ms_step, 3) if unfused_ms else None,
+        "stages": stages,
+        "other_workloads": other or None,
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 

@@ -1,4 +1,4 @@
-"""CPU checks of bench.py's reporting helpers: the DRAM-traffic figure is
+"""CPU checks of bench.py's reporting helpers and launch rule: the DRAM-traffic figure is
 read from the profile summary only while its source digest matches the
 kernel sources, and the clock sampler's summary reports the median SM clock
 and every throttle reason that was active."""
@@ -61,3 +61,17 @@ def test_clock_summary_without_samples(tmp_path):
     assert _summary(tmp_path, ["no numbers here"]) is None
     s = bench.ClockSampler(None)
     assert s.stop() is None          # never started
+
+
+def test_multi_gpu_launch_is_refused():
+    """The benchmark is single-GPU: --gpus > 1 and WORLD_SIZE > 1 exit with
+    code 2 before touching a device (the cluster GEMMs' TMA multicast stays
+    in code that one GPU runs alone)."""
+    import subprocess
+    import sys
+    bench_py = os.path.join(os.path.dirname(bench.__file__), "bench.py")
+    r = subprocess.run([sys.executable, bench_py, "--gpus", "2"], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2 and "one GPU only" in r.stderr
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1")
+    r = subprocess.run([sys.executable, bench_py], capture_output=True, text=True, timeout=120, env=env)
+    assert r.returncode == 2 and r.stdout == ""
