@@ -29,7 +29,9 @@ Readings where the pages are silent (each is also listed in the design notes):
   * QK-RMSNorm: per head over head_dim, gains shared by all heads, applied
     before RoPE.
   * Cross-entropy: natural log, mean over rows whose label != ignore_index;
-    all rows ignored gives NaN (0/0) and a zero gradient.
+    all rows ignored gives NaN (0/0) and a zero gradient; a label outside
+    [0, V) other than ignore_index is reported as a range error and its row
+    counts as ignored.
 
 Parity status: every function below is pinned by a test in
 ``tests/test_oracle_pins.py`` (identities, closed forms, library special
@@ -278,32 +280,45 @@ def _lse(z):
     return (m + np.log(np.exp(z - m).sum(axis=-1, keepdims=True)))[..., 0]
 
 
+def _ce_valid(labels, ignore_index, V):
+    """Rows that enter the loss: label != ignore_index and 0 <= label < V.
+    A label outside [0, V) other than ignore_index is a range error; the row
+    counts as ignored (reading: the pages give no rule for bad labels)."""
+    in_range = (labels >= 0) & (labels < V)
+    valid = (labels != ignore_index) & in_range
+    bad = (labels != ignore_index) & ~in_range
+    return valid, bool(bad.any())
+
+
 def linear_cross_entropy_fwd(X, W, labels, ignore_index=-100):
     """z = X W^T; lse_i = log sum_j exp(z_ij); loss_i = lse_i - z_{i, y_i};
-    mean over rows with y_i != ignore_index.
+    mean over rows with y_i != ignore_index and 0 <= y_i < V.
 
     [P1] §3.1 class 5 (running max / sum-exp state for online log-sum-exp and
     cross-entropy) and [P3]'s linear_cross_entropy.  Returns a dict with
-    loss (scalar), lse [M], per-row loss [M] (0 on ignored rows), n_valid."""
+    loss (scalar), lse [M], per-row loss [M] (0 on ignored rows), n_valid,
+    and label_range_error (some label other than ignore_index lies outside
+    [0, V); such rows count as ignored)."""
     labels = np.asarray(labels)
     z = X @ W.T
     lse = _lse(z)
-    valid = labels != ignore_index
+    valid, bad = _ce_valid(labels, ignore_index, W.shape[0])
     rows = np.nonzero(valid)[0]
     per_row = np.zeros(X.shape[0])
     per_row[rows] = lse[rows] - z[rows, labels[rows]]
     n_valid = int(valid.sum())
     loss = per_row[rows].sum() / n_valid if n_valid > 0 else float("nan")
-    return {"loss": loss, "lse": lse, "per_row": per_row, "n_valid": n_valid}
+    return {"loss": loss, "lse": lse, "per_row": per_row, "n_valid": n_valid, "label_range_error": bad}
 
 
 def linear_cross_entropy_bwd(X, W, labels, ignore_index=-100, dloss=1.0):
     """dZ = (softmax(z) - onehot(y)) * dloss / n_valid on valid rows, 0 on
-    ignored rows; dX = dZ W, dW = dZ^T X (chain rule)."""
+    ignored rows (label == ignore_index or outside [0, V)); dX = dZ W,
+    dW = dZ^T X (chain rule)."""
     labels = np.asarray(labels)
     z = X @ W.T
     p = np.exp(z - _lse(z)[:, None])
-    valid = labels != ignore_index
+    valid, _ = _ce_valid(labels, ignore_index, W.shape[0])
     rows = np.nonzero(valid)[0]
     n_valid = int(valid.sum())
     dZ = np.zeros_like(z)

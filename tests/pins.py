@@ -363,6 +363,35 @@ def check_ce_all_ignored(o):
     return 0.0 if ok else 1.0
 
 
+def check_ce_bad_labels(o):
+    """Labels outside [0, V) other than -100 (a negative one and two at or
+    above V) count as ignored and raise the range flag: loss, per-row loss
+    and n_valid equal torch cross_entropy(ignore_index=-100) on the labels
+    with the bad ones replaced by -100; the gradient equals finite
+    differences of that loss and is zero on the bad rows; the flag is off
+    when every label is valid or ignored."""
+    r = RNG(17)
+    M, K, V = 7, 5, 9
+    X = r.standard_normal((M, K))
+    W = r.standard_normal((V, K))
+    lab = np.array([2, -5, V, -100, 0, V + 3, V - 1])
+    clean = np.where((lab >= 0) & (lab < V), lab, -100)
+    f = o.linear_cross_entropy_fwd(X, W, lab)
+    z = torch.from_numpy(X @ W.T)
+    ref = F.cross_entropy(z, torch.from_numpy(clean).long(), ignore_index=-100).item()
+    ref_rows = F.cross_entropy(z, torch.from_numpy(clean).long(), ignore_index=-100, reduction="none").numpy()
+    e = [abs(f["loss"] - ref) / abs(ref), _rel(f["per_row"], ref_rows), abs(f["n_valid"] - 3),
+         0.0 if f["label_range_error"] is True else 1.0]
+    b = o.linear_cross_entropy_bwd(X, W, lab)
+    e.append(float(np.max(np.abs(b["dZ"][[1, 2, 3, 5]]))))
+
+    def L():
+        return o.linear_cross_entropy_fwd(X, W, lab)["loss"]
+    e += [_rel(b["dX"], _fd_grad(L, X)), _rel(b["dW"], _fd_grad(L, W))]
+    e.append(0.0 if o.linear_cross_entropy_fwd(X, W, clean)["label_range_error"] is False else 1.0)
+    return max(e)
+
+
 # ---------------------------------------------------------------------------
 # the block
 # ---------------------------------------------------------------------------
@@ -782,6 +811,7 @@ ALL_CHECKS = {
     "ce_uniform": (check_ce_uniform, 1e-14),
     "ce_library": (check_ce_library, 1e-7),
     "ce_all_ignored": (check_ce_all_ignored, 0.5),
+    "ce_bad_labels": (check_ce_bad_labels, 1e-7),
     "ce_lse_merge": (check_ce_lse_merge, 1e-14),
     "block_special_cases": (check_block_special_cases, 1e-12),
     "block_grad": (check_block_grad, 1e-7),

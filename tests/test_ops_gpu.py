@@ -174,21 +174,38 @@ def test_linear_cross_entropy(coda, shape):
 
 
 def test_cross_entropy_all_ignored_and_bad_label(coda):
+    """All rows ignored: NaN loss, n_valid 0, the oracle's lse, zero
+    gradients.  Labels outside [0, V) other than -100 (one negative, one at
+    V + 5): CODA_ERR_LABEL_RANGE in the status word, and lse, loss, n_valid,
+    dX and dW equal the oracle's, which counts those rows as ignored."""
     s = synth.CeShape(64, 128, 1024)
     t = synth.make_ce(s, seed=5)
-    d = dev(t)
-    lab = torch.full((s.tokens,), -100, dtype=torch.int32, device=DEV)
-    out = coda.linear_cross_entropy(d["X"], d["W"], lab)
-    assert math.isnan(out["loss"].item()) and int(out["n_valid"].item()) == 0
-    g = coda.linear_cross_entropy_bwd(d["X"], d["W"], lab, out["lse"], out["n_valid"], 1.0)
+    d, o = dev(t), f64(t)
+    lab = torch.full((s.tokens,), -100, dtype=torch.int32)
+    out = coda.linear_cross_entropy(d["X"], d["W"], lab.to(DEV))
+    f = O.linear_cross_entropy_fwd(o["X"], o["W"], lab.numpy())
+    assert math.isnan(out["loss"].item()) and math.isnan(f["loss"])
+    assert int(out["n_valid"].item()) == f["n_valid"] == 0
+    assert_f32(out["lse"], f["lse"], "lse (all ignored)")
+    g = coda.linear_cross_entropy_bwd(d["X"], d["W"], lab.to(DEV), out["lse"], out["n_valid"], 1.0)
     assert not torch.any(g["dX"].float() != 0) and not torch.any(g["dW"].float() != 0)
     assert coda.get_status(out["ws"]) == 0
-    lab2 = d["labels"].clone()
+    lab2 = t["labels"].clone()
     lab2[3] = s.vocab + 5
-    out2 = coda.linear_cross_entropy(d["X"], d["W"], lab2)
+    lab2[7] = -5
+    lab2[11] = -100
+    out2 = coda.linear_cross_entropy(d["X"], d["W"], lab2.to(DEV))
     assert coda.get_status(out2["ws"]) == 7   # CODA_ERR_LABEL_RANGE
-    valid = (lab2 != -100) & (lab2 >= 0) & (lab2 < s.vocab)
-    assert int(out2["n_valid"].item()) == int(valid.sum().item())
+    f2 = O.linear_cross_entropy_fwd(o["X"], o["W"], lab2.numpy())
+    assert f2["label_range_error"]
+    assert int(out2["n_valid"].item()) == f2["n_valid"] == int(((lab2 >= 0) & (lab2 < s.vocab)).sum())
+    assert_f32(out2["lse"], f2["lse"], "lse")
+    assert_f32(out2["loss"], [f2["loss"]], "loss")
+    g2 = coda.linear_cross_entropy_bwd(d["X"], d["W"], lab2.to(DEV), out2["lse"], out2["n_valid"], 1.0)
+    b2 = O.linear_cross_entropy_bwd(o["X"], o["W"], lab2.numpy())
+    assert_bf16(g2["dX"], b2["dX"], "dX")
+    assert_bf16(g2["dW"], b2["dW"], "dW")
+    assert not torch.any(g2["dX"][[3, 7, 11]].float() != 0)
 
 
 # ---------------------------------------------------------------- transformer block (scaled)
