@@ -28,7 +28,9 @@ void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_ce_scratch on the current device.  In host code the
 // name g_ce_scratch is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress, once per device, with that device current.  It is
+// kept for the life of the process; a cudaDeviceReset reloads the module at
+// another address, which is why the header rules out calls after a reset.
 void* scratch_on_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;

@@ -550,7 +550,11 @@ int coda_rmsnorm_linear_cross_entropy_bwd(const coda_bf16* X, const float* rstd,
  * with CODA_ERR_WORKSPACE before anything is enqueued (at V = 128256 that is
  * M above about 32,000 tokens).  The first call on a device looks up the
  * array's device address (set-up, once per device, with that device
- * current); make that first call before any stream capture.  Every call
+ * current); make that first call before any stream capture.  The address
+ * is kept until the process exits: after cudaDeviceReset on a device the
+ * library's device image is loaded again elsewhere, so do not call this
+ * entry point on that device after a reset (the regular
+ * coda_linear_cross_entropy with a workspace has no such limit).  Every call
  * shares the array, so calls that overlap on the GPU (different streams or
  * threads) race and must be serialised by the caller.
  * status_out (optional device int32) receives this call's device status word:

@@ -7,12 +7,18 @@ the regular kernels with the library's fixed device scratch.  This file is
 named so that pytest collects it last.  The test calls the entry point through
 the C ABI twice in a row (the scratch keeps the first call's contents) and
 compares each result with the regular coda_linear_cross_entropy on the same
-inputs, within the parity tolerances of the other tests."""
+inputs and with the fp64 oracle, within the parity tolerances of the other
+tests; a third call with every label ignored and a call with no rows check
+that nothing the previous calls left in the shared scratch reaches the
+result."""
+import math
+
 import pytest
 import torch
 
 import synth
-from parity import assert_f32
+from oracle import coda_oracle as O
+from parity import assert_f32, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -48,13 +54,38 @@ def test_noalloc_matches_regular_twice(coda):
         t = synth.make_ce(s, seed=10 + call)
         X, W, lab = t["X"].to(DEV), t["W"].to(DEV), t["labels"].to(DEV)
         ref = coda.linear_cross_entropy(X, W, lab)
+        f = O.linear_cross_entropy_fwd(to_np(t["X"]), to_np(t["W"]), t["labels"].numpy())
         out = _fresh_out(s.tokens)
         assert _noalloc_via_abi(lib, X, W, lab, out, s.tokens, s.vocab, s.hidden) == 0
         torch.cuda.synchronize()
         assert int(out["status"].item()) == 0
-        assert int(out["n_valid"].item()) == int(ref["n_valid"].item())
-        assert_f32(out["lse"], ref["lse"], f"lse call {call}")
-        assert_f32(out["loss"], ref["loss"], f"loss call {call}")
+        assert int(out["n_valid"].item()) == int(ref["n_valid"].item()) == f["n_valid"]
+        assert_f32(out["lse"], ref["lse"], f"lse call {call} vs the regular entry point")
+        assert_f32(out["loss"], ref["loss"], f"loss call {call} vs the regular entry point")
+        assert_f32(out["lse"], f["lse"], f"lse call {call} vs the oracle")
+        assert_f32(out["loss"], [f["loss"]], f"loss call {call} vs the oracle")
+    # a third call with every row ignored: the combine must not read the
+    # target logits the previous calls left in the shared scratch
+    s = shapes[0]
+    t = synth.make_ce(s, seed=10)
+    X, W = t["X"].to(DEV), t["W"].to(DEV)
+    lab = torch.full((s.tokens,), -100, dtype=torch.int32)
+    ref = coda.linear_cross_entropy(X, W, lab.to(DEV))
+    f = O.linear_cross_entropy_fwd(to_np(t["X"]), to_np(t["W"]), lab.numpy())
+    out = _fresh_out(s.tokens)
+    assert _noalloc_via_abi(lib, X, W, lab.to(DEV), out, s.tokens, s.vocab, s.hidden) == 0
+    torch.cuda.synchronize()
+    assert int(out["status"].item()) == 0
+    assert int(out["n_valid"].item()) == int(ref["n_valid"].item()) == f["n_valid"] == 0
+    assert math.isnan(out["loss"].item()) and math.isnan(ref["loss"].item()) and math.isnan(f["loss"])
+    assert_f32(out["lse"], ref["lse"], "lse, all ignored, vs the regular entry point")
+    assert_f32(out["lse"], f["lse"], "lse, all ignored, vs the oracle")
+    # and a call with no rows: only the mean (NaN) and the count (0) are written
+    out = _fresh_out(1)
+    assert _noalloc_via_abi(lib, X, W, lab.to(DEV), out, 0, s.vocab, s.hidden) == 0
+    torch.cuda.synchronize()
+    assert int(out["status"].item()) == 0
+    assert int(out["n_valid"].item()) == 0 and math.isnan(out["loss"].item())
 
 
 def test_noalloc_reports_label_errors_and_rejects_oversize(coda):
