@@ -311,10 +311,14 @@ def linear_cross_entropy_fwd(X, W, labels, ignore_index=-100):
     return {"loss": loss, "lse": lse, "per_row": per_row, "n_valid": n_valid, "label_range_error": bad}
 
 
-def linear_cross_entropy_bwd(X, W, labels, ignore_index=-100, dloss=1.0):
+def linear_cross_entropy_bwd(X, W, labels, ignore_index=-100, dloss=1.0, vocab_rows=None):
     """dZ = (softmax(z) - onehot(y)) * dloss / n_valid on valid rows, 0 on
     ignored rows (label == ignore_index or outside [0, V)); dX = dZ W,
-    dW = dZ^T X (chain rule)."""
+    dW = dZ^T X (chain rule).
+
+    With vocab_rows (indices into the vocabulary) only those rows of dW are
+    returned, as "dW_rows" = dZ[:, vocab_rows]^T X (the softmax still
+    normalises over the whole vocabulary); dX is then not formed."""
     labels = np.asarray(labels)
     z = X @ W.T
     p = np.exp(z - _lse(z)[:, None])
@@ -326,6 +330,8 @@ def linear_cross_entropy_bwd(X, W, labels, ignore_index=-100, dloss=1.0):
         dZ[rows] = p[rows]
         dZ[rows, labels[rows]] -= 1.0
         dZ *= dloss / n_valid
+    if vocab_rows is not None:
+        return {"dW_rows": dZ[:, np.asarray(vocab_rows)].T @ X}
     return {"dX": dZ @ W, "dW": dZ.T @ X, "dZ": dZ}
 
 

@@ -392,6 +392,32 @@ def check_ce_bad_labels(o):
     return max(e)
 
 
+def check_ce_dw_rows(o):
+    """dW restricted to a few vocabulary rows equals those rows of finite
+    differences of the mean loss in W (the softmax still normalises over
+    the whole vocabulary), also when the rows are summed over token blocks
+    with dloss = the block's valid count / the total valid count."""
+    r = RNG(18)
+    M, K, V = 8, 4, 13
+    X = r.standard_normal((M, K))
+    W = r.standard_normal((V, K))
+    lab = np.array([0, 12, -100, 5, 5, 7, -100, 12])
+    ids = np.array([0, 5, 9, 12])
+
+    def L():
+        return o.linear_cross_entropy_fwd(X, W, lab)["loss"]
+    fd = _fd_grad(L, W)[ids]
+    e = [_rel(o.linear_cross_entropy_bwd(X, W, lab, vocab_rows=ids)["dW_rows"], fd)]
+    nv = int((lab != -100).sum())
+    acc = np.zeros((len(ids), K))
+    for lo, hi in ((0, 3), (3, 8)):
+        lb = lab[lo:hi]
+        acc += o.linear_cross_entropy_bwd(X[lo:hi], W, lb, dloss=int((lb != -100).sum()) / nv,
+                                          vocab_rows=ids)["dW_rows"]
+    e.append(_rel(acc, fd))
+    return max(e)
+
+
 # ---------------------------------------------------------------------------
 # the block
 # ---------------------------------------------------------------------------
@@ -812,6 +838,7 @@ ALL_CHECKS = {
     "ce_library": (check_ce_library, 1e-7),
     "ce_all_ignored": (check_ce_all_ignored, 0.5),
     "ce_bad_labels": (check_ce_bad_labels, 1e-7),
+    "ce_dw_rows": (check_ce_dw_rows, 1e-7),
     "ce_lse_merge": (check_ce_lse_merge, 1e-14),
     "block_special_cases": (check_block_special_cases, 1e-12),
     "block_grad": (check_block_grad, 1e-7),

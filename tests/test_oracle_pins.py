@@ -208,6 +208,9 @@ MUTANTS = {
                                       "np.array([0.0, 0.5, 1.0, 1.5, 2.0, 2.5, 4.0, 6.0])"),
     "sigmoid_gate_grad_without_s": _source_mutant('out["dZ"] = dY * s', 'out["dZ"] = dY'),
     "ce_grad_ignores_dloss": _source_mutant("dZ *= dloss / n_valid", "dZ *= 1.0 / n_valid"),
+    "ce_dw_rows_without_onehot": _source_mutant("return {\"dW_rows\": dZ[:, np.asarray(vocab_rows)].T @ X}",
+                                                "return {\"dW_rows\": (p * dloss / max(n_valid, 1))"
+                                                "[:, np.asarray(vocab_rows)].T @ X}"),
     # a negative label wraps around to column V + label (numpy indexing)
     "ce_negative_label_wraps": _source_mutant("in_range = (labels >= 0) & (labels < V)",
                                               "in_range = labels < V"),
