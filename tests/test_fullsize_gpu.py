@@ -3,19 +3,29 @@ linear + cross-entropy at vocabulary 128256, the block at hidden 8192 and the
 FP8 / NVFP4 gate/up legs at its shape; the RMSNorm-linear workload runs in
 full in test_ops_gpu.py), in the launch configuration bench.py times.
 
-The fp64 oracle cannot evaluate these workloads whole in a test's time, so it
-is evaluated exactly on samples:
+The fp64 oracle cannot evaluate the largest workloads whole in a test's
+time, so it is evaluated exactly on samples or on sub-problems whose
+outputs equal the full problem's:
 
   * row-local outputs (every forward output, dX, dA, dx0, dx1, lse) on sampled
-    token rows -- the oracle run on those rows alone is exact for them;
+    token rows -- the oracle run on those rows alone is exact for them; the
+    cross-entropy lse and mean loss on every row, in row blocks;
   * weight gradients of the SwiGLU MLP on sampled intermediate units -- an
     MLP restricted to a subset of its intermediate units (rows of Wg, Wu,
     columns of Wd) has exactly those units' dWg, dWu rows and dWd columns;
+  * the cross-entropy dW on sampled vocabulary rows (the softmax of every
+    row normalised over the whole vocabulary, summed over token blocks);
+  * the block's QKV-side gradients (dWqkv, dgamma_attn, dgamma_q, dgamma_k)
+    whole: they depend on x0, the gains, Wqkv, pos and dQ, dK, dV only, so
+    the oracle's block with the MLP cut to a few units and the attention
+    output to one 128-wide slice has exactly the same ones;
+  * dgamma_mlp whole, as the sum over blocks of intermediate units of the
+    restricted MLPs' dgamma (the gain gradient is linear in the MLP's
+    per-unit contributions).
 
-and, where no exact sample is cheap, through properties that hold at any
-size: dgamma_k * gamma_k = sum_n W_nk dW_nk for the RMSNorm-reparameterised
-projections, mean loss = mean over valid rows of (lse_i - z_{i,y_i}), and the
-columns of the cross-entropy dW summing to ~0 (softmax - onehot rows sum to 0).
+dWo, a sum over every token of dx1 (which needs the whole MLP backward), is
+checked through a property that holds at any size: dWo v = dx1^T (A v) for a
+random vector v, with dx1 itself checked against the oracle on sampled rows.
 """
 import math
 
@@ -31,6 +41,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 DEV = "cuda"
 N_ROWS = 48
 N_UNITS = 24
+MLP_UNIT_BLOCK = 4096
 
 
 @pytest.fixture(scope="module")
@@ -51,13 +62,6 @@ def _at(t, idx, dim=0):
     """Rows (dim 0) or columns (dim 1) `idx` of a device tensor, on the host."""
     ix = torch.as_tensor(idx, dtype=torch.long, device=t.device)
     return t.index_select(dim, ix).cpu()
-
-
-def _gamma_property(dgamma, gamma, pairs, name):
-    """dgamma_k * gamma_k == sum over (W, dW) pairs of sum_n W_nk dW_nk."""
-    lhs = to_np(dgamma) * to_np(gamma)
-    rhs = sum((to_np(W) * to_np(dW)).sum(axis=0) for W, dW in pairs)
-    assert_bf16(lhs, rhs, name)
 
 
 # ---------------------------------------------------------------- SwiGLU MLP, hidden 4096
@@ -84,6 +88,9 @@ def test_mlp_fullsize(coda):
 
 
 # ---------------------------------------------------------------- linear + cross-entropy, vocabulary 128256
+CE_ROW_BLOCK = 512
+
+
 def test_cross_entropy_fullsize(coda):
     s = synth.FULL["linear_ce"]
     t = synth.make_ce(s, seed=0)
@@ -95,23 +102,30 @@ def test_cross_entropy_fullsize(coda):
     labels = t["labels"].numpy()
     n_valid = int((labels != s.ignore_index).sum())
     assert int(out["n_valid"].item()) == n_valid == s.tokens - math.floor(0.05 * s.tokens)
-    rows = synth.sample_rows(s.tokens, N_ROWS).numpy()
     X, W = to_np(t["X"]), to_np(t["W"])
+    # vocabulary rows of dW: both ends, rows that are some token's label
+    # (their one-hot term), and rows no label hits
+    lab_ids = np.unique(labels[labels >= 0])
+    pick = torch.randperm(len(lab_ids), generator=torch.Generator().manual_seed(21))[:14].numpy()
+    ids = np.unique(np.concatenate([[0, s.vocab - 1], lab_ids[pick], _units(s.vocab, 16, 22)]))
+    lse = np.empty(s.tokens)
+    per_row = np.empty(s.tokens)
+    dw_rows = np.zeros((len(ids), s.hidden))
+    for lo in range(0, s.tokens, CE_ROW_BLOCK):
+        sl = slice(lo, lo + CE_ROW_BLOCK)
+        f = O.linear_cross_entropy_fwd(X[sl], W, labels[sl])
+        lse[sl], per_row[sl] = f["lse"], f["per_row"]
+        # the block's share of the mean: dloss = its valid count / the total
+        dw_rows += O.linear_cross_entropy_bwd(X[sl], W, labels[sl], dloss=f["n_valid"] / n_valid,
+                                              vocab_rows=ids)["dW_rows"]
+    assert_f32(out["lse"], lse, "lse, every row")
+    assert_f32(out["loss"], [per_row.sum() / n_valid], "mean loss")
+    assert_bf16(_at(g["dW"], ids), dw_rows, f"dW, {len(ids)} sampled vocabulary rows")
+    rows = synth.sample_rows(s.tokens, N_ROWS).numpy()
     f = O.linear_cross_entropy_fwd(X[rows], W, labels[rows])
-    assert_f32(_at(out["lse"], rows), f["lse"], "lse rows")
     # the oracle's mean over the sample uses the sample's own count: rescale
     b = O.linear_cross_entropy_bwd(X[rows], W, labels[rows], dloss=f["n_valid"] / n_valid)
     assert_bf16(_at(g["dX"], rows), b["dX"], "dX rows")
-    # mean loss vs lse (checked above on samples) and exact target logits
-    valid = np.nonzero(labels != s.ignore_index)[0]
-    z_t = np.einsum("ij,ij->i", X[valid], W[labels[valid]])
-    mean = (to_np(out["lse"])[valid] - z_t).mean()
-    assert_f32(out["loss"], [mean], "mean loss vs per-row lse")
-    # rows of softmax - onehot sum to zero, so do the columns of dW
-    dW = to_np(g["dW"])
-    colsum = dW.sum(axis=0)
-    scale = np.sqrt((dW ** 2).sum(axis=0))
-    assert float(np.max(np.abs(colsum) / scale)) < 3e-2, "columns of dW do not sum to ~0"
 
 
 # ---------------------------------------------------------------- block, hidden 8192 (the bench workload)
@@ -143,11 +157,33 @@ def test_block_fullsize(coda):
     assert_bf16(_at(gr["dWg"], iu), bu["dWg"], "dWg sampled units")
     assert_bf16(_at(gr["dWu"], iu), bu["dWu"], "dWu sampled units")
     assert_bf16(_at(gr["dWd"], iu, 1), bu["dWd"], "dWd sampled units")
-    # gain gradients: consistency with the weight gradients at full size
-    _gamma_property(gr["dgamma_mlp"], t["gamma_mlp"], [(t["Wg"], gr["dWg"]), (t["Wu"], gr["dWu"])],
-                    "dgamma_mlp * gamma vs sum W dW")
-    _gamma_property(gr["dgamma_attn"], t["gamma_attn"], [(t["Wqkv"], gr["dWqkv"])],
-                    "dgamma_attn * gamma vs sum W dW")
+    # dgamma_mlp: the sum over blocks of intermediate units of the restricted
+    # MLPs' gain gradients
+    dgm = np.zeros(s.hidden)
+    for lo in range(0, s.inter, MLP_UNIT_BLOCK):
+        c = slice(lo, lo + MLP_UNIT_BLOCK)
+        dgm += O.mlp_bwd(x1, o["Wg"][c], o["Wu"][c], o["Wd"][:, c], to_np(t["dx2"]), o["gamma_mlp"],
+                         s.eps)["dgamma"]
+    assert_bf16(gr["dgamma_mlp"], dgm, "dgamma_mlp")
+    del x1
+    # QKV-side gradients whole: the oracle's block with every head, the MLP
+    # cut to the sampled units and the attention output to one 128-wide
+    # slice (neither enters dWqkv or the three gains)
+    sub = {k: to_np(v) for k, v in t.items() if k not in ("Wg", "Wu", "Wd", "A", "Wo")}
+    sub["pos"] = t["pos"].numpy()
+    sub["Wg"], sub["Wu"], sub["Wd"] = o["Wg"][iu], o["Wu"][iu], o["Wd"][:, iu]
+    sub["A"], sub["Wo"] = to_np(t["A"])[:, :128], o["Wo"][:, :128]
+    rq = O.block_bwd(sub, **cfg)
+    assert_bf16(gr["dWqkv"], rq["dWqkv"], "dWqkv, every row")
+    for k in ("dgamma_attn", "dgamma_q", "dgamma_k"):
+        assert_bf16(gr[k], rq[k], k)
+    del sub, rq
+    # dWo = dx1^T A: probed with a random vector against dx1 (checked above
+    # on sampled rows)
+    v = np.random.default_rng(23).standard_normal(s.n_q * s.head_dim)
+    lhs = to_np(gr["dWo"]) @ v
+    rhs = to_np(gr["dx1"]).T @ (to_np(t["A"]) @ v)
+    assert_bf16(lhs, rhs, "dWo v vs dx1^T (A v)")
 
 
 # ---------------------------------------------------------------- low-precision gate/up legs (bench shape)
