@@ -246,7 +246,7 @@ void wait_sleep(uint32_t& producer, uint32_t& epilogue) {
 // runtime until the work it tracks has completed).
 class EventSet {
  public:
-  explicit EventSet(int n) : n_(n) {
+  explicit EventSet(int n) : n_(n < 12 ? n : 12) {
     for (int i = 0; i < n_; ++i)
       if (cudaEventCreateWithFlags(&e_[i], cudaEventDisableTiming) != cudaSuccess) ok_ = false;
   }
@@ -262,7 +262,7 @@ class EventSet {
  private:
   int n_;
   bool ok_ = true;
-  cudaEvent_t e_[4] = {};
+  cudaEvent_t e_[12] = {};
 };
 
 // Kernel dispatch by epilogue kind and operand type.  With a.query_clusters
@@ -365,14 +365,17 @@ int prepare(const Plan& p, int* status, int cg, int nb_base, int n_tiles, CUtens
   return CODA_OK;
 }
 
-// The stream that carries the CTA-pair slice of a split launch issued on
-// `s`: one non-blocking stream per (device, caller stream), created once and
-// kept for the process, so that GEMMs the caller runs concurrently on
-// different streams do not queue behind each other's slices.
-cudaStream_t side_stream(cudaStream_t s) {
+// Helper streams of a call issued on `s`: role 0 carries the CTA-pair slice
+// of a split launch, roles 1 and 2 the dX and dW GEMMs of the sliced
+// cross-entropy backward.  One non-blocking stream per (device, caller
+// stream, role), created once and kept for the process, so that GEMMs the
+// caller runs concurrently on different streams do not queue behind each
+// other's helpers.
+cudaStream_t side_stream(cudaStream_t s, int role = 0) {
   static std::mutex mu;
-  constexpr int kSlots = 64;
+  constexpr int kSlots = 96;
   static int dev_of[kSlots];
+  static int role_of[kSlots];
   static cudaStream_t key[kSlots];
   static cudaStream_t val[kSlots];
   static int used = 0;
@@ -380,11 +383,12 @@ cudaStream_t side_stream(cudaStream_t s) {
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < used; ++i)
-    if (dev_of[i] == dev && key[i] == s) return val[i];
-  if (used == kSlots) return nullptr;  // no more slots: the caller launches unsplit
+    if (dev_of[i] == dev && key[i] == s && role_of[i] == role) return val[i];
+  if (used == kSlots) return nullptr;  // no more slots: the caller stays on s
   cudaStream_t t = nullptr;
   if (cudaStreamCreateWithFlags(&t, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
   dev_of[used] = dev;
+  role_of[used] = role;
   key[used] = s;
   val[used] = t;
   ++used;
@@ -810,7 +814,6 @@ int coda_rmsnorm_linear(const coda_bf16* X, const float* rstd_in, const coda_bf1
 size_t coda_rmsnorm_linear_bwd_workspace_size(int64_t M, int64_t N, int64_t K) {
   SizeCursor c;
   c.take<__nv_bfloat16>(static_cast<size_t>(M) * N);  // G'
-  c.take<float>(M);                                    // s
   c.take<float>(M);                                    // coef
   c.take<float>(static_cast<size_t>(4 * cdiv(M, 128)) * K);  // dgamma partials per (token block, warp)
   return c.off;
@@ -832,13 +835,13 @@ int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_
   if (sms <= 0) return CODA_ERR_CUDA;
   WsCursor w(ws);
   __nv_bfloat16* Gp = w.take<__nv_bfloat16>(static_cast<size_t>(M) * N);
-  float* srow = w.take<float>(M);
   float* coef = w.take<float>(M);
   const int64_t ntb = cdiv(M, 128);
   float* dgp = w.take<float>(static_cast<size_t>(4 * ntb) * K);
   int* status = static_cast<int*>(ws);
   cudaStream_t s = S(stream);
-  CU(coda::launch_rms_bwd_prepass(BF(dY), BF(Y), BF(R), rstd, M, N, Gp, srow, sms, s));
+  CU(coda::launch_rms_bwd_prepass(BF(dY), BF(Y), BF(R), rstd, M, N, 1.f / static_cast<float>(K), Gp, coef, sms,
+                                  s));
   // With a side stream, dW runs beside c -> dX (both read only G', X, W), so
   // each GEMM's partly filled last wave overlaps the other; they share only
   // the status word (atomic OR).
@@ -849,7 +852,6 @@ int coda_rmsnorm_linear_bwd(const coda_bf16* dY, const coda_bf16* X, const coda_
     CU(cudaEventRecord(ev[0], s));
     CU(cudaStreamWaitEvent(s2, ev[0], 0));
   }
-  CU(coda::launch_combine_rows(srow, M, 1, M, 1.f / static_cast<float>(K), 0.f, rstd, coef, 1, s));
   {  // D = G' W;  dX = gamma D - c X, dgamma column partials sum_i X_ik D_ik
     Plan p;
     p.kind = coda::EpiKind::RmsDx;
@@ -1225,7 +1227,6 @@ size_t coda_linear_qknorm_rope_bwd_workspace_size(int64_t M, int64_t Kdim, int32
   const int64_t N = static_cast<int64_t>(n_q + 2 * n_kv) * head_dim;
   SizeCursor c;
   c.take<__nv_bfloat16>(static_cast<size_t>(M) * N);          // G'
-  c.take<float>(M);                                           // s
   c.take<float>(M);                                           // coef
   c.take<float>(static_cast<size_t>(qk_bwd_blocks(M)) * 256);  // dgamma_q|k partials
   c.take<float>(static_cast<size_t>(4 * cdiv(M, 128)) * Kdim);  // dgamma_in partials per (token block, warp)
@@ -1265,7 +1266,6 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
   if (sms <= 0) return CODA_ERR_CUDA;
   WsCursor w(ws);
   __nv_bfloat16* Gp = w.take<__nv_bfloat16>(static_cast<size_t>(M) * N);
-  float* srow = w.take<float>(M);
   float* coef = w.take<float>(M);
   const int nblk = qk_bwd_blocks(M);
   float* dgqk = w.take<float>(static_cast<size_t>(nblk) * 256);
@@ -1273,13 +1273,12 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
   float* dgp = w.take<float>(static_cast<size_t>(4 * ntb) * Kdim);
   int* status = static_cast<int*>(ws);
   cudaStream_t s = S(stream);
+  // the map also writes the input RMSNorm's row coefficient c (with rstd)
   CU(coda::launch_qk_bwd(BF(dQ), BF(dK), BF(dV), BF(qk_save), BF(V), gamma_q, gamma_k, pos,
-                         reinterpret_cast<const float2*>(cos_sin), max_pos, eps, n_q, n_kv, rstd, M, Gp, srow, dgqk,
-                         nblk, status, s, rope_pairing == CODA_ROPE_HALF));
-  CU(coda::launch_colsum(dgqk, nblk, 128, 256, dgamma_q, s));
-  CU(coda::launch_colsum(dgqk + 128, nblk, 128, 256, dgamma_k, s));
-  if (norm)
-    CU(coda::launch_combine_rows(srow, M, 1, M, 1.f / static_cast<float>(Kdim), 0.f, rstd, coef, 1, s));
+                         reinterpret_cast<const float2*>(cos_sin), max_pos, eps, n_q, n_kv, rstd, M,
+                         1.f / static_cast<float>(Kdim), Gp, norm ? coef : nullptr, dgqk, nblk, status, s,
+                         rope_pairing == CODA_ROPE_HALF));
+  CU(coda::launch_colsum(dgqk, nblk, 256, 256, dgamma_q, s, 128, dgamma_k));
   {  // D = G' W_qkv;  dX = gamma_in D - c X + dX_resid with the dgamma_in column
      // partials sum_i X_ik D_ik  (without RMSNorm: D + dX_resid)
     Plan p;
@@ -1472,6 +1471,241 @@ int run_nvfp4(coda::EpiKind kind, const uint8_t* A, const uint8_t* B0, const uin
   return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
 }
 
+namespace {
+
+// ------------------------------------------------------------------ cross-entropy backward, by vocabulary slice
+// The backward never holds the gradient of the whole logit matrix: the
+// vocabulary is cut into slices of CE_SLICE columns, and for each slice s
+//   dZ_s = softmax part of (softmax - onehot) * w   (recomputed z; bf16)
+//   dX  += dZ_s W_s                                  (fp32 running sum)
+//   dW_s = dZ_s^T X                                  (its rows of dW)
+// The one-hot terms (-w_i W[y_i] for dX, -sum_{i: y_i = v} w_i X[i] for dW)
+// are applied exactly in fp32 in the epilogues; the last slice's dX GEMM adds
+// the running sum and writes bf16.  dZ_s is double-buffered: slice s + 1's
+// logits GEMM runs on the caller's stream while slice s's dX and dW GEMMs run
+// on two helper streams, so the launches' partly filled last waves overlap.
+// With the final RMSNorm folded into the head (rstd set) the stored dZ is
+// row-scaled, each slice's epilogue also emits the row partials sum p z and
+// the target logit for the RMSNorm-backward coefficient c_i, the last dX GEMM
+// subtracts c_i X_i and adds the residual-stream gradient, and dW is scaled
+// by gamma while its epilogue reduces W dW' over rows into dgamma partials.
+constexpr int64_t CE_SLICE = 16384;  // vocabulary columns per slice (64 tiles)
+
+int64_t ce_slice_cols(int64_t V) { return std::min<int64_t>(V, CE_SLICE); }
+
+size_t ce_bwd_workspace(int64_t M, int64_t V, int64_t K, bool rms) {
+  const int64_t sl = ce_slice_cols(V);
+  const int64_t nsl = sl > 0 ? cdiv(V, sl) : 0;
+  SizeCursor c;
+  c.take<__nv_bfloat16>(static_cast<size_t>(M) * sl);      // dZ_s, buffer 0
+  if (nsl > 1) {
+    c.take<__nv_bfloat16>(static_cast<size_t>(M) * sl);    // dZ_s, buffer 1
+    c.take<float>(static_cast<size_t>(M) * K);             // running dX (fp32)
+  }
+  c.take<float>(M);                                        // w_i (r_i w_i with rstd)
+  c.take<int32_t>(M);                                      // label of valid rows
+  c.take<int32_t>(V);                                      // counts per vocabulary row
+  c.take<int32_t>(V);                                      // scatter cursors
+  c.take<int32_t>(V + 1);                                  // CSR offsets
+  c.take<int32_t>(M);                                      // CSR token indices
+  if (rms) {
+    c.take<float>(static_cast<size_t>(cdiv(V, BN)) * M);   // row partials sum p z
+    c.take<float>(M);                                      // target logits
+    c.take<float>(M);                                      // RMSNorm coefficient c
+    c.take<float>(static_cast<size_t>(4 * cdiv(V, 128)) * K);  // dgamma partials
+  }
+  return c.off;
+}
+
+struct CeBwd {
+  const coda_bf16* X = nullptr;
+  const coda_bf16* W = nullptr;      // the weight the logits GEMM reads (gamma-folded with rstd)
+  const coda_bf16* W_raw = nullptr;  // rstd: the unfolded weight (dgamma partials)
+  const float* rstd = nullptr;       // final RMSNorm folded into the head
+  const float* gamma = nullptr;
+  const int32_t* labels = nullptr;
+  int32_t ignore_index = -100;
+  const float* lse = nullptr;
+  const int32_t* n_valid = nullptr;
+  float dloss = 1.f;
+  const coda_bf16* dX_resid = nullptr;
+  coda_bf16* dX = nullptr;
+  coda_bf16* dW = nullptr;
+  float* dgamma = nullptr;
+  int64_t M = 0, V = 0, K = 0;
+};
+
+int ce_backward(const CeBwd& a, void* ws, cudaStream_t s) {
+  const int64_t M = a.M, V = a.V, K = a.K;
+  const bool rms = a.rstd != nullptr;
+  const int64_t sl = ce_slice_cols(V);
+  const int nsl = static_cast<int>(cdiv(V, sl));
+  WsCursor w(ws);
+  __nv_bfloat16* dZ[2];
+  dZ[0] = w.take<__nv_bfloat16>(static_cast<size_t>(M) * sl);
+  dZ[1] = dZ[0];
+  float* acc = nullptr;
+  if (nsl > 1) {
+    dZ[1] = w.take<__nv_bfloat16>(static_cast<size_t>(M) * sl);
+    acc = w.take<float>(static_cast<size_t>(M) * K);
+  }
+  float* wrow = w.take<float>(M);
+  int32_t* lrow = w.take<int32_t>(M);
+  int32_t* counts = w.take<int32_t>(V);
+  int32_t* cursor = w.take<int32_t>(V);
+  int32_t* off = w.take<int32_t>(V + 1);
+  int32_t* idx = w.take<int32_t>(M);
+  float *pz = nullptr, *target = nullptr, *coef = nullptr, *dgp = nullptr;
+  const int ntile = static_cast<int>(cdiv(V, BN));
+  const int64_t nmb = cdiv(V, 128);
+  if (rms) {
+    pz = w.take<float>(static_cast<size_t>(ntile) * M);
+    target = w.take<float>(M);
+    coef = w.take<float>(M);
+    dgp = w.take<float>(static_cast<size_t>(4 * nmb) * K);
+  }
+  int* status = static_cast<int*>(ws);
+  CU(coda::launch_ce_onehot_prep(a.labels, a.ignore_index, M, V, a.n_valid, a.dloss, a.rstd, wrow, lrow, counts,
+                                 cursor, off, idx, s));
+  // helper streams for the dX and dW GEMMs; without them everything stays on s
+  cudaStream_t sx = side_stream(s, 1), sw = side_stream(s, 2);
+  if (!sx || !sw) sx = sw = s;
+  const bool conc = sx != s;
+  // events: 0 fork, 1-2 slice logits ready (per buffer), 3-4 dX done, 5-6 dW
+  // done, 7 RMSNorm coefficient ready
+  EventSet ev(8);
+  if (!ev.ok()) return CODA_ERR_CUDA;
+  if (conc) {
+    CU(cudaEventRecord(ev[0], s));
+    CU(cudaStreamWaitEvent(sx, ev[0], 0));
+    CU(cudaStreamWaitEvent(sw, ev[0], 0));
+  }
+  for (int i = 0; i < nsl; ++i) {
+    const int64_t v0 = static_cast<int64_t>(i) * sl;
+    const int64_t vs = std::min<int64_t>(sl, V - v0);
+    const int b = i & 1;
+    const bool last = i == nsl - 1;
+    const coda_bf16* Ws = a.W + v0 * K;
+    if (conc && i >= 2) {  // buffer b is free once slice i - 2's dX and dW have read it
+      CU(cudaStreamWaitEvent(s, ev[3 + b], 0));
+      CU(cudaStreamWaitEvent(s, ev[5 + b], 0));
+    }
+    {  // dZ_s = softmax(z_s) * w (row-scaled with rstd); z_s recomputed
+      Plan p;
+      p.kind = coda::EpiKind::CeDlogits;
+      p.A = a.X;
+      p.lda = K;
+      p.B = Ws;
+      p.ldb = K;
+      p.M = M;
+      p.N = vs;
+      p.K = K;
+      p.e.D = dZ[b];
+      p.e.ldd = sl;
+      p.e.labels = a.labels;
+      p.e.ignore_index = a.ignore_index;
+      p.e.lse = a.lse;
+      p.e.n_valid = a.n_valid;
+      p.e.dloss = a.dloss;
+      p.e.col_base = v0;
+      p.e.n_total = V;
+      if (rms) {
+        p.e.row_scale = a.rstd;
+        p.e.partials = pz + (v0 / BN) * M;
+        p.e.ld_part = M;
+        p.e.target_logit = target;
+      }
+      CK(run(p, status, s));
+    }
+    if (conc) {
+      CU(cudaEventRecord(ev[1 + b], s));
+      CU(cudaStreamWaitEvent(sx, ev[1 + b], 0));
+      CU(cudaStreamWaitEvent(sw, ev[1 + b], 0));
+    }
+    if (rms && last) {  // c_i from the row partials of every slice
+      CU(coda::launch_ce_norm_coef(pz, M, ntile, target, a.rstd, wrow, M, 1.f / static_cast<float>(K), coef, s));
+      if (conc) {
+        CU(cudaEventRecord(ev[7], s));
+        CU(cudaStreamWaitEvent(sx, ev[7], 0));
+      }
+    }
+    {  // dX: running fp32 sum of dZ_s W_s; the last slice writes bf16 with the row terms
+      Plan p;
+      p.A = dZ[b];
+      p.lda = sl;
+      p.B = Ws;
+      p.ldb = K;
+      p.b_mn = 1;
+      p.M = M;
+      p.N = K;
+      p.K = vs;
+      p.e.ldd = K;
+      if (!last) {
+        p.e.D = acc;
+        p.e.d_f32 = 1;
+        p.e.beta = i > 0;
+      } else {
+        p.e.D = a.dX;
+        p.e.acc_in = i > 0 ? acc : nullptr;
+        p.e.ld_acc_in = K;
+        p.e.row_coef = wrow;  // - w_i W[y_i] (r_i w_i Wf[y_i] with rstd)
+        p.e.aux1 = BF(a.W);
+        p.e.ld_aux1 = K;
+        p.e.gather_rows = lrow;
+        if (rms) {
+          p.e.aux0 = BF(a.dX_resid);
+          p.e.ld_aux0 = K;
+          p.e.row_coef2 = coef;  // - c_i X_i
+          p.e.aux3 = BF(a.X);
+          p.e.ld_aux3 = K;
+        }
+      }
+      CK(run(p, status, sx));
+    }
+    {  // dW rows of the slice: dZ_s^T X minus the one-hot rows (CSR of tokens per label)
+      Plan p;
+      p.A = dZ[b];
+      p.lda = sl;
+      p.a_mn = 1;
+      p.B = a.X;
+      p.ldb = K;
+      p.b_mn = 1;
+      p.M = vs;
+      p.N = K;
+      p.K = M;
+      p.e.D = a.dW + v0 * K;
+      p.e.ldd = K;
+      p.e.aux2 = BF(a.X);
+      p.e.ld_aux2 = K;
+      p.e.csr_off = off + v0;
+      p.e.csr_idx = idx;
+      p.e.csr_w = wrow;
+      if (rms) {  // dW = dW' diag(gamma); dgamma partials sum_rows W dW'
+        p.kind = coda::EpiKind::ColDot;
+        p.e.col_scale = a.gamma;
+        p.e.aux0 = BF(a.W_raw + v0 * K);
+        p.e.ld_aux0 = K;
+        p.e.partials = dgp + (v0 / 128) * 4 * K;
+        p.e.ld_part = K;
+      }
+      CK(run(p, status, sw));
+    }
+    if (conc) {
+      CU(cudaEventRecord(ev[3 + b], sx));
+      CU(cudaEventRecord(ev[5 + b], sw));
+    }
+  }
+  if (conc) {  // join: the helper streams' last records cover all their work
+    const int b = (nsl - 1) & 1;
+    CU(cudaStreamWaitEvent(s, ev[3 + b], 0));
+    CU(cudaStreamWaitEvent(s, ev[5 + b], 0));
+  }
+  if (rms) CU(coda::launch_colsum(dgp, 4 * nmb, K, K, a.dgamma, s));
+  return CODA_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int32_t* labels, int32_t ignore_index,
@@ -1480,16 +1714,8 @@ int coda_linear_cross_entropy(const coda_bf16* X, const coda_bf16* W, const int3
   return ce_forward(X, W, labels, ignore_index, nullptr, loss_mean, lse, n_valid, M, V, K, ws, ws_bytes, stream);
 }
 
-size_t coda_linear_cross_entropy_bwd_workspace_size(int64_t M, int64_t V, int64_t) {
-  SizeCursor c;
-  c.take<__nv_bfloat16>(static_cast<size_t>(M) * V);  // dZ (softmax part)
-  c.take<float>(M);                                    // w_i
-  c.take<int32_t>(M);                                  // label of valid rows
-  c.take<int32_t>(V);                                  // counts per vocabulary row
-  c.take<int32_t>(V);                                  // scatter cursors
-  c.take<int32_t>(V + 1);                              // CSR offsets
-  c.take<int32_t>(M);                                  // CSR token indices
-  return c.off;
+size_t coda_linear_cross_entropy_bwd_workspace_size(int64_t M, int64_t V, int64_t K) {
+  return ce_bwd_workspace(M, V, K, false);
 }
 
 int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const int32_t* labels,
@@ -1509,76 +1735,20 @@ int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const 
     CU(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * K * 2, S(stream)));
     return CODA_OK;
   }
-  WsCursor w(ws);
-  __nv_bfloat16* dZ = w.take<__nv_bfloat16>(static_cast<size_t>(M) * V);
-  float* wrow = w.take<float>(M);
-  int32_t* lrow = w.take<int32_t>(M);
-  int32_t* counts = w.take<int32_t>(V);
-  int32_t* cursor = w.take<int32_t>(V);
-  int32_t* off = w.take<int32_t>(V + 1);
-  int32_t* idx = w.take<int32_t>(M);
-  int* status = static_cast<int*>(ws);
-  cudaStream_t s = S(stream);
-  CU(coda::launch_ce_onehot_prep(labels, ignore_index, M, V, n_valid, dloss, nullptr, wrow, lrow, counts, cursor,
-                                 off, idx, s));
-  {  // dZ = softmax * dloss / n_valid (the one-hot part is applied exactly below)
-    Plan p;
-    p.kind = coda::EpiKind::CeDlogits;
-    p.A = X;
-    p.lda = K;
-    p.B = W;
-    p.ldb = K;
-    p.M = M;
-    p.N = V;
-    p.K = K;
-    p.e.D = dZ;
-    p.e.ldd = V;
-    p.e.labels = labels;
-    p.e.ignore_index = ignore_index;
-    p.e.lse = lse;
-    p.e.n_valid = n_valid;
-    p.e.dloss = dloss;
-    CK(run(p, status, s));
-  }
-  {  // dX = dZ W - w_i W[y_i]
-    Plan p;
-    p.A = dZ;
-    p.lda = V;
-    p.B = W;
-    p.ldb = K;
-    p.b_mn = 1;
-    p.M = M;
-    p.N = K;
-    p.K = V;
-    p.e.D = dX;
-    p.e.ldd = K;
-    p.e.row_coef = wrow;
-    p.e.aux1 = BF(W);
-    p.e.ld_aux1 = K;
-    p.e.gather_rows = lrow;
-    CK(run(p, status, s));
-  }
-  {  // dW = dZ^T X - sum over tokens labelled v of w_i X[i]
-    Plan p;
-    p.A = dZ;
-    p.lda = V;
-    p.a_mn = 1;
-    p.B = X;
-    p.ldb = K;
-    p.b_mn = 1;
-    p.M = V;
-    p.N = K;
-    p.K = M;
-    p.e.D = dW;
-    p.e.ldd = K;
-    p.e.aux2 = BF(X);
-    p.e.ld_aux2 = K;
-    p.e.csr_off = off;
-    p.e.csr_idx = idx;
-    p.e.csr_w = wrow;
-    CK(run(p, status, s));
-  }
-  return CODA_OK;
+  CeBwd a;
+  a.X = X;
+  a.W = W;
+  a.labels = labels;
+  a.ignore_index = ignore_index;
+  a.lse = lse;
+  a.n_valid = n_valid;
+  a.dloss = dloss;
+  a.dX = dX;
+  a.dW = dW;
+  a.M = M;
+  a.V = V;
+  a.K = K;
+  return ce_backward(a, ws, S(stream));
 }
 
 
@@ -1596,19 +1766,7 @@ int coda_rmsnorm_linear_cross_entropy(const coda_bf16* X, const float* rstd, con
 }
 
 size_t coda_rmsnorm_linear_cross_entropy_bwd_workspace_size(int64_t M, int64_t V, int64_t K) {
-  SizeCursor c;
-  c.take<__nv_bfloat16>(static_cast<size_t>(M) * V);           // G' = r * softmax * w
-  c.take<float>(M);                                             // r_i w_i
-  c.take<int32_t>(M);                                           // label of valid rows
-  c.take<int32_t>(V);                                           // counts
-  c.take<int32_t>(V);                                           // cursors
-  c.take<int32_t>(V + 1);                                       // CSR offsets
-  c.take<int32_t>(M);                                           // CSR token indices
-  c.take<float>(static_cast<size_t>(cdiv(V, BN)) * M);          // row partials sum p z
-  c.take<float>(M);                                             // target logits
-  c.take<float>(M);                                             // RMSNorm coefficient c
-  c.take<float>(static_cast<size_t>(4 * cdiv(V, 128)) * K);     // dgamma partials
-  return c.off;
+  return ce_bwd_workspace(M, V, K, true);
 }
 
 int coda_rmsnorm_linear_cross_entropy_bwd(const coda_bf16* X, const float* rstd, const float* gamma,
@@ -1628,99 +1786,25 @@ int coda_rmsnorm_linear_cross_entropy_bwd(const coda_bf16* X, const float* rstd,
   for (const void* q : {(const void*)X, (const void*)gamma, (const void*)W, (const void*)Wf, (const void*)dX_resid,
                         (const void*)dX, (const void*)dW})
     CK(al(q));
-  WsCursor w(ws);
-  __nv_bfloat16* Gp = w.take<__nv_bfloat16>(static_cast<size_t>(M) * V);
-  float* rw = w.take<float>(M);
-  int32_t* lrow = w.take<int32_t>(M);
-  int32_t* counts = w.take<int32_t>(V);
-  int32_t* cursor = w.take<int32_t>(V);
-  int32_t* off = w.take<int32_t>(V + 1);
-  int32_t* idx = w.take<int32_t>(M);
-  const int ntile = static_cast<int>(cdiv(V, BN));
-  float* pz = w.take<float>(static_cast<size_t>(ntile) * M);
-  float* target = w.take<float>(M);
-  float* coef = w.take<float>(M);
-  const int64_t nmb = cdiv(V, 128);
-  float* dgp = w.take<float>(static_cast<size_t>(4 * nmb) * K);
-  int* status = static_cast<int*>(ws);
-  cudaStream_t s = S(stream);
-  CU(coda::launch_ce_onehot_prep(labels, ignore_index, M, V, n_valid, dloss, rstd, rw, lrow, counts, cursor, off,
-                                 idx, s));
-  {  // G' = r * softmax(r * X Wf^T) * w; row partials sum p z; target logits
-    Plan p;
-    p.kind = coda::EpiKind::CeDlogits;
-    p.A = X;
-    p.lda = K;
-    p.B = Wf;
-    p.ldb = K;
-    p.M = M;
-    p.N = V;
-    p.K = K;
-    p.e.D = Gp;
-    p.e.ldd = V;
-    p.e.row_scale = rstd;
-    p.e.labels = labels;
-    p.e.ignore_index = ignore_index;
-    p.e.lse = lse;
-    p.e.n_valid = n_valid;
-    p.e.dloss = dloss;
-    p.e.partials = pz;
-    p.e.ld_part = M;
-    p.e.target_logit = target;
-    CK(run(p, status, s));
-  }
-  CU(coda::launch_ce_norm_coef(pz, M, ntile, target, rstd, rw, M, 1.f / static_cast<float>(K), coef, s));
-  {  // dX = G' Wf - r_i w_i Wf[y_i] - c_i X_i (+ dX_resid)
-    Plan p;
-    p.A = Gp;
-    p.lda = V;
-    p.B = Wf;
-    p.ldb = K;
-    p.b_mn = 1;
-    p.M = M;
-    p.N = K;
-    p.K = V;
-    p.e.D = dX;
-    p.e.ldd = K;
-    p.e.aux0 = BF(dX_resid);
-    p.e.ld_aux0 = K;
-    p.e.row_coef = rw;
-    p.e.aux1 = BF(Wf);
-    p.e.ld_aux1 = K;
-    p.e.gather_rows = lrow;
-    p.e.row_coef2 = coef;
-    p.e.aux3 = BF(X);
-    p.e.ld_aux3 = K;
-    CK(run(p, status, s));
-  }
-  {  // dW = (G'^T X - one-hot rows) diag(gamma); dgamma partials
-    Plan p;
-    p.kind = coda::EpiKind::ColDot;
-    p.A = Gp;
-    p.lda = V;
-    p.a_mn = 1;
-    p.B = X;
-    p.ldb = K;
-    p.b_mn = 1;
-    p.M = V;
-    p.N = K;
-    p.K = M;
-    p.e.D = dW;
-    p.e.ldd = K;
-    p.e.col_scale = gamma;
-    p.e.aux0 = BF(W);
-    p.e.ld_aux0 = K;
-    p.e.partials = dgp;
-    p.e.ld_part = K;
-    p.e.aux2 = BF(X);
-    p.e.ld_aux2 = K;
-    p.e.csr_off = off;
-    p.e.csr_idx = idx;
-    p.e.csr_w = rw;
-    CK(run(p, status, s));
-  }
-  CU(coda::launch_colsum(dgp, 4 * nmb, K, K, dgamma, s));
-  return CODA_OK;
+  CeBwd a;
+  a.X = X;
+  a.W = Wf;
+  a.W_raw = W;
+  a.rstd = rstd;
+  a.gamma = gamma;
+  a.labels = labels;
+  a.ignore_index = ignore_index;
+  a.lse = lse;
+  a.n_valid = n_valid;
+  a.dloss = dloss;
+  a.dX_resid = dX_resid;
+  a.dX = dX;
+  a.dW = dW;
+  a.dgamma = dgamma;
+  a.M = M;
+  a.V = V;
+  a.K = K;
+  return ce_backward(a, ws, S(stream));
 }
 
 

@@ -111,10 +111,11 @@ cudaError_t launch_combine_rows(const float* p, int64_t ld, int nparts, int64_t 
 }
 
 // ---------------------------------------------------------------- RMSNorm-bwd pre-pass
-// G' = bf16(r * G);  s_i = sum_n G_in (Y - R)_in
+// G' = bf16(r * G);  c_i = r_i^2 * sum_n G_in (Y - R)_in * inv_k, the row
+// coefficient of the RMSNorm backward (inv_k = 1 / K of the projection)
 __global__ void rms_bwd_prepass_kernel(const __nv_bfloat16* __restrict__ G, const __nv_bfloat16* __restrict__ Y,
                                        const __nv_bfloat16* __restrict__ R, const float* __restrict__ rstd,
-                                       int64_t M, int64_t N, __nv_bfloat16* Gp, float* srow) {
+                                       int64_t M, int64_t N, float inv_k, __nv_bfloat16* Gp, float* coef) {
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -140,24 +141,26 @@ __global__ void rms_bwd_prepass_kernel(const __nv_bfloat16* __restrict__ G, cons
       store_bf16x8(Gp + o, g);
     }
     s = warp_sum(s);
-    if (lane == 0) srow[row] = s;
+    if (lane == 0) coef[row] = r * r * s * inv_k;
   }
 }
 
 cudaError_t launch_rms_bwd_prepass(const __nv_bfloat16* G, const __nv_bfloat16* Y, const __nv_bfloat16* R,
-                                   const float* rstd, int64_t M, int64_t N, __nv_bfloat16* Gp, float* srow,
-                                   int num_sms, cudaStream_t s) {
+                                   const float* rstd, int64_t M, int64_t N, float inv_k, __nv_bfloat16* Gp,
+                                   float* coef, int num_sms, cudaStream_t s) {
   const int64_t blocks = std::min<int64_t>((M + 7) / 8, static_cast<int64_t>(num_sms) * 8);
   rms_bwd_prepass_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(G, Y, R, rstd, M, N,
-                                                                                             Gp, srow);
+                                                                                             inv_k, Gp, coef);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- column sums
-// out[k] = sum_r p[r*ld + k], fixed summation order (deterministic).
+// out[k] = sum_r p[r*ld + k], fixed summation order (deterministic); columns
+// from `split` on go to out2[k - split] instead (two vectors in one launch).
 // Block = 32 columns x 32 row groups; row group g sums rows g, g+32, ...;
 // the 32 group sums are then added in order.
-__global__ void colsum_kernel(const float* __restrict__ p, int64_t nrows, int64_t ncols, int64_t ld, float* out) {
+__global__ void colsum_kernel(const float* __restrict__ p, int64_t nrows, int64_t ncols, int64_t ld, float* out,
+                              int64_t split, float* out2) {
   griddep_launch_dependents();
   __shared__ float part[32][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
@@ -170,12 +173,17 @@ __global__ void colsum_kernel(const float* __restrict__ p, int64_t nrows, int64_
   if (ty == 0 && col < ncols) {
     float t = 0.f;
     for (int g = 0; g < 32; ++g) t += part[g][tx];
-    out[col] = t;
+    if (col < split)
+      out[col] = t;
+    else
+      out2[col - split] = t;
   }
 }
 
-cudaError_t launch_colsum(const float* p, int64_t nrows, int64_t ncols, int64_t ld, float* out, cudaStream_t s) {
-  colsum_kernel<<<static_cast<unsigned>((ncols + 31) / 32), 1024, 0, s>>>(p, nrows, ncols, ld, out);
+cudaError_t launch_colsum(const float* p, int64_t nrows, int64_t ncols, int64_t ld, float* out, cudaStream_t s,
+                          int64_t split, float* out2) {
+  if (split < 0 || !out2) split = ncols;
+  colsum_kernel<<<static_cast<unsigned>((ncols + 31) / 32), 1024, 0, s>>>(p, nrows, ncols, ld, out, split, out2);
   return cudaGetLastError();
 }
 
@@ -484,22 +492,39 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* p, const float* v) {
   *reinterpret_cast<uint2*>(p) = q;
 }
 
+// Four warp sums at once: the shuffles of the four chains interleave.
+__device__ __forceinline__ void warp_sum4(float* v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], o);
+  }
+}
+
 // HALF: RoPE pairs (j, j + 64) of each head (lanes l and l + 16 hold the
 // two elements of a pair) instead of interleaved pairs (2j, 2j + 1).
+// A warp owns one token row and takes its heads four at a time: the four
+// heads' gradient and saved-input loads are issued together, and their
+// per-head reductions run as interleaved shuffle chains, so each warp keeps
+// 2 KB of loads in flight instead of 512 bytes.  With rstd given, the row
+// coefficient c_i = r_i^2 * sum_j dq_ij x_ij * inv_k of the input RMSNorm's
+// backward is written to coef (no separate combine pass).
 template <bool HALF>
 __global__ void __launch_bounds__(QK_BWD_WARPS * 32)
     qk_bwd_kernel(const __nv_bfloat16* __restrict__ dQ, const __nv_bfloat16* __restrict__ dK,
                   const __nv_bfloat16* __restrict__ dV, const __nv_bfloat16* __restrict__ qk_save,
                   const __nv_bfloat16* __restrict__ Vs, const float* __restrict__ gq, const float* __restrict__ gk,
                   const int32_t* __restrict__ pos, const float2* __restrict__ cs, int max_pos, float eps, int n_q,
-                  int n_kv, const float* __restrict__ rstd, int64_t M, __nv_bfloat16* Gp, float* srow,
-                  float* dgam_part, int* status) {
+                  int n_kv, const float* __restrict__ rstd, int64_t M, float inv_k, __nv_bfloat16* Gp,
+                  float* coef, float* dgam_part, int* status) {
   griddep_launch_dependents();
   constexpr int D = 128;
+  constexpr int HG = 4;  // heads per group
   __shared__ float red[QK_BWD_WARPS][2 * D];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t ldq = static_cast<int64_t>(n_q) * D, ldkv = static_cast<int64_t>(n_kv) * D;
   const int64_t ldsave = ldq + ldkv, ldg = ldq + 2 * ldkv;
+  const int nqk = n_q + n_kv;
   float aq[4] = {0.f, 0.f, 0.f, 0.f}, ak[4] = {0.f, 0.f, 0.f, 0.f};
   float g_q[4], g_k[4];
   {
@@ -525,66 +550,105 @@ __global__ void __launch_bounds__(QK_BWD_WARPS * 32)
     }
     const float r = rstd ? rstd[row] : 1.f;
     float s = 0.f;
-    for (int h = 0; h < n_q + n_kv; ++h) {
-      const bool is_q = h < n_q;
-      const __nv_bfloat16* src = is_q ? dQ + row * ldq + h * D : dK + row * ldkv + (h - n_q) * D;
-      float d[4], x[4];
-      load_bf16x4(src + 4 * lane, d);
-      load_bf16x4(qk_save + row * ldsave + h * D + 4 * lane, x);
-      const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
-      const float rho = rsqrtf(ss * (1.f / D) + eps);
-      float n[4], dn[4];
+    for (int h0 = 0; h0 < nqk; h0 += HG) {
+      float d[HG][4], x[HG][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) n[i] = x[i] * rho;
-      if constexpr (HALF) {
-        // inverse rotation of (first half, second half) element pairs; the
-        // partner sits in lane l ^ 16 at the same index
-        const bool second = lane >= 16;
+      for (int j = 0; j < HG; ++j) {
+        const int h = h0 + j;
+        if (h < nqk) {
+          const __nv_bfloat16* src = h < n_q ? dQ + row * ldq + h * D : dK + row * ldkv + (h - n_q) * D;
+          load_bf16x4(src + 4 * lane, d[j]);
+          load_bf16x4(qk_save + row * ldsave + h * D + 4 * lane, x[j]);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float dp = __shfl_xor_sync(0xffffffffu, d[i], 16);
-          dn[i] = second ? -dp * ch[i].y + d[i] * ch[i].x : d[i] * ch[i].x + dp * ch[i].y;
+          for (int i = 0; i < 4; ++i) d[j][i] = x[j][i] = 0.f;
         }
-      } else {
-        // inverse rotation of pairs (0,1) with c0 and (2,3) with c1
-        dn[0] = d[0] * c0.x + d[1] * c0.y;
-        dn[1] = -d[0] * c0.y + d[1] * c0.x;
-        dn[2] = d[2] * c1.x + d[3] * c1.y;
-        dn[3] = -d[2] * c1.y + d[3] * c1.x;
       }
-      const float* g = is_q ? g_q : g_k;
-      float* acc = is_q ? aq : ak;
-      float dng[4];
-      float t = 0.f;
+      float rho[HG];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[i] += dn[i] * n[i];
-        dng[i] = dn[i] * g[i];
-        t += n[i] * dng[i];
-      }
-      t = warp_sum(t) * (1.f / D);
-      float dq[4];
+      for (int j = 0; j < HG; ++j)
+        rho[j] = x[j][0] * x[j][0] + x[j][1] * x[j][1] + x[j][2] * x[j][2] + x[j][3] * x[j][3];
+      warp_sum4(rho);
+      float n[HG][4], dng[HG][4], t[HG];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        dq[i] = rho * (dng[i] - n[i] * t);
-        s += dq[i] * x[i];
-        dq[i] *= r;
+      for (int j = 0; j < HG; ++j) {
+        rho[j] = rsqrtf(rho[j] * (1.f / D) + eps);
+        const bool is_q = h0 + j < n_q;
+        float dn[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) n[j][i] = x[j][i] * rho[j];
+        if constexpr (HALF) {
+          // inverse rotation of (first half, second half) element pairs; the
+          // partner sits in lane l ^ 16 at the same index
+          const bool second = lane >= 16;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float dp = __shfl_xor_sync(0xffffffffu, d[j][i], 16);
+            dn[i] = second ? -dp * ch[i].y + d[j][i] * ch[i].x : d[j][i] * ch[i].x + dp * ch[i].y;
+          }
+        } else {
+          // inverse rotation of pairs (0,1) with c0 and (2,3) with c1
+          dn[0] = d[j][0] * c0.x + d[j][1] * c0.y;
+          dn[1] = -d[j][0] * c0.y + d[j][1] * c0.x;
+          dn[2] = d[j][2] * c1.x + d[j][3] * c1.y;
+          dn[3] = -d[j][2] * c1.y + d[j][3] * c1.x;
+        }
+        t[j] = 0.f;
+        if (h0 + j < nqk) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float gg = is_q ? g_q[i] : g_k[i];
+            if (is_q)
+              aq[i] += dn[i] * n[j][i];
+            else
+              ak[i] += dn[i] * n[j][i];
+            dng[j][i] = dn[i] * gg;
+            t[j] += n[j][i] * dng[j][i];
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dng[j][i] = 0.f;
+        }
       }
-      store_bf16x4(Gp + row * ldg + h * D + 4 * lane, dq);
+      warp_sum4(t);
+#pragma unroll
+      for (int j = 0; j < HG; ++j) {
+        const int h = h0 + j;
+        if (h < nqk) {
+          float dq[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            dq[i] = rho[j] * (dng[j][i] - n[j][i] * t[j] * (1.f / D));
+            s += dq[i] * x[j][i];
+            dq[i] *= r;
+          }
+          store_bf16x4(Gp + row * ldg + h * D + 4 * lane, dq);
+        }
+      }
     }
-    for (int h = 0; h < n_kv; ++h) {
-      float d[4], v[4];
-      load_bf16x4(dV + row * ldkv + h * D + 4 * lane, d);
-      load_bf16x4(Vs + row * ldkv + h * D + 4 * lane, v);
+    for (int h0 = 0; h0 < n_kv; h0 += HG) {
+      float d[HG][4], v[HG][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        s += d[i] * v[i];
-        d[i] *= r;
+      for (int j = 0; j < HG; ++j) {
+        if (h0 + j < n_kv) {
+          load_bf16x4(dV + row * ldkv + (h0 + j) * D + 4 * lane, d[j]);
+          load_bf16x4(Vs + row * ldkv + (h0 + j) * D + 4 * lane, v[j]);
+        }
       }
-      store_bf16x4(Gp + row * ldg + ldsave + h * D + 4 * lane, d);
+#pragma unroll
+      for (int j = 0; j < HG; ++j) {
+        if (h0 + j < n_kv) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            s += d[j][i] * v[j][i];
+            d[j][i] *= r;
+          }
+          store_bf16x4(Gp + row * ldg + ldsave + (h0 + j) * D + 4 * lane, d[j]);
+        }
+      }
     }
     s = warp_sum(s);
-    if (lane == 0) srow[row] = s;
+    if (lane == 0 && coef) coef[row] = r * r * s * inv_k;
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -602,14 +666,14 @@ __global__ void __launch_bounds__(QK_BWD_WARPS * 32)
 cudaError_t launch_qk_bwd(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, const __nv_bfloat16* dV,
                           const __nv_bfloat16* qk_save, const __nv_bfloat16* V, const float* gq, const float* gk,
                           const int32_t* pos, const float2* cs, int max_pos, float eps, int n_q, int n_kv,
-                          const float* rstd, int64_t M, __nv_bfloat16* Gp, float* srow, float* dgam_part,
-                          int nblk, int* status, cudaStream_t s, bool rope_half) {
+                          const float* rstd, int64_t M, float inv_k, __nv_bfloat16* Gp, float* coef,
+                          float* dgam_part, int nblk, int* status, cudaStream_t s, bool rope_half) {
   if (rope_half)
     qk_bwd_kernel<true><<<nblk, QK_BWD_WARPS * 32, 0, s>>>(dQ, dK, dV, qk_save, V, gq, gk, pos, cs, max_pos, eps,
-                                                           n_q, n_kv, rstd, M, Gp, srow, dgam_part, status);
+                                                           n_q, n_kv, rstd, M, inv_k, Gp, coef, dgam_part, status);
   else
     qk_bwd_kernel<false><<<nblk, QK_BWD_WARPS * 32, 0, s>>>(dQ, dK, dV, qk_save, V, gq, gk, pos, cs, max_pos, eps,
-                                                            n_q, n_kv, rstd, M, Gp, srow, dgam_part, status);
+                                                            n_q, n_kv, rstd, M, inv_k, Gp, coef, dgam_part, status);
   return cudaGetLastError();
 }
 

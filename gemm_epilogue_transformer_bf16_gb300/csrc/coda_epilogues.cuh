@@ -108,8 +108,8 @@ __device__ __forceinline__ void warp_colsum_partial(float* p, int lane) {
 }
 
 // ---------------------------------------------------------------------------
-// PLAIN:  D = rs_i * cs_j * acc + aux0 - coef_i * aux1[g_i] - coef2_i * aux3
-//             - sum_{t in csr(i)} w_t * aux2[t]  (+ D if beta)
+// PLAIN:  D = rs_i * cs_j * acc + aux0 (+ acc_in) - coef_i * aux1[g_i]
+//             - coef2_i * aux3 - sum_{t in csr(i)} w_t * aux2[t]  (+ D if beta)
 // optional row partial  sum_j D_ij^2  (of the stored, rounded values), and
 // optional second output  out1 = bf16(D_ij * cs2_j)  (D as stored: the
 // input of the next RMSNorm-reparameterised GEMM, x ⊙ gamma, written by the
@@ -164,6 +164,12 @@ struct EpiPlain {
               load_bf16x8(e.aux0 + static_cast<int64_t>(row) * e.ld_aux0 + cc, r8);
 #pragma unroll
               for (int i = 0; i < 8; ++i) x[i] += r8[i];
+            }
+            if (e.acc_in) {
+              float a8[8];
+              load_f32x8(e.acc_in + static_cast<int64_t>(row) * e.ld_acc_in + cc, a8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[i] += a8[i];
             }
             if (e.row_coef && arow >= 0) {
               float r8[8];
@@ -594,6 +600,9 @@ struct EpiCeLse {
 // reparameterised backward), and for the RMSNorm backward coefficient the
 // epilogue also emits row partials sum_j p_ij z_ij (partials[nb][row]) and
 // the target logit z_{i,y_i} (target_logit).
+// A launch may cover one slice of the vocabulary: its column 0 is vocabulary
+// column col_base, and n_total is the vocabulary size that decides which
+// labels are valid.
 // ---------------------------------------------------------------------------
 template <int BN>
 struct EpiCeDlogits {
@@ -608,9 +617,13 @@ struct EpiCeDlogits {
     if (rv) {
       lab = e.labels[row];
       const int nv = *e.n_valid;
-      const bool valid = lab != e.ignore_index && lab >= 0 && lab < t.N && nv > 0;
+      const int64_t vocab = e.n_total ? e.n_total : t.N;
+      const bool valid = lab != e.ignore_index && lab >= 0 && lab < vocab && nv > 0;
       w = valid ? e.dloss / static_cast<float>(nv) : 0.f;
-      if (!valid) lab = -1;
+      // the label's column within this launch (a slice of the vocabulary
+      // starts at col_base); outside the launch it matches no column
+      const int64_t rel = static_cast<int64_t>(lab) - e.col_base;
+      lab = (valid && rel >= 0 && rel < t.N) ? static_cast<int>(rel) : -1;
       lse = e.lse[row];
     }
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;

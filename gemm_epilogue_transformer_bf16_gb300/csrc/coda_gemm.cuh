@@ -104,6 +104,10 @@ struct EpiArgs {
   int aux_prefetch;             // DSWIGLU: request the tile's g/u rows into L2 before the chunk loop
   int mode;                     // SIGMOID: 0 forward, 1 backward on the recomputed logits
   float* target_logit;
+  int64_t col_base;             // CE_DLOGITS: vocabulary column of the launch's column 0 (a vocabulary slice)
+  int64_t n_total;              // CE_DLOGITS: vocabulary size (0: the launch's N)
+  const float* acc_in;          // PLAIN (bf16 D): fp32 tile added to the result (a running sum over slices)
+  int64_t ld_acc_in;
   // QK-RMSNorm + RoPE
   const int32_t* pos;
   const float2* cos_sin;

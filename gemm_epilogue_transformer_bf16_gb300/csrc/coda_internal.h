@@ -80,10 +80,13 @@ cudaError_t launch_row_rstd(const __nv_bfloat16* X, int64_t ldx, int64_t M, int6
 // mode 0: out = 1/sqrt(sum_t p[t] * inv_k + eps);  mode 1: out = r^2 * sum_t p[t] * inv_k
 cudaError_t launch_combine_rows(const float* p, int64_t ld, int nparts, int64_t M, float inv_k, float eps,
                                 const float* r, float* out, int mode, cudaStream_t s);
+// G' = bf16(r G) and the RMSNorm-backward row coefficient c = r^2 sum G (Y - R) * inv_k
 cudaError_t launch_rms_bwd_prepass(const __nv_bfloat16* G, const __nv_bfloat16* Y, const __nv_bfloat16* R,
-                                   const float* rstd, int64_t M, int64_t N, __nv_bfloat16* Gp, float* srow,
-                                   int num_sms, cudaStream_t s);
-cudaError_t launch_colsum(const float* p, int64_t nrows, int64_t ncols, int64_t ld, float* out, cudaStream_t s);
+                                   const float* rstd, int64_t M, int64_t N, float inv_k, __nv_bfloat16* Gp,
+                                   float* coef, int num_sms, cudaStream_t s);
+// column sums; with out2, columns from `split` on go to out2
+cudaError_t launch_colsum(const float* p, int64_t nrows, int64_t ncols, int64_t ld, float* out, cudaStream_t s,
+                          int64_t split = -1, float* out2 = nullptr);
 cudaError_t launch_ce_combine(const float2* part, int64_t ld, int nchunks, const float* target,
                               const int32_t* labels, int32_t ignore, int64_t M, int64_t V, float* lse,
                               double* blk_loss, int* blk_cnt, int nblk, float* loss_mean, int32_t* n_valid,
@@ -100,8 +103,8 @@ cudaError_t launch_rope_table(double theta, int head_dim, int max_pos, float2* c
 cudaError_t launch_qk_bwd(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, const __nv_bfloat16* dV,
                           const __nv_bfloat16* qk_save, const __nv_bfloat16* V, const float* gq, const float* gk,
                           const int32_t* pos, const float2* cs, int max_pos, float eps, int n_q, int n_kv,
-                          const float* rstd, int64_t M, __nv_bfloat16* Gp, float* srow, float* dgam_part,
-                          int nblk, int* status, cudaStream_t s, bool rope_half = false);
+                          const float* rstd, int64_t M, float inv_k, __nv_bfloat16* Gp, float* coef,
+                          float* dgam_part, int nblk, int* status, cudaStream_t s, bool rope_half = false);
 
 constexpr int QK_BWD_WARPS = 8;
 constexpr int CE_COMBINE_THREADS = 256;

@@ -523,7 +523,9 @@ int coda_rmsnorm_linear_cross_entropy(const coda_bf16* X, const float* rstd, con
  *   dX = G' Wf - c ⊙ X (+ dX_resid),  c_i = r_i^2 sum_v G_iv z_iv / K,
  *   dW = (G'^T X) diag(gamma),  dgamma_k = sum_v W_vk (G'^T X)_vk.
  * The one-hot part of G' is applied exactly in fp32 (row gather of Wf for dX,
- * a label -> token list for dW); only r * softmax * w is staged in bf16.
+ * a label -> token list for dW); only r * softmax * w is staged in bf16, one
+ * vocabulary slice of 16384 columns at a time, as in
+ * coda_linear_cross_entropy_bwd (workspace of order M x min(V, 16384)).
  * Inputs: X [M,K] (the un-normalised residual stream), rstd [M], gamma [K],
  * W and Wf [V,K], labels [M], lse [M] and n_valid from the forward,
  * dX_resid [M,K] or NULL.  Outputs: dX [M,K], dW [V,K] bf16, dgamma [K] fp32. */
@@ -568,8 +570,17 @@ int coda_linear_cross_entropy_noalloc(const coda_bf16* X, const coda_bf16* W, co
 /* Backward for upstream gradient dloss of the mean loss:
  *   dZ = (softmax(z) - onehot(y)) * dloss / n_valid (0 on ignored rows),
  *   dX = dZ W [M, K], dW = dZ^T X [V, K] (bf16).
- * lse and n_valid are the forward's outputs (device pointers).  dZ is
- * recomputed tile by tile from X W^T and staged in the workspace. */
+ * lse and n_valid are the forward's outputs (device pointers).  The
+ * gradient of the whole logit matrix is never held: the vocabulary is taken
+ * in slices of 16384 columns, and for each slice dZ_s is recomputed from
+ * X W_s^T into the workspace (bf16, two buffers of M x 16384), dX += dZ_s W_s
+ * is summed in fp32 (an M x K buffer) and dW_s = dZ_s^T X written; the
+ * one-hot part is applied exactly in fp32 by the dX and dW epilogues.  The
+ * workspace therefore grows as M x min(V, 16384) (about 0.6 GB at
+ * M = 8192, K = 2048), not as M x V.  The dX and dW GEMMs of each slice run
+ * on two helper streams forked from and joined back to `stream` (created on
+ * the first call; the call is CUDA-graph capturable once that first call
+ * has run outside the capture). */
 size_t coda_linear_cross_entropy_bwd_workspace_size(int64_t M, int64_t V, int64_t K);
 int coda_linear_cross_entropy_bwd(const coda_bf16* X, const coda_bf16* W, const int32_t* labels,
                                   int32_t ignore_index, const float* lse, const int32_t* n_valid,

@@ -152,13 +152,25 @@ def test_swiglu_mlp_fwd_bwd(coda, shape):
 
 
 # ---------------------------------------------------------------- linear + cross-entropy (scaled)
-@pytest.mark.parametrize("shape", [synth.CeShape(512, 256, 4000), synth.CeShape(300, 136, 8192)])
-def test_linear_cross_entropy(coda, shape):
-    t = synth.make_ce(shape, seed=0)
+# The backward takes the vocabulary in slices of 16384 columns: one slice up
+# to 16384, then several with a ragged last one; labels sit on both sides of
+# the slice boundaries.
+CE_SHAPES = [synth.CeShape(512, 256, 4000), synth.CeShape(300, 136, 8192), synth.CeShape(300, 136, 40008)]
+
+
+def _ce_labels(t, vocab):
     lab = t["labels"].clone()
     lab[1] = 0
-    lab[2] = shape.vocab - 1
+    lab[2] = vocab - 1
+    if vocab > 16384:
+        lab[3], lab[4], lab[5] = 16383, 16384, 32768 if vocab > 32768 else 16385
     t["labels"] = lab
+
+
+@pytest.mark.parametrize("shape", CE_SHAPES)
+def test_linear_cross_entropy(coda, shape):
+    t = synth.make_ce(shape, seed=0)
+    _ce_labels(t, shape.vocab)
     d, o = dev(t), f64(t)
     labels_np = t["labels"].numpy()
     out = coda.linear_cross_entropy(d["X"], d["W"], d["labels"])
@@ -237,13 +249,11 @@ def test_block_fwd_bwd(coda, shape, fold_weights):
 
 
 # ---------------------------------------------------------------- final RMSNorm -> LM head -> CE
-@pytest.mark.parametrize("shape", [synth.CeShape(512, 256, 4000), synth.CeShape(300, 136, 8200)])
+@pytest.mark.parametrize("shape", [synth.CeShape(512, 256, 4000), synth.CeShape(300, 136, 8200),
+                                   synth.CeShape(260, 128, 33000)])
 def test_rmsnorm_linear_cross_entropy(coda, shape):
     t = synth.make_ce(shape, seed=0)
-    lab = t["labels"].clone()
-    lab[1] = 0
-    lab[2] = shape.vocab - 1
-    t["labels"] = lab
+    _ce_labels(t, shape.vocab)
     t["gamma"] = synth.gain_f32(shape.hidden, 9)
     t["R"] = synth.randn_bf16((shape.tokens, shape.hidden), 1.0, 10)
     d, o = dev(t), f64(t)
