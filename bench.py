@@ -39,6 +39,9 @@ METRIC = "fused GEMM-epilogue TFLOP/s & % bf16 peak; block fwd+bwd ms vs unfused
 WORKLOAD = ("non-attention transformer block fwd+bwd: tokens 8192 (4x2048), hidden 8192, 64 q / 8 kv heads x 128, "
             "SwiGLU intermediate 28672; QKV+QK-RMSNorm+RoPE, O-proj+residual+partial RMS, gate/up+SwiGLU, "
             "down+residual epilogues and their backward")
+N_LEG = 50            # timed calls per leg (median reported)
+W_LEG = 10            # untimed calls before them
+FLUSH_BYTES = 256 << 20   # buffer written between timed calls of a leg (L2 flush)
 DOMINANT = "gateup"   # the step's largest single GEMM-epilogue launch (row-scale + SwiGLU epilogue)
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gateup_swiglu_gemm_block8192.md")
 
@@ -52,10 +55,10 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-unfused", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--no-ce", action="store_true",
-                   help="skip the side measurements (linear + cross-entropy, FP8 gate/up, MLP, RMSNorm-linear)")
-    p.add_argument("--legs", default="ce,fp8,nvfp4,mlp,rms",
-                   help="side measurements to run (comma list of ce, fp8, nvfp4, mlp, rms)")
+    p.add_argument("--legs", default="swiglu,rms,mlp,ce,fp8,nvfp4",
+                   help="other workloads to time after the block step (comma list of swiglu, rms, mlp, ce, fp8, "
+                        "nvfp4; empty for none)")
+    p.add_argument("--no-block", action="store_true", help="skip the block step (profiling of the other legs)")
     p.add_argument("--serial", action="store_true", help="run the step's calls on one stream")
     p.add_argument("--fold-weights", action="store_true",
                    help="fold the RMSNorm gains into the weights each step instead of applying them in the "
@@ -238,6 +241,65 @@ def oracle_sample_timing(tokens, p):
     return flops / dt / 1e12, dt, flops
 
 
+def oracle_workload_timings(tokens, block_sample):
+    """The fp64 oracle (as it stands) on every workload, on the host cores:
+    linear + SwiGLU (256 x 512 -> 1024) and the RMSNorm-linear fwd+bwd
+    (4096 x 2048 -> 2048) in full; the SwiGLU MLP, linear + cross-entropy and
+    the block on their first `tokens` tokens with full weights, the seconds
+    scaled to the full token count by FLOPs and labelled "extrapolated"."""
+    from oracle import coda_oracle as O
+    import synth
+
+    def f64(d):
+        return {k: (v.double().numpy() if v.dtype != torch_int32() else v.numpy()) for k, v in d.items()}
+
+    out = {}
+
+    def entry(name, secs, flops, how):
+        out[name] = {"seconds": round(secs, 3), "tflops": round(flops / secs / 1e12, 4), "how": how}
+
+    s1 = synth.FULL["swiglu"]
+    p = f64(synth.make_swiglu(s1, seed=0))
+    t0 = time.perf_counter()
+    O.swiglu_fwd(p["X"], p["Wg"], p["Wu"])
+    entry("swiglu", time.perf_counter() - t0, 2 * s1.tokens * s1.hidden * s1.inter * 2, "full")
+    s2 = synth.FULL["rmsnorm_linear"]
+    p = f64(synth.make_rms_linear(s2, seed=0))
+    t0 = time.perf_counter()
+    O.rmsnorm_linear_fwd(p["X"], p["gamma"], p["W"], s2.eps, p["R"])
+    O.rmsnorm_linear_bwd(p["X"], p["gamma"], p["W"], s2.eps, p["G"])
+    entry("rmsnorm_linear", time.perf_counter() - t0, 2 * s2.tokens * s2.hidden * s2.out * 3, "full")
+    s3 = synth.FULL["mlp"]
+    p = f64(synth.make_mlp(s3, seed=0))
+    sl = slice(0, tokens)
+    t0 = time.perf_counter()
+    O.mlp_fwd(p["X"][sl], p["Wg"], p["Wu"], p["Wd"], p["R"][sl])
+    O.mlp_bwd(p["X"][sl], p["Wg"], p["Wu"], p["Wd"], p["dY"][sl])
+    dt = time.perf_counter() - t0
+    full = O.mlp_flops(s3.tokens, s3.hidden, s3.inter)
+    entry("mlp_swiglu", dt * full / O.mlp_flops(tokens, s3.hidden, s3.inter), full,
+          f"extrapolated by FLOPs from the first {tokens} tokens ({dt:.2f} s)")
+    s4 = synth.FULL["linear_ce"]
+    p = f64(synth.make_ce(s4, seed=0))
+    t0 = time.perf_counter()
+    O.linear_cross_entropy_fwd(p["X"][sl], p["W"], p["labels"][sl])
+    O.linear_cross_entropy_bwd(p["X"][sl], p["W"], p["labels"][sl])
+    dt = time.perf_counter() - t0
+    full = O.ce_flops(s4.tokens, s4.hidden, s4.vocab)
+    entry("linear_cross_entropy", dt * full / O.ce_flops(tokens, s4.hidden, s4.vocab), full,
+          f"extrapolated by FLOPs from the first {tokens} tokens ({dt:.2f} s)")
+    _, bdt, bfl = block_sample
+    s5 = synth.FULL["block"]
+    full = O.block_flops(s5.tokens, s5.hidden, s5.qkv_out, s5.n_q * s5.head_dim, s5.inter)
+    entry("block", bdt * full / bfl, full, f"extrapolated by FLOPs from the first {tokens} tokens ({bdt:.2f} s)")
+    return out
+
+
+def torch_int32():
+    import torch
+    return torch.int32
+
+
 def cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -298,337 +360,245 @@ def main():
     s = dataclasses.replace(synth.FULL["block"], tokens=args.tokens)
     host = synth.make_block(s, seed=0)
     t = {k: v.to(dev) for k, v in host.items()}
-    blk = Block(s, t, device=dev, concurrent=not args.serial, fold_weights=args.fold_weights)
-    flops_step = sum(blk.gemm_flops().values())
-    launches_step = sum(blk.launches().values())
     stream = torch.cuda.current_stream(dev)
-    args_step = (t["x0"], t["A"], t["pos"], t["dx2"], t["dQ"], t["dK"], t["dV"])
-
-    # ---------------------------------------------------------------- device-resident timing
-    names = list(blk.launches())
-    for _ in range(args.warmup):
-        blk.step(*args_step)
-    torch.cuda.synchronize(dev)
-    st = coda.get_status(blk.ws)
-    if st != 0:
-        raise RuntimeError(f"device status after warm-up: {coda.status_string(st)}")
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
-    gpu_id = None
-    try:
-        gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
-        gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
-    except Exception:
-        gpu_id = None
-    clocks = ClockSampler(gpu_id)
-    torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.3)
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for i in range(args.steps):
-        ev = marks[i]
-        ev[0].record(stream)
-        j = [1]
-
-        def mark(name, ev=ev, j=j):
-            ev[j[0]].record(stream)
-            j[0] += 1
-        blk.step(*args_step, mark=mark)
-    stop.record(stream)
-    torch.cuda.synchronize(dev)
-    clk = clocks.stop()
-    ms_total = start.elapsed_time(stop)
-    ms_step = ms_total / args.steps
-    value = flops_step * args.steps / (ms_total / 1e3) / 1e12
-    stage_ms = {n: statistics.median(marks[i][k].elapsed_time(marks[i][k + 1]) for i in range(args.steps))
-                for k, n in enumerate(names)}
-    gf = blk.gemm_flops()
     burst, sustained, hbm, peak_src = measured_peaks()
-    stages = {n: {"ms": round(stage_ms[n], 4), "launches": blk.launches()[n],
-                  "tflops": round(gf[n] / (stage_ms[n] / 1e3) / 1e12, 1) if gf[n] else None} for n in names}
-    ach = gf[DOMINANT] / (stage_ms[DOMINANT] / 1e3) / 1e12
-    roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": sustained, "unit": "TFLOP/s",
-                "frac": round(ach / sustained, 4), "traffic": profiled_traffic(),
-                "kernel": "coda_gemm_kernel<256, EpiSwiglu> (gate/up GEMM, 8192x57344x8192)",
-                "peak_kind": f"bf16 sustained ({peak_src})"}
-    torch.cuda.synchronize(dev)
-    if coda.get_status(blk.ws) != 0:
-        raise RuntimeError("device status error in timed region")
+    def block_leg():
+        """The block step: device-resident timing (the headline), end to end
+        through pinned host buffers, and the eager-torch comparison."""
+        blk = Block(s, t, device=dev, concurrent=not args.serial, fold_weights=args.fold_weights)
+        flops_step = sum(blk.gemm_flops().values())
+        launches_step = sum(blk.launches().values())
+        args_step = (t["x0"], t["A"], t["pos"], t["dx2"], t["dQ"], t["dK"], t["dV"])
 
-    # ---------------------------------------------------------------- end to end through host buffers
-    # Every step copies its inputs (x0, A, positions, dx2, dQ, dK, dV) from
-    # pinned host memory and reads its results (x2, dx0) back, inside the timed
-    # region.  The copies are pipelined the way a training loop prefetches: the
-    # next step's inputs go host->device on their own stream into a second
-    # buffer set while the current step computes, and results come back on a
-    # third stream.  Events order every reuse: an input buffer is refilled only
-    # after the step that read it has finished, a step starts only when its
-    # inputs have landed, and x2 / dx0 are overwritten only after the previous
-    # step's copy-out.
-    e2e = None
-    if not args.no_e2e:
-        in_keys = ("x0", "A", "pos", "dx2", "dQ", "dK", "dV")
-        hin = {k: host[k].pin_memory() for k in in_keys}
-        hx2 = torch.empty_like(host["x0"]).pin_memory()
-        hdx0 = torch.empty_like(host["x0"]).pin_memory()
-        dbuf = [{k: torch.empty_like(t[k]) for k in in_keys} for _ in range(2)]
-        h2d = sum(v.numel() * v.element_size() for v in hin.values())
-        d2h = hx2.numel() * hx2.element_size() + hdx0.numel() * hdx0.element_size()
-        h2d_s = torch.cuda.Stream(device=dev)
-        d2h_s = torch.cuda.Stream(device=dev)
-        ev_in = [torch.cuda.Event(), torch.cuda.Event()]
-        ev_used = [torch.cuda.Event(), torch.cuda.Event()]
-        ev_x2, ev_x2_out, ev_dx0_out = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
-
-        def copy_in(bi, after=None):
-            with torch.cuda.stream(h2d_s):
-                if after is not None:
-                    h2d_s.wait_event(after)
-                for k in in_keys:
-                    dbuf[bi][k].copy_(hin[k], non_blocking=True)
-                ev_in[bi].record(h2d_s)
-
-        def e2e_run(nsteps, start_ev=None):
-            if start_ev is not None:
-                h2d_s.wait_event(start_ev)
-            copy_in(0)
-            for i in range(nsteps):
-                bi = i % 2
-                if i + 1 < nsteps:
-                    copy_in(1 - bi, ev_used[1 - bi] if i >= 1 else None)
-                stream.wait_event(ev_in[bi])
-                if i >= 1:
-                    stream.wait_event(ev_x2_out)
-                d = dbuf[bi]
-                f = blk.forward(d["x0"], d["A"], d["pos"])
-                ev_x2.record(stream)
-                with torch.cuda.stream(d2h_s):
-                    d2h_s.wait_event(ev_x2)
-                    hx2.copy_(f["x2"], non_blocking=True)
-                    ev_x2_out.record(d2h_s)
-                if i >= 1:
-                    stream.wait_event(ev_dx0_out)
-                g = blk.backward(d["x0"], d["A"], d["pos"], d["dx2"], d["dQ"], d["dK"], d["dV"])
-                ev_used[bi].record(stream)
-                with torch.cuda.stream(d2h_s):
-                    d2h_s.wait_event(ev_used[bi])
-                    hdx0.copy_(g["dx0"], non_blocking=True)
-                    ev_dx0_out.record(d2h_s)
-            stream.wait_stream(h2d_s)
-            stream.wait_stream(d2h_s)
-
-        e2e_run(max(2, args.warmup // 2))
+        # ---------------------------------------------------------------- device-resident timing
+        names = list(blk.launches())
+        for _ in range(args.warmup):
+            blk.step(*args_step)
         torch.cuda.synchronize(dev)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_run(args.steps, a)
-        b.record(stream)
+        st = coda.get_status(blk.ws)
+        if st != 0:
+            raise RuntimeError(f"device status after warm-up: {coda.status_string(st)}")
+        marks = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
+        gpu_id = None
+        try:
+            gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
+            gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
+        except Exception:
+            gpu_id = None
+        clocks = ClockSampler(gpu_id)
         torch.cuda.synchronize(dev)
-        ms_e2e = a.elapsed_time(b)
-        if not (torch.equal(hx2, blk.x2.cpu()) and torch.equal(hdx0, blk.grads_qkv["dX"].cpu())):
-            raise RuntimeError("e2e results read back do not match the device buffers")
-        e2e = {"value": round(flops_step * args.steps / (ms_e2e / 1e3) / 1e12, 2), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e / args.steps, 3),
-               "copies": "pinned host buffers; next step's inputs prefetched on a copy stream, results read back "
-                         "on another"}
+        clocks.start()
+        time.sleep(0.3)
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            ev = marks[i]
+            ev[0].record(stream)
+            j = [1]
 
-    # ---------------------------------------------------------------- unfused torch comparison
-    unfused_ms = None
-    if not args.no_unfused:
-        del blk
-        torch.cuda.empty_cache()
-        step = unfused_step_fn(t, t, s)
-        for _ in range(2):
-            step()
+            def mark(name, ev=ev, j=j):
+                ev[j[0]].record(stream)
+                j[0] += 1
+            blk.step(*args_step, mark=mark)
+        stop.record(stream)
         torch.cuda.synchronize(dev)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        n_unf = max(3, args.steps // 3)
-        a.record(stream)
-        for _ in range(n_unf):
-            step()
-        b.record(stream)
+        clk = clocks.stop()
+        ms_total = start.elapsed_time(stop)
+        ms_step = ms_total / args.steps
+        value = flops_step * args.steps / (ms_total / 1e3) / 1e12
+        median_step = statistics.median(marks[i][0].elapsed_time(marks[i][-1]) for i in range(args.steps))
+        stage_ms = {n: statistics.median(marks[i][k].elapsed_time(marks[i][k + 1]) for i in range(args.steps))
+                    for k, n in enumerate(names)}
+        gf = blk.gemm_flops()
+        stages = {n: {"ms": round(stage_ms[n], 4), "launches": blk.launches()[n],
+                      "tflops": round(gf[n] / (stage_ms[n] / 1e3) / 1e12, 1) if gf[n] else None} for n in names}
+        ach = gf[DOMINANT] / (stage_ms[DOMINANT] / 1e3) / 1e12
+        # the step lasts about 25 ms and the timed region about a second, so
+        # the kernel is held to the burst peak (the sustained figure is a
+        # seconds-long loop under the power cap)
+        roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": burst, "unit": "TFLOP/s",
+                    "frac": round(ach / burst, 4), "traffic": profiled_traffic(),
+                    "kernel": "coda_gemm_kernel<256, EpiSwiglu> (gate/up GEMM, 8192x57344x8192)",
+                    "peak_kind": f"bf16 burst ({peak_src})"}
         torch.cuda.synchronize(dev)
-        unfused_ms = a.elapsed_time(b) / n_unf
+        if coda.get_status(blk.ws) != 0:
+            raise RuntimeError("device status error in timed region")
 
-    # ---------------------------------------------------------------- linear + CE (rows a8, a12)
-    # Not part of the block step: the 8192 x 2048 x 128256 linear + cross-entropy
-    # workload, forward and backward, timed the same way and reported beside it.
+        # ---------------------------------------------------------------- end to end through host buffers
+        # Every step copies its inputs (x0, A, positions, dx2, dQ, dK, dV) from
+        # pinned host memory and reads its results (x2, dx0) back, inside the timed
+        # region.  The copies are pipelined the way a training loop prefetches: the
+        # next step's inputs go host->device on their own stream into a second
+        # buffer set while the current step computes, and results come back on a
+        # third stream.  Events order every reuse: an input buffer is refilled only
+        # after the step that read it has finished, a step starts only when its
+        # inputs have landed, and x2 / dx0 are overwritten only after the previous
+        # step's copy-out.
+        e2e = None
+        if not args.no_e2e:
+            in_keys = ("x0", "A", "pos", "dx2", "dQ", "dK", "dV")
+            hin = {k: host[k].pin_memory() for k in in_keys}
+            hx2 = torch.empty_like(host["x0"]).pin_memory()
+            hdx0 = torch.empty_like(host["x0"]).pin_memory()
+            dbuf = [{k: torch.empty_like(t[k]) for k in in_keys} for _ in range(2)]
+            h2d = sum(v.numel() * v.element_size() for v in hin.values())
+            d2h = hx2.numel() * hx2.element_size() + hdx0.numel() * hdx0.element_size()
+            h2d_s = torch.cuda.Stream(device=dev)
+            d2h_s = torch.cuda.Stream(device=dev)
+            ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+            ev_used = [torch.cuda.Event(), torch.cuda.Event()]
+            ev_x2, ev_x2_out, ev_dx0_out = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+
+            def copy_in(bi, after=None):
+                with torch.cuda.stream(h2d_s):
+                    if after is not None:
+                        h2d_s.wait_event(after)
+                    for k in in_keys:
+                        dbuf[bi][k].copy_(hin[k], non_blocking=True)
+                    ev_in[bi].record(h2d_s)
+
+            def e2e_run(nsteps, start_ev=None):
+                if start_ev is not None:
+                    h2d_s.wait_event(start_ev)
+                copy_in(0)
+                for i in range(nsteps):
+                    bi = i % 2
+                    if i + 1 < nsteps:
+                        copy_in(1 - bi, ev_used[1 - bi] if i >= 1 else None)
+                    stream.wait_event(ev_in[bi])
+                    if i >= 1:
+                        stream.wait_event(ev_x2_out)
+                    d = dbuf[bi]
+                    f = blk.forward(d["x0"], d["A"], d["pos"])
+                    ev_x2.record(stream)
+                    with torch.cuda.stream(d2h_s):
+                        d2h_s.wait_event(ev_x2)
+                        hx2.copy_(f["x2"], non_blocking=True)
+                        ev_x2_out.record(d2h_s)
+                    if i >= 1:
+                        stream.wait_event(ev_dx0_out)
+                    g = blk.backward(d["x0"], d["A"], d["pos"], d["dx2"], d["dQ"], d["dK"], d["dV"])
+                    ev_used[bi].record(stream)
+                    with torch.cuda.stream(d2h_s):
+                        d2h_s.wait_event(ev_used[bi])
+                        hdx0.copy_(g["dx0"], non_blocking=True)
+                        ev_dx0_out.record(d2h_s)
+                stream.wait_stream(h2d_s)
+                stream.wait_stream(d2h_s)
+
+            e2e_run(max(2, args.warmup // 2))
+            torch.cuda.synchronize(dev)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_run(args.steps, a)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ms_e2e = a.elapsed_time(b)
+            if not (torch.equal(hx2, blk.x2.cpu()) and torch.equal(hdx0, blk.grads_qkv["dX"].cpu())):
+                raise RuntimeError("e2e results read back do not match the device buffers")
+            e2e = {"value": round(flops_step * args.steps / (ms_e2e / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e / args.steps, 3),
+                   "copies": "pinned host buffers; next step's inputs prefetched on a copy stream, results read back "
+                             "on another"}
+
+        # ---------------------------------------------------------------- unfused torch comparison
+        unfused_ms = None
+        if not args.no_unfused:
+            del blk
+            torch.cuda.empty_cache()
+            step = unfused_step_fn(t, t, s)
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize(dev)
+            n_unf = max(N_LEG, args.steps)
+            ue = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_unf)]
+            for e in ue:
+                e[0].record(stream)
+                step()
+                e[1].record(stream)
+            torch.cuda.synchronize(dev)
+            unfused_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ue)
+        return dict(value=value, ms_step=ms_step, median_step=median_step, flops_step=flops_step,
+                    launches_step=launches_step, roofline=roofline, e2e=e2e, clk=clk, unfused_ms=unfused_ms,
+                    stages=stages)
+
+    blk_res = None if args.no_block else block_leg()
+
+    # ---------------------------------------------------------------- the other workloads
+    # One leg per other workload, each timed the same way: 10 untimed
+    # calls, then N_LEG calls, each between two CUDA events on the launching
+    # stream with a 256 MB buffer written before it (an L2 flush, outside
+    # the events); the median is reported.  Rates are 2*M*N*K per GEMM
+    # against the measured bf16 burst peak (each call is timed alone).  The
+    # eager-torch comparison of a leg runs the same workload as cuBLAS
+    # matmuls plus unfused element-wise ops with an autograd backward, timed
+    # the same way.
     other = {}
     legs = set(args.legs.split(","))
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
-    def time_calls(fn, n=5, warm=2):
+    def median_ms(fn, n=N_LEG, warm=W_LEG, parts=1):
+        """Median over n calls of fn's device time (parts > 1: fn(mark) marks
+        part boundaries, and the medians of every part are returned)."""
         for _ in range(warm):
-            fn()
+            fn(lambda: None) if parts > 1 else fn()
         torch.cuda.synchronize(dev)
-        ev[0].record(stream)
-        for _ in range(n):
-            fn()
-        ev[1].record(stream)
-        torch.cuda.synchronize(dev)
-        return ev[0].elapsed_time(ev[1]) / n
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(parts + 1)] for _ in range(n)]
+        for k in range(n):
+            flush_buf.zero_()
+            e = evs[k]
+            e[0].record(stream)
+            if parts > 1:
+                pos = [1]
 
-    def unfused_leg(entry, fn, ours_ms, n=3):
-        """Time the same workload as eager torch (cuBLAS matmuls, unfused
-        element-wise ops, autograd backward) and add it to the leg's entry."""
+                def mark(e=e, pos=pos):
+                    e[pos[0]].record(stream)
+                    pos[0] += 1
+                fn(mark)
+            else:
+                fn()
+            e[parts].record(stream)
+        torch.cuda.synchronize(dev)
+        med = [statistics.median(e[p].elapsed_time(e[p + 1]) for e in evs) for p in range(parts)]
+        return med if parts > 1 else med[0]
+
+    def rate(flops, ms):
+        return round(flops / (ms / 1e3) / 1e12, 1)
+
+    def unfused_leg(entry, fn, ours_ms):
         if args.no_unfused:
             return
-        ms = time_calls(fn, n=n, warm=1)
-        entry["unfused_ms"] = round(ms, 3)
+        ms = median_ms(fn)
+        entry["unfused_ms"] = round(ms, 4)
         entry["speedup_vs_unfused"] = round(ms / ours_ms, 3)
 
-    if not args.no_ce and "ce" in legs:
-        from gemm_epilogue_transformer_bf16_gb300.block import LinearCE
-        cs_ = synth.FULL["linear_ce"]
-        hc = synth.make_ce(cs_, seed=0)
-        dc = {k: v.to(dev) for k, v in hc.items()}
-        ce = LinearCE(cs_.tokens, cs_.vocab, cs_.hidden, device=dev)
-        for _ in range(2):
-            ce.step(dc["X"], dc["W"], dc["labels"])
-        torch.cuda.synchronize(dev)
-        n_ce = 3
-        fw, bw = [], []
-        for _ in range(n_ce):
-            ev[0].record(stream)
-            coda.linear_cross_entropy(dc["X"], dc["W"], dc["labels"], out=ce.out, ws=ce.ws)
-            ev[1].record(stream)
-            coda.linear_cross_entropy_bwd(dc["X"], dc["W"], dc["labels"], ce.out["lse"], ce.out["n_valid"], 1.0,
-                                          out=ce.grads, ws=ce.ws)
-            ev[2].record(stream)
-            torch.cuda.synchronize(dev)
-            fw.append(ev[0].elapsed_time(ev[1]))
-            bw.append(ev[1].elapsed_time(ev[2]))
-        if coda.get_status(ce.ws) != 0:
-            raise RuntimeError("device status error in the linear-CE measurement")
-        # 2*M*N*K: the logits GEMM forward; the backward recomputes them, then dX and dW
-        f_fwd = 2 * cs_.tokens * cs_.hidden * cs_.vocab
-        f_all = 4 * f_fwd
-        mf, mb = statistics.median(fw), statistics.median(bw)
-        other["linear_cross_entropy"] = {
-            "workload": "tokens 8192, hidden 2048, vocab 128256, 5% ignored labels; fwd (online LSE epilogue + "
-                        "combine) and bwd (softmax-minus-onehot epilogue, dX, dW)",
-            "fwd_ms": round(mf, 3), "bwd_ms": round(mb, 3),
-            "fwd_tflops": round(f_fwd / (mf / 1e3) / 1e12, 1),
-            "fwd_bwd_tflops": round(f_all / ((mf + mb) / 1e3) / 1e12, 1)}
-        del ce
-        Xr = dc["X"].detach().requires_grad_(True)
-        Wr = dc["W"].detach().requires_grad_(True)
-        lab_long = dc["labels"].long()
+    if "swiglu" in legs:
+        # linear + SwiGLU forward, 256 x 512 -> 1024 (launch-latency bound)
+        s1 = synth.FULL["swiglu"]
+        d1 = {k: v.to(dev) for k, v in synth.make_swiglu(s1, seed=0).items()}
+        ws1 = coda.workspace(256, dev)
+        H1 = torch.empty(s1.tokens, s1.inter, dtype=torch.bfloat16, device=dev)
+        m1 = median_ms(lambda: coda.linear_swiglu(d1["X"], d1["Wg"], d1["Wu"], H=H1, g=None, u=None, ws=ws1,
+                                                  save=False))
+        f1 = 2 * s1.tokens * s1.hidden * s1.inter * 2
+        other["swiglu"] = {"workload": f"linear + SwiGLU forward, {s1.tokens} x {s1.hidden} -> {s1.inter} "
+                                       f"(launch-latency bound)",
+                           "ms": round(m1, 4), "tflops": rate(f1, m1), "frac_of_burst": round(rate(f1, m1) / burst, 4)}
 
-        def ce_unfused():
-            # bf16 logits from cuBLAS (2.1 GB, they fit), fp32 cross-entropy, autograd backward
-            z = Xr @ Wr.t()
-            torch.nn.functional.cross_entropy(z.float(), lab_long, ignore_index=cs_.ignore_index).backward()
-            Xr.grad = None
-            Wr.grad = None
-        unfused_leg(other["linear_cross_entropy"], ce_unfused, mf + mb)
-        del dc, Xr, Wr
+        def swiglu_unfused():
+            torch.nn.functional.silu(d1["X"] @ d1["Wg"].t()) * (d1["X"] @ d1["Wu"].t())
+        unfused_leg(other["swiglu"], swiglu_unfused, m1)
+        del d1
 
-    if not args.no_ce and ("fp8" in legs or "nvfp4" in legs):
-        T_, H_, I_ = s.tokens, s.hidden, s.inter
-        r_ = coda.rms_rstd(t["x0"], s.eps)
-        Hq = torch.empty(T_, I_, dtype=torch.bfloat16, device=dev)
-        gq8, uq8 = torch.empty_like(Hq), torch.empty_like(Hq)
-        ws8 = coda.workspace(256, dev)
-    if not args.no_ce and "fp8" in legs:
-        # FP8 (e4m3) gate/up + SwiGLU at the block's shape (NEXT row: the same
-        # mainloop with kind::f8f6f4), beside the bf16 launch timed above.
-        xq, sx = coda.quantize_fp8_rows(t["x0"])
-        gq, sg = coda.quantize_fp8_rows(t["Wg"])
-        uq, su = coda.quantize_fp8_rows(t["Wu"])
-        f8 = []
-        for i in range(5):
-            ev[0].record(stream)
-            coda.linear_swiglu_fp8(xq, sx, gq, sg, uq, su, rstd=r_, H=Hq, g=gq8, u=uq8, ws=ws8)
-            ev[1].record(stream)
-            torch.cuda.synchronize(dev)
-            if i >= 2:
-                f8.append(ev[0].elapsed_time(ev[1]))
-        if coda.get_status(ws8) != 0:
-            raise RuntimeError("device status error in the FP8 measurement")
-        m8 = statistics.median(f8)
-        fp8_peak = 2 * burst
-        other["fp8_gateup_swiglu"] = {
-            "workload": f"e4m3 gate/up GEMM with row-scale + SwiGLU epilogue, {T_} x 2x{I_} x {H_}, per-row scales",
-            "ms": round(m8, 3), "tflops": round(gf[DOMINANT] / (m8 / 1e3) / 1e12, 1),
-            "peak": round(fp8_peak, 1), "peak_kind": f"fp8 = 2 x bf16 burst ({peak_src}, nominal ratio)",
-            "frac": round(gf[DOMINANT] / (m8 / 1e3) / 1e12 / fp8_peak, 4)}
-        del xq, gq, uq
-    if not args.no_ce and "nvfp4" in legs:
-        # NVFP4 (e2m1 + e4m3 block scales) gate/up + SwiGLU at the same shape:
-        # the block-scaled kind::mxf4nvf4 mainloop, single CTAs.
-        fq = []
-        xq4, sfx4, sx4 = coda.quantize_nvfp4_rows(t["x0"])
-        gq4, sfg4, sg4 = coda.quantize_nvfp4_rows(t["Wg"])
-        uq4, sfu4, su4 = coda.quantize_nvfp4_rows(t["Wu"])
-        for i in range(5):
-            ev[0].record(stream)
-            coda.quantize_nvfp4_rows(t["x0"])
-            ev[1].record(stream)
-            coda.linear_swiglu_nvfp4(xq4, sfx4, sx4, gq4, sfg4, sg4, uq4, sfu4, su4, rstd=r_, H=Hq, g=gq8, u=uq8,
-                                     ws=ws8)
-            ev[2].record(stream)
-            torch.cuda.synchronize(dev)
-            if i >= 2:
-                fq.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
-        if coda.get_status(ws8) != 0:
-            raise RuntimeError("device status error in the NVFP4 measurement")
-        mq4 = statistics.median(q for q, _ in fq)
-        m4 = statistics.median(g for _, g in fq)
-        fp4_peak = 6 * burst
-        other["nvfp4_gateup_swiglu"] = {
-            "workload": f"NVFP4 gate/up GEMM (e2m1, e4m3 scale per 16, fp32 row scale) with row-scale + SwiGLU "
-                        f"epilogue, {T_} x 2x{I_} x {H_}, single-CTA tiles",
-            "ms": round(m4, 3), "tflops": round(gf[DOMINANT] / (m4 / 1e3) / 1e12, 1),
-            "peak": round(fp4_peak, 1), "peak_kind": f"fp4 = 6 x bf16 burst ({peak_src}, nominal ratio)",
-            "frac": round(gf[DOMINANT] / (m4 / 1e3) / 1e12 / fp4_peak, 4),
-            "quantize_x_ms": round(mq4, 3)}
-        del xq4, gq4, uq4, sfx4, sfg4, sfu4
-    if not args.no_ce and ("fp8" in legs or "nvfp4" in legs):
-        del Hq, gq8, uq8
-
-    # Two more workloads (also parity workloads), forward + backward, timed the
-    # same way: the SwiGLU MLP at hidden 4096 and the RMSNorm-reparameterised
-    # projection + residual at 4096 x 2048 (gain folded into W: the standalone
-    # operator's form).  FLOPs 2*M*N*K per GEMM.
-    if not args.no_ce and "mlp" in legs:
-        s3 = synth.FULL["mlp"]
-        d3 = {k: v.to(dev) for k, v in synth.make_mlp(s3, seed=0).items()}
-        ws3 = coda.workspace(max(coda.load().coda_linear_swiglu_bwd_workspace_size(s3.tokens, s3.inter, s3.hidden),
-                                 coda.load().coda_linear_residual_workspace_size(s3.tokens, s3.hidden, s3.inter)), dev)
-        o3 = {}
-        side3 = torch.cuda.Stream(device=dev)
-
-        def mlp_step():
-            H3, g3, u3 = coda.linear_swiglu(d3["X"], d3["Wg"], d3["Wu"], ws=ws3)
-            coda.linear_residual(H3, d3["Wd"], d3["R"], ws=ws3)
-            o3["g"] = coda.linear_swiglu_bwd(d3["dY"], d3["X"], d3["Wg"], d3["Wu"], d3["Wd"], g3, u3, H3, ws=ws3,
-                                             side_stream=side3)
-        m3 = time_calls(mlp_step)
-        f3 = 2 * s3.tokens * s3.hidden * s3.inter * 3 * 3       # fwd 3 GEMMs, bwd 6
-        other["mlp_swiglu"] = {
-            "workload": f"SwiGLU MLP fwd+bwd, tokens {s3.tokens}, hidden {s3.hidden}, intermediate {s3.inter}",
-            "ms": round(m3, 3), "tflops": round(f3 / (m3 / 1e3) / 1e12, 1),
-            "frac_of_sustained": round(f3 / (m3 / 1e3) / 1e12 / sustained, 4)}
-        del o3, ws3
-        p3 = {k: d3[k].detach().requires_grad_(True) for k in ("X", "Wg", "Wu", "Wd")}
-
-        def mlp_unfused():
-            p = p3
-            H = torch.nn.functional.silu(p["X"] @ p["Wg"].t()) * (p["X"] @ p["Wu"].t())
-            (d3["R"] + H @ p["Wd"].t()).backward(d3["dY"])
-            for v in p.values():
-                v.grad = None
-        unfused_leg(other["mlp_swiglu"], mlp_unfused, m3)
-        del d3, p3
-    if not args.no_ce and "rms" in legs:
+    if "rms" in legs:
+        # RMSNorm-reparameterised projection + residual, 4096 x 2048 -> 2048,
+        # forward and backward (gain fold, row RMS, prepass and combines
+        # included); outputs and workspaces held across calls as a training
+        # loop holds them; dW on a second stream beside c -> dX
         s2 = synth.FULL["rmsnorm_linear"]
         d2 = {k: v.to(dev) for k, v in synth.make_rms_linear(s2, seed=0).items()}
-        # outputs and workspaces allocated once, as a training loop holds them;
-        # dW on a second stream beside c -> dX
         M2, N2, K2 = s2.tokens, s2.out, s2.hidden
         lib = coda.load()
         Wf2 = torch.empty_like(d2["W"])
@@ -645,7 +615,7 @@ def main():
             coda.rmsnorm_linear(d2["X"], Wf2, d2["R"], eps=s2.eps, rstd_out=r2, Y=Y2, ws=ws2a)
             coda.rmsnorm_linear_bwd(d2["G"], d2["X"], d2["W"], d2["gamma"], r2, Y2, d2["R"], ws=ws2b, out=g2,
                                     side_stream=side2)
-        m2 = time_calls(rms_step, n=20, warm=3)
+        m2 = median_ms(rms_step)
         # the same calls captured once into a CUDA graph (on a capture stream
         # that has run them once outside the capture) and replayed
         cap2 = torch.cuda.Stream(device=dev)
@@ -656,16 +626,16 @@ def main():
         graph2 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph2, stream=cap2):
             rms_step()
-        mg2 = time_calls(graph2.replay, n=20, warm=3)
+        mg2 = median_ms(graph2.replay)
         if coda.get_status(ws2a) != 0 or coda.get_status(ws2b) != 0:
             raise RuntimeError("device status error in the RMSNorm-linear measurement")
         f2 = 2 * s2.tokens * s2.hidden * s2.out * 3               # fwd 1 GEMM, bwd 2
         other["rmsnorm_linear"] = {
             "workload": f"RMSNorm-reparameterised projection + residual fwd+bwd, tokens {s2.tokens}, "
                         f"hidden {s2.hidden}, out {s2.out} (gain fold, row RMS, prepass and combines included)",
-            "ms": round(m2, 3), "tflops": round(f2 / (m2 / 1e3) / 1e12, 1),
-            "frac_of_sustained": round(f2 / (m2 / 1e3) / 1e12 / sustained, 4),
-            "graph_ms": round(mg2, 3), "graph_tflops": round(f2 / (mg2 / 1e3) / 1e12, 1)}
+            "ms": round(m2, 4), "tflops": rate(f2, m2), "frac_of_burst": round(rate(f2, m2) / burst, 4),
+            "graph_ms": round(mg2, 4), "graph_tflops": rate(f2, mg2),
+            "graph_frac_of_burst": round(rate(f2, mg2) / burst, 4)}
         del graph2
         p2 = {"X": d2["X"].detach().requires_grad_(True), "W": d2["W"].detach().requires_grad_(True),
               "gamma": d2["gamma"].detach().requires_grad_(True)}
@@ -677,8 +647,128 @@ def main():
             (d2["R"] + xn @ p["W"].t()).backward(d2["G"])
             for v in p.values():
                 v.grad = None
-        unfused_leg(other["rmsnorm_linear"], rms_unfused, m2, n=20)
+        unfused_leg(other["rmsnorm_linear"], rms_unfused, m2)
         del d2, p2
+
+    if "mlp" in legs:
+        # SwiGLU MLP fwd+bwd at hidden 4096 (weight gradients on a side stream)
+        s3 = synth.FULL["mlp"]
+        d3 = {k: v.to(dev) for k, v in synth.make_mlp(s3, seed=0).items()}
+        ws3 = coda.workspace(max(coda.load().coda_linear_swiglu_bwd_workspace_size(s3.tokens, s3.inter, s3.hidden),
+                                 coda.load().coda_linear_residual_workspace_size(s3.tokens, s3.hidden, s3.inter)), dev)
+        side3 = torch.cuda.Stream(device=dev)
+        o3 = {"H": torch.empty(s3.tokens, s3.inter, dtype=torch.bfloat16, device=dev)}
+        o3["g"], o3["u"] = torch.empty_like(o3["H"]), torch.empty_like(o3["H"])
+        o3["Y"] = torch.empty_like(d3["R"])
+        o3["grads"] = {"dX": torch.empty_like(d3["X"]), "dWg": torch.empty_like(d3["Wg"]),
+                       "dWu": torch.empty_like(d3["Wu"]), "dWd": torch.empty_like(d3["Wd"])}
+
+        def mlp_step():
+            coda.linear_swiglu(d3["X"], d3["Wg"], d3["Wu"], H=o3["H"], g=o3["g"], u=o3["u"], ws=ws3)
+            coda.linear_residual(o3["H"], d3["Wd"], d3["R"], Y=o3["Y"], ws=ws3)
+            coda.linear_swiglu_bwd(d3["dY"], d3["X"], d3["Wg"], d3["Wu"], d3["Wd"], o3["g"], o3["u"], o3["H"],
+                                   ws=ws3, out=o3["grads"], side_stream=side3)
+        m3 = median_ms(mlp_step)
+        f3 = 2 * s3.tokens * s3.hidden * s3.inter * 3 * 3       # fwd 3 GEMMs, bwd 6
+        other["mlp_swiglu"] = {
+            "workload": f"SwiGLU MLP fwd+bwd, tokens {s3.tokens}, hidden {s3.hidden}, intermediate {s3.inter}",
+            "ms": round(m3, 4), "tflops": rate(f3, m3), "frac_of_burst": round(rate(f3, m3) / burst, 4)}
+        p3 = {k: d3[k].detach().requires_grad_(True) for k in ("X", "Wg", "Wu", "Wd")}
+
+        def mlp_unfused():
+            p = p3
+            H = torch.nn.functional.silu(p["X"] @ p["Wg"].t()) * (p["X"] @ p["Wu"].t())
+            (d3["R"] + H @ p["Wd"].t()).backward(d3["dY"])
+            for v in p.values():
+                v.grad = None
+        unfused_leg(other["mlp_swiglu"], mlp_unfused, m3)
+        del d3, p3, o3, ws3
+
+    if "ce" in legs:
+        # linear + cross-entropy, 8192 x 2048, vocabulary 128256: forward
+        # (online LSE epilogue + combine) and backward (vocabulary slices)
+        from gemm_epilogue_transformer_bf16_gb300.block import LinearCE
+        cs_ = synth.FULL["linear_ce"]
+        dc = {k: v.to(dev) for k, v in synth.make_ce(cs_, seed=0).items()}
+        ce = LinearCE(cs_.tokens, cs_.vocab, cs_.hidden, device=dev)
+
+        def ce_step(mark):
+            coda.linear_cross_entropy(dc["X"], dc["W"], dc["labels"], out=ce.out, ws=ce.ws)
+            mark()
+            coda.linear_cross_entropy_bwd(dc["X"], dc["W"], dc["labels"], ce.out["lse"], ce.out["n_valid"], 1.0,
+                                          out=ce.grads, ws=ce.ws)
+        mf, mb = median_ms(ce_step, parts=2)
+        if coda.get_status(ce.ws) != 0:
+            raise RuntimeError("device status error in the linear-CE measurement")
+        f_fwd = 2 * cs_.tokens * cs_.hidden * cs_.vocab
+        f_all = 4 * f_fwd        # the backward recomputes the logits, then dX and dW
+        other["linear_cross_entropy"] = {
+            "workload": "tokens 8192, hidden 2048, vocab 128256, 5% ignored labels; fwd (online LSE epilogue + "
+                        "combine) and bwd (softmax-minus-onehot epilogue, dX, dW, by vocabulary slices of 16384)",
+            "fwd_ms": round(mf, 4), "bwd_ms": round(mb, 4), "ms": round(mf + mb, 4),
+            "fwd_tflops": rate(f_fwd, mf), "bwd_tflops": rate(3 * f_fwd, mb), "tflops": rate(f_all, mf + mb),
+            "frac_of_burst": round(rate(f_all, mf + mb) / burst, 4),
+            "bwd_workspace_bytes": coda.load().coda_linear_cross_entropy_bwd_workspace_size(cs_.tokens, cs_.vocab,
+                                                                                           cs_.hidden)}
+        del ce
+        Xr = dc["X"].detach().requires_grad_(True)
+        Wr = dc["W"].detach().requires_grad_(True)
+        lab_long = dc["labels"].long()
+
+        def ce_unfused():
+            # bf16 logits from cuBLAS (2.1 GB, they fit), fp32 cross-entropy, autograd backward
+            z = Xr @ Wr.t()
+            torch.nn.functional.cross_entropy(z.float(), lab_long, ignore_index=cs_.ignore_index).backward()
+            Xr.grad = None
+            Wr.grad = None
+        unfused_leg(other["linear_cross_entropy"], ce_unfused, mf + mb)
+        del dc, Xr, Wr
+
+    if "fp8" in legs or "nvfp4" in legs:
+        T_, H_, I_ = s.tokens, s.hidden, s.inter
+        x0_ = {k: t[k] for k in ("x0", "Wg", "Wu")}
+        r_ = coda.rms_rstd(x0_["x0"], s.eps)
+        Hq = torch.empty(T_, I_, dtype=torch.bfloat16, device=dev)
+        gq8, uq8 = torch.empty_like(Hq), torch.empty_like(Hq)
+        ws8 = coda.workspace(256, dev)
+        f_gu = 2 * T_ * H_ * 2 * I_
+    if "fp8" in legs:
+        # e4m3 gate/up + SwiGLU at the block's shape (the same mainloop with
+        # kind::f8f6f4), beside the bf16 launch timed in the block step
+        xq, sx = coda.quantize_fp8_rows(x0_["x0"])
+        gq, sg = coda.quantize_fp8_rows(x0_["Wg"])
+        uq, su = coda.quantize_fp8_rows(x0_["Wu"])
+        m8 = median_ms(lambda: coda.linear_swiglu_fp8(xq, sx, gq, sg, uq, su, rstd=r_, H=Hq, g=gq8, u=uq8, ws=ws8))
+        if coda.get_status(ws8) != 0:
+            raise RuntimeError("device status error in the FP8 measurement")
+        fp8_peak = 2 * burst
+        other["fp8_gateup_swiglu"] = {
+            "workload": f"e4m3 gate/up GEMM with row-scale + SwiGLU epilogue, {T_} x 2x{I_} x {H_}, per-row scales",
+            "ms": round(m8, 4), "tflops": rate(f_gu, m8),
+            "peak": round(fp8_peak, 1), "peak_kind": f"fp8 = 2 x bf16 burst ({peak_src}, nominal ratio)",
+            "frac": round(rate(f_gu, m8) / fp8_peak, 4)}
+        del xq, gq, uq
+    if "nvfp4" in legs:
+        # NVFP4 (e2m1 + e4m3 block scales) gate/up + SwiGLU at the same shape:
+        # the block-scaled kind::mxf4nvf4 mainloop, single CTAs
+        xq4, sfx4, sx4 = coda.quantize_nvfp4_rows(x0_["x0"])
+        gq4, sfg4, sg4 = coda.quantize_nvfp4_rows(x0_["Wg"])
+        uq4, sfu4, su4 = coda.quantize_nvfp4_rows(x0_["Wu"])
+        mq4 = median_ms(lambda: coda.quantize_nvfp4_rows(x0_["x0"]))
+        m4 = median_ms(lambda: coda.linear_swiglu_nvfp4(xq4, sfx4, sx4, gq4, sfg4, sg4, uq4, sfu4, su4, rstd=r_,
+                                                        H=Hq, g=gq8, u=uq8, ws=ws8))
+        if coda.get_status(ws8) != 0:
+            raise RuntimeError("device status error in the NVFP4 measurement")
+        fp4_peak = 6 * burst
+        other["nvfp4_gateup_swiglu"] = {
+            "workload": f"NVFP4 gate/up GEMM (e2m1, e4m3 scale per 16, fp32 row scale) with row-scale + SwiGLU "
+                        f"epilogue, {T_} x 2x{I_} x {H_}, single-CTA tiles",
+            "ms": round(m4, 4), "tflops": rate(f_gu, m4),
+            "peak": round(fp4_peak, 1), "peak_kind": f"fp4 = 6 x bf16 burst ({peak_src}, nominal ratio)",
+            "frac": round(rate(f_gu, m4) / fp4_peak, 4), "quantize_x_ms": round(mq4, 4)}
+        del xq4, gq4, uq4, sfx4, sfg4, sfu4
+    if "fp8" in legs or "nvfp4" in legs:
+        del Hq, gq8, uq8, x0_
 
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None
@@ -687,33 +777,38 @@ def main():
         v, dt, fl = oracle_sample_timing(args.cpu_tokens, oracle_inputs(host, args.cpu_tokens))
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
                "sample": f"fp64 NumPy block_fwd+block_bwd on the first {args.cpu_tokens} of 8192 tokens "
-                         f"(full weights): {fl / 1e12:.3f} TFLOP in {dt:.1f} s"}
+                         f"(full weights): {fl / 1e12:.3f} TFLOP in {dt:.1f} s",
+               "per_workload": oracle_workload_timings(args.cpu_tokens, (v, dt, fl))}
 
+    r = blk_res or {}
+    value, ms_step = r.get("value"), r.get("ms_step")
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
+        "metric": METRIC, "value": round(value, 2) if value else None, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3) if ms_step else None,
+        "median_ms_per_step": round(r["median_step"], 3) if r else None, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "tokens": s.tokens, "hidden": s.hidden, "n_q": s.n_q,
-                   "n_kv": s.n_kv, "head_dim": s.head_dim, "inter": s.inter, "tflop_per_step":
-                   round(flops_step / 1e12, 3), "l2": "inputs (1.7 GB of weights + activations) exceed the "
-                   "129 MB L2; no flush", "parallelism": "single GPU",
+                   "n_kv": s.n_kv, "head_dim": s.head_dim, "inter": s.inter,
+                   "tflop_per_step": round(r["flops_step"] / 1e12, 3) if r else None,
+                   "l2": "block step: inputs (1.7 GB of weights + activations) exceed the 129 MB L2, no flush; "
+                         f"other workloads: {FLUSH_BYTES >> 20} MB written between timed calls",
+                   "parallelism": "single GPU",
                    "rmsnorm_gain": "folded into the weights each step" if args.fold_weights
                    else "applied by the producing epilogue (u = x ⊙ gamma)"},
         "pct_bf16_peak": {"burst": round(value / burst, 4), "sustained": round(value / sustained, 4),
-                          "source": peak_src},
-        "roofline": roofline,
+                          "source": peak_src} if value else None,
+        "roofline": r.get("roofline"),
         "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": launches_step * args.steps,
-        "clocks": clk,
-        "unfused_ms_per_step": round(unfused_ms, 3) if unfused_ms else None,
-        "speedup_vs_unfused": round(unfused_ms / ms_step, 3) if unfused_ms else None,
-        "stages": stages,
+        "e2e": r.get("e2e"),
+        "gpu_launches": r["launches_step"] * args.steps if r else None,
+        "clocks": r.get("clk"),
+        "unfused_ms_per_step": round(r["unfused_ms"], 3) if r.get("unfused_ms") else None,
+        "speedup_vs_unfused": round(r["unfused_ms"] / r["median_step"], 3) if r.get("unfused_ms") else None,
+        "stages": r.get("stages"),
         "other_workloads": other or None,
     }
     print(json.dumps(line), flush=True)
     return 0
-
 
 if __name__ == "__main__":
     sys.exit(main())

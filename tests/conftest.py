@@ -8,6 +8,15 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+@pytest.fixture(autouse=True)
+def _parity_test_name(request):
+    """Names the running test in the parity report (see parity.py)."""
+    import parity
+    parity.CURRENT["test"] = request.node.nodeid
+    yield
+    parity.CURRENT["test"] = None
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
     config.addinivalue_line("markers", "slow: full-size workload check")

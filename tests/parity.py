@@ -17,6 +17,9 @@ bound is unchanged.
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -45,10 +48,24 @@ def bf16_metrics(got, ref):
     return float(np.max(np.abs(err) / bound)) * BF16_MAX_REL_RMS, fro
 
 
+# The test that is running (set by an autouse fixture in conftest.py); with
+# CODA_PARITY_REPORT set in the environment every comparison appends one JSON
+# line (test, output, measured errors) to that file.
+CURRENT = {"test": None}
+
+
+def _report(**rec):
+    path = os.environ.get("CODA_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(test=CURRENT["test"], **rec)) + "\n")
+
+
 def assert_bf16(got, ref, name):
     g = to_np(got)
     assert np.all(np.isfinite(g)), f"{name}: non-finite values"
     mx, fro = bf16_metrics(got, ref)
+    _report(kind="bf16", name=name, max_over_rms=mx, rel_frob=fro, elements=int(g.size))
     assert mx <= BF16_MAX_REL_RMS and fro <= BF16_FROB, \
         f"{name}: max|err|/(RMS + half-ulp) = {mx:.3e} (<= {BF16_MAX_REL_RMS}), " \
         f"rel Frobenius = {fro:.3e} (<= {BF16_FROB})"
@@ -59,5 +76,6 @@ def assert_f32(got, ref, name, tol=F32_REL):
     g, r = to_np(got), to_np(ref)
     assert g.shape == r.shape, f"{name}: shape {g.shape} != {r.shape}"
     rel = float(np.max(np.abs(g - r) / np.maximum(np.abs(r), 1e-30)))
+    _report(kind="f32", name=name, max_rel=rel, elements=int(g.size))
     assert rel <= tol, f"{name}: max relative error {rel:.3e} > {tol}"
     return rel
