@@ -53,6 +53,8 @@ __all__ = [
     "rmsnorm_linear_cross_entropy_fwd", "rmsnorm_linear_cross_entropy_bwd",
     "sigmoid", "linear_sigmoid_fwd", "linear_sigmoid_bwd",
     "E4M3_MAX", "quantize_fp8_rows", "linear_fp8_fwd", "swiglu_fp8_fwd",
+    "quantize_fp8_cols", "linear_qknorm_rope_fp8_fwd", "linear_cross_entropy_fp8_fwd",
+    "linear_cross_entropy_fp8_bwd", "dswiglu_fp8", "rmsnorm_linear_dx_fp8",
     "E2M1_MAX", "E2M1_GRID", "NVFP4_BLOCK", "e2m1_round", "e2m1_value", "quantize_nvfp4_rows",
     "rmsnorm_scale_nvfp4",
     "linear_nvfp4_fwd", "swiglu_nvfp4_fwd",
@@ -407,6 +409,88 @@ def swiglu_fp8_fwd(Xv, sx, Wgv, sg, Wuv, su, row_scale=None):
         A = A * np.asarray(row_scale, dtype=np.float64)[:, None]
     return swiglu_fwd(A, Wgv * np.asarray(sg, dtype=np.float64)[:, None],
                       Wuv * np.asarray(su, dtype=np.float64)[:, None])
+
+
+
+def quantize_fp8_cols(X):
+    """Column quantiser, the row quantiser's rule along the other axis:
+    scale_j = max_i |x_ij| / 448 (fp32; 1 for an all-zero column),
+    q_ij = e4m3(x_ij / scale_j).  Returned transposed, as the K-major operand
+    of a GEMM that contracts over X's rows: (codes uint8 [C, R] of X^T,
+    values float64 [C, R], scales float32 [C]); x_ij ~= values[j, i] * scale_j."""
+    import torch
+    x32 = np.asarray(X, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=0) if x32.shape[0] else np.zeros(x32.shape[1], np.float32)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    v = np.clip((x32 / scale[None, :]).astype(np.float32), -E4M3_MAX, E4M3_MAX)
+    q = torch.from_numpy(np.ascontiguousarray(v.T)).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).numpy(), q.double().numpy(), scale
+
+
+def _deq(values, scales):
+    """Dequantised operand: values * per-row scales."""
+    return np.asarray(values, dtype=np.float64) * np.asarray(scales, dtype=np.float64)[:, None]
+
+
+def linear_qknorm_rope_fp8_fwd(Xv, sx, Wv, sw, gamma_q, gamma_k, pos, theta, eps, n_q, n_kv, head_dim,
+                               row_scale=None, pairing="interleaved"):
+    """The QKV projection with QK-RMSNorm + RoPE on e4m3 operands:
+    [q | k | v] = r ⊙ ((Xv sx)(Wv sw)^T) (r = 1 without row_scale), then per
+    head Q = RoPE(RMSNorm_d(q) ⊙ gamma_q), K likewise, V = v ([P3]'s
+    linear_qknorm_rope on the dequantised operands).  Returns Q, K, V and
+    the pre-norm q|k, flattened per token."""
+    qkv = gemm_epilogue_plain(_deq(Xv, sx), _deq(Wv, sw), row_scale=row_scale)
+    d, M = head_dim, qkv.shape[0]
+    q = _heads(qkv[:, : n_q * d], n_q, d)
+    k = _heads(qkv[:, n_q * d: (n_q + n_kv) * d], n_kv, d)
+    Q = qk_rmsnorm_rope_fwd(q, gamma_q, pos, theta, eps, pairing)
+    K = qk_rmsnorm_rope_fwd(k, gamma_k, pos, theta, eps, pairing)
+    return {"Q": Q.reshape(M, -1), "K": K.reshape(M, -1), "V": qkv[:, (n_q + n_kv) * d:],
+            "qk": qkv[:, : (n_q + n_kv) * d]}
+
+
+def linear_cross_entropy_fp8_fwd(Xv, sx, Wv, sw, labels, ignore_index=-100):
+    """linear_cross_entropy_fwd on the dequantised e4m3 operands."""
+    return linear_cross_entropy_fwd(_deq(Xv, sx), _deq(Wv, sw), labels, ignore_index)
+
+
+def linear_cross_entropy_fp8_bwd(Xv, sx, Wv, sw, X, W, labels, ignore_index=-100, dloss=1.0):
+    """The softmax gradient dZ of linear_cross_entropy_bwd at the logits of
+    the dequantised e4m3 operands, then dX = dZ W and dW = dZ^T X with the
+    operands X, W of the two gradient GEMMs (bf16)."""
+    dZ = linear_cross_entropy_bwd(_deq(Xv, sx), _deq(Wv, sw), labels, ignore_index, dloss)["dZ"]
+    return {"dX": dZ @ W, "dW": dZ.T @ X, "dZ": dZ}
+
+
+def dswiglu_fp8(dYv, sdy, WdTv, swd, g, u, row_scale=None):
+    """The dSwiGLU map on the dH GEMM with e4m3 operands:
+    dH = (dYv sdy)(WdTv swd)^T  (dY Wd with Wd^T quantised per unit),
+    dG = dH ⊙ u ⊙ silu'(g),  dU = dH ⊙ silu(g)  (g, u the saved projections);
+    returns G' = r ⊙ [dG | dU] ([M, 2I]; r = 1 without row_scale), the row
+    sums dot_i = sum_j (dG g + dU u)_ij that the RMSNorm backward needs, H =
+    silu(g) ⊙ u and dH.  (The chain rule of mlp_fwd's H = silu(g) u.)"""
+    dH = _deq(dYv, sdy) @ _deq(WdTv, swd).T
+    g = np.asarray(g, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    dG = dH * u * silu_grad(g)
+    dU = dH * silu(g)
+    r = np.ones(dH.shape[0]) if row_scale is None else np.asarray(row_scale, dtype=np.float64)
+    return {"Gp": np.concatenate([dG, dU], axis=1) * r[:, None], "dot": (dG * g + dU * u).sum(axis=1),
+            "H": silu(g) * u, "dH": dH}
+
+
+def rmsnorm_linear_dx_fp8(Gv, sgp, WTv, sw, X, gamma, coef, dX_resid=None):
+    """The input gradient of an RMSNorm-reparameterised projection with e4m3
+    operands: D = (Gv sgp)(WTv sw)^T (G' W with W^T quantised per input
+    feature), dX = gamma ⊙ D - coef ⊙ X (+ dX_resid), dgamma_k = sum_i X_ik D_ik
+    (the backward of y = r ⊙ ((X ⊙ gamma) W^T) written out by the chain
+    rule; coef_i = r_i^2 sum_n G_in y_in / K comes from the caller)."""
+    D = _deq(Gv, sgp) @ _deq(WTv, sw).T
+    X = np.asarray(X, dtype=np.float64)
+    dX = D * np.asarray(gamma, dtype=np.float64)[None, :] - np.asarray(coef, dtype=np.float64)[:, None] * X
+    if dX_resid is not None:
+        dX = dX + dX_resid
+    return {"dX": dX, "dgamma": (X * D).sum(axis=0), "D": D}
 
 
 # ---------------------------------------------------------------------------

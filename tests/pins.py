@@ -631,6 +631,105 @@ def check_fp8_linear(o):
     return max(_rel(H, H0), _rel(g, g0), _rel(u, u0), _rel(y, X @ Wg.T))
 
 
+def check_fp8_cols_quantizer(o):
+    """The column quantiser is the row quantiser of the transpose, bit for
+    bit (codes, values, scales), and each column's maximum maps to +-448."""
+    r = RNG(24)
+    X = r.standard_normal((37, 24)) * np.array([1e-3, 1, 30, 1e4] * 6)[None, :]
+    X[:, 5] = 0.0
+    qc, qv, sc = o.quantize_fp8_cols(X)
+    rc, rv, rs = o.quantize_fp8_rows(np.ascontiguousarray(X.T))
+    e = [float(np.any(qc != rc)), float(np.any(sc != rs)), float(np.max(np.abs(qv - rv)))]
+    nz = np.abs(X).max(axis=0) > 0
+    e.append(float(np.max(np.abs(np.abs(qv[nz]).max(axis=1) - 448.0))))
+    return max(e)
+
+
+def _e4m3_exact(r, shape, vals):
+    """Exact e4m3 values times 2^-6 with one 448 * 2^-6 per row, so that the
+    row quantiser's scale is exactly 2^-6 and every code is exact."""
+    X = vals[r.integers(0, len(vals), size=shape)] * (2.0 ** -6)
+    X[:, 0] = 448.0 * 2.0 ** -6
+    return X
+
+
+def check_fp8_epilogue_ops(o):
+    """With exact e4m3 operands, the FP8 operators equal the bf16 definitions:
+    QKV + QK-norm + RoPE equals qk_rmsnorm_rope_fwd of the projection heads;
+    the cross-entropy forward equals torch cross_entropy and the backward
+    equals linear_cross_entropy_bwd (dX, dW with the same operands); the
+    dSwiGLU map equals mlp_bwd's dg, du (and G' carries the row factor), and
+    its row dot equals r dL/dr by finite differences; the RMSNorm input
+    gradient equals rmsnorm_linear_bwd's dX and dgamma."""
+    codes, vals = _e4m3_table()
+    vals = vals[np.abs(vals) <= 448.0]
+    r = RNG(25)
+    e = []
+    # QKV + QK-norm + RoPE (2 q heads, 1 kv head of 8)
+    d, n_q, n_kv, M, K = 8, 2, 1, 3, 16
+    X = _e4m3_exact(r, (M, K), vals)
+    W = _e4m3_exact(r, ((n_q + 2 * n_kv) * d, K), vals)
+    _, xv, sx = o.quantize_fp8_rows(X)
+    _, wv, sw = o.quantize_fp8_rows(W)
+    gq, gk = 1 + 0.1 * r.standard_normal(d), 1 + 0.1 * r.standard_normal(d)
+    pos, rs = np.array([0, 5, 9]), np.array([0.5, 2.0, 1.25])
+    f = o.linear_qknorm_rope_fp8_fwd(xv, sx, wv, sw, gq, gk, pos, 1e4, 1e-6, n_q, n_kv, d, row_scale=rs)
+    qkv = (X @ W.T) * rs[:, None]
+    Qr = o.qk_rmsnorm_rope_fwd(qkv[:, : n_q * d].reshape(M, n_q, d), gq, pos, 1e4, 1e-6).reshape(M, -1)
+    Kr = o.qk_rmsnorm_rope_fwd(qkv[:, n_q * d: (n_q + n_kv) * d].reshape(M, n_kv, d), gk, pos, 1e4,
+                               1e-6).reshape(M, -1)
+    e += [_rel(f["Q"], Qr), _rel(f["K"], Kr), _rel(f["V"], qkv[:, (n_q + n_kv) * d:])]
+    # cross-entropy forward and backward
+    M, K, V = 5, 16, 9
+    X = _e4m3_exact(r, (M, K), vals)
+    W = _e4m3_exact(r, (V, K), vals)
+    lab = np.array([0, 8, -100, 3, 3])
+    _, xv, sx = o.quantize_fp8_rows(X)
+    _, wv, sw = o.quantize_fp8_rows(W)
+    fce = o.linear_cross_entropy_fp8_fwd(xv, sx, wv, sw, lab)
+    ref = F.cross_entropy(torch.from_numpy(X @ W.T), torch.from_numpy(lab).long(), ignore_index=-100).item()
+    e.append(abs(fce["loss"] - ref) / abs(ref))
+    bce = o.linear_cross_entropy_fp8_bwd(xv, sx, wv, sw, X, W, lab, dloss=0.7)
+    b0 = o.linear_cross_entropy_bwd(X, W, lab, dloss=0.7)
+    e += [_rel(bce["dX"], b0["dX"]), _rel(bce["dW"], b0["dW"])]
+    # dSwiGLU on the dH GEMM
+    M, Hd, I = 3, 16, 6
+    X = r.standard_normal((M, Hd))
+    Wg, Wu = r.standard_normal((I, Hd)) * 0.4, r.standard_normal((I, Hd)) * 0.4
+    Wd = _e4m3_exact(r, (I, Hd), vals).T.copy()          # Wd [Hd, I]; its transpose exact per unit row
+    dY = _e4m3_exact(r, (M, Hd), vals)
+    fm = o.mlp_fwd(X, Wg, Wu, Wd, np.zeros((M, Hd)))
+    _, dyv, sdy = o.quantize_fp8_rows(dY)
+    _, wdv, swd = o.quantize_fp8_rows(np.ascontiguousarray(Wd.T))
+    rr = np.array([0.5, 1.0, 3.0])
+    ds = o.dswiglu_fp8(dyv, sdy, wdv, swd, fm["g"], fm["u"], row_scale=rr)
+    mb = o.mlp_bwd(X, Wg, Wu, Wd, dY)
+    e += [_rel(ds["Gp"][:, :I], mb["dg"] * rr[:, None]), _rel(ds["Gp"][:, I:], mb["du"] * rr[:, None]),
+          _rel(ds["H"], fm["H"])]
+
+    def L(t):
+        return float((dY * o.mlp_fwd(t * X, Wg, Wu, Wd, np.zeros((M, Hd)))["y"]).sum(axis=1)[i_row])
+    h = 1e-6
+    for i_row in range(M):
+        e.append(abs((L(1 + h) - L(1 - h)) / (2 * h) - ds["dot"][i_row]) / max(abs(ds["dot"][i_row]), 1e-12))
+    # RMSNorm-reparameterised input gradient
+    M, K, N = 4, 16, 8
+    X = r.standard_normal((M, K))
+    gam = 1 + 0.1 * r.standard_normal(K)
+    W = _e4m3_exact(r, (K, N), vals).T.copy()              # W [N, K]; W^T [K, N] exact per row
+    Gp = _e4m3_exact(r, (M, N), vals)                       # G' = r G, exact
+    rstd = o.rms_inv(X, 1e-6)
+    G = Gp / rstd[:, None]
+    y, _ = o.rmsnorm_linear_fwd(X, gam, W, 1e-6)
+    coef = rstd ** 2 * (G * y).sum(axis=1) / K
+    _, gv, sg = o.quantize_fp8_rows(Gp)
+    _, wtv, swt = o.quantize_fp8_rows(np.ascontiguousarray(W.T))
+    dx = o.rmsnorm_linear_dx_fp8(gv, sg, wtv, swt, X, gam, coef)
+    b = o.rmsnorm_linear_bwd(X, gam, W, 1e-6, G)
+    e += [_rel(dx["dX"], b["dX"]), _rel(dx["dgamma"], b["dgamma"])]
+    return max(e)
+
+
 def _e2m1_decode_table():
     """The 16 e2m1 codes decoded from the format's definition: bit 3 sign,
     bits 1-2 exponent with bias 1, bit 0 mantissa; exponent 0 is subnormal
@@ -814,6 +913,8 @@ ALL_CHECKS = {
     "nvfp4_linear": (check_nvfp4_linear, 1e-14),
     "fp8_quantizer": (check_fp8_quantizer, 1e-12),
     "fp8_linear": (check_fp8_linear, 1e-14),
+    "fp8_cols_quantizer": (check_fp8_cols_quantizer, 0.0),
+    "fp8_epilogue_ops": (check_fp8_epilogue_ops, 1e-7),
     "quantised_swiglu_row_factor": (check_quantised_swiglu_row_factor, 1e-12),
     "linear_sigmoid": (check_linear_sigmoid, 1e-7),
     "rmsnorm_ce_library": (check_rmsnorm_ce_library, 1e-12),

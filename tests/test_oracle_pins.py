@@ -211,6 +211,13 @@ MUTANTS = {
     "ce_dw_rows_without_onehot": _source_mutant("return {\"dW_rows\": dZ[:, np.asarray(vocab_rows)].T @ X}",
                                                 "return {\"dW_rows\": (p * dloss / max(n_valid, 1))"
                                                 "[:, np.asarray(vocab_rows)].T @ X}"),
+    "fp8_cols_scale_from_whole_matrix": _source_mutant(
+        "amax = np.max(np.abs(x32), axis=0) if x32.shape[0] else np.zeros(x32.shape[1], np.float32)",
+        "amax = np.full(x32.shape[1], np.max(np.abs(x32)), np.float32)"),
+    "dswiglu_fp8_gate_grad_is_silu": _source_mutant("dG = dH * u * silu_grad(g)", "dG = dH * u * silu(g)"),
+    "rms_dx_fp8_drops_gamma": _source_mutant(
+        "dX = D * np.asarray(gamma, dtype=np.float64)[None, :] - np.asarray(coef, dtype=np.float64)[:, None] * X",
+        "dX = D - np.asarray(coef, dtype=np.float64)[:, None] * X"),
     # a negative label wraps around to column V + label (numpy indexing)
     "ce_negative_label_wraps": _source_mutant("in_range = (labels >= 0) & (labels < V)",
                                               "in_range = labels < V"),
