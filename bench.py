@@ -747,6 +747,65 @@ def main():
             "ms": round(m8, 4), "tflops": rate(f_gu, m8),
             "peak": round(fp8_peak, 1), "peak_kind": f"fp8 = 2 x bf16 burst ({peak_src}, nominal ratio)",
             "frac": round(rate(f_gu, m8) / fp8_peak, 4)}
+        # the other epilogues on the FP8 mainloop at the block's shapes: the
+        # QKV projection with QK-norm + RoPE (8192 x 10240 x 8192), and the
+        # MLP backward's input-gradient chain -- dH GEMM with the dSwiGLU
+        # epilogue (8192 x 28672 x 8192), G' quantised per row, the dX GEMM
+        # with the RMSNorm-backward epilogue (8192 x 8192 x 57344); weights'
+        # transposed operands from the column quantiser (timed separately)
+        n_qkv = s.qkv_out
+        wqkv_q, swqkv = coda.quantize_fp8_rows(t["Wqkv"])
+        qk_out = {"Q": torch.empty(T_, s.n_q * s.head_dim, dtype=torch.bfloat16, device=dev),
+                  "K": torch.empty(T_, s.n_kv * s.head_dim, dtype=torch.bfloat16, device=dev),
+                  "V": torch.empty(T_, s.n_kv * s.head_dim, dtype=torch.bfloat16, device=dev),
+                  "qk_save": torch.empty(T_, (s.n_q + s.n_kv) * s.head_dim, dtype=torch.bfloat16, device=dev)}
+        cs8 = coda.rope_table(s.theta, s.head_dim, s.seq_len, device=dev)
+        gam = t["gamma_q"], t["gamma_k"]
+        mq = median_ms(lambda: coda.linear_qknorm_rope_fp8(xq, sx, wqkv_q, swqkv, gam[0], gam[1], t["pos"], cs8,
+                                                           s.n_q, s.n_kv, rstd=r_, eps=s.eps, out=qk_out, ws=ws8))
+        mqb = median_ms(lambda: coda.linear_qknorm_rope(t["x0"], t["Wqkv"], gam[0], gam[1], t["pos"], cs8, s.n_q,
+                                                        s.n_kv, rstd=r_, eps=s.eps, out=qk_out, ws=ws8))
+        f_qkv = 2 * T_ * H_ * n_qkv
+        other["fp8_qknorm_rope"] = {
+            "workload": f"e4m3 QKV GEMM with QK-RMSNorm + RoPE epilogue, {T_} x {n_qkv} x {H_}",
+            "ms": round(mq, 4), "tflops": rate(f_qkv, mq), "frac": round(rate(f_qkv, mq) / fp8_peak, 4),
+            "bf16_ms": round(mqb, 4), "speedup_vs_bf16": round(mqb / mq, 3)}
+        del wqkv_q, qk_out
+        mwd = median_ms(lambda: coda.quantize_fp8_cols(t["Wd"]))
+        wdt_q, swdt = coda.quantize_fp8_cols(t["Wd"])
+        mwgu = median_ms(lambda: coda.quantize_fp8_cols(t["Wg"], t["Wu"]))
+        wgut_q, swgut = coda.quantize_fp8_cols(t["Wg"], t["Wu"])
+        dyq, sdy = coda.quantize_fp8_rows(t["dx2"])
+        Gp8 = torch.empty(T_, 2 * I_, dtype=torch.bfloat16, device=dev)
+        gq_, sgq_ = torch.empty(T_, 2 * I_, dtype=torch.uint8, device=dev), torch.empty(T_, dtype=torch.float32,
+                                                                                       device=dev)
+        dot8 = torch.empty(T_, dtype=torch.float32, device=dev)
+        coef8 = torch.zeros(T_, dtype=torch.float32, device=dev)
+        dx8 = {"dX": torch.empty(T_, H_, dtype=torch.bfloat16, device=dev),
+               "dgamma": torch.empty(H_, dtype=torch.float32, device=dev)}
+        ws_ds = coda.workspace(coda.load().coda_linear_dswiglu_fp8_workspace_size(T_, I_, H_), dev)
+        ws_dx = coda.workspace(coda.load().coda_rmsnorm_linear_dx_fp8_workspace_size(T_, 2 * I_, H_), dev)
+
+        def fp8_dgrad(mark):
+            coda.linear_dswiglu_fp8(dyq, sdy, wdt_q, swdt, gq8, uq8, rstd=r_,
+                                    out={"Gp": Gp8, "dot": dot8, "H": None}, ws=ws_ds)
+            mark()
+            coda.quantize_fp8_rows(Gp8, Xq=gq_, scale=sgq_)
+            mark()
+            coda.rmsnorm_linear_dx_fp8(gq_, sgq_, wgut_q, swgut, t["x0"], t["gamma_mlp"], coef8,
+                                       dX_resid=t["dx2"], out=dx8, ws=ws_dx)
+        md = median_ms(fp8_dgrad, parts=3)
+        if coda.get_status(ws_ds) != 0 or coda.get_status(ws_dx) != 0:
+            raise RuntimeError("device status error in the FP8 backward measurement")
+        f_dh, f_dx = 2 * T_ * H_ * I_, 2 * T_ * 2 * I_ * H_
+        other["fp8_mlp_dgrad"] = {
+            "workload": f"e4m3 MLP input-gradient chain: dH GEMM + dSwiGLU epilogue {T_} x {I_} x {H_}, G' row "
+                        f"quantisation, dX GEMM + RMSNorm-backward epilogue {T_} x {H_} x {2 * I_}",
+            "ms": round(sum(md), 4), "dswiglu_ms": round(md[0], 4), "quantize_g_ms": round(md[1], 4),
+            "rms_dx_ms": round(md[2], 4), "dswiglu_tflops": rate(f_dh, md[0]), "rms_dx_tflops": rate(f_dx, md[2]),
+            "gemm_frac": round(rate(f_dh + f_dx, md[0] + md[2]) / fp8_peak, 4),
+            "weight_quant_ms": {"Wd^T": round(mwd, 4), "[Wg;Wu]^T": round(mwgu, 4)}}
+        del wdt_q, wgut_q, dyq, Gp8, gq_, ws_ds, ws_dx, dx8
         del xq, gq, uq
     if "nvfp4" in legs:
         # NVFP4 (e2m1 + e4m3 block scales) gate/up + SwiGLU at the same shape:

@@ -83,6 +83,19 @@ _SIGS = {
     "coda_linear_fp8": ([_P] * 6 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_linear_swiglu_fp8_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_linear_swiglu_fp8": ([_P] * 10 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_quantize_fp8_cols": ([_P, _I64, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _P], ctypes.c_int),
+    "coda_linear_qknorm_rope_fp8_workspace_size": ([_I64, _I64, _I32, _I32, _I32], _SZ),
+    "coda_linear_qknorm_rope_fp8": ([_P] * 9 + [_I32, _F, _I32, _I32, _I32, _I32] + [_P] * 4
+                                    + [_I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_cross_entropy_fp8_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_cross_entropy_fp8": ([_P] * 5 + [_I32, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_cross_entropy_bwd_fp8_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_cross_entropy_bwd_fp8": ([_P] * 7 + [_I32, _P, _P, _F, _P, _P, _I64, _I64, _I64, _P, _SZ, _P],
+                                          ctypes.c_int),
+    "coda_linear_dswiglu_fp8_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_linear_dswiglu_fp8": ([_P] * 10 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_rmsnorm_linear_dx_fp8_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "coda_rmsnorm_linear_dx_fp8": ([_P] * 10 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_nvfp4_scale_bytes": ([_I64, _I64], _SZ),
     "coda_quantize_nvfp4_rows": ([_P, _I64, _I64, _I64, _P, _P, _P, _P], ctypes.c_int),
     "coda_rmsnorm_scale_nvfp4": ([_P, _I64, _I64, _I64, _F, _P, _P, _P, _P, _P, _P], ctypes.c_int),
@@ -152,6 +165,7 @@ class EpilogueDesc(ctypes.Structure):
         ("positions", _P), ("cos_sin", _P), ("max_pos", _I32), ("n_q_heads", _I32),
         ("n_kv_heads", _I32), ("head_dim", _I32), ("eps", _F), ("gamma_q", _P), ("gamma_k", _P),
         ("Q", _P), ("K", _P), ("V", _P), ("rope_pairing", _I32),
+        ("operand_type", _I32), ("acc_row_scale", _P), ("acc_col_scale", _P),
     ]
 
 
@@ -547,6 +561,118 @@ def linear_swiglu_fp8(Xq, sx, Wgq, sg, Wuq, su, rstd=None, save=True, H=None, g=
         _u8(Xq, "Xq"), _f32(sx, "sx"), _f32(rstd, "rstd"), _u8(Wgq, "Wgq"), _f32(sg, "sg"), _u8(Wuq, "Wuq"),
         _f32(su, "su"), _bf(H, "H"), _bf(g, "g"), _bf(u, "u"), M, I, K, _ptr(ws), ws.numel(), _stream(stream)))
     return H, g, u
+
+
+def quantize_fp8_cols(X, X2=None, XTq=None, scale=None, stream=None):
+    """Per-column e4m3 quantisation of X [R, C] (with X2 [R2, C] stacked
+    below it): returns (codes uint8 [C, R + R2] of the transpose, scale fp32
+    [C]) -- the K-major operand of a GEMM that contracts over X's rows."""
+    R, C = X.shape
+    R2 = 0 if X2 is None else X2.shape[0]
+    XTq = torch.empty(C, R + R2, dtype=torch.uint8, device=X.device) if XTq is None else XTq
+    scale = torch.empty(C, dtype=torch.float32, device=X.device) if scale is None else scale
+    _check("coda_quantize_fp8_cols", load().coda_quantize_fp8_cols(
+        _bf(X, "X"), X.stride(0), R, _bf(X2, "X2"), X2.stride(0) if X2 is not None else 0, R2, C,
+        _u8(XTq, "XTq"), XTq.stride(0), _f32(scale, "scale"), _stream(stream)))
+    return XTq, scale
+
+
+def linear_qknorm_rope_fp8(Xq, sx, Wq, sw, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, rstd=None, eps=1e-6,
+                           head_dim=128, save=True, out=None, ws=None, stream=None, pairing="interleaved"):
+    """linear_qknorm_rope on e4m3 operands (coda_linear_qknorm_rope_fp8)."""
+    lib = load()
+    M, Kd = Xq.shape
+    dev = Xq.device
+    if out is None:
+        out = {"Q": torch.empty(M, n_q * head_dim, dtype=torch.bfloat16, device=dev),
+               "K": torch.empty(M, n_kv * head_dim, dtype=torch.bfloat16, device=dev),
+               "V": torch.empty(M, n_kv * head_dim, dtype=torch.bfloat16, device=dev),
+               "qk_save": torch.empty(M, (n_q + n_kv) * head_dim, dtype=torch.bfloat16, device=dev)
+               if save else None}
+    ws = _ws(ws, lib.coda_linear_qknorm_rope_fp8_workspace_size(M, Kd, n_q, n_kv, head_dim), dev)
+    _check("coda_linear_qknorm_rope_fp8", lib.coda_linear_qknorm_rope_fp8(
+        _u8(Xq, "Xq"), _f32(sx, "sx"), _f32(rstd, "rstd"), _u8(Wq, "Wq"), _f32(sw, "sw"),
+        _f32(gamma_q, "gamma_q"), _f32(gamma_k, "gamma_k"), _i32(pos, "pos"), _f32(cos_sin, "cos_sin"),
+        cos_sin.shape[0], float(eps), n_q, n_kv, head_dim, _pairing(pairing), _bf(out["Q"], "Q"),
+        _bf(out["K"], "K"), _bf(out["V"], "V"), _bf(out.get("qk_save"), "qk_save"), M, Kd, _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+def linear_cross_entropy_fp8(Xq, sx, Wq, sw, labels, ignore_index=-100, out=None, ws=None, stream=None):
+    """linear_cross_entropy on e4m3 operands (coda_linear_cross_entropy_fp8)."""
+    lib = load()
+    M, K = Xq.shape
+    V = Wq.shape[0]
+    dev = Xq.device
+    if out is None:
+        out = {"loss": torch.empty(1, dtype=torch.float32, device=dev),
+               "lse": torch.empty(M, dtype=torch.float32, device=dev),
+               "n_valid": torch.empty(1, dtype=torch.int32, device=dev)}
+    ws = _ws(ws, lib.coda_linear_cross_entropy_fp8_workspace_size(M, V, K), dev)
+    _check("coda_linear_cross_entropy_fp8", lib.coda_linear_cross_entropy_fp8(
+        _u8(Xq, "Xq"), _f32(sx, "sx"), _u8(Wq, "Wq"), _f32(sw, "sw"), _i32(labels, "labels"), int(ignore_index),
+        _f32(out["loss"], "loss"), _f32(out["lse"], "lse"), _i32(out["n_valid"], "n_valid"), M, V, K, _ptr(ws),
+        ws.numel(), _stream(stream)))
+    out["ws"] = ws
+    return out
+
+
+def linear_cross_entropy_bwd_fp8(Xq, sx, Wq, sw, X, W, labels, lse, n_valid, dloss=1.0, ignore_index=-100,
+                                 out=None, ws=None, stream=None):
+    """Backward with the logits recomputed from the e4m3 operands and dX, dW
+    from the bf16 X, W (coda_linear_cross_entropy_bwd_fp8)."""
+    lib = load()
+    M, K = X.shape
+    V = W.shape[0]
+    if out is None:
+        out = {"dX": torch.empty_like(X), "dW": torch.empty_like(W)}
+    ws = _ws(ws, lib.coda_linear_cross_entropy_bwd_fp8_workspace_size(M, V, K), X.device)
+    _check("coda_linear_cross_entropy_bwd_fp8", lib.coda_linear_cross_entropy_bwd_fp8(
+        _u8(Xq, "Xq"), _f32(sx, "sx"), _u8(Wq, "Wq"), _f32(sw, "sw"), _bf(X, "X"), _bf(W, "W"),
+        _i32(labels, "labels"), int(ignore_index), _f32(lse, "lse"), _i32(n_valid, "n_valid"), float(dloss),
+        _bf(out["dX"], "dX"), _bf(out["dW"], "dW"), M, V, K, _ptr(ws), ws.numel(), _stream(stream)))
+    out["ws"] = ws
+    return out
+
+
+def linear_dswiglu_fp8(dYq, sdy, WdTq, swd, g, u, rstd=None, want_dot=True, want_H=False, out=None, ws=None,
+                       stream=None):
+    """dH GEMM on e4m3 operands with the dSwiGLU epilogue
+    (coda_linear_dswiglu_fp8): returns {"Gp": [M, 2I] = r [dG | dU],
+    "dot": [M] or None, "H": [M, I] or None}."""
+    lib = load()
+    M, K = dYq.shape
+    I = WdTq.shape[0]
+    dev = dYq.device
+    if out is None:
+        out = {"Gp": torch.empty(M, 2 * I, dtype=torch.bfloat16, device=dev),
+               "dot": torch.empty(M, dtype=torch.float32, device=dev) if want_dot else None,
+               "H": torch.empty(M, I, dtype=torch.bfloat16, device=dev) if want_H else None}
+    ws = _ws(ws, lib.coda_linear_dswiglu_fp8_workspace_size(M, I, K), dev)
+    _check("coda_linear_dswiglu_fp8", lib.coda_linear_dswiglu_fp8(
+        _u8(dYq, "dYq"), _f32(sdy, "sdy"), _u8(WdTq, "WdTq"), _f32(swd, "swd"), _bf(g, "g"), _bf(u, "u"),
+        _f32(rstd, "rstd"), _bf(out["Gp"], "Gp"), _f32(out.get("dot"), "dot"), _bf(out.get("H"), "H"), M, I, K,
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def rmsnorm_linear_dx_fp8(Gq, sg, WTq, sw, X, gamma, coef, dX_resid=None, out=None, ws=None, stream=None):
+    """Input gradient of an RMSNorm-reparameterised projection on e4m3
+    operands (coda_rmsnorm_linear_dx_fp8): returns {"dX", "dgamma"}."""
+    lib = load()
+    M, N = Gq.shape
+    K = WTq.shape[0]
+    dev = Gq.device
+    if out is None:
+        out = {"dX": torch.empty(M, K, dtype=torch.bfloat16, device=dev),
+               "dgamma": torch.empty(K, dtype=torch.float32, device=dev)}
+    ws = _ws(ws, lib.coda_rmsnorm_linear_dx_fp8_workspace_size(M, N, K), dev)
+    _check("coda_rmsnorm_linear_dx_fp8", lib.coda_rmsnorm_linear_dx_fp8(
+        _u8(Gq, "Gq"), _f32(sg, "sg"), _u8(WTq, "WTq"), _f32(sw, "sw"), _bf(X, "X"), _f32(gamma, "gamma"),
+        _f32(coef, "coef"), _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"), _f32(out["dgamma"], "dgamma"), M, N,
+        K, _ptr(ws), ws.numel(), _stream(stream)))
+    return out
 
 
 def quantize_nvfp4_rows(X, stream=None):

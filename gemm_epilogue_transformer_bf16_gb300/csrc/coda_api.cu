@@ -271,12 +271,19 @@ int dispatch(const Plan& p, int sms, int cg, cudaStream_t s, const CUtensorMap* 
   const int nu = a.num_units;
   cudaError_t err;
   if (p.fp8) {
-    if (p.kind == coda::EpiKind::Plain)
-      err = coda::launch_gemm_plain_fp8(nu, sms, cg, s, maps, a);
-    else if (p.kind == coda::EpiKind::Swiglu)
-      err = coda::launch_gemm_swiglu_fp8(nu, sms, cg, s, maps, a);
-    else
-      return CODA_ERR_UNSUPPORTED;
+    switch (p.kind) {
+      case coda::EpiKind::Plain: err = coda::launch_gemm_plain_fp8(nu, sms, cg, s, maps, a); break;
+      case coda::EpiKind::Swiglu: err = coda::launch_gemm_swiglu_fp8(nu, sms, cg, s, maps, a); break;
+      case coda::EpiKind::QkRope:
+        err = p.rope_half ? coda::launch_gemm_qkrope_half_fp8(nu, sms, cg, s, maps, a)
+                          : coda::launch_gemm_qkrope_fp8(nu, sms, cg, s, maps, a);
+        break;
+      case coda::EpiKind::CeLse: err = coda::launch_gemm_celse_fp8(nu, sms, cg, s, maps, a); break;
+      case coda::EpiKind::CeDlogits: err = coda::launch_gemm_cedlogits_fp8(nu, sms, cg, s, maps, a); break;
+      case coda::EpiKind::DSwiglu: err = coda::launch_gemm_dswiglu_fp8(nu, sms, cg, s, maps, a); break;
+      case coda::EpiKind::RmsDx: err = coda::launch_gemm_rmsdx_fp8(nu, sms, cg, s, maps, a); break;
+      default: return CODA_ERR_UNSUPPORTED;
+    }
     return err == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
   }
   switch (p.kind) {
@@ -597,7 +604,22 @@ int coda_gemm_epilogue(const coda_epilogue_desc* d, const coda_bf16* A, int64_t 
   p.M = M;
   p.N = N;
   p.K = K;
+  if (d->operand_type != CODA_OPERAND_BF16 && d->operand_type != CODA_OPERAND_E4M3) return CODA_ERR_INVALID_ARG;
+  if (d->operand_type == CODA_OPERAND_E4M3) {
+    // e4m3 operands: K-major, 16-byte rows
+    if (a_major != CODA_K_MAJOR || b_major != CODA_K_MAJOR) return CODA_ERR_UNSUPPORTED;
+    if (K % 16 || (d->K2 && d->K2 % 16) || lda % 16 || ldb % 16) return CODA_ERR_UNSUPPORTED;
+    if (d->map == CODA_MAP_COLDOT || d->map == CODA_MAP_SIGMOID || d->map == CODA_MAP_DSIGMOID)
+      return CODA_ERR_UNSUPPORTED;
+    CK(al(d->acc_row_scale));
+    CK(al(d->acc_col_scale));
+    p.fp8 = 1;
+  } else if (d->acc_row_scale || d->acc_col_scale) {
+    return CODA_ERR_INVALID_ARG;
+  }
   EpiArgs& e = p.e;
+  e.acc_rs = d->acc_row_scale;
+  e.acc_cs = d->acc_col_scale;
   e.D = D;
   e.ldd = ldd;
   e.d_f32 = d_dtype == CODA_F32;
@@ -1218,6 +1240,16 @@ int coda_linear_qknorm_rope(const coda_bf16* X, const float* rstd, const coda_bf
                             Kdim, ws, ws_bytes, stream);
 }
 
+// The QK backward map stages rows by bulk copies (default); CODA_QK_TMA=0
+// in the environment selects the register-staged map (for comparisons).
+static bool qk_tma_enabled() {
+  static const bool v = [] {
+    const char* e = std::getenv("CODA_QK_TMA");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
+
 static int qk_bwd_blocks(int64_t M) {
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(M, coda::QK_BWD_WARPS), 1184)));
 }
@@ -1273,12 +1305,23 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
   float* dgp = w.take<float>(static_cast<size_t>(4 * ntb) * Kdim);
   int* status = static_cast<int*>(ws);
   cudaStream_t s = S(stream);
-  // the map also writes the input RMSNorm's row coefficient c (with rstd)
-  CU(coda::launch_qk_bwd(BF(dQ), BF(dK), BF(dV), BF(qk_save), BF(V), gamma_q, gamma_k, pos,
-                         reinterpret_cast<const float2*>(cos_sin), max_pos, eps, n_q, n_kv, rstd, M,
-                         1.f / static_cast<float>(Kdim), Gp, norm ? coef : nullptr, dgqk, nblk, status, s,
-                         rope_pairing == CODA_ROPE_HALF));
-  CU(coda::launch_colsum(dgqk, nblk, 256, 256, dgamma_q, s, 128, dgamma_k));
+  // the map also writes the input RMSNorm's row coefficient c (with rstd);
+  // rows staged by bulk copies (one block per SM) unless a row's tensors are
+  // too large for the shared-memory ring
+  int nmap = nblk;
+  if (qk_tma_enabled() && coda::qk_bwd_tma_stages(n_q, n_kv) > 0) {
+    nmap = std::min(nblk, sms);
+    CU(coda::launch_qk_bwd_tma(BF(dQ), BF(dK), BF(dV), BF(qk_save), BF(V), gamma_q, gamma_k, pos,
+                               reinterpret_cast<const float2*>(cos_sin), max_pos, eps, n_q, n_kv, rstd, M,
+                               1.f / static_cast<float>(Kdim), Gp, norm ? coef : nullptr, dgqk, nmap, status, s,
+                               rope_pairing == CODA_ROPE_HALF, TIMEOUT_NS));
+  } else {
+    CU(coda::launch_qk_bwd(BF(dQ), BF(dK), BF(dV), BF(qk_save), BF(V), gamma_q, gamma_k, pos,
+                           reinterpret_cast<const float2*>(cos_sin), max_pos, eps, n_q, n_kv, rstd, M,
+                           1.f / static_cast<float>(Kdim), Gp, norm ? coef : nullptr, dgqk, nblk, status, s,
+                           rope_pairing == CODA_ROPE_HALF));
+  }
+  CU(coda::launch_colsum(dgqk, nmap, 256, 256, dgamma_q, s, 128, dgamma_k));
   {  // D = G' W_qkv;  dX = gamma_in D - c X + dX_resid with the dgamma_in column
      // partials sum_i X_ik D_ik  (without RMSNorm: D + dX_resid)
     Plan p;
@@ -1344,9 +1387,11 @@ size_t coda_linear_cross_entropy_workspace_size(int64_t M, int64_t V, int64_t) {
 
 // Linear + cross-entropy forward; `rstd` (optional) scales each row's logits
 // (the final RMSNorm folded into the head).
+// With fp8 set, X and W are e4m3 codes with per-row scales sx, sw.
 static int ce_forward(const coda_bf16* X, const coda_bf16* W, const int32_t* labels, int32_t ignore_index,
                       const float* rstd, float* loss_mean, float* lse, int32_t* n_valid, int64_t M, int64_t V,
-                      int64_t K, void* ws, size_t ws_bytes, coda_stream stream) {
+                      int64_t K, void* ws, size_t ws_bytes, coda_stream stream, int fp8 = 0,
+                      const float* sx = nullptr, const float* sw = nullptr) {
   CK(dims_ok(M, V, K));
   CK(ws_ok(ws, ws_bytes, coda_linear_cross_entropy_workspace_size(M, V, K)));
   CK(req(loss_mean));
@@ -1376,6 +1421,9 @@ static int ce_forward(const coda_bf16* X, const coda_bf16* W, const int32_t* lab
     p.N = V;
     p.K = K;
     p.n_per_unit = CE_TILES_PER_UNIT;
+    p.fp8 = fp8;
+    p.e.acc_rs = sx;
+    p.e.acc_cs = sw;
     p.e.row_scale = rstd;
     p.e.labels = labels;
     p.e.target_logit = target;
@@ -1518,6 +1566,12 @@ size_t ce_bwd_workspace(int64_t M, int64_t V, int64_t K, bool rms) {
 }
 
 struct CeBwd {
+  // e4m3 operands of the logits GEMM (Xq [M, K], Wq [V, K] codes with per-row
+  // scales sx, sw), or null: the logits come from X, W
+  const uint8_t* Xq = nullptr;
+  const float* sx = nullptr;
+  const uint8_t* Wq = nullptr;
+  const float* sw = nullptr;
   const coda_bf16* X = nullptr;
   const coda_bf16* W = nullptr;      // the weight the logits GEMM reads (gamma-folded with rstd)
   const coda_bf16* W_raw = nullptr;  // rstd: the unfolded weight (dgamma partials)
@@ -1597,6 +1651,13 @@ int ce_backward(const CeBwd& a, void* ws, cudaStream_t s) {
       p.lda = K;
       p.B = Ws;
       p.ldb = K;
+      if (a.Xq) {  // the logits from the e4m3 operands
+        p.fp8 = 1;
+        p.A = a.Xq;
+        p.B = a.Wq + v0 * K;
+        p.e.acc_rs = a.sx;
+        p.e.acc_cs = a.sw + v0;
+      }
       p.M = M;
       p.N = vs;
       p.K = K;
@@ -1997,6 +2058,242 @@ int coda_linear_swiglu_fp8(const uint8_t* Xq, const float* sx, const float* rstd
   p.e.out2 = BF(u_save);
   p.e.ld_out2 = I;
   return run(p, static_cast<int*>(ws), S(stream));
+}
+
+int coda_quantize_fp8_cols(const coda_bf16* X, int64_t ldx, int64_t R, const coda_bf16* X2, int64_t ldx2,
+                           int64_t R2, int64_t C, uint8_t* XTq, int64_t ldo, float* scale, coda_stream stream) {
+  if (R < 0 || R2 < 0 || C < 0) return CODA_ERR_INVALID_ARG;
+  if (!X2 && R2 > 0) return CODA_ERR_INVALID_ARG;
+  const int64_t RT = R + R2;
+  if (C % 8 || RT % 16) return CODA_ERR_UNSUPPORTED;  // 16-byte rows of bf16 input and e4m3 output
+  if (C == 0 || RT == 0) return CODA_OK;
+  for (const void* q : {(const void*)XTq, (const void*)scale}) CK(req(q));
+  if (R > 0) {
+    CK(req(X));
+    CK(ldok(ldx, C));
+  }
+  if (R2 > 0) CK(ldok(ldx2, C));
+  for (const void* q : {(const void*)X, (const void*)X2, (const void*)XTq}) CK(al(q));
+  if (ldo < RT || ldo % 16) return ldo < RT ? CODA_ERR_INVALID_ARG : CODA_ERR_ALIGNMENT;
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  CU(coda::launch_quantize_fp8_cols(BF(X), ldx, R, BF(X2), ldx2, R2, C, XTq, ldo, scale, sms, S(stream)));
+  return CODA_OK;
+}
+
+size_t coda_linear_qknorm_rope_fp8_workspace_size(int64_t, int64_t, int32_t, int32_t, int32_t) { return WS_HEADER; }
+
+int coda_linear_qknorm_rope_fp8(const uint8_t* Xq, const float* sx, const float* rstd, const uint8_t* Wq,
+                                const float* sw, const float* gamma_q, const float* gamma_k, const int32_t* pos,
+                                const float* cos_sin, int32_t max_pos, float eps, int32_t n_q, int32_t n_kv,
+                                int32_t head_dim, int32_t rope_pairing, coda_bf16* Q, coda_bf16* K, coda_bf16* V,
+                                coda_bf16* qk_save, int64_t M, int64_t Kdim, void* ws, size_t ws_bytes,
+                                coda_stream stream) {
+  if (head_dim != 128) return CODA_ERR_UNSUPPORTED;
+  if (n_q <= 0 || n_kv < 0) return CODA_ERR_INVALID_ARG;
+  const int64_t N = static_cast<int64_t>(n_q + 2 * n_kv) * head_dim;
+  CK(dims_ok(M, N, Kdim));
+  if (Kdim % 16) return CODA_ERR_UNSUPPORTED;
+  CK(ws_ok(ws, ws_bytes, WS_HEADER));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)Xq, (const void*)sx, (const void*)Wq, (const void*)sw}) CK(req(q));
+  coda_epilogue_desc d;
+  std::memset(&d, 0, sizeof(d));
+  d.map = CODA_MAP_QKNORM_ROPE;
+  d.operand_type = CODA_OPERAND_E4M3;
+  d.acc_row_scale = sx;
+  d.acc_col_scale = sw;
+  d.row_scale = rstd;
+  d.aux_out[0] = qk_save;
+  d.ld_aux_out[0] = static_cast<int64_t>(n_q + n_kv) * head_dim;
+  d.positions = pos;
+  d.cos_sin = cos_sin;
+  d.max_pos = max_pos;
+  d.n_q_heads = n_q;
+  d.n_kv_heads = n_kv;
+  d.head_dim = head_dim;
+  d.rope_pairing = rope_pairing;
+  d.eps = eps;
+  d.gamma_q = gamma_q;
+  d.gamma_k = gamma_k;
+  d.Q = Q;
+  d.K = K;
+  d.V = V;
+  CK(al(rstd));
+  return coda_gemm_epilogue(&d, reinterpret_cast<const coda_bf16*>(Xq), Kdim, CODA_K_MAJOR,
+                            reinterpret_cast<const coda_bf16*>(Wq), Kdim, CODA_K_MAJOR, nullptr, N, CODA_BF16, M, N,
+                            Kdim, ws, ws_bytes, stream);
+}
+
+size_t coda_linear_cross_entropy_fp8_workspace_size(int64_t M, int64_t V, int64_t K) {
+  return coda_linear_cross_entropy_workspace_size(M, V, K);
+}
+
+int coda_linear_cross_entropy_fp8(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw,
+                                  const int32_t* labels, int32_t ignore_index, float* loss_mean, float* lse,
+                                  int32_t* n_valid, int64_t M, int64_t V, int64_t K, void* ws, size_t ws_bytes,
+                                  coda_stream stream) {
+  if (K % 16) return CODA_ERR_UNSUPPORTED;
+  if (M > 0)
+    for (const void* q : {(const void*)sx, (const void*)sw}) CK(req(q));
+  CK(al(sw));
+  return ce_forward(reinterpret_cast<const coda_bf16*>(Xq), reinterpret_cast<const coda_bf16*>(Wq), labels,
+                    ignore_index, nullptr, loss_mean, lse, n_valid, M, V, K, ws, ws_bytes, stream, 1, sx, sw);
+}
+
+size_t coda_linear_cross_entropy_bwd_fp8_workspace_size(int64_t M, int64_t V, int64_t K) {
+  return ce_bwd_workspace(M, V, K, false);
+}
+
+int coda_linear_cross_entropy_bwd_fp8(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw,
+                                      const coda_bf16* X, const coda_bf16* W, const int32_t* labels,
+                                      int32_t ignore_index, const float* lse, const int32_t* n_valid, float dloss,
+                                      coda_bf16* dX, coda_bf16* dW, int64_t M, int64_t V, int64_t K, void* ws,
+                                      size_t ws_bytes, coda_stream stream) {
+  CK(dims_ok(M, V, K));
+  if (K % 16) return CODA_ERR_UNSUPPORTED;
+  CK(ws_ok(ws, ws_bytes, coda_linear_cross_entropy_bwd_fp8_workspace_size(M, V, K)));
+  CK(req(dW));
+  if (M > 0)
+    for (const void* q : {(const void*)Xq, (const void*)sx, (const void*)Wq, (const void*)sw, (const void*)X,
+                          (const void*)W, (const void*)labels, (const void*)lse, (const void*)n_valid,
+                          (const void*)dX})
+      CK(req(q));
+  for (const void* q : {(const void*)Xq, (const void*)Wq, (const void*)sw, (const void*)X, (const void*)W,
+                        (const void*)dX, (const void*)dW})
+    CK(al(q));
+  if (V == 0) return CODA_ERR_INVALID_ARG;
+  if (M == 0) {
+    CU(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * K * 2, S(stream)));
+    return CODA_OK;
+  }
+  CeBwd a;
+  a.Xq = Xq;
+  a.sx = sx;
+  a.Wq = Wq;
+  a.sw = sw;
+  a.X = X;
+  a.W = W;
+  a.labels = labels;
+  a.ignore_index = ignore_index;
+  a.lse = lse;
+  a.n_valid = n_valid;
+  a.dloss = dloss;
+  a.dX = dX;
+  a.dW = dW;
+  a.M = M;
+  a.V = V;
+  a.K = K;
+  return ce_backward(a, ws, S(stream));
+}
+
+size_t coda_linear_dswiglu_fp8_workspace_size(int64_t M, int64_t I, int64_t) {
+  SizeCursor c;
+  c.take<float>(static_cast<size_t>(cdiv(I, BN)) * M);  // row partials of sum(dG g + dU u)
+  return c.off;
+}
+
+int coda_linear_dswiglu_fp8(const uint8_t* dYq, const float* sdy, const uint8_t* WdTq, const float* swd,
+                            const coda_bf16* g, const coda_bf16* u, const float* rstd, coda_bf16* Gp, float* dot,
+                            coda_bf16* H, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
+                            coda_stream stream) {
+  CK(dims_ok(M, I, K));
+  if (K % 16) return CODA_ERR_UNSUPPORTED;
+  CK(ws_ok(ws, ws_bytes, coda_linear_dswiglu_fp8_workspace_size(M, I, K)));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)dYq, (const void*)sdy, (const void*)WdTq, (const void*)swd, (const void*)g,
+                        (const void*)u, (const void*)Gp})
+    CK(req(q));
+  for (const void* q : {(const void*)dYq, (const void*)WdTq, (const void*)swd, (const void*)g, (const void*)u,
+                        (const void*)Gp, (const void*)H})
+    CK(al(q));
+  WsCursor w(ws);
+  float* spart = w.take<float>(static_cast<size_t>(cdiv(I, BN)) * M);
+  int* status = static_cast<int*>(ws);
+  cudaStream_t s = S(stream);
+  Plan p;
+  p.kind = coda::EpiKind::DSwiglu;
+  p.fp8 = 1;
+  p.A = dYq;
+  p.lda = K;
+  p.B = WdTq;
+  p.ldb = K;
+  p.M = M;
+  p.N = I;
+  p.K = K;
+  p.e.acc_rs = sdy;
+  p.e.acc_cs = swd;
+  p.e.aux0 = BF(g);
+  p.e.ld_aux0 = I;
+  p.e.aux1 = BF(u);
+  p.e.ld_aux1 = I;
+  p.e.out1 = BF(Gp);
+  p.e.ld_out1 = 2 * I;
+  p.e.out2 = BF(Gp) + I;
+  p.e.ld_out2 = 2 * I;
+  p.e.out3 = BF(H);
+  p.e.ld_out3 = I;
+  p.e.row_scale = rstd;
+  if (dot) {
+    p.e.partials = spart;
+    p.e.ld_part = M;
+  }
+  CK(run(p, status, s));
+  if (dot)  // dot_i = sum over the N tiles' partials
+    CU(coda::launch_combine_rows(spart, M, static_cast<int>(cdiv(I, BN)), M, 1.f, 0.f, nullptr, dot, 1, s));
+  return CODA_OK;
+}
+
+size_t coda_rmsnorm_linear_dx_fp8_workspace_size(int64_t M, int64_t, int64_t K) {
+  SizeCursor c;
+  c.take<float>(static_cast<size_t>(4 * cdiv(M, 128)) * K);  // dgamma partials per (token block, warp)
+  return c.off;
+}
+
+int coda_rmsnorm_linear_dx_fp8(const uint8_t* Gq, const float* sg, const uint8_t* WTq, const float* sw,
+                               const coda_bf16* X, const float* gamma, const float* coef, const coda_bf16* dX_resid,
+                               coda_bf16* dX, float* dgamma, int64_t M, int64_t N, int64_t K, void* ws,
+                               size_t ws_bytes, coda_stream stream) {
+  CK(dims_ok(M, K, N));
+  if (N % 16) return CODA_ERR_UNSUPPORTED;
+  CK(ws_ok(ws, ws_bytes, coda_rmsnorm_linear_dx_fp8_workspace_size(M, N, K)));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)Gq, (const void*)sg, (const void*)WTq, (const void*)sw, (const void*)X,
+                        (const void*)gamma, (const void*)coef, (const void*)dX, (const void*)dgamma})
+    CK(req(q));
+  for (const void* q : {(const void*)Gq, (const void*)WTq, (const void*)sw, (const void*)X, (const void*)gamma,
+                        (const void*)dX_resid, (const void*)dX})
+    CK(al(q));
+  WsCursor w(ws);
+  const int64_t ntb = cdiv(M, 128);
+  float* dgp = w.take<float>(static_cast<size_t>(4 * ntb) * K);
+  int* status = static_cast<int*>(ws);
+  cudaStream_t s = S(stream);
+  Plan p;
+  p.kind = coda::EpiKind::RmsDx;
+  p.fp8 = 1;
+  p.A = Gq;
+  p.lda = N;
+  p.B = WTq;
+  p.ldb = N;
+  p.M = M;
+  p.N = K;
+  p.K = N;
+  p.e.acc_rs = sg;
+  p.e.acc_cs = sw;
+  p.e.D = dX;
+  p.e.ldd = K;
+  p.e.aux0 = BF(dX_resid);
+  p.e.ld_aux0 = K;
+  p.e.row_coef = coef;
+  p.e.aux1 = BF(X);
+  p.e.ld_aux1 = K;
+  p.e.col_scale = gamma;
+  p.e.partials = dgp;
+  p.e.ld_part = K;
+  CK(run(p, status, s));
+  CU(coda::launch_colsum(dgp, 4 * ntb, K, K, dgamma, s));
+  return CODA_OK;
 }
 
 // ------------------------------------------------------------------ NVFP4 operands

@@ -6,6 +6,7 @@
 // QK-RMSNorm + RoPE backward).  All are HBM-bound: 16-byte vector accesses,
 // warp-per-row for row work, grids sized to the SM count.
 #include <cmath>
+#include <mutex>
 
 #include <cuda_fp8.h>
 
@@ -419,6 +420,113 @@ __global__ void quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ X, in
   }
 }
 
+// ---------------------------------------------------------------- FP8 (e4m3) column quantisation
+// The transposed K-major operand of a GEMM that contracts over X's rows:
+// scale_c = max_r |x_rc| / 448 (1 for an all-zero column), out[c, r] =
+// e4m3(x_rc / scale_c), for X [R, C] with an optional X2 [R2, C] stacked
+// below it (rows R .. R + R2 - 1 of the column).  Three passes: column
+// maxima (as float bits; non-negative floats order like their bit patterns)
+// reduced with atomicMax into `scale`, maxima -> scales in place, then a
+// 64 x 64 shared-memory transpose that writes 16-byte rows of codes.
+__global__ void fp8_col_amax_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int64_t R,
+                                    const __nv_bfloat16* __restrict__ X2, int64_t ldx2, int64_t R2, int64_t C,
+                                    int rows_per_block, unsigned int* amax_bits) {
+  griddep_launch_dependents();
+  __shared__ float red[8][256];
+  const int cg = threadIdx.x & 31, rp = threadIdx.x >> 5;  // 8 columns per thread, 8 row phases
+  const int64_t c0 = blockIdx.x * 256 + cg * 8;
+  const int64_t r_begin = static_cast<int64_t>(blockIdx.y) * rows_per_block;
+  const int64_t r_end = min(R + R2, r_begin + rows_per_block);
+  float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (c0 < C) {
+    for (int64_t r = r_begin + rp; r < r_end; r += 8) {
+      const __nv_bfloat16* src = r < R ? X + r * ldx + c0 : X2 + (r - R) * ldx2 + c0;
+      float v[8];
+      load_bf16x8(src, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m[j] = fmaxf(m[j], fabsf(v[j]));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) red[rp][cg * 8 + j] = m[j];
+  __syncthreads();
+  const int64_t c = blockIdx.x * 256 + threadIdx.x;
+  if (c < C) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t = fmaxf(t, red[k][threadIdx.x]);
+    atomicMax(amax_bits + c, __float_as_uint(t));
+  }
+}
+
+__global__ void fp8_amax_to_scale_kernel(float* scale, int64_t C) {
+  griddep_launch_dependents();
+  for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < C;
+       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float a = __uint_as_float(reinterpret_cast<unsigned int*>(scale)[c]);
+    scale[c] = a > 0.f ? a / 448.f : 1.f;
+  }
+}
+
+__global__ void fp8_col_quant_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int64_t R,
+                                     const __nv_bfloat16* __restrict__ X2, int64_t ldx2, int64_t R2, int64_t C,
+                                     const float* __restrict__ scale, uint8_t* out, int64_t ldo) {
+  griddep_launch_dependents();
+  __shared__ float tile[64][65];
+  const int64_t RT = R + R2;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
+  // load: 64 rows x 64 columns, 8 columns (16 bytes) per thread and step
+  for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {
+    const int rr = i >> 3, cc = (i & 7) * 8;
+    const int64_t r = r0 + rr, c = c0 + cc;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (r < RT && c < C) load_bf16x8(r < R ? X + r * ldx + c : X2 + (r - R) * ldx2 + c, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) tile[rr][cc + j] = v[j];
+  }
+  __syncthreads();
+  // store: output row c = c0 + t / 4 takes rows r0 + 16 (t % 4) .. + 15 as one 16-byte chunk
+  const int cc = threadIdx.x >> 2, part = threadIdx.x & 3;
+  const int64_t c = c0 + cc;
+  if (c < C) {
+    const float sc = scale[c];
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int rr = part * 16 + j;
+      const uint32_t b = static_cast<uint32_t>(__nv_cvt_float_to_fp8(tile[rr][cc] / sc, __NV_SATFINITE, __NV_E4M3));
+      w[j >> 2] |= b << (8 * (j & 3));
+    }
+    const int64_t r = r0 + part * 16;
+    if (r + 16 <= RT) {
+      *reinterpret_cast<uint4*>(out + c * ldo + r) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      for (int j = 0; j < 16 && r + j < RT; ++j) out[c * ldo + r + j] = static_cast<uint8_t>(w[j >> 2] >> (8 * (j & 3)));
+    }
+  }
+}
+
+cudaError_t launch_quantize_fp8_cols(const __nv_bfloat16* X, int64_t ldx, int64_t R, const __nv_bfloat16* X2,
+                                     int64_t ldx2, int64_t R2, int64_t C, uint8_t* out, int64_t ldo, float* scale,
+                                     int num_sms, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(scale, 0, sizeof(float) * C, s);
+  if (e != cudaSuccess) return e;
+  const int64_t RT = R + R2;
+  const int64_t cblk = (C + 255) / 256;
+  // about four blocks per SM in all, each over a run of rows
+  const int64_t want = std::max<int64_t>(1, (4 * static_cast<int64_t>(num_sms) + cblk - 1) / cblk);
+  const int64_t rsplit = std::min<int64_t>(want, std::max<int64_t>(1, (RT + 63) / 64));
+  const int rows = static_cast<int>((RT + rsplit - 1) / rsplit);
+  fp8_col_amax_kernel<<<dim3(static_cast<unsigned>(cblk), static_cast<unsigned>(rsplit)), 256, 0, s>>>(
+      X, ldx, R, X2, ldx2, R2, C, rows, reinterpret_cast<unsigned int*>(scale));
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  fp8_amax_to_scale_kernel<<<static_cast<unsigned>(std::min<int64_t>((C + 255) / 256, 1024)), 256, 0, s>>>(scale, C);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  fp8_col_quant_kernel<<<dim3(static_cast<unsigned>((C + 63) / 64), static_cast<unsigned>((RT + 63) / 64)), 256, 0,
+                         s>>>(X, ldx, R, X2, ldx2, R2, C, scale, out, ldo);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_fp8_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq,
                                      int64_t ldq, float* scale, int num_sms, cudaStream_t s) {
   const int64_t blocks = std::min<int64_t>((M + 7) / 8, static_cast<int64_t>(num_sms) * 8);
@@ -661,6 +769,294 @@ __global__ void __launch_bounds__(QK_BWD_WARPS * 32)
     for (int ww = 0; ww < QK_BWD_WARPS; ++ww) t += red[ww][j];
     dgam_part[static_cast<int64_t>(blockIdx.x) * 2 * D + j] = t;
   }
+}
+
+// The same map with its rows staged by bulk copies.  One persistent block
+// per SM: a producer warp copies each token row's tensors -- dQ, dK, the
+// saved pre-norm q|k, dV, V (each contiguous within the row) and the row's
+// (cos, sin) table entry -- into a ring of shared-memory stages with
+// cp.async.bulk, counted on the stage's "full" barrier; eight compute warps
+// take the row's heads (warp w: heads w, w + 8, ..., four at a time), store
+// G' and arrive on the stage's "empty" barrier with their partial of the
+// RMSNorm coefficient sum; the producer adds the eight partials when it
+// reuses the stage (or at the end) and writes c for that row.  The copies
+// keep a whole ring of rows in flight per SM, which a warp per row with
+// register loads cannot.  Every wait is bounded (CODA_DEV_TIMEOUT).
+constexpr int QKT_WARPS = 8;
+
+template <bool HALF>
+__global__ void __launch_bounds__((QKT_WARPS + 1) * 32, 1)
+    qk_bwd_tma_kernel(const __nv_bfloat16* __restrict__ dQ, const __nv_bfloat16* __restrict__ dK,
+                      const __nv_bfloat16* __restrict__ dV, const __nv_bfloat16* __restrict__ qk_save,
+                      const __nv_bfloat16* __restrict__ Vs, const float* __restrict__ gq,
+                      const float* __restrict__ gk, const int32_t* __restrict__ pos, const float2* __restrict__ cs,
+                      int max_pos, float eps, int n_q, int n_kv, const float* __restrict__ rstd, int64_t M,
+                      float inv_k, __nv_bfloat16* Gp, float* coef, float* dgam_part, int* status, int stages,
+                      uint64_t timeout_ns) {
+  griddep_launch_dependents();
+  constexpr int D = 128;
+  constexpr int HG = 4;
+  extern __shared__ __align__(128) uint8_t qkt_smem[];
+  __shared__ float red[QKT_WARPS][2 * D];
+  __shared__ float part[8][QKT_WARPS];  // per stage (at most 8), per compute warp: partial of sum dq x
+  __shared__ uint64_t full[8], empty[8];
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int nqk = n_q + n_kv;
+  const int64_t ldq = static_cast<int64_t>(n_q) * D, ldkv = static_cast<int64_t>(n_kv) * D;
+  const int64_t ldsave = ldq + ldkv, ldg = ldq + 2 * ldkv;
+  // stage layout (bytes): header {pos, r}, dQ, dK, saved q|k, dV, V, (cos, sin)[64]
+  const uint32_t o_dq = 16, o_dk = o_dq + static_cast<uint32_t>(n_q) * 2 * D;
+  const uint32_t o_sv = o_dk + static_cast<uint32_t>(n_kv) * 2 * D;
+  const uint32_t o_dv = o_sv + static_cast<uint32_t>(nqk) * 2 * D;
+  const uint32_t o_v = o_dv + static_cast<uint32_t>(n_kv) * 2 * D;
+  const uint32_t o_cs = o_v + static_cast<uint32_t>(n_kv) * 2 * D;
+  const uint32_t stage_bytes = o_cs + (D / 2) * 8;
+  const uint32_t tx_bytes = stage_bytes - 16;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], QKT_WARPS);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int64_t G = gridDim.x;
+  if (w == QKT_WARPS) {
+    // ------------------------------------------------------------ producer
+    const uint32_t el = elect_one();
+    int64_t it = 0;
+    bool ok = true;
+    for (int64_t row = blockIdx.x; row < M; row += G, ++it) {
+      const int st = static_cast<int>(it % stages);
+      const uint32_t ph = static_cast<uint32_t>((it / stages) & 1);
+      if (it >= stages) {
+        if (!mbar_wait_bounded(&empty[st], ph ^ 1, &abort_flag, status, timeout_ns)) {
+          ok = false;
+          break;
+        }
+        if (el && coef) {  // the row that used this stage before
+          const int64_t prev = row - static_cast<int64_t>(stages) * G;
+          float t = 0.f;
+          for (int k = 0; k < QKT_WARPS; ++k) t += part[st][k];
+          const float r = rstd ? rstd[prev] : 1.f;
+          coef[prev] = r * r * t * inv_k;
+        }
+      }
+      uint8_t* sb = qkt_smem + static_cast<size_t>(st) * stage_bytes;
+      int p = pos[row];
+      if (p < 0 || p >= max_pos) {
+        if (el && status) atomicOr(status, CODA_DEV_POSITION_RANGE);
+        p = p < 0 ? 0 : max_pos - 1;
+      }
+      if (el) {
+        reinterpret_cast<int*>(sb)[0] = p;
+        reinterpret_cast<float*>(sb)[1] = rstd ? rstd[row] : 1.f;
+      }
+      mbar_arrive_expect_tx(&full[st], tx_bytes, el);
+      // (no copy of an empty range: a model without q or kv heads)
+      const uint32_t el_q = n_q > 0 ? el : 0u, el_kv = n_kv > 0 ? el : 0u;
+      bulk_load(sb + o_dq, dQ + row * ldq, static_cast<uint32_t>(ldq) * 2, &full[st], el_q);
+      bulk_load(sb + o_dk, dK + row * ldkv, static_cast<uint32_t>(ldkv) * 2, &full[st], el_kv);
+      bulk_load(sb + o_sv, qk_save + row * ldsave, static_cast<uint32_t>(ldsave) * 2, &full[st], el);
+      bulk_load(sb + o_dv, dV + row * ldkv, static_cast<uint32_t>(ldkv) * 2, &full[st], el_kv);
+      bulk_load(sb + o_v, Vs + row * ldkv, static_cast<uint32_t>(ldkv) * 2, &full[st], el_kv);
+      bulk_load(sb + o_cs, cs + static_cast<int64_t>(p) * (D / 2), (D / 2) * 8, &full[st], el);
+    }
+    if (ok) {
+      // the last rows of each stage: wait for their consumers, then write c
+      const int64_t n_it = it;
+      for (int64_t j = n_it > stages ? n_it - stages : 0; j < n_it; ++j) {
+        const int st = static_cast<int>(j % stages);
+        if (!mbar_wait_bounded(&empty[st], static_cast<uint32_t>((j / stages) & 1), &abort_flag, status,
+                               timeout_ns))
+          break;
+        if (el && coef) {
+          const int64_t row = blockIdx.x + j * G;
+          float t = 0.f;
+          for (int k = 0; k < QKT_WARPS; ++k) t += part[st][k];
+          const float r = rstd ? rstd[row] : 1.f;
+          coef[row] = r * r * t * inv_k;
+        }
+      }
+    } else {
+      // let every issued copy land before the block's shared memory is released
+      for (int64_t j = it > stages ? it - stages : 0; j < it; ++j)
+        mbar_wait_drain(&full[j % stages], static_cast<uint32_t>((j / stages) & 1), 200000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ compute warps
+    float aq[4] = {0.f, 0.f, 0.f, 0.f}, ak[4] = {0.f, 0.f, 0.f, 0.f};
+    float g_q[4], g_k[4];
+    {
+      const float4 a = *reinterpret_cast<const float4*>(gq + 4 * lane);
+      const float4 b = *reinterpret_cast<const float4*>(gk + 4 * lane);
+      g_q[0] = a.x; g_q[1] = a.y; g_q[2] = a.z; g_q[3] = a.w;
+      g_k[0] = b.x; g_k[1] = b.y; g_k[2] = b.z; g_k[3] = b.w;
+    }
+    int64_t it = 0;
+    for (int64_t row = blockIdx.x; row < M; row += G, ++it) {
+      const int st = static_cast<int>(it % stages);
+      if (!mbar_wait_bounded(&full[st], static_cast<uint32_t>((it / stages) & 1), &abort_flag, status,
+                             timeout_ns))
+        break;
+      const uint8_t* sb = qkt_smem + static_cast<size_t>(st) * stage_bytes;
+      const float r = reinterpret_cast<const float*>(sb)[1];
+      const float2* css = reinterpret_cast<const float2*>(sb + o_cs);
+      const float2 c0 = css[2 * lane], c1 = css[2 * lane + 1];
+      float2 ch[4];
+      if constexpr (HALF) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ch[i] = css[4 * (lane & 15) + i];
+      }
+      float s = 0.f;
+      for (int k0 = 0; w + k0 * QKT_WARPS < nqk; k0 += HG) {
+        float d[HG][4], x[HG][4];
+#pragma unroll
+        for (int j = 0; j < HG; ++j) {
+          const int h = w + (k0 + j) * QKT_WARPS;
+          if (h < nqk) {
+            const uint8_t* src = h < n_q ? sb + o_dq + h * 2 * D : sb + o_dk + (h - n_q) * 2 * D;
+            const uint2 dr = *reinterpret_cast<const uint2*>(src + 8 * lane);
+            const uint2 xr = *reinterpret_cast<const uint2*>(sb + o_sv + h * 2 * D + 8 * lane);
+            d[j][0] = bf16_lo(dr.x); d[j][1] = bf16_hi(dr.x); d[j][2] = bf16_lo(dr.y); d[j][3] = bf16_hi(dr.y);
+            x[j][0] = bf16_lo(xr.x); x[j][1] = bf16_hi(xr.x); x[j][2] = bf16_lo(xr.y); x[j][3] = bf16_hi(xr.y);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[j][i] = x[j][i] = 0.f;
+          }
+        }
+        float rho[HG];
+#pragma unroll
+        for (int j = 0; j < HG; ++j)
+          rho[j] = x[j][0] * x[j][0] + x[j][1] * x[j][1] + x[j][2] * x[j][2] + x[j][3] * x[j][3];
+        warp_sum4(rho);
+        float t[HG];
+#pragma unroll
+        for (int j = 0; j < HG; ++j) {
+          const int h = w + (k0 + j) * QKT_WARPS;
+          rho[j] = rsqrtf(rho[j] * (1.f / D) + eps);
+          float dn[4];
+          if constexpr (HALF) {
+            // inverse rotation of (first half, second half) element pairs; the
+            // partner sits in lane l ^ 16 at the same index
+            const bool second = lane >= 16;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float dp = __shfl_xor_sync(0xffffffffu, d[j][i], 16);
+              dn[i] = second ? -dp * ch[i].y + d[j][i] * ch[i].x : d[j][i] * ch[i].x + dp * ch[i].y;
+            }
+          } else {
+            dn[0] = d[j][0] * c0.x + d[j][1] * c0.y;
+            dn[1] = -d[j][0] * c0.y + d[j][1] * c0.x;
+            dn[2] = d[j][2] * c1.x + d[j][3] * c1.y;
+            dn[3] = -d[j][2] * c1.y + d[j][3] * c1.x;
+          }
+          t[j] = 0.f;
+          if (h < nqk) {
+            const bool is_q = h < n_q;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float n = x[j][i] * rho[j];
+              if (is_q)
+                aq[i] += dn[i] * n;
+              else
+                ak[i] += dn[i] * n;
+              d[j][i] = dn[i] * (is_q ? g_q[i] : g_k[i]);  // dn * gamma
+              t[j] += n * d[j][i];
+            }
+          }
+        }
+        warp_sum4(t);
+#pragma unroll
+        for (int j = 0; j < HG; ++j) {
+          const int h = w + (k0 + j) * QKT_WARPS;
+          if (h < nqk) {
+            float dq[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float n = x[j][i] * rho[j];
+              dq[i] = rho[j] * (d[j][i] - n * t[j] * (1.f / D));
+              s += dq[i] * x[j][i];
+              dq[i] *= r;
+            }
+            store_bf16x4(Gp + row * ldg + h * D + 4 * lane, dq);
+          }
+        }
+      }
+      for (int h = w; h < n_kv; h += QKT_WARPS) {
+        const uint2 dr = *reinterpret_cast<const uint2*>(sb + o_dv + h * 2 * D + 8 * lane);
+        const uint2 vr = *reinterpret_cast<const uint2*>(sb + o_v + h * 2 * D + 8 * lane);
+        float d[4] = {bf16_lo(dr.x), bf16_hi(dr.x), bf16_lo(dr.y), bf16_hi(dr.y)};
+        const float v[4] = {bf16_lo(vr.x), bf16_hi(vr.x), bf16_lo(vr.y), bf16_hi(vr.y)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          s += d[i] * v[i];
+          d[i] *= r;
+        }
+        store_bf16x4(Gp + row * ldg + ldsave + h * D + 4 * lane, d);
+      }
+      s = warp_sum(s);
+      __syncwarp();
+      if (lane == 0) {
+        part[st][w] = s;
+        mbar_arrive(&empty[st]);  // this warp's reads of the stage are done
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      red[w][4 * lane + i] = aq[i];
+      red[w][D + 4 * lane + i] = ak[i];
+    }
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < 2 * D; j += blockDim.x) {
+    float t = 0.f;
+    for (int ww = 0; ww < QKT_WARPS; ++ww) t += red[ww][j];
+    dgam_part[static_cast<int64_t>(blockIdx.x) * 2 * D + j] = t;
+  }
+}
+
+// Bytes of one stage of qk_bwd_tma_kernel and the stages that fit.
+uint32_t qk_bwd_stage_bytes(int n_q, int n_kv) {
+  return 16 + static_cast<uint32_t>(2 * n_q + 4 * n_kv) * 2 * 128 + 64 * 8;
+}
+int qk_bwd_tma_stages(int n_q, int n_kv) {
+  const uint32_t b = qk_bwd_stage_bytes(n_q, n_kv);
+  const int st = static_cast<int>(std::min<uint32_t>(4u, (200u * 1024u) / b));
+  return st >= 2 ? st : 0;
+}
+
+cudaError_t launch_qk_bwd_tma(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, const __nv_bfloat16* dV,
+                              const __nv_bfloat16* qk_save, const __nv_bfloat16* V, const float* gq,
+                              const float* gk, const int32_t* pos, const float2* cs, int max_pos, float eps, int n_q,
+                              int n_kv, const float* rstd, int64_t M, float inv_k, __nv_bfloat16* Gp, float* coef,
+                              float* dgam_part, int nblk, int* status, cudaStream_t s, bool rope_half,
+                              uint64_t timeout_ns) {
+  const int stages = qk_bwd_tma_stages(n_q, n_kv);
+  if (stages == 0) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(stages) * qk_bwd_stage_bytes(n_q, n_kv);
+  auto k = rope_half ? qk_bwd_tma_kernel<true> : qk_bwd_tma_kernel<false>;
+  // the shared-memory limit, raised once per device and variant to the
+  // largest ring any call may use
+  static std::mutex mu;
+  static bool raised[64][2] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!raised[dev][rope_half]) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (e != cudaSuccess) return e;
+      raised[dev][rope_half] = true;
+    }
+  }
+  k<<<nblk, (QKT_WARPS + 1) * 32, smem, s>>>(dQ, dK, dV, qk_save, V, gq, gk, pos, cs, max_pos, eps, n_q, n_kv, rstd,
+                                             M, inv_k, Gp, coef, dgam_part, status, stages, timeout_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_qk_bwd(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, const __nv_bfloat16* dV,

@@ -107,6 +107,29 @@ __device__ __forceinline__ void warp_colsum_partial(float* p, int lane) {
   }
 }
 
+// The accumulator chunk of columns col0 .. col0 + 31 with the FP8 operand
+// scales applied: acc * acc_rs[row] * acc_cs[col] (columns >= N scaled by 0).
+// Without FP8 operands (both null) it is tmem_ld32.
+__device__ __forceinline__ void tmem_ld32_acc(uint32_t taddr, float (&v)[32], const EpiArgs& e, int row, bool rv,
+                                              int col0, int N) {
+  tmem_ld32(taddr, v);
+  if (e.acc_rs || e.acc_cs) {
+    const float rs = (e.acc_rs && rv) ? e.acc_rs[row] : 1.f;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float s8[8];
+      if (e.acc_cs && col0 + g * 8 < N) {
+        load_f32x8(e.acc_cs + col0 + g * 8, s8);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s8[i] = (col0 + g * 8 < N) ? 1.f : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[g * 8 + i] *= rs * s8[i];
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // PLAIN:  D = rs_i * cs_j * acc + aux0 (+ acc_in) - coef_i * aux1[g_i]
 //             - coef2_i * aux3 - sum_{t in csr(i)} w_t * aux2[t]  (+ D if beta)
@@ -124,6 +147,24 @@ struct EpiPlain {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  // Issued before the tile's accumulator is ready (while its mainloop still
+  // runs): the thread's row segments of the tile's input tiles are requested
+  // into L2, so the chunk loop's loads wait on L2 rather than on DRAM once
+  // per chunk (the last tile's epilogue has no mainloop to hide behind).
+  static __device__ __forceinline__ void prefetch(const EpiArgs& e, const TileInfo& t) {
+    const int row = t.row;
+    const int cbase = t.nb * BN;
+    if (!e.aux_prefetch || row >= t.M || cbase >= t.N) return;
+    const int cols = min(BN, t.N - cbase);
+    const int64_t arow = e.gather_rows ? e.gather_rows[row] : row;
+    if (e.aux0) prefetch_l2_span(e.aux0 + static_cast<int64_t>(row) * e.ld_aux0 + cbase, cols * 2);
+    if (e.acc_in) prefetch_l2_span(e.acc_in + static_cast<int64_t>(row) * e.ld_acc_in + cbase, cols * 4);
+    if (e.row_coef && arow >= 0) prefetch_l2_span(e.aux1 + arow * e.ld_aux1 + cbase, cols * 2);
+    if (e.row_coef2) prefetch_l2_span(e.aux3 + static_cast<int64_t>(row) * e.ld_aux3 + cbase, cols * 2);
+    if (e.beta)
+      prefetch_l2_span(static_cast<const uint8_t*>(e.D) + (static_cast<int64_t>(row) * e.ldd + cbase) * (e.d_f32 ? 4 : 2),
+                       cols * (e.d_f32 ? 4 : 2));
+  }
   static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
@@ -138,10 +179,29 @@ struct EpiPlain {
     }
     float ss = 0.f;
     const int row0 = row - static_cast<int>(threadIdx.x & 31);
+    // The residual tile (aux0) is loaded into registers one 32-column chunk
+    // ahead, so its L2 round trip overlaps the previous chunk's math and
+    // stores: with one epilogue warp per lane quarter, a load, then the
+    // math, then the stores of each chunk in turn made the epilogue of a
+    // K = 2048 tile longer than its mainloop.
+    const int64_t aoff = static_cast<int64_t>(row) * e.ld_aux0;
+    uint4 an[4];
+    auto fetch = [&](int col0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cc = col0 + q * 8;
+        an[q] = (rv && cc < t.N) ? *reinterpret_cast<const uint4*>(e.aux0 + aoff + cc) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    if (e.aux0) fetch(t.nb * BN);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int col0 = t.nb * BN + c;
       if (col0 >= t.N) break;
+      uint4 ac[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ac[q] = an[q];
+      if (e.aux0 && c + 32 < BN) fetch(col0 + 32);
       float v[32];
       __syncwarp();
       tmem_ld32(t.taddr + c, v);
@@ -161,7 +221,7 @@ struct EpiPlain {
             }
             if (e.aux0) {
               float r8[8];
-              load_bf16x8(e.aux0 + static_cast<int64_t>(row) * e.ld_aux0 + cc, r8);
+              bf16x8_to_f32(ac[g], r8);
 #pragma unroll
               for (int i = 0; i < 8; ++i) x[i] += r8[i];
             }
@@ -261,6 +321,7 @@ struct EpiSwiglu {
   static constexpr int HALF = BN / 2;
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void prefetch(const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
@@ -318,25 +379,28 @@ struct EpiDSwiglu {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void prefetch(const EpiArgs& e, const TileInfo& t) {
+    const int cbase = t.nb * BN;
+    if (!e.aux_prefetch || t.row >= t.M || cbase >= t.N) return;
+    const int bytes = min(BN, t.N - cbase) * 2;
+    prefetch_l2_span(e.aux0 + static_cast<int64_t>(t.row) * e.ld_aux0 + cbase, bytes);
+    prefetch_l2_span(e.aux1 + static_cast<int64_t>(t.row) * e.ld_aux1 + cbase, bytes);
+  }
   static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
     float dot = 0.f;
     const int row0 = row - static_cast<int>(threadIdx.x & 31);
-    // The thread's row segments of g and u for the whole tile are requested
-    // into L2 first, and each 32-column chunk's g and u are loaded into
-    // registers one chunk ahead, so that their latency overlaps the previous
-    // chunk's math and stores (at K = 4096 one round trip per chunk made
-    // this epilogue longer than the next tile's mainloop).
+    // The thread's row segments of g and u for the whole tile were requested
+    // into L2 by prefetch(), before the accumulator was ready, and each
+    // 32-column chunk's g and u are loaded into registers one chunk ahead, so
+    // that their latency overlaps the previous chunk's math and stores (at
+    // K = 4096 one round trip per chunk made this epilogue longer than the
+    // next tile's mainloop).
     const int cbase = t.nb * BN;
     const int64_t goff = static_cast<int64_t>(row) * e.ld_aux0;
     const int64_t uoff = static_cast<int64_t>(row) * e.ld_aux1;
-    if (e.aux_prefetch && rv && cbase < t.N) {
-      const int bytes = min(BN, t.N - cbase) * 2;
-      prefetch_l2_span(e.aux0 + goff + cbase, bytes);
-      prefetch_l2_span(e.aux1 + uoff + cbase, bytes);
-    }
     uint4 gn[4], un[4];  // the next chunk's g and u, raw bf16
     auto fetch = [&](int col0) {
 #pragma unroll
@@ -365,7 +429,7 @@ struct EpiDSwiglu {
       if (c + 32 < BN) fetch(col0 + 32);
       float dh[32], du[32] = {}, h[32] = {};  // rows past M keep zeros (never stored)
       __syncwarp();
-      tmem_ld32(t.taddr + c, dh);
+      tmem_ld32_acc(t.taddr + c, dh, e, row, rv, col0, t.N);
       if (rv) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -410,6 +474,7 @@ struct EpiColDot {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void prefetch(const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
@@ -478,32 +543,60 @@ struct EpiRmsDx {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  // the tile's rows of x (and dX_resid) into L2 before the accumulator is ready
+  static __device__ __forceinline__ void prefetch(const EpiArgs& e, const TileInfo& t) {
+    const int cbase = t.nb * BN;
+    if (!e.aux_prefetch || t.row >= t.M || cbase >= t.N) return;
+    const int cols = min(BN, t.N - cbase);
+    prefetch_l2_span(e.aux1 + static_cast<int64_t>(t.row) * e.ld_aux1 + cbase, cols * 2);
+    if (e.aux0) prefetch_l2_span(e.aux0 + static_cast<int64_t>(t.row) * e.ld_aux0 + cbase, cols * 2);
+  }
   static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;
     const float rc = (e.row_coef && rv) ? e.row_coef[row] : 0.f;
+    // x (aux1) and dX_resid (aux0) are loaded one 32-column chunk ahead
+    // (as the residual in EpiPlain)
+    const int64_t xoff = static_cast<int64_t>(row) * e.ld_aux1, roff = static_cast<int64_t>(row) * e.ld_aux0;
+    uint4 xn[4], rn[4];
+    auto fetch = [&](int col0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cc = col0 + q * 8;
+        const bool in = rv && cc < t.N;
+        xn[q] = in ? *reinterpret_cast<const uint4*>(e.aux1 + xoff + cc) : make_uint4(0u, 0u, 0u, 0u);
+        rn[q] = (in && e.aux0) ? *reinterpret_cast<const uint4*>(e.aux0 + roff + cc) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    fetch(t.nb * BN);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int col0 = t.nb * BN + c;
       if (col0 >= t.N) break;
+      uint4 xc[4], rcur[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        xc[q] = xn[q];
+        rcur[q] = rn[q];
+      }
+      if (c + 32 < BN) fetch(col0 + 32);
       float v[32];
       __syncwarp();
-      tmem_ld32(t.taddr + c, v);
+      tmem_ld32_acc(t.taddr + c, v, e, row, rv, col0, t.N);
       float p[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) p[i] = 0.f;
       if (rv) {
-        const int64_t off = static_cast<int64_t>(row);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int cc = col0 + g * 8;
           if (cc < t.N) {
             float x8[8], s8[8], r8[8];
-            load_bf16x8(e.aux1 + off * e.ld_aux1 + cc, x8);
+            bf16x8_to_f32(xc[g], x8);
             load_f32x8(e.col_scale + cc, s8);
-            if (e.aux0) load_bf16x8(e.aux0 + off * e.ld_aux0 + cc, r8);
+            if (e.aux0) bf16x8_to_f32(rcur[g], r8);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float d = v[g * 8 + i];
@@ -546,6 +639,7 @@ struct EpiCeLse {
       reinterpret_cast<float2*>(e.partials)[static_cast<int64_t>(t.unit_chunk) * e.ld_part + t.row] =
           make_float2(st.m, st.s);
   }
+  static __device__ __forceinline__ void prefetch(const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t) {
     const bool rv = t.row < t.M;
     const float rs = (e.row_scale && rv) ? e.row_scale[t.row] : 1.f;
@@ -555,7 +649,7 @@ struct EpiCeLse {
       if (col0 >= t.N) break;
       float z[32];
       __syncwarp();
-      tmem_ld32(t.taddr + c, z);
+      tmem_ld32_acc(t.taddr + c, z, e, t.row, rv, col0, t.N);
       if (rv) {
         if (e.row_scale) {
 #pragma unroll
@@ -609,6 +703,7 @@ struct EpiCeDlogits {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void prefetch(const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
@@ -636,7 +731,7 @@ struct EpiCeDlogits {
       if (col0 >= t.N) break;
       float z[32];
       __syncwarp();
-      tmem_ld32(t.taddr + c, z);
+      tmem_ld32_acc(t.taddr + c, z, e, row, rv, col0, t.N);
       if (rv) {
         __nv_bfloat16* d = static_cast<__nv_bfloat16*>(e.D) + static_cast<int64_t>(row) * e.ldd;
 #pragma unroll
@@ -672,6 +767,7 @@ struct EpiSigmoid {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void prefetch(const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
@@ -732,6 +828,7 @@ struct EpiQkRope {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
+  static __device__ __forceinline__ void prefetch(const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
     constexpr int D = 128;
     const int row = t.row;
@@ -758,7 +855,7 @@ struct EpiQkRope {
         for (int c = 0; c < D; c += 32) {
           float v[32];
           __syncwarp();
-          tmem_ld32(tcol + c, v);
+          tmem_ld32_acc(tcol + c, v, e, row, rv, head * D + c, t.N);
           if (rv) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= rs;
@@ -776,7 +873,7 @@ struct EpiQkRope {
       for (int c = 0; c < D; c += 32) {
         float v[32];
         __syncwarp();
-        tmem_ld32(tcol + c, v);
+        tmem_ld32_acc(tcol + c, v, e, row, rv, head * D + c, t.N);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           v[i] *= rs;
@@ -794,8 +891,8 @@ struct EpiQkRope {
         for (int c = 0; c < D / 2; c += 32) {
           float v1[32], v2[32];
           __syncwarp();
-          tmem_ld32(tcol + c, v1);
-          tmem_ld32(tcol + D / 2 + c, v2);
+          tmem_ld32_acc(tcol + c, v1, e, row, rv, head * D + c, t.N);
+          tmem_ld32_acc(tcol + D / 2 + c, v2, e, row, rv, head * D + D / 2 + c, t.N);
           if (rv) {
             float g1[32], g2[32];
 #pragma unroll
@@ -823,7 +920,7 @@ struct EpiQkRope {
         for (int c = 0; c < D; c += 32) {
           float v[32];
           __syncwarp();
-          tmem_ld32(tcol + c, v);
+          tmem_ld32_acc(tcol + c, v, e, row, rv, head * D + c, t.N);
           if (rv) {
             float gm[32];
 #pragma unroll

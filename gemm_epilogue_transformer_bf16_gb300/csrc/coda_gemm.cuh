@@ -101,13 +101,18 @@ struct EpiArgs {
   float dloss;
   int onehot;                   // CE_DLOGITS: include -w at the label column
   int st_stream;                // epilogue tile stores as streaming (.cs) stores
-  int aux_prefetch;             // DSWIGLU: request the tile's g/u rows into L2 before the chunk loop
+  int aux_prefetch;             // request the tile's auxiliary rows into L2 before its accumulator is ready
   int mode;                     // SIGMOID: 0 forward, 1 backward on the recomputed logits
   float* target_logit;
   int64_t col_base;             // CE_DLOGITS: vocabulary column of the launch's column 0 (a vocabulary slice)
   int64_t n_total;              // CE_DLOGITS: vocabulary size (0: the launch's N)
   const float* acc_in;          // PLAIN (bf16 D): fp32 tile added to the result (a running sum over slices)
   int64_t ld_acc_in;
+  // FP8 operands: the accumulator is acc * acc_rs[i] * acc_cs[j] (the two
+  // operands' per-row scales) before any epilogue math; null = 1.  PLAIN and
+  // SWIGLU take these scales through their row/column scale fields instead.
+  const float* acc_rs;
+  const float* acc_cs;
   // QK-RMSNorm + RoPE
   const int32_t* pos;
   const float2* cos_sin;
@@ -458,6 +463,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       Epi::begin(st, args.e, ti);
       for (int j = 0; j < nlen; ++j, ++t) {
         const uint32_t buf = t & 1;
+        ti.nb = nb0 + j;
+        Epi::prefetch(args.e, ti);  // the tile's auxiliary rows into L2 while its mainloop runs
         if (!mbar_wait_bounded(&tfull[buf], (t >> 1) & 1, abort_flag, args.status, args.timeout_ns,
                                args.epilogue_sleep_ns)) {
           aborted = true;

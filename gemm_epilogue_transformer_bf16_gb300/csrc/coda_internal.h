@@ -35,6 +35,18 @@ cudaError_t launch_gemm_plain_fp8(int num_units, int sms, int cg, cudaStream_t s
                                   const GemmArgs& a);
 cudaError_t launch_gemm_swiglu_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                                    const GemmArgs& a);
+cudaError_t launch_gemm_qkrope_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
+                                   const GemmArgs& a);
+cudaError_t launch_gemm_qkrope_half_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
+                                        const GemmArgs& a);
+cudaError_t launch_gemm_celse_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
+                                  const GemmArgs& a);
+cudaError_t launch_gemm_cedlogits_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
+                                      const GemmArgs& a);
+cudaError_t launch_gemm_dswiglu_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
+                                    const GemmArgs& a);
+cudaError_t launch_gemm_rmsdx_fp8(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
+                                  const GemmArgs& a);
 cudaError_t launch_gemm_rmsdx(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
                               const GemmArgs& a);
 cudaError_t launch_gemm_coldot(int num_units, int sms, int cg, cudaStream_t s, const CUtensorMap* m,
@@ -98,6 +110,11 @@ cudaError_t launch_ce_norm_coef(const float* pz, int64_t ld, int nparts, const f
                                 const float* rw, int64_t M, float inv_k, float* coef, cudaStream_t s);
 cudaError_t launch_quantize_fp8_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq,
                                      int64_t ldq, float* scale, int num_sms, cudaStream_t s);
+// e4m3 codes of the transpose of X [R, C] (with X2 [R2, C] stacked below, or
+// NULL): out [C, R + R2] (row stride ldo), per-column scales [C].
+cudaError_t launch_quantize_fp8_cols(const __nv_bfloat16* X, int64_t ldx, int64_t R, const __nv_bfloat16* X2,
+                                     int64_t ldx2, int64_t R2, int64_t C, uint8_t* out, int64_t ldo, float* scale,
+                                     int num_sms, cudaStream_t s);
 cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 cudaError_t launch_rope_table(double theta, int head_dim, int max_pos, float2* cs, cudaStream_t s);
 cudaError_t launch_qk_bwd(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, const __nv_bfloat16* dV,
@@ -105,6 +122,18 @@ cudaError_t launch_qk_bwd(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, cons
                           const int32_t* pos, const float2* cs, int max_pos, float eps, int n_q, int n_kv,
                           const float* rstd, int64_t M, float inv_k, __nv_bfloat16* Gp, float* coef,
                           float* dgam_part, int nblk, int* status, cudaStream_t s, bool rope_half = false);
+
+// The same map with its rows staged in shared memory by bulk copies (one
+// persistent block per SM, nblk <= the SM count); qk_bwd_tma_stages() is 0
+// when a row's tensors are too large for two stages, and then only
+// launch_qk_bwd applies.
+int qk_bwd_tma_stages(int n_q, int n_kv);
+cudaError_t launch_qk_bwd_tma(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, const __nv_bfloat16* dV,
+                              const __nv_bfloat16* qk_save, const __nv_bfloat16* V, const float* gq,
+                              const float* gk, const int32_t* pos, const float2* cs, int max_pos, float eps, int n_q,
+                              int n_kv, const float* rstd, int64_t M, float inv_k, __nv_bfloat16* Gp, float* coef,
+                              float* dgam_part, int nblk, int* status, cudaStream_t s, bool rope_half,
+                              uint64_t timeout_ns);
 
 constexpr int QK_BWD_WARPS = 8;
 constexpr int CE_COMBINE_THREADS = 256;

@@ -74,17 +74,6 @@ constexpr uint32_t F4_SMEM = 1024 + F4_STAGES * F4_STAGE_BYTES + F4_BAR_BYTES + 
 static_assert(F4_SMEM <= 232448, "shared memory per CTA");
 static_assert(F4_SF_COL0 + F4_STAGES * F4_SF_SLOT_COLS <= F4_TMEM_COLS, "TMEM columns");
 
-// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of
-// 16), completion counted in bytes on `bar`; issued when p != 0.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint32_t p) {
-  asm volatile(
-      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %3, 0;\n\t"
-      "@P cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%4];\n\t}" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(p), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // The same, written to the same offset in every CTA of `mask` in the
 // cluster, completion counted on each destination CTA's barrier at `bar`'s
 // offset.

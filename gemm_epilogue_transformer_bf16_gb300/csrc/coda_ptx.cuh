@@ -104,6 +104,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
 }
 
 // L2 eviction-priority policies for the TMA loads below.
+// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of
+// 16), completion counted in bytes on `bar`; issued when p != 0.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint32_t p) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %3, 0;\n\t"
+      "@P cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%4];\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(p), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));

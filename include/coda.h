@@ -138,7 +138,19 @@ typedef struct coda_epilogue_desc {
   coda_bf16* K;                  /* [M, n_kv*head_dim] */
   coda_bf16* V;                  /* [M, n_kv*head_dim] */
   int32_t rope_pairing;          /* coda_rope_pairing (0 = interleaved) */
+  /* Operand type.  CODA_OPERAND_E4M3: A, B (and A2, B2) are e4m3 bytes,
+   * K-major, K a multiple of 16, and the accumulator is dequantised as
+   * acc[i, j] * acc_row_scale[i] * acc_col_scale[j] (each NULL = 1) before
+   * the map runs -- the two operands' per-row scales of
+   * coda_quantize_fp8_rows / coda_quantize_fp8_cols.  MAP_NONE and
+   * MAP_SWIGLU take those scales in row_scale / col_scale instead. */
+  int32_t operand_type;          /* CODA_OPERAND_BF16 (0) or CODA_OPERAND_E4M3 (1) */
+  const float* acc_row_scale;    /* [M] or NULL */
+  const float* acc_col_scale;    /* [N] or NULL */
 } coda_epilogue_desc;
+
+/* Operand element type of coda_epilogue_desc.operand_type. */
+enum { CODA_OPERAND_BF16 = 0, CODA_OPERAND_E4M3 = 1 };
 
 /* ------------------------------------------------------------------------
  * Library / device status
@@ -440,6 +452,83 @@ int coda_linear_swiglu_fp8(const uint8_t* Xq, const float* sx, const float* rstd
                            const float* sg, const uint8_t* Wuq, const float* su, coda_bf16* H, coda_bf16* g_save,
                            coda_bf16* u_save, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
                            coda_stream stream);
+
+/* X [R, C] bf16 (row stride ldx), with X2 [R2, C] (row stride ldx2) stacked
+ * below it when given -> XTq [C, R + R2] e4m3 (row stride ldo >= R + R2, a
+ * multiple of 16), scale [C] fp32: scale_c = max over the column of |x| /
+ * 448, codes of x / scale_c (the row rule along columns).  This is the
+ * K-major operand of a GEMM that contracts over X's rows, e.g. the W^T of a
+ * backward GEMM dX = G W: coda_quantize_fp8_cols(W) gives W^T quantised per
+ * input feature.  C % 8 == 0 and (R + R2) % 16 == 0.  `scale` also serves as
+ * scratch for the column maxima (no workspace). */
+int coda_quantize_fp8_cols(const coda_bf16* X, int64_t ldx, int64_t R, const coda_bf16* X2, int64_t ldx2,
+                           int64_t R2, int64_t C, uint8_t* XTq, int64_t ldo, float* scale, coda_stream stream);
+
+/* linear_qknorm_rope on e4m3 operands: [q | k | v] = r ⊙ ((sx ⊙ Xq)(sw ⊙ Wq)^T),
+ * then per head RMSNorm + RoPE as in coda_linear_qknorm_rope (same layouts,
+ * gains, positions, table, pairing and outputs).  Xq [M, Kdim], sx [M],
+ * Wq [(n_q+2n_kv)*128, Kdim], sw [(n_q+2n_kv)*128]; Kdim % 16 == 0. */
+size_t coda_linear_qknorm_rope_fp8_workspace_size(int64_t M, int64_t Kdim, int32_t n_q, int32_t n_kv,
+                                                  int32_t head_dim);
+int coda_linear_qknorm_rope_fp8(const uint8_t* Xq, const float* sx, const float* rstd, const uint8_t* Wq,
+                                const float* sw, const float* gamma_q, const float* gamma_k, const int32_t* pos,
+                                const float* cos_sin, int32_t max_pos, float eps, int32_t n_q, int32_t n_kv,
+                                int32_t head_dim, int32_t rope_pairing, coda_bf16* Q, coda_bf16* K, coda_bf16* V,
+                                coda_bf16* qk_save, int64_t M, int64_t Kdim, void* ws, size_t ws_bytes,
+                                coda_stream stream);
+
+/* linear_cross_entropy on e4m3 operands: z = (sx ⊙ Xq)(sw ⊙ Wq)^T, then the
+ * online log-sum-exp and loss of coda_linear_cross_entropy (same outputs and
+ * label rules).  Xq [M, K], sx [M], Wq [V, K], sw [V]; K % 16 == 0. */
+size_t coda_linear_cross_entropy_fp8_workspace_size(int64_t M, int64_t V, int64_t K);
+int coda_linear_cross_entropy_fp8(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw,
+                                  const int32_t* labels, int32_t ignore_index, float* loss_mean, float* lse,
+                                  int32_t* n_valid, int64_t M, int64_t V, int64_t K, void* ws, size_t ws_bytes,
+                                  coda_stream stream);
+
+/* Its backward: the softmax gradient dZ = (softmax(z) - onehot) * dloss /
+ * n_valid at the logits z of the e4m3 operands (recomputed, by vocabulary
+ * slices as in coda_linear_cross_entropy_bwd), then dX = dZ W and
+ * dW = dZ^T X in bf16 GEMMs with the bf16 operands X [M, K], W [V, K]
+ * (softmax probabilities of a 128k vocabulary lie far below e4m3's range,
+ * so the gradient GEMMs keep dZ in bf16). */
+size_t coda_linear_cross_entropy_bwd_fp8_workspace_size(int64_t M, int64_t V, int64_t K);
+int coda_linear_cross_entropy_bwd_fp8(const uint8_t* Xq, const float* sx, const uint8_t* Wq, const float* sw,
+                                      const coda_bf16* X, const coda_bf16* W, const int32_t* labels,
+                                      int32_t ignore_index, const float* lse, const int32_t* n_valid, float dloss,
+                                      coda_bf16* dX, coda_bf16* dW, int64_t M, int64_t V, int64_t K, void* ws,
+                                      size_t ws_bytes, coda_stream stream);
+
+/* The first GEMM of the SwiGLU MLP backward on e4m3 operands, with the
+ * dSwiGLU pairwise map in its epilogue:
+ *   dH = (sdy ⊙ dYq)(swd ⊙ WdTq)^T   (dY Wd; WdTq = coda_quantize_fp8_cols(Wd)),
+ *   dG = dH ⊙ u ⊙ silu'(g),  dU = dH ⊙ silu(g),
+ *   Gp [M, 2I] = r ⊙ [dG | dU] bf16 (r = rstd, or 1 when NULL),
+ *   dot [M] fp32 = sum_j (dG g + dU u)_ij (or NULL), H [M, I] = silu(g) ⊙ u
+ *   (or NULL).
+ * dYq [M, K], sdy [M], WdTq [I, K], swd [I]; g, u [M, I] the forward's saved
+ * projections; K % 16 == 0.  dot feeds the RMSNorm-backward coefficient
+ * c_i = r_i^2 dot_i / K of the dX GEMM (coda_rmsnorm_linear_dx_fp8). */
+size_t coda_linear_dswiglu_fp8_workspace_size(int64_t M, int64_t I, int64_t K);
+int coda_linear_dswiglu_fp8(const uint8_t* dYq, const float* sdy, const uint8_t* WdTq, const float* swd,
+                            const coda_bf16* g, const coda_bf16* u, const float* rstd, coda_bf16* Gp, float* dot,
+                            coda_bf16* H, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
+                            coda_stream stream);
+
+/* The input gradient of an RMSNorm-reparameterised projection
+ * y = r ⊙ ((X ⊙ gamma) W^T) on e4m3 operands, with the RMSNorm backward in
+ * its epilogue:
+ *   D = (sg ⊙ Gq)(sw ⊙ WTq)^T   (G' W; WTq = coda_quantize_fp8_cols(W)),
+ *   dX = gamma ⊙ D - coef ⊙ X (+ dX_resid),  dgamma_k = sum_i X_ik D_ik.
+ * Gq [M, N] (G' = r ⊙ G quantised per row), sg [M], WTq [K, N], sw [K],
+ * X [M, K], gamma [K], coef [M] (c_i = r_i^2 sum_n G_in y_in / K),
+ * dX_resid [M, K] or NULL; outputs dX [M, K] bf16, dgamma [K] fp32.
+ * N % 16 == 0. */
+size_t coda_rmsnorm_linear_dx_fp8_workspace_size(int64_t M, int64_t N, int64_t K);
+int coda_rmsnorm_linear_dx_fp8(const uint8_t* Gq, const float* sg, const uint8_t* WTq, const float* sw,
+                               const coda_bf16* X, const float* gamma, const float* coef, const coda_bf16* dX_resid,
+                               coda_bf16* dX, float* dgamma, int64_t M, int64_t N, int64_t K, void* ws,
+                               size_t ws_bytes, coda_stream stream);
 
 /* ------------------------------------------------------------------------
  * NVFP4 operands: 4-bit e2m1 elements, one e4m3 scale per 16 consecutive

@@ -38,7 +38,8 @@ def main():
     rf, rb = O.block_fwd(o, **cfg), O.block_bwd(o, **cfg)
     for k in ("Q", "K", "V", "x1", "x2"):
         assert_bf16(f[k], rf[k], k)
-    for k in ("dx0", "dA", "dWqkv", "dWo", "dWg", "dWu", "dWd", "dgamma_attn", "dgamma_mlp"):
+    for k in ("dx0", "dA", "dWqkv", "dWo", "dWg", "dWu", "dWd", "dgamma_attn", "dgamma_mlp", "dgamma_q",
+              "dgamma_k"):
         assert_bf16(g[k], rb[k], k)
     # FP8 linear + residual on an M that spans several cluster sizes' tiles
     M, N, K = 700, 520, 256

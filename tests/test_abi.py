@@ -61,10 +61,11 @@ def test_epilogue_desc_layout_matches_header():
 #include <stddef.h>
 #include "coda.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(coda_epilogue_desc), offsetof(coda_epilogue_desc, partials),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(coda_epilogue_desc), offsetof(coda_epilogue_desc, partials),
          offsetof(coda_epilogue_desc, K2), offsetof(coda_epilogue_desc, dloss),
          offsetof(coda_epilogue_desc, eps), offsetof(coda_epilogue_desc, V),
-         offsetof(coda_epilogue_desc, rope_pairing));
+         offsetof(coda_epilogue_desc, rope_pairing), offsetof(coda_epilogue_desc, operand_type),
+         offsetof(coda_epilogue_desc, acc_col_scale));
   return 0;
 }
 '''
@@ -76,7 +77,7 @@ int main(void) {
         got = [int(x) for x in subprocess.check_output([exe]).split()]
     D = coda.EpilogueDesc
     want = [ctypes.sizeof(D), D.partials.offset, D.K2.offset, D.dloss.offset, D.eps.offset, D.V.offset,
-            D.rope_pairing.offset]
+            D.rope_pairing.offset, D.operand_type.offset, D.acc_col_scale.offset]
     assert got == want
 
 

@@ -1,0 +1,132 @@
+"""GPU parity of the FP8 (e4m3) instances of the epilogues against the fp64
+oracle on the dequantised operands: QKV + QK-norm + RoPE (both pairings),
+linear + cross-entropy forward and backward (vocabularies of one and of
+three backward slices), dSwiGLU on the dH GEMM and the RMSNorm-reparameterised
+input gradient, and the column quantiser that gives the backward GEMMs their
+K-major transposed operands.
+
+Quantisation codes and scales are decisions: the GPU quantisers are checked
+bit for bit against the oracle's, and each operator then runs on the codes
+that both sides computed from the same bf16 input.  Shapes span several
+tiles with ragged tails."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import coda_oracle as O
+from parity import assert_bf16, assert_f32, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def coda():
+    import gemm_epilogue_transformer_bf16_gb300 as c
+    from gemm_epilogue_transformer_bf16_gb300 import _build
+    _build.build()
+    c.load()
+    return c
+
+
+def _rows(coda, X):
+    """GPU row quantisation, checked bit for bit against the oracle's;
+    returns (device codes, device scales, oracle values, oracle scales)."""
+    q, s = coda.quantize_fp8_rows(X.to(DEV))
+    oc, ov, osc = O.quantize_fp8_rows(to_np(X))
+    assert np.array_equal(q.cpu().numpy(), oc) and np.array_equal(s.cpu().numpy(), osc)
+    return q, s, ov, osc
+
+
+def _cols(coda, X, X2=None):
+    q, s = coda.quantize_fp8_cols(X.to(DEV), None if X2 is None else X2.to(DEV))
+    full = to_np(X) if X2 is None else np.vstack([to_np(X), to_np(X2)])
+    oc, ov, osc = O.quantize_fp8_cols(full)
+    assert np.array_equal(q.cpu().numpy(), oc) and np.array_equal(s.cpu().numpy(), osc)
+    return q, s, ov, osc
+
+
+@pytest.mark.parametrize("R,R2,C", [(304, 0, 264), (256, 48, 520), (8192, 0, 128)])
+def test_quantize_fp8_cols(coda, R, R2, C):
+    X = synth.randn_bf16((R, C), 1.0, 31)
+    X[:, 3] = 0                                   # an all-zero column: scale 1, zero codes
+    X2 = synth.randn_bf16((R2, C), 3.0, 32) if R2 else None
+    _cols(coda, X, X2)
+
+
+@pytest.mark.parametrize("pairing", ["interleaved", "half"])
+def test_linear_qknorm_rope_fp8(coda, pairing):
+    M, Kd, n_q, n_kv, d = 300, 272, 2, 1, 128
+    X = synth.randn_bf16((M, Kd), 1.0, 41)
+    W = synth.randn_bf16(((n_q + 2 * n_kv) * d, Kd), 1 / math.sqrt(Kd), 42)
+    gq, gk = synth.gain_f32(d, 43), synth.gain_f32(d, 44)
+    rstd = (0.5 + torch.rand(M, generator=torch.Generator().manual_seed(45))).float()
+    pos = (torch.arange(M, dtype=torch.int32) * 7) % 1024
+    cs = coda.rope_table(500000.0, d, 1024)
+    xq, sx, xv, osx = _rows(coda, X)
+    wq, sw, wv, osw = _rows(coda, W)
+    out = coda.linear_qknorm_rope_fp8(xq, sx, wq, sw, gq.to(DEV), gk.to(DEV), pos.to(DEV), cs, n_q, n_kv,
+                                      rstd=rstd.to(DEV), pairing=pairing)
+    f = O.linear_qknorm_rope_fp8_fwd(xv, osx, wv, osw, to_np(gq), to_np(gk), pos.numpy(), 500000.0, 1e-6, n_q,
+                                     n_kv, d, row_scale=to_np(rstd), pairing=pairing)
+    for k, ref in (("Q", f["Q"]), ("K", f["K"]), ("V", f["V"]), ("qk_save", f["qk"])):
+        assert_bf16(out[k], ref, f"fp8 {k}")
+
+
+@pytest.mark.parametrize("shape", [synth.CeShape(300, 144, 8200), synth.CeShape(260, 128, 40008)])
+def test_linear_cross_entropy_fp8(coda, shape):
+    t = synth.make_ce(shape, seed=4)
+    lab = t["labels"].clone()
+    lab[1], lab[2] = 0, shape.vocab - 1
+    if shape.vocab > 16384:
+        lab[3], lab[4] = 16383, 16384
+    xq, sx, xv, osx = _rows(coda, t["X"])
+    wq, sw, wv, osw = _rows(coda, t["W"])
+    d = {k: v.to(DEV) for k, v in t.items()}
+    out = coda.linear_cross_entropy_fp8(xq, sx, wq, sw, lab.to(DEV))
+    f = O.linear_cross_entropy_fp8_fwd(xv, osx, wv, osw, lab.numpy())
+    assert coda.get_status(out["ws"]) == 0
+    assert int(out["n_valid"].item()) == f["n_valid"]
+    assert_f32(out["lse"], f["lse"], "fp8 lse")
+    assert_f32(out["loss"], [f["loss"]], "fp8 loss")
+    g = coda.linear_cross_entropy_bwd_fp8(xq, sx, wq, sw, d["X"], d["W"], lab.to(DEV), out["lse"], out["n_valid"],
+                                          0.8)
+    b = O.linear_cross_entropy_fp8_bwd(xv, osx, wv, osw, to_np(t["X"]), to_np(t["W"]), lab.numpy(), dloss=0.8)
+    assert coda.get_status(g["ws"]) == 0
+    assert_bf16(g["dX"], b["dX"], "fp8 CE dX")
+    assert_bf16(g["dW"], b["dW"], "fp8 CE dW")
+
+
+def test_linear_dswiglu_fp8(coda):
+    M, K, I = 300, 272, 392
+    dY = synth.randn_bf16((M, K), 1.0, 51)
+    Wd = synth.randn_bf16((K, I), 1 / math.sqrt(I), 52)
+    g = synth.randn_bf16((M, I), 1.5, 53)
+    u = synth.randn_bf16((M, I), 1.0, 54)
+    rstd = (0.5 + torch.rand(M, generator=torch.Generator().manual_seed(55))).float()
+    dyq, sdy, dyv, osdy = _rows(coda, dY)
+    wdq, swd, wdv, oswd = _cols(coda, Wd)
+    out = coda.linear_dswiglu_fp8(dyq, sdy, wdq, swd, g.to(DEV), u.to(DEV), rstd=rstd.to(DEV), want_H=True)
+    r = O.dswiglu_fp8(dyv, osdy, wdv, oswd, to_np(g), to_np(u), row_scale=to_np(rstd))
+    assert_bf16(out["Gp"], r["Gp"], "fp8 G' = r [dG | dU]")
+    assert_bf16(out["H"], r["H"], "fp8 dSwiGLU H")
+    assert_bf16(out["dot"], r["dot"], "fp8 dSwiGLU row dot")
+
+
+def test_rmsnorm_linear_dx_fp8(coda):
+    M, N, K = 300, 400, 272
+    Gp = synth.randn_bf16((M, N), 1.0, 61)
+    W = synth.randn_bf16((N, K), 1 / math.sqrt(K), 62)
+    X = synth.randn_bf16((M, K), 1.0, 63)
+    R = synth.randn_bf16((M, K), 1.0, 64)
+    gam = synth.gain_f32(K, 65)
+    coef = (0.1 * torch.randn(M, generator=torch.Generator().manual_seed(66))).float()
+    gq, sg, gv, osg = _rows(coda, Gp)
+    wq, sw, wv, osw = _cols(coda, W)
+    out = coda.rmsnorm_linear_dx_fp8(gq, sg, wq, sw, X.to(DEV), gam.to(DEV), coef.to(DEV), dX_resid=R.to(DEV))
+    r = O.rmsnorm_linear_dx_fp8(gv, osg, wv, osw, to_np(X), to_np(gam), to_np(coef), dX_resid=to_np(R))
+    assert_bf16(out["dX"], r["dX"], "fp8 RMSNorm dX")
+    assert_bf16(out["dgamma"], r["dgamma"], "fp8 RMSNorm dgamma")
