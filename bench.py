@@ -55,9 +55,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-unfused", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--legs", default="swiglu,rms,mlp,ce,fp8,nvfp4",
+    p.add_argument("--legs", default="swiglu,rms,mlp,ce,fp8,fp8block,nvfp4",
                    help="other workloads to time after the block step (comma list of swiglu, rms, mlp, ce, fp8, "
-                        "nvfp4; empty for none)")
+                        "fp8block, nvfp4; none for none)")
     p.add_argument("--no-block", action="store_true", help="skip the block step (profiling of the other legs)")
     p.add_argument("--serial", action="store_true", help="run the step's calls on one stream")
     p.add_argument("--fold-weights", action="store_true",
@@ -724,7 +724,7 @@ def main():
         unfused_leg(other["linear_cross_entropy"], ce_unfused, mf + mb)
         del dc, Xr, Wr
 
-    if "fp8" in legs or "nvfp4" in legs:
+    if "fp8" in legs or "nvfp4" in legs or "fp8block" in legs:
         T_, H_, I_ = s.tokens, s.hidden, s.inter
         x0_ = {k: t[k] for k in ("x0", "Wg", "Wu")}
         r_ = coda.rms_rstd(x0_["x0"], s.eps)
@@ -779,8 +779,7 @@ def main():
         Gp8 = torch.empty(T_, 2 * I_, dtype=torch.bfloat16, device=dev)
         gq_, sgq_ = torch.empty(T_, 2 * I_, dtype=torch.uint8, device=dev), torch.empty(T_, dtype=torch.float32,
                                                                                        device=dev)
-        dot8 = torch.empty(T_, dtype=torch.float32, device=dev)
-        coef8 = torch.zeros(T_, dtype=torch.float32, device=dev)
+        coef8 = torch.empty(T_, dtype=torch.float32, device=dev)
         dx8 = {"dX": torch.empty(T_, H_, dtype=torch.bfloat16, device=dev),
                "dgamma": torch.empty(H_, dtype=torch.float32, device=dev)}
         ws_ds = coda.workspace(coda.load().coda_linear_dswiglu_fp8_workspace_size(T_, I_, H_), dev)
@@ -788,7 +787,7 @@ def main():
 
         def fp8_dgrad(mark):
             coda.linear_dswiglu_fp8(dyq, sdy, wdt_q, swdt, gq8, uq8, rstd=r_,
-                                    out={"Gp": Gp8, "dot": dot8, "H": None}, ws=ws_ds)
+                                    out={"Gp": Gp8, "row": coef8, "H": None}, ws=ws_ds)
             mark()
             coda.quantize_fp8_rows(Gp8, Xq=gq_, scale=sgq_)
             mark()
@@ -807,6 +806,31 @@ def main():
             "weight_quant_ms": {"Wd^T": round(mwd, 4), "[Wg;Wu]^T": round(mwgu, 4)}}
         del wdt_q, wgut_q, dyq, Gp8, gq_, ws_ds, ws_dx, dx8
         del xq, gq, uq
+    if "fp8block" in legs:
+        # the whole block step with the FP8 GEMMs (BlockFP8): forward
+        # projections and the MLP / O-projection input gradients on e4m3
+        # operands, weights quantised every step inside the step
+        from gemm_epilogue_transformer_bf16_gb300.block import BlockFP8
+        b8 = BlockFP8(s, t, device=dev)
+        args8 = (t["x0"], t["A"], t["pos"], t["dx2"], t["dQ"], t["dK"], t["dV"])
+
+        def fp8_step(mark):
+            b8.step(*args8, mark=lambda name: mark())
+        n8 = max(10, min(args.steps, 30))
+        mq8, mf8, mb8 = median_ms(fp8_step, n=n8, warm=3, parts=3)
+        if coda.get_status(b8.ws) != 0 or coda.get_status(b8.ws2) != 0:
+            raise RuntimeError("device status error in the FP8 block measurement")
+        f_blk = sum(b8.gemm_flops().values())
+        m8 = mq8 + mf8 + mb8
+        other["fp8_block"] = {
+            "workload": "the block step (tokens 8192, hidden 8192) with e4m3 forward projections and MLP / "
+                        "O-projection input-gradient GEMMs, weights quantised inside the step; weight gradients "
+                        "and the QKV backward in bf16",
+            "ms": round(m8, 4), "tflops": rate(f_blk, m8), "quantize_weights_ms": round(mq8, 4),
+            "fwd_ms": round(mf8, 4), "bwd_ms": round(mb8, 4),
+            "bf16_block_ms": round(blk_res["median_step"], 4) if blk_res else None,
+            "speedup_vs_bf16_block": round(blk_res["median_step"] / m8, 3) if blk_res else None}
+        del b8
     if "nvfp4" in legs:
         # NVFP4 (e2m1 + e4m3 block scales) gate/up + SwiGLU at the same shape:
         # the block-scaled kind::mxf4nvf4 mainloop, single CTAs
@@ -826,7 +850,7 @@ def main():
             "peak": round(fp4_peak, 1), "peak_kind": f"fp4 = 6 x bf16 burst ({peak_src}, nominal ratio)",
             "frac": round(rate(f_gu, m4) / fp4_peak, 4), "quantize_x_ms": round(mq4, 4)}
         del xq4, gq4, uq4, sfx4, sfg4, sfu4
-    if "fp8" in legs or "nvfp4" in legs:
+    if "fp8" in legs or "nvfp4" in legs or "fp8block" in legs:
         del Hq, gq8, uq8, x0_
 
     # ---------------------------------------------------------------- CPU oracle baseline

@@ -636,23 +636,24 @@ def linear_cross_entropy_bwd_fp8(Xq, sx, Wq, sw, X, W, labels, lse, n_valid, dlo
     return out
 
 
-def linear_dswiglu_fp8(dYq, sdy, WdTq, swd, g, u, rstd=None, want_dot=True, want_H=False, out=None, ws=None,
+def linear_dswiglu_fp8(dYq, sdy, WdTq, swd, g, u, rstd=None, want_row=True, want_H=False, out=None, ws=None,
                        stream=None):
     """dH GEMM on e4m3 operands with the dSwiGLU epilogue
     (coda_linear_dswiglu_fp8): returns {"Gp": [M, 2I] = r [dG | dU],
-    "dot": [M] or None, "H": [M, I] or None}."""
+    "row": [M] (with rstd the RMSNorm-backward coefficient c, else the row
+    sum) or None, "H": [M, I] or None}."""
     lib = load()
     M, K = dYq.shape
     I = WdTq.shape[0]
     dev = dYq.device
     if out is None:
         out = {"Gp": torch.empty(M, 2 * I, dtype=torch.bfloat16, device=dev),
-               "dot": torch.empty(M, dtype=torch.float32, device=dev) if want_dot else None,
+               "row": torch.empty(M, dtype=torch.float32, device=dev) if want_row else None,
                "H": torch.empty(M, I, dtype=torch.bfloat16, device=dev) if want_H else None}
     ws = _ws(ws, lib.coda_linear_dswiglu_fp8_workspace_size(M, I, K), dev)
     _check("coda_linear_dswiglu_fp8", lib.coda_linear_dswiglu_fp8(
         _u8(dYq, "dYq"), _f32(sdy, "sdy"), _u8(WdTq, "WdTq"), _f32(swd, "swd"), _bf(g, "g"), _bf(u, "u"),
-        _f32(rstd, "rstd"), _bf(out["Gp"], "Gp"), _f32(out.get("dot"), "dot"), _bf(out.get("H"), "H"), M, I, K,
+        _f32(rstd, "rstd"), _bf(out["Gp"], "Gp"), _f32(out.get("row"), "row"), _bf(out.get("H"), "H"), M, I, K,
         _ptr(ws), ws.numel(), _stream(stream)))
     return out
 

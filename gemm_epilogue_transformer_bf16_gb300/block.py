@@ -43,9 +43,11 @@ from __future__ import annotations
 
 import torch
 
-from . import (fold_gamma, linear_cross_entropy, linear_cross_entropy_bwd, linear_qknorm_rope,
-               linear_qknorm_rope_bwd, linear_residual, linear_residual_bwd, linear_swiglu, linear_swiglu_bwd,
-               load, rms_rstd, rmsnorm_scale, rope_table, workspace)
+from . import (K_MAJOR, MN_MAJOR, EpilogueDesc, fold_gamma, gemm_epilogue, linear_cross_entropy,
+               linear_cross_entropy_bwd, linear_dswiglu_fp8, linear_fp8, linear_qknorm_rope, linear_qknorm_rope_bwd,
+               linear_qknorm_rope_fp8, linear_residual, linear_residual_bwd, linear_swiglu, linear_swiglu_bwd,
+               linear_swiglu_fp8, load, quantize_fp8_cols, quantize_fp8_rows, rms_rstd, rmsnorm_linear_dx_fp8,
+               rmsnorm_scale, rope_table, workspace)
 
 
 class Block:
@@ -181,6 +183,154 @@ class Block:
                 "dWqkv": self.grads_qkv["dW"], "dWo": self.grads_o["dW"], "dWg": self.grads_mlp["dWg"],
                 "dWu": self.grads_mlp["dWu"], "dWd": self.grads_mlp["dWd"],
                 "dgamma_attn": self.grads_qkv["dgamma_in"], "dgamma_mlp": self.grads_mlp["dgamma"],
+                "dgamma_q": self.grads_qkv["dgamma_q"], "dgamma_k": self.grads_qkv["dgamma_k"]}
+
+    def step(self, x0, A, pos, dx2, dQ, dK, dV, mark=None):
+        self.forward(x0, A, pos, mark)
+        return self.backward(x0, A, pos, dx2, dQ, dK, dV, mark)
+
+
+class BlockFP8:
+    """The same block step with the GEMMs that have e4m3 instances on e4m3
+    operands: the forward projections (QKV + QK-norm + RoPE, O-projection +
+    residual, gate/up + SwiGLU, down + residual) and the input-gradient
+    GEMMs of the MLP (dH with the dSwiGLU epilogue, dX with the
+    RMSNorm-backward epilogue) and of the O-projection (dA).  Activations are
+    quantised per token and weights per output row (forward) or per input
+    column (backward, transposed by the column quantiser) every step, since
+    the weights change every step; weight gradients and the QKV backward
+    stay bf16.  The O-projection's output x1 goes through the RMSNorm scale
+    pass for r1 and u1 (the bf16 block gets them from its epilogue)."""
+
+    def __init__(self, shape, weights, device="cuda", concurrent=True):
+        self.s = s = shape
+        self.w = w = weights
+        lib = load()
+        T, Hd, I, d = s.tokens, s.hidden, s.inter, s.head_dim
+        nqkv, a_in = s.qkv_out, s.n_q * s.head_dim
+        bf = dict(dtype=torch.bfloat16, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        u8 = dict(dtype=torch.uint8, device=device)
+        e = torch.empty
+        self.device = device
+
+        def q(rows, cols):
+            return (e(rows, cols, **u8), e(rows, **f32))
+        # weights: forward (per output row) and backward (per input column, transposed)
+        self.Wqkv_q, self.Wo_q, self.Wg_q, self.Wu_q, self.Wd_q = (q(nqkv, Hd), q(Hd, a_in), q(I, Hd), q(I, Hd),
+                                                                   q(Hd, I))
+        self.WdT_q, self.WguT_q, self.WoT_q = q(I, Hd), q(Hd, 2 * I), q(a_in, Hd)
+        # activations
+        self.U0, self.U1 = e(T, Hd, **bf), e(T, Hd, **bf)
+        self.U0_q, self.A_q, self.U1_q, self.H_q = q(T, Hd), q(T, a_in), q(T, Hd), q(T, I)
+        self.dx2_q, self.G_q, self.dx1_q = q(T, Hd), q(T, 2 * I), q(T, Hd)
+        self.cos_sin = rope_table(s.theta, d, s.seq_len, device=device)
+        self.rstd0, self.rstd1, self.coef1 = e(T, **f32), e(T, **f32), e(T, **f32)
+        self.fwd = {"Q": e(T, s.n_q * d, **bf), "K": e(T, s.n_kv * d, **bf), "V": e(T, s.n_kv * d, **bf),
+                    "qk_save": e(T, (s.n_q + s.n_kv) * d, **bf)}
+        self.x1, self.x2 = e(T, Hd, **bf), e(T, Hd, **bf)
+        self.H, self.g, self.u = e(T, I, **bf), e(T, I, **bf), e(T, I, **bf)
+        self.Gp = e(T, 2 * I, **bf)
+        self.dx1 = {"dX": e(T, Hd, **bf), "dgamma": e(Hd, **f32)}
+        self.dA = e(T, a_in, **bf)
+        self.dW = {"dWg": e(I, Hd, **bf), "dWu": e(I, Hd, **bf), "dWd": e(Hd, I, **bf), "dWo": e(Hd, a_in, **bf)}
+        self.grads_qkv = {"dX": e(T, Hd, **bf), "dW": e(nqkv, Hd, **bf), "dgamma_in": e(Hd, **f32),
+                          "dgamma_q": e(d, **f32), "dgamma_k": e(d, **f32)}
+        need = max(lib.coda_linear_qknorm_rope_fp8_workspace_size(T, Hd, s.n_q, s.n_kv, d),
+                   lib.coda_linear_fp8_workspace_size(T, Hd, a_in), lib.coda_linear_swiglu_fp8_workspace_size(T, I, Hd),
+                   lib.coda_linear_dswiglu_fp8_workspace_size(T, I, Hd),
+                   lib.coda_rmsnorm_linear_dx_fp8_workspace_size(T, 2 * I, Hd),
+                   lib.coda_linear_qknorm_rope_bwd_workspace_size(T, Hd, s.n_q, s.n_kv, d),
+                   lib.coda_gemm_epilogue_workspace_size())
+        self.ws = workspace(need, device)
+        self.s2 = torch.cuda.Stream(device=device) if concurrent else None
+        self.ws2 = workspace(need, device) if concurrent else self.ws
+
+    LAUNCHES = {"quant_w": 14, "fwd": 12, "bwd": 20}
+
+    def launches(self):
+        return self.LAUNCHES
+
+    def gemm_flops(self):
+        return Block.gemm_flops(self)
+
+    def _side(self):
+        return Block._side(self)
+
+    def _join(self):
+        Block._join(self)
+
+    def quantize_weights(self):
+        """The step's e4m3 copies of the weights (they change every step)."""
+        w = self.w
+        for src, dst in ((w["Wqkv"], self.Wqkv_q), (w["Wo"], self.Wo_q), (w["Wg"], self.Wg_q), (w["Wu"], self.Wu_q),
+                         (w["Wd"], self.Wd_q)):
+            quantize_fp8_rows(src, Xq=dst[0], scale=dst[1])
+        quantize_fp8_cols(w["Wd"], XTq=self.WdT_q[0], scale=self.WdT_q[1])
+        quantize_fp8_cols(w["Wg"], w["Wu"], XTq=self.WguT_q[0], scale=self.WguT_q[1])
+        quantize_fp8_cols(w["Wo"], XTq=self.WoT_q[0], scale=self.WoT_q[1])
+
+    def _wgrad(self, A, lda, B, ldb, D, M, N, K, col_scale=None, ws=None):
+        """D [M, N] = A^T B (A stored [K, M], B stored [K, N]) in bf16, with an
+        optional column scale: the weight-gradient GEMMs."""
+        d = EpilogueDesc()
+        if col_scale is not None:
+            d.col_scale = col_scale.data_ptr()
+        gemm_epilogue(d, A, B, D, M, N, K, a_major=MN_MAJOR, b_major=MN_MAJOR, lda=lda, ldb=ldb, ws=ws)
+
+    def forward(self, x0, A, pos, mark=None):
+        s, w = self.s, self.w
+        mark = mark or (lambda name: None)
+        self.quantize_weights()
+        mark("quant_w")
+        rmsnorm_scale(x0, w["gamma_attn"], s.eps, rstd=self.rstd0, U=self.U0)
+        quantize_fp8_rows(self.U0, Xq=self.U0_q[0], scale=self.U0_q[1])
+        linear_qknorm_rope_fp8(self.U0_q[0], self.U0_q[1], self.Wqkv_q[0], self.Wqkv_q[1], w["gamma_q"],
+                               w["gamma_k"], pos, self.cos_sin, s.n_q, s.n_kv, rstd=self.rstd0, eps=s.eps,
+                               head_dim=s.head_dim, out=self.fwd, ws=self.ws)
+        quantize_fp8_rows(A, Xq=self.A_q[0], scale=self.A_q[1])
+        linear_fp8(self.A_q[0], self.A_q[1], self.Wo_q[0], self.Wo_q[1], R=x0, Y=self.x1, ws=self.ws)
+        rmsnorm_scale(self.x1, w["gamma_mlp"], s.eps, rstd=self.rstd1, U=self.U1)
+        quantize_fp8_rows(self.U1, Xq=self.U1_q[0], scale=self.U1_q[1])
+        linear_swiglu_fp8(self.U1_q[0], self.U1_q[1], self.Wg_q[0], self.Wg_q[1], self.Wu_q[0], self.Wu_q[1],
+                          rstd=self.rstd1, H=self.H, g=self.g, u=self.u, ws=self.ws)
+        quantize_fp8_rows(self.H, Xq=self.H_q[0], scale=self.H_q[1])
+        linear_fp8(self.H_q[0], self.H_q[1], self.Wd_q[0], self.Wd_q[1], R=self.x1, Y=self.x2, ws=self.ws)
+        mark("fwd")
+        return {"Q": self.fwd["Q"], "K": self.fwd["K"], "V": self.fwd["V"], "x1": self.x1, "x2": self.x2}
+
+    def backward(self, x0, A, pos, dx2, dQ, dK, dV, mark=None):
+        s, w = self.s, self.w
+        mark = mark or (lambda name: None)
+        T, Hd, I, a_in = s.tokens, s.hidden, s.inter, s.n_q * s.head_dim
+        quantize_fp8_rows(dx2, Xq=self.dx2_q[0], scale=self.dx2_q[1])
+        linear_dswiglu_fp8(self.dx2_q[0], self.dx2_q[1], self.WdT_q[0], self.WdT_q[1], self.g, self.u,
+                           rstd=self.rstd1, out={"Gp": self.Gp, "row": self.coef1, "H": None}, ws=self.ws)
+        ctx, ws2 = self._side()
+        with ctx:   # weight gradients of the MLP beside its input gradient
+            self._wgrad(dx2, Hd, self.H, I, self.dW["dWd"], Hd, I, T, ws=ws2)
+            self._wgrad(self.Gp, 2 * I, self.U1, Hd, self.dW["dWg"], I, Hd, T, ws=ws2)
+            # the up half of G' (a flat view from its first element; rows 2I apart)
+            self._wgrad(self.Gp.view(-1)[I:], 2 * I, self.U1, Hd, self.dW["dWu"], I, Hd, T, ws=ws2)
+        quantize_fp8_rows(self.Gp, Xq=self.G_q[0], scale=self.G_q[1])
+        rmsnorm_linear_dx_fp8(self.G_q[0], self.G_q[1], self.WguT_q[0], self.WguT_q[1], self.x1, w["gamma_mlp"],
+                              self.coef1, dX_resid=dx2, out=self.dx1, ws=self.ws)
+        dx1 = self.dx1["dX"]
+        quantize_fp8_rows(dx1, Xq=self.dx1_q[0], scale=self.dx1_q[1])
+        linear_fp8(self.dx1_q[0], self.dx1_q[1], self.WoT_q[0], self.WoT_q[1], Y=self.dA, ws=self.ws)
+        self._join()
+        ctx, ws2 = self._side()
+        with ctx:
+            self._wgrad(dx1, Hd, A, a_in, self.dW["dWo"], Hd, a_in, T, ws=ws2)
+        linear_qknorm_rope_bwd(dQ, dK, dV, self.fwd["qk_save"], self.fwd["V"], w["gamma_q"], w["gamma_k"], pos,
+                               self.cos_sin, s.n_q, s.n_kv, x0, w["Wqkv"], rstd=self.rstd0,
+                               gamma_in=w["gamma_attn"], dX_resid=dx1, eps=s.eps, head_dim=s.head_dim,
+                               ws=self.ws, out=self.grads_qkv)
+        self._join()
+        mark("bwd")
+        return {"dx0": self.grads_qkv["dX"], "dA": self.dA, "dx1": dx1, "dWqkv": self.grads_qkv["dW"],
+                "dWo": self.dW["dWo"], "dWg": self.dW["dWg"], "dWu": self.dW["dWu"], "dWd": self.dW["dWd"],
+                "dgamma_attn": self.grads_qkv["dgamma_in"], "dgamma_mlp": self.dx1["dgamma"],
                 "dgamma_q": self.grads_qkv["dgamma_q"], "dgamma_k": self.grads_qkv["dgamma_k"]}
 
     def step(self, x0, A, pos, dx2, dQ, dK, dV, mark=None):

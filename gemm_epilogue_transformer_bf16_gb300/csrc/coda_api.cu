@@ -2194,7 +2194,7 @@ size_t coda_linear_dswiglu_fp8_workspace_size(int64_t M, int64_t I, int64_t) {
 }
 
 int coda_linear_dswiglu_fp8(const uint8_t* dYq, const float* sdy, const uint8_t* WdTq, const float* swd,
-                            const coda_bf16* g, const coda_bf16* u, const float* rstd, coda_bf16* Gp, float* dot,
+                            const coda_bf16* g, const coda_bf16* u, const float* rstd, coda_bf16* Gp, float* row_out,
                             coda_bf16* H, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
                             coda_stream stream) {
   CK(dims_ok(M, I, K));
@@ -2234,13 +2234,16 @@ int coda_linear_dswiglu_fp8(const uint8_t* dYq, const float* sdy, const uint8_t*
   p.e.out3 = BF(H);
   p.e.ld_out3 = I;
   p.e.row_scale = rstd;
-  if (dot) {
+  if (row_out) {
     p.e.partials = spart;
     p.e.ld_part = M;
   }
   CK(run(p, status, s));
-  if (dot)  // dot_i = sum over the N tiles' partials
-    CU(coda::launch_combine_rows(spart, M, static_cast<int>(cdiv(I, BN)), M, 1.f, 0.f, nullptr, dot, 1, s));
+  // the N tiles' partials summed: with rstd the RMSNorm-backward coefficient
+  // c_i = r_i^2 * sum / K, without it the sum itself
+  if (row_out)
+    CU(coda::launch_combine_rows(spart, M, static_cast<int>(cdiv(I, BN)), M,
+                                 rstd ? 1.f / static_cast<float>(K) : 1.f, 0.f, rstd, row_out, 1, s));
   return CODA_OK;
 }
 

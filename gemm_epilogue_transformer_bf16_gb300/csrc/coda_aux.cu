@@ -826,33 +826,45 @@ __global__ void __launch_bounds__((QKT_WARPS + 1) * 32, 1)
   if (w == QKT_WARPS) {
     // ------------------------------------------------------------ producer
     const uint32_t el = elect_one();
+    const int lane_p = threadIdx.x & 31;
     int64_t it = 0;
     bool ok = true;
+    // the positions and row factors of the block's next 32 rows, one per
+    // lane, read by the whole warp at once (a row's cos/sin copy needs its
+    // position: read row by row, each waited a global round trip)
+    int pos_v = 0;
+    float r_v = 1.f;
     for (int64_t row = blockIdx.x; row < M; row += G, ++it) {
       const int st = static_cast<int>(it % stages);
       const uint32_t ph = static_cast<uint32_t>((it / stages) & 1);
+      if ((it & 31) == 0) {
+        const int64_t rl = row + static_cast<int64_t>(lane_p) * G;
+        pos_v = rl < M ? pos[rl] : 0;
+        r_v = (rstd && rl < M) ? rstd[rl] : 1.f;
+      }
+      uint8_t* sb = qkt_smem + static_cast<size_t>(st) * stage_bytes;
       if (it >= stages) {
         if (!mbar_wait_bounded(&empty[st], ph ^ 1, &abort_flag, status, timeout_ns)) {
           ok = false;
           break;
         }
-        if (el && coef) {  // the row that used this stage before
+        if (el && coef) {  // the row that used this stage before (its r is in the stage header)
           const int64_t prev = row - static_cast<int64_t>(stages) * G;
           float t = 0.f;
           for (int k = 0; k < QKT_WARPS; ++k) t += part[st][k];
-          const float r = rstd ? rstd[prev] : 1.f;
+          const float r = reinterpret_cast<const float*>(sb)[1];
           coef[prev] = r * r * t * inv_k;
         }
       }
-      uint8_t* sb = qkt_smem + static_cast<size_t>(st) * stage_bytes;
-      int p = pos[row];
+      int p = __shfl_sync(0xffffffffu, pos_v, static_cast<int>(it & 31));
+      const float rrow = __shfl_sync(0xffffffffu, r_v, static_cast<int>(it & 31));
       if (p < 0 || p >= max_pos) {
         if (el && status) atomicOr(status, CODA_DEV_POSITION_RANGE);
         p = p < 0 ? 0 : max_pos - 1;
       }
       if (el) {
         reinterpret_cast<int*>(sb)[0] = p;
-        reinterpret_cast<float*>(sb)[1] = rstd ? rstd[row] : 1.f;
+        reinterpret_cast<float*>(sb)[1] = rrow;
       }
       mbar_arrive_expect_tx(&full[st], tx_bytes, el);
       // (no copy of an empty range: a model without q or kv heads)
@@ -876,7 +888,7 @@ __global__ void __launch_bounds__((QKT_WARPS + 1) * 32, 1)
           const int64_t row = blockIdx.x + j * G;
           float t = 0.f;
           for (int k = 0; k < QKT_WARPS; ++k) t += part[st][k];
-          const float r = rstd ? rstd[row] : 1.f;
+          const float r = reinterpret_cast<const float*>(qkt_smem + static_cast<size_t>(st) * stage_bytes)[1];
           coef[row] = r * r * t * inv_k;
         }
       }

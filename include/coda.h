@@ -504,14 +504,15 @@ int coda_linear_cross_entropy_bwd_fp8(const uint8_t* Xq, const float* sx, const 
  *   dH = (sdy ⊙ dYq)(swd ⊙ WdTq)^T   (dY Wd; WdTq = coda_quantize_fp8_cols(Wd)),
  *   dG = dH ⊙ u ⊙ silu'(g),  dU = dH ⊙ silu(g),
  *   Gp [M, 2I] = r ⊙ [dG | dU] bf16 (r = rstd, or 1 when NULL),
- *   dot [M] fp32 = sum_j (dG g + dU u)_ij (or NULL), H [M, I] = silu(g) ⊙ u
- *   (or NULL).
+ *   row_out [M] fp32 (or NULL): with rstd the RMSNorm-backward coefficient
+ *   c_i = r_i^2 sum_j (dG g + dU u)_ij / K that the dX GEMM
+ *   (coda_rmsnorm_linear_dx_fp8) takes as coef; without rstd the sum itself;
+ *   H [M, I] = silu(g) ⊙ u (or NULL).
  * dYq [M, K], sdy [M], WdTq [I, K], swd [I]; g, u [M, I] the forward's saved
- * projections; K % 16 == 0.  dot feeds the RMSNorm-backward coefficient
- * c_i = r_i^2 dot_i / K of the dX GEMM (coda_rmsnorm_linear_dx_fp8). */
+ * projections; K % 16 == 0. */
 size_t coda_linear_dswiglu_fp8_workspace_size(int64_t M, int64_t I, int64_t K);
 int coda_linear_dswiglu_fp8(const uint8_t* dYq, const float* sdy, const uint8_t* WdTq, const float* swd,
-                            const coda_bf16* g, const coda_bf16* u, const float* rstd, coda_bf16* Gp, float* dot,
+                            const coda_bf16* g, const coda_bf16* u, const float* rstd, coda_bf16* Gp, float* row_out,
                             coda_bf16* H, int64_t M, int64_t I, int64_t K, void* ws, size_t ws_bytes,
                             coda_stream stream);
 

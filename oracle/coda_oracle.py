@@ -467,15 +467,18 @@ def dswiglu_fp8(dYv, sdy, WdTv, swd, g, u, row_scale=None):
     dH = (dYv sdy)(WdTv swd)^T  (dY Wd with Wd^T quantised per unit),
     dG = dH ⊙ u ⊙ silu'(g),  dU = dH ⊙ silu(g)  (g, u the saved projections);
     returns G' = r ⊙ [dG | dU] ([M, 2I]; r = 1 without row_scale), the row
-    sums dot_i = sum_j (dG g + dU u)_ij that the RMSNorm backward needs, H =
-    silu(g) ⊙ u and dH.  (The chain rule of mlp_fwd's H = silu(g) u.)"""
+    sums dot_i = sum_j (dG g + dU u)_ij, with row_scale the RMSNorm-backward
+    coefficient coef_i = r_i^2 dot_i / K (K = dY's width), H = silu(g) ⊙ u
+    and dH.  (The chain rule of mlp_fwd's H = silu(g) u.)"""
     dH = _deq(dYv, sdy) @ _deq(WdTv, swd).T
     g = np.asarray(g, dtype=np.float64)
     u = np.asarray(u, dtype=np.float64)
     dG = dH * u * silu_grad(g)
     dU = dH * silu(g)
     r = np.ones(dH.shape[0]) if row_scale is None else np.asarray(row_scale, dtype=np.float64)
-    return {"Gp": np.concatenate([dG, dU], axis=1) * r[:, None], "dot": (dG * g + dU * u).sum(axis=1),
+    dot = (dG * g + dU * u).sum(axis=1)
+    coef = None if row_scale is None else r * r * dot / np.asarray(dYv).shape[1]
+    return {"Gp": np.concatenate([dG, dU], axis=1) * r[:, None], "dot": dot, "coef": coef,
             "H": silu(g) * u, "dH": dH}
 
 

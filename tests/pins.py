@@ -712,6 +712,20 @@ def check_fp8_epilogue_ops(o):
     h = 1e-6
     for i_row in range(M):
         e.append(abs((L(1 + h) - L(1 - h)) / (2 * h) - ds["dot"][i_row]) / max(abs(ds["dot"][i_row]), 1e-12))
+    # the MLP's input-gradient chain through the input RMSNorm: the dSwiGLU
+    # map's coefficient and G' fed to the RMSNorm input gradient (operands
+    # given as values with unit scales) equal mlp_bwd's dX and dgamma
+    M, Hd, I = 3, 16, 6
+    x = r.standard_normal((M, Hd))
+    gam = 1 + 0.1 * r.standard_normal(Hd)
+    Wg, Wu = r.standard_normal((I, Hd)) * 0.4, r.standard_normal((I, Hd)) * 0.4
+    Wd, dY = r.standard_normal((Hd, I)) * 0.3, r.standard_normal((M, Hd))
+    fm = o.mlp_fwd(x, Wg, Wu, Wd, np.zeros((M, Hd)), gam, 1e-6)
+    rx = o.rms_inv(x, 1e-6)
+    ds = o.dswiglu_fp8(dY, np.ones(M), Wd.T, np.ones(I), fm["g"], fm["u"], row_scale=rx)
+    dxr = o.rmsnorm_linear_dx_fp8(ds["Gp"], np.ones(M), np.hstack([Wg.T, Wu.T]), np.ones(Hd), x, gam, ds["coef"])
+    mb = o.mlp_bwd(x, Wg, Wu, Wd, dY, gam, 1e-6)
+    e += [_rel(dxr["dX"], mb["dX"]), _rel(dxr["dgamma"], mb["dgamma"])]
     # RMSNorm-reparameterised input gradient
     M, K, N = 4, 16, 8
     X = r.standard_normal((M, K))

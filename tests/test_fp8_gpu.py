@@ -113,7 +113,7 @@ def test_linear_dswiglu_fp8(coda):
     r = O.dswiglu_fp8(dyv, osdy, wdv, oswd, to_np(g), to_np(u), row_scale=to_np(rstd))
     assert_bf16(out["Gp"], r["Gp"], "fp8 G' = r [dG | dU]")
     assert_bf16(out["H"], r["H"], "fp8 dSwiGLU H")
-    assert_bf16(out["dot"], r["dot"], "fp8 dSwiGLU row dot")
+    assert_bf16(out["row"], r["coef"], "fp8 dSwiGLU RMSNorm coefficient")
 
 
 def test_rmsnorm_linear_dx_fp8(coda):
@@ -130,3 +130,35 @@ def test_rmsnorm_linear_dx_fp8(coda):
     r = O.rmsnorm_linear_dx_fp8(gv, osg, wv, osw, to_np(X), to_np(gam), to_np(coef), dX_resid=to_np(R))
     assert_bf16(out["dX"], r["dX"], "fp8 RMSNorm dX")
     assert_bf16(out["dgamma"], r["dgamma"], "fp8 RMSNorm dgamma")
+
+
+def test_block_fp8_step(coda):
+    """The block step with its forward projections and its MLP and
+    O-projection input gradients on e4m3 operands (BlockFP8), against the
+    fp64 oracle's bf16-free block on a ragged shape.  Each FP8 operator is
+    checked exactly above on shared codes; here the quantisation of every
+    activation and weight compounds (one e4m3 rounding is up to 2^-4 of a
+    value, about 4 % RMS on a product of two quantised operands, and the
+    chains run through two or three such GEMMs), so the bound is a relative
+    Frobenius error of 0.15 per output: it catches wiring mistakes (a
+    transposed operand, a wrong scale), which give errors of order one."""
+    from gemm_epilogue_transformer_bf16_gb300.block import BlockFP8
+    shape = synth.BlockShape(tokens=256, hidden=512, n_q=4, n_kv=2, head_dim=128, inter=1024, seq_len=128)
+    t = synth.make_block(shape, seed=0)
+    d = {k: v.to(DEV) for k, v in t.items()}
+    o = {k: (v.numpy() if v.dtype in (torch.int32, torch.int64) else to_np(v)) for k, v in t.items()}
+    blk = BlockFP8(shape, d)
+    f = blk.forward(d["x0"], d["A"], d["pos"])
+    g = blk.backward(d["x0"], d["A"], d["pos"], d["dx2"], d["dQ"], d["dK"], d["dV"])
+    torch.cuda.synchronize()
+    assert coda.get_status(blk.ws) == 0 and coda.get_status(blk.ws2) == 0
+    cfg = dict(n_q=shape.n_q, n_kv=shape.n_kv, head_dim=shape.head_dim, theta=shape.theta, eps=shape.eps)
+    rf, rb = O.block_fwd(o, **cfg), O.block_bwd(o, **cfg)
+    errs = {}
+    for k, got, ref in [(k, f[k], rf[k]) for k in ("Q", "K", "V", "x1", "x2")] + \
+            [(k, g[k], rb[k]) for k in ("dx0", "dA", "dx1", "dWqkv", "dWo", "dWg", "dWu", "dWd", "dgamma_attn",
+                                        "dgamma_mlp", "dgamma_q", "dgamma_k")]:
+        gv, rv = to_np(got), np.asarray(ref, dtype=np.float64)
+        assert np.all(np.isfinite(gv)), k
+        errs[k] = float(np.linalg.norm(gv - rv) / np.linalg.norm(rv))
+    assert max(errs.values()) <= 0.15, errs
