@@ -79,17 +79,18 @@ int num_sms() {
 }
 
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride
-// `ld` elements; box = box_cols x box_rows, 128-byte swizzle, zero fill.
+// `ld` elements; box = box_cols x box_rows, 128-byte swizzle (or `swz`),
+// zero fill.
 bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_cols,
-                uint32_t box_rows, int elem_bytes = 2) {
+                uint32_t box_rows, int elem_bytes = 2, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * elem_bytes};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -180,6 +181,17 @@ int aux_prefetch() {
   static const int v = [] {
     const char* e = std::getenv("CODA_AUX_PREFETCH");
     return (e && e[0] == '0') ? 0 : 1;
+  }();
+  return v;
+}
+
+// The plain epilogue's residual comes through the TMA ring (copies of 32 x
+// 32 tiles into shared memory issued ahead of the chunk loop) instead of
+// per-thread loads.  CODA_EPI_RING=0 turns it off (for comparisons).
+bool epi_ring_enabled() {
+  static const bool v = [] {
+    const char* e = std::getenv("CODA_EPI_RING");
+    return !(e && e[0] == '0');
   }();
   return v;
 }
@@ -311,7 +323,7 @@ int prepare(const Plan& p, int* status, int cg, int nb_base, int n_tiles, CUtens
   // K-major B rows one TMA copy stages: the tile's N, its half per pair CTA,
   // a quarter per CTA with two pairs (each copy multicast to both pairs)
   const uint32_t b_box_rows = static_cast<uint32_t>(BN / cg);
-  std::memset(maps, 0, 4 * sizeof(CUtensorMap));
+  std::memset(maps, 0, 6 * sizeof(CUtensorMap));
   // a k-slice is 128 bytes: 64 bf16 or 128 e4m3 elements
   const int esz = p.fp8 ? 1 : 2;
   const uint32_t kbox = p.fp8 ? 2 * coda::BK : coda::BK;
@@ -369,6 +381,14 @@ int prepare(const Plan& p, int* status, int cg, int nb_base, int n_tiles, CUtens
     a.e.st_stream = stream_stores(p.M * cols * esz * n_out);
   }
   a.e.aux_prefetch = aux_prefetch();
+  a.e.ring = 0;
+  if (p.kind == coda::EpiKind::Plain && p.e.aux0 && epi_ring_enabled() && al16(p.e.aux0) && p.e.ld_aux0 % 8 == 0 &&
+      p.e.ld_aux0 >= p.N) {
+    // the residual as [M, N] with row stride ld_aux0, read in 32 x 32 boxes
+    if (!encode_map(&maps[4], p.e.aux0, p.M, p.N, p.e.ld_aux0, 32, 32, 2, CU_TENSOR_MAP_SWIZZLE_64B))
+      return CODA_ERR_CUDA;
+    a.e.ring = 1;
+  }
   return CODA_OK;
 }
 
@@ -423,7 +443,7 @@ int run(const Plan& p, int* status, cudaStream_t s) {
   if (sms <= 0) return CODA_ERR_CUDA;
   const int cg = cluster_ctas(p.M, p.a_mn, p.b_mn, p.K + p.K2);
   const int num_n = static_cast<int>(cdiv(p.N, p.b_dual ? BN / 2 : BN));
-  CUtensorMap maps[4];
+  CUtensorMap maps[6];
   GemmArgs a;
   int cg_run = cg;
   if (cg == 4 && p.n_per_unit <= 1 && (split_enabled() || pair_waves_enabled())) {
@@ -461,7 +481,7 @@ int run(const Plan& p, int* status, cudaStream_t s) {
         CU(cudaStreamWaitEvent(s2, ev[0], 0));
         CK(prepare(p, status, 4, 0, num_n - best, maps, a));
         CK(dispatch(p, sms, 4, s, maps, a));
-        CUtensorMap maps2[4];
+        CUtensorMap maps2[6];
         GemmArgs a2;
         CK(prepare(p, status, 2, num_n - best, best, maps2, a2));
         a2.max_clusters = extra;

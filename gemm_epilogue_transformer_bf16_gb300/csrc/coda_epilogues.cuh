@@ -38,13 +38,14 @@ __device__ __forceinline__ void store_f32x8(float* p, const float* v) {
 // 16-byte stores that each cover 8 rows x 64 contiguous bytes (whole 32-byte
 // sectors) instead of 32 rows x 16 bytes.  Rows >= M and columns >= N are
 // not written (N is a multiple of 8).  Called by all 32 lanes.
-__device__ __forceinline__ void warp_store_bf16x32(uint8_t* stage, __nv_bfloat16* base, int64_t ld, int row0,
-                                                   int M, int col0, int N, const float* v, bool stream) {
+// Same, from the 32 values already rounded and packed in pairs (pk[i] holds
+// columns 2i and 2i + 1).
+__device__ __forceinline__ void warp_store_bf16x32_packed(uint8_t* stage, __nv_bfloat16* base, int64_t ld, int row0,
+                                                          int M, int col0, int N, const uint32_t* pk, bool stream) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
-    const uint4 w = make_uint4(pack_bf16x2(v[p * 8 + 0], v[p * 8 + 1]), pack_bf16x2(v[p * 8 + 2], v[p * 8 + 3]),
-                               pack_bf16x2(v[p * 8 + 4], v[p * 8 + 5]), pack_bf16x2(v[p * 8 + 6], v[p * 8 + 7]));
+    const uint4 w = make_uint4(pk[p * 4 + 0], pk[p * 4 + 1], pk[p * 4 + 2], pk[p * 4 + 3]);
     *reinterpret_cast<uint4*>(stage + lane * 64 + ((p ^ ((lane >> 1) & 3)) * 16)) = w;
   }
   __syncwarp();
@@ -64,6 +65,13 @@ __device__ __forceinline__ void warp_store_bf16x32(uint8_t* stage, __nv_bfloat16
     }
   }
   __syncwarp();
+}
+__device__ __forceinline__ void warp_store_bf16x32(uint8_t* stage, __nv_bfloat16* base, int64_t ld, int row0,
+                                                   int M, int col0, int N, const float* v, bool stream) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  warp_store_bf16x32_packed(stage, base, ld, row0, M, col0, N, pk, stream);
 }
 
 // Reduce-scatter over the warp: on entry thread `lane` holds p[0..31] of its
@@ -145,19 +153,34 @@ __device__ __forceinline__ void tmem_ld32_acc(uint32_t taddr, float (&v)[32], co
 template <int BN>
 struct EpiPlain {
   struct State {};
+  static constexpr int RING = 1;  // the residual (aux0) can come through the TMA ring
+  static __device__ __forceinline__ int chunks(const TileInfo& t) {
+    return max(0, min(BN / 32, (t.N - t.nb * BN + 31) / 32));
+  }
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
   // Issued before the tile's accumulator is ready (while its mainloop still
-  // runs): the thread's row segments of the tile's input tiles are requested
-  // into L2, so the chunk loop's loads wait on L2 rather than on DRAM once
-  // per chunk (the last tile's epilogue has no mainloop to hide behind).
+  // runs).  With the ring, the first RING_SLOTS chunks of the warp's
+  // residual rows are copied into shared memory; otherwise the thread's row
+  // segments of the tile's input tiles are requested into L2, so the chunk
+  // loop's loads wait on L2 rather than on DRAM once per chunk (the last
+  // tile's epilogue has no mainloop to hide behind).
   static __device__ __forceinline__ void prefetch(const EpiArgs& e, const TileInfo& t) {
+    if (e.ring) {
+      const int n = min(chunks(t), RING_SLOTS);
+      const uint32_t g0 = t.ring_cnt[0];
+      const int row0 = t.row - static_cast<int>(threadIdx.x & 31);
+      for (int c = 0; c < n; ++c) ring_issue(t, 1, g0 + c, t.nb * BN + c * 32, row0);
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) t.ring_cnt[0] = g0 + n;
+      __syncwarp();
+    }
     const int row = t.row;
     const int cbase = t.nb * BN;
     if (!e.aux_prefetch || row >= t.M || cbase >= t.N) return;
     const int cols = min(BN, t.N - cbase);
     const int64_t arow = e.gather_rows ? e.gather_rows[row] : row;
-    if (e.aux0) prefetch_l2_span(e.aux0 + static_cast<int64_t>(row) * e.ld_aux0 + cbase, cols * 2);
+    if (e.aux0 && !e.ring) prefetch_l2_span(e.aux0 + static_cast<int64_t>(row) * e.ld_aux0 + cbase, cols * 2);
     if (e.acc_in) prefetch_l2_span(e.acc_in + static_cast<int64_t>(row) * e.ld_acc_in + cbase, cols * 4);
     if (e.row_coef && arow >= 0) prefetch_l2_span(e.aux1 + arow * e.ld_aux1 + cbase, cols * 2);
     if (e.row_coef2) prefetch_l2_span(e.aux3 + static_cast<int64_t>(row) * e.ld_aux3 + cbase, cols * 2);
@@ -179,11 +202,12 @@ struct EpiPlain {
     }
     float ss = 0.f;
     const int row0 = row - static_cast<int>(threadIdx.x & 31);
-    // The residual tile (aux0) is loaded into registers one 32-column chunk
-    // ahead, so its L2 round trip overlaps the previous chunk's math and
-    // stores: with one epilogue warp per lane quarter, a load, then the
-    // math, then the stores of each chunk in turn made the epilogue of a
-    // K = 2048 tile longer than its mainloop.
+    // The residual tile (aux0) arrives either through the TMA ring (issued
+    // RING_SLOTS chunks ahead, the first ones before the accumulator was
+    // ready) or, without it, in registers one 32-column chunk ahead, so its
+    // L2 round trip overlaps the previous chunk's math and stores.  Per-lane
+    // loads of 32 different rows wait ~3000 cycles on a busy SM, longer than
+    // a chunk's math and stores, which is what the ring removes.
     const int64_t aoff = static_cast<int64_t>(row) * e.ld_aux0;
     uint4 an[4];
     auto fetch = [&](int col0) {
@@ -193,15 +217,30 @@ struct EpiPlain {
         an[q] = (rv && cc < t.N) ? *reinterpret_cast<const uint4*>(e.aux0 + aoff + cc) : make_uint4(0u, 0u, 0u, 0u);
       }
     };
-    if (e.aux0) fetch(t.nb * BN);
+    const bool use_ring = e.ring != 0;
+    const int nch = chunks(t);
+    uint32_t g_done = use_ring ? t.ring_cnt[1] : 0u, g_issued = use_ring ? t.ring_cnt[0] : 0u;
+    if (e.aux0 && !use_ring) fetch(t.nb * BN);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int col0 = t.nb * BN + c;
       if (col0 >= t.N) break;
       uint4 ac[4];
+      if (use_ring) {
+        if (!ring_wait(t, g_done)) break;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) ac[q] = an[q];
-      if (e.aux0 && c + 32 < BN) fetch(col0 + 32);
+        for (int q = 0; q < 4; ++q) ac[q] = ring_read(t, 1, g_done, 0, q);
+        __syncwarp();
+        ++g_done;
+        if (c / 32 + RING_SLOTS < nch) {
+          ring_issue(t, 1, g_issued, col0 + RING_SLOTS * 32, row0);
+          ++g_issued;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ac[q] = an[q];
+        if (e.aux0 && c + 32 < BN) fetch(col0 + 32);
+      }
       float v[32];
       __syncwarp();
       tmem_ld32(t.taddr + c, v);
@@ -271,19 +310,32 @@ struct EpiPlain {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) x[i] += o8[i];
               }
-              if (e.partials) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float y = round_bf16(x[i]);
-                  ss += y * y;
-                }
-              }
             }
           }
         }
       }
       if (!e.d_f32) {
-        warp_store_bf16x32(t.stage, static_cast<__nv_bfloat16*>(e.D), e.ldd, row0, t.M, col0, t.N, v, e.st_stream);
+        // Each output is rounded to bf16 once (packed in pairs); the row's
+        // partial sum of squares and the second output read the rounded
+        // values back from the packed words.
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        if (e.partials && rv) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (col0 + g * 8 < t.N) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float lo = bf16_lo(pk[g * 4 + i]), hi = bf16_hi(pk[g * 4 + i]);
+                ss += lo * lo;
+                ss += hi * hi;
+              }
+            }
+          }
+        }
+        warp_store_bf16x32_packed(t.stage, static_cast<__nv_bfloat16*>(e.D), e.ldd, row0, t.M, col0, t.N, pk,
+                                  e.st_stream);
         if (e.out1) {
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -294,11 +346,22 @@ struct EpiPlain {
 #pragma unroll
               for (int i = 0; i < 8; ++i) s8[i] = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[g * 8 + i] = round_bf16(v[g * 8 + i]) * s8[i];
+            for (int i = 0; i < 4; ++i) {
+              v[g * 8 + 2 * i] = bf16_lo(pk[g * 4 + i]) * s8[2 * i];
+              v[g * 8 + 2 * i + 1] = bf16_hi(pk[g * 4 + i]) * s8[2 * i + 1];
+            }
           }
           warp_store_bf16x32(t.stage, e.out1, e.ld_out1, row0, t.M, col0, t.N, v, e.st_stream);
         }
       }
+    }
+    if (use_ring) {
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) {
+        t.ring_cnt[0] = g_issued;
+        t.ring_cnt[1] = g_done;
+      }
+      __syncwarp();
     }
     if (e.partials && rv) e.partials[static_cast<int64_t>(t.nb) * e.ld_part + row] = ss;
   }
@@ -563,11 +626,11 @@ struct EpiRmsDx {
     uint4 xn[4], rn[4];
     auto fetch = [&](int col0) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int cc = col0 + q * 8;
+      for (int k = 0; k < 4; ++k) {
+        const int cc = col0 + k * 8;
         const bool in = rv && cc < t.N;
-        xn[q] = in ? *reinterpret_cast<const uint4*>(e.aux1 + xoff + cc) : make_uint4(0u, 0u, 0u, 0u);
-        rn[q] = (in && e.aux0) ? *reinterpret_cast<const uint4*>(e.aux0 + roff + cc) : make_uint4(0u, 0u, 0u, 0u);
+        xn[k] = in ? *reinterpret_cast<const uint4*>(e.aux1 + xoff + cc) : make_uint4(0u, 0u, 0u, 0u);
+        rn[k] = (in && e.aux0) ? *reinterpret_cast<const uint4*>(e.aux0 + roff + cc) : make_uint4(0u, 0u, 0u, 0u);
       }
     };
     fetch(t.nb * BN);
@@ -577,9 +640,9 @@ struct EpiRmsDx {
       if (col0 >= t.N) break;
       uint4 xc[4], rcur[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xc[q] = xn[q];
-        rcur[q] = rn[q];
+      for (int k = 0; k < 4; ++k) {
+        xc[k] = xn[k];
+        rcur[k] = rn[k];
       }
       if (c + 32 < BN) fetch(col0 + 32);
       float v[32];

@@ -30,6 +30,7 @@
 // returns.
 #pragma once
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -47,18 +48,40 @@ constexpr int NUM_THREADS = 192;
 #ifndef CODA_PAIR_STAGES
 #define CODA_PAIR_STAGES 6
 #endif
-template <int BN, bool PAIR = false>
+// Epilogue ring: an epilogue that reads bf16 [M, N] tensors tile by tile
+// (the residual) has them copied by TMA, 32 rows x 32 columns (2 KB, 64-byte
+// swizzle) per copy, into RING_SLOTS slots per epilogue warp, issued before
+// the tile's accumulator is ready and RING_SLOTS chunks ahead of the chunk
+// being read.  RING = tensors per slot (0: no ring).
+constexpr int RING_SLOTS = 3;
+constexpr uint32_t RING_CHUNK_BYTES = 32 * 32 * 2;
+
+template <int BN, bool PAIR = false, int RING = 0>
 struct GemmCfg {
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows staged by one CTA
-  static constexpr int STAGES = PAIR ? CODA_PAIR_STAGES : (BN >= 256 ? 4 : 6);
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr uint32_t BAR_BYTES = 256;
+  static constexpr uint32_t BAR_BYTES = 512;
   static constexpr uint32_t EPI_STAGE_BYTES = 4 * 2048;  // 2 KB store-transpose buffer per epilogue warp
-  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + EPI_STAGE_BYTES;
+  static constexpr uint32_t RING_BYTES = 4u * RING_SLOTS * RING_CHUNK_BYTES * RING;
+  static constexpr int STAGES_WANT = PAIR ? CODA_PAIR_STAGES : (BN >= 256 ? 4 : 6);
+  static constexpr int STAGES_FIT =
+      static_cast<int>((232448u - 1024u - BAR_BYTES - EPI_STAGE_BYTES - RING_BYTES) / STAGE_BYTES);
+  static constexpr int STAGES = STAGES_WANT < STAGES_FIT ? STAGES_WANT : STAGES_FIT;
+  static constexpr uint32_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + RING_BYTES + BAR_BYTES + EPI_STAGE_BYTES;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+// Tensors an epilogue stages through the ring (Epi::RING, 0 if absent).
+template <class E, class = void>
+struct EpiRing {
+  static constexpr int value = 0;
+};
+template <class E>
+struct EpiRing<E, std::void_t<decltype(E::RING)>> {
+  static constexpr int value = E::RING;
 };
 
 // Everything an epilogue may read or write.  Unused fields are null/zero.
@@ -102,6 +125,7 @@ struct EpiArgs {
   int onehot;                   // CE_DLOGITS: include -w at the label column
   int st_stream;                // epilogue tile stores as streaming (.cs) stores
   int aux_prefetch;             // request the tile's auxiliary rows into L2 before its accumulator is ready
+  int ring;                     // tensors the epilogue reads through the TMA ring (0: plain loads)
   int mode;                     // SIGMOID: 0 forward, 1 backward on the recomputed logits
   float* target_logit;
   int64_t col_base;             // CE_DLOGITS: vocabulary column of the launch's column 0 (a vocabulary slice)
@@ -159,7 +183,45 @@ struct TileInfo {
   uint32_t taddr;   // TMEM address of this warp's lane quarter, column 0
   int* status;
   uint8_t* stage;   // this warp's 2 KB shared-memory store-transpose buffer
+  // epilogue ring (used when EpiArgs::ring is set)
+  uint8_t* ring;            // this warp's RING_SLOTS slots
+  uint64_t* ring_bar;       // one barrier per slot
+  uint32_t* ring_cnt;       // [0] chunks issued, [1] chunks consumed (this warp's, in shared memory)
+  const CUtensorMap* emap0; // first ring tensor
+  const CUtensorMap* emap1; // second ring tensor
+  volatile int* abort_flag;
+  uint64_t timeout_ns;
 };
+
+// Ring chunk g (this warp's running chunk count) = columns [col, col + 32)
+// of rows [row0, row0 + 32) of each ring tensor, into slot g % RING_SLOTS.
+// Called by the whole warp with uniform arguments; lane 0 issues.  Rows and
+// columns outside the tensor arrive as zeros.  The fence orders the warp's
+// earlier reads of the slot (generic proxy) before the copy's writes.
+__device__ __forceinline__ void ring_issue(const TileInfo& t, int ntens, uint32_t g, int col, int row0) {
+  const int sl = static_cast<int>(g % RING_SLOTS);
+  uint8_t* dst = t.ring + sl * ntens * RING_CHUNK_BYTES;
+  const uint32_t l0 = (threadIdx.x & 31) == 0;
+  if (l0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_arrive_expect_tx(&t.ring_bar[sl], ntens * RING_CHUNK_BYTES, l0);
+  tma_load_2d(dst, t.emap0, &t.ring_bar[sl], col, row0, l0);
+  if (ntens > 1) tma_load_2d(dst + RING_CHUNK_BYTES, t.emap1, &t.ring_bar[sl], col, row0, l0);
+}
+
+// Wait for ring chunk g; warp-uniform result (false: timed out or aborted).
+__device__ __forceinline__ bool ring_wait(const TileInfo& t, uint32_t g) {
+  const bool ok = mbar_wait_bounded(&t.ring_bar[g % RING_SLOTS], (g / RING_SLOTS) & 1, t.abort_flag, t.status,
+                                    t.timeout_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// 16-byte piece p (columns 8p .. 8p + 7) of this lane's row in tensor `k` of
+// slot g % RING_SLOTS (64-byte swizzle: piece p of row r at r * 64 + (p ^ ((r >> 1) & 3)) * 16).
+__device__ __forceinline__ uint4 ring_read(const TileInfo& t, int ntens, uint32_t g, int k, int p) {
+  const int r = threadIdx.x & 31;
+  const uint8_t* slot = t.ring + static_cast<int>(g % RING_SLOTS) * ntens * RING_CHUNK_BYTES + k * RING_CHUNK_BYTES;
+  return *reinterpret_cast<const uint4*>(slot + r * 64 + ((p ^ ((r >> 1) & 3)) * 16));
+}
 
 // Unit -> (m block, first n block, number of n blocks).
 __device__ __forceinline__ void unit_coords(const GemmArgs& a, int u, int& mb, int& nb0, int& nlen, int& chunk) {
@@ -192,23 +254,29 @@ template <int BN, class Epi, int CG, bool FP8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     coda_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mB0,
                      const __grid_constant__ CUtensorMap mA1, const __grid_constant__ CUtensorMap mB1,
+                     const __grid_constant__ CUtensorMap mE0, const __grid_constant__ CUtensorMap mE1,
                      const GemmArgs args) {
   constexpr bool PAIR = CG >= 2;
   constexpr bool QUAD = CG == 4;
   static_assert(CG == 1 || CG == 2 || CG == 4, "cluster size");
-  using Cfg = GemmCfg<BN, PAIR>;
+  constexpr int RING = EpiRing<Epi>::value;
+  using Cfg = GemmCfg<BN, PAIR, RING>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
+  uint8_t* ring = smem + S * Cfg::STAGE_BYTES;  // 1024-byte aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + Cfg::RING_BYTES);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* ring_bar = drain + 1;  // RING_SLOTS per epilogue warp
+  uint32_t* ring_cnt = reinterpret_cast<uint32_t*>(ring_bar + 4 * RING_SLOTS);  // 2 per epilogue warp
+  uint32_t* tmem_slot = ring_cnt + 8;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint8_t* epi_stage = smem + S * Cfg::STAGE_BYTES + Cfg::BAR_BYTES;
+  static_assert((2 * 6 + 5 + 4 * RING_SLOTS) * 8 + 10 * 4 <= Cfg::BAR_BYTES, "barrier area");
+  uint8_t* epi_stage = ring + Cfg::RING_BYTES + Cfg::BAR_BYTES;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -230,6 +298,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&tempty[b], PAIR ? 8 : 4);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 4 * RING_SLOTS; ++i) mbar_init(&ring_bar[i], 1);
+    for (int i = 0; i < 8; ++i) ring_cnt[i] = 0;
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -241,6 +311,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tma_prefetch_desc(&mB1);
     }
     if (args.b_dual) tma_prefetch_desc(&mB1);
+    if (RING > 0 && args.e.ring > 0) tma_prefetch_desc(&mE0);
+    if (RING > 1 && args.e.ring > 1) tma_prefetch_desc(&mE1);
   }
   if (warp == 1) {
     tmem_alloc<PAIR>(tmem_slot, Cfg::TMEM_COLS);
@@ -459,6 +531,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ti.N = args.N;
       ti.status = args.status;
       ti.stage = epi_stage + q * 2048;
+      ti.ring = ring + q * RING_SLOTS * RING * RING_CHUNK_BYTES;
+      ti.ring_bar = ring_bar + q * RING_SLOTS;
+      ti.ring_cnt = ring_cnt + q * 2;
+      ti.emap0 = &mE0;
+      ti.emap1 = &mE1;
+      ti.abort_flag = abort_flag;
+      ti.timeout_ns = args.timeout_ns;
       typename Epi::State st;
       Epi::begin(st, args.e, ti);
       for (int j = 0; j < nlen; ++j, ++t) {
@@ -486,6 +565,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (aborted) break;
       Epi::end(st, args.e, ti);
+    }
+    if (RING > 0 && args.e.ring > 0) {
+      // ring copies issued but not consumed (an aborted tile) land before
+      // the CTA's shared memory is released
+      __syncwarp();
+      uint64_t* rb = ring_bar + q * RING_SLOTS;
+      const uint32_t issued = ring_cnt[q * 2], done = ring_cnt[q * 2 + 1];
+      for (uint32_t g = done; g < issued; ++g) mbar_wait_drain(&rb[g % RING_SLOTS], (g / RING_SLOTS) & 1, 200000000ull);
     }
   }
 

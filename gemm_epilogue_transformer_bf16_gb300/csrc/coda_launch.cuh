@@ -1,5 +1,6 @@
 // Launch helper for one (tile width, epilogue) instantiation of
-// coda_gemm_kernel: raises the dynamic shared-memory limit once per device and
+// coda_gemm_kernel (m: six tensor maps -- A0, B0, A1, B1 and the two
+// epilogue-ring tensors): raises the dynamic shared-memory limit once per device and
 // launches the persistent grid -- one 192-thread CTA per SM, or, for the
 // clustered variants (CTA pairs, two pairs sharing B), as many 2- or 4-CTA
 // clusters as can be resident at once (cudaOccupancyMaxActiveClusters).
@@ -25,7 +26,7 @@ inline bool programmatic_launch() {
 
 template <int BN, class Epi, int CG, bool FP8>
 cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CUtensorMap* m, const GemmArgs& a) {
-  constexpr uint32_t smem = GemmCfg<BN, (CG >= 2)>::SMEM_BYTES;
+  constexpr uint32_t smem = GemmCfg<BN, (CG >= 2), EpiRing<Epi>::value>::SMEM_BYTES;
   // per device, set up once (first calls from several host threads are
   // serialised on `init`): the shared-memory limit and the resident-cluster
   // count; afterwards read without the lock
@@ -94,7 +95,7 @@ cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CU
     cfg.attrs = attr;
     ++cfg.numAttrs;
   }
-  e = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], a);
+  e = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], m[4], m[5], a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
