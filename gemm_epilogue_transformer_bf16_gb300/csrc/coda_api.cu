@@ -185,6 +185,18 @@ int aux_prefetch() {
   return v;
 }
 
+// The plain epilogue runs a chunk loop compiled for its launch's features
+// (row scale, residual, partial sums, second output) unless the launch
+// needs others; CODA_EPI_LEAN=0 makes every launch take the general loop
+// (for comparisons).
+int epi_no_lean() {
+  static const int v = [] {
+    const char* e = std::getenv("CODA_EPI_LEAN");
+    return (e && e[0] == '0') ? 1 : 0;
+  }();
+  return v;
+}
+
 // The plain epilogue's residual comes through the TMA ring (copies of 32 x
 // 32 tiles into shared memory issued ahead of the chunk loop) instead of
 // per-thread loads.  CODA_EPI_RING=0 turns it off (for comparisons).
@@ -381,6 +393,7 @@ int prepare(const Plan& p, int* status, int cg, int nb_base, int n_tiles, CUtens
     a.e.st_stream = stream_stores(p.M * cols * esz * n_out);
   }
   a.e.aux_prefetch = aux_prefetch();
+  a.e.no_lean = epi_no_lean();
   a.e.ring = 0;
   if (p.kind == coda::EpiKind::Plain && p.e.aux0 && epi_ring_enabled() && al16(p.e.aux0) && p.e.ld_aux0 % 8 == 0 &&
       p.e.ld_aux0 >= p.N) {

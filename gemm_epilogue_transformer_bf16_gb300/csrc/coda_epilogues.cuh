@@ -118,10 +118,11 @@ __device__ __forceinline__ void warp_colsum_partial(float* p, int lane) {
 // The accumulator chunk of columns col0 .. col0 + 31 with the FP8 operand
 // scales applied: acc * acc_rs[row] * acc_cs[col] (columns >= N scaled by 0).
 // Without FP8 operands (both null) it is tmem_ld32.
-__device__ __forceinline__ void tmem_ld32_acc(uint32_t taddr, float (&v)[32], const EpiArgs& e, int row, bool rv,
-                                              int col0, int N) {
+template <bool SCALED>
+__device__ __forceinline__ void tmem_ld32_acc_t(uint32_t taddr, float (&v)[32], const EpiArgs& e, int row, bool rv,
+                                                int col0, int N) {
   tmem_ld32(taddr, v);
-  if (e.acc_rs || e.acc_cs) {
+  if (SCALED) {
     const float rs = (e.acc_rs && rv) ? e.acc_rs[row] : 1.f;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -136,6 +137,13 @@ __device__ __forceinline__ void tmem_ld32_acc(uint32_t taddr, float (&v)[32], co
       for (int i = 0; i < 8; ++i) v[g * 8 + i] *= rs * s8[i];
     }
   }
+}
+__device__ __forceinline__ void tmem_ld32_acc(uint32_t taddr, float (&v)[32], const EpiArgs& e, int row, bool rv,
+                                              int col0, int N) {
+  if (e.acc_rs || e.acc_cs)
+    tmem_ld32_acc_t<true>(taddr, v, e, row, rv, col0, N);
+  else
+    tmem_ld32_acc_t<false>(taddr, v, e, row, rv, col0, N);
 }
 
 // ---------------------------------------------------------------------------
@@ -188,15 +196,36 @@ struct EpiPlain {
       prefetch_l2_span(static_cast<const uint8_t*>(e.D) + (static_cast<int64_t>(row) * e.ldd + cbase) * (e.d_f32 ? 4 : 2),
                        cols * (e.d_f32 ? 4 : 2));
   }
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
+  // GEN = false compiles the chunk loop for the launches that need only the
+  // row scale, the residual, the row partial sums and the second output (the
+  // block's projections, the RMSNorm-linear forward): with one epilogue warp
+  // per SM sub-partition, the other features' per-chunk tests cost as much
+  // as the arithmetic they guard.
+  // RES (lean loops only): the residual is absent (0), loaded into registers
+  // (1) or read from the TMA ring (2).
+  static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t) {
+    const bool gen = e.no_lean || e.col_scale || e.acc_in || e.row_coef || e.row_coef2 || e.csr_off || e.d_f32 ||
+                     e.beta || e.gather_rows;
+    if (gen)
+      tile_impl<true, 1>(st, e, t);
+    else if (!e.aux0)
+      tile_impl<false, 0>(st, e, t);
+    else if (e.ring)
+      tile_impl<false, 2>(st, e, t);
+    else
+      tile_impl<false, 1>(st, e, t);
+  }
+  template <bool GEN, int RES>
+  static __device__ __forceinline__ void tile_impl(State&, const EpiArgs& e, const TileInfo& t) {
+    const bool has_res = GEN ? e.aux0 != nullptr : RES > 0;
     const int row = t.row;
     const bool rv = row < t.M;
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
-    const float rc = (e.row_coef && rv) ? e.row_coef[row] : 0.f;
-    const float rc2 = (e.row_coef2 && rv) ? e.row_coef2[row] : 0.f;
-    const int64_t arow = e.gather_rows ? (rv ? e.gather_rows[row] : -1) : row;
+    const float rc = (GEN && e.row_coef && rv) ? e.row_coef[row] : 0.f;
+    const float rc2 = (GEN && e.row_coef2 && rv) ? e.row_coef2[row] : 0.f;
+    const int64_t arow = (GEN && e.gather_rows) ? (rv ? e.gather_rows[row] : -1) : row;
     int cb0 = 0, cb1 = 0;
-    if (e.csr_off && rv) {
+    if (GEN && e.csr_off && rv) {
       cb0 = e.csr_off[row];
       cb1 = e.csr_off[row + 1];
     }
@@ -217,10 +246,10 @@ struct EpiPlain {
         an[q] = (rv && cc < t.N) ? *reinterpret_cast<const uint4*>(e.aux0 + aoff + cc) : make_uint4(0u, 0u, 0u, 0u);
       }
     };
-    const bool use_ring = e.ring != 0;
+    const bool use_ring = GEN ? e.ring != 0 : RES == 2;
     const int nch = chunks(t);
     uint32_t g_done = use_ring ? t.ring_cnt[1] : 0u, g_issued = use_ring ? t.ring_cnt[0] : 0u;
-    if (e.aux0 && !use_ring) fetch(t.nb * BN);
+    if (has_res && !use_ring) fetch(t.nb * BN);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int col0 = t.nb * BN + c;
@@ -239,7 +268,7 @@ struct EpiPlain {
       } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q) ac[q] = an[q];
-        if (e.aux0 && c + 32 < BN) fetch(col0 + 32);
+        if (has_res && c + 32 < BN) fetch(col0 + 32);
       }
       float v[32];
       __syncwarp();
@@ -252,37 +281,37 @@ struct EpiPlain {
           if (cc < t.N) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] *= rs;
-            if (e.col_scale) {
+            if (GEN && e.col_scale) {
               float s8[8];
               load_f32x8(e.col_scale + cc, s8);
 #pragma unroll
               for (int i = 0; i < 8; ++i) x[i] *= s8[i];
             }
-            if (e.aux0) {
+            if (has_res) {
               float r8[8];
               bf16x8_to_f32(ac[g], r8);
 #pragma unroll
               for (int i = 0; i < 8; ++i) x[i] += r8[i];
             }
-            if (e.acc_in) {
+            if (GEN && e.acc_in) {
               float a8[8];
               load_f32x8(e.acc_in + static_cast<int64_t>(row) * e.ld_acc_in + cc, a8);
 #pragma unroll
               for (int i = 0; i < 8; ++i) x[i] += a8[i];
             }
-            if (e.row_coef && arow >= 0) {
+            if (GEN && e.row_coef && arow >= 0) {
               float r8[8];
               load_bf16x8(e.aux1 + arow * e.ld_aux1 + cc, r8);
 #pragma unroll
               for (int i = 0; i < 8; ++i) x[i] -= rc * r8[i];
             }
-            if (e.row_coef2) {
+            if (GEN && e.row_coef2) {
               float r8[8];
               load_bf16x8(e.aux3 + static_cast<int64_t>(row) * e.ld_aux3 + cc, r8);
 #pragma unroll
               for (int i = 0; i < 8; ++i) x[i] -= rc2 * r8[i];
             }
-            for (int j = cb0; j < cb1; ++j) {
+            for (int j = cb0; GEN && j < cb1; ++j) {
               const int32_t t2 = e.csr_idx[j];
               const float w2 = e.csr_w[t2];
               float r8[8];
@@ -290,7 +319,7 @@ struct EpiPlain {
 #pragma unroll
               for (int i = 0; i < 8; ++i) x[i] -= w2 * r8[i];
             }
-            if (e.d_f32) {
+            if (GEN && e.d_f32) {
               float* d = static_cast<float*>(e.D) + static_cast<int64_t>(row) * e.ldd + cc;
               if (e.beta) {
                 float o8[8];
@@ -304,7 +333,7 @@ struct EpiPlain {
                 for (int i = 0; i < 8; ++i) ss += x[i] * x[i];
               }
             } else {
-              if (e.beta) {
+              if (GEN && e.beta) {
                 float o8[8];
                 load_bf16x8(static_cast<const __nv_bfloat16*>(e.D) + static_cast<int64_t>(row) * e.ldd + cc, o8);
 #pragma unroll
@@ -314,7 +343,7 @@ struct EpiPlain {
           }
         }
       }
-      if (!e.d_f32) {
+      if (!GEN || !e.d_f32) {
         // Each output is rounded to bf16 once (packed in pairs); the row's
         // partial sum of squares and the second output read the rounded
         // values back from the packed words.
@@ -449,7 +478,24 @@ struct EpiDSwiglu {
     prefetch_l2_span(e.aux0 + static_cast<int64_t>(t.row) * e.ld_aux0 + cbase, bytes);
     prefetch_l2_span(e.aux1 + static_cast<int64_t>(t.row) * e.ld_aux1 + cbase, bytes);
   }
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
+  // The per-tile choice of loop (FP8 operand scales, the H output) keeps
+  // feature tests out of the chunk loop.
+  static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t) {
+    const bool scaled = e.acc_rs || e.acc_cs;
+    if (e.out3) {
+      if (scaled)
+        tile_impl<true, true>(st, e, t);
+      else
+        tile_impl<false, true>(st, e, t);
+    } else {
+      if (scaled)
+        tile_impl<true, false>(st, e, t);
+      else
+        tile_impl<false, false>(st, e, t);
+    }
+  }
+  template <bool SCALED, bool OUT3>
+  static __device__ __forceinline__ void tile_impl(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
@@ -492,7 +538,7 @@ struct EpiDSwiglu {
       if (c + 32 < BN) fetch(col0 + 32);
       float dh[32], du[32] = {}, h[32] = {};  // rows past M keep zeros (never stored)
       __syncwarp();
-      tmem_ld32_acc(t.taddr + c, dh, e, row, rv, col0, t.N);
+      tmem_ld32_acc_t<SCALED>(t.taddr + c, dh, e, row, rv, col0, t.N);
       if (rv) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -517,7 +563,7 @@ struct EpiDSwiglu {
       }
       warp_store_bf16x32(t.stage, e.out1, e.ld_out1, row0, t.M, col0, t.N, dh, e.st_stream);
       warp_store_bf16x32(t.stage, e.out2, e.ld_out2, row0, t.M, col0, t.N, du, e.st_stream);
-      if (e.out3) warp_store_bf16x32(t.stage, e.out3, e.ld_out3, row0, t.M, col0, t.N, h, e.st_stream);
+      if (OUT3) warp_store_bf16x32(t.stage, e.out3, e.ld_out3, row0, t.M, col0, t.N, h, e.st_stream);
     }
     if (e.partials && rv) e.partials[static_cast<int64_t>(t.nb) * e.ld_part + row] = dot;
   }
@@ -606,15 +652,36 @@ struct EpiRmsDx {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
-  // the tile's rows of x (and dX_resid) into L2 before the accumulator is ready
+  // the tile's rows of x (and dX_resid) into L2, and its slice of gamma
+  // (read by every lane) into L1, before the accumulator is ready
   static __device__ __forceinline__ void prefetch(const EpiArgs& e, const TileInfo& t) {
     const int cbase = t.nb * BN;
-    if (!e.aux_prefetch || t.row >= t.M || cbase >= t.N) return;
+    if (!e.aux_prefetch || cbase >= t.N) return;
     const int cols = min(BN, t.N - cbase);
+    const int lane = threadIdx.x & 31;
+    if (lane * 32 < cols) asm volatile("prefetch.global.L1 [%0];" ::"l"(e.col_scale + cbase + lane * 32));
+    if (t.row >= t.M) return;
     prefetch_l2_span(e.aux1 + static_cast<int64_t>(t.row) * e.ld_aux1 + cbase, cols * 2);
     if (e.aux0) prefetch_l2_span(e.aux0 + static_cast<int64_t>(t.row) * e.ld_aux0 + cbase, cols * 2);
   }
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
+  // The per-tile choice of loop (residual gradient present, FP8 operand
+  // scales) keeps feature tests out of the chunk loop.
+  static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t) {
+    const bool scaled = e.acc_rs || e.acc_cs;
+    if (e.aux0) {
+      if (scaled)
+        tile_impl<true, true>(st, e, t);
+      else
+        tile_impl<true, false>(st, e, t);
+    } else {
+      if (scaled)
+        tile_impl<false, true>(st, e, t);
+      else
+        tile_impl<false, false>(st, e, t);
+    }
+  }
+  template <bool RESID, bool SCALED>
+  static __device__ __forceinline__ void tile_impl(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     const int lane = threadIdx.x & 31;
@@ -630,7 +697,7 @@ struct EpiRmsDx {
         const int cc = col0 + k * 8;
         const bool in = rv && cc < t.N;
         xn[k] = in ? *reinterpret_cast<const uint4*>(e.aux1 + xoff + cc) : make_uint4(0u, 0u, 0u, 0u);
-        rn[k] = (in && e.aux0) ? *reinterpret_cast<const uint4*>(e.aux0 + roff + cc) : make_uint4(0u, 0u, 0u, 0u);
+        rn[k] = (in && RESID) ? *reinterpret_cast<const uint4*>(e.aux0 + roff + cc) : make_uint4(0u, 0u, 0u, 0u);
       }
     };
     fetch(t.nb * BN);
@@ -647,7 +714,7 @@ struct EpiRmsDx {
       if (c + 32 < BN) fetch(col0 + 32);
       float v[32];
       __syncwarp();
-      tmem_ld32_acc(t.taddr + c, v, e, row, rv, col0, t.N);
+      tmem_ld32_acc_t<SCALED>(t.taddr + c, v, e, row, rv, col0, t.N);
       float p[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) p[i] = 0.f;
@@ -659,13 +726,13 @@ struct EpiRmsDx {
             float x8[8], s8[8], r8[8];
             bf16x8_to_f32(xc[g], x8);
             load_f32x8(e.col_scale + cc, s8);
-            if (e.aux0) bf16x8_to_f32(rcur[g], r8);
+            if (RESID) bf16x8_to_f32(rcur[g], r8);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float d = v[g * 8 + i];
               p[g * 8 + i] = x8[i] * d;
               float o = d * s8[i];
-              if (e.aux0) o += r8[i];
+              if (RESID) o += r8[i];
               v[g * 8 + i] = o - rc * x8[i];
             }
           }

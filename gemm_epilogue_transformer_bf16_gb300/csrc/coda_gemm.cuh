@@ -126,6 +126,7 @@ struct EpiArgs {
   int st_stream;                // epilogue tile stores as streaming (.cs) stores
   int aux_prefetch;             // request the tile's auxiliary rows into L2 before its accumulator is ready
   int ring;                     // tensors the epilogue reads through the TMA ring (0: plain loads)
+  int no_lean;                  // 1: the plain epilogue runs its general chunk loop (for comparisons)
   int mode;                     // SIGMOID: 0 forward, 1 backward on the recomputed logits
   float* target_logit;
   int64_t col_base;             // CE_DLOGITS: vocabulary column of the launch's column 0 (a vocabulary slice)
