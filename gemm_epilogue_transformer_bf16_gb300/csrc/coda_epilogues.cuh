@@ -414,7 +414,24 @@ struct EpiSwiglu {
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void prefetch(const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
+  // per-tile choice of loop: per-column scales (FP8 weights), stored g and u
+  static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t) {
+    const bool gu = e.out1 && e.out2;
+    if (e.col_scale) {
+      if (gu)
+        tile_impl<true, true>(st, e, t);
+      else
+        tile_impl<true, false>(st, e, t);
+    } else {
+      if (gu)
+        tile_impl<false, true>(st, e, t);
+      else
+        tile_impl<false, false>(st, e, t);
+    }
+  }
+  // GU: both g and u are stored (otherwise each only if its pointer is set)
+  template <bool CS, bool GU>
+  static __device__ __forceinline__ void tile_impl(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     const float rs = ((e.row_scale && rv) ? e.row_scale[row] : 1.f) * ((e.row_scale2 && rv) ? e.row_scale2[row] : 1.f);
@@ -432,7 +449,7 @@ struct EpiSwiglu {
         for (int q = 0; q < 4; ++q) {
           const int cc = col0 + q * 8;
           float cg[8], cu[8];
-          if (e.col_scale && cc < t.N) {
+          if (CS && cc < t.N) {
             load_f32x8(e.col_scale + cc, cg);
             load_f32x8(e.col_scale2 + cc, cu);
           }
@@ -440,7 +457,7 @@ struct EpiSwiglu {
           for (int i = 0; i < 8; ++i) {
             g[q * 8 + i] *= rs;
             u[q * 8 + i] *= rs;
-            if (e.col_scale && cc < t.N) {
+            if (CS && cc < t.N) {
               g[q * 8 + i] *= cg[i];
               u[q * 8 + i] *= cu[i];
             }
@@ -452,8 +469,8 @@ struct EpiSwiglu {
       for (int i = 0; i < 32; ++i) h[i] = g[i] / (1.f + __expf(-g[i])) * u[i];
       auto* D = static_cast<__nv_bfloat16*>(e.D);
       warp_store_bf16x32(t.stage, D, e.ldd, row0, t.M, col0, t.N, h, e.st_stream);
-      if (e.out1) warp_store_bf16x32(t.stage, e.out1, e.ld_out1, row0, t.M, col0, t.N, g, e.st_stream);
-      if (e.out2) warp_store_bf16x32(t.stage, e.out2, e.ld_out2, row0, t.M, col0, t.N, u, e.st_stream);
+      if (GU || e.out1) warp_store_bf16x32(t.stage, e.out1, e.ld_out1, row0, t.M, col0, t.N, g, e.st_stream);
+      if (GU || e.out2) warp_store_bf16x32(t.stage, e.out2, e.ld_out2, row0, t.M, col0, t.N, u, e.st_stream);
     }
   }
 };
@@ -770,18 +787,33 @@ struct EpiCeLse {
           make_float2(st.m, st.s);
   }
   static __device__ __forceinline__ void prefetch(const EpiArgs&, const TileInfo&) {}
+  // per-tile choice of loop: FP8 operand scales, row scale
   static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t) {
+    if (e.acc_rs || e.acc_cs) {
+      if (e.row_scale)
+        tile_impl<true, true>(st, e, t);
+      else
+        tile_impl<true, false>(st, e, t);
+    } else {
+      if (e.row_scale)
+        tile_impl<false, true>(st, e, t);
+      else
+        tile_impl<false, false>(st, e, t);
+    }
+  }
+  template <bool SCALED, bool ROWSCALE>
+  static __device__ __forceinline__ void tile_impl(State& st, const EpiArgs& e, const TileInfo& t) {
     const bool rv = t.row < t.M;
-    const float rs = (e.row_scale && rv) ? e.row_scale[t.row] : 1.f;
+    const float rs = (ROWSCALE && rv) ? e.row_scale[t.row] : 1.f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int col0 = t.nb * BN + c;
       if (col0 >= t.N) break;
       float z[32];
       __syncwarp();
-      tmem_ld32_acc(t.taddr + c, z, e, t.row, rv, col0, t.N);
+      tmem_ld32_acc_t<SCALED>(t.taddr + c, z, e, t.row, rv, col0, t.N);
       if (rv) {
-        if (e.row_scale) {
+        if (ROWSCALE) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) z[i] *= rs;
         }
@@ -834,7 +866,23 @@ struct EpiCeDlogits {
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void prefetch(const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
+  // The per-tile choice of loop (FP8 operand scales, the -w label term, the
+  // target-logit output) keeps feature tests out of the per-element math.
+  static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t) {
+    const int k = ((e.acc_rs || e.acc_cs) ? 4 : 0) | (e.onehot ? 2 : 0) | (e.target_logit ? 1 : 0);
+    switch (k) {
+      case 0: tile_impl<false, false, false>(st, e, t); break;
+      case 1: tile_impl<false, false, true>(st, e, t); break;
+      case 2: tile_impl<false, true, false>(st, e, t); break;
+      case 3: tile_impl<false, true, true>(st, e, t); break;
+      case 4: tile_impl<true, false, false>(st, e, t); break;
+      case 5: tile_impl<true, false, true>(st, e, t); break;
+      case 6: tile_impl<true, true, false>(st, e, t); break;
+      default: tile_impl<true, true, true>(st, e, t); break;
+    }
+  }
+  template <bool SCALED, bool ONEHOT, bool TARGET>
+  static __device__ __forceinline__ void tile_impl(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
     int lab = -1;
@@ -854,6 +902,7 @@ struct EpiCeDlogits {
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
     const float ws = w * rs;
     const float lb = lse * LOG2E;
+    const int row0 = row - static_cast<int>(threadIdx.x & 31);
     float pz = 0.f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
@@ -861,26 +910,24 @@ struct EpiCeDlogits {
       if (col0 >= t.N) break;
       float z[32];
       __syncwarp();
-      tmem_ld32_acc(t.taddr + c, z, e, row, rv, col0, t.N);
+      tmem_ld32_acc_t<SCALED>(t.taddr + c, z, e, row, rv, col0, t.N);
       if (rv) {
-        __nv_bfloat16* d = static_cast<__nv_bfloat16*>(e.D) + static_cast<int64_t>(row) * e.ldd;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int cc = col0 + g * 8;
           if (cc < t.N) {
-            float x[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float zz = z[g * 8 + i] * rs;
               const float p = exp2f(fmaf(zz, LOG2E, -lb));
-              x[i] = (p - (e.onehot && cc + i == lab ? 1.f : 0.f)) * ws;
+              z[g * 8 + i] = (p - (ONEHOT && cc + i == lab ? 1.f : 0.f)) * ws;
               pz += p * zz;
-              if (e.target_logit && cc + i == lab) e.target_logit[row] = zz;
+              if (TARGET && cc + i == lab) e.target_logit[row] = zz;
             }
-            store_bf16x8(d + cc, x, e.st_stream);
           }
         }
       }
+      warp_store_bf16x32(t.stage, static_cast<__nv_bfloat16*>(e.D), e.ldd, row0, t.M, col0, t.N, z, e.st_stream);
     }
     if (e.partials && rv) e.partials[static_cast<int64_t>(t.nb) * e.ld_part + row] = pz;
   }
