@@ -1005,11 +1005,42 @@ struct EpiQkRope {
   struct State {};
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void prefetch(const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
+  // Before the accumulator is ready: the lane's row of the cos/sin table
+  // (512 bytes at its position) into L2 and the two gains into L1.
+  static __device__ __forceinline__ void prefetch(const EpiArgs& e, const TileInfo& t) {
+    if (!e.aux_prefetch) return;
+    const int lane = threadIdx.x & 31;
+    if (lane < 4 && e.gamma_q) asm volatile("prefetch.global.L1 [%0];" ::"l"(e.gamma_q + lane * 32));
+    else if (lane >= 4 && lane < 8 && e.gamma_k)
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(e.gamma_k + (lane - 4) * 32));
+    if (t.row >= t.M) return;
+    int pos = e.pos[t.row];
+    pos = pos < 0 ? 0 : (pos >= e.max_pos ? e.max_pos - 1 : pos);
+    prefetch_l2_span(e.cos_sin + static_cast<int64_t>(pos) * 64, 64 * 8);
+  }
+  // per-tile choice of loop: FP8 operand scales, saved pre-norm q|k (out1)
+  static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t) {
+    const bool scaled = e.acc_rs || e.acc_cs;
+    if (e.out1) {
+      if (scaled)
+        tile_impl<true, true>(st, e, t);
+      else
+        tile_impl<false, true>(st, e, t);
+    } else {
+      if (scaled)
+        tile_impl<true, false>(st, e, t);
+      else
+        tile_impl<false, false>(st, e, t);
+    }
+  }
+  // Outputs leave through the warp's transpose buffer (rows row0 .. row0 + 31
+  // of a head's 128 columns); the cos/sin pairs are read 16 bytes at a time.
+  template <bool SCALED, bool OUT1>
+  static __device__ __forceinline__ void tile_impl(State&, const EpiArgs& e, const TileInfo& t) {
     constexpr int D = 128;
     const int row = t.row;
     const bool rv = row < t.M;
+    const int row0 = row - static_cast<int>(threadIdx.x & 31);
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
     int pos = 0;
     if (rv) {
@@ -1019,101 +1050,93 @@ struct EpiQkRope {
         pos = pos < 0 ? 0 : e.max_pos - 1;
       }
     }
-    const float2* cs = e.cos_sin + static_cast<int64_t>(pos) * (D / 2);
-    const int64_t off = static_cast<int64_t>(row);
+    const float4* cs4 = reinterpret_cast<const float4*>(e.cos_sin + static_cast<int64_t>(pos) * (D / 2));
+    const bool st = e.st_stream != 0;
 #pragma unroll 1
     for (int hh = 0; hh < BN / D; ++hh) {
       const int head = t.nb * (BN / D) + hh;
       if (head * D >= t.N) break;
       const uint32_t tcol = t.taddr + hh * D;
       if (head >= e.n_q + e.n_kv) {
-        __nv_bfloat16* vout = e.V + off * e.ldv + (head - e.n_q - e.n_kv) * D;
+        __nv_bfloat16* vbase = e.V + (head - e.n_q - e.n_kv) * D;
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           float v[32];
           __syncwarp();
-          tmem_ld32_acc(tcol + c, v, e, row, rv, head * D + c, t.N);
-          if (rv) {
+          tmem_ld32_acc_t<SCALED>(tcol + c, v, e, row, rv, head * D + c, t.N);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= rs;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) store_bf16x8(vout + c + g * 8, v + g * 8, e.st_stream);
-          }
+          for (int i = 0; i < 32; ++i) v[i] *= rs;
+          warp_store_bf16x32(t.stage, vbase, e.ldv, row0, t.M, c, D, v, st);
         }
         continue;
       }
       const bool is_q = head < e.n_q;
       const float* gamma = is_q ? e.gamma_q : e.gamma_k;
-      __nv_bfloat16* out = is_q ? e.Q + off * e.ldq + head * D : e.Kh + off * e.ldk + (head - e.n_q) * D;
+      __nv_bfloat16* obase = is_q ? e.Q + head * D : e.Kh + (head - e.n_q) * D;
+      const int64_t ldo = is_q ? e.ldq : e.ldk;
       float ss = 0.f;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         float v[32];
         __syncwarp();
-        tmem_ld32_acc(tcol + c, v, e, row, rv, head * D + c, t.N);
+        tmem_ld32_acc_t<SCALED>(tcol + c, v, e, row, rv, head * D + c, t.N);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           v[i] *= rs;
           ss += v[i] * v[i];
         }
-        if (rv && e.out1) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) store_bf16x8(e.out1 + off * e.ld_out1 + head * D + c + g * 8, v + g * 8, e.st_stream);
-        }
+        if (OUT1) warp_store_bf16x32(t.stage, e.out1 + head * D, e.ld_out1, row0, t.M, c, D, v, st);
       }
       const float rho = rsqrtf(ss * (1.f / D) + e.eps);
+      const float sr = rs * rho;
       if constexpr (HALF) {
         // pair j = c + i of the first half with j + 64 of the second half
 #pragma unroll 1
         for (int c = 0; c < D / 2; c += 32) {
           float v1[32], v2[32];
           __syncwarp();
-          tmem_ld32_acc(tcol + c, v1, e, row, rv, head * D + c, t.N);
-          tmem_ld32_acc(tcol + D / 2 + c, v2, e, row, rv, head * D + D / 2 + c, t.N);
-          if (rv) {
-            float g1[32], g2[32];
+          tmem_ld32_acc_t<SCALED>(tcol + c, v1, e, row, rv, head * D + c, t.N);
+          tmem_ld32_acc_t<SCALED>(tcol + D / 2 + c, v2, e, row, rv, head * D + D / 2 + c, t.N);
+          float g1[32], g2[32];
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              load_f32x8(gamma + c + g * 8, g1 + g * 8);
-              load_f32x8(gamma + D / 2 + c + g * 8, g2 + g * 8);
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float2 r = cs[c + i];
-              const float a = v1[i] * rs * rho * g1[i];
-              const float b = v2[i] * rs * rho * g2[i];
-              v1[i] = a * r.x - b * r.y;
-              v2[i] = a * r.y + b * r.x;
-            }
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              store_bf16x8(out + c + g * 8, v1 + g * 8, e.st_stream);
-              store_bf16x8(out + D / 2 + c + g * 8, v2 + g * 8, e.st_stream);
-            }
+          for (int g = 0; g < 4; ++g) {
+            load_f32x8(gamma + c + g * 8, g1 + g * 8);
+            load_f32x8(gamma + D / 2 + c + g * 8, g2 + g * 8);
           }
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float4 r = cs4[(c + i) / 2];  // pairs c + i and c + i + 1
+            const float a0 = v1[i] * sr * g1[i], b0 = v2[i] * sr * g2[i];
+            const float a1 = v1[i + 1] * sr * g1[i + 1], b1 = v2[i + 1] * sr * g2[i + 1];
+            v1[i] = a0 * r.x - b0 * r.y;
+            v2[i] = a0 * r.y + b0 * r.x;
+            v1[i + 1] = a1 * r.z - b1 * r.w;
+            v2[i + 1] = a1 * r.w + b1 * r.z;
+          }
+          warp_store_bf16x32(t.stage, obase, ldo, row0, t.M, c, D, v1, st);
+          warp_store_bf16x32(t.stage, obase, ldo, row0, t.M, D / 2 + c, D, v2, st);
         }
       } else {
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           float v[32];
           __syncwarp();
-          tmem_ld32_acc(tcol + c, v, e, row, rv, head * D + c, t.N);
-          if (rv) {
-            float gm[32];
+          tmem_ld32_acc_t<SCALED>(tcol + c, v, e, row, rv, head * D + c, t.N);
+          float gm[32];
 #pragma unroll
-            for (int g = 0; g < 4; ++g) load_f32x8(gamma + c + g * 8, gm + g * 8);
-            float o[32];
+          for (int g = 0; g < 4; ++g) load_f32x8(gamma + c + g * 8, gm + g * 8);
+          float o[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float2 r = cs[c / 2 + i];
-              const float a = v[2 * i] * rs * rho * gm[2 * i];
-              const float b = v[2 * i + 1] * rs * rho * gm[2 * i + 1];
-              o[2 * i] = a * r.x - b * r.y;
-              o[2 * i + 1] = a * r.y + b * r.x;
-            }
-#pragma unroll
-            for (int g = 0; g < 4; ++g) store_bf16x8(out + c + g * 8, o + g * 8, e.st_stream);
+          for (int i = 0; i < 16; i += 2) {
+            const float4 r = cs4[(c / 2 + i) / 2];  // pairs c/2 + i and c/2 + i + 1
+            const float a0 = v[2 * i] * sr * gm[2 * i], b0 = v[2 * i + 1] * sr * gm[2 * i + 1];
+            const float a1 = v[2 * i + 2] * sr * gm[2 * i + 2], b1 = v[2 * i + 3] * sr * gm[2 * i + 3];
+            o[2 * i] = a0 * r.x - b0 * r.y;
+            o[2 * i + 1] = a0 * r.y + b0 * r.x;
+            o[2 * i + 2] = a1 * r.z - b1 * r.w;
+            o[2 * i + 3] = a1 * r.w + b1 * r.z;
           }
+          warp_store_bf16x32(t.stage, obase, ldo, row0, t.M, c, D, o, st);
         }
       }
     }
