@@ -596,7 +596,8 @@ def main():
         # RMSNorm-reparameterised projection + residual, 4096 x 2048 -> 2048,
         # forward and backward (gain fold, row RMS, prepass and combines
         # included); outputs and workspaces held across calls as a training
-        # loop holds them; dW on a second stream beside c -> dX
+        # loop holds them; the gain fold beside the row RMS and dW beside
+        # c -> dX on second streams
         s2 = synth.FULL["rmsnorm_linear"]
         d2 = {k: v.to(dev) for k, v in synth.make_rms_linear(s2, seed=0).items()}
         M2, N2, K2 = s2.tokens, s2.out, s2.hidden
@@ -609,10 +610,22 @@ def main():
         g2 = {"dX": torch.empty_like(d2["X"]), "dW": torch.empty_like(d2["W"]),
               "dgamma": torch.empty(K2, dtype=torch.float32, device=dev)}
         side2 = torch.cuda.Stream(device=dev)
+        side2f = torch.cuda.Stream(device=dev)
+        ev_prev, ev_fold = torch.cuda.Event(), torch.cuda.Event()
 
         def rms_step():
-            coda.fold_gamma(d2["W"], d2["gamma"], out=Wf2)
-            coda.rmsnorm_linear(d2["X"], Wf2, d2["R"], eps=s2.eps, rstd_out=r2, Y=Y2, ws=ws2a)
+            # the gain fold runs on a second stream beside the row RMS (each
+            # reads only inputs, and the fold waits for the previous step's
+            # reads of W'); the projection waits for both
+            cur = torch.cuda.current_stream()
+            ev_prev.record(cur)
+            side2f.wait_event(ev_prev)
+            with torch.cuda.stream(side2f):
+                coda.fold_gamma(d2["W"], d2["gamma"], out=Wf2)
+                ev_fold.record(side2f)
+            coda.rms_rstd(d2["X"], s2.eps, out=r2)
+            cur.wait_event(ev_fold)
+            coda.rmsnorm_linear(d2["X"], Wf2, d2["R"], rstd_in=r2, Y=Y2, ws=ws2a)
             coda.rmsnorm_linear_bwd(d2["G"], d2["X"], d2["W"], d2["gamma"], r2, Y2, d2["R"], ws=ws2b, out=g2,
                                     side_stream=side2)
         m2 = median_ms(rms_step)

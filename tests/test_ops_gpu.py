@@ -61,6 +61,27 @@ def test_rmsnorm_linear_fwd_bwd(coda, shape):
     assert_bf16(g["dgamma"], b["dgamma"], "dgamma")
 
 
+@pytest.mark.parametrize("shape", [synth.RmsLinearShape(), synth.RmsLinearShape(300, 264, 200)])
+def test_rmsnorm_linear_rstd_in(coda, shape):
+    """The projection with a row factor computed beforehand (coda_rms_rstd,
+    passed as rstd_in), the fold and the row RMS on two streams: the same Y as
+    the oracle's RMSNorm-linear forward."""
+    t = synth.make_rms_linear(shape, seed=0)
+    d, o = dev(t), f64(t)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        Wf = coda.fold_gamma(d["W"], d["gamma"])
+    r = coda.rms_rstd(d["X"], shape.eps)
+    torch.cuda.current_stream().wait_stream(side)
+    Y, r2 = coda.rmsnorm_linear(d["X"], Wf, R=d["R"], rstd_in=r, eps=shape.eps)
+    torch.cuda.synchronize()
+    assert r2 is r
+    yr, rr = O.rmsnorm_linear_fwd(o["X"], o["gamma"], o["W"], shape.eps, o["R"])
+    assert_f32(r, rr, "rstd")
+    assert_bf16(Y, yr, "Y (rstd_in)")
+
+
 def test_fold_gamma_and_rstd(coda):
     t = synth.make_rms_linear(synth.RmsLinearShape(64, 128, 72), seed=3)
     d, o = dev(t), f64(t)
