@@ -28,7 +28,8 @@ __all__ = [
     "linear_cross_entropy", "linear_cross_entropy_bwd", "linear_cross_entropy_noalloc", "workspace",
     "rmsnorm_linear_cross_entropy", "rmsnorm_linear_cross_entropy_bwd", "rms_rstd",
     "linear_sigmoid", "linear_sigmoid_bwd", "quantize_fp8_rows", "linear_fp8", "linear_swiglu_fp8", "quantize_nvfp4_rows", "rmsnorm_scale_nvfp4", "linear_nvfp4",
-    "linear_swiglu_nvfp4",
+    "linear_swiglu_nvfp4", "quantize_fp8_cols", "linear_qknorm_rope_fp8", "linear_cross_entropy_fp8",
+    "linear_cross_entropy_bwd_fp8", "linear_dswiglu_fp8", "rmsnorm_linear_dx_fp8", "launch_count",
     "MAP_NONE", "MAP_SWIGLU", "MAP_DSWIGLU", "MAP_QKNORM_ROPE", "MAP_CE_LSE",
     "MAP_CE_DLOGITS", "MAP_COLDOT", "MAP_SIGMOID", "MAP_DSIGMOID", "K_MAJOR", "MN_MAJOR",
 ]
@@ -47,6 +48,7 @@ _SZ = ctypes.c_size_t
 # name -> argtypes (restype int unless noted)
 _SIGS = {
     "coda_version": ([], ctypes.c_char_p),
+    "coda_launch_count": ([], ctypes.c_uint64),
     "coda_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "coda_get_status": ([_P, _P], ctypes.c_int),
     "coda_reset_status": ([_P, _P], ctypes.c_int),
@@ -262,6 +264,11 @@ def get_status(ws, stream=None):
 
 def reset_status(ws, stream=None):
     _check("coda_reset_status", load().coda_reset_status(_ptr(ws), _stream(stream)))
+
+
+def launch_count():
+    """Kernels this library has launched in this process (coda_launch_count)."""
+    return int(load().coda_launch_count())
 
 
 # ---------------------------------------------------------------------------

@@ -17,6 +17,13 @@
 #include "coda_internal.h"
 #include "coda_status.h"
 
+namespace coda {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace coda
+
 using coda::EpiArgs;
 using coda::GemmArgs;
 
@@ -539,6 +546,8 @@ __nv_bfloat16* BF(coda_bf16* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
 extern "C" {
 
 const char* coda_version(void) { return "coda-gb300 0.1.0 (sm_103a)"; }
+
+uint64_t coda_launch_count(void) { return coda::g_launches.load(std::memory_order_relaxed); }
 
 const char* coda_status_string(int st) {
   switch (st) {

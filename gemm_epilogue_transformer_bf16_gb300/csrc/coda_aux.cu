@@ -43,6 +43,7 @@ cudaError_t launch_fold_gamma(const __nv_bfloat16* W, const float* gamma, __nv_b
                               int num_sms, cudaStream_t s) {
   const int64_t total8 = N * K / 8;
   const int64_t blocks = std::min<int64_t>((total8 + 255) / 256, static_cast<int64_t>(num_sms) * 8);
+  note_launch();
   fold_gamma_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(W, gamma, Wf, N, K);
   return cudaGetLastError();
 }
@@ -81,6 +82,7 @@ __global__ void row_rstd_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx
 cudaError_t launch_row_rstd(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, float eps, float* rstd,
                             int num_sms, cudaStream_t s, const float* gamma, __nv_bfloat16* U, int64_t ldu) {
   const int64_t blocks = std::min<int64_t>((M + 7) / 8, static_cast<int64_t>(num_sms) * 8);
+  note_launch();
   row_rstd_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(X, ldx, M, K, eps, rstd, gamma,
                                                                                        U, ldu);
   return cudaGetLastError();
@@ -106,6 +108,7 @@ __global__ void combine_rows_kernel(const float* __restrict__ p, int64_t ld, int
 cudaError_t launch_combine_rows(const float* p, int64_t ld, int nparts, int64_t M, float inv_k, float eps,
                                 const float* r, float* out, int mode, cudaStream_t s) {
   const int64_t blocks = std::min<int64_t>((M + 255) / 256, 4096);
+  note_launch();
   combine_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(p, ld, nparts, M, inv_k,
                                                                                           eps, r, out, mode);
   return cudaGetLastError();
@@ -150,6 +153,7 @@ cudaError_t launch_rms_bwd_prepass(const __nv_bfloat16* G, const __nv_bfloat16* 
                                    const float* rstd, int64_t M, int64_t N, float inv_k, __nv_bfloat16* Gp,
                                    float* coef, int num_sms, cudaStream_t s) {
   const int64_t blocks = std::min<int64_t>((M + 7) / 8, static_cast<int64_t>(num_sms) * 8);
+  note_launch();
   rms_bwd_prepass_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(G, Y, R, rstd, M, N,
                                                                                              inv_k, Gp, coef);
   return cudaGetLastError();
@@ -184,6 +188,7 @@ __global__ void colsum_kernel(const float* __restrict__ p, int64_t nrows, int64_
 cudaError_t launch_colsum(const float* p, int64_t nrows, int64_t ncols, int64_t ld, float* out, cudaStream_t s,
                           int64_t split, float* out2) {
   if (split < 0 || !out2) split = ncols;
+  note_launch();
   colsum_kernel<<<static_cast<unsigned>((ncols + 31) / 32), 1024, 0, s>>>(p, nrows, ncols, ld, out, split, out2);
   return cudaGetLastError();
 }
@@ -256,10 +261,12 @@ cudaError_t launch_ce_combine(const float2* part, int64_t ld, int nchunks, const
                               const int32_t* labels, int32_t ignore, int64_t M, int64_t V, float* lse,
                               double* blk_loss, int* blk_cnt, int nblk, float* loss_mean, int32_t* n_valid,
                               int* status, cudaStream_t s) {
+  note_launch();
   ce_combine_kernel<<<nblk, CE_COMBINE_THREADS, 0, s>>>(part, ld, nchunks, target, labels, ignore, M, V, lse,
                                                         blk_loss, blk_cnt, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  note_launch();
   ce_finalize_kernel<<<1, 32, 0, s>>>(blk_loss, blk_cnt, nblk, loss_mean, n_valid);
   return cudaGetLastError();
 }
@@ -343,13 +350,17 @@ cudaError_t launch_ce_onehot_prep(const int32_t* labels, int32_t ignore, int64_t
   if ((e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * V, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(cursor, 0, sizeof(int32_t) * V, s)) != cudaSuccess) return e;
   const unsigned mb = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((M + 255) / 256, 1024)));
+  note_launch();
   ce_prep_kernel<<<mb, 256, 0, s>>>(labels, ignore, M, V, n_valid, dloss, rstd, wrow, lrow, counts);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  note_launch();
   scan_counts_kernel<<<1, 1024, 0, s>>>(counts, V, off);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  note_launch();
   ce_fill_kernel<<<mb, 256, 0, s>>>(lrow, M, off, cursor, idx);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const unsigned vb = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((V + 255) / 256, 1024)));
+  note_launch();
   ce_sort_buckets_kernel<<<vb, 256, 0, s>>>(off, V, idx);
   return cudaGetLastError();
 }
@@ -378,6 +389,7 @@ __global__ void ce_norm_coef_kernel(const float* __restrict__ pz, int64_t ld, in
 cudaError_t launch_ce_norm_coef(const float* pz, int64_t ld, int nparts, const float* target, const float* rstd,
                                 const float* rw, int64_t M, float inv_k, float* coef, cudaStream_t s) {
   const int64_t blocks = std::min<int64_t>((M + 255) / 256, 4096);
+  note_launch();
   ce_norm_coef_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(pz, ld, nparts, target,
                                                                                           rstd, rw, M, inv_k, coef);
   return cudaGetLastError();
@@ -517,11 +529,14 @@ cudaError_t launch_quantize_fp8_cols(const __nv_bfloat16* X, int64_t ldx, int64_
   const int64_t want = std::max<int64_t>(1, (4 * static_cast<int64_t>(num_sms) + cblk - 1) / cblk);
   const int64_t rsplit = std::min<int64_t>(want, std::max<int64_t>(1, (RT + 63) / 64));
   const int rows = static_cast<int>((RT + rsplit - 1) / rsplit);
+  note_launch();
   fp8_col_amax_kernel<<<dim3(static_cast<unsigned>(cblk), static_cast<unsigned>(rsplit)), 256, 0, s>>>(
       X, ldx, R, X2, ldx2, R2, C, rows, reinterpret_cast<unsigned int*>(scale));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  note_launch();
   fp8_amax_to_scale_kernel<<<static_cast<unsigned>(std::min<int64_t>((C + 255) / 256, 1024)), 256, 0, s>>>(scale, C);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  note_launch();
   fp8_col_quant_kernel<<<dim3(static_cast<unsigned>((C + 63) / 64), static_cast<unsigned>((RT + 63) / 64)), 256, 0,
                          s>>>(X, ldx, R, X2, ldx2, R2, C, scale, out, ldo);
   return cudaGetLastError();
@@ -530,6 +545,7 @@ cudaError_t launch_quantize_fp8_cols(const __nv_bfloat16* X, int64_t ldx, int64_
 cudaError_t launch_quantize_fp8_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq,
                                      int64_t ldq, float* scale, int num_sms, cudaStream_t s) {
   const int64_t blocks = std::min<int64_t>((M + 7) / 8, static_cast<int64_t>(num_sms) * 8);
+  note_launch();
   quantize_fp8_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(X, ldx, M, K, Xq,
                                                                                                ldq, scale);
   return cudaGetLastError();
@@ -551,6 +567,7 @@ __global__ void selftest_wait_timeout_kernel(uint64_t limit_ns, int* status) {
 }
 
 cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t s) {
+  note_launch();
   selftest_wait_timeout_kernel<<<1, 32, 0, s>>>(limit_ns, status);
   return cudaGetLastError();
 }
@@ -574,6 +591,7 @@ __global__ void rope_table_kernel(double theta, int head_dim, int max_pos, float
 cudaError_t launch_rope_table(double theta, int head_dim, int max_pos, float2* cs, cudaStream_t s) {
   const int64_t total = static_cast<int64_t>(max_pos) * (head_dim / 2);
   const int64_t blocks = std::min<int64_t>((total + 255) / 256, 4096);
+  note_launch();
   rope_table_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(theta, head_dim, max_pos,
                                                                                        cs);
   return cudaGetLastError();
@@ -1066,6 +1084,7 @@ cudaError_t launch_qk_bwd_tma(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, 
       raised[dev][rope_half] = true;
     }
   }
+  note_launch();
   k<<<nblk, (QKT_WARPS + 1) * 32, smem, s>>>(dQ, dK, dV, qk_save, V, gq, gk, pos, cs, max_pos, eps, n_q, n_kv, rstd,
                                              M, inv_k, Gp, coef, dgam_part, status, stages, timeout_ns);
   return cudaGetLastError();
@@ -1076,6 +1095,7 @@ cudaError_t launch_qk_bwd(const __nv_bfloat16* dQ, const __nv_bfloat16* dK, cons
                           const int32_t* pos, const float2* cs, int max_pos, float eps, int n_q, int n_kv,
                           const float* rstd, int64_t M, float inv_k, __nv_bfloat16* Gp, float* coef,
                           float* dgam_part, int nblk, int* status, cudaStream_t s, bool rope_half) {
+  note_launch();
   if (rope_half)
     qk_bwd_kernel<true><<<nblk, QK_BWD_WARPS * 32, 0, s>>>(dQ, dK, dV, qk_save, V, gq, gk, pos, cs, max_pos, eps,
                                                            n_q, n_kv, rstd, M, inv_k, Gp, coef, dgam_part, status);

@@ -12,6 +12,10 @@ namespace coda {
 
 enum class EpiKind : int { Plain = 0, Swiglu, DSwiglu, QkRope, CeLse, CeDlogits, ColDot, Sigmoid, RmsDx };
 
+// Counts a kernel launch issued by this library (every launch site calls it
+// just before its launch); coda_launch_count returns the process-wide total.
+void note_launch();
+
 // Tensor maps in the order A0, B0, A1, B1.  `cg` is the cluster size: 1
 // (single CTAs), 2 (a cta_group::2 pair) or 4 (two pairs sharing B by TMA
 // multicast); the launcher sizes the persistent grid.

@@ -95,6 +95,7 @@ cudaError_t launch_gemm_variant(int num_units, int sms, cudaStream_t s, const CU
     cfg.attrs = attr;
     ++cfg.numAttrs;
   }
+  note_launch();
   e = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], m[4], m[5], a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -678,6 +678,7 @@ cudaError_t launch_nvfp4(int num_units, int sms, cudaStream_t s, const CUtensorM
   }
   const int resident = max_clusters[dev].load(std::memory_order_relaxed);
   cfg.gridDim = dim3(static_cast<unsigned>(CG * std::min(num_units, resident)));
+  note_launch();
   e = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], a, sc);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -954,6 +955,7 @@ cudaError_t launch_nvfp4_pair(int num_units, int sms, cudaStream_t s, const CUte
   }
   const int resident = max_clusters[dev].load(std::memory_order_relaxed);
   cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(num_units, resident)));
+  note_launch();
   e = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], m[4], m[5], a, sc);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -999,6 +1001,7 @@ cudaError_t launch_quantize_nvfp4_rows(const __nv_bfloat16* X, int64_t ldx, int6
   const int64_t kt = (K + 255) / 256;
   const int64_t blocks = std::min<int64_t>((rows_pad + 7) / 8, static_cast<int64_t>(num_sms) * 8);
   const unsigned grid = static_cast<unsigned>(std::max<int64_t>(blocks, 1));
+  note_launch();
   if (gamma && rstd)
     quantize_nvfp4_rows_kernel<true, true><<<grid, 256, 0, s>>>(X, ldx, M, K, Q, SF, scale, rows_pad, kt, gamma,
                                                                   rstd, eps);

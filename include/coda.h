@@ -159,6 +159,13 @@ enum { CODA_OPERAND_BF16 = 0, CODA_OPERAND_E4M3 = 1 };
 /* Version string of the library. */
 const char* coda_version(void);
 
+/* Number of kernels this library has launched in the calling process, on
+ * every device and stream, since it was loaded (a host-side counter: each
+ * launch site counts its launch as it issues it; failed launches included,
+ * driver memsets and copies not).  Read it before and after a region to
+ * count that region's launches.  Never fails. */
+uint64_t coda_launch_count(void);
+
 /* Human-readable name of a status code. */
 const char* coda_status_string(int status);
 

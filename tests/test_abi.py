@@ -22,7 +22,7 @@ def lib():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"\b(?:int|size_t|const char\s*\*)\s+(coda_\w+)\s*\(", src)
+    names = re.findall(r"\b(?:int|size_t|uint64_t|const char\s*\*)\s+(coda_\w+)\s*\(", src)
     return sorted(set(names))
 
 
@@ -43,6 +43,18 @@ def test_binding_covers_every_symbol():
     import gemm_epilogue_transformer_bf16_gb300 as coda
     missing = [n for n in declared_functions() if n not in coda._SIGS]
     assert not missing, f"no ctypes signature for: {missing}"
+
+
+def test_launch_count_without_launches(lib):
+    """The launch counter is host state: readable without a GPU, and zero
+    on a host without one (nothing can have been launched)."""
+    import torch
+    import gemm_epilogue_transformer_bf16_gb300 as coda
+    assert "coda_launch_count" in declared_functions()
+    n = coda.launch_count()
+    assert n >= 0
+    if not torch.cuda.is_available():
+        assert n == 0
 
 
 def test_version_and_status_strings(lib):

@@ -82,6 +82,20 @@ def test_rmsnorm_linear_rstd_in(coda, shape):
     assert_bf16(Y, yr, "Y (rstd_in)")
 
 
+def test_launch_count(coda):
+    """coda_launch_count counts each kernel launch once: the gain fold and
+    the row RMS are one kernel each."""
+    t = synth.make_rms_linear(synth.RmsLinearShape(64, 128, 72), seed=3)
+    d = dev(t)
+    c0 = coda.launch_count()
+    coda.fold_gamma(d["W"], d["gamma"])
+    c1 = coda.launch_count()
+    coda.rms_rstd(d["X"], 1e-6)
+    c2 = coda.launch_count()
+    torch.cuda.synchronize()
+    assert (c1 - c0, c2 - c1) == (1, 1)
+
+
 def test_fold_gamma_and_rstd(coda):
     t = synth.make_rms_linear(synth.RmsLinearShape(64, 128, 72), seed=3)
     d, o = dev(t), f64(t)
