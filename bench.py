@@ -832,26 +832,32 @@ def main():
         # projections and the MLP / O-projection input gradients on e4m3
         # operands, weights quantised every step inside the step
         from gemm_epilogue_transformer_bf16_gb300.block import BlockFP8
-        b8 = BlockFP8(s, t, device=dev)
         args8 = (t["x0"], t["A"], t["pos"], t["dx2"], t["dQ"], t["dK"], t["dV"])
-
-        def fp8_step(mark):
-            b8.step(*args8, mark=lambda name: mark())
         n8 = max(10, min(args.steps, 30))
-        mq8, mf8, mb8 = median_ms(fp8_step, n=n8, warm=3, parts=3)
-        if coda.get_status(b8.ws) != 0 or coda.get_status(b8.ws2) != 0:
-            raise RuntimeError("device status error in the FP8 block measurement")
-        f_blk = sum(b8.gemm_flops().values())
+        res8 = {}
+        for fw in (True, False):
+            b8 = BlockFP8(s, t, device=dev, fp8_wgrad=fw)
+
+            def fp8_step(mark, b8=b8):
+                b8.step(*args8, mark=lambda name: mark())
+            res8[fw] = median_ms(fp8_step, n=n8, warm=3, parts=3)
+            if coda.get_status(b8.ws) != 0 or coda.get_status(b8.ws2) != 0:
+                raise RuntimeError("device status error in the FP8 block measurement")
+            f_blk = sum(b8.gemm_flops().values())
+            del b8
+        mq8, mf8, mb8 = res8[True]
         m8 = mq8 + mf8 + mb8
+        m8b = sum(res8[False])
         other["fp8_block"] = {
-            "workload": "the block step (tokens 8192, hidden 8192) with e4m3 forward projections and MLP / "
-                        "O-projection input-gradient GEMMs, weights quantised inside the step; weight gradients "
-                        "and the QKV backward in bf16",
+            "workload": "the block step (tokens 8192, hidden 8192) with e4m3 forward projections, MLP / "
+                        "O-projection input-gradient GEMMs and MLP / O-projection weight-gradient GEMMs "
+                        "(operands quantised per column over the tokens), weights quantised inside the step; "
+                        "the QKV backward in bf16",
             "ms": round(m8, 4), "tflops": rate(f_blk, m8), "quantize_weights_ms": round(mq8, 4),
             "fwd_ms": round(mf8, 4), "bwd_ms": round(mb8, 4),
+            "bf16_weight_gradients_ms": round(m8b, 4),
             "bf16_block_ms": round(blk_res["median_step"], 4) if blk_res else None,
             "speedup_vs_bf16_block": round(blk_res["median_step"] / m8, 3) if blk_res else None}
-        del b8
     if "nvfp4" in legs:
         # NVFP4 (e2m1 + e4m3 block scales) gate/up + SwiGLU at the same shape:
         # the block-scaled kind::mxf4nvf4 mainloop, single CTAs

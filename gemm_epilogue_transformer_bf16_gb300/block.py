@@ -200,11 +200,15 @@ class BlockFP8:
     RMSNorm-backward epilogue) and of the O-projection (dA).  Activations are
     quantised per token and weights per output row (forward) or per input
     column (backward, transposed by the column quantiser) every step, since
-    the weights change every step; weight gradients and the QKV backward
-    stay bf16.  The O-projection's output x1 goes through the RMSNorm scale
-    pass for r1 and u1 (the bf16 block gets them from its epilogue)."""
+    the weights change every step.  With fp8_wgrad (the default) the weight
+    gradients of the MLP and the O-projection are e4m3 GEMMs as well: both
+    operands quantised per column over the tokens by the transposing
+    quantiser, dW = (G^T)_q (X^T)_q^T with the two column scales.  The QKV
+    backward stays bf16.  The O-projection's output x1 goes through the
+    RMSNorm scale pass for r1 and u1 (the bf16 block gets them from its
+    epilogue)."""
 
-    def __init__(self, shape, weights, device="cuda", concurrent=True):
+    def __init__(self, shape, weights, device="cuda", concurrent=True, fp8_wgrad=True):
         self.s = s = shape
         self.w = w = weights
         lib = load()
@@ -226,6 +230,10 @@ class BlockFP8:
         self.U0, self.U1 = e(T, Hd, **bf), e(T, Hd, **bf)
         self.U0_q, self.A_q, self.U1_q, self.H_q = q(T, Hd), q(T, a_in), q(T, Hd), q(T, I)
         self.dx2_q, self.G_q, self.dx1_q = q(T, Hd), q(T, 2 * I), q(T, Hd)
+        self.fp8_wgrad = fp8_wgrad
+        if fp8_wgrad:  # transposed, per-column codes of the weight gradients' operands
+            self.dx2T_q, self.HT_q, self.GT_q = q(Hd, T), q(I, T), q(2 * I, T)
+            self.U1T_q, self.dx1T_q, self.AT_q = q(Hd, T), q(Hd, T), q(a_in, T)
         self.cos_sin = rope_table(s.theta, d, s.seq_len, device=device)
         self.rstd0, self.rstd1, self.coef1 = e(T, **f32), e(T, **f32), e(T, **f32)
         self.fwd = {"Q": e(T, s.n_q * d, **bf), "K": e(T, s.n_kv * d, **bf), "V": e(T, s.n_kv * d, **bf),
@@ -235,7 +243,8 @@ class BlockFP8:
         self.Gp = e(T, 2 * I, **bf)
         self.dx1 = {"dX": e(T, Hd, **bf), "dgamma": e(Hd, **f32)}
         self.dA = e(T, a_in, **bf)
-        self.dW = {"dWg": e(I, Hd, **bf), "dWu": e(I, Hd, **bf), "dWd": e(Hd, I, **bf), "dWo": e(Hd, a_in, **bf)}
+        self.dWgu = e(2 * I, Hd, **bf)   # dWg above dWu: one GEMM over G' = [G'_g | G'_u]
+        self.dW = {"dWg": self.dWgu[:I], "dWu": self.dWgu[I:], "dWd": e(Hd, I, **bf), "dWo": e(Hd, a_in, **bf)}
         self.grads_qkv = {"dX": e(T, Hd, **bf), "dW": e(nqkv, Hd, **bf), "dgamma_in": e(Hd, **f32),
                           "dgamma_q": e(d, **f32), "dgamma_k": e(d, **f32)}
         need = max(lib.coda_linear_qknorm_rope_fp8_workspace_size(T, Hd, s.n_q, s.n_kv, d),
@@ -243,7 +252,8 @@ class BlockFP8:
                    lib.coda_linear_dswiglu_fp8_workspace_size(T, I, Hd),
                    lib.coda_rmsnorm_linear_dx_fp8_workspace_size(T, 2 * I, Hd),
                    lib.coda_linear_qknorm_rope_bwd_workspace_size(T, Hd, s.n_q, s.n_kv, d),
-                   lib.coda_gemm_epilogue_workspace_size())
+                   lib.coda_gemm_epilogue_workspace_size(), lib.coda_linear_fp8_workspace_size(Hd, I, T),
+                   lib.coda_linear_fp8_workspace_size(2 * I, Hd, T), lib.coda_linear_fp8_workspace_size(Hd, a_in, T))
         self.ws = workspace(need, device)
         self.s2 = torch.cuda.Stream(device=device) if concurrent else None
         self.ws2 = workspace(need, device) if concurrent else self.ws
@@ -280,6 +290,13 @@ class BlockFP8:
             d.col_scale = col_scale.data_ptr()
         gemm_epilogue(d, A, B, D, M, N, K, a_major=MN_MAJOR, b_major=MN_MAJOR, lda=lda, ldb=ldb, ws=ws)
 
+    def _wgrad_fp8(self, G, GT_q, X, XT_q, D, ws):
+        """D [m, n] = G^T X over the tokens (G [T, m], X [T, n]) as an e4m3 GEMM
+        on the column-quantised transposes."""
+        quantize_fp8_cols(G, XTq=GT_q[0], scale=GT_q[1])
+        quantize_fp8_cols(X, XTq=XT_q[0], scale=XT_q[1])
+        linear_fp8(GT_q[0], GT_q[1], XT_q[0], XT_q[1], Y=D, ws=ws)
+
     def forward(self, x0, A, pos, mark=None):
         s, w = self.s, self.w
         mark = mark or (lambda name: None)
@@ -310,10 +327,14 @@ class BlockFP8:
                            rstd=self.rstd1, out={"Gp": self.Gp, "row": self.coef1, "H": None}, ws=self.ws)
         ctx, ws2 = self._side()
         with ctx:   # weight gradients of the MLP beside its input gradient
-            self._wgrad(dx2, Hd, self.H, I, self.dW["dWd"], Hd, I, T, ws=ws2)
-            self._wgrad(self.Gp, 2 * I, self.U1, Hd, self.dW["dWg"], I, Hd, T, ws=ws2)
-            # the up half of G' (a flat view from its first element; rows 2I apart)
-            self._wgrad(self.Gp.view(-1)[I:], 2 * I, self.U1, Hd, self.dW["dWu"], I, Hd, T, ws=ws2)
+            if self.fp8_wgrad:
+                self._wgrad_fp8(dx2, self.dx2T_q, self.H, self.HT_q, self.dW["dWd"], ws2)
+                self._wgrad_fp8(self.Gp, self.GT_q, self.U1, self.U1T_q, self.dWgu, ws2)
+            else:
+                self._wgrad(dx2, Hd, self.H, I, self.dW["dWd"], Hd, I, T, ws=ws2)
+                self._wgrad(self.Gp, 2 * I, self.U1, Hd, self.dW["dWg"], I, Hd, T, ws=ws2)
+                # the up half of G' (a flat view from its first element; rows 2I apart)
+                self._wgrad(self.Gp.view(-1)[I:], 2 * I, self.U1, Hd, self.dW["dWu"], I, Hd, T, ws=ws2)
         quantize_fp8_rows(self.Gp, Xq=self.G_q[0], scale=self.G_q[1])
         rmsnorm_linear_dx_fp8(self.G_q[0], self.G_q[1], self.WguT_q[0], self.WguT_q[1], self.x1, w["gamma_mlp"],
                               self.coef1, dX_resid=dx2, out=self.dx1, ws=self.ws)
@@ -323,7 +344,10 @@ class BlockFP8:
         self._join()
         ctx, ws2 = self._side()
         with ctx:
-            self._wgrad(dx1, Hd, A, a_in, self.dW["dWo"], Hd, a_in, T, ws=ws2)
+            if self.fp8_wgrad:
+                self._wgrad_fp8(dx1, self.dx1T_q, A, self.AT_q, self.dW["dWo"], ws2)
+            else:
+                self._wgrad(dx1, Hd, A, a_in, self.dW["dWo"], Hd, a_in, T, ws=ws2)
         linear_qknorm_rope_bwd(dQ, dK, dV, self.fwd["qk_save"], self.fwd["V"], w["gamma_q"], w["gamma_k"], pos,
                                self.cos_sin, s.n_q, s.n_kv, x0, w["Wqkv"], rstd=self.rstd0,
                                gamma_in=w["gamma_attn"], dX_resid=dx1, eps=s.eps, head_dim=s.head_dim,

@@ -132,9 +132,12 @@ def test_rmsnorm_linear_dx_fp8(coda):
     assert_bf16(out["dgamma"], r["dgamma"], "fp8 RMSNorm dgamma")
 
 
-def test_block_fp8_step(coda):
+@pytest.mark.parametrize("fp8_wgrad", [True, False])
+def test_block_fp8_step(coda, fp8_wgrad):
     """The block step with its forward projections and its MLP and
-    O-projection input gradients on e4m3 operands (BlockFP8), against the
+    O-projection input gradients on e4m3 operands (BlockFP8) -- and, with
+    fp8_wgrad, the MLP and O-projection weight gradients on the
+    column-quantised transposes of their operands -- against the
     fp64 oracle's bf16-free block on a ragged shape.  Each FP8 operator is
     checked exactly above on shared codes; here the quantisation of every
     activation and weight compounds (one e4m3 rounding is up to 2^-4 of a
@@ -147,7 +150,7 @@ def test_block_fp8_step(coda):
     t = synth.make_block(shape, seed=0)
     d = {k: v.to(DEV) for k, v in t.items()}
     o = {k: (v.numpy() if v.dtype in (torch.int32, torch.int64) else to_np(v)) for k, v in t.items()}
-    blk = BlockFP8(shape, d)
+    blk = BlockFP8(shape, d, fp8_wgrad=fp8_wgrad)
     f = blk.forward(d["x0"], d["A"], d["pos"])
     g = blk.backward(d["x0"], d["A"], d["pos"], d["dx2"], d["dQ"], d["dK"], d["dV"])
     torch.cuda.synchronize()
