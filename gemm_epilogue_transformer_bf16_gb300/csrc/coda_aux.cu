@@ -6,6 +6,7 @@
 // QK-RMSNorm + RoPE backward).  All are HBM-bound: 16-byte vector accesses,
 // warp-per-row for row work, grids sized to the SM count.
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 
 #include <cuda_fp8.h>
@@ -432,6 +433,101 @@ __global__ void quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ X, in
   }
 }
 
+// Same rule, one block per row at a time: each row is brought into shared
+// memory by one bulk copy (double-buffered: the next row's copy is issued
+// before this row's work), so HBM reads every element once and the block's
+// 256 threads find the amax and write the codes from shared memory.  The
+// copy wait is bounded: a row whose bytes do not arrive within the limit
+// gets a NaN scale (its codes are not written), which no valid row has.
+constexpr int QROW_THREADS = 256;
+constexpr size_t QROW_SMEM_MAX = 232448;  // the per-block dynamic shared-memory limit
+
+__global__ void __launch_bounds__(QROW_THREADS) quantize_fp8_rows_smem_kernel(
+    const __nv_bfloat16* __restrict__ X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq, int64_t ldq, float* scale,
+    uint32_t row_bytes_padded, uint64_t timeout_ns) {
+  extern __shared__ __align__(128) uint8_t qsm[];
+  griddep_launch_dependents();
+  auto buf = [&](int b) { return qsm + b * row_bytes_padded; };
+  uint64_t* bar = reinterpret_cast<uint64_t*>(qsm + 2 * row_bytes_padded);
+  float* red = reinterpret_cast<float*>(bar + 2);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t bytes = static_cast<uint32_t>(K * 2);
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  griddep_wait();
+  int64_t row = blockIdx.x;
+  if (tid == 0 && row < M) {
+    mbar_arrive_expect_tx(&bar[0], bytes, 1);
+    bulk_load(buf(0), X + row * ldx, bytes, &bar[0], 1);
+  }
+  bool failed = false;
+  uint32_t i = 0;
+  for (; row < M; ++i, row += gridDim.x) {
+    const int b = i & 1;
+    const int64_t next = row + gridDim.x;
+    if (tid == 0 && next < M && !failed) {  // the other buffer was released by the last iteration's barrier
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_expect_tx(&bar[b ^ 1], bytes, 1);
+      bulk_load(buf(b ^ 1), X + next * ldx, bytes, &bar[b ^ 1], 1);
+    }
+    bool ok = false;
+    if (!failed) {  // bounded wait for this row's bytes (every thread polls the barrier)
+      ok = mbar_try_wait(smem_u32(&bar[b]), (i >> 1) & 1);
+      const uint64_t t0 = globaltimer_ns();
+      while (!ok && globaltimer_ns() - t0 < timeout_ns) ok = mbar_try_wait(smem_u32(&bar[b]), (i >> 1) & 1);
+    }
+    ok = __syncthreads_and(ok);
+    if (!ok) {  // no more copies from this block; its remaining rows get NaN scales
+      if (tid == 0) scale[row] = __int_as_float(0x7fc00000);
+      if (!failed && tid == 0 && next < M) {  // the next row's copy was issued: let it land (bounded)
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&bar[b ^ 1]), ((i + 1) >> 1) & 1) && globaltimer_ns() - t0 < timeout_ns) {
+        }
+      }
+      failed = true;
+      continue;
+    }
+    const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(buf(b));
+    float amax = 0.f;
+    for (int64_t k = tid * 8; k < K; k += QROW_THREADS * 8) {
+      float v[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(x + k), v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < QROW_THREADS / 32; ++w) amax = fmaxf(amax, red[w]);
+    const float sc = amax > 0.f ? amax / 448.f : 1.f;
+    if (tid == 0) scale[row] = sc;
+    uint8_t* q = Xq + row * ldq;
+    for (int64_t k = tid * 8; k < K; k += QROW_THREADS * 8) {
+      float v[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(x + k), v);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        lo |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(v[j] / sc, __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        hi |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(v[4 + j] / sc, __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+      *reinterpret_cast<uint2*>(q + k) = make_uint2(lo, hi);
+    }
+    __syncthreads();  // buffer b and red[] are free for the next rows
+  }
+  // every copy issued was waited for: the copy of row `next` is issued only
+  // when that row belongs to this block's loop, which waits for it (or, after
+  // a timeout, drains it above)
+}
+
 // ---------------------------------------------------------------- FP8 (e4m3) column quantisation
 // The transposed K-major operand of a GEMM that contracts over X's rows:
 // scale_c = max_r |x_rc| / 448 (1 for an all-zero column), out[c, r] =
@@ -451,6 +547,8 @@ __global__ void fp8_col_amax_kernel(const __nv_bfloat16* __restrict__ X, int64_t
   const int64_t r_end = min(R + R2, r_begin + rows_per_block);
   float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (c0 < C) {
+    // unrolled so that several independent 16-byte loads per thread are in flight
+#pragma unroll 4
     for (int64_t r = r_begin + rp; r < r_end; r += 8) {
       const __nv_bfloat16* src = r < R ? X + r * ldx + c0 : X2 + (r - R) * ldx2 + c0;
       float v[8];
@@ -525,8 +623,9 @@ cudaError_t launch_quantize_fp8_cols(const __nv_bfloat16* X, int64_t ldx, int64_
   if (e != cudaSuccess) return e;
   const int64_t RT = R + R2;
   const int64_t cblk = (C + 255) / 256;
-  // about four blocks per SM in all, each over a run of rows
-  const int64_t want = std::max<int64_t>(1, (4 * static_cast<int64_t>(num_sms) + cblk - 1) / cblk);
+  // about sixteen blocks per SM in all (eight resident), each over a run of
+  // rows: enough loads in flight to stream X at HBM speed
+  const int64_t want = std::max<int64_t>(1, (16 * static_cast<int64_t>(num_sms) + cblk - 1) / cblk);
   const int64_t rsplit = std::min<int64_t>(want, std::max<int64_t>(1, (RT + 63) / 64));
   const int rows = static_cast<int>((RT + rsplit - 1) / rsplit);
   note_launch();
@@ -542,8 +641,51 @@ cudaError_t launch_quantize_fp8_cols(const __nv_bfloat16* X, int64_t ldx, int64_
   return cudaGetLastError();
 }
 
+// CODA_QROW_SMEM=0 in the environment selects the warp-per-row quantiser
+// (for comparisons).
+static bool qrow_staged_enabled() {
+  static const bool v = [] {
+    const char* e = std::getenv("CODA_QROW_SMEM");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
+
 cudaError_t launch_quantize_fp8_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq,
                                      int64_t ldq, float* scale, int num_sms, cudaStream_t s) {
+  // rows staged in shared memory when at least two blocks (four rows) fit
+  // on an SM and the bulk copies' addresses and sizes are 16-byte
+  // multiples; otherwise a warp per row.  With one 8-warp block per SM (rows
+  // wider than ~28k elements) the codes' fp32 divisions are latency-bound
+  // and the warp-per-row kernel's 64 warps per SM are faster (G' of the SwiGLU
+  // MLP, 8192 x 57344: 0.625 against 0.659 ms).
+  const uint32_t rowp = static_cast<uint32_t>((K * 2 + 127) / 128 * 128);
+  const size_t smem = 2 * static_cast<size_t>(rowp) + 2 * sizeof(uint64_t) + 8 * sizeof(float);
+  const int per_sm = static_cast<int>(std::min<size_t>(8, (228 * 1024) / (smem + 1024)));
+  const bool staged = K > 0 && K % 8 == 0 && ldx % 8 == 0 && (reinterpret_cast<uintptr_t>(X) & 15) == 0 &&
+                      smem <= QROW_SMEM_MAX && per_sm >= 2 && M > 0 && qrow_staged_enabled();
+  if (staged) {
+    static std::mutex mu;
+    static bool raised[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      if (!raised[dev]) {
+        e = cudaFuncSetAttribute(quantize_fp8_rows_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(QROW_SMEM_MAX));
+        if (e != cudaSuccess) return e;
+        raised[dev] = true;
+      }
+    }
+    const int64_t blocks = std::min<int64_t>(M, static_cast<int64_t>(num_sms) * per_sm);
+    note_launch();
+    quantize_fp8_rows_smem_kernel<<<static_cast<unsigned>(blocks), QROW_THREADS, smem, s>>>(
+        X, ldx, M, K, Xq, ldq, scale, rowp, 1000000000ull);
+    return cudaGetLastError();
+  }
   const int64_t blocks = std::min<int64_t>((M + 7) / 8, static_cast<int64_t>(num_sms) * 8);
   note_launch();
   quantize_fp8_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(X, ldx, M, K, Xq,
