@@ -396,6 +396,27 @@ cudaError_t launch_ce_norm_coef(const float* pz, int64_t ld, int nparts, const f
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- division by a fixed scale
+// x / s rounded to nearest (fp32) for one divisor and many dividends, by
+// Markstein's correction (P. Markstein, "Computation of elementary functions
+// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+// y = RN(1/s), the first quotient q = RN(x y) is within an ulp of x / s, the
+// residual x - s q is exact in one FMA, and RN(q + (x - s q) y) is the
+// correctly rounded quotient, barring overflow and results below the normal
+// range (a quantiser's quotients lie in [0, 448], and one below 2^-126 rounds
+// to a zero code either way).  The quotient takes x's sign (s > 0), which
+// also keeps -0 / s = -0.  Three FP32 operations per element instead of a
+// full division; the GPU tests compare the codes bit for bit with the
+// oracle's IEEE division.
+struct DivBy {
+  float s, y;
+  __device__ __forceinline__ explicit DivBy(float s_) : s(s_), y(1.f / s_) {}  // RN(1/s): one IEEE division
+  __device__ __forceinline__ float operator()(float x) const {
+    const float q = x * y;
+    return copysignf(fmaf(fmaf(-s, q, x), y, q), x);
+  }
+};
+
 // ---------------------------------------------------------------- FP8 (e4m3) row quantisation
 // Warp per row: scale = amax / 448 (fp32; 1 for an all-zero row), codes =
 // e4m3(x / scale), fp32 division, round to nearest even, saturating.
@@ -417,6 +438,7 @@ __global__ void quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ X, in
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = amax > 0.f ? amax / 448.f : 1.f;
     if (lane == 0) scale[row] = s;
+    const DivBy div(s);
     uint8_t* q = Xq + row * ldq;
     for (int64_t k = lane * 8; k < K; k += 256) {
       float v[8];
@@ -424,10 +446,10 @@ __global__ void quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ X, in
       uint32_t lo = 0, hi = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        lo |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(v[j] / s, __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+        lo |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(div(v[j]), __NV_SATFINITE, __NV_E4M3)) << (8 * j);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        hi |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(v[4 + j] / s, __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+        hi |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(div(v[4 + j]), __NV_SATFINITE, __NV_E4M3)) << (8 * j);
       *reinterpret_cast<uint2*>(q + k) = make_uint2(lo, hi);
     }
   }
@@ -508,6 +530,7 @@ __global__ void __launch_bounds__(QROW_THREADS) quantize_fp8_rows_smem_kernel(
     for (int w = 1; w < QROW_THREADS / 32; ++w) amax = fmaxf(amax, red[w]);
     const float sc = amax > 0.f ? amax / 448.f : 1.f;
     if (tid == 0) scale[row] = sc;
+    const DivBy div(sc);
     uint8_t* q = Xq + row * ldq;
     for (int64_t k = tid * 8; k < K; k += QROW_THREADS * 8) {
       float v[8];
@@ -515,10 +538,10 @@ __global__ void __launch_bounds__(QROW_THREADS) quantize_fp8_rows_smem_kernel(
       uint32_t lo = 0, hi = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        lo |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(v[j] / sc, __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+        lo |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(div(v[j]), __NV_SATFINITE, __NV_E4M3)) << (8 * j);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        hi |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(v[4 + j] / sc, __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+        hi |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(div(v[4 + j]), __NV_SATFINITE, __NV_E4M3)) << (8 * j);
       *reinterpret_cast<uint2*>(q + k) = make_uint2(lo, hi);
     }
     __syncthreads();  // buffer b and red[] are free for the next rows
@@ -599,12 +622,12 @@ __global__ void fp8_col_quant_kernel(const __nv_bfloat16* __restrict__ X, int64_
   const int cc = threadIdx.x >> 2, part = threadIdx.x & 3;
   const int64_t c = c0 + cc;
   if (c < C) {
-    const float sc = scale[c];
+    const DivBy div(scale[c]);
     uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int rr = part * 16 + j;
-      const uint32_t b = static_cast<uint32_t>(__nv_cvt_float_to_fp8(tile[rr][cc] / sc, __NV_SATFINITE, __NV_E4M3));
+      const uint32_t b = static_cast<uint32_t>(__nv_cvt_float_to_fp8(div(tile[rr][cc]), __NV_SATFINITE, __NV_E4M3));
       w[j >> 2] |= b << (8 * (j & 3));
     }
     const int64_t r = r0 + part * 16;

@@ -49,6 +49,38 @@ def _cols(coda, X, X2=None):
     return q, s, ov, osc
 
 
+def _every_bf16(width, n_gains=16, seed=7):
+    """Rows of bf16 values covering every finite bf16 magnitude up to a gain
+    g, both signs, for n_gains random gains: each group of rows holds all
+    finite patterns with |x| <= g (others zeroed) and starts with g itself, so
+    every row's scale is g / 448 and every quotient x / s the codes need is
+    taken.  Returns [rows, width] bf16."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float()
+    gains = (torch.rand(n_gains, generator=torch.Generator().manual_seed(seed)) * 2000 + 1e-3)
+    rows = []
+    for g in gains.to(torch.bfloat16).float():
+        v = torch.where(torch.isfinite(bits) & (bits.abs() <= g), bits, torch.zeros_like(bits))
+        v = v.view(-1, width).clone()
+        v[:, 0] = g
+        rows.append(v)
+    return torch.cat(rows).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("width", [8192, 32768])
+def test_quantize_fp8_rows_every_bf16(coda, width):
+    """The codes for every finite bf16 value at 16 scales, bit for bit against
+    the oracle's IEEE division (8192-wide rows take the shared-memory staged
+    quantiser, 32768-wide rows the warp-per-row one)."""
+    _rows(coda, _every_bf16(width))
+
+
+def test_quantize_fp8_cols_every_bf16(coda):
+    """The same values through the column quantiser (the transpose: every
+    column holds all finite bf16 values up to its gain)."""
+    X = _every_bf16(8192, n_gains=4).t().contiguous()
+    _cols(coda, X)
+
+
 @pytest.mark.parametrize("R,R2,C", [(304, 0, 264), (256, 48, 520), (8192, 0, 128)])
 def test_quantize_fp8_cols(coda, R, R2, C):
     X = synth.randn_bf16((R, C), 1.0, 31)
