@@ -676,17 +676,15 @@ static bool qrow_staged_enabled() {
 
 cudaError_t launch_quantize_fp8_rows(const __nv_bfloat16* X, int64_t ldx, int64_t M, int64_t K, uint8_t* Xq,
                                      int64_t ldq, float* scale, int num_sms, cudaStream_t s) {
-  // rows staged in shared memory when at least two blocks (four rows) fit
-  // on an SM and the bulk copies' addresses and sizes are 16-byte
-  // multiples; otherwise a warp per row.  With one 8-warp block per SM (rows
-  // wider than ~28k elements) the codes' fp32 divisions are latency-bound
-  // and the warp-per-row kernel's 64 warps per SM are faster (G' of the SwiGLU
-  // MLP, 8192 x 57344: 0.625 against 0.659 ms).
+  // rows staged in shared memory when two of them fit in a block's shared
+  // memory and the bulk copies' addresses and sizes are 16-byte multiples;
+  // otherwise a warp per row (which reads each row twice).  G' of the SwiGLU
+  // MLP, 8192 x 57344 (one block per SM): 0.365 against 0.460 ms.
   const uint32_t rowp = static_cast<uint32_t>((K * 2 + 127) / 128 * 128);
   const size_t smem = 2 * static_cast<size_t>(rowp) + 2 * sizeof(uint64_t) + 8 * sizeof(float);
   const int per_sm = static_cast<int>(std::min<size_t>(8, (228 * 1024) / (smem + 1024)));
   const bool staged = K > 0 && K % 8 == 0 && ldx % 8 == 0 && (reinterpret_cast<uintptr_t>(X) & 15) == 0 &&
-                      smem <= QROW_SMEM_MAX && per_sm >= 2 && M > 0 && qrow_staged_enabled();
+                      smem <= QROW_SMEM_MAX && per_sm >= 1 && M > 0 && qrow_staged_enabled();
   if (staged) {
     static std::mutex mu;
     static bool raised[64] = {};
