@@ -115,9 +115,10 @@ __device__ __forceinline__ void warp_colsum_partial(float* p, int lane) {
   }
 }
 
-// The accumulator chunk of columns col0 .. col0 + 31 with the FP8 operand
-// scales applied: acc * acc_rs[row] * acc_cs[col] (columns >= N scaled by 0).
-// Without FP8 operands (both null) it is tmem_ld32.
+// The accumulator chunk of columns col0 .. col0 + 31, with the FP8 operand
+// scales applied when SCALED: acc * acc_rs[row] * acc_cs[col] (columns >= N
+// scaled by 0).  Without them it is tmem_ld32; each epilogue chooses SCALED
+// once per tile.
 template <bool SCALED>
 __device__ __forceinline__ void tmem_ld32_acc_t(uint32_t taddr, float (&v)[32], const EpiArgs& e, int row, bool rv,
                                                 int col0, int N) {
@@ -137,13 +138,6 @@ __device__ __forceinline__ void tmem_ld32_acc_t(uint32_t taddr, float (&v)[32], 
       for (int i = 0; i < 8; ++i) v[g * 8 + i] *= rs * s8[i];
     }
   }
-}
-__device__ __forceinline__ void tmem_ld32_acc(uint32_t taddr, float (&v)[32], const EpiArgs& e, int row, bool rv,
-                                              int col0, int N) {
-  if (e.acc_rs || e.acc_cs)
-    tmem_ld32_acc_t<true>(taddr, v, e, row, rv, col0, N);
-  else
-    tmem_ld32_acc_t<false>(taddr, v, e, row, rv, col0, N);
 }
 
 // ---------------------------------------------------------------------------
@@ -945,47 +939,54 @@ struct EpiSigmoid {
   static __device__ __forceinline__ void begin(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void end(State&, const EpiArgs&, const TileInfo&) {}
   static __device__ __forceinline__ void prefetch(const EpiArgs&, const TileInfo&) {}
-  static __device__ __forceinline__ void tile(State&, const EpiArgs& e, const TileInfo& t) {
+  // per-tile choice of loop: gated (Z = aux0), forward or backward, dZ output
+  static __device__ __forceinline__ void tile(State& st, const EpiArgs& e, const TileInfo& t) {
+    const bool gated = e.aux0 != nullptr;
+    if (e.mode == 0)
+      gated ? tile_impl<true, 0, false>(st, e, t) : tile_impl<false, 0, false>(st, e, t);
+    else if (e.out2)
+      gated ? tile_impl<true, 1, true>(st, e, t) : tile_impl<false, 1, true>(st, e, t);
+    else
+      gated ? tile_impl<true, 1, false>(st, e, t) : tile_impl<false, 1, false>(st, e, t);
+  }
+  template <bool GATED, int MODE, bool OUT2>
+  static __device__ __forceinline__ void tile_impl(State&, const EpiArgs& e, const TileInfo& t) {
     const int row = t.row;
     const bool rv = row < t.M;
+    const int row0 = row - static_cast<int>(threadIdx.x & 31);
     const float rs = (e.row_scale && rv) ? e.row_scale[row] : 1.f;
     const int64_t off = static_cast<int64_t>(row);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int col0 = t.nb * BN + c;
       if (col0 >= t.N) break;
-      float v[32];
+      float v[32], o2[32];
       __syncwarp();
       tmem_ld32(t.taddr + c, v);
-      if (rv) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int cc = col0 + g * 8;
-          if (cc < t.N) {
-            float sg[8], z8[8];
+      for (int g = 0; g < 4; ++g) {
+        const int cc = col0 + g * 8;
+        const bool in = rv && cc < t.N;
+        float z8[8] = {}, dy[8] = {};
+        if (GATED && in) load_bf16x8(e.aux0 + off * e.ld_aux0 + cc, z8);
+        if (MODE == 1 && in) load_bf16x8(e.aux1 + off * e.ld_aux1 + cc, dy);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) sg[i] = 1.f / (1.f + __expf(-v[g * 8 + i] * rs));
-            if (e.aux0) load_bf16x8(e.aux0 + off * e.ld_aux0 + cc, z8);
-            if (e.mode == 0) {
-              float y[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) y[i] = e.aux0 ? sg[i] * z8[i] : sg[i];
-              store_bf16x8(static_cast<__nv_bfloat16*>(e.D) + off * e.ldd + cc, y, e.st_stream);
-            } else {
-              float dy[8], dz[8], dg[8];
-              load_bf16x8(e.aux1 + off * e.ld_aux1 + cc, dy);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float gg = e.aux0 ? dy[i] * z8[i] : dy[i];
-                dz[i] = gg * sg[i] * (1.f - sg[i]);
-                dg[i] = dy[i] * sg[i];
-              }
-              store_bf16x8(e.out1 + off * e.ld_out1 + cc, dz, e.st_stream);
-              if (e.out2) store_bf16x8(e.out2 + off * e.ld_out2 + cc, dg, e.st_stream);
-            }
+        for (int i = 0; i < 8; ++i) {
+          const float sg = 1.f / (1.f + __expf(-v[g * 8 + i] * rs));
+          if (MODE == 0) {
+            v[g * 8 + i] = GATED ? sg * z8[i] : sg;
+          } else {
+            const float gg = GATED ? dy[i] * z8[i] : dy[i];
+            v[g * 8 + i] = gg * sg * (1.f - sg);   // dz
+            o2[g * 8 + i] = dy[i] * sg;             // dZ
           }
         }
       }
+      if (MODE == 0)
+        warp_store_bf16x32(t.stage, static_cast<__nv_bfloat16*>(e.D), e.ldd, row0, t.M, col0, t.N, v, e.st_stream);
+      else
+        warp_store_bf16x32(t.stage, e.out1, e.ld_out1, row0, t.M, col0, t.N, v, e.st_stream);
+      if (MODE == 1 && OUT2) warp_store_bf16x32(t.stage, e.out2, e.ld_out2, row0, t.M, col0, t.N, o2, e.st_stream);
     }
   }
 };

@@ -429,8 +429,5 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16* p, const float* v, b
   else
     *reinterpret_cast<uint4*>(p) = make_uint4(x, y, z, w);
 }
-__device__ __forceinline__ float round_bf16(float x) {
-  return __bfloat162float(__float2bfloat16_rn(x));
-}
 
 }  // namespace coda
