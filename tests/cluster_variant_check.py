@@ -1,7 +1,9 @@
 """Run by test_cluster_variants_gpu.py in a fresh process (the cluster-size
 switches are read once per process): a ragged transformer block forward and
 backward, a SwiGLU MLP backward, an FP8 linear and a linear + residual whose
-shape the launch policy runs as CTA pairs, against the fp64 oracle.
+shape the launch policy runs as CTA pairs, and the RMSNorm-linear forward
+and backward with its dW GEMM on a second stream (the two backward GEMMs
+share the grid), against the fp64 oracle.
 Exits non-zero on the first mismatch."""
 import os
 import sys
@@ -63,6 +65,20 @@ def main():
     ur, rr = O.linear_residual_fwd(to_np(X), to_np(W), to_np(R), 1e-6)
     assert_bf16(Y, ur, "8192x4096 Y")
     assert_f32(r, rr, "8192x4096 rstd")
+    # RMSNorm-linear forward and backward, dW on a second stream
+    rs = synth.RmsLinearShape(1000, 520, 264)
+    tr = synth.make_rms_linear(rs, seed=5)
+    dr, orr = {k: v.to(dev) for k, v in tr.items()}, f64(tr)
+    Wf = coda.fold_gamma(dr["W"], dr["gamma"])
+    Yr, rstd = coda.rmsnorm_linear(dr["X"], Wf, R=dr["R"], eps=rs.eps)
+    side = torch.cuda.Stream()
+    gr = coda.rmsnorm_linear_bwd(dr["G"], dr["X"], dr["W"], dr["gamma"], rstd, Yr, dr["R"], side_stream=side)
+    torch.cuda.synchronize()
+    yr_, _ = O.rmsnorm_linear_fwd(orr["X"], orr["gamma"], orr["W"], rs.eps, orr["R"])
+    br = O.rmsnorm_linear_bwd(orr["X"], orr["gamma"], orr["W"], rs.eps, orr["G"])
+    assert_bf16(Yr, yr_, "rmsnorm-linear Y")
+    for k in ("dX", "dW", "dgamma"):
+        assert_bf16(gr[k], br[k], "rmsnorm-linear " + k)
     print("ok")
 
 

@@ -9,7 +9,9 @@ epilogues' auxiliary rows (CODA_AUX_PREFETCH=0) and the shared-memory
 staging of the QK-norm + RoPE backward map's rows (CODA_QK_TMA=0) and the
 TMA ring that brings the plain epilogue's residual into shared memory
 (CODA_EPI_RING=0), and the plain epilogue's chunk loops compiled per
-feature set (CODA_EPI_LEAN=0 runs the general loop); and the defaults.  The
+feature set (CODA_EPI_LEAN=0 runs the general loop), and the RMSNorm-linear
+backward's two GEMMs on half the grid each (CODA_RMS_SHARE=0 gives each the
+whole grid); and the defaults.  The
 switches are read once per process, so each variant runs
 cluster_variant_check.py (block forward/backward, FP8 linear, against the
 fp64 oracle) in a fresh process."""
@@ -26,7 +28,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 @pytest.mark.parametrize("env", [{"CODA_CTA_PAIR": "0"}, {"CODA_CTA_QUAD": "0"}, {"CODA_CTA_QUAD": "2"},
                                  {"CODA_SPLIT": "0"}, {"CODA_PDL": "0"}, {"CODA_L2_HINTS": "0"},
                                  {"CODA_PAIR_WAVES": "0"}, {"CODA_AUX_PREFETCH": "0"}, {"CODA_QK_TMA": "0"},
-                                 {"CODA_EPI_RING": "0"}, {"CODA_EPI_LEAN": "0"}, {}])
+                                 {"CODA_EPI_RING": "0"}, {"CODA_EPI_LEAN": "0"}, {"CODA_RMS_SHARE": "0"}, {}])
 def test_cluster_variant(env):
     e = dict(os.environ)
     e.update(env)

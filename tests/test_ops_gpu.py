@@ -46,7 +46,10 @@ def test_linear_swiglu(coda, shape):
 
 # ---------------------------------------------------------------- RMSNorm-reparameterised projection
 @pytest.mark.parametrize("shape", [synth.RmsLinearShape(), synth.RmsLinearShape(300, 264, 200)])
-def test_rmsnorm_linear_fwd_bwd(coda, shape):
+@pytest.mark.parametrize("side", [False, True])
+def test_rmsnorm_linear_fwd_bwd(coda, shape, side):
+    """Forward and backward; with `side` the dW GEMM runs on a second stream
+    and the two backward GEMMs each take half of the grid."""
     t = synth.make_rms_linear(shape, seed=0)
     d, o = dev(t), f64(t)
     Wf = coda.fold_gamma(d["W"], d["gamma"])
@@ -54,7 +57,9 @@ def test_rmsnorm_linear_fwd_bwd(coda, shape):
     yr, rr = O.rmsnorm_linear_fwd(o["X"], o["gamma"], o["W"], shape.eps, o["R"])
     assert_bf16(Y, yr, "Y")
     assert_f32(rstd, rr, "rstd")
-    g = coda.rmsnorm_linear_bwd(d["G"], d["X"], d["W"], d["gamma"], rstd, Y, d["R"])
+    g = coda.rmsnorm_linear_bwd(d["G"], d["X"], d["W"], d["gamma"], rstd, Y, d["R"],
+                                side_stream=torch.cuda.Stream() if side else None)
+    torch.cuda.synchronize()
     b = O.rmsnorm_linear_bwd(o["X"], o["gamma"], o["W"], shape.eps, o["G"])
     assert_bf16(g["dX"], b["dX"], "dX")
     assert_bf16(g["dW"], b["dW"], "dW")
