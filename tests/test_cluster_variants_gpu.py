@@ -11,7 +11,8 @@ TMA ring that brings the plain epilogue's residual into shared memory
 (CODA_EPI_RING=0), and the plain epilogue's chunk loops compiled per
 feature set (CODA_EPI_LEAN=0 runs the general loop), and the RMSNorm-linear
 backward's two GEMMs on half the grid each (CODA_RMS_SHARE=0 gives each the
-whole grid); and the defaults.  The
+whole grid), and the e4m3 row quantiser's shared-memory staging
+(CODA_QROW_SMEM=0 runs a warp per row); and the defaults.  The
 switches are read once per process, so each variant runs
 cluster_variant_check.py (block forward/backward, FP8 linear, against the
 fp64 oracle) in a fresh process."""
@@ -28,7 +29,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 @pytest.mark.parametrize("env", [{"CODA_CTA_PAIR": "0"}, {"CODA_CTA_QUAD": "0"}, {"CODA_CTA_QUAD": "2"},
                                  {"CODA_SPLIT": "0"}, {"CODA_PDL": "0"}, {"CODA_L2_HINTS": "0"},
                                  {"CODA_PAIR_WAVES": "0"}, {"CODA_AUX_PREFETCH": "0"}, {"CODA_QK_TMA": "0"},
-                                 {"CODA_EPI_RING": "0"}, {"CODA_EPI_LEAN": "0"}, {"CODA_RMS_SHARE": "0"}, {}])
+                                 {"CODA_EPI_RING": "0"}, {"CODA_EPI_LEAN": "0"}, {"CODA_RMS_SHARE": "0"},
+                                 {"CODA_QROW_SMEM": "0"}, {}])
 def test_cluster_variant(env):
     e = dict(os.environ)
     e.update(env)
