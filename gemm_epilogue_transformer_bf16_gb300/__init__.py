@@ -29,7 +29,8 @@ __all__ = [
     "rmsnorm_linear_cross_entropy", "rmsnorm_linear_cross_entropy_bwd", "rms_rstd",
     "linear_sigmoid", "linear_sigmoid_bwd", "quantize_fp8_rows", "linear_fp8", "linear_swiglu_fp8", "quantize_nvfp4_rows", "rmsnorm_scale_nvfp4", "linear_nvfp4",
     "linear_swiglu_nvfp4", "quantize_fp8_cols", "linear_qknorm_rope_fp8", "linear_cross_entropy_fp8",
-    "linear_cross_entropy_bwd_fp8", "linear_dswiglu_fp8", "rmsnorm_linear_dx_fp8", "launch_count",
+    "linear_cross_entropy_bwd_fp8", "linear_dswiglu_fp8", "rmsnorm_linear_dx_fp8",
+    "linear_qknorm_rope_bwd_fp8", "launch_count",
     "MAP_NONE", "MAP_SWIGLU", "MAP_DSWIGLU", "MAP_QKNORM_ROPE", "MAP_CE_LSE",
     "MAP_CE_DLOGITS", "MAP_COLDOT", "MAP_SIGMOID", "MAP_DSIGMOID", "K_MAJOR", "MN_MAJOR",
 ]
@@ -98,6 +99,9 @@ _SIGS = {
     "coda_linear_dswiglu_fp8": ([_P] * 10 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_rmsnorm_linear_dx_fp8_workspace_size": ([_I64, _I64, _I64], _SZ),
     "coda_rmsnorm_linear_dx_fp8": ([_P] * 10 + [_I64, _I64, _I64, _P, _SZ, _P], ctypes.c_int),
+    "coda_linear_qknorm_rope_bwd_fp8_workspace_size": ([_I64, _I64, _I32, _I32, _I32], _SZ),
+    "coda_linear_qknorm_rope_bwd_fp8": ([_P] * 9 + [_I32, _F, _I32, _I32, _I32, _I32] + [_P] * 13
+                                        + [_I64, _I64, _P, _SZ, _P], ctypes.c_int),
     "coda_nvfp4_scale_bytes": ([_I64, _I64], _SZ),
     "coda_quantize_nvfp4_rows": ([_P, _I64, _I64, _I64, _P, _P, _P, _P], ctypes.c_int),
     "coda_rmsnorm_scale_nvfp4": ([_P, _I64, _I64, _I64, _F, _P, _P, _P, _P, _P, _P], ctypes.c_int),
@@ -680,6 +684,38 @@ def rmsnorm_linear_dx_fp8(Gq, sg, WTq, sw, X, gamma, coef, dX_resid=None, out=No
         _u8(Gq, "Gq"), _f32(sg, "sg"), _u8(WTq, "WTq"), _f32(sw, "sw"), _bf(X, "X"), _f32(gamma, "gamma"),
         _f32(coef, "coef"), _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"), _f32(out["dgamma"], "dgamma"), M, N,
         K, _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def linear_qknorm_rope_bwd_fp8(dQ, dK, dV, qk_save, V, gamma_q, gamma_k, pos, cos_sin, n_q, n_kv, WTq, sw, UTq,
+                               su, X=None, rstd=None, gamma_in=None, dX_resid=None, eps=1e-6, head_dim=128, ws=None,
+                               out=None, stream=None, pairing="interleaved"):
+    """QK-RMSNorm + RoPE projection backward with both GEMMs on e4m3 operands
+    (coda_linear_qknorm_rope_bwd_fp8): WTq, sw = quantize_fp8_cols(W_qkv),
+    UTq, su = quantize_fp8_cols(U) of the forward GEMM's input U (x ⊙ gamma_in
+    with the input RMSNorm, x without).  X (the un-normalised input) is
+    needed with rstd only.  Returns {"dX", "dW", "dgamma_in", "dgamma_q",
+    "dgamma_k"}."""
+    lib = load()
+    Kd, M = UTq.shape
+    dev = UTq.device
+    nqkv = (n_q + 2 * n_kv) * head_dim
+    if out is None:
+        out = {"dX": torch.empty(M, Kd, dtype=torch.bfloat16, device=dev),
+               "dW": torch.empty(nqkv, Kd, dtype=torch.bfloat16, device=dev),
+               "dgamma_in": torch.empty(Kd, dtype=torch.float32, device=dev) if rstd is not None else None,
+               "dgamma_q": torch.empty(head_dim, dtype=torch.float32, device=dev),
+               "dgamma_k": torch.empty(head_dim, dtype=torch.float32, device=dev)}
+    max_pos = cos_sin.shape[0]
+    ws = _ws(ws, lib.coda_linear_qknorm_rope_bwd_fp8_workspace_size(M, Kd, n_q, n_kv, head_dim), dev)
+    _check("coda_linear_qknorm_rope_bwd_fp8", lib.coda_linear_qknorm_rope_bwd_fp8(
+        _bf(dQ, "dQ"), _bf(dK, "dK"), _bf(dV, "dV"), _bf(qk_save, "qk_save"), _bf(V, "V"),
+        _f32(gamma_q, "gamma_q"), _f32(gamma_k, "gamma_k"), _i32(pos, "pos"), _f32(cos_sin, "cos_sin"),
+        max_pos, float(eps), n_q, n_kv, head_dim, _pairing(pairing), _bf(X, "X"), _f32(rstd, "rstd"),
+        _f32(gamma_in, "gamma_in"), _u8(WTq, "WTq"), _f32(sw, "sw"), _u8(UTq, "UTq"), _f32(su, "su"),
+        _bf(dX_resid, "dX_resid"), _bf(out["dX"], "dX"), _bf(out["dW"], "dW"),
+        _f32(out.get("dgamma_in"), "dgamma_in"), _f32(out["dgamma_q"], "dgamma_q"), _f32(out["dgamma_k"], "dgamma_k"),
+        M, Kd, _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

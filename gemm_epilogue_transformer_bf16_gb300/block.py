@@ -45,7 +45,7 @@ import torch
 
 from . import (K_MAJOR, MN_MAJOR, EpilogueDesc, fold_gamma, gemm_epilogue, linear_cross_entropy,
                linear_cross_entropy_bwd, linear_dswiglu_fp8, linear_fp8, linear_qknorm_rope, linear_qknorm_rope_bwd,
-               linear_qknorm_rope_fp8, linear_residual, linear_residual_bwd, linear_swiglu, linear_swiglu_bwd,
+               linear_qknorm_rope_bwd_fp8, linear_qknorm_rope_fp8, linear_residual, linear_residual_bwd, linear_swiglu, linear_swiglu_bwd,
                linear_swiglu_fp8, load, quantize_fp8_cols, quantize_fp8_rows, rms_rstd, rmsnorm_linear_dx_fp8,
                rmsnorm_scale, rope_table, workspace)
 
@@ -201,12 +201,15 @@ class BlockFP8:
     quantised per token and weights per output row (forward) or per input
     column (backward, transposed by the column quantiser) every step, since
     the weights change every step.  With fp8_wgrad (the default) the weight
-    gradients of the MLP and the O-projection are e4m3 GEMMs as well: both
-    operands quantised per column over the tokens by the transposing
-    quantiser, dW = (G^T)_q (X^T)_q^T with the two column scales.  The QKV
-    backward stays bf16.  The O-projection's output x1 goes through the
-    RMSNorm scale pass for r1 and u1 (the bf16 block gets them from its
-    epilogue)."""
+    gradients are e4m3 GEMMs as well: both operands quantised per column
+    over the tokens by the transposing quantiser, dW = (G^T)_q (X^T)_q^T
+    with the two column scales; and the QKV backward takes both of its GEMMs
+    on e4m3 operands (linear_qknorm_rope_bwd_fp8: G' quantised per row for
+    dx0 and per column for dWqkv, against W_qkv^T and the column codes of
+    the forward's u0 = x0 ⊙ gamma_attn).  Without it the weight gradients
+    and the whole QKV backward are bf16.  The O-projection's output x1 goes
+    through the RMSNorm scale pass for r1 and u1 (the bf16 block gets them
+    from its epilogue)."""
 
     def __init__(self, shape, weights, device="cuda", concurrent=True, fp8_wgrad=True):
         self.s = s = shape
@@ -226,6 +229,7 @@ class BlockFP8:
         self.Wqkv_q, self.Wo_q, self.Wg_q, self.Wu_q, self.Wd_q = (q(nqkv, Hd), q(Hd, a_in), q(I, Hd), q(I, Hd),
                                                                    q(Hd, I))
         self.WdT_q, self.WguT_q, self.WoT_q = q(I, Hd), q(Hd, 2 * I), q(a_in, Hd)
+        self.WqkvT_q = q(Hd, nqkv) if fp8_wgrad else None
         # activations
         self.U0, self.U1 = e(T, Hd, **bf), e(T, Hd, **bf)
         self.U0_q, self.A_q, self.U1_q, self.H_q = q(T, Hd), q(T, a_in), q(T, Hd), q(T, I)
@@ -234,6 +238,7 @@ class BlockFP8:
         if fp8_wgrad:  # transposed, per-column codes of the weight gradients' operands
             self.dx2T_q, self.HT_q, self.GT_q = q(Hd, T), q(I, T), q(2 * I, T)
             self.U1T_q, self.dx1T_q, self.AT_q = q(Hd, T), q(Hd, T), q(a_in, T)
+            self.U0T_q = q(Hd, T)
         self.cos_sin = rope_table(s.theta, d, s.seq_len, device=device)
         self.rstd0, self.rstd1, self.coef1 = e(T, **f32), e(T, **f32), e(T, **f32)
         self.fwd = {"Q": e(T, s.n_q * d, **bf), "K": e(T, s.n_kv * d, **bf), "V": e(T, s.n_kv * d, **bf),
@@ -252,16 +257,20 @@ class BlockFP8:
                    lib.coda_linear_dswiglu_fp8_workspace_size(T, I, Hd),
                    lib.coda_rmsnorm_linear_dx_fp8_workspace_size(T, 2 * I, Hd),
                    lib.coda_linear_qknorm_rope_bwd_workspace_size(T, Hd, s.n_q, s.n_kv, d),
+                   lib.coda_linear_qknorm_rope_bwd_fp8_workspace_size(T, Hd, s.n_q, s.n_kv, d),
                    lib.coda_gemm_epilogue_workspace_size(), lib.coda_linear_fp8_workspace_size(Hd, I, T),
                    lib.coda_linear_fp8_workspace_size(2 * I, Hd, T), lib.coda_linear_fp8_workspace_size(Hd, a_in, T))
         self.ws = workspace(need, device)
         self.s2 = torch.cuda.Stream(device=device) if concurrent else None
         self.ws2 = workspace(need, device) if concurrent else self.ws
 
-    LAUNCHES = {"quant_w": 14, "fwd": 12, "bwd": 20}
+    # kernels per stage (coda_launch_count at 8192 tokens, hidden 8192, the
+    # default launch switches: split GEMM launches count twice)
+    LAUNCHES = {"quant_w": 17, "fwd": 14, "bwd": 48}
+    LAUNCHES_BF16_WGRAD = {"quant_w": 14, "fwd": 14, "bwd": 25}
 
     def launches(self):
-        return self.LAUNCHES
+        return self.LAUNCHES if self.fp8_wgrad else self.LAUNCHES_BF16_WGRAD
 
     def gemm_flops(self):
         return Block.gemm_flops(self)
@@ -281,6 +290,8 @@ class BlockFP8:
         quantize_fp8_cols(w["Wd"], XTq=self.WdT_q[0], scale=self.WdT_q[1])
         quantize_fp8_cols(w["Wg"], w["Wu"], XTq=self.WguT_q[0], scale=self.WguT_q[1])
         quantize_fp8_cols(w["Wo"], XTq=self.WoT_q[0], scale=self.WoT_q[1])
+        if self.fp8_wgrad:
+            quantize_fp8_cols(w["Wqkv"], XTq=self.WqkvT_q[0], scale=self.WqkvT_q[1])
 
     def _wgrad(self, A, lda, B, ldb, D, M, N, K, col_scale=None, ws=None):
         """D [M, N] = A^T B (A stored [K, M], B stored [K, N]) in bf16, with an
@@ -330,6 +341,8 @@ class BlockFP8:
             if self.fp8_wgrad:
                 self._wgrad_fp8(dx2, self.dx2T_q, self.H, self.HT_q, self.dW["dWd"], ws2)
                 self._wgrad_fp8(self.Gp, self.GT_q, self.U1, self.U1T_q, self.dWgu, ws2)
+                # the QKV backward's dW operand: u0 = x0 ⊙ gamma_attn per column
+                quantize_fp8_cols(self.U0, XTq=self.U0T_q[0], scale=self.U0T_q[1])
             else:
                 self._wgrad(dx2, Hd, self.H, I, self.dW["dWd"], Hd, I, T, ws=ws2)
                 self._wgrad(self.Gp, 2 * I, self.U1, Hd, self.dW["dWg"], I, Hd, T, ws=ws2)
@@ -348,10 +361,17 @@ class BlockFP8:
                 self._wgrad_fp8(dx1, self.dx1T_q, A, self.AT_q, self.dW["dWo"], ws2)
             else:
                 self._wgrad(dx1, Hd, A, a_in, self.dW["dWo"], Hd, a_in, T, ws=ws2)
-        linear_qknorm_rope_bwd(dQ, dK, dV, self.fwd["qk_save"], self.fwd["V"], w["gamma_q"], w["gamma_k"], pos,
-                               self.cos_sin, s.n_q, s.n_kv, x0, w["Wqkv"], rstd=self.rstd0,
-                               gamma_in=w["gamma_attn"], dX_resid=dx1, eps=s.eps, head_dim=s.head_dim,
-                               ws=self.ws, out=self.grads_qkv)
+        if self.fp8_wgrad:
+            linear_qknorm_rope_bwd_fp8(dQ, dK, dV, self.fwd["qk_save"], self.fwd["V"], w["gamma_q"], w["gamma_k"],
+                                       pos, self.cos_sin, s.n_q, s.n_kv, self.WqkvT_q[0], self.WqkvT_q[1],
+                                       self.U0T_q[0], self.U0T_q[1], X=x0, rstd=self.rstd0,
+                                       gamma_in=w["gamma_attn"], dX_resid=dx1, eps=s.eps, head_dim=s.head_dim,
+                                       ws=self.ws, out=self.grads_qkv)
+        else:
+            linear_qknorm_rope_bwd(dQ, dK, dV, self.fwd["qk_save"], self.fwd["V"], w["gamma_q"], w["gamma_k"], pos,
+                                   self.cos_sin, s.n_q, s.n_kv, x0, w["Wqkv"], rstd=self.rstd0,
+                                   gamma_in=w["gamma_attn"], dX_resid=dx1, eps=s.eps, head_dim=s.head_dim,
+                                   ws=self.ws, out=self.grads_qkv)
         self._join()
         mark("bwd")
         return {"dx0": self.grads_qkv["dX"], "dA": self.dA, "dx1": dx1, "dWqkv": self.grads_qkv["dW"],

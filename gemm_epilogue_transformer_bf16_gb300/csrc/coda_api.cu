@@ -1320,6 +1320,34 @@ static int qk_bwd_blocks(int64_t M) {
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(M, coda::QK_BWD_WARPS), 1184)));
 }
 
+// The per-head map of the QK-norm + RoPE backward into G' = r ⊙ [dq | dk | dv]
+// (bf16 [M, N]); with coef it also writes the input RMSNorm's row coefficient
+// c.  Token rows are staged by bulk copies (one block per SM) unless a row's
+// tensors are too large for the shared-memory ring.  Then dgamma_q | dgamma_k
+// from the blocks' partials (dgqk, nblk x 256).
+static int qk_bwd_map(const coda_bf16* dQ, const coda_bf16* dK, const coda_bf16* dV, const coda_bf16* qk_save,
+                      const coda_bf16* V, const float* gamma_q, const float* gamma_k, const int32_t* pos,
+                      const float* cos_sin, int32_t max_pos, float eps, int32_t n_q, int32_t n_kv,
+                      int32_t rope_pairing, const float* rstd, int64_t M, int64_t Kdim, __nv_bfloat16* Gp,
+                      float* coef, float* dgqk, int nblk, float* dgamma_q, float* dgamma_k, int sms, int* status,
+                      cudaStream_t s) {
+  int nmap = nblk;
+  if (qk_tma_enabled() && coda::qk_bwd_tma_stages(n_q, n_kv) > 0) {
+    nmap = std::min(nblk, sms);
+    CU(coda::launch_qk_bwd_tma(BF(dQ), BF(dK), BF(dV), BF(qk_save), BF(V), gamma_q, gamma_k, pos,
+                               reinterpret_cast<const float2*>(cos_sin), max_pos, eps, n_q, n_kv, rstd, M,
+                               1.f / static_cast<float>(Kdim), Gp, coef, dgqk, nmap, status, s,
+                               rope_pairing == CODA_ROPE_HALF, TIMEOUT_NS));
+  } else {
+    CU(coda::launch_qk_bwd(BF(dQ), BF(dK), BF(dV), BF(qk_save), BF(V), gamma_q, gamma_k, pos,
+                           reinterpret_cast<const float2*>(cos_sin), max_pos, eps, n_q, n_kv, rstd, M,
+                           1.f / static_cast<float>(Kdim), Gp, coef, dgqk, nblk, status, s,
+                           rope_pairing == CODA_ROPE_HALF));
+  }
+  CU(coda::launch_colsum(dgqk, nmap, 256, 256, dgamma_q, s, 128, dgamma_k));
+  return CODA_OK;
+}
+
 size_t coda_linear_qknorm_rope_bwd_workspace_size(int64_t M, int64_t Kdim, int32_t n_q, int32_t n_kv,
                                                   int32_t head_dim) {
   const int64_t N = static_cast<int64_t>(n_q + 2 * n_kv) * head_dim;
@@ -1371,23 +1399,8 @@ int coda_linear_qknorm_rope_bwd(const coda_bf16* dQ, const coda_bf16* dK, const 
   float* dgp = w.take<float>(static_cast<size_t>(4 * ntb) * Kdim);
   int* status = static_cast<int*>(ws);
   cudaStream_t s = S(stream);
-  // the map also writes the input RMSNorm's row coefficient c (with rstd);
-  // rows staged by bulk copies (one block per SM) unless a row's tensors are
-  // too large for the shared-memory ring
-  int nmap = nblk;
-  if (qk_tma_enabled() && coda::qk_bwd_tma_stages(n_q, n_kv) > 0) {
-    nmap = std::min(nblk, sms);
-    CU(coda::launch_qk_bwd_tma(BF(dQ), BF(dK), BF(dV), BF(qk_save), BF(V), gamma_q, gamma_k, pos,
-                               reinterpret_cast<const float2*>(cos_sin), max_pos, eps, n_q, n_kv, rstd, M,
-                               1.f / static_cast<float>(Kdim), Gp, norm ? coef : nullptr, dgqk, nmap, status, s,
-                               rope_pairing == CODA_ROPE_HALF, TIMEOUT_NS));
-  } else {
-    CU(coda::launch_qk_bwd(BF(dQ), BF(dK), BF(dV), BF(qk_save), BF(V), gamma_q, gamma_k, pos,
-                           reinterpret_cast<const float2*>(cos_sin), max_pos, eps, n_q, n_kv, rstd, M,
-                           1.f / static_cast<float>(Kdim), Gp, norm ? coef : nullptr, dgqk, nblk, status, s,
-                           rope_pairing == CODA_ROPE_HALF));
-  }
-  CU(coda::launch_colsum(dgqk, nmap, 256, 256, dgamma_q, s, 128, dgamma_k));
+  CK(qk_bwd_map(dQ, dK, dV, qk_save, V, gamma_q, gamma_k, pos, cos_sin, max_pos, eps, n_q, n_kv, rope_pairing, rstd,
+                M, Kdim, Gp, norm ? coef : nullptr, dgqk, nblk, dgamma_q, dgamma_k, sms, status, s));
   {  // D = G' W_qkv;  dX = gamma_in D - c X + dX_resid with the dgamma_in column
      // partials sum_i X_ik D_ik  (without RMSNorm: D + dX_resid)
     Plan p;
@@ -2362,6 +2375,121 @@ int coda_rmsnorm_linear_dx_fp8(const uint8_t* Gq, const float* sg, const uint8_t
   p.e.ld_part = K;
   CK(run(p, status, s));
   CU(coda::launch_colsum(dgp, 4 * ntb, K, K, dgamma, s));
+  return CODA_OK;
+}
+
+size_t coda_linear_qknorm_rope_bwd_fp8_workspace_size(int64_t M, int64_t Kdim, int32_t n_q, int32_t n_kv,
+                                                      int32_t head_dim) {
+  const int64_t N = static_cast<int64_t>(n_q + 2 * n_kv) * head_dim;
+  SizeCursor c;
+  c.take<__nv_bfloat16>(static_cast<size_t>(M) * N);          // G'
+  c.take<float>(M);                                           // coef
+  c.take<float>(static_cast<size_t>(qk_bwd_blocks(M)) * 256);  // dgamma_q|k partials
+  c.take<float>(static_cast<size_t>(4 * cdiv(M, 128)) * Kdim);  // dgamma_in partials per (token block, warp)
+  c.take<uint8_t>(static_cast<size_t>(M) * N);                // Gq: G' per row
+  c.take<float>(M);                                           // sg
+  c.take<uint8_t>(static_cast<size_t>(N) * M);                // GTq: G'^T per column of G'
+  c.take<float>(N);                                           // sgT
+  return c.off;
+}
+
+int coda_linear_qknorm_rope_bwd_fp8(const coda_bf16* dQ, const coda_bf16* dK, const coda_bf16* dV,
+                                    const coda_bf16* qk_save, const coda_bf16* V, const float* gamma_q,
+                                    const float* gamma_k, const int32_t* pos, const float* cos_sin, int32_t max_pos,
+                                    float eps, int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t rope_pairing,
+                                    const coda_bf16* X, const float* rstd, const float* gamma_in,
+                                    const uint8_t* WTq, const float* sw, const uint8_t* UTq, const float* su,
+                                    const coda_bf16* dX_resid, coda_bf16* dX, coda_bf16* dW_qkv, float* dgamma_in,
+                                    float* dgamma_q, float* dgamma_k, int64_t M, int64_t Kdim, void* ws,
+                                    size_t ws_bytes, coda_stream stream) {
+  if (head_dim != 128) return CODA_ERR_UNSUPPORTED;
+  if (n_q <= 0 || n_kv <= 0 || max_pos <= 0) return CODA_ERR_INVALID_ARG;
+  if (rope_pairing != CODA_ROPE_INTERLEAVED && rope_pairing != CODA_ROPE_HALF) return CODA_ERR_INVALID_ARG;
+  const int64_t N = static_cast<int64_t>(n_q + 2 * n_kv) * head_dim;
+  CK(dims_ok(M, N, Kdim));
+  if (M % 16) return CODA_ERR_UNSUPPORTED;  // 16-byte rows of the K-major token operands of the dW GEMM
+  CK(ws_ok(ws, ws_bytes, coda_linear_qknorm_rope_bwd_fp8_workspace_size(M, Kdim, n_q, n_kv, head_dim)));
+  if (M == 0) return CODA_OK;
+  for (const void* q : {(const void*)dQ, (const void*)dK, (const void*)dV, (const void*)qk_save, (const void*)V,
+                        (const void*)gamma_q, (const void*)gamma_k, (const void*)pos, (const void*)cos_sin,
+                        (const void*)WTq, (const void*)sw, (const void*)UTq, (const void*)su, (const void*)dX,
+                        (const void*)dW_qkv, (const void*)dgamma_q, (const void*)dgamma_k})
+    CK(req(q));
+  for (const void* q : {(const void*)dQ, (const void*)dK, (const void*)dV, (const void*)qk_save, (const void*)V,
+                        (const void*)gamma_q, (const void*)gamma_k, (const void*)cos_sin, (const void*)X,
+                        (const void*)rstd, (const void*)gamma_in, (const void*)WTq, (const void*)sw,
+                        (const void*)UTq, (const void*)su, (const void*)dX_resid, (const void*)dX,
+                        (const void*)dW_qkv, (const void*)dgamma_in, (const void*)dgamma_q, (const void*)dgamma_k})
+    CK(al(q));
+  const bool norm = rstd != nullptr;
+  if (norm && (!gamma_in || !dgamma_in || !X)) return CODA_ERR_INVALID_ARG;
+  const int sms = num_sms();
+  if (sms <= 0) return CODA_ERR_CUDA;
+  WsCursor w(ws);
+  __nv_bfloat16* Gp = w.take<__nv_bfloat16>(static_cast<size_t>(M) * N);
+  float* coef = w.take<float>(M);
+  const int nblk = qk_bwd_blocks(M);
+  float* dgqk = w.take<float>(static_cast<size_t>(nblk) * 256);
+  const int64_t ntb = cdiv(M, 128);
+  float* dgp = w.take<float>(static_cast<size_t>(4 * ntb) * Kdim);
+  uint8_t* Gq = w.take<uint8_t>(static_cast<size_t>(M) * N);
+  float* sg = w.take<float>(M);
+  uint8_t* GTq = w.take<uint8_t>(static_cast<size_t>(N) * M);
+  float* sgT = w.take<float>(N);
+  int* status = static_cast<int*>(ws);
+  cudaStream_t s = S(stream);
+  CK(qk_bwd_map(dQ, dK, dV, qk_save, V, gamma_q, gamma_k, pos, cos_sin, max_pos, eps, n_q, n_kv, rope_pairing, rstd,
+                M, Kdim, Gp, norm ? coef : nullptr, dgqk, nblk, dgamma_q, dgamma_k, sms, status, s));
+  CU(coda::launch_quantize_fp8_rows(Gp, N, M, N, Gq, N, sg, sms, s));
+  {  // D = G' W_qkv on the codes;  dX = gamma_in D - c X + dX_resid with the
+     // dgamma_in column partials  (without RMSNorm: D + dX_resid)
+    Plan p;
+    p.kind = norm ? coda::EpiKind::RmsDx : coda::EpiKind::Plain;
+    p.fp8 = 1;
+    p.A = Gq;
+    p.lda = N;
+    p.B = WTq;
+    p.ldb = N;
+    p.M = M;
+    p.N = Kdim;
+    p.K = N;
+    p.e.D = dX;
+    p.e.ldd = Kdim;
+    p.e.aux0 = BF(dX_resid);
+    p.e.ld_aux0 = Kdim;
+    if (norm) {
+      p.e.acc_rs = sg;
+      p.e.acc_cs = sw;
+      p.e.row_coef = coef;
+      p.e.aux1 = BF(X);
+      p.e.ld_aux1 = Kdim;
+      p.e.col_scale = gamma_in;
+      p.e.partials = dgp;
+      p.e.ld_part = Kdim;
+    } else {
+      p.e.row_scale = sg;
+      p.e.col_scale = sw;
+    }
+    CK(run(p, status, s));
+  }
+  if (norm) CU(coda::launch_colsum(dgp, 4 * ntb, Kdim, Kdim, dgamma_in, s));
+  CU(coda::launch_quantize_fp8_cols(Gp, N, M, nullptr, 0, 0, N, GTq, M, sgT, sms, s));
+  {  // dW_qkv = G'^T U on the column codes of both
+    Plan p;
+    p.fp8 = 1;
+    p.A = GTq;
+    p.lda = M;
+    p.B = UTq;
+    p.ldb = M;
+    p.M = N;
+    p.N = Kdim;
+    p.K = M;
+    p.e.D = dW_qkv;
+    p.e.ldd = Kdim;
+    p.e.row_scale = sgT;
+    p.e.col_scale = su;
+    CK(run(p, status, s));
+  }
   return CODA_OK;
 }
 

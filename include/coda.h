@@ -538,6 +538,35 @@ int coda_rmsnorm_linear_dx_fp8(const uint8_t* Gq, const float* sg, const uint8_t
                                coda_bf16* dX, float* dgamma, int64_t M, int64_t N, int64_t K, void* ws,
                                size_t ws_bytes, coda_stream stream);
 
+/* The backward of linear_qknorm_rope with both of its GEMMs on e4m3
+ * operands.  The per-head map (RoPE^-1, QK-RMSNorm backward, dgamma_q,
+ * dgamma_k) and the RMSNorm coefficient c are those of
+ * coda_linear_qknorm_rope_bwd and write G' = r ⊙ [dq | dk | dv] in bf16
+ * into the workspace; G' is then quantised per row (Gq, sg) and per column
+ * (GTq, sgT) into the workspace, and
+ *   D  = (sg ⊙ Gq)(sw ⊙ WTq)^T          (G' W_qkv; WTq = coda_quantize_fp8_cols(W_qkv)),
+ *   dX = gamma_in ⊙ D - c ⊙ X + dX_resid,  dgamma_in_k = sum_i X_ik D_ik
+ *        (without rstd: dX = D + dX_resid),
+ *   dW_qkv = (sgT ⊙ GTq)(su ⊙ UTq)^T     (G'^T U; UTq = coda_quantize_fp8_cols(U)),
+ * where U is the forward GEMM's input: U = X ⊙ gamma_in (the U of
+ * coda_rmsnorm_scale) with the input RMSNorm, X without it, so that
+ * G'^T U = (G'^T X) diag(gamma_in).  Arguments as in
+ * coda_linear_qknorm_rope_bwd, with W_qkv replaced by WTq [Kdim, N] uint8
+ * (row stride N = (n_q+2n_kv)*128), sw [Kdim], and the codes of U by
+ * UTq [Kdim, M] uint8 (row stride M), su [Kdim].  M % 16 == 0 (the dW GEMM
+ * contracts over the tokens); CODA_ERR_UNSUPPORTED otherwise. */
+size_t coda_linear_qknorm_rope_bwd_fp8_workspace_size(int64_t M, int64_t Kdim, int32_t n_q, int32_t n_kv,
+                                                      int32_t head_dim);
+int coda_linear_qknorm_rope_bwd_fp8(const coda_bf16* dQ, const coda_bf16* dK, const coda_bf16* dV,
+                                    const coda_bf16* qk_save, const coda_bf16* V, const float* gamma_q,
+                                    const float* gamma_k, const int32_t* pos, const float* cos_sin, int32_t max_pos,
+                                    float eps, int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t rope_pairing,
+                                    const coda_bf16* X, const float* rstd, const float* gamma_in,
+                                    const uint8_t* WTq, const float* sw, const uint8_t* UTq, const float* su,
+                                    const coda_bf16* dX_resid, coda_bf16* dX, coda_bf16* dW_qkv, float* dgamma_in,
+                                    float* dgamma_q, float* dgamma_k, int64_t M, int64_t Kdim, void* ws,
+                                    size_t ws_bytes, coda_stream stream);
+
 /* ------------------------------------------------------------------------
  * NVFP4 operands: 4-bit e2m1 elements, one e4m3 scale per 16 consecutive
  * elements along K, an fp32 scale per row; the GEMM runs on tcgen05.mma

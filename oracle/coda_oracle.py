@@ -496,6 +496,58 @@ def rmsnorm_linear_dx_fp8(Gv, sgp, WTv, sw, X, gamma, coef, dX_resid=None):
     return {"dX": dX, "dgamma": (X * D).sum(axis=0), "D": D}
 
 
+def _bf16(x):
+    """Round to bfloat16 (nearest even), returned as float64."""
+    import torch
+    return torch.from_numpy(np.asarray(x, dtype=np.float64)).to(torch.bfloat16).double().numpy()
+
+
+def linear_qknorm_rope_fp8_bwd(dQ, dK, dV, qk_save, V, gamma_q, gamma_k, pos, theta, eps, n_q, n_kv, head_dim,
+                               WTv, sw, UTv, su, X=None, row_scale=None, gamma_in=None, dX_resid=None,
+                               pairing="interleaved"):
+    """The backward of linear_qknorm_rope_fp8_fwd with both gradient GEMMs on
+    e4m3 operands.  Per head the inverse rotation and the QK-RMSNorm backward
+    (qk_rmsnorm_rope_bwd) at the saved pre-norm q|k give dq, dk; with dv = dV,
+    G = [dq | dk | dv] is the gradient of the projection y = [q | k | v] and
+    G' = r ⊙ G (r = 1 without row_scale).  Reading: G' is held in bf16 and
+    quantised per row (for D = G' W) and per column (for dW = G'^T U) by the
+    rules of quantize_fp8_rows / quantize_fp8_cols; W enters as W^T quantised
+    per input feature (WTv, sw) and U, the forward GEMM's input (x ⊙ gamma_in
+    with the input RMSNorm), likewise (UTv, su).  Then
+        D = (G'_q)(W^T_q)^T,   dW = (G'^T_q)(U^T_q)^T,
+        with row_scale: c_i = r_i^2 sum_n G_in y_in / K  (K = X's width),
+        dX = gamma_in ⊙ D - c ⊙ X (+ dX_resid),  dgamma_in = sum_i X_i ⊙ D_i;
+        without: dX = D (+ dX_resid)
+    (the chain rule of y = r ⊙ ((X ⊙ gamma_in) W^T), as in
+    rmsnorm_linear_dx_fp8)."""
+    d = head_dim
+    qk_save = np.asarray(qk_save, dtype=np.float64)
+    M = qk_save.shape[0]
+    q = _heads(qk_save[:, : n_q * d], n_q, d)
+    k = _heads(qk_save[:, n_q * d:], n_kv, d)
+    dq, dgq = qk_rmsnorm_rope_bwd(q, gamma_q, pos, theta, eps, _heads(dQ, n_q, d), pairing)
+    dk, dgk = qk_rmsnorm_rope_bwd(k, gamma_k, pos, theta, eps, _heads(dK, n_kv, d), pairing)
+    G = np.concatenate([dq.reshape(M, -1), dk.reshape(M, -1), np.asarray(dV, dtype=np.float64)], axis=1)
+    r = np.ones(M) if row_scale is None else np.asarray(row_scale, dtype=np.float64)
+    Gp = _bf16(G * r[:, None])
+    _, gv, sg = quantize_fp8_rows(Gp)
+    _, gtv, sgt = quantize_fp8_cols(Gp)
+    D = _deq(gv, sg) @ _deq(WTv, sw).T
+    out = {"Gr": G * r[:, None], "Gp": Gp, "D": D, "dgamma_q": dgq, "dgamma_k": dgk,
+           "dW": _deq(gtv, sgt) @ _deq(UTv, su).T}
+    if row_scale is None:
+        dX = D
+    else:
+        Xf = np.asarray(X, dtype=np.float64)
+        y = np.concatenate([qk_save, np.asarray(V, dtype=np.float64)], axis=1)
+        coef = r * r * (G * y).sum(axis=1) / Xf.shape[1]
+        dX = D * np.asarray(gamma_in, dtype=np.float64)[None, :] - coef[:, None] * Xf
+        out["dgamma_in"] = (Xf * D).sum(axis=0)
+        out["coef"] = coef
+    out["dX"] = dX if dX_resid is None else dX + np.asarray(dX_resid, dtype=np.float64)
+    return out
+
+
 # ---------------------------------------------------------------------------
 # NVFP4 operands: e2m1 elements, an e4m3 scale per 16 elements, fp32 row scale
 # ---------------------------------------------------------------------------

@@ -744,6 +744,93 @@ def check_fp8_epilogue_ops(o):
     return max(e)
 
 
+def _bf16_t(x):
+    """bf16 rounding through torch (nearest even), as float64."""
+    return torch.from_numpy(np.asarray(x, dtype=np.float64)).to(torch.bfloat16).double().numpy()
+
+
+def check_fp8_qkv_bwd(o):
+    """The QKV + QK-norm + RoPE backward on e4m3 operands.
+    (1) dQ = dK = 0 and operands every quantiser takes exactly: token rows
+    X_i = +-1/r_i with r = (1, 1/2, 1/4), so that at eps = 0 the input
+    RMSNorm factor is exactly r_i and the columns of U = X ⊙ gamma are
+    exact; W^T rows exact; dV of e4m3 values of magnitude >= 2^-4 (or 0)
+    times 2^-6 with 448 * 2^-6 on its first row and column, so that
+    G' = r ⊙ [0 | 0 | dV] is exact per row and per column.  Then dX, dW and
+    dgamma_in equal rmsnorm_linear_bwd (G = [0 | 0 | dV]); without the input
+    RMSNorm, dX = G W + dX_resid and dW = G^T X (X column-exact).
+    (2) General dQ, dK, dV (QK eps 0.5, so the q and k terms of c count):
+    G' equals r ⊙ block_bwd's dqkv rounded to bf16; dgamma_q and dgamma_k
+    equal block_bwd's; c_i equals r_i^2 dL/dt / K for L(t) = <dQ, Q> +
+    <dK, K> + <dV, V> at token i's projection scaled by t (finite
+    differences); and D = G'_q W, dW = G'^T_q U lie within the e4m3
+    rounding bound of G' (half a step: 2^-4 |g| in the normal range,
+    2^-10 s below it, s the scale of g's row of G' or G'^T) around G' W and
+    G'^T U, row by row, with one token's gradients 10^-6 of the others' (the
+    other axis's scales would flush them to zero)."""
+    codes, vals = _e4m3_table()
+    vals = vals[(np.abs(vals) <= 448.0) & ((np.abs(vals) >= 2.0 ** -4) | (vals == 0))]
+    rg = RNG(27)
+    p, cfg = tiny_block(seed=16)
+    n_q, n_kv, d, theta = cfg["n_q"], cfg["n_kv"], cfg["head_dim"], cfg["theta"]
+    M, h = p["x0"].shape
+    nqk, N = (n_q + n_kv) * d, (n_q + 2 * n_kv) * d
+    r = np.array([1.0, 0.5, 0.25])
+    X = np.where(rg.standard_normal((M, h)) < 0, -1.0, 1.0) / r[:, None]
+    gam = p["gamma_attn"]
+    W = _e4m3_exact(rg, (h, N), vals).T.copy()
+    U = X * gam[None, :]
+    _, wtv, sw = o.quantize_fp8_cols(W)
+    _, utv, su = o.quantize_fp8_cols(U)
+    gq, gk, pos = p["gamma_q"], p["gamma_k"], p["pos"]
+    e = []
+    # (1) exact operands
+    y = o.rmsnorm(X, gam, 0.0) @ W.T
+    dV = vals[rg.integers(0, len(vals), size=(M, n_kv * d))] * 2.0 ** -6
+    dV[0, :] = np.where(rg.standard_normal(n_kv * d) < 0, -448.0, 448.0) * 2.0 ** -6
+    dV[:, 0] = 448.0 * 2.0 ** -6
+    zq, zk = np.zeros((M, n_q * d)), np.zeros((M, n_kv * d))
+    G = np.hstack([zq, zk, dV])
+    out = o.linear_qknorm_rope_fp8_bwd(zq, zk, dV, y[:, :nqk], y[:, nqk:], gq, gk, pos, theta, 1e-6, n_q, n_kv, d,
+                                       wtv, sw, utv, su, X=X, row_scale=r, gamma_in=gam)
+    b = o.rmsnorm_linear_bwd(X, gam, W, 0.0, G)
+    e += [_rel(out["dX"], b["dX"]), _rel(out["dW"], b["dW"]), _rel(out["dgamma_in"], b["dgamma"])]
+    X2 = _e4m3_exact(rg, (h, M), vals).T.copy()
+    _, xtv, sx = o.quantize_fp8_cols(X2)
+    R = rg.standard_normal((M, h))
+    out = o.linear_qknorm_rope_fp8_bwd(zq, zk, dV, y[:, :nqk], y[:, nqk:], gq, gk, pos, theta, 1e-6, n_q, n_kv, d,
+                                       wtv, sw, xtv, sx, dX_resid=R)
+    e += [_rel(out["dX"], G @ W + R), _rel(out["dW"], G.T @ X2)]
+    # (2) general gradients
+    eps = 0.5
+    rr = o.rms_inv(X, eps)
+    y = o.rmsnorm(X, gam, eps) @ W.T
+    # token 2's gradients 1e-6 of the others': quantised with the other
+    # tokens' scale (per column) they would underflow, outside the bound
+    tiny = np.array([1.0, 1.0, 1e-6])[:, None]
+    dQ, dK, dV = p["dQ"] * tiny, p["dK"] * tiny, p["dV"] * tiny
+    out = o.linear_qknorm_rope_fp8_bwd(dQ, dK, dV, y[:, :nqk], y[:, nqk:], gq, gk, pos, theta, eps, n_q, n_kv, d,
+                                       wtv, sw, utv, su, X=X, row_scale=rr, gamma_in=gam)
+    bb = o.block_bwd(dict(p, x0=X, Wqkv=W, gamma_attn=gam, dQ=dQ, dK=dK, dV=dV), n_q, n_kv, d, theta, eps)
+    Gp = _bf16_t(bb["dqkv"] * rr[:, None])
+    e += [_rel(out["Gp"], Gp), _rel(out["dgamma_q"], bb["dgamma_q"]), _rel(out["dgamma_k"], bb["dgamma_k"])]
+
+    def L(i, t):
+        yt = y.copy()
+        yt[i] *= t
+        Q = o.qk_rmsnorm_rope_fwd(yt[:, : n_q * d].reshape(M, n_q, d), gq, pos, theta, eps).reshape(M, -1)
+        K = o.qk_rmsnorm_rope_fwd(yt[:, n_q * d: nqk].reshape(M, n_kv, d), gk, pos, theta, eps).reshape(M, -1)
+        return float((dQ * Q).sum() + (dK * K).sum() + (dV * yt[:, nqk:]).sum())
+    fd = np.array([(L(i, 1 + 1e-6) - L(i, 1 - 1e-6)) / 2e-6 for i in range(M)])
+    e.append(_rel(out["coef"], rr ** 2 * fd / h))
+    for got, A, B in ((out["D"], Gp, W), (out["dW"], Gp.T, U)):   # got ~ A B, A quantised per row
+        s = np.abs(A).max(axis=1) / 448.0
+        bound = (2.0 ** -4 * np.abs(A) + 2.0 ** -10 * s[:, None]) @ np.abs(B) * (1 + 1e-6)
+        ex = np.maximum(np.abs(got - A @ B) - bound, 0.0).max(axis=1) / np.abs(A @ B).max(axis=1)
+        e.append(float(ex.max()))
+    return max(e)
+
+
 def _e2m1_decode_table():
     """The 16 e2m1 codes decoded from the format's definition: bit 3 sign,
     bits 1-2 exponent with bias 1, bit 0 mantissa; exponent 0 is subnormal
@@ -929,6 +1016,7 @@ ALL_CHECKS = {
     "fp8_linear": (check_fp8_linear, 1e-14),
     "fp8_cols_quantizer": (check_fp8_cols_quantizer, 0.0),
     "fp8_epilogue_ops": (check_fp8_epilogue_ops, 1e-7),
+    "fp8_qkv_bwd": (check_fp8_qkv_bwd, 1e-6),
     "quantised_swiglu_row_factor": (check_quantised_swiglu_row_factor, 1e-12),
     "linear_sigmoid": (check_linear_sigmoid, 1e-7),
     "rmsnorm_ce_library": (check_rmsnorm_ce_library, 1e-12),

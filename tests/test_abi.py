@@ -45,6 +45,42 @@ def test_binding_covers_every_symbol():
     assert not missing, f"no ctypes signature for: {missing}"
 
 
+def declared_parameters():
+    """name -> list of parameter declarations, from include/coda.h."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(?:int|size_t|uint64_t|const char\s*\*)\s+(coda_\w+)\s*\(([^)]*)\)", src):
+        params = [p.strip() for p in m.group(2).split(",")]
+        out[m.group(1)] = [] if params in ([""], ["void"]) else params
+    return out
+
+
+def _ctype_of(param):
+    """The ctypes type a C parameter declaration is marshalled as."""
+    if "*" in param or param.startswith("coda_stream"):
+        return ctypes.c_void_p
+    base = param.rsplit(" ", 1)[0].replace("const ", "").strip()
+    return {"int64_t": ctypes.c_int64, "int32_t": ctypes.c_int32, "int": ctypes.c_int, "uint32_t": ctypes.c_uint32,
+            "float": ctypes.c_float, "size_t": ctypes.c_size_t}[base]
+
+
+def test_binding_signatures_match_header():
+    """Every ctypes signature has the header's parameter count and, position
+    by position, the type each parameter is passed as (a pointer or a
+    stream handle as void*, each integer and float at its width)."""
+    import gemm_epilogue_transformer_bf16_gb300 as coda
+    bad = []
+    for name, params in declared_parameters().items():
+        want = [_ctype_of(p) for p in params]
+        got = coda._SIGS[name][0]
+        if len(got) != len(want) or any(ctypes.sizeof(a) != ctypes.sizeof(b) or
+                                         (a is ctypes.c_void_p) != (b is ctypes.c_void_p) or
+                                         (a is ctypes.c_float) != (b is ctypes.c_float)
+                                         for a, b in zip(got, want)):
+            bad.append((name, len(got), len(want)))
+    assert not bad, f"ctypes signatures that differ from include/coda.h: {bad}"
+
+
 def test_launch_count_without_launches(lib):
     """The launch counter is host state: readable without a GPU, and zero
     on a host without one (nothing can have been launched)."""

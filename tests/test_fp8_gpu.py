@@ -17,7 +17,7 @@ import torch
 
 import synth
 from oracle import coda_oracle as O
-from parity import assert_bf16, assert_f32, to_np
+from parity import assert_bf16, assert_bf16_within, assert_f32, e4m3_step_allowance, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -162,6 +162,61 @@ def test_rmsnorm_linear_dx_fp8(coda):
     r = O.rmsnorm_linear_dx_fp8(gv, osg, wv, osw, to_np(X), to_np(gam), to_np(coef), dX_resid=to_np(R))
     assert_bf16(out["dX"], r["dX"], "fp8 RMSNorm dX")
     assert_bf16(out["dgamma"], r["dgamma"], "fp8 RMSNorm dgamma")
+
+
+@pytest.mark.parametrize("norm,pairing", [(True, "interleaved"), (False, "half")])
+def test_linear_qknorm_rope_bwd_fp8(coda, norm, pairing):
+    """The QKV backward with both GEMMs on e4m3 operands: the per-head map
+    into G' (in the workspace), G' quantised per row for dX and per column
+    for dW, W^T and U^T given as column codes (checked bit for bit against
+    the oracle's).  The saved q|k and v are seeded inputs (the backward is
+    defined at any saved values).  G' is computed in fp32 by the kernel and
+    in fp64 by the oracle, so at a bf16 rounding tie the two may round it
+    differently and the e4m3 codes taken from it may differ by one step;
+    the max-error bound of dX, dW and dgamma_in carries that admissible
+    change through the GEMMs (parity.e4m3_step_allowance); dgamma_q and
+    dgamma_k take no quantised operand and are held to the plain rule.
+    304 tokens (two 128-token tiles and a ragged tail), 272 features, 2 q
+    and 1 kv heads."""
+    M, Kd, n_q, n_kv, d = 304, 272, 2, 1, 128
+    N = (n_q + 2 * n_kv) * d
+    qk = synth.randn_bf16((M, (n_q + n_kv) * d), 1.0, 71)
+    V = synth.randn_bf16((M, n_kv * d), 1.0, 72)
+    dQ = synth.randn_bf16((M, n_q * d), 1.0, 73)
+    dK = synth.randn_bf16((M, n_kv * d), 1.0, 74)
+    dV = synth.randn_bf16((M, n_kv * d), 1.0, 75)
+    W = synth.randn_bf16((N, Kd), 1 / math.sqrt(Kd), 76)
+    X = synth.randn_bf16((M, Kd), 1.0, 77)
+    R = synth.randn_bf16((M, Kd), 1.0, 78)
+    gin, gq, gk = synth.gain_f32(Kd, 79), synth.gain_f32(d, 80), synth.gain_f32(d, 81)
+    rstd = (0.5 + torch.rand(M, generator=torch.Generator().manual_seed(82))).float() if norm else None
+    pos = (torch.arange(M, dtype=torch.int32) * 7) % 1024
+    U = (X.float() * gin[None, :]).to(torch.bfloat16) if norm else X    # the forward GEMM's input
+    cs = coda.rope_table(500000.0, d, 1024)
+    wtq, sw, wtv, osw = _cols(coda, W)
+    utq, su, utv, osu = _cols(coda, U)
+    dv = lambda t: None if t is None else t.to(DEV)
+    ws = coda.workspace(coda.load().coda_linear_qknorm_rope_bwd_fp8_workspace_size(M, Kd, n_q, n_kv, d))
+    g = coda.linear_qknorm_rope_bwd_fp8(dQ.to(DEV), dK.to(DEV), dV.to(DEV), qk.to(DEV), V.to(DEV), gq.to(DEV),
+                                        gk.to(DEV), pos.to(DEV), cs, n_q, n_kv, wtq, sw, utq, su, X=dv(X),
+                                        rstd=dv(rstd), gamma_in=dv(gin) if norm else None, dX_resid=R.to(DEV),
+                                        eps=1e-6, pairing=pairing, ws=ws)
+    torch.cuda.synchronize()
+    assert coda.get_status(ws) == 0
+    ref = O.linear_qknorm_rope_fp8_bwd(to_np(dQ), to_np(dK), to_np(dV), to_np(qk), to_np(V), to_np(gq), to_np(gk),
+                                       pos.numpy(), 500000.0, 1e-6, n_q, n_kv, d, wtv, osw, utv, osu, X=to_np(X),
+                                       row_scale=None if rstd is None else to_np(rstd),
+                                       gamma_in=to_np(gin) if norm else None, dX_resid=to_np(R), pairing=pairing)
+    a_d = e4m3_step_allowance(ref["Gr"]) @ np.abs(wtv * osw[:, None].astype(np.float64)).T
+    a_w = e4m3_step_allowance(ref["Gr"].T) @ np.abs(utv * osu[:, None].astype(np.float64)).T
+    a_x = a_d * np.abs(to_np(gin))[None, :] if norm else a_d
+    assert_bf16_within(g["dX"], ref["dX"], a_x, f"fp8 QKV dX ({pairing})")
+    assert_bf16_within(g["dW"], ref["dW"], a_w, f"fp8 QKV dW ({pairing})")
+    if norm:
+        assert_bf16_within(g["dgamma_in"], ref["dgamma_in"], (np.abs(to_np(X)) * a_d).sum(axis=0),
+                           "fp8 QKV dgamma_in")
+    assert_bf16(g["dgamma_q"], ref["dgamma_q"], "fp8 QKV dgamma_q")
+    assert_bf16(g["dgamma_k"], ref["dgamma_k"], "fp8 QKV dgamma_k")
 
 
 @pytest.mark.parametrize("fp8_wgrad", [True, False])

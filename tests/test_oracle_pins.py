@@ -218,6 +218,15 @@ MUTANTS = {
     "rms_dx_fp8_drops_gamma": _source_mutant(
         "dX = D * np.asarray(gamma, dtype=np.float64)[None, :] - np.asarray(coef, dtype=np.float64)[:, None] * X",
         "dX = D - np.asarray(coef, dtype=np.float64)[:, None] * X"),
+    "qkv_bwd_fp8_coef_single_r": _source_mutant("coef = r * r * (G * y).sum(axis=1) / Xf.shape[1]",
+                                                "coef = r * (G * y).sum(axis=1) / Xf.shape[1]"),
+    "qkv_bwd_fp8_dw_drops_u_scale": _source_mutant('"dW": _deq(gtv, sgt) @ _deq(UTv, su).T',
+                                                   '"dW": _deq(gtv, sgt) @ np.asarray(UTv, dtype=np.float64).T'),
+    "qkv_bwd_fp8_k_gain_q": _source_mutant("dk, dgk = qk_rmsnorm_rope_bwd(k, gamma_k, pos",
+                                           "dk, dgk = qk_rmsnorm_rope_bwd(k, gamma_q, pos"),
+    "qkv_bwd_fp8_g_unrounded": _source_mutant("Gp = _bf16(G * r[:, None])", "Gp = G * r[:, None]"),
+    "qkv_bwd_fp8_d_from_column_codes": _source_mutant("D = _deq(gv, sg) @ _deq(WTv, sw).T",
+                                                      "D = _deq(gtv, sgt).T @ _deq(WTv, sw).T"),
     # a negative label wraps around to column V + label (numpy indexing)
     "ce_negative_label_wraps": _source_mutant("in_range = (labels >= 0) & (labels < V)",
                                               "in_range = labels < V"),
