@@ -176,6 +176,11 @@ def test_rejects_bad_arguments_on_host(lib):
     assert lib.coda_linear_swiglu_nvfp4(*([FAKE] * 10), FAKE, None, None, 0, 64, 64, ws, 4096, None) == 0
     assert lib.coda_rmsnorm_scale_nvfp4(FAKE, 64, 16, 64, 1e-6, None, None, FAKE, FAKE, FAKE, None) == 1
     assert lib.coda_rmsnorm_scale_nvfp4(FAKE, 48, 16, 48, 1e-6, FAKE, None, FAKE, FAKE, FAKE, None) == 3
+    # FP8 QKV backward: the dW GEMM contracts over the tokens, M % 16 == 0
+    assert lib.coda_linear_qknorm_rope_bwd_fp8(*([FAKE] * 9), 16, 1e-6, 2, 1, 128, 0, *([FAKE] * 13), 20, 64, ws,
+                                               1 << 30, None) == 3
+    assert lib.coda_linear_qknorm_rope_bwd_fp8(*([FAKE] * 9), 16, 1e-6, 2, 1, 128, 0, *([FAKE] * 13), 0, 64, ws,
+                                               1 << 30, None) == 0
     assert lib.coda_nvfp4_scale_bytes(300, 224) == 4 * 1 * 2048
     assert lib.coda_nvfp4_scale_bytes(600, 512) == 8 * 2 * 2048
 
