@@ -986,14 +986,18 @@ __global__ void __launch_bounds__(QK_BWD_WARPS * 32)
 // per SM: a producer warp copies each token row's tensors -- dQ, dK, the
 // saved pre-norm q|k, dV, V (each contiguous within the row) and the row's
 // (cos, sin) table entry -- into a ring of shared-memory stages with
-// cp.async.bulk, counted on the stage's "full" barrier; eight compute warps
-// take the row's heads (warp w: heads w, w + 8, ..., four at a time), store
-// G' and arrive on the stage's "empty" barrier with their partial of the
-// RMSNorm coefficient sum; the producer adds the eight partials when it
-// reuses the stage (or at the end) and writes c for that row.  The copies
-// keep a whole ring of rows in flight per SM, which a warp per row with
-// register loads cannot.  Every wait is bounded (CODA_DEV_TIMEOUT).
-constexpr int QKT_WARPS = 8;
+// cp.async.bulk, counted on the stage's "full" barrier; 18 compute warps
+// take the row's heads (warp w: heads w, w + 18, ..., four at a time: the
+// 64 + 8 q and k heads of a 70B-width block are one group of four per
+// warp), store G' and arrive on the stage's "empty" barrier with their
+// partial of the RMSNorm coefficient sum; the producer adds the partials
+// when it reuses the stage (or at the end) and writes c for that row.  The
+// copies keep a whole ring of rows in flight per SM, which a warp per row
+// with register loads cannot.  Every wait is bounded (CODA_DEV_TIMEOUT).
+// (8 compute warps, three groups each with a quarter of the slots idle:
+// 84 us for 4096 such rows; 9: 74 us; 18: 62 us at 96 registers; 24 and
+// more spill.)
+constexpr int QKT_WARPS = 18;
 
 template <bool HALF>
 __global__ void __launch_bounds__((QKT_WARPS + 1) * 32, 1)
