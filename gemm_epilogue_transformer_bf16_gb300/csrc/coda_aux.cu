@@ -417,6 +417,14 @@ struct DivBy {
   }
 };
 
+// Four e4m3 codes, a in the low byte: two paired conversions (nearest even,
+// saturating to +-448) instead of four single ones and their byte shifts.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
 // ---------------------------------------------------------------- FP8 (e4m3) row quantisation
 // Warp per row: scale = amax / 448 (fp32; 1 for an all-zero row), codes =
 // e4m3(x / scale), fp32 division, round to nearest even, saturating.
@@ -443,13 +451,8 @@ __global__ void quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ X, in
     for (int64_t k = lane * 8; k < K; k += 256) {
       float v[8];
       load_bf16x8(x + k, v);
-      uint32_t lo = 0, hi = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        lo |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(div(v[j]), __NV_SATFINITE, __NV_E4M3)) << (8 * j);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        hi |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(div(v[4 + j]), __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+      const uint32_t lo = e4m3x4(div(v[0]), div(v[1]), div(v[2]), div(v[3]));
+      const uint32_t hi = e4m3x4(div(v[4]), div(v[5]), div(v[6]), div(v[7]));
       *reinterpret_cast<uint2*>(q + k) = make_uint2(lo, hi);
     }
   }
@@ -535,13 +538,8 @@ __global__ void __launch_bounds__(QROW_THREADS) quantize_fp8_rows_smem_kernel(
     for (int64_t k = tid * 8; k < K; k += QROW_THREADS * 8) {
       float v[8];
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(x + k), v);
-      uint32_t lo = 0, hi = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        lo |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(div(v[j]), __NV_SATFINITE, __NV_E4M3)) << (8 * j);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        hi |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(div(v[4 + j]), __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+      const uint32_t lo = e4m3x4(div(v[0]), div(v[1]), div(v[2]), div(v[3]));
+      const uint32_t hi = e4m3x4(div(v[4]), div(v[5]), div(v[6]), div(v[7]));
       *reinterpret_cast<uint2*>(q + k) = make_uint2(lo, hi);
     }
     __syncthreads();  // buffer b and red[] are free for the next rows
@@ -643,12 +641,11 @@ __global__ void fp8_col_quant_kernel(const __nv_bfloat16* __restrict__ X, int64_
     __syncthreads();
     if (r0 + 64 < r_end) load(r0 + 64);  // in flight while this tile is converted and stored
     if (c < C) {
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      uint32_t w[4];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int rr = part * 16 + j;
-        const uint32_t b = static_cast<uint32_t>(__nv_cvt_float_to_fp8(div(tile[rr][cc]), __NV_SATFINITE, __NV_E4M3));
-        w[j >> 2] |= b << (8 * (j & 3));
+      for (int j = 0; j < 4; ++j) {
+        const int rr = part * 16 + 4 * j;
+        w[j] = e4m3x4(div(tile[rr][cc]), div(tile[rr + 1][cc]), div(tile[rr + 2][cc]), div(tile[rr + 3][cc]));
       }
       const int64_t r = r0 + part * 16;
       if (r + 16 <= r_end) {
