@@ -1,7 +1,7 @@
 """The GEMM kernel in each cluster size: single CTAs (CODA_CTA_PAIR=0), CTA
 pairs only (CODA_CTA_QUAD=0), the per-GEMM policy CODA_CTA_QUAD=2 and split
-launches turned off (CODA_SPLIT=0; by default a two-pair kernel and a pair
-kernel share the GPU); and the launch options turned off: programmatic
+launches (CODA_SPLIT=1: a two-pair kernel and a pair kernel share the GPU);
+and the launch options turned off: programmatic
 dependent launch (CODA_PDL=0), streaming epilogue stores for large
 outputs (CODA_L2_HINTS=0), CTA pairs for GEMMs whose two-pair units fill
 the last wave poorly (CODA_PAIR_WAVES=0), the L2 prefetch of the
@@ -27,7 +27,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 @pytest.mark.parametrize("env", [{"CODA_CTA_PAIR": "0"}, {"CODA_CTA_QUAD": "0"}, {"CODA_CTA_QUAD": "2"},
-                                 {"CODA_SPLIT": "0"}, {"CODA_PDL": "0"}, {"CODA_L2_HINTS": "0"},
+                                 {"CODA_SPLIT": "1"}, {"CODA_PDL": "0"}, {"CODA_L2_HINTS": "0"},
                                  {"CODA_PAIR_WAVES": "0"}, {"CODA_AUX_PREFETCH": "0"}, {"CODA_QK_TMA": "0"},
                                  {"CODA_EPI_RING": "0"}, {"CODA_EPI_LEAN": "0"}, {"CODA_RMS_SHARE": "0"},
                                  {"CODA_QROW_SMEM": "0"}, {}])
