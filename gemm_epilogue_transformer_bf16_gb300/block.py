@@ -30,14 +30,15 @@ its GEMMs read x; the backward is the same either way.
 
 Every step is a libcoda.so call; buffers and workspaces are allocated once,
 so a step launches only the library's kernels.  With ``concurrent`` (the
-default) independent calls run on a second stream: in the forward the QKV
-branch (row RMS of x0, QKV projection; with folded weights also the Wqkv
-fold) runs beside the O-projection (and the MLP weights' folds that follow
-it, which share SMs with the tensor-bound GEMM), and in the backward
-the O-projection backward overlaps the QKV backward, and inside the MLP
-backward the weight-gradient GEMMs run on the second stream beside the
-dH -> dX chain, filling each other's last-wave tails.  The gate/up and down
-GEMMs run alone.
+default) the forward's QKV branch (row RMS of x0, QKV projection; with
+folded weights also the Wqkv fold) runs on a second stream beside the
+O-projection (and the MLP weights' folds that follow it, which share SMs
+with the tensor-bound GEMM).  With ``concurrent_bwd`` the backward does the
+same (the O-projection backward beside the QKV backward, the MLP's
+weight-gradient GEMMs beside its dH -> dX chain); it is off by default:
+two persistent GEMMs started together split the SMs by whichever places its
+CTAs first, and in a loop of steps the backward ran 1 % slower that way than
+on one stream.  The gate/up and down GEMMs run alone.
 """
 from __future__ import annotations
 
@@ -51,10 +52,11 @@ from . import (K_MAJOR, MN_MAJOR, EpilogueDesc, fold_gamma, gemm_epilogue, linea
 
 
 class Block:
-    def __init__(self, shape, weights, device="cuda", concurrent=True, fold_weights=False):
+    def __init__(self, shape, weights, device="cuda", concurrent=True, fold_weights=False, concurrent_bwd=False):
         self.s = s = shape
         self.w = weights
         self.concurrent = concurrent
+        self.concurrent_bwd = concurrent and concurrent_bwd
         self.fold_weights = fold_weights
         lib = load()
         T, Hd, I, d = s.tokens, s.hidden, s.inter, s.head_dim
@@ -169,10 +171,11 @@ class Block:
     def backward(self, x0, A, pos, dx2, dQ, dK, dV, mark=None):
         s, w = self.s, self.w
         mark = mark or (lambda name: None)
+        side = self.s2 if self.concurrent_bwd else None
         linear_swiglu_bwd(dx2, self.x1, w["Wg"], w["Wu"], w["Wd"], self.g, self.u, self.H, rstd=self.rstd1,
-                          gamma=w["gamma_mlp"], dX_resid=dx2, ws=self.ws, out=self.grads_mlp, side_stream=self.s2)
+                          gamma=w["gamma_mlp"], dX_resid=dx2, ws=self.ws, out=self.grads_mlp, side_stream=side)
         mark("mlp_bwd")
-        ctx, ws2 = self._side()
+        ctx, ws2 = self._side() if self.concurrent_bwd else (_NullCtx(), self.ws)
         with ctx:   # both need only dx1
             linear_residual_bwd(self.dx1, A, w["Wo"], ws=ws2, out=self.grads_o)
         linear_qknorm_rope_bwd(dQ, dK, dV, self.fwd["qk_save"], self.fwd["V"], w["gamma_q"], w["gamma_k"], pos,
@@ -265,9 +268,9 @@ class BlockFP8:
         self.ws2 = workspace(need, device) if concurrent else self.ws
 
     # kernels per stage (coda_launch_count at 8192 tokens, hidden 8192, the
-    # default launch switches: split GEMM launches count twice)
-    LAUNCHES = {"quant_w": 17, "fwd": 14, "bwd": 48}
-    LAUNCHES_BF16_WGRAD = {"quant_w": 14, "fwd": 14, "bwd": 25}
+    # default launch switches)
+    LAUNCHES = {"quant_w": 17, "fwd": 10, "bwd": 41}
+    LAUNCHES_BF16_WGRAD = {"quant_w": 14, "fwd": 10, "bwd": 17}
 
     def launches(self):
         return self.LAUNCHES if self.fp8_wgrad else self.LAUNCHES_BF16_WGRAD

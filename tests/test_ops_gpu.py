@@ -265,15 +265,16 @@ SMALL_BLOCK = synth.BlockShape(tokens=256, hidden=512, n_q=4, n_kv=2, head_dim=1
 RAGGED_BLOCK = synth.BlockShape(tokens=200, hidden=264, n_q=2, n_kv=1, head_dim=128, inter=392, seq_len=64)
 
 
-@pytest.mark.parametrize("fold_weights", [False, True])
+@pytest.mark.parametrize("fold_weights,concurrent_bwd", [(False, False), (True, False), (False, True)])
 @pytest.mark.parametrize("shape", [SMALL_BLOCK, RAGGED_BLOCK])
-def test_block_fwd_bwd(coda, shape, fold_weights):
+def test_block_fwd_bwd(coda, shape, fold_weights, concurrent_bwd):
     """Both ways of applying the RMSNorm gains: in the producing epilogue
-    (u = x ⊙ gamma, the default) and folded into the weights."""
+    (u = x ⊙ gamma, the default) and folded into the weights; and the
+    backward on one stream (the default) or with its second stream."""
     from gemm_epilogue_transformer_bf16_gb300.block import Block
     t = synth.make_block(shape, seed=0)
     d, o = dev(t), f64(t)
-    blk = Block(shape, d, fold_weights=fold_weights)
+    blk = Block(shape, d, fold_weights=fold_weights, concurrent_bwd=concurrent_bwd)
     f = blk.forward(d["x0"], d["A"], d["pos"])
     g = blk.backward(d["x0"], d["A"], d["pos"], d["dx2"], d["dQ"], d["dK"], d["dV"])
     torch.cuda.synchronize()
