@@ -497,19 +497,23 @@ def main():
 
             e2e_run(max(2, args.warmup // 2))
             torch.cuda.synchronize(dev)
+            clocks_e2e = ClockSampler(gpu_id)   # the clocks of this loop too: it runs after the other
+            clocks_e2e.start()
+            time.sleep(0.3)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
             e2e_run(args.steps, a)
             b.record(stream)
             torch.cuda.synchronize(dev)
+            clk_e2e = clocks_e2e.stop()
             ms_e2e = a.elapsed_time(b)
             if not (torch.equal(hx2, blk.x2.cpu()) and torch.equal(hdx0, blk.grads_qkv["dX"].cpu())):
                 raise RuntimeError("e2e results read back do not match the device buffers")
             e2e = {"value": round(flops_step * args.steps / (ms_e2e / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e / args.steps, 3),
                    "copies": "pinned host buffers; next step's inputs prefetched on a copy stream, results read back "
-                             "on another"}
+                             "on another", "clocks": clk_e2e}
 
         # ---------------------------------------------------------------- unfused torch comparison
         unfused_ms = None
