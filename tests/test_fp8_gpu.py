@@ -164,8 +164,9 @@ def test_rmsnorm_linear_dx_fp8(coda):
     assert_bf16(out["dgamma"], r["dgamma"], "fp8 RMSNorm dgamma")
 
 
-@pytest.mark.parametrize("norm,pairing", [(True, "interleaved"), (False, "half")])
-def test_linear_qknorm_rope_bwd_fp8(coda, norm, pairing):
+@pytest.mark.parametrize("norm,pairing,shape", [(True, "interleaved", (304, 272, 2, 1)), (False, "half", (304, 272, 2, 1)),
+                                                (True, "half", (160, 200, 4, 2))])
+def test_linear_qknorm_rope_bwd_fp8(coda, norm, pairing, shape):
     """The QKV backward with both GEMMs on e4m3 operands: the per-head map
     into G' (in the workspace), G' quantised per row for dX and per column
     for dW, W^T and U^T given as column codes (checked bit for bit against
@@ -177,8 +178,8 @@ def test_linear_qknorm_rope_bwd_fp8(coda, norm, pairing):
     change through the GEMMs (parity.e4m3_step_allowance); dgamma_q and
     dgamma_k take no quantised operand and are held to the plain rule.
     304 tokens (two 128-token tiles and a ragged tail), 272 features, 2 q
-    and 1 kv heads."""
-    M, Kd, n_q, n_kv, d = 304, 272, 2, 1, 128
+    and 1 kv heads; and 160 tokens, 200 features, 4 q and 2 kv heads."""
+    (M, Kd, n_q, n_kv), d = shape, 128
     N = (n_q + 2 * n_kv) * d
     qk = synth.randn_bf16((M, (n_q + n_kv) * d), 1.0, 71)
     V = synth.randn_bf16((M, n_kv * d), 1.0, 72)
