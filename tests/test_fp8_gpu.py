@@ -220,8 +220,8 @@ def test_linear_qknorm_rope_bwd_fp8(coda, norm, pairing, shape):
     assert_bf16(g["dgamma_k"], ref["dgamma_k"], "fp8 QKV dgamma_k")
 
 
-@pytest.mark.parametrize("fp8_wgrad", [True, False])
-def test_block_fp8_step(coda, fp8_wgrad):
+@pytest.mark.parametrize("fp8_wgrad,concurrent", [(True, True), (False, True), (True, False)])
+def test_block_fp8_step(coda, fp8_wgrad, concurrent):
     """The block step with its forward projections and its MLP and
     O-projection input gradients on e4m3 operands (BlockFP8) -- and, with
     fp8_wgrad, the MLP and O-projection weight gradients on the
@@ -232,13 +232,15 @@ def test_block_fp8_step(coda, fp8_wgrad):
     value, about 4 % RMS on a product of two quantised operands, and the
     chains run through two or three such GEMMs), so the bound is a relative
     Frobenius error of 0.15 per output: it catches wiring mistakes (a
-    transposed operand, a wrong scale), which give errors of order one."""
+    transposed operand, a wrong scale), which give errors of order one.
+    Also on one stream (the default runs the weight gradients and their
+    quantisers on a second one)."""
     from gemm_epilogue_transformer_bf16_gb300.block import BlockFP8
     shape = synth.BlockShape(tokens=256, hidden=512, n_q=4, n_kv=2, head_dim=128, inter=1024, seq_len=128)
     t = synth.make_block(shape, seed=0)
     d = {k: v.to(DEV) for k, v in t.items()}
     o = {k: (v.numpy() if v.dtype in (torch.int32, torch.int64) else to_np(v)) for k, v in t.items()}
-    blk = BlockFP8(shape, d, fp8_wgrad=fp8_wgrad)
+    blk = BlockFP8(shape, d, fp8_wgrad=fp8_wgrad, concurrent=concurrent)
     f = blk.forward(d["x0"], d["A"], d["pos"])
     g = blk.backward(d["x0"], d["A"], d["pos"], d["dx2"], d["dQ"], d["dK"], d["dV"])
     torch.cuda.synchronize()
